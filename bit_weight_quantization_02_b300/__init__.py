@@ -1,0 +1,208 @@
+"""libw4: int4 weight-only quantization and the bf16 x int4 linear on B300.
+
+Thin Python binding over the C ABI in ``include/w4.h``.  The functions keep
+the C names (``w4_quantize``, ``w4_dequantize``, ``w4_linear`` ...); they only
+marshal arguments: torch allocates the outputs and the workspace on the
+tensors' device, and every step of the computation runs in the CUDA kernels
+of ``libw4.so``.  There is no CPU fallback: if the library is missing or fails
+to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "W4Error", "W4_FORMAT_VERSION", "KERNEL_AUTO", "KERNEL_SKINNY", "KERNEL_GEMM",
+    "library_path", "load_library", "w4_quantize", "w4_dequantize", "w4_linear",
+    "w4_linear_ex", "w4_linear_workspace_bytes", "w4_packed_bytes", "w4_qparam_bytes",
+    "w4_device_fault", "w4_format_version", "Workspace",
+]
+
+W4_FORMAT_VERSION = 1
+KERNEL_AUTO, KERNEL_SKINNY, KERNEL_GEMM = 0, 1, 2
+_STATUS = {0: "W4_OK", 1: "W4_ERR_INVALID_ARG", 2: "W4_ERR_UNSUPPORTED", 3: "W4_ERR_MISALIGNED",
+           4: "W4_ERR_CUDA", 5: "W4_ERR_TIMEOUT"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lock = threading.Lock()
+_lib = None
+
+
+class W4Error(RuntimeError):
+    def __init__(self, status: int, call: str, detail: str):
+        self.status = status
+        super().__init__(f"{call} failed: {_STATUS.get(status, status)}: {detail}")
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libw4.so")
+
+
+def load_library():
+    """Load libw4.so (built in-tree by ``_build.build()``); raise if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libw4.so not found at {path}: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(path)
+        p, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+        sigs = {
+            "w4_quantize": ([p, i64, i64, i32, p, p, p, p], i32),
+            "w4_dequantize": ([p, p, p, i64, i64, i32, p, p], i32),
+            "w4_linear_workspace_bytes": ([i64, i64, i64, i32], sz),
+            "w4_linear": ([p, i64, i64, p, p, p, i64, i32, p, p, sz, p], i32),
+            "w4_linear_ex": ([p, i64, i64, p, p, p, i64, i32, p, p, sz, i32, p], i32),
+            "w4_packed_bytes": ([i64, i64], sz),
+            "w4_qparam_bytes": ([i64, i64, i32], sz),
+            "w4_device_fault": ([p], i32),
+            "w4_status_string": ([i32], ctypes.c_char_p),
+            "w4_last_error_detail": ([], ctypes.c_char_p),
+            "w4_format_version": ([], i32),
+        }
+        for name, (args, res) in sigs.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        if lib.w4_format_version() != W4_FORMAT_VERSION:
+            raise RuntimeError("libw4.so format version does not match the binding")
+        _lib = lib
+        return lib
+
+
+def _check(status: int, call: str):
+    if status != 0:
+        detail = load_library().w4_last_error_detail()
+        raise W4Error(status, call, detail.decode() if detail else "")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(t: torch.Tensor):
+    if t.device.type != "cuda":
+        raise ValueError("libw4 works on CUDA tensors only (there is no CPU path)")
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _bits16(t: torch.Tensor, name: str) -> torch.Tensor:
+    if t.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError(f"{name} must be bf16 (or its 16-bit pattern), got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def w4_packed_bytes(N: int, K: int) -> int:
+    return load_library().w4_packed_bytes(N, K)
+
+
+def w4_qparam_bytes(N: int, K: int, group_size: int) -> int:
+    return load_library().w4_qparam_bytes(N, K, group_size)
+
+
+def w4_format_version() -> int:
+    return load_library().w4_format_version()
+
+
+def w4_quantize(W: torch.Tensor, group_size: int, out=None):
+    """W bf16 [N,K] (CUDA) -> (Wq uint8 [N,K/2], scales bf16 [N,K/g], offsets bf16 [N,K/g])."""
+    lib = load_library()
+    _bits16(W, "W")
+    N, K = W.shape
+    if out is None:
+        ng = K // group_size if group_size and K % group_size == 0 else 0
+        Wq = torch.empty((N, K // 2), dtype=torch.uint8, device=W.device)
+        sc = torch.empty((N, ng), dtype=torch.bfloat16, device=W.device)
+        of = torch.empty((N, ng), dtype=torch.bfloat16, device=W.device)
+    else:
+        Wq, sc, of = out
+    _check(lib.w4_quantize(_ptr(W), N, K, group_size, _ptr(Wq), _ptr(sc), _ptr(of), _stream(W)), "w4_quantize")
+    return Wq, sc, of
+
+
+def w4_dequantize(Wq: torch.Tensor, scales: torch.Tensor, offsets: torch.Tensor, group_size: int, out=None):
+    """Packed int4 weights -> bf16 [N,K]."""
+    lib = load_library()
+    N, half = Wq.shape
+    K = 2 * half
+    W = out if out is not None else torch.empty((N, K), dtype=torch.bfloat16, device=Wq.device)
+    _check(lib.w4_dequantize(_ptr(Wq), _ptr(scales), _ptr(offsets), N, K, group_size, _ptr(W), _stream(Wq)),
+           "w4_dequantize")
+    return W
+
+
+def w4_linear_workspace_bytes(M: int, N: int, K: int, group_size: int) -> int:
+    return load_library().w4_linear_workspace_bytes(M, N, K, group_size)
+
+
+class Workspace:
+    """Zero-filled device workspace for w4_linear, grown on demand.
+
+    One instance per stream: calls that can overlap on the GPU must not share
+    a workspace.  Growing it allocates (through torch), so size it before
+    capturing a CUDA graph or timing."""
+
+    def __init__(self, device=None, nbytes: int = 0):
+        self.device = torch.device(device or "cuda")
+        self.buf = None
+        if nbytes:
+            self.reserve(nbytes)
+
+    def reserve(self, nbytes: int):
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+        return self
+
+    def reserve_for(self, M: int, N: int, K: int, group_size: int):
+        return self.reserve(w4_linear_workspace_bytes(M, N, K, group_size))
+
+    @property
+    def nbytes(self) -> int:
+        return 0 if self.buf is None else self.buf.numel()
+
+
+_default_ws = {}
+
+
+def _workspace_for(X: torch.Tensor, M, N, K, g, workspace):
+    if workspace is None:
+        key = (X.device.index, torch.cuda.current_stream(X.device).cuda_stream)
+        workspace = _default_ws.get(key)
+        if workspace is None:
+            workspace = _default_ws[key] = Workspace(X.device)
+    return workspace.reserve_for(M, N, K, g)
+
+
+def w4_linear_ex(X: torch.Tensor, Wq: torch.Tensor, scales: torch.Tensor, offsets: torch.Tensor,
+                 group_size: int, kernel: int = KERNEL_AUTO, out=None, workspace: Workspace | None = None):
+    """Y bf16 [M,N] = X bf16 [M,K] . dequant(Wq)^T with fp32 accumulation."""
+    lib = load_library()
+    _bits16(X, "X")
+    M, K = X.shape
+    N = Wq.shape[0]
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    ws = _workspace_for(X, M, N, K, group_size, workspace)
+    _check(lib.w4_linear_ex(_ptr(X), M, K, _ptr(Wq), _ptr(scales), _ptr(offsets), N, group_size, _ptr(Y),
+                            _ptr(ws.buf), ws.nbytes, kernel, _stream(X)), "w4_linear")
+    return Y
+
+
+def w4_linear(X, Wq, scales, offsets, group_size, out=None, workspace=None):
+    """Y bf16 [M,N] = X . dequant(Wq)^T; skinny kernel for M <= 32, tensor-core GEMM above."""
+    return w4_linear_ex(X, Wq, scales, offsets, group_size, KERNEL_AUTO, out, workspace)
+
+
+def w4_device_fault(device=None) -> None:
+    """Synchronize the current stream and raise W4Error if a kernel gave up a bounded wait."""
+    lib = load_library()
+    dev = torch.device(device or "cuda")
+    _check(lib.w4_device_fault(ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)), "w4_device_fault")

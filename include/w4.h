@@ -1,0 +1,167 @@
+/*
+ * w4.h -- C ABI of libw4: group-wise int4 weight-only quantization of a
+ * linear layer's bf16 weights, and the mixed bf16 x int4 linear that consumes
+ * them, on one NVIDIA B300 (sm_103a).
+ *
+ * The method, as the pages state it:
+ *  - a linear layer's weights are quantized once, ahead of time, to int4 in
+ *    groups of 32, 64 or 128 (torchao README, "Quick start": quantize_ with
+ *    Int4WeightOnlyConfig(group_size=32); torchao guide, section 3.1 "One
+ *    line of code for INT4 quantization"; TorchAO 0.14.0 release notes,
+ *    "Deprecations", group_size=128), then the quantized layer is called;
+ *  - below 8 bits the projection is group-wise affine with an offset ("zero
+ *    point") and the integer mapping is torch.round(), i.e. round half to
+ *    even (Optimum Quanto, "Design overview / Tensors");
+ *  - groups run along the first axis, the output features (Optimum Quanto,
+ *    "Design overview / Modules"), so for W[N,K] a group is g consecutive k
+ *    of one output row n;
+ *  - bias is not quantized (same section); this ABI has no bias argument;
+ *  - the matmul result is accumulated at higher precision than its inputs
+ *    (Optimum Quanto, "Pitfalls when quantizing activations"); bf16 x int4
+ *    matmuls are accelerated on CUDA (Optimum Quanto, feature list).
+ *
+ * Conventions shared by every call:
+ *  - bf16 values travel as uint16_t bit patterns;
+ *  - every tensor pointer is a DEVICE pointer owned by the caller, 16-byte
+ *    aligned, row-major and densely packed; outputs must not alias inputs;
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *    only enqueues work: it returns before the GPU has run it, keeps no state
+ *    between calls, never allocates device or pinned memory and never
+ *    synchronizes;
+ *  - all argument checks happen on the host before any launch; on an error
+ *    nothing is written and no CUDA call is made;
+ *  - inputs must be finite.  A group whose range (max - min) overflows fp32
+ *    (|w| near the bf16 maximum) gives unspecified but non-faulting output;
+ *  - a call with N == 0 (or M == 0 for the linear) succeeds with no launch.
+ */
+#ifndef W4_H
+#define W4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Packed layout version: plain row-major codes, two per byte with the code of
+ * the even k in the low nibble, qparams [N, K/g] bf16 row-major. */
+#define W4_FORMAT_VERSION 1
+
+typedef enum w4_status {
+    W4_OK = 0,
+    W4_ERR_INVALID_ARG = 1,  /* bad size, K % group_size != 0, NULL pointer, overflow */
+    W4_ERR_UNSUPPORTED = 2,  /* group_size not in {32, 64, 128} */
+    W4_ERR_MISALIGNED = 3,   /* a pointer is not 16-byte aligned */
+    W4_ERR_CUDA = 4,         /* a CUDA call failed; see w4_last_error_detail() */
+    W4_ERR_TIMEOUT = 5       /* a kernel gave up a bounded wait (w4_device_fault) */
+} w4_status;
+
+/* Kernel choice for w4_linear_ex. */
+typedef enum w4_kernel {
+    W4_KERNEL_AUTO = 0,    /* skinny kernel for M <= 32, tensor-core GEMM above */
+    W4_KERNEL_SKINNY = 1,  /* memory-bound decode kernel; requires M <= 32 */
+    W4_KERNEL_GEMM = 2     /* tcgen05 tensor-core GEMM; any M >= 1 */
+} w4_kernel;
+
+/*
+ * w4_quantize -- W[N,K] bf16 -> Wq[N,K/2] uint8, scales[N,K/g] bf16,
+ * offsets[N,K/g] bf16.
+ *
+ * For each row n and group j (k in [j*g, (j+1)*g)), with IEEE fp32 arithmetic:
+ *   mn, mx = min, max of the group (-0.0 ranks below +0.0)
+ *   s32    = (mx - mn) / 15;  s32 = 1e-6 if s32 < 1e-6
+ *   s      = bf16(s32) (round to nearest even) -> scales[n, j]
+ *   o      = mn (exactly a bf16 value)          -> offsets[n, j]
+ *   q      = clamp(round_half_even((w - o) / s), 0, 15)
+ *   codes of k = 2p and 2p+1 share byte p of row n; even k in the low nibble.
+ * Source: the affine group projection with an offset and torch.round
+ * mapping of Optimum Quanto, "Design overview / Tensors"; the formulas are the
+ * plainest reading of it (the eps value and coding with the stored bf16 scale
+ * are readings).  Results are bit-exact, independent of launch shape.
+ * Errors: W4_ERR_UNSUPPORTED (group_size), W4_ERR_INVALID_ARG (K <= 0,
+ * N < 0, K % group_size, NULL, N*K >= 2^62), W4_ERR_MISALIGNED, W4_ERR_CUDA.
+ */
+w4_status w4_quantize(const uint16_t *W, int64_t N, int64_t K, int group_size,
+                      uint8_t *Wq, uint16_t *scales, uint16_t *offsets,
+                      void *stream);
+
+/*
+ * w4_dequantize -- W_out[n,k] = bf16(fp32(q) * s + o): one exact fp32
+ * product, one fp32 add, one rounding to bf16 (round to nearest even).
+ * Bit-exact.  Source: Optimum Quanto, "Pitfalls when quantizing
+ * activations" (the quantized result is brought back to float).
+ * Errors as w4_quantize.
+ */
+w4_status w4_dequantize(const uint8_t *Wq, const uint16_t *scales,
+                        const uint16_t *offsets, int64_t N, int64_t K,
+                        int group_size, uint16_t *W_out, void *stream);
+
+/*
+ * w4_linear_workspace_bytes -- bytes of workspace that lets w4_linear split
+ * K across thread blocks for this problem (0 if it never needs any).  A
+ * smaller workspace is accepted: the call then splits less (still correct,
+ * possibly slower).
+ */
+size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int group_size);
+
+/*
+ * w4_linear -- Y[M,N] bf16 = X[M,K] bf16 . dequant(Wq, scales, offsets)^T,
+ * products and sums in fp32, one rounding to bf16 at the end, no bias.
+ * Source: the mixed bf16 x int4 matmul of Optimum Quanto (feature list and
+ * "Pitfalls when quantizing activations": accumulation in fp32).
+ *
+ * The kernels dequantize each weight as bf16(q * s + o) with a single
+ * rounding, which can differ from w4_dequantize's double rounding by one bf16
+ * ulp; the summation order is the kernel's own.  Accuracy contract against
+ * y_ref = sum_k X[m,k] W'[n,k] in fp64 (W' = w4_dequantize output):
+ *   |y - y_ref| <= 4e-3 |y_ref| + 1e-2 rms(y_ref).
+ *
+ * workspace: device memory of `workspace_bytes` bytes (may be NULL with 0),
+ * used by the skinny kernel to combine partial sums across K slices.  It must
+ * be zero-filled once before its first use; every call leaves it ready for
+ * the next (its counters back at zero).  Two calls that may run at the same
+ * time on the GPU must not share a workspace.  Results do not depend on the
+ * workspace size (fixed summation order per launch shape).
+ * Errors as w4_quantize, plus W4_ERR_INVALID_ARG for M < 0.
+ */
+w4_status w4_linear(const uint16_t *X, int64_t M, int64_t K, const uint8_t *Wq,
+                    const uint16_t *scales, const uint16_t *offsets, int64_t N,
+                    int group_size, uint16_t *Y, void *workspace,
+                    size_t workspace_bytes, void *stream);
+
+/* w4_linear with an explicit kernel choice (tests and benchmarks use it to
+ * run both kernels on the same problem).  W4_KERNEL_SKINNY with M > 32 gives
+ * W4_ERR_INVALID_ARG. */
+w4_status w4_linear_ex(const uint16_t *X, int64_t M, int64_t K,
+                       const uint8_t *Wq, const uint16_t *scales,
+                       const uint16_t *offsets, int64_t N, int group_size,
+                       uint16_t *Y, void *workspace, size_t workspace_bytes,
+                       w4_kernel kernel, void *stream);
+
+/* Sizes of the packed outputs: N*K/2 bytes of codes, N*(K/g)*2 bytes for each
+ * of scales and offsets.  0 for invalid arguments. */
+size_t w4_packed_bytes(int64_t N, int64_t K);
+size_t w4_qparam_bytes(int64_t N, int64_t K, int group_size);
+
+/*
+ * w4_device_fault -- synchronizes `stream`, then reports whether any libw4
+ * kernel on the current device gave up a bounded wait since the last call
+ * (W4_ERR_TIMEOUT), and clears the flag.  Kernels that time out set the flag,
+ * release what they hold and return; their outputs are then undefined.
+ */
+w4_status w4_device_fault(void *stream);
+
+/* Human-readable text of a status, and the detail (CUDA error string, failed
+ * check) of the last failing call on this host thread. */
+const char *w4_status_string(w4_status s);
+const char *w4_last_error_detail(void);
+
+/* W4_FORMAT_VERSION of the built library. */
+int w4_format_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4_H */

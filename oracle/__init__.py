@@ -1,0 +1,144 @@
+"""CPU oracle for int4 weight-only quantization and the bf16 x int4 linear.
+
+TEST INFRASTRUCTURE ONLY.  The test-suite, ``__graft_entry__.smoke()`` and
+the CPU-baseline / reference leg of ``bench.py`` are the only callers allowed
+to import this package.  The product path (the ``bit_weight_quantization_02_b300``
+package and its CUDA library) never imports, links or executes it.
+
+The arithmetic lives in ``w4_oracle.c`` (plain C, IEEE fp32 with contraction
+off, fp64 for the linear); this module only builds it with gcc and marshals
+numpy arrays.  bf16 tensors travel as ``uint16`` bit patterns.
+
+Pins: every function here is checked by ``tests/test_oracle_pins.py`` against
+worked examples derived by hand (``tests/golden/``), exact-arithmetic
+invariants, brute force over the 16 codes and an independent fp64 matmul.
+Parity unpinned (a reading both sides implement, with nothing in the pages to
+check it against): the eps value of the scale clamp, the -0.0 < +0.0 order of
+the group minimum and the nibble order of the packed codes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "w4_oracle.c")
+_LIB = os.path.join(_HERE, "libw4_oracle.so")
+_CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no CUDA involved) and return the .so path."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *_CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            p = ctypes.c_void_p
+            i64 = ctypes.c_int64
+            lib.w4_ref_quantize.argtypes = [p, i64, i64, ctypes.c_int, p, p, p]
+            lib.w4_ref_quantize.restype = ctypes.c_int
+            lib.w4_ref_dequantize.argtypes = [p, p, p, i64, i64, ctypes.c_int, p]
+            lib.w4_ref_dequantize.restype = ctypes.c_int
+            lib.w4_ref_linear.argtypes = [p, i64, i64, p, p, p, i64, ctypes.c_int, p]
+            lib.w4_ref_linear.restype = ctypes.c_int
+            lib.w4_ref_eps.argtypes = []
+            lib.w4_ref_eps.restype = ctypes.c_float
+            _lib = lib
+    return _lib
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError(f"expected uint16 bf16 bit patterns, got {a.dtype}")
+    return a
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def ref_eps() -> float:
+    return float(_load().w4_ref_eps())
+
+
+def ref_quantize(W: np.ndarray, group_size: int):
+    """W: uint16 [N,K] bf16 bits -> (Wq uint8 [N,K/2], scales uint16 [N,K/g], offsets uint16 [N,K/g])."""
+    W = _u16(W)
+    N, K = W.shape
+    if group_size not in (32, 64, 128) or K % group_size:
+        raise ValueError("unsupported shape / group size")
+    Wq = np.zeros((N, K // 2), np.uint8)
+    sc = np.zeros((N, K // group_size), np.uint16)
+    of = np.zeros((N, K // group_size), np.uint16)
+    rc = _load().w4_ref_quantize(_ptr(W), N, K, group_size, _ptr(Wq), _ptr(sc), _ptr(of))
+    if rc:
+        raise RuntimeError(f"w4_ref_quantize failed: {rc}")
+    return Wq, sc, of
+
+
+def ref_dequantize(Wq: np.ndarray, scales: np.ndarray, offsets: np.ndarray, group_size: int) -> np.ndarray:
+    """Packed codes + qparams -> uint16 [N,K] bf16 bits of W'."""
+    Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+    scales, offsets = _u16(scales), _u16(offsets)
+    N, half = Wq.shape
+    K = 2 * half
+    out = np.zeros((N, K), np.uint16)
+    rc = _load().w4_ref_dequantize(_ptr(Wq), _ptr(scales), _ptr(offsets), N, K, group_size, _ptr(out))
+    if rc:
+        raise RuntimeError(f"w4_ref_dequantize failed: {rc}")
+    return out
+
+
+def ref_linear(X: np.ndarray, Wq: np.ndarray, scales: np.ndarray, offsets: np.ndarray,
+               group_size: int) -> np.ndarray:
+    """X uint16 [M,K] bf16 bits, packed weights of [N,K] -> fp64 [M,N] = X . W'^T."""
+    X = _u16(X)
+    Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+    scales, offsets = _u16(scales), _u16(offsets)
+    M, K = X.shape
+    N = Wq.shape[0]
+    if Wq.shape[1] * 2 != K:
+        raise ValueError("X and Wq disagree on K")
+    Y = np.zeros((M, N), np.float64)
+    rc = _load().w4_ref_linear(_ptr(X), M, K, _ptr(Wq), _ptr(scales), _ptr(offsets), N, group_size, _ptr(Y))
+    if rc:
+        raise RuntimeError(f"w4_ref_linear failed: {rc}")
+    return Y
+
+
+def bf16_bits_to_f64(a: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns to fp64 (bit placement, no arithmetic)."""
+    a = _u16(a)
+    return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def within_linear_tolerance(y: np.ndarray, y_ref: np.ndarray):
+    """The linear's acceptance test: |y - y_ref| <= 4e-3 |y_ref| + 1e-2 rms(y_ref),
+    rms taken over the whole output of one call.  Returns (ok, worst ratio)."""
+    y = np.asarray(y, np.float64)
+    y_ref = np.asarray(y_ref, np.float64)
+    rms = float(np.sqrt(np.mean(y_ref * y_ref))) if y_ref.size else 0.0
+    bound = 4e-3 * np.abs(y_ref) + 1e-2 * rms
+    err = np.abs(y - y_ref)
+    if y_ref.size == 0:
+        return True, 0.0
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(bound > 0, err / bound, np.where(err > 0, np.inf, 0.0))
+    worst = float(np.max(ratio))
+    return bool(np.all(err <= bound)), worst

@@ -1,0 +1,224 @@
+/*
+ * w4_oracle.c -- plain, slow CPU oracle for group-wise int4 weight-only
+ * quantization and the mixed bf16 x int4 linear.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call this code:
+ * only the test-suite, the smoke check and the CPU-baseline leg of the
+ * benchmark load it.  It shares no code, header, table or constant with the
+ * CUDA library; the only thing both sides share is the seeded input
+ * generator, which holds none of the method's arithmetic.
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -shared -fPIC.
+ * On x86-64 float arithmetic is IEEE binary32 with round-to-nearest-even, and
+ * -ffp-contract=off forbids fusing a*b+c, so every float operation below is
+ * exactly one correctly rounded IEEE operation.
+ *
+ * What the pages fix, and where:
+ *  - weights below 8 bits are projected group-wise and affinely, with an
+ *    offset ("zero point"):  Optimum Quanto, "Design overview / Tensors";
+ *  - the integer mapping is plain rounding, torch.round(), which rounds half
+ *    to even:  Optimum Quanto, "Design overview / Tensors";
+ *  - the projection aims to avoid saturated and flushed values, so the whole
+ *    [min, max] of a group maps onto the code range:  same section;
+ *  - weights are grouped along their first axis (output features), i.e. the
+ *    groups of W[N,K] run along K inside one output row:  Optimum Quanto,
+ *    "Design overview / Modules" and "Pitfalls when quantizing activations";
+ *  - group sizes 32 / 64 / 128:  torchao README "Quick start"; torchao guide
+ *    section 3.1; TorchAO 0.14.0 release notes "Deprecations";
+ *  - the matmul result is accumulated at higher precision than its inputs:
+ *    Optimum Quanto, "Pitfalls when quantizing activations".
+ * The concrete formulas (scale = (max-min)/15 with an eps clamp,
+ * q = clamp(rne((w-min)/scale), 0, 15), w' = q*scale + min) are the plainest
+ * reading consistent with all of the above; the readings of points the pages
+ * leave open (eps value, stored-scale coding, -0 ordering, nibble order) are
+ * marked "reading" below.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <math.h>
+
+/* reading: the pages say nothing about the clamp; 1e-6 (fp32) keeps the
+ * clamp inactive for every non-constant group of realistic weights. */
+#define REF_EPS 1e-6f
+
+/* ---- bf16 <-> fp32 ---------------------------------------------------- */
+
+/* A bf16 value is the top 16 bits of the fp32 value: exact widening. */
+static float ref_bf16_to_float(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Round an fp32 value to the nearest bf16, ties to even.  The format is
+ * sign-magnitude, so rounding the 32-bit pattern at bit 16 rounds the
+ * magnitude; a carry out of the mantissa correctly bumps the exponent. */
+static uint16_t ref_float_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0u)
+        return (uint16_t)((u >> 16) | 0x0040u); /* keep NaN a (quiet) NaN */
+    uint32_t upper = u >> 16;
+    uint32_t rest = u & 0xFFFFu;
+    if (rest > 0x8000u || (rest == 0x8000u && (upper & 1u)))
+        upper += 1u;
+    return (uint16_t)upper;
+}
+
+/* Total order used for the group min / max: the usual < on finite values,
+ * and -0.0 below +0.0 (reading: the pages leave the choice between two equal
+ * zeros open; this one makes the result independent of scan order). */
+static int ref_less(float a, float b)
+{
+    if (a < b)
+        return 1;
+    if (a == 0.0f && b == 0.0f)
+        return signbit(a) && !signbit(b);
+    return 0;
+}
+
+static int ref_group_ok(int64_t N, int64_t K, int g)
+{
+    if (g != 32 && g != 64 && g != 128)
+        return 0;
+    if (N < 0 || K <= 0 || K % g != 0)
+        return 0;
+    return 1;
+}
+
+/* ---- quantize --------------------------------------------------------- */
+
+/*
+ * W[N,K] bf16 (row-major)  ->  Wq[N,K/2] packed codes, scales[N,K/g] bf16,
+ * offsets[N,K/g] bf16.  For each row n and each group j of g consecutive
+ * k, in this order:
+ *   1. mn, mx = min and max of the group (ref_less order);
+ *   2. s32 = (mx - mn) / 15, two IEEE fp32 operations;
+ *   3. s32 = eps if s32 < eps;
+ *   4. s = bf16(s32): the stored scale; the codes are computed with it
+ *      (reading: coding with the stored scale keeps w' self-consistent);
+ *   5. o = mn, stored as bf16 (exact, mn already is a bf16 value);
+ *   6. q = clamp(round_half_even((w - o) / s), 0, 15), fp32 subtract and
+ *      divide, then rintf() in the default round-to-nearest-even mode;
+ *   7. codes k = 2p and 2p+1 share byte p of the row: even k in the low
+ *      nibble (reading: the pages name packing formats but define none).
+ * Returns 0, or -1 on an unsupported shape.
+ */
+int w4_ref_quantize(const uint16_t *W, int64_t N, int64_t K, int g,
+                    uint8_t *Wq, uint16_t *scales, uint16_t *offsets)
+{
+    if (!ref_group_ok(N, K, g))
+        return -1;
+    const int64_t groups = K / g;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t j = 0; j < groups; ++j) {
+            const uint16_t *wg = W + n * K + j * g;
+            float mn = ref_bf16_to_float(wg[0]);
+            float mx = mn;
+            for (int i = 1; i < g; ++i) {
+                float v = ref_bf16_to_float(wg[i]);
+                if (ref_less(v, mn))
+                    mn = v;
+                if (ref_less(mx, v))
+                    mx = v;
+            }
+            float range = mx - mn;
+            float s32 = range / 15.0f;
+            if (s32 < REF_EPS)
+                s32 = REF_EPS;
+            uint16_t s_bits = ref_float_to_bf16(s32);
+            uint16_t o_bits = ref_float_to_bf16(mn);
+            float s = ref_bf16_to_float(s_bits);
+            float o = ref_bf16_to_float(o_bits);
+            scales[n * groups + j] = s_bits;
+            offsets[n * groups + j] = o_bits;
+            for (int i = 0; i < g; ++i) {
+                float v = ref_bf16_to_float(wg[i]);
+                float d = v - o;
+                float t = d / s;
+                float r = rintf(t);
+                int q = (int)r;
+                if (q < 0)
+                    q = 0;
+                if (q > 15)
+                    q = 15;
+                int64_t k = j * g + i;
+                uint8_t *byte = Wq + n * (K / 2) + k / 2;
+                if ((k & 1) == 0)
+                    *byte = (uint8_t)q;
+                else
+                    *byte = (uint8_t)(*byte | (q << 4));
+            }
+        }
+    }
+    return 0;
+}
+
+/* ---- dequantize ------------------------------------------------------- */
+
+/* One weight: w' = bf16( fp32(q) * s + o ), one fp32 multiply (exact: a
+ * 4-bit integer times an 8-bit significand), one fp32 add, then rounding to
+ * bf16.  Optimum Quanto, "Pitfalls when quantizing activations": the result
+ * of the quantized matmul is brought back to float. */
+static uint16_t ref_dequant_one(const uint8_t *Wq, const uint16_t *scales,
+                                const uint16_t *offsets, int64_t K, int g,
+                                int64_t n, int64_t k)
+{
+    uint8_t byte = Wq[n * (K / 2) + k / 2];
+    int q = (k & 1) ? (byte >> 4) : (byte & 0x0F);
+    float s = ref_bf16_to_float(scales[n * (K / g) + k / g]);
+    float o = ref_bf16_to_float(offsets[n * (K / g) + k / g]);
+    float t = (float)q * s;
+    float u = t + o;
+    return ref_float_to_bf16(u);
+}
+
+int w4_ref_dequantize(const uint8_t *Wq, const uint16_t *scales,
+                      const uint16_t *offsets, int64_t N, int64_t K, int g,
+                      uint16_t *W_out)
+{
+    if (!ref_group_ok(N, K, g))
+        return -1;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k)
+            W_out[n * K + k] = ref_dequant_one(Wq, scales, offsets, K, g, n, k);
+    return 0;
+}
+
+/* ---- linear ----------------------------------------------------------- */
+
+/*
+ * Y[m,n] = sum_k X[m,k] * W'[n,k] in fp64, with W' the bf16 dequantized
+ * weights of w4_ref_dequantize: the reference value y_ref of the tolerance
+ * |y - y_ref| <= 4e-3 |y_ref| + 1e-2 rms(y_ref).  Y is fp64 [M,N].
+ */
+int w4_ref_linear(const uint16_t *X, int64_t M, int64_t K, const uint8_t *Wq,
+                  const uint16_t *scales, const uint16_t *offsets, int64_t N,
+                  int g, double *Y)
+{
+    if (!ref_group_ok(N, K, g) || M < 0)
+        return -1;
+    double *wrow = (double *)malloc((size_t)K * sizeof(double));
+    if (wrow == NULL)
+        return -2;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t k = 0; k < K; ++k)
+            wrow[k] = (double)ref_bf16_to_float(
+                ref_dequant_one(Wq, scales, offsets, K, g, n, k));
+        for (int64_t m = 0; m < M; ++m) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += (double)ref_bf16_to_float(X[m * K + k]) * wrow[k];
+            Y[m * N + n] = acc;
+        }
+    }
+    free(wrow);
+    return 0;
+}
+
+/* The clamp constant, exported so tests can state which reading they pin. */
+float w4_ref_eps(void) { return REF_EPS; }

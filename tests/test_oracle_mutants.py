@@ -1,0 +1,108 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each mutant is a temporary copy of oracle/w4_oracle.c with one planted error
+(a dropped term, a wrong rounding, a swapped index ...), compiled with gcc and
+loaded on the CPU.  The worked examples, invariants and closed forms of
+test_oracle_pins.py must reject every one of them.  Nothing here touches a GPU.
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from tests.test_oracle_pins import GOLDEN_CASES, unpack_codes
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "w4_oracle.c")
+
+MUTANTS = {
+    "round_half_up": ("float r = rintf(t);", "float r = floorf(t + 0.5f);"),
+    "truncate_codes": ("float r = rintf(t);", "float r = truncf(t);"),
+    "scale_over_16": ("float s32 = range / 15.0f;", "float s32 = range / 16.0f;"),
+    "offset_is_max": ("uint16_t o_bits = ref_float_to_bf16(mn);", "uint16_t o_bits = ref_float_to_bf16(mx);"),
+    "code_with_fp32_scale": ("float t = d / s;", "float t = d / s32;"),
+    "odd_k_in_low_nibble": ("if ((k & 1) == 0)\n                    *byte", "if ((k & 1) == 1)\n                    *byte"),
+    "dequant_drops_offset": ("float u = t + o;", "float u = t;"),
+    "linear_output_transposed": ("Y[m * N + n] = acc;", "Y[n * M + m] = acc;"),
+    "no_eps_clamp": ("if (s32 < REF_EPS)\n                s32 = REF_EPS;", ""),
+    "bf16_truncates": ("upper += 1u;", "upper += 0u;"),
+    "zero_order_ignored": ("return signbit(a) && !signbit(b);", "return 0;"),
+    "scale_not_rounded_to_bf16": ("float s = ref_bf16_to_float(s_bits);", "float s = s32;"),
+}
+
+
+def _build_mutant(tmp_path, name):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} is not unique"
+    c = tmp_path / f"{name}.c"
+    c.write_text(src.replace(old, new))
+    so = tmp_path / f"{name}.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+                    "-o", str(so), str(c), "-lm"], check=True)
+    lib = ctypes.CDLL(str(so))
+    p, i64 = ctypes.c_void_p, ctypes.c_int64
+    lib.w4_ref_quantize.argtypes = [p, i64, i64, ctypes.c_int, p, p, p]
+    lib.w4_ref_dequantize.argtypes = [p, p, p, i64, i64, ctypes.c_int, p]
+    lib.w4_ref_linear.argtypes = [p, i64, i64, p, p, p, i64, ctypes.c_int, p]
+    return lib
+
+
+def _pins_reject(lib) -> bool:
+    """Run the hand-derived examples and one closed form through a mutant;
+    True if any of them disagrees."""
+    P = lambda a: ctypes.c_void_p(a.ctypes.data)
+    for case in GOLDEN_CASES:
+        g = case["g"]
+        W = np.ascontiguousarray(case["values"].reshape(1, g))
+        Wq = np.zeros((1, g // 2), np.uint8)
+        sc = np.zeros((1, 1), np.uint16)
+        of = np.zeros((1, 1), np.uint16)
+        lib.w4_ref_quantize(P(W), 1, g, g, P(Wq), P(sc), P(of))
+        if sc[0, 0] != case["scale"] or of[0, 0] != case["offset"]:
+            return True
+        if not np.array_equal(unpack_codes(Wq)[0], case["codes"]):
+            return True
+        if "bytes" in case and not np.array_equal(Wq[0], case["bytes"]):
+            return True
+        if "deq" in case:
+            out = np.zeros((1, g), np.uint16)
+            lib.w4_ref_dequantize(P(Wq), P(sc), P(of), 1, g, g, P(out))
+            if not np.array_equal(out[0], case["deq"]):
+                return True
+    # one-hot closed form of the linear: X = e_k -> Y[k, n] = W'[n, k]
+    g, N, K = 32, 3, 32
+    case = GOLDEN_CASES[0]
+    W = np.ascontiguousarray(np.tile(case["values"], (N, 1)))
+    Wq = np.zeros((N, K // 2), np.uint8)
+    sc = np.zeros((N, 1), np.uint16)
+    of = np.zeros((N, 1), np.uint16)
+    lib.w4_ref_quantize(P(W), N, K, g, P(Wq), P(sc), P(of))
+    X = np.zeros((K, K), np.uint16)
+    X[np.arange(K), np.arange(K)] = 0x3F80
+    Y = np.zeros((K, N), np.float64)
+    lib.w4_ref_linear(P(X), K, K, P(Wq), P(sc), P(of), N, g, P(Y))
+    expect = oracle.bf16_bits_to_f64(case["deq"])
+    return not np.array_equal(Y, np.tile(expect[:, None], (1, N)))
+
+
+def test_unmutated_oracle_passes(tmp_path):
+    src = open(SRC).read()
+    c = tmp_path / "clean.c"
+    c.write_text(src)
+    so = tmp_path / "clean.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+                    "-o", str(so), str(c), "-lm"], check=True)
+    lib = ctypes.CDLL(str(so))
+    p, i64 = ctypes.c_void_p, ctypes.c_int64
+    lib.w4_ref_quantize.argtypes = [p, i64, i64, ctypes.c_int, p, p, p]
+    lib.w4_ref_dequantize.argtypes = [p, p, p, i64, i64, ctypes.c_int, p]
+    lib.w4_ref_linear.argtypes = [p, i64, i64, p, p, p, i64, ctypes.c_int, p]
+    assert not _pins_reject(lib)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(tmp_path, name):
+    assert _pins_reject(_build_mutant(tmp_path, name)), f"pins did not catch mutant {name}"

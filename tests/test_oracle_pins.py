@@ -1,0 +1,315 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+* hand-derived worked examples (tests/golden/quantize_worked_examples.txt);
+* exact-arithmetic invariants of the affine group projection (Optimum Quanto,
+  "Design overview / Tensors"): codes in [0, 15], |w - w'| <= s/2, the group
+  minimum codes to 0 and the maximum to 15, the scale is range/15 up to bf16
+  rounding, constant groups come back exactly;
+* brute force over all 16 codes for the half-to-even rounding (torch.round);
+* the memory ratio "about float bits / integer bits" (Optimum Quanto,
+  "Performance");
+* smaller groups are at least as accurate (torchao guide, section 3.1 tip);
+* the fp64 linear against one-hot closed forms, a pure-Python triple loop and
+  numpy's float64 matmul.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_weight_quantization_02_b300 import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "quantize_worked_examples.txt")
+
+
+def _bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _expand(tokens):
+    out = []
+    for t in tokens:
+        if "*" in t:
+            v, n = t.split("*")
+            out.extend([v] * int(n))
+        else:
+            out.append(t)
+    return out
+
+
+def load_golden():
+    cases, cur = [], None
+    for raw in open(GOLDEN):
+        line = raw.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, *rest = line.split()
+        if key == "case":
+            cur = {"name": rest[0]}
+        elif key == "end":
+            cases.append(cur)
+            cur = None
+        elif key == "g":
+            cur["g"] = int(rest[0])
+        elif key in ("values", "deq"):
+            cur[key] = np.array([int(v, 16) for v in _expand(rest)], np.uint16)
+        elif key in ("scale", "offset"):
+            cur[key] = int(rest[0], 16)
+        elif key == "codes":
+            cur[key] = np.array([int(v) for v in _expand(rest)], np.int64)
+        elif key == "bytes":
+            cur[key] = np.array([int(v, 16) for v in _expand(rest)], np.uint8)
+        else:
+            raise ValueError(f"bad golden line: {line}")
+    return cases
+
+
+GOLDEN_CASES = load_golden()
+
+
+def unpack_codes(Wq: np.ndarray) -> np.ndarray:
+    """Packed bytes [N, K/2] -> codes [N, K]; even k in the low nibble."""
+    lo = (Wq & 0x0F).astype(np.int64)
+    hi = (Wq >> 4).astype(np.int64)
+    return np.stack([lo, hi], axis=-1).reshape(Wq.shape[0], -1)
+
+
+def bits_f64(a):
+    return oracle.bf16_bits_to_f64(np.ascontiguousarray(a, np.uint16))
+
+
+def test_golden_file_is_complete():
+    assert len(GOLDEN_CASES) >= 9
+    for c in GOLDEN_CASES:
+        assert len(c["values"]) == c["g"], c["name"]
+        assert len(c["codes"]) == c["g"], c["name"]
+        if "deq" in c:
+            assert len(c["deq"]) == c["g"], c["name"]
+
+
+@pytest.mark.parametrize("case", GOLDEN_CASES, ids=[c["name"] for c in GOLDEN_CASES])
+def test_golden_single_group(case):
+    g = case["g"]
+    W = case["values"].reshape(1, g)
+    Wq, sc, of = oracle.ref_quantize(W, g)
+    assert sc[0, 0] == case["scale"], f"scale {sc[0,0]:04X} != {case['scale']:04X}"
+    assert of[0, 0] == case["offset"], f"offset {of[0,0]:04X} != {case['offset']:04X}"
+    np.testing.assert_array_equal(unpack_codes(Wq)[0], case["codes"])
+    if "bytes" in case:
+        np.testing.assert_array_equal(Wq[0], case["bytes"])
+    if "deq" in case:
+        np.testing.assert_array_equal(oracle.ref_dequantize(Wq, sc, of, g)[0], case["deq"])
+
+
+@pytest.mark.parametrize("case", GOLDEN_CASES, ids=[c["name"] for c in GOLDEN_CASES])
+def test_golden_group_embedded_in_matrix(case):
+    """The worked group placed at row 2, group 3 of a random 4 x 5g matrix: the
+    oracle must put its outputs at that position (pins row/group indexing)."""
+    g = case["g"]
+    rng = np.random.default_rng(7)
+    W = _bits(torch.from_numpy(rng.normal(0, 0.02, (4, 5 * g)).astype(np.float32)).to(torch.bfloat16)).copy()
+    W[2, 3 * g:4 * g] = case["values"]
+    Wq, sc, of = oracle.ref_quantize(W, g)
+    assert sc[2, 3] == case["scale"]
+    assert of[2, 3] == case["offset"]
+    np.testing.assert_array_equal(unpack_codes(Wq)[2, 3 * g:4 * g], case["codes"])
+    if "deq" in case:
+        np.testing.assert_array_equal(oracle.ref_dequantize(Wq, sc, of, g)[2, 3 * g:4 * g], case["deq"])
+
+
+def adversarial_matrix(g: int, seed: int = 3) -> np.ndarray:
+    """Rows of random groups plus hand-picked awkward ones: constant, two-valued,
+    signed zeros, tiny (subnormal-range) values, a huge range, exact half-steps."""
+    rng = np.random.default_rng(seed)
+    rows = []
+    base = rng.normal(0, 0.02, (24, 4 * g)).astype(np.float32)
+    base[5] *= 100.0
+    base[6] *= 1e-37  # bf16 subnormal range (|w| ~ 2e-39)
+    base[7] = rng.choice([-1.0, 3.0], size=4 * g)
+    base[8] = 0.0
+    base[8, ::3] = -0.0
+    base[9] = 0.123
+    base[10] = rng.normal(0, 1e37, 4 * g)  # large but finite range
+    base[11] = (rng.integers(0, 31, 4 * g) * 0.5 - 3.0)  # many exact half-steps
+    rows.append(base)
+    W = torch.from_numpy(np.concatenate(rows)).to(torch.bfloat16)
+    return _bits(W).copy()
+
+
+@pytest.mark.parametrize("g", [32, 64, 128])
+@pytest.mark.parametrize("src", ["normal_outliers", "adversarial"])
+def test_affine_projection_invariants(g, src):
+    if src == "normal_outliers":
+        W = _bits(workloads.gen_weight(64, 8 * g, seed=11, outliers=True))
+    else:
+        W = adversarial_matrix(g)
+    N, K = W.shape
+    Wq, sc, of = oracle.ref_quantize(W, g)
+    q = unpack_codes(Wq)
+    assert q.min() >= 0 and q.max() <= 15
+    w = bits_f64(W).reshape(N, K // g, g)
+    s = bits_f64(sc)[..., None]
+    o = bits_f64(of)[..., None]
+    qg = q.reshape(N, K // g, g).astype(np.float64)
+    # |w - (q s + o)| <= s/2, up to the fp32 rounding of the subtract and the divide
+    err = np.abs(w - (qg * s + o))
+    assert np.all(err <= s / 2 * (1 + 2.0 ** -16)), float(np.max(err / s))
+    # the offset is the group minimum and codes to 0
+    np.testing.assert_array_equal(o[..., 0], w.min(axis=-1))
+    amin = w.argmin(axis=-1)
+    assert np.all(np.take_along_axis(qg, amin[..., None], -1) == 0)
+    # the scale is (max - min)/15 up to bf16 rounding, unless the eps clamp is active
+    rng_ = w.max(axis=-1) - w.min(axis=-1)
+    ideal = rng_ / 15.0
+    eps = oracle.ref_eps()
+    unclamped = ideal > eps * (1 + 2.0 ** -8)
+    rel = np.abs(s[..., 0] - ideal) / np.where(ideal > 0, ideal, 1.0)
+    assert np.all(rel[unclamped] <= 2.0 ** -8)
+    assert np.all(s[..., 0][~unclamped] >= eps * (1 - 2.0 ** -8))
+    # and the group maximum then codes to 15
+    amax = w.argmax(axis=-1)
+    qmax = np.take_along_axis(qg, amax[..., None], -1)[..., 0]
+    assert np.all(qmax[unclamped] == 15)
+
+
+def _nearest_even_code(t: np.float32) -> int:
+    """Brute force: the code in [0, 15] nearest to t, ties to the even code."""
+    best, best_d = None, None
+    for c in range(16):
+        d = abs(float(t) - c)
+        if best is None or d < best_d or (d == best_d and c % 2 == 0):
+            best, best_d = c, d
+    return best
+
+
+@pytest.mark.parametrize("g", [32, 64, 128])
+def test_rounding_by_brute_force(g):
+    """Every code is the nearest of the 16 codes to the fp32 quotient
+    (w - o)/s, ties to even (torch.round), saturating at 0 and 15."""
+    W = np.concatenate([_bits(workloads.gen_weight(6, 2 * g, seed=21 + g)), adversarial_matrix(g)[:12, :2 * g]])
+    Wq, sc, of = oracle.ref_quantize(W, g)
+    q = unpack_codes(Wq)
+    N, K = W.shape
+    wf = (W.astype(np.uint32) << 16).view(np.float32)
+    sf = (sc.astype(np.uint32) << 16).view(np.float32)
+    of_ = (of.astype(np.uint32) << 16).view(np.float32)
+    for n in range(N):
+        for k in range(K):
+            j = k // g
+            t = np.float32(np.float32(wf[n, k]) - of_[n, j]) / sf[n, j]
+            assert q[n, k] == _nearest_even_code(t), (n, k, float(t))
+
+
+@pytest.mark.parametrize("g", [32, 64, 128])
+def test_dequantize_is_q_times_s_plus_o(g):
+    W = _bits(workloads.gen_weight(32, 4 * g, seed=5, outliers=True))
+    Wq, sc, of = oracle.ref_quantize(W, g)
+    Wd = oracle.ref_dequantize(Wq, sc, of, g)
+    q = unpack_codes(Wq).astype(np.float64)
+    s = np.repeat(bits_f64(sc), g, axis=1)
+    o = np.repeat(bits_f64(of), g, axis=1)
+    exact = q * s + o
+    wd = bits_f64(Wd)
+    # one fp32 rounding then one bf16 rounding: within half a bf16 ulp plus half an fp32 ulp
+    ulp_bf16 = np.spacing(np.abs(wd).astype(np.float32)).astype(np.float64) * 2 ** 16
+    assert np.all(np.abs(wd - exact) <= ulp_bf16 / 2 + ulp_bf16 / 2 ** 17)
+
+
+@pytest.mark.parametrize("g", [32, 64, 128])
+def test_memory_ratio(g):
+    """Device memory ~ float bits / integer bits: 4/16 for the codes plus two
+    bf16 qparams per group, i.e. exactly (4 + 32/g)/16 of the bf16 weights."""
+    W = _bits(workloads.gen_weight(16, 2 * g, seed=1))
+    Wq, sc, of = oracle.ref_quantize(W, g)
+    ratio = (Wq.nbytes + sc.nbytes + of.nbytes) / W.nbytes
+    assert ratio == pytest.approx((4 + 32 / g) / 16, abs=0)
+    assert abs(ratio - 4 / 16) <= 32 / g / 16 + 1e-12
+
+
+def test_smaller_groups_are_at_least_as_accurate():
+    W = _bits(workloads.gen_weight(256, 1024, seed=9, outliers=True))
+    errs = []
+    for g in (32, 64, 128):
+        Wq, sc, of = oracle.ref_quantize(W, g)
+        errs.append(float(np.mean(np.abs(bits_f64(oracle.ref_dequantize(Wq, sc, of, g)) - bits_f64(W)))))
+    assert errs[0] <= errs[1] <= errs[2], errs
+
+
+def test_rows_quantize_independently():
+    W = _bits(workloads.gen_weight(40, 256, seed=2, outliers=True))
+    full = oracle.ref_quantize(W, 64)
+    part = oracle.ref_quantize(W[13:29], 64)
+    for a, b in zip(full, part):
+        np.testing.assert_array_equal(a[13:29], b)
+
+
+def test_unsupported_shapes_rejected():
+    W = np.zeros((2, 96), np.uint16)
+    with pytest.raises(ValueError):
+        oracle.ref_quantize(W, 64)
+    with pytest.raises(ValueError):
+        oracle.ref_quantize(np.zeros((2, 64), np.uint16), 16)
+
+
+# ---- the fp64 linear -------------------------------------------------------
+
+def _packed(N, K, g, seed):
+    W = _bits(workloads.gen_weight(N, K, seed=seed, outliers=True))
+    return oracle.ref_quantize(W, g)
+
+
+@pytest.mark.parametrize("g", [32, 128])
+def test_linear_one_hot_picks_a_column(g):
+    """X = e_k gives y[n] = W'[n, k] exactly: pins which operand is transposed."""
+    N, K = 24, 2 * g
+    Wq, sc, of = _packed(N, K, g, 31)
+    Wd = bits_f64(oracle.ref_dequantize(Wq, sc, of, g))
+    X = np.zeros((K, K), np.uint16)
+    X[np.arange(K), np.arange(K)] = 0x3F80  # 1.0
+    Y = oracle.ref_linear(X, Wq, sc, of, g)
+    np.testing.assert_array_equal(Y, Wd.T)
+
+
+def test_linear_brute_force_triple_loop():
+    g, M, N, K = 32, 3, 5, 64
+    Wq, sc, of = _packed(N, K, g, 41)
+    X = _bits(workloads.gen_activation(M, K, seed=42))
+    Wd = bits_f64(oracle.ref_dequantize(Wq, sc, of, g))
+    Xd = bits_f64(X)
+    Y = oracle.ref_linear(X, Wq, sc, of, g)
+    for m in range(M):
+        for n in range(N):
+            acc = 0.0
+            for k in range(K):
+                acc += Xd[m, k] * Wd[n, k]
+            assert Y[m, n] == acc
+
+
+@pytest.mark.parametrize("shape", [(1, 7, 32), (4, 33, 96), (9, 64, 256)])
+def test_linear_matches_numpy_float64(shape):
+    M, N, K = shape
+    g = 32
+    Wq, sc, of = _packed(N, K, g, 51 + N)
+    X = _bits(workloads.gen_activation(M, K, seed=52 + N))
+    Y = oracle.ref_linear(X, Wq, sc, of, g)
+    ref = bits_f64(X) @ bits_f64(oracle.ref_dequantize(Wq, sc, of, g)).T
+    np.testing.assert_allclose(Y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_linear_scales_exactly_with_powers_of_two():
+    g, M, N, K = 64, 2, 8, 128
+    Wq, sc, of = _packed(N, K, g, 61)
+    X = _bits(workloads.gen_activation(M, K, seed=62))
+    X4 = _bits((torch.from_numpy(bits_f64(X)).to(torch.float32) * 4).to(torch.bfloat16))
+    np.testing.assert_array_equal(oracle.ref_linear(X4, Wq, sc, of, g), 4 * oracle.ref_linear(X, Wq, sc, of, g))
+
+
+def test_tolerance_rule():
+    """|y - y_ref| <= 4e-3 |y_ref| + 1e-2 rms(y_ref), rms over the whole output."""
+    y_ref = np.array([3.0, -4.0, 0.0, 0.0])  # rms = 2.5
+    ok, _ = oracle.within_linear_tolerance(y_ref + np.array([0.012 + 0.025, 0, 0.025, -0.025]), y_ref)
+    assert ok
+    ok, worst = oracle.within_linear_tolerance(y_ref + np.array([0, 0, 0.0251, 0]), y_ref)
+    assert not ok and worst > 1.0
