@@ -1,0 +1,560 @@
+#!/usr/bin/env python3
+"""Benchmark of libw4 on one B300 (or N independent replicas under torchrun).
+
+Headline: w4_linear HBM throughput in the M=1 decode regime on the Llama-3-8B
+decode linears (int4, g=32, 0.1 % x10 outlier weights), one step = one pass
+of M=1 through the 7 linears (q, k, v, o, gate, up, down) of all 32 blocks,
+224 skinny-kernel launches replayed from one CUDA graph.  The 4.4 GB of packed
+weights per step are larger than L2, so every step streams them from HBM.
+value = algorithmic bytes (N*K/2 + 4*N*K/g + 2*M*K + 2*M*N per linear) / time.
+
+The same JSON line carries the other rows of the hot path: the tcgen05
+prefill GEMMs (TFLOP/s), batched decode (M = 2..32, g=64), the full 32-block
+g=128 stack at M=1 and M=16, w4_quantize and w4_dequantize throughput, the
+roofline of the dominant kernel, the end-to-end number through the public API
+with host buffers, the CPU oracle timed on a bounded sample, and the SM clocks
+sampled during the measurements.
+
+--impl reference times the CPU oracle (the slow, plain definition of the
+method) on the same workload and metric, a bounded sample per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "w4_linear HBM GB/s (M=1 decode) & TFLOP/s (prefill) vs roofline"
+WORKLOAD = ("Llama-3-8B decode linears, M=1, int4 g=32, W~N(0,0.02) with 0.1% outliers x10, X~N(0,1) bf16; "
+            "one step = q,k,v,o,gate,up,down of 32 blocks (224 linears, 4.36 GB packed)")
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+# --------------------------------------------------------------------------- helpers
+
+def linear_bytes(M, N, K, g):
+    """Algorithmic bytes of one w4_linear: packed codes + qparams + X + Y."""
+    return N * K // 2 + 4 * N * K // g + 2 * M * K + 2 * M * N
+
+
+def quantize_bytes(N, K, g):
+    return 2 * N * K + N * K // 2 + 4 * N * K // g
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    return dict(FALLBACK_PEAKS)
+
+
+def source_sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def load_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, keyed by (kernel, shape),
+    valid only while the kernel source still has the hash it was captured with."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    out = {}
+    if not os.path.exists(p):
+        return out
+    for line in open(p):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        kernel, shape, src, sha, nbytes = line.split()
+        if os.path.exists(os.path.join(ROOT, src)) and source_sha(os.path.join(ROOT, src)) == sha:
+            out[(kernel, shape)] = float(nbytes)
+    return out
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the GPU works."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        loaded = [s for s, p in zip(sm, power) if p > 0.25 * max(power)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power)}
+
+
+class Dist:
+    """Rank bookkeeping; the N>1 case runs N independent replicas (no data-path collective)."""
+
+    def __init__(self, backend):
+        import torch.distributed as dist
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.dist = dist
+        self.on = self.world > 1
+        if self.on and not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+    def barrier(self):
+        if self.on:
+            self.dist.barrier()
+
+    def max(self, x: float, device=None) -> float:
+        if not self.on:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.on and self.dist.is_initialized():
+            self.dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def quantize_linears(cases, device, w4, wl):
+    """Quantize each case's weights on the GPU (bf16 freed right after)."""
+    import torch
+    out = []
+    for c in cases:
+        W = wl.gen_weight(c.N, c.K, c.w_seed, outliers=c.outliers, device=device)
+        Wq, sc, of = w4.w4_quantize(W, c.group_size)
+        del W
+        out.append((Wq, sc, of))
+    torch.cuda.synchronize(device)
+    return out
+
+
+class LinearStack:
+    """Packed weights, inputs and outputs of a sequence of linears, with all X in
+    one device buffer and all Y in another (one copy each way per step)."""
+
+    def __init__(self, cases, device, w4, wl, packed=None):
+        import torch
+        self.cases = cases
+        self.device = device
+        self.packed = packed if packed is not None else quantize_linears(cases, device, w4, wl)
+        xs = sum(c.M * c.K for c in cases)
+        ys = sum(c.M * c.N for c in cases)
+        self.X = torch.empty(xs, dtype=torch.bfloat16, device=device)
+        self.Y = torch.empty(ys, dtype=torch.bfloat16, device=device)
+        self.xv, self.yv = [], []
+        xo = yo = 0
+        for c in cases:
+            self.xv.append(self.X[xo:xo + c.M * c.K].view(c.M, c.K))
+            self.yv.append(self.Y[yo:yo + c.M * c.N].view(c.M, c.N))
+            self.xv[-1].copy_(wl.gen_activation(c.M, c.K, c.x_seed, device=device))
+            xo += c.M * c.K
+            yo += c.M * c.N
+        need = max(w4.w4_linear_workspace_bytes(c.M, c.N, c.K, c.group_size) for c in cases)
+        self.ws = w4.Workspace(device, need)
+        self.bytes = sum(linear_bytes(c.M, c.N, c.K, c.group_size) for c in cases)
+        self.flops = sum(2 * c.M * c.N * c.K for c in cases)
+        self.w4 = w4
+
+    def run(self):
+        for c, x, y, (Wq, sc, of) in zip(self.cases, self.xv, self.yv, self.packed):
+            self.w4.w4_linear(x, Wq, sc, of, c.group_size, out=y, workspace=self.ws)
+
+    def capture(self, stream):
+        import torch
+        with torch.cuda.stream(stream):
+            self.run()  # warm-up on the capture stream (kernel attributes set, nothing allocated)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                self.run()
+        return g
+
+
+def time_region(fn, steps, warmup, stream, dist, device):
+    """W untimed steps, then K steps between events on `stream`, barrier + sync on both sides;
+    returns the max over ranks of the elapsed milliseconds."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize(device)
+    dist.barrier()
+    torch.cuda.synchronize(device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    dist.barrier()
+    ms = start.elapsed_time(end)
+    return dist.max(ms, device)
+
+
+def time_each(fn, iters, stream, flush=None):
+    """Median event time of single calls, optionally flushing L2 before each."""
+    import torch
+    ts = []
+    for _ in range(iters):
+        if flush is not None:
+            flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def gpu_arm(args):
+    import torch
+    import bit_weight_quantization_02_b300 as w4
+    from bit_weight_quantization_02_b300 import workloads as wl
+
+    dist = Dist("nccl")
+    device = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(device)
+    w4.load_library()
+    peaks = load_peaks()
+    traffic = load_traffic()
+    stream = torch.cuda.Stream(device)
+    clocks = ClockSampler(dist.local_rank).start()
+
+    # ---- headline: M=1 decode through 32 blocks of Llama-3-8B linears (g=32)
+    cases = [c for layer in range(wl.LLAMA3_8B_LAYERS) for c in wl.config2(layer)]
+    stack = LinearStack(cases, device, w4, wl)
+    graph = stack.capture(stream)
+    with torch.cuda.stream(stream):
+        ms = time_region(graph.replay, args.steps, args.warmup, stream, dist, device)
+    step_ms = ms / args.steps
+    units = stack.bytes * args.steps * dist.world
+    value = units / (ms * 1e-3) / 1e9
+    launches = len(cases) * args.steps
+    # dominant kernel: the skinny decode kernel is the only kernel of the step
+    achieved = stack.bytes / (step_ms * 1e-3) / 1e9
+    tr = traffic.get(("skinny_kernel", "llama3_8b_decode_step"))
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": (round(tr / len(cases)) if tr is not None else None),
+                "algorithmic_bytes_per_launch": round(stack.bytes / len(cases)),
+                "peak_source": f"{peaks['source']} copy bandwidth (MEASURED_PEAKS hbm_gbs)"
+                if peaks["source"] == "measured" else "fallback 6.4 TB/s",
+                "frac_of_nominal_8TBs": round(achieved / 8000.0, 4)}
+
+    # ---- end to end through the public API with host buffers: pinned X -> device,
+    # the captured linears, Y -> pinned host, every step
+    xh = torch.empty(stack.X.shape, dtype=torch.bfloat16, pin_memory=True)
+    xh.copy_(stack.X)
+    yh = torch.empty(stack.Y.shape, dtype=torch.bfloat16, pin_memory=True)
+
+    def e2e_step():
+        stack.X.copy_(xh, non_blocking=True)
+        graph.replay()
+        yh.copy_(stack.Y, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_ms = time_region(e2e_step, args.steps, args.warmup, stream, dist, device)
+    e2e_val = stack.bytes * args.steps * dist.world / (e2e_ms * 1e-3) / 1e9
+
+    def e2e_eager_step():
+        stack.X.copy_(xh, non_blocking=True)
+        stack.run()
+        yh.copy_(stack.Y, non_blocking=True)
+
+    eager_steps = max(3, args.steps // 10)
+    with torch.cuda.stream(stream):
+        eager_ms = time_region(e2e_eager_step, eager_steps, 2, stream, dist, device)
+    e2e = {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": stack.X.numel() * 2,
+           "d2h_bytes_per_step": stack.Y.numel() * 2, "ms_per_step": round(e2e_ms / args.steps, 4),
+           "how": "pinned X -> device, CUDA graph of the 224 w4_linear calls, Y -> pinned host, per step",
+           "eager_python_calls": {"value": round(stack.bytes * eager_steps * dist.world / (eager_ms * 1e-3) / 1e9, 1),
+                                  "ms_per_step": round(eager_ms / eager_steps, 4)}}
+
+    rows = {}
+    if not args.headline_only:
+        rows = other_rows(args, w4, wl, device, stream, peaks, dist)
+
+    del graph, stack
+    clk = clocks.stop()
+    cpu = None
+    if dist.rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_sample(args.cpu_seconds)
+
+    if dist.rank == 0:
+        line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": dist.world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic (seeded; random-init Llama-3-8B-shaped weights)",
+                "config": {"workload": WORKLOAD, "l2": "inputs larger than L2 (4.36 GB of packed weights per step)",
+                           "group_size": 32, "M": 1, "linears_per_step": len(cases),
+                           "parallelism": "replicas" if dist.world > 1 else "single GPU"},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+                "clocks": clk, "peaks": {k: peaks.get(k) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained",
+                                                                     "source")},
+                "rows": rows}
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+def other_rows(args, w4, wl, device, stream, peaks, dist):
+    """Prefill GEMMs, batched decode, the g=128 stack, quantize / dequantize."""
+    import torch
+    rows = {}
+    flush_buf = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    # prefill (tcgen05 GEMM), L2 flushed before every timed call
+    pre = []
+    for c in wl.config4():
+        (Wq, sc, of), = quantize_linears([c], device, w4, wl)
+        X = wl.gen_activation(c.M, c.K, c.x_seed, device=device)
+        Y = torch.empty((c.M, c.N), dtype=torch.bfloat16, device=device)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                w4.w4_linear(X, Wq, sc, of, c.group_size, out=Y)
+            t = time_each(lambda: w4.w4_linear(X, Wq, sc, of, c.group_size, out=Y), args.prefill_iters, stream, flush)
+        tf = 2 * c.M * c.N * c.K / (t * 1e-3) / 1e12
+        pre.append({"M": c.M, "N": c.N, "K": c.K, "ms": round(t, 4), "tflops": round(tf, 1),
+                    "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+                    "hbm_gbs": round(linear_bytes(c.M, c.N, c.K, c.group_size) / (t * 1e-3) / 1e9, 1)})
+        del Wq, sc, of, X, Y
+    best = max(pre, key=lambda r: r["tflops"])
+    rows["prefill_gemm"] = {"unit": "TFLOP/s", "cases": pre, "kernel": "gemm_kernel (tcgen05, TMEM accumulators)",
+                            "roofline": {"bound": "tensor", "achieved": best["tflops"], "peak": peaks["bf16_tflops"],
+                                         "unit": "TFLOP/s", "frac": round(best["tflops"] / peaks["bf16_tflops"], 4),
+                                         "traffic": None,
+                                         "peak_source": "MEASURED_PEAKS bf16_tflops (burst, kernel timed alone)"},
+                            "l2": "flushed (512 MB write) before every timed call"}
+
+    # batched decode, config 3 (g=64): weights rotated through copies totalling > 4x L2
+    b3 = []
+    for c in wl.config3():
+        (Wq, sc, of), = quantize_linears([c], device, w4, wl)
+        copies = max(2, int(4 * 126e6 // (c.N * c.K * 0.5625)) + 1)
+        reps = [(Wq.clone(), sc.clone(), of.clone()) for _ in range(copies)]
+        X = wl.gen_activation(c.M, c.K, c.x_seed, device=device)
+        Y = torch.empty((c.M, c.N), dtype=torch.bfloat16, device=device)
+        ws = w4.Workspace(device).reserve_for(c.M, c.N, c.K, c.group_size)
+        it = {"i": 0}
+
+        def one():
+            r = reps[it["i"] % copies]
+            it["i"] += 1
+            w4.w4_linear(X, *r, c.group_size, out=Y, workspace=ws)
+
+        with torch.cuda.stream(stream):
+            g = torch.cuda.CUDAGraph()
+            one()
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(copies):
+                    one()
+            t = time_region(g.replay, 20, 3, stream, dist, device) / (20 * copies)
+        gbs = linear_bytes(c.M, c.N, c.K, c.group_size) / (t * 1e-3) / 1e9
+        b3.append({"M": c.M, "N": c.N, "K": c.K, "us": round(t * 1e3, 2), "gbs": round(gbs, 1),
+                   "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
+                   "tflops": round(2 * c.M * c.N * c.K / (t * 1e-3) / 1e12, 2)})
+        del reps, Wq, sc, of, g
+    rows["batched_decode_g64"] = {"unit": "GB/s", "cases": b3,
+                                  "l2": "graph of back-to-back calls over weight copies totalling > 4x L2"}
+
+    # full 32-block stack at g=128: quantize every weight, then M=1 and M=16 passes
+    torch.cuda.synchronize(device)
+    c5 = wl.config5(1)
+    t0 = time.perf_counter()
+    packed = []
+    qbytes = 0
+    q_ms = 0.0
+    for c in c5:
+        W = wl.gen_weight(c.N, c.K, c.w_seed, device=device)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        packed.append(w4.w4_quantize(W, c.group_size))
+        b.record()
+        b.synchronize()
+        q_ms += a.elapsed_time(b)
+        qbytes += quantize_bytes(c.N, c.K, c.group_size)
+        del W
+    setup_s = time.perf_counter() - t0
+    stack_rows = {"quantize": {"weights": wl.config5_weight_count(), "ms": round(q_ms, 3),
+                               "gbs": round(qbytes / (q_ms * 1e-3) / 1e9, 1),
+                               "frac_of_hbm_peak": round(qbytes / (q_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                               "algorithmic_bytes": qbytes, "setup_s": round(setup_s, 1)}}
+    for M in (1, 16):
+        cases = wl.config5(M)
+        st = LinearStack(cases, device, w4, wl, packed=packed)
+        g = st.capture(stream)
+        with torch.cuda.stream(stream):
+            t = time_region(g.replay, 10, 3, stream, dist, device) / 10
+        stack_rows[f"M{M}"] = {"ms": round(t, 4), "gbs": round(st.bytes / (t * 1e-3) / 1e9, 1),
+                               "frac_of_hbm_peak": round(st.bytes / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                               "algorithmic_bytes": st.bytes}
+        del g, st
+    rows["llama3_8b_stack_g128"] = stack_rows
+    del packed
+
+    # dequantize throughput on the gate/up shape, L2 flushed
+    c = wl.config2()[4]
+    (Wq, sc, of), = quantize_linears([c], device, w4, wl)
+    out = torch.empty((c.N, c.K), dtype=torch.bfloat16, device=device)
+    with torch.cuda.stream(stream):
+        t = time_each(lambda: w4.w4_dequantize(Wq, sc, of, c.group_size, out=out), 20, stream, flush)
+    db = c.N * c.K // 2 + 4 * c.N * c.K // c.group_size + 2 * c.N * c.K
+    rows["dequantize"] = {"N": c.N, "K": c.K, "g": c.group_size, "us": round(t * 1e3, 2),
+                          "gbs": round(db / (t * 1e-3) / 1e9, 1), "frac_of_hbm_peak": round(db / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+    del flush_buf
+    return rows
+
+
+# --------------------------------------------------------------------------- CPU oracle
+
+def _oracle_decode_inputs(cases):
+    import numpy as np
+    import oracle
+    from bit_weight_quantization_02_b300 import workloads as wl
+
+    def bits(t):
+        return t.contiguous().view(__import__("torch").int16).numpy().view(np.uint16)
+
+    prepared = []
+    for c in cases:
+        W = bits(wl.gen_weight(c.N, c.K, c.w_seed, outliers=c.outliers))
+        prepared.append((c, bits(wl.gen_activation(c.M, c.K, c.x_seed)), oracle.ref_quantize(W, c.group_size)))
+    return prepared
+
+
+def cpu_baseline_sample(seconds):
+    """The oracle, as it stands (single-threaded C, fp64 accumulation), on one block's
+    7 decode linears repeated for about `seconds`; GB/s of algorithmic bytes."""
+    import oracle
+    from bit_weight_quantization_02_b300 import workloads as wl
+    prepared = _oracle_decode_inputs(wl.config2(0))
+    nbytes, t_total, passes = 0, 0.0, 0
+    while t_total < seconds or passes == 0:
+        for c, X, (Wq, sc, of) in prepared:
+            t = time.perf_counter()
+            oracle.ref_linear(X, Wq, sc, of, c.group_size)
+            t_total += time.perf_counter() - t
+            nbytes += linear_bytes(c.M, c.N, c.K, c.group_size)
+        passes += 1
+    return {"value": round(nbytes / t_total / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{passes} pass(es) of the 7 M=1 g=32 decode linears of one Llama-3-8B block "
+                      f"({t_total:.1f} s of single-threaded C, fp64 accumulation)",
+            "host_cores_available": os.cpu_count()}
+
+
+def reference_arm(args):
+    """The CPU oracle on the headline workload: one step = one linear of the 224 (the 7
+    shapes in turn), timed on the host; rank 0 only."""
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    import oracle
+    from bit_weight_quantization_02_b300 import workloads as wl
+    prepared = _oracle_decode_inputs(wl.config2(0))
+
+    def step(i):
+        c, X, (Wq, sc, of) = prepared[i % len(prepared)]
+        oracle.ref_linear(X, Wq, sc, of, c.group_size)
+        return linear_bytes(c.M, c.N, c.K, c.group_size)
+
+    for i in range(args.warmup):
+        step(i)
+    nbytes = 0
+    t = time.perf_counter()
+    for i in range(args.steps):
+        nbytes += step(i)
+    el = time.perf_counter() - t
+    value = nbytes / el / 1e9
+    line = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "impl": "reference", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; random-init Llama-3-8B-shaped weights)",
+            "config": {"workload": WORKLOAD, "group_size": 32, "M": 1},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "one of the 7 decode linears of a block per step, in turn "
+                                       "(single-threaded C oracle: dequantize + fp64 dot products)"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- main
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["libw4", "reference"], default="libw4")
+    ap.add_argument("--headline-only", action="store_true", help="skip the secondary rows")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--prefill-iters", type=int, default=10)
+    a = ap.parse_args(argv)
+    if a.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    return a
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -174,12 +174,14 @@ _default_ws = {}
 
 
 def _workspace_for(X: torch.Tensor, M, N, K, g, workspace):
-    if workspace is None:
-        key = (X.device.index, torch.cuda.current_stream(X.device).cuda_stream)
-        workspace = _default_ws.get(key)
-        if workspace is None:
-            workspace = _default_ws[key] = Workspace(X.device)
-    return workspace.reserve_for(M, N, K, g)
+    """The caller's workspace as given, or this stream's default one grown to fit."""
+    if workspace is not None:
+        return workspace
+    key = (X.device.index, torch.cuda.current_stream(X.device).cuda_stream)
+    ws = _default_ws.get(key)
+    if ws is None:
+        ws = _default_ws[key] = Workspace(X.device)
+    return ws.reserve_for(M, N, K, g)
 
 
 def w4_linear_ex(X: torch.Tensor, Wq: torch.Tensor, scales: torch.Tensor, offsets: torch.Tensor,

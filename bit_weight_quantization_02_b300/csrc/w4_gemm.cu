@@ -1,0 +1,354 @@
+// w4_gemm.cu -- compute-bound bf16 x int4 linear for many tokens, on the
+// 5th-generation tensor cores (tcgen05) of sm_103a.
+//
+// Y[m,n] = sum_k X[m,k] * w'[n,k], w' = bf16(q*s + o), fp32 accumulation in
+// tensor memory (Optimum Quanto: bf16 x int4 matmul with higher-precision
+// accumulation, "Pitfalls when quantizing activations").  With M in the
+// thousands this is a dense contraction (2*M*N*K flops against ~0.6 bytes per
+// weight), so the int4 codes are expanded to bf16 on chip and fed to UMMA.
+//
+// One thread block computes a BM x BN = 128 tokens x 256 weight rows tile of
+// Y, walking K in BK = 64 steps through a 3-stage shared-memory ring:
+//   warp 0      TMA producer: X tile (128 x 64 bf16, 128-byte swizzle) and
+//               the packed code tile (256 rows x 32 bytes) per stage;
+//   warp 1      TMEM owner (alloc/dealloc of 256 fp32 columns) and, on one
+//               lane, the UMMA issuer: 4 x tcgen05.mma (M=128, N=256, K=16)
+//               per stage, tcgen05.commit frees the stage;
+//   warps 2..9  dequantization: one weight row per thread, codes from the
+//               staged tile -> bf16 w' written straight into the UMMA B
+//               operand layout (K-major, 128-byte swizzle), then
+//               fence.proxy.async and an mbarrier arrive; afterwards the same
+//               warps run the epilogue (tcgen05.ld -> bf16 -> global).
+// Every mbarrier wait is bounded in time; a block that gives up sets the
+// device fault word, waits (bounded) for its own copies and MMAs, frees its
+// tensor memory and exits.
+#include "w4_device.cuh"
+#include "w4_internal.h"
+
+#include <cuda.h>
+#include <mutex>
+
+namespace w4 {
+
+constexpr int GM_BM = 128;
+constexpr int GM_BN = 256;
+constexpr int GM_BK = 64;
+constexpr int GM_STAGES = 3;
+constexpr int GM_DEQ_WARPS = 8;
+constexpr int GM_THREADS = 64 + GM_DEQ_WARPS * 32;
+constexpr int GM_TMEM_COLS = 256;
+
+constexpr int GM_X_BYTES = GM_BM * GM_BK * 2;  // 16 KB
+constexpr int GM_W_BYTES = GM_BN * GM_BK * 2;  // 32 KB
+constexpr int GM_P_BYTES = GM_BN * GM_BK / 2;  //  8 KB
+constexpr int GM_OFF_X = 0;
+constexpr int GM_OFF_W = GM_OFF_X + GM_STAGES * GM_X_BYTES;
+constexpr int GM_OFF_P = GM_OFF_W + GM_STAGES * GM_W_BYTES;
+constexpr int GM_OFF_BAR = GM_OFF_P + GM_STAGES * GM_P_BYTES;
+constexpr int GM_NBAR = 3 * GM_STAGES + 2;  // full_tma, full_deq, empty per stage; tmem_full; drain
+constexpr int GM_OFF_MISC = GM_OFF_BAR + GM_NBAR * 8;
+constexpr int GM_SMEM_USED = GM_OFF_MISC + 16;
+constexpr int GM_SMEM_BYTES = GM_SMEM_USED + 1024;  // + alignment slack for the 1024-byte swizzle atoms
+
+constexpr uint64_t GM_WAIT_LIMIT_NS = 2000000000ull;   // 2 s per wait
+constexpr uint64_t GM_DRAIN_LIMIT_NS = 1000000000ull;  // 1 s per drain wait
+
+__device__ unsigned int g_gemm_fault;
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
+// A and B bf16 (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t gm_idesc() {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(GM_BN >> 3) << 17) | ((uint32_t)(GM_BM >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor for a K-major operand stored as rows of
+// 64 bf16 (128 bytes) with the 128-byte swizzle, 8-row atoms 1024 bytes
+// apart: start address >> 4 (bits 0-13), leading-byte offset 16 B (unused
+// for swizzled K-major, bits 16-29), stride-byte offset 1024 B (bits 32-45),
+// descriptor version 1 (bits 46-47), swizzle mode 2 = 128 B (bits 61-63).
+__device__ __forceinline__ uint64_t gm_sdesc(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(16 >> 4) << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           (1ull << 46) | (2ull << 61);
+}
+
+// Byte offset of 16-byte chunk `c` (k = 8c..8c+7) of row `r` inside a
+// 128-byte-swizzled K-major tile: rows 128 B apart, the chunk index xor-ed
+// with the row's position inside its 8-row atom (what TMA's 128-byte swizzle
+// writes and what the UMMA descriptor above reads).
+__device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
+    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+template <int G>
+__global__ void __launch_bounds__(GM_THREADS, 1)
+gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_p,
+            const uint16_t* __restrict__ scales, const uint16_t* __restrict__ offsets, uint16_t* __restrict__ Y,
+            int M, int N, int K) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + GM_OFF_BAR;
+    auto full_tma = [&](int s) { return bar0 + 8u * s; };
+    auto full_deq = [&](int s) { return bar0 + 8u * (GM_STAGES + s); };
+    auto empty = [&](int s) { return bar0 + 8u * (2 * GM_STAGES + s); };
+    const uint32_t tmem_full = bar0 + 8u * (3 * GM_STAGES);
+    const uint32_t drain = bar0 + 8u * (3 * GM_STAGES + 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + GM_OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + GM_OFF_MISC + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * GM_BN, m0 = blockIdx.y * GM_BM;
+    const int nkb = (K + GM_BK - 1) / GM_BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < GM_STAGES; ++s) {
+            mbar_init(full_tma(s), 1);
+            mbar_init(full_deq(s), GM_DEQ_WARPS * 32);
+            mbar_init(empty(s), 1);
+        }
+        mbar_init(tmem_full, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), GM_TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_x);
+            tma_prefetch_desc(&tm_p);
+            int issued = 0;
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int s = kb % GM_STAGES;
+                const uint32_t ph = (kb / GM_STAGES) & 1;
+                if (!mbar_wait_bounded(empty(s), ph ^ 1, abort_flag, &g_gemm_fault, 1u, GM_WAIT_LIMIT_NS)) break;
+                mbar_arrive_expect_tx(full_tma(s), GM_X_BYTES + GM_P_BYTES);
+                tma_load_2d(sbase + GM_OFF_X + s * GM_X_BYTES, &tm_x, full_tma(s), kb * GM_BK, m0);
+                tma_load_2d(sbase + GM_OFF_P + s * GM_P_BYTES, &tm_p, full_tma(s), kb * (GM_BK / 2), n0);
+                ++issued;
+            }
+            // never leave the block with copies still landing in its shared memory
+            for (int kb = (issued > GM_STAGES ? issued - GM_STAGES : 0); kb < issued; ++kb)
+                mbar_drain_bounded(full_tma(kb % GM_STAGES), (kb / GM_STAGES) & 1, GM_DRAIN_LIMIT_NS);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ UMMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = gm_idesc();
+            int issued = 0;
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int s = kb % GM_STAGES;
+                const uint32_t ph = (kb / GM_STAGES) & 1;
+                if (!mbar_wait_bounded(full_tma(s), ph, abort_flag, &g_gemm_fault, 2u, GM_WAIT_LIMIT_NS)) break;
+                if (!mbar_wait_bounded(full_deq(s), ph, abort_flag, &g_gemm_fault, 2u, GM_WAIT_LIMIT_NS)) break;
+                tc_fence_after();
+                const uint64_t adesc = gm_sdesc(sbase + GM_OFF_X + s * GM_X_BYTES);
+                const uint64_t bdesc = gm_sdesc(sbase + GM_OFF_W + s * GM_W_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < GM_BK / 16; ++kk)  // +32 bytes of K per MMA = +2 in the address field
+                    umma_bf16(tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc, (kb | kk) != 0);
+                umma_commit(empty(s));
+                ++issued;
+            }
+            if (issued == nkb) umma_commit(tmem_full);
+            // the MMAs must be finished before tensor memory is released
+            if (issued > 0) {
+                umma_commit(drain);
+                mbar_drain_bounded(drain, 0, GM_DRAIN_LIMIT_NS);
+            }
+        }
+    } else {
+        // ------------------------------------------------------- dequantization warps
+        const int r = threadIdx.x - 64;  // weight row within the tile, 0..255
+        const int n = n0 + r;
+        const bool nvalid = n < N;
+        const int ng = K / G;
+        const int64_t qrow = (int64_t)(nvalid ? n : 0) * ng;
+        // rows 4..7 of each 8 read their two 16-byte halves in the other order:
+        // the 8 lanes of a quarter-warp then hit 8 distinct bank groups
+        const int hfirst = (r >> 2) & 1;
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int s = kb % GM_STAGES;
+            const uint32_t ph = (kb / GM_STAGES) & 1;
+            if (!mbar_wait_bounded(full_tma(s), ph, abort_flag, &g_gemm_fault, 4u, GM_WAIT_LIMIT_NS)) {
+                ok = false;
+                break;
+            }
+            const unsigned char* prow = smem + GM_OFF_P + s * GM_P_BYTES + r * 32;
+            const uint4 first = *reinterpret_cast<const uint4*>(prow + 16 * hfirst);
+            const uint4 second = *reinterpret_cast<const uint4*>(prow + 16 * (hfirst ^ 1));
+            const uint4 h0 = hfirst ? second : first;
+            const uint4 h1 = hfirst ? first : second;
+            const uint32_t words[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+            unsigned char* wtile = smem + GM_OFF_W + s * GM_W_BYTES;
+            const int kbase = kb * GM_BK;
+            uint32_t s2 = 0, o2 = 0;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {  // 8 codes (one 16-byte bf16 chunk) per step
+                const int k = kbase + 8 * c;
+                if ((8 * c) % G == 0) {  // first chunk of a group inside this k block
+                    const int j = k / G;
+                    uint32_t sv = 0, ov = 0;
+                    if (nvalid && j < ng) {
+                        sv = ldg_nc_u16(scales + qrow + j);
+                        ov = ldg_nc_u16(offsets + qrow + j);
+                    }
+                    s2 = sv | (sv << 16);
+                    o2 = ov | (ov << 16);
+                }
+                uint4 out = make_uint4(0u, 0u, 0u, 0u);
+                if (k < K) {
+                    const uint32_t w = words[c];
+                    const uint32_t p04 = dequant_pair(nib_pair_biased(w), s2, o2);        // (k0, k4)
+                    const uint32_t p15 = dequant_pair(nib_pair_biased(w >> 4), s2, o2);   // (k1, k5)
+                    const uint32_t p26 = dequant_pair(nib_pair_biased(w >> 8), s2, o2);   // (k2, k6)
+                    const uint32_t p37 = dequant_pair(nib_pair_biased(w >> 12), s2, o2);  // (k3, k7)
+                    out.x = __byte_perm(p04, p15, 0x5410);  // (k0, k1)
+                    out.y = __byte_perm(p26, p37, 0x5410);  // (k2, k3)
+                    out.z = __byte_perm(p04, p15, 0x7632);  // (k4, k5)
+                    out.w = __byte_perm(p26, p37, 0x7632);  // (k6, k7)
+                }
+                *reinterpret_cast<uint4*>(wtile + sw128_offset(r, c)) = out;
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(full_deq(s));
+        }
+        // ----------------------------------------------------------------- epilogue
+        if (ok && mbar_wait_bounded(tmem_full, 0, abort_flag, &g_gemm_fault, 8u, GM_WAIT_LIMIT_NS)) {
+            tc_fence_after();
+            const int quad = warp & 3;             // TMEM lanes 32*quad .. +31 (this warp's sub-partition)
+            const int half = (warp - 2) >> 2;      // columns [128*half, 128*half + 128)
+            const int m = m0 + quad * 32 + lane;   // token of this thread's TMEM lane
+            const bool mvalid = m < M;
+            const bool vec = (N % 8) == 0;
+#pragma unroll 1
+            for (int cc = 0; cc < 4; ++cc) {
+                const int col = half * 128 + cc * 32;
+                uint32_t v[32];
+                tmem_ld_32cols(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)col, v);
+                tmem_ld_wait();
+                const int nb = n0 + col;
+                if (!mvalid || nb >= N) continue;
+                uint16_t* yrow = Y + (int64_t)m * N + nb;
+                if (vec && nb + 32 <= N) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 o;
+                        o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
+                        o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
+                        o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
+                        o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
+                        *reinterpret_cast<uint4*>(yrow + 8 * q) = o;
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (nb + i < N) yrow[i] = (uint16_t)float_to_bf16_bits(__uint_as_float(v[i]));
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, GM_TMEM_COLS);
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+template <int G>
+static cudaError_t launch_gemm_g(const CUtensorMap& tx, const CUtensorMap& tp, const uint16_t* scales,
+                                 const uint16_t* offsets, uint16_t* Y, int M, int N, int K, cudaStream_t stream) {
+    auto kern = gemm_kernel<G>;
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), GM_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)((N + GM_BN - 1) / GM_BN), (unsigned)((M + GM_BM - 1) / GM_BM));
+    kern<<<grid, GM_THREADS, GM_SMEM_BYTES, stream>>>(tx, tp, scales, offsets, Y, M, N, K);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
+                        const uint16_t* offsets, int64_t N, int g, uint16_t* Y, cudaStream_t stream,
+                        const char** detail) {
+    EncodeTiledFn encode = get_encode_fn();
+    if (!encode) {
+        *detail = "cuTensorMapEncodeTiled is not available from the driver";
+        return cudaErrorNotSupported;
+    }
+    if ((N + GM_BN - 1) / GM_BN > 0x7FFFFFFF || (M + GM_BM - 1) / GM_BM > 65535) {
+        *detail = "problem too large for the GEMM grid";
+        return cudaErrorInvalidValue;
+    }
+    CUtensorMap tx, tp;
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+        const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+        const cuuint32_t box[2] = {GM_BK, GM_BM};
+        const cuuint32_t estr[2] = {1, 1};
+        if (encode(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(X), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+            *detail = "tensor map for X rejected";
+            return cudaErrorInvalidValue;
+        }
+    }
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)N};
+        const cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
+        const cuuint32_t box[2] = {GM_BK / 2, GM_BN};
+        const cuuint32_t estr[2] = {1, 1};
+        if (encode(&tp, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(Wq), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+            *detail = "tensor map for the packed codes rejected";
+            return cudaErrorInvalidValue;
+        }
+    }
+    switch (g) {
+        case 32: return launch_gemm_g<32>(tx, tp, scales, offsets, Y, (int)M, (int)N, (int)K, stream);
+        case 64: return launch_gemm_g<64>(tx, tp, scales, offsets, Y, (int)M, (int)N, (int)K, stream);
+        default: return launch_gemm_g<128>(tx, tp, scales, offsets, Y, (int)M, (int)N, (int)K, stream);
+    }
+}
+
+cudaError_t read_and_clear_gemm_fault(cudaStream_t stream, unsigned int* fault) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyFromSymbol(fault, g_gemm_fault, sizeof(unsigned int));
+    if (e != cudaSuccess) return e;
+    if (*fault) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_gemm_fault, &zero, sizeof(unsigned int));
+    }
+    return e;
+}
+
+}  // namespace w4

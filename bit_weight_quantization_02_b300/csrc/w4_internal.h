@@ -1,0 +1,46 @@
+// w4_internal.h -- host-side launchers shared between the libw4 translation
+// units.  Arguments are already validated by w4_api.cu; launchers only pick a
+// launch shape, enqueue on `stream` and return the launch error.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace w4 {
+
+cudaError_t launch_quantize(const uint16_t* W, int64_t N, int64_t K, int g, uint8_t* Wq, uint16_t* scales,
+                            uint16_t* offsets, cudaStream_t stream);
+cudaError_t launch_dequantize(const uint8_t* Wq, const uint16_t* scales, const uint16_t* offsets, int64_t N,
+                              int64_t K, int g, uint16_t* W_out, cudaStream_t stream);
+
+// Skinny (M <= 32) decode kernel.
+struct SkinnyPlan {
+    int tiles;        // row tiles of SKINNY_ROWS rows
+    int splits;       // K slices (grid.y); > 1 needs the workspace
+    int ks;           // k per slice, a multiple of 128
+    size_t smem;      // dynamic shared memory bytes
+    size_t ws_bytes;  // workspace bytes this plan needs
+};
+constexpr int SKINNY_ROWS = 64;
+constexpr int SKINNY_MAX_M = 32;
+// Plan for the given problem and available workspace; returns false if no
+// plan fits (the slice of X would not fit in shared memory without a split
+// that the workspace cannot hold).
+bool plan_skinny(int64_t M, int64_t N, int64_t K, int g, size_t ws_avail, SkinnyPlan* plan);
+cudaError_t launch_skinny(const SkinnyPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
+                          const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
+                          void* workspace, cudaStream_t stream);
+
+// tcgen05 tensor-core GEMM (any M).
+cudaError_t launch_gemm(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
+                        const uint16_t* offsets, int64_t N, int g, uint16_t* Y, cudaStream_t stream,
+                        const char** detail);
+// Reads and clears the GEMM's device fault word (bounded-wait timeouts).
+cudaError_t read_and_clear_gemm_fault(cudaStream_t stream, unsigned int* fault);
+
+// Raises a kernel's dynamic shared-memory limit to `bytes`, once per device
+// and kernel (later calls, e.g. during CUDA-graph capture, make no CUDA call).
+cudaError_t ensure_smem_limit(const void* kernel, int bytes);
+
+}  // namespace w4

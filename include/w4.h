@@ -40,6 +40,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define W4_API __attribute__((visibility("default")))
+#else
+#define W4_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -82,7 +88,7 @@ typedef enum w4_kernel {
  * Errors: W4_ERR_UNSUPPORTED (group_size), W4_ERR_INVALID_ARG (K <= 0,
  * N < 0, K % group_size, NULL, N*K >= 2^62), W4_ERR_MISALIGNED, W4_ERR_CUDA.
  */
-w4_status w4_quantize(const uint16_t *W, int64_t N, int64_t K, int group_size,
+W4_API w4_status w4_quantize(const uint16_t *W, int64_t N, int64_t K, int group_size,
                       uint8_t *Wq, uint16_t *scales, uint16_t *offsets,
                       void *stream);
 
@@ -93,7 +99,7 @@ w4_status w4_quantize(const uint16_t *W, int64_t N, int64_t K, int group_size,
  * activations" (the quantized result is brought back to float).
  * Errors as w4_quantize.
  */
-w4_status w4_dequantize(const uint8_t *Wq, const uint16_t *scales,
+W4_API w4_status w4_dequantize(const uint8_t *Wq, const uint16_t *scales,
                         const uint16_t *offsets, int64_t N, int64_t K,
                         int group_size, uint16_t *W_out, void *stream);
 
@@ -103,7 +109,7 @@ w4_status w4_dequantize(const uint8_t *Wq, const uint16_t *scales,
  * smaller workspace is accepted: the call then splits less (still correct,
  * possibly slower).
  */
-size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int group_size);
+W4_API size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int group_size);
 
 /*
  * w4_linear -- Y[M,N] bf16 = X[M,K] bf16 . dequant(Wq, scales, offsets)^T,
@@ -121,11 +127,12 @@ size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int group_size
  * used by the skinny kernel to combine partial sums across K slices.  It must
  * be zero-filled once before its first use; every call leaves it ready for
  * the next (its counters back at zero).  Two calls that may run at the same
- * time on the GPU must not share a workspace.  Results do not depend on the
- * workspace size (fixed summation order per launch shape).
+ * time on the GPU must not share a workspace.  The library picks the K split
+ * from the problem size and the workspace size; for a given (M, N, K,
+ * group_size, workspace_bytes) the result is deterministic, bit for bit.
  * Errors as w4_quantize, plus W4_ERR_INVALID_ARG for M < 0.
  */
-w4_status w4_linear(const uint16_t *X, int64_t M, int64_t K, const uint8_t *Wq,
+W4_API w4_status w4_linear(const uint16_t *X, int64_t M, int64_t K, const uint8_t *Wq,
                     const uint16_t *scales, const uint16_t *offsets, int64_t N,
                     int group_size, uint16_t *Y, void *workspace,
                     size_t workspace_bytes, void *stream);
@@ -133,7 +140,7 @@ w4_status w4_linear(const uint16_t *X, int64_t M, int64_t K, const uint8_t *Wq,
 /* w4_linear with an explicit kernel choice (tests and benchmarks use it to
  * run both kernels on the same problem).  W4_KERNEL_SKINNY with M > 32 gives
  * W4_ERR_INVALID_ARG. */
-w4_status w4_linear_ex(const uint16_t *X, int64_t M, int64_t K,
+W4_API w4_status w4_linear_ex(const uint16_t *X, int64_t M, int64_t K,
                        const uint8_t *Wq, const uint16_t *scales,
                        const uint16_t *offsets, int64_t N, int group_size,
                        uint16_t *Y, void *workspace, size_t workspace_bytes,
@@ -141,8 +148,8 @@ w4_status w4_linear_ex(const uint16_t *X, int64_t M, int64_t K,
 
 /* Sizes of the packed outputs: N*K/2 bytes of codes, N*(K/g)*2 bytes for each
  * of scales and offsets.  0 for invalid arguments. */
-size_t w4_packed_bytes(int64_t N, int64_t K);
-size_t w4_qparam_bytes(int64_t N, int64_t K, int group_size);
+W4_API size_t w4_packed_bytes(int64_t N, int64_t K);
+W4_API size_t w4_qparam_bytes(int64_t N, int64_t K, int group_size);
 
 /*
  * w4_device_fault -- synchronizes `stream`, then reports whether any libw4
@@ -150,15 +157,15 @@ size_t w4_qparam_bytes(int64_t N, int64_t K, int group_size);
  * (W4_ERR_TIMEOUT), and clears the flag.  Kernels that time out set the flag,
  * release what they hold and return; their outputs are then undefined.
  */
-w4_status w4_device_fault(void *stream);
+W4_API w4_status w4_device_fault(void *stream);
 
 /* Human-readable text of a status, and the detail (CUDA error string, failed
  * check) of the last failing call on this host thread. */
-const char *w4_status_string(w4_status s);
-const char *w4_last_error_detail(void);
+W4_API const char *w4_status_string(w4_status s);
+W4_API const char *w4_last_error_detail(void);
 
 /* W4_FORMAT_VERSION of the built library. */
-int w4_format_version(void);
+W4_API int w4_format_version(void);
 
 #ifdef __cplusplus
 }

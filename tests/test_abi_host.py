@@ -1,0 +1,132 @@
+"""libw4's C ABI on the host: the library loads, exports every call that
+include/w4.h declares, and rejects bad arguments before touching the GPU.
+Nothing here launches a kernel, so it runs without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bit_weight_quantization_02_b300 as w4
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w4.h")
+
+OK, INVALID, UNSUPPORTED, MISALIGNED = 0, 1, 2, 3
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(w4_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bit_weight_quantization_02_b300 import _build
+    _build.build()
+    return w4.load_library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"w4_quantize", "w4_dequantize", "w4_linear", "w4_linear_ex", "w4_linear_workspace_bytes",
+            "w4_device_fault"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in w4.h but not exported"
+
+
+def test_only_the_abi_is_exported(lib):
+    # the library is built with hidden visibility: no C++ internals leak out
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", w4.library_path()], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert exported, out
+    assert {e for e in exported if e.startswith("w4_")} == set(declared_functions())
+
+
+def test_format_version_and_status_strings(lib):
+    assert lib.w4_format_version() == w4.W4_FORMAT_VERSION == 1
+    for s, name in [(0, b"W4_OK"), (1, b"W4_ERR_INVALID_ARG"), (2, b"W4_ERR_UNSUPPORTED"),
+                    (3, b"W4_ERR_MISALIGNED"), (4, b"W4_ERR_CUDA"), (5, b"W4_ERR_TIMEOUT")]:
+        assert lib.w4_status_string(s) == name
+
+
+def test_sizes(lib):
+    assert lib.w4_packed_bytes(14336, 4096) == 14336 * 2048
+    assert lib.w4_qparam_bytes(14336, 4096, 32) == 14336 * 128 * 2
+    assert lib.w4_qparam_bytes(4096, 14336, 128) == 4096 * 112 * 2
+    assert lib.w4_qparam_bytes(10, 100, 32) == 0  # K % g
+    assert lib.w4_qparam_bytes(10, 128, 16) == 0  # unsupported g
+    assert lib.w4_packed_bytes(-1, 64) == 0
+
+
+def test_workspace_plan(lib):
+    # decode shapes split K across blocks and need a workspace; the GEMM range needs none
+    assert lib.w4_linear_workspace_bytes(1, 1024, 4096, 32) > 0
+    assert lib.w4_linear_workspace_bytes(32, 4096, 14336, 64) > 0
+    assert lib.w4_linear_workspace_bytes(33, 4096, 4096, 32) == 0
+    assert lib.w4_linear_workspace_bytes(2048, 4096, 4096, 32) == 0
+    assert lib.w4_linear_workspace_bytes(1, 100, 96, 32) == 0  # one K slice only
+
+
+FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced: every call below fails its checks first
+
+
+@pytest.mark.parametrize("g,expect", [(16, UNSUPPORTED), (96, UNSUPPORTED), (0, UNSUPPORTED)])
+def test_unsupported_group_sizes(lib, g, expect):
+    assert lib.w4_quantize(FAKE, 4, 256, g, FAKE, FAKE, FAKE, None) == expect
+    assert lib.w4_dequantize(FAKE, FAKE, FAKE, 4, 256, g, FAKE, None) == expect
+    assert lib.w4_linear(FAKE, 1, 256, FAKE, FAKE, FAKE, 4, g, FAKE, None, 0, None) == expect
+
+
+@pytest.mark.parametrize("N,K", [(4, 0), (4, -32), (-1, 64), (4, 96 + 16), (1 << 31, 64), (4, 1 << 31)])
+def test_invalid_shapes(lib, N, K):
+    assert lib.w4_quantize(FAKE, N, K, 32, FAKE, FAKE, FAKE, None) == INVALID
+    assert lib.w4_dequantize(FAKE, FAKE, FAKE, N, K, 32, FAKE, None) == INVALID
+    assert lib.w4_linear(FAKE, 1, K, FAKE, FAKE, FAKE, N, 32, FAKE, None, 0, None) == INVALID
+    assert lib.w4_last_error_detail()
+
+
+def test_null_and_misaligned_pointers(lib):
+    assert lib.w4_quantize(None, 4, 64, 32, FAKE, FAKE, FAKE, None) == INVALID
+    assert lib.w4_quantize(FAKE + 2, 4, 64, 32, FAKE, FAKE, FAKE, None) == MISALIGNED
+    assert lib.w4_quantize(FAKE, 4, 64, 32, FAKE + 8, FAKE, FAKE, None) == MISALIGNED
+    assert lib.w4_dequantize(FAKE, None, FAKE, 4, 64, 32, FAKE, None) == INVALID
+    assert lib.w4_dequantize(FAKE, FAKE, FAKE, 4, 64, 32, FAKE + 4, None) == MISALIGNED
+    assert lib.w4_linear(FAKE, 2, 64, FAKE, FAKE, None, 4, 32, FAKE, None, 0, None) == INVALID
+    assert lib.w4_linear(FAKE + 2, 2, 64, FAKE, FAKE, FAKE, 4, 32, FAKE, None, 0, None) == MISALIGNED
+    assert lib.w4_linear(FAKE, 2, 64, FAKE, FAKE, FAKE, 4, 32, FAKE, FAKE + 8, 64, None) == MISALIGNED
+    assert b"aligned" in lib.w4_last_error_detail()
+
+
+def test_empty_problems_succeed_without_launch(lib):
+    # N == 0 or M == 0: nothing to do, no pointer is touched, no CUDA call is made
+    assert lib.w4_quantize(None, 0, 64, 32, None, None, None, None) == OK
+    assert lib.w4_dequantize(None, None, None, 0, 64, 32, None, None) == OK
+    assert lib.w4_linear(None, 0, 64, None, None, None, 8, 32, None, None, 0, None) == OK
+    assert lib.w4_linear(None, 3, 64, None, None, None, 0, 32, None, None, 0, None) == OK
+
+
+def test_linear_argument_rules(lib):
+    assert lib.w4_linear(FAKE, -1, 64, FAKE, FAKE, FAKE, 4, 32, FAKE, None, 0, None) == INVALID
+    # the skinny kernel only takes M <= 32
+    assert lib.w4_linear_ex(FAKE, 33, 64, FAKE, FAKE, FAKE, 4, 32, FAKE, None, 0, 1, None) == INVALID
+    assert lib.w4_linear_ex(FAKE, 1, 64, FAKE, FAKE, FAKE, 4, 32, FAKE, None, 0, 7, None) == INVALID
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    with pytest.raises(ValueError):
+        w4.w4_quantize(torch.zeros(4, 64, dtype=torch.bfloat16), 32)
+
+
+def test_product_package_does_not_touch_the_oracle():
+    """The product path never imports, links or runs the oracle."""
+    pkg = os.path.join(ROOT, "bit_weight_quantization_02_b300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".c")):
+                text = open(os.path.join(dirpath, f)).read()
+                for needle in ("import oracle", "from oracle", "w4_ref_", "libw4_oracle", "w4_oracle"):
+                    assert needle not in text, (f, needle)

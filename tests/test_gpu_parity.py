@@ -1,0 +1,330 @@
+"""GPU parity: libw4's kernels (through the C ABI) against the CPU oracle.
+
+* w4_quantize / w4_dequantize: bit-exact, including ragged shapes and
+  adversarial groups;
+* w4_linear (skinny decode kernel and tcgen05 GEMM): within
+  |y - y_ref| <= 4e-3 |y_ref| + 1e-2 rms(y_ref), y_ref the oracle's fp64
+  product with the dequantized weights; rms over the whole output of the call,
+  or over the sampled outputs where only a sample is computed;
+* every output buffer sits between guard bytes that must survive the call
+  (out-of-bounds writes would show there);
+* the full-size workloads, in the launch configuration the benchmark times,
+  on sampled rows and columns that the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import bit_weight_quantization_02_b300 as w4
+from bit_weight_quantization_02_b300 import workloads as wl
+from tests.test_oracle_pins import adversarial_matrix
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+CANARY = 0x5A
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def f64(t: torch.Tensor) -> np.ndarray:
+    return oracle.bf16_bits_to_f64(bits(t))
+
+
+class Guarded:
+    """A device tensor with 256 canary bytes on both sides."""
+    PAD = 256
+
+    def __init__(self, shape, dtype):
+        n = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
+        self.raw = torch.full((n + 2 * self.PAD,), CANARY, dtype=torch.uint8, device=DEV)
+        self.n = n
+        self.t = self.raw[self.PAD:self.PAD + n].view(dtype).view(shape)
+
+    def check(self):
+        torch.cuda.synchronize()
+        head = self.raw[:self.PAD]
+        tail = self.raw[self.PAD + self.n:]
+        assert bool((head == CANARY).all()) and bool((tail == CANARY).all()), "write outside the output buffer"
+
+
+def gpu_quantize(W, g):
+    N, K = W.shape
+    out = (Guarded((N, K // 2), torch.uint8), Guarded((N, K // g), torch.bfloat16),
+           Guarded((N, K // g), torch.bfloat16))
+    w4.w4_quantize(W, g, out=tuple(o.t for o in out))
+    for o in out:
+        o.check()
+    return tuple(o.t for o in out)
+
+
+def gpu_linear(X, Wq, sc, of, g, kernel=w4.KERNEL_AUTO, workspace=None):
+    M, N = X.shape[0], Wq.shape[0]
+    Y = Guarded((M, N), torch.bfloat16)
+    w4.w4_linear_ex(X, Wq, sc, of, g, kernel, out=Y.t, workspace=workspace)
+    Y.check()
+    return Y.t
+
+
+def assert_linear_ok(y_gpu: torch.Tensor, y_ref: np.ndarray, what: str):
+    ok, worst = oracle.within_linear_tolerance(f64(y_gpu), y_ref)
+    assert ok, f"{what}: outside |y-y_ref| <= 4e-3|y_ref| + 1e-2 rms, worst ratio {worst:.3f}"
+
+
+# ----------------------------------------------------------------- quantize
+
+QUANT_SHAPES = [(512, 512), (300, 4224), (7, 128), (64, 14336), (1, 4096)]
+
+
+@pytest.mark.parametrize("g", [32, 64, 128])
+@pytest.mark.parametrize("shape", QUANT_SHAPES, ids=[f"{n}x{k}" for n, k in QUANT_SHAPES])
+def test_quantize_bit_exact(g, shape):
+    N, K = shape
+    W = wl.gen_weight(N, K, seed=100 + N + g, outliers=True)
+    Wq, sc, of = gpu_quantize(W.to(DEV), g)
+    rq, rs, ro = oracle.ref_quantize(bits(W), g)
+    np.testing.assert_array_equal(Wq.cpu().numpy(), rq)
+    np.testing.assert_array_equal(bits(sc), rs)
+    np.testing.assert_array_equal(bits(of), ro)
+
+
+@pytest.mark.parametrize("g", [32, 64, 128])
+def test_quantize_adversarial_groups_bit_exact(g):
+    Wb = adversarial_matrix(g)
+    W = torch.from_numpy(Wb.view(np.int16)).view(torch.bfloat16).to(DEV)
+    Wq, sc, of = gpu_quantize(W, g)
+    rq, rs, ro = oracle.ref_quantize(Wb, g)
+    np.testing.assert_array_equal(Wq.cpu().numpy(), rq)
+    np.testing.assert_array_equal(bits(sc), rs)
+    np.testing.assert_array_equal(bits(of), ro)
+
+
+def test_quantize_golden_cases():
+    from tests.test_oracle_pins import GOLDEN_CASES, unpack_codes
+    for case in GOLDEN_CASES:
+        g = case["g"]
+        W = torch.from_numpy(case["values"].reshape(1, g).view(np.int16)).view(torch.bfloat16).to(DEV)
+        Wq, sc, of = gpu_quantize(W, g)
+        assert bits(sc)[0, 0] == case["scale"] and bits(of)[0, 0] == case["offset"], case["name"]
+        np.testing.assert_array_equal(unpack_codes(Wq.cpu().numpy())[0], case["codes"])
+
+
+# --------------------------------------------------------------- dequantize
+
+@pytest.mark.parametrize("g", [32, 64, 128])
+@pytest.mark.parametrize("shape", [(300, 4224), (64, 128), (3, 14336)])
+def test_dequantize_bit_exact_on_arbitrary_codes(g, shape):
+    """Random code bytes and random finite qparams, independent of w4_quantize."""
+    N, K = shape
+    rng = np.random.default_rng(N * K + g)
+    rq = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    rs = bits(torch.from_numpy(np.abs(rng.normal(0, 0.01, (N, K // g))).astype(np.float32) + 1e-6).to(torch.bfloat16))
+    ro = bits(torch.from_numpy(rng.normal(0, 0.05, (N, K // g)).astype(np.float32)).to(torch.bfloat16))
+    Wq = torch.from_numpy(rq).to(DEV)
+    sc = torch.from_numpy(rs.view(np.int16)).view(torch.bfloat16).to(DEV)
+    of = torch.from_numpy(ro.view(np.int16)).view(torch.bfloat16).to(DEV)
+    out = Guarded((N, K), torch.bfloat16)
+    w4.w4_dequantize(Wq, sc, of, g, out=out.t)
+    out.check()
+    np.testing.assert_array_equal(bits(out.t), oracle.ref_dequantize(rq, rs, ro, g))
+
+
+# ------------------------------------------------------------------- linear
+
+def _problem(M, N, K, g, seed, outliers=True):
+    W = wl.gen_weight(N, K, seed=seed, outliers=outliers)
+    X = wl.gen_activation(M, K, seed=seed + wl.ACT_SEED_OFFSET)
+    rq, rs, ro = oracle.ref_quantize(bits(W), g)
+    dev = (X.to(DEV), torch.from_numpy(rq).to(DEV),
+           torch.from_numpy(rs.view(np.int16)).view(torch.bfloat16).to(DEV),
+           torch.from_numpy(ro.view(np.int16)).view(torch.bfloat16).to(DEV))
+    y_ref = oracle.ref_linear(bits(X), rq, rs, ro, g)
+    return dev, y_ref
+
+
+SKINNY_M = [1, 2, 3, 5, 8, 9, 16, 17, 24, 31, 32]
+SKINNY_NK = [(200, 4160), (520, 512), (64, 96), (1030, 1024)]
+
+
+@pytest.mark.parametrize("g", [32, 64, 128])
+@pytest.mark.parametrize("nk", SKINNY_NK, ids=[f"{n}x{k}" for n, k in SKINNY_NK])
+def test_linear_skinny(g, nk):
+    N, K = nk
+    if K % g:
+        pytest.skip("K not a multiple of g")
+    for M in SKINNY_M:
+        (X, Wq, sc, of), y_ref = _problem(M, N, K, g, seed=7 * M + N + g)
+        assert_linear_ok(gpu_linear(X, Wq, sc, of, g, w4.KERNEL_SKINNY), y_ref, f"skinny M={M} N={N} K={K} g={g}")
+
+
+GEMM_M = [1, 33, 127, 129, 300]
+GEMM_NK = [(200, 4160), (520, 512), (256, 64), (1000, 96)]
+
+
+@pytest.mark.parametrize("g", [32, 64, 128])
+@pytest.mark.parametrize("nk", GEMM_NK, ids=[f"{n}x{k}" for n, k in GEMM_NK])
+def test_linear_gemm(g, nk):
+    N, K = nk
+    if K % g:
+        pytest.skip("K not a multiple of g")
+    for M in GEMM_M:
+        (X, Wq, sc, of), y_ref = _problem(M, N, K, g, seed=11 * M + N + g)
+        assert_linear_ok(gpu_linear(X, Wq, sc, of, g, w4.KERNEL_GEMM), y_ref, f"gemm M={M} N={N} K={K} g={g}")
+    w4.w4_device_fault(DEV)
+
+
+def test_linear_auto_dispatch_and_both_kernels_agree():
+    (X, Wq, sc, of), y_ref = _problem(32, 768, 2048, 32, seed=5)
+    ys = gpu_linear(X, Wq, sc, of, 32, w4.KERNEL_SKINNY)
+    yg = gpu_linear(X, Wq, sc, of, 32, w4.KERNEL_GEMM)
+    ya = gpu_linear(X, Wq, sc, of, 32)
+    assert torch.equal(ys.view(torch.int16), ya.view(torch.int16))  # M <= 32 goes to the skinny kernel
+    assert_linear_ok(ys, y_ref, "skinny")
+    assert_linear_ok(yg, y_ref, "gemm")
+    # the two kernels round differently but agree to bf16 precision
+    assert float((ys.float() - yg.float()).abs().max()) <= 2e-2 * float(yg.float().abs().max())
+
+
+def test_linear_without_workspace_and_with_small_workspace():
+    (X, Wq, sc, of), y_ref = _problem(4, 1024, 4096, 32, seed=8)
+    none_ws = w4.Workspace(DEV)  # zero bytes: no K split, one block row tile per slice of K
+    y0 = gpu_linear(X, Wq, sc, of, 32, w4.KERNEL_AUTO, workspace=none_ws)
+    small = w4.Workspace(DEV, w4.w4_linear_workspace_bytes(4, 1024, 4096, 32) // 3)
+    y1 = gpu_linear(X, Wq, sc, of, 32, w4.KERNEL_AUTO, workspace=small)
+    y2 = gpu_linear(X, Wq, sc, of, 32)
+    for y, what in ((y0, "no workspace"), (y1, "small workspace"), (y2, "full workspace")):
+        assert_linear_ok(y, y_ref, what)
+
+
+def test_linear_is_deterministic_and_reuses_its_workspace():
+    (X, Wq, sc, of), y_ref = _problem(3, 2048, 4096, 64, seed=9)
+    ws = w4.Workspace(DEV).reserve_for(3, 2048, 4096, 64)
+    assert ws.nbytes > 0
+    first = gpu_linear(X, Wq, sc, of, 64, workspace=ws)
+    for _ in range(5):
+        again = gpu_linear(X, Wq, sc, of, 64, workspace=ws)
+        assert torch.equal(first.view(torch.int16), again.view(torch.int16))
+    # the split-K tickets are back at zero after every call
+    ntick = (2048 + 63) // 64
+    assert int(ws.buf[: 4 * ntick].view(torch.int32).abs().sum()) == 0
+    assert_linear_ok(first, y_ref, "repeat")
+
+
+def test_linear_edge_shapes():
+    for M, N, K, g in [(1, 1, 32, 32), (1, 7, 64, 64), (2, 65, 128, 128), (32, 257, 32, 32), (129, 9, 128, 32),
+                       (1, 4096, 128, 128), (5, 3, 14336, 32)]:
+        (X, Wq, sc, of), y_ref = _problem(M, N, K, g, seed=M + N + K)
+        assert_linear_ok(gpu_linear(X, Wq, sc, of, g), y_ref, f"edge M={M} N={N} K={K} g={g}")
+        assert_linear_ok(gpu_linear(X, Wq, sc, of, g, w4.KERNEL_GEMM), y_ref, f"edge gemm M={M} N={N} K={K}")
+
+
+def test_empty_problems():
+    X = torch.zeros((0, 64), dtype=torch.bfloat16, device=DEV)
+    Wq = torch.zeros((8, 32), dtype=torch.uint8, device=DEV)
+    sc = torch.zeros((8, 2), dtype=torch.bfloat16, device=DEV)
+    Y = w4.w4_linear(X, Wq, sc, sc, 32)
+    assert Y.shape == (0, 8)
+    W = torch.zeros((0, 64), dtype=torch.bfloat16, device=DEV)
+    q, s, o = w4.w4_quantize(W, 32)
+    assert q.shape == (0, 32)
+
+
+def test_cuda_graph_capture_matches_eager():
+    probs = [_problem(1, N, K, 32, seed=20 + i) for i, (N, K) in enumerate([(1024, 4096), (4096, 1024), (768, 2048)])]
+    wss = [w4.Workspace(DEV).reserve_for(1, p[0][1].shape[0], p[0][0].shape[1], 32) for p in probs]
+    outs = [torch.empty((1, p[0][1].shape[0]), dtype=torch.bfloat16, device=DEV) for p in probs]
+    eager = [gpu_linear(*p[0], 32, workspace=ws).clone() for p, ws in zip(probs, wss)]
+    s = torch.cuda.Stream(DEV)
+    s.wait_stream(torch.cuda.current_stream(DEV))
+    with torch.cuda.stream(s):
+        for (dev, _), ws, out in zip(probs, wss, outs):  # warm up on the capture stream
+            w4.w4_linear(*dev, 32, out=out, workspace=ws)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            for (dev, _), ws, out in zip(probs, wss, outs):
+                w4.w4_linear(*dev, 32, out=out, workspace=ws)
+    torch.cuda.current_stream(DEV).wait_stream(s)
+    for out in outs:
+        out.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    for e, o in zip(eager, outs):
+        assert torch.equal(e.view(torch.int16), o.view(torch.int16))
+
+
+def test_no_device_fault_pending():
+    w4.w4_device_fault(DEV)
+
+
+# ------------------------------------------ full-size workloads, sampled
+
+def _sampled_quantize_check(W_dev, g, rows):
+    Wq, sc, of = w4.w4_quantize(W_dev, g)
+    Wr = bits(W_dev[rows])
+    rq, rs, ro = oracle.ref_quantize(Wr, g)
+    np.testing.assert_array_equal(Wq[rows].cpu().numpy(), rq)
+    np.testing.assert_array_equal(bits(sc[rows]), rs)
+    np.testing.assert_array_equal(bits(of[rows]), ro)
+    return Wq, sc, of, (rq, rs, ro)
+
+
+def _rows(N, n=48, seed=0):
+    rng = np.random.default_rng(seed)
+    r = np.unique(np.concatenate([rng.choice(N, size=min(n, N), replace=False), [0, N - 1]]))
+    return torch.from_numpy(r).to(DEV)
+
+
+@pytest.mark.parametrize("case", wl.config2(), ids=[c.name for c in wl.config2()])
+def test_full_size_decode_config2(case):
+    """Llama-3-8B decode linears, M=1, g=32, 0.1 % x10 outliers."""
+    W = wl.gen_weight(case.N, case.K, case.w_seed, outliers=True, device=DEV)
+    rows = _rows(case.N, seed=case.w_seed)
+    Wq, sc, of, (rq, rs, ro) = _sampled_quantize_check(W, case.group_size, rows)
+    X = wl.gen_activation(case.M, case.K, case.x_seed, device=DEV)
+    Y = gpu_linear(X, Wq, sc, of, case.group_size)
+    y_ref = oracle.ref_linear(bits(X), rq, rs, ro, case.group_size)
+    assert_linear_ok(Y[:, rows], y_ref, f"config2 {case.name}")
+
+
+def test_full_size_batched_decode_config3():
+    for case in wl.config3():
+        W = wl.gen_weight(case.N, case.K, case.w_seed, device=DEV)
+        rows = _rows(case.N, n=24, seed=case.w_seed + case.M)
+        Wq, sc, of, (rq, rs, ro) = _sampled_quantize_check(W, case.group_size, rows)
+        X = wl.gen_activation(case.M, case.K, case.x_seed + case.M, device=DEV)
+        Y = gpu_linear(X, Wq, sc, of, case.group_size)
+        y_ref = oracle.ref_linear(bits(X), rq, rs, ro, case.group_size)
+        assert_linear_ok(Y[:, rows], y_ref, f"config3 {case.name}")
+
+
+def test_full_size_prefill_config4():
+    for case in wl.config4():
+        W = wl.gen_weight(case.N, case.K, case.w_seed, device=DEV)
+        rows = _rows(case.N, n=24, seed=case.w_seed)
+        Wq, sc, of, (rq, rs, ro) = _sampled_quantize_check(W, case.group_size, rows)
+        X = wl.gen_activation(case.M, case.K, case.x_seed + case.M, device=DEV)
+        Y = gpu_linear(X, Wq, sc, of, case.group_size)
+        toks = _rows(case.M, n=40, seed=case.M)
+        y_ref = oracle.ref_linear(bits(X[toks]), rq, rs, ro, case.group_size)
+        assert_linear_ok(Y[toks][:, rows], y_ref, f"config4 {case.name}")
+        del W, Wq, sc, of, X, Y
+    w4.w4_device_fault(DEV)
+
+
+@pytest.mark.parametrize("layer", [0, 31])
+def test_full_size_stack_config5_layers(layer):
+    """Two blocks of the 32-layer g=128 stack: every linear, M=1 and M=16."""
+    for i, (name, N, K) in enumerate(wl.LLAMA3_8B_LINEARS):
+        seed = wl.weight_seed(5, layer, i)
+        W = wl.gen_weight(N, K, seed, device=DEV)
+        rows = _rows(N, n=16, seed=seed)
+        Wq, sc, of, (rq, rs, ro) = _sampled_quantize_check(W, 128, rows)
+        del W
+        for M in (1, 16):
+            X = wl.gen_activation(M, K, seed + wl.ACT_SEED_OFFSET + M, device=DEV)
+            Y = gpu_linear(X, Wq, sc, of, 128)
+            y_ref = oracle.ref_linear(bits(X), rq, rs, ro, 128)
+            assert_linear_ok(Y[:, rows], y_ref, f"config5 L{layer}.{name} M={M}")
