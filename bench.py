@@ -270,7 +270,7 @@ def gpu_arm(args):
     clocks = ClockSampler(dist.local_rank).start()
 
     # ---- headline: M=1 decode through 32 blocks of Llama-3-8B linears (g=32)
-    cases = [c for layer in range(wl.LLAMA3_8B_LAYERS) for c in wl.config2(layer)]
+    cases = [c for layer in range(args.layers) for c in wl.config2(layer)]
     stack = LinearStack(cases, device, w4, wl)
     graph = stack.capture(stream)
     with torch.cuda.stream(stream):
@@ -323,6 +323,7 @@ def gpu_arm(args):
     if not args.headline_only:
         rows = other_rows(args, w4, wl, device, stream, peaks, dist)
 
+    step_bytes = stack.bytes
     del graph, stack
     clk = clocks.stop()
     cpu = None
@@ -334,7 +335,8 @@ def gpu_arm(args):
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
                 "data": "synthetic (seeded; random-init Llama-3-8B-shaped weights)",
-                "config": {"workload": WORKLOAD, "l2": "inputs larger than L2 (4.36 GB of packed weights per step)",
+                "config": {"workload": WORKLOAD if args.layers == 32 else f"{args.layers}-block profiling cut of: " + WORKLOAD,
+                           "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB of packed weights per step)",
                            "group_size": 32, "M": 1, "linears_per_step": len(cases),
                            "parallelism": "replicas" if dist.world > 1 else "single GPU"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
@@ -542,6 +544,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--prefill-iters", type=int, default=10)
+    ap.add_argument("--layers", type=int, default=32,
+                    help="Llama-3-8B blocks in the headline step (32 = the whole model; fewer only for profiling)")
     a = ap.parse_args(argv)
     if a.warmup < 3:
         ap.error("--warmup must be at least 3")

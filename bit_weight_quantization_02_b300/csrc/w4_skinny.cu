@@ -256,10 +256,15 @@ skinny_kernel(const SkinnyArgs p) {
 static size_t skinny_smem_bytes(int M, int ks, int g) {
     return (size_t)M * (ks * 2 + 16) + (size_t)SKINNY_ROWS * (ks / g + 1) * 4;
 }
-static size_t skinny_ws_bytes(int M, int64_t N, int tiles, int splits) {
+// Workspace layout: a fixed region of SK_MAX_TICKETS arrival counters at the
+// start (the same bytes for every problem, so a workspace shared by calls of
+// different shapes keeps its counters at zero), then [splits][M][N] fp32
+// partial sums.
+static constexpr int SK_MAX_TICKETS = 16384;  // row tiles: N <= 1,048,576
+static constexpr size_t SK_TICKET_BYTES = SK_MAX_TICKETS * 4;
+static size_t skinny_ws_bytes(int M, int64_t N, int splits) {
     if (splits <= 1) return 0;
-    const size_t tickets = ((size_t)tiles * 4 + 255) / 256 * 256;
-    return tickets + (size_t)splits * M * N * 4;
+    return SK_TICKET_BYTES + (size_t)splits * M * N * 4;
 }
 
 static constexpr int SK_TARGET_BLOCKS = 148 * 8;  // 8 blocks per SM on a 148-SM B300
@@ -281,7 +286,8 @@ bool plan_skinny(int64_t M, int64_t N, int64_t K, int g, size_t ws_avail, Skinny
     ks = std::min(ks, ks_cap);
     splits = (int)((K + ks - 1) / ks);
     // shrink the split until the workspace holds it (larger slices, fewer blocks)
-    while (splits > 1 && skinny_ws_bytes((int)M, N, tiles, splits) > ws_avail) {
+    if (tiles > SK_MAX_TICKETS) splits = 1;  // no split for more rows than the ticket region covers
+    while (splits > 1 && skinny_ws_bytes((int)M, N, splits) > ws_avail) {
         if (ks + SK_KSTEP > ks_cap) return false;
         ks += SK_KSTEP;
         splits = (int)((K + ks - 1) / ks);
@@ -291,7 +297,7 @@ bool plan_skinny(int64_t M, int64_t N, int64_t K, int g, size_t ws_avail, Skinny
     plan->splits = splits;
     plan->ks = ks;
     plan->smem = skinny_smem_bytes((int)M, ks, g);
-    plan->ws_bytes = skinny_ws_bytes((int)M, N, tiles, splits);
+    plan->ws_bytes = skinny_ws_bytes((int)M, N, splits);
     return true;
 }
 
@@ -332,9 +338,8 @@ cudaError_t launch_skinny(const SkinnyPlan& plan, const uint16_t* X, int64_t M, 
     a.scales = scales;
     a.offsets = offsets;
     a.Y = Y;
-    const size_t tickets = ((size_t)plan.tiles * 4 + 255) / 256 * 256;
     a.ws_ticket = plan.splits > 1 ? static_cast<unsigned int*>(workspace) : nullptr;
-    a.ws_part = plan.splits > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + tickets) : nullptr;
+    a.ws_part = plan.splits > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + SK_TICKET_BYTES) : nullptr;
     a.M = (int)M;
     a.N = (int)N;
     a.K = (int)K;

@@ -124,9 +124,10 @@ W4_API size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int gro
  *   |y - y_ref| <= 4e-3 |y_ref| + 1e-2 rms(y_ref).
  *
  * workspace: device memory of `workspace_bytes` bytes (may be NULL with 0),
- * used by the skinny kernel to combine partial sums across K slices.  It must
- * be zero-filled once before its first use; every call leaves it ready for
- * the next (its counters back at zero).  Two calls that may run at the same
+ * used by the skinny kernel to combine partial sums across K slices.  Its
+ * first 64 KiB hold arrival counters: they must be zero before the first use,
+ * and every call leaves them at zero again, so one workspace can serve calls
+ * of any shape in sequence.  Two calls that may run at the same
  * time on the GPU must not share a workspace.  The library picks the K split
  * from the problem size and the workspace size; for a given (M, N, K,
  * group_size, workspace_bytes) the result is deterministic, bit for bit.

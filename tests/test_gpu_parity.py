@@ -213,6 +213,17 @@ def test_linear_is_deterministic_and_reuses_its_workspace():
     assert_linear_ok(first, y_ref, "repeat")
 
 
+def test_workspace_shared_by_calls_of_different_shapes():
+    """One workspace, calls whose row-tile counts and partial-sum sizes differ, in
+    both orders: the arrival counters must stay clear of every call's partials."""
+    small_tiles = _problem(32, 1030, 1024, 32, seed=31)   # few tiles, large partials
+    many_tiles = _problem(1, 14336, 1024, 32, seed=32)    # many tiles
+    ws = w4.Workspace(DEV).reserve(max(w4.w4_linear_workspace_bytes(32, 1030, 1024, 32),
+                                       w4.w4_linear_workspace_bytes(1, 14336, 1024, 32)))
+    for (dev, y_ref) in (small_tiles, many_tiles, small_tiles, many_tiles):
+        assert_linear_ok(gpu_linear(*dev, 32, workspace=ws), y_ref, "shared workspace")
+
+
 def test_linear_edge_shapes():
     for M, N, K, g in [(1, 1, 32, 32), (1, 7, 64, 64), (2, 65, 128, 128), (32, 257, 32, 32), (129, 9, 128, 32),
                        (1, 4096, 128, 128), (5, 3, 14336, 32)]:
