@@ -78,16 +78,9 @@ w4_status w4_dequantize(const uint8_t* Wq, const uint16_t* scales, const uint16_
     return e == cudaSuccess ? W4_OK : cuda_fail(e, "dequantize launch");
 }
 
-size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int group_size) {
-    if (check_shape(N, K, group_size) != W4_OK || M < 1 || M > w4::SKINNY_MAX_M || N == 0) return 0;
-    w4::SkinnyPlan plan;
-    if (!w4::plan_skinny(M, N, K, group_size, ~size_t(0), &plan)) return 0;
-    return plan.ws_bytes;
-}
-
 w4_status w4_linear_ex(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
-                       const uint16_t* offsets, int64_t N, int group_size, uint16_t* Y, void* workspace,
-                       size_t workspace_bytes, w4_kernel kernel, void* stream) {
+                       const uint16_t* offsets, int64_t N, int group_size, uint16_t* Y, w4_kernel kernel,
+                       void* stream) {
     W4_TRY(check_shape(N, K, group_size));
     if (M < 0) return fail(W4_ERR_INVALID_ARG, "M = %lld must not be negative", (long long)M);
     if (M > 0x7FFFFFFFLL) return fail(W4_ERR_INVALID_ARG, "M must be below 2^31");
@@ -101,20 +94,13 @@ w4_status w4_linear_ex(const uint16_t* X, int64_t M, int64_t K, const uint8_t* W
     W4_TRY(check_ptr(scales, "scales"));
     W4_TRY(check_ptr(offsets, "offsets"));
     W4_TRY(check_ptr(Y, "Y"));
-    if (workspace == nullptr) workspace_bytes = 0;
-    if (workspace_bytes > 0 && !aligned16(workspace)) return fail(W4_ERR_MISALIGNED, "workspace is not 16-byte aligned");
 
-    bool use_skinny = (kernel == W4_KERNEL_SKINNY) || (kernel == W4_KERNEL_AUTO && M <= w4::SKINNY_MAX_M);
-    w4::SkinnyPlan plan;
-    if (use_skinny && !w4::plan_skinny(M, N, K, group_size, workspace_bytes, &plan)) {
-        if (kernel == W4_KERNEL_SKINNY)
-            return fail(W4_ERR_INVALID_ARG, "workspace of %zu bytes is too small for the skinny kernel (needs %zu)",
-                        workspace_bytes, w4_linear_workspace_bytes(M, N, K, group_size));
-        use_skinny = false;
-    }
+    const bool use_skinny = (kernel == W4_KERNEL_SKINNY) || (kernel == W4_KERNEL_AUTO && M <= w4::SKINNY_MAX_M);
     cudaError_t e;
     if (use_skinny) {
-        e = w4::launch_skinny(plan, X, M, K, Wq, scales, offsets, N, group_size, Y, workspace, (cudaStream_t)stream);
+        w4::SkinnyPlan plan;
+        if (!w4::plan_skinny(M, N, K, group_size, &plan)) return fail(W4_ERR_INVALID_ARG, "no skinny launch plan");
+        e = w4::launch_skinny(plan, X, M, K, Wq, scales, offsets, N, group_size, Y, (cudaStream_t)stream);
         return e == cudaSuccess ? W4_OK : cuda_fail(e, "skinny linear launch");
     }
     const char* detail = "";
@@ -124,10 +110,8 @@ w4_status w4_linear_ex(const uint16_t* X, int64_t M, int64_t K, const uint8_t* W
 }
 
 w4_status w4_linear(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
-                    const uint16_t* offsets, int64_t N, int group_size, uint16_t* Y, void* workspace,
-                    size_t workspace_bytes, void* stream) {
-    return w4_linear_ex(X, M, K, Wq, scales, offsets, N, group_size, Y, workspace, workspace_bytes, W4_KERNEL_AUTO,
-                        stream);
+                    const uint16_t* offsets, int64_t N, int group_size, uint16_t* Y, void* stream) {
+    return w4_linear_ex(X, M, K, Wq, scales, offsets, N, group_size, Y, W4_KERNEL_AUTO, stream);
 }
 
 size_t w4_packed_bytes(int64_t N, int64_t K) {

@@ -16,21 +16,18 @@ cudaError_t launch_dequantize(const uint8_t* Wq, const uint16_t* scales, const u
 
 // Skinny (M <= 32) decode kernel.
 struct SkinnyPlan {
-    int tiles;        // row tiles of SKINNY_ROWS rows
-    int splits;       // K slices (grid.y); > 1 needs the workspace
-    int ks;           // k per slice, a multiple of 128
-    size_t smem;      // dynamic shared memory bytes
-    size_t ws_bytes;  // workspace bytes this plan needs
+    int tiles;    // row tiles of SKINNY_ROWS rows (grid.x)
+    int splits;   // K slices (grid.y), one thread-block cluster per row tile
+    int ks;       // k per slice
+    int kc;       // k per staged activation sub-chunk
+    size_t smem;  // dynamic shared memory bytes
 };
 constexpr int SKINNY_ROWS = 64;
 constexpr int SKINNY_MAX_M = 32;
-// Plan for the given problem and available workspace; returns false if no
-// plan fits (the slice of X would not fit in shared memory without a split
-// that the workspace cannot hold).
-bool plan_skinny(int64_t M, int64_t N, int64_t K, int g, size_t ws_avail, SkinnyPlan* plan);
+bool plan_skinny(int64_t M, int64_t N, int64_t K, int g, SkinnyPlan* plan);
 cudaError_t launch_skinny(const SkinnyPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
                           const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
-                          void* workspace, cudaStream_t stream);
+                          cudaStream_t stream);
 
 // tcgen05 tensor-core GEMM (any M).
 cudaError_t launch_gemm(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,

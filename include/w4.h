@@ -104,48 +104,38 @@ W4_API w4_status w4_dequantize(const uint8_t *Wq, const uint16_t *scales,
                         int group_size, uint16_t *W_out, void *stream);
 
 /*
- * w4_linear_workspace_bytes -- bytes of workspace that lets w4_linear split
- * K across thread blocks for this problem (0 if it never needs any).  A
- * smaller workspace is accepted: the call then splits less (still correct,
- * possibly slower).
- */
-W4_API size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int group_size);
-
-/*
  * w4_linear -- Y[M,N] bf16 = X[M,K] bf16 . dequant(Wq, scales, offsets)^T,
  * products and sums in fp32, one rounding to bf16 at the end, no bias.
  * Source: the mixed bf16 x int4 matmul of Optimum Quanto (feature list and
  * "Pitfalls when quantizing activations": accumulation in fp32).
  *
- * The kernels dequantize each weight as bf16(q * s + o) with a single
- * rounding, which can differ from w4_dequantize's double rounding by one bf16
- * ulp; the summation order is the kernel's own.  Accuracy contract against
- * y_ref = sum_k X[m,k] W'[n,k] in fp64 (W' = w4_dequantize output):
+ * M <= 32 runs the memory-bound skinny kernel, larger M the tcgen05
+ * tensor-core GEMM.  The kernels dequantize each weight as bf16(q * s + o)
+ * with a single rounding, which can differ from w4_dequantize's double
+ * rounding by one bf16 ulp; the summation order is the kernel's own, fixed for
+ * a given (M, N, K, group_size), so results are deterministic bit for bit.
+ * Accuracy contract against y_ref = sum_k X[m,k] W'[n,k] in fp64
+ * (W' = w4_dequantize output):
  *   |y - y_ref| <= 4e-3 |y_ref| + 1e-2 rms(y_ref).
- *
- * workspace: device memory of `workspace_bytes` bytes (may be NULL with 0),
- * used by the skinny kernel to combine partial sums across K slices.  Its
- * first 64 KiB hold arrival counters: they must be zero before the first use,
- * and every call leaves them at zero again, so one workspace can serve calls
- * of any shape in sequence.  Two calls that may run at the same
- * time on the GPU must not share a workspace.  The library picks the K split
- * from the problem size and the workspace size; for a given (M, N, K,
- * group_size, workspace_bytes) the result is deterministic, bit for bit.
+ * The call needs no workspace: partial sums of a split K are combined in the
+ * distributed shared memory of a thread-block cluster.
+ * Kernels of consecutive w4_linear calls on one stream may overlap (the next
+ * one starts streaming its weights while the previous one finishes); each
+ * still reads X only after everything earlier on the stream has completed,
+ * so the weights of a call must not be written by the call just before it.
  * Errors as w4_quantize, plus W4_ERR_INVALID_ARG for M < 0.
  */
 W4_API w4_status w4_linear(const uint16_t *X, int64_t M, int64_t K, const uint8_t *Wq,
-                    const uint16_t *scales, const uint16_t *offsets, int64_t N,
-                    int group_size, uint16_t *Y, void *workspace,
-                    size_t workspace_bytes, void *stream);
+                           const uint16_t *scales, const uint16_t *offsets, int64_t N,
+                           int group_size, uint16_t *Y, void *stream);
 
 /* w4_linear with an explicit kernel choice (tests and benchmarks use it to
  * run both kernels on the same problem).  W4_KERNEL_SKINNY with M > 32 gives
  * W4_ERR_INVALID_ARG. */
 W4_API w4_status w4_linear_ex(const uint16_t *X, int64_t M, int64_t K,
-                       const uint8_t *Wq, const uint16_t *scales,
-                       const uint16_t *offsets, int64_t N, int group_size,
-                       uint16_t *Y, void *workspace, size_t workspace_bytes,
-                       w4_kernel kernel, void *stream);
+                              const uint8_t *Wq, const uint16_t *scales,
+                              const uint16_t *offsets, int64_t N, int group_size,
+                              uint16_t *Y, w4_kernel kernel, void *stream);
 
 /* Sizes of the packed outputs: N*K/2 bytes of codes, N*(K/g)*2 bytes for each
  * of scales and offsets.  0 for invalid arguments. */

@@ -61,10 +61,10 @@ def gpu_quantize(W, g):
     return tuple(o.t for o in out)
 
 
-def gpu_linear(X, Wq, sc, of, g, kernel=w4.KERNEL_AUTO, workspace=None):
+def gpu_linear(X, Wq, sc, of, g, kernel=w4.KERNEL_AUTO):
     M, N = X.shape[0], Wq.shape[0]
     Y = Guarded((M, N), torch.bfloat16)
-    w4.w4_linear_ex(X, Wq, sc, of, g, kernel, out=Y.t, workspace=workspace)
+    w4.w4_linear_ex(X, Wq, sc, of, g, kernel, out=Y.t)
     Y.check()
     return Y.t
 
@@ -188,40 +188,36 @@ def test_linear_auto_dispatch_and_both_kernels_agree():
     assert float((ys.float() - yg.float()).abs().max()) <= 2e-2 * float(yg.float().abs().max())
 
 
-def test_linear_without_workspace_and_with_small_workspace():
-    (X, Wq, sc, of), y_ref = _problem(4, 1024, 4096, 32, seed=8)
-    none_ws = w4.Workspace(DEV)  # zero bytes: no K split, one block row tile per slice of K
-    y0 = gpu_linear(X, Wq, sc, of, 32, w4.KERNEL_AUTO, workspace=none_ws)
-    small = w4.Workspace(DEV, w4.w4_linear_workspace_bytes(4, 1024, 4096, 32) // 3)
-    y1 = gpu_linear(X, Wq, sc, of, 32, w4.KERNEL_AUTO, workspace=small)
-    y2 = gpu_linear(X, Wq, sc, of, 32)
-    for y, what in ((y0, "no workspace"), (y1, "small workspace"), (y2, "full workspace")):
-        assert_linear_ok(y, y_ref, what)
-
-
-def test_linear_is_deterministic_and_reuses_its_workspace():
+def test_linear_is_deterministic():
     (X, Wq, sc, of), y_ref = _problem(3, 2048, 4096, 64, seed=9)
-    ws = w4.Workspace(DEV).reserve_for(3, 2048, 4096, 64)
-    assert ws.nbytes > 0
-    first = gpu_linear(X, Wq, sc, of, 64, workspace=ws)
+    first = gpu_linear(X, Wq, sc, of, 64)
     for _ in range(5):
-        again = gpu_linear(X, Wq, sc, of, 64, workspace=ws)
+        again = gpu_linear(X, Wq, sc, of, 64)
         assert torch.equal(first.view(torch.int16), again.view(torch.int16))
-    # the split-K tickets are back at zero after every call
-    ntick = (2048 + 63) // 64
-    assert int(ws.buf[: 4 * ntick].view(torch.int32).abs().sum()) == 0
     assert_linear_ok(first, y_ref, "repeat")
 
 
-def test_workspace_shared_by_calls_of_different_shapes():
-    """One workspace, calls whose row-tile counts and partial-sum sizes differ, in
-    both orders: the arrival counters must stay clear of every call's partials."""
-    small_tiles = _problem(32, 1030, 1024, 32, seed=31)   # few tiles, large partials
-    many_tiles = _problem(1, 14336, 1024, 32, seed=32)    # many tiles
-    ws = w4.Workspace(DEV).reserve(max(w4.w4_linear_workspace_bytes(32, 1030, 1024, 32),
-                                       w4.w4_linear_workspace_bytes(1, 14336, 1024, 32)))
-    for (dev, y_ref) in (small_tiles, many_tiles, small_tiles, many_tiles):
-        assert_linear_ok(gpu_linear(*dev, 32, workspace=ws), y_ref, "shared workspace")
+def test_consecutive_linears_overlap_safely():
+    """Back-to-back skinny launches on one stream may overlap (programmatic
+    dependent launch): a chain where each call reads the previous call's output
+    must still see it complete."""
+    K = 1024
+    Ws = [wl.gen_weight(K, K, seed=40 + i) for i in range(6)]
+    packed = [oracle.ref_quantize(bits(W), 32) for W in Ws]
+    dev = [(torch.from_numpy(q).to(DEV), torch.from_numpy(s.view(np.int16)).view(torch.bfloat16).to(DEV),
+            torch.from_numpy(o.view(np.int16)).view(torch.bfloat16).to(DEV)) for q, s, o in packed]
+    x = wl.gen_activation(1, K, seed=47)
+    y = x.to(DEV)
+    for d in dev:
+        y = w4.w4_linear(y, *d, 32)
+    torch.cuda.synchronize()
+    # the same chain, one linear at a time against the oracle's fp64 product of the previous GPU output
+    y = x.to(DEV)
+    for (q, s, o), d in zip(packed, dev):
+        y_ref = oracle.ref_linear(bits(y), q, s, o, 32)
+        y = w4.w4_linear(y, *d, 32)
+        torch.cuda.synchronize()
+        assert_linear_ok(y, y_ref, "chain")
 
 
 def test_linear_edge_shapes():
@@ -245,18 +241,17 @@ def test_empty_problems():
 
 def test_cuda_graph_capture_matches_eager():
     probs = [_problem(1, N, K, 32, seed=20 + i) for i, (N, K) in enumerate([(1024, 4096), (4096, 1024), (768, 2048)])]
-    wss = [w4.Workspace(DEV).reserve_for(1, p[0][1].shape[0], p[0][0].shape[1], 32) for p in probs]
     outs = [torch.empty((1, p[0][1].shape[0]), dtype=torch.bfloat16, device=DEV) for p in probs]
-    eager = [gpu_linear(*p[0], 32, workspace=ws).clone() for p, ws in zip(probs, wss)]
+    eager = [gpu_linear(*p[0], 32).clone() for p in probs]
     s = torch.cuda.Stream(DEV)
     s.wait_stream(torch.cuda.current_stream(DEV))
     with torch.cuda.stream(s):
-        for (dev, _), ws, out in zip(probs, wss, outs):  # warm up on the capture stream
-            w4.w4_linear(*dev, 32, out=out, workspace=ws)
+        for (dev, _), out in zip(probs, outs):  # warm up on the capture stream
+            w4.w4_linear(*dev, 32, out=out)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=s):
-            for (dev, _), ws, out in zip(probs, wss, outs):
-                w4.w4_linear(*dev, 32, out=out, workspace=ws)
+            for (dev, _), out in zip(probs, outs):
+                w4.w4_linear(*dev, 32, out=out)
     torch.cuda.current_stream(DEV).wait_stream(s)
     for out in outs:
         out.zero_()
