@@ -125,10 +125,15 @@ size_t w4_qparam_bytes(int64_t N, int64_t K, int group_size) {
 }
 
 w4_status w4_device_fault(void* stream) {
-    unsigned int fault = 0;
-    cudaError_t e = w4::read_and_clear_gemm_fault((cudaStream_t)stream, &fault);
-    if (e != cudaSuccess) return cuda_fail(e, "reading the device fault word");
-    if (fault) return fail(W4_ERR_TIMEOUT, "a tensor-core linear block gave up a bounded wait (code 0x%x)", fault);
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "synchronizing the stream");
+    unsigned int gemm = 0, skinny = 0;
+    e = w4::read_and_clear_gemm_fault(&gemm);
+    if (e == cudaSuccess) e = w4::read_and_clear_skinny_fault(&skinny);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device fault words");
+    if (gemm || skinny)
+        return fail(W4_ERR_TIMEOUT, "a block gave up a bounded wait (tensor-core linear 0x%x, skinny linear 0x%x)",
+                    gemm, skinny);
     return W4_OK;
 }
 
@@ -156,7 +161,7 @@ int w4_format_version(void) { return W4_FORMAT_VERSION; }
 
 namespace w4 {
 
-cudaError_t ensure_smem_limit(const void* kernel, int bytes) {
+cudaError_t ensure_kernel_attrs(const void* kernel, int smem_bytes, bool big_clusters) {
     static std::mutex mu;
     static std::unordered_map<const void*, uint64_t> done;  // kernel -> bitmask of devices already set
     int dev = 0;
@@ -165,7 +170,8 @@ cudaError_t ensure_smem_limit(const void* kernel, int bytes) {
     const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
     std::lock_guard<std::mutex> lock(mu);
     if (bit && (done[kernel] & bit)) return cudaSuccess;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e == cudaSuccess && big_clusters) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e == cudaSuccess && bit) done[kernel] |= bit;
     return e;
 }

@@ -129,6 +129,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
         :: "r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y) : "memory");
 }
+// Plain (untiled) bulk copy global -> this block's shared memory, completing
+// `bytes` on the mbarrier.  Both addresses 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
 // Generic-proxy writes to shared memory become visible to the async proxy
 // (tcgen05.mma operand reads) after this fence.
 __device__ __forceinline__ void fence_proxy_async_smem() {

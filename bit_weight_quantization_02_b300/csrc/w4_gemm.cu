@@ -288,7 +288,7 @@ template <int G>
 static cudaError_t launch_gemm_g(const CUtensorMap& tx, const CUtensorMap& tp, const uint16_t* scales,
                                  const uint16_t* offsets, uint16_t* Y, int M, int N, int K, cudaStream_t stream) {
     auto kern = gemm_kernel<G>;
-    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), GM_SMEM_BYTES);
+    cudaError_t e = ensure_kernel_attrs(reinterpret_cast<const void*>(kern), GM_SMEM_BYTES, false);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((N + GM_BN - 1) / GM_BN), (unsigned)((M + GM_BM - 1) / GM_BM));
     kern<<<grid, GM_THREADS, GM_SMEM_BYTES, stream>>>(tx, tp, scales, offsets, Y, M, N, K);
@@ -339,10 +339,8 @@ cudaError_t launch_gemm(const uint16_t* X, int64_t M, int64_t K, const uint8_t* 
     }
 }
 
-cudaError_t read_and_clear_gemm_fault(cudaStream_t stream, unsigned int* fault) {
-    cudaError_t e = cudaStreamSynchronize(stream);
-    if (e != cudaSuccess) return e;
-    e = cudaMemcpyFromSymbol(fault, g_gemm_fault, sizeof(unsigned int));
+cudaError_t read_and_clear_gemm_fault(unsigned int* fault) {
+    cudaError_t e = cudaMemcpyFromSymbol(fault, g_gemm_fault, sizeof(unsigned int));
     if (e != cudaSuccess) return e;
     if (*fault) {
         const unsigned int zero = 0;

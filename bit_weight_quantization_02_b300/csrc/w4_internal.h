@@ -21,6 +21,7 @@ struct SkinnyPlan {
     int ks;       // k per slice
     int kc;       // k per staged activation sub-chunk
     size_t smem;  // dynamic shared memory bytes
+    bool qtma;    // qparam rows 16-byte aligned: copied by TMA with the codes
 };
 constexpr int SKINNY_ROWS = 64;
 constexpr int SKINNY_MAX_M = 32;
@@ -33,11 +34,14 @@ cudaError_t launch_skinny(const SkinnyPlan& plan, const uint16_t* X, int64_t M, 
 cudaError_t launch_gemm(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
                         const uint16_t* offsets, int64_t N, int g, uint16_t* Y, cudaStream_t stream,
                         const char** detail);
-// Reads and clears the GEMM's device fault word (bounded-wait timeouts).
-cudaError_t read_and_clear_gemm_fault(cudaStream_t stream, unsigned int* fault);
+// Read and clear the kernels' device fault words (bounded-wait timeouts); the
+// caller has synchronized the stream.
+cudaError_t read_and_clear_gemm_fault(unsigned int* fault);
+cudaError_t read_and_clear_skinny_fault(unsigned int* fault);
 
-// Raises a kernel's dynamic shared-memory limit to `bytes`, once per device
-// and kernel (later calls, e.g. during CUDA-graph capture, make no CUDA call).
-cudaError_t ensure_smem_limit(const void* kernel, int bytes);
+// Raises a kernel's dynamic shared-memory limit to `smem_bytes` (and allows
+// cluster sizes above 8 if asked), once per device and kernel: later calls,
+// e.g. during CUDA-graph capture, make no CUDA call.
+cudaError_t ensure_kernel_attrs(const void* kernel, int smem_bytes, bool big_clusters);
 
 }  // namespace w4

@@ -7,10 +7,12 @@
 // and k), so the kernel is built to stream them at HBM speed with as few
 // instructions per weight as possible:
 //
-//  * Thread block = 4 warps = 64 output rows x one K slice.  A warp owns 16
-//    rows; each lane streams 16 bytes (32 codes) of two rows per 128-k step
-//    with 128-bit non-allocating loads, plus the two rows' scale and offset,
-//    ping-ponging between two register buffers a few steps ahead.
+//  * Thread block = 4 warps = 64 output rows x one K slice.  At block start,
+//    64 threads each issue one TMA bulk copy of their row's codes (and, when
+//    16-byte aligned, its scales and offsets) into shared memory, all landing
+//    on one mbarrier: the block's whole slice is in flight at once, before the
+//    block even waits for the previous kernel.  Warps then read 16 bytes (32
+//    codes) of two rows per 128-k step from shared memory.
 //  * In-register dequantization: one LOP3 turns a 32-bit word of codes into
 //    the bf16 pairs (128+q_i, 128+q_{i+4}); an exact subtract and one bf16 FMA
 //    give w' = bf16(q*s + o) with a single rounding.
@@ -44,7 +46,6 @@ namespace w4 {
 constexpr int SK_WARPS = 4;
 constexpr int SK_THREADS = SK_WARPS * 32;
 constexpr int SK_KSTEP = 128;  // k per step: 4 lanes x 32 codes
-constexpr int SK_U = 2;        // steps per register buffer
 
 static_assert(SKINNY_ROWS == 16 * SK_WARPS, "row tile");
 
@@ -75,21 +76,48 @@ struct SkinnyArgs {
     const uint16_t* offsets;
     uint16_t* Y;
     int M, N, K;
-    int ks;      // k per slice (multiple of SK_KSTEP * SK_U)
-    int kc;      // k per staged X sub-chunk (multiple of SK_KSTEP * SK_U, divides ks)
+    int ks;      // k per slice (multiple of 256)
+    int kc;      // k per staged X sub-chunk (multiple of 256, divides ks)
     int splits;  // K slices = cluster size along grid.y
+    int qtma;    // 1: qparam rows are 16-byte aligned and copied by TMA; 0: plain loads
 };
 
-template <int U>
-struct WBuf {
-    uint4 a[U], b[U];       // 16 bytes of codes of rows a and b per step
-    uint32_t qa[U], qb[U];  // (scale | offset << 16) of rows a and b per step
+// Byte offsets inside the dynamic shared memory of one block (host and device
+// compute the same layout).
+struct SkLayout {
+    int wpitch, qpitch, xpitch;
+    int off_s, off_o, off_x, off_z, off_part, off_bar, total;
 };
+__host__ __device__ inline SkLayout sk_layout(int M, int ks, int kc, int g, int splits) {
+    SkLayout L;
+    L.wpitch = ks / 2 + 64;  // = 64 (mod 128): the two rows of a quarter-warp use other banks
+    L.qpitch = ((2 * (ks / g) + 15) / 16) * 16 + 16;
+    L.xpitch = kc * 2 + 16;
+    int off = SKINNY_ROWS * L.wpitch;
+    L.off_s = off;
+    off += SKINNY_ROWS * L.qpitch;
+    L.off_o = off;
+    off += SKINNY_ROWS * L.qpitch;
+    L.off_x = off;
+    off += M * L.xpitch;
+    L.off_z = off;
+    off += L.xpitch;
+    L.off_part = off;
+    off += splits > 1 ? M * SKINNY_ROWS * 4 : 0;
+    L.off_bar = off;
+    off += 16;
+    L.total = off;
+    return L;
+}
+
+__device__ unsigned int g_skinny_fault;
+constexpr uint64_t SK_WAIT_LIMIT_NS = 2000000000ull;
 
 template <int MT, int G>
 __global__ void __launch_bounds__(SK_THREADS)
 skinny_kernel(const SkinnyArgs p) {
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
+    const SkLayout L = sk_layout(p.M, p.ks, p.kc, G, p.splits);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, tq = lane & 3;
@@ -97,51 +125,72 @@ skinny_kernel(const SkinnyArgs p) {
     const int k0 = slice * p.ks;
     const int klen = min(p.K - k0, p.ks);  // multiple of 32
     const int nsteps = (klen + SK_KSTEP - 1) / SK_KSTEP;
-    const int nbuf = (nsteps + SK_U - 1) / SK_U;  // register buffers to consume
-    const int pitch = p.kc * 2 + 16;              // bytes per staged token row
+    const int row0 = tile * SKINNY_ROWS;
+    const int nrows = min(SKINNY_ROWS, p.N - row0);
+    const int ng = p.K / G;
+    const int nqs = klen / G;  // groups of this slice (>= 1)
 
-    unsigned char* xs = smem;                              // [M][pitch]
-    unsigned char* zrow = smem + (size_t)p.M * pitch;      // [pitch] zeros
-    float* part = reinterpret_cast<float*>(zrow + pitch);  // [M][64]
+    unsigned char* wsm = smem;                                           // [64][wpitch] codes
+    uint16_t* ssm = reinterpret_cast<uint16_t*>(smem + L.off_s);         // [64][qpitch/2] scales
+    uint16_t* osm = reinterpret_cast<uint16_t*>(smem + L.off_o);         // [64][qpitch/2] offsets
+    unsigned char* xs = smem + L.off_x;                                  // [M][xpitch] staged X
+    unsigned char* zrow = smem + L.off_z;                                // [xpitch] zeros
+    float* part = reinterpret_cast<float*>(smem + L.off_part);           // [M][64] partial sums
+    const uint32_t bar = smem_u32(smem + L.off_bar);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.off_bar + 8);
 
     griddep_launch_dependents();
 
-    const int row0 = tile * SKINNY_ROWS;
-    const int ra = row0 + warp * 16 + gid;
-    const int rb = ra + 8;
-    const bool va = ra < p.N, vb = rb < p.N;
-    const uint8_t* wa = p.Wq + (int64_t)(va ? ra : 0) * (p.K / 2) + k0 / 2;
-    const uint8_t* wb = p.Wq + (int64_t)(vb ? rb : 0) * (p.K / 2) + k0 / 2;
-    const int ng = p.K / G;
-    const int64_t qoffa = (int64_t)(va ? ra : 0) * ng + k0 / G;
-    const int64_t qoffb = (int64_t)(vb ? rb : 0) * ng + k0 / G;
-
-    auto load = [&](int buf, WBuf<SK_U>& w) {
-#pragma unroll
-        for (int u = 0; u < SK_U; ++u) {
-            const int kk = (buf * SK_U + u) * SK_KSTEP + 32 * tq;  // this lane's 32 codes, within the slice
-            const bool in = kk < klen;
-            const int j = kk / G;
-            w.a[u] = (in && va) ? ldg_stream_v4(wa + kk / 2) : make_uint4(0u, 0u, 0u, 0u);
-            w.b[u] = (in && vb) ? ldg_stream_v4(wb + kk / 2) : make_uint4(0u, 0u, 0u, 0u);
-            w.qa[u] = (in && va) ? (ldg_nc_u16(p.scales + qoffa + j) | (ldg_nc_u16(p.offsets + qoffa + j) << 16)) : 0u;
-            w.qb[u] = (in && vb) ? (ldg_nc_u16(p.scales + qoffb + j) | (ldg_nc_u16(p.offsets + qoffb + j) << 16)) : 0u;
+    // ---- the block's whole weight slice, in flight at once (before waiting on the previous kernel)
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+    const uint32_t wbytes = (uint32_t)klen / 2;
+    const uint32_t qbytes = p.qtma ? (uint32_t)(2 * nqs) : 0u;
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(bar, (uint32_t)nrows * (wbytes + 2u * qbytes));
+    __syncthreads();
+    if ((int)threadIdx.x < nrows) {
+        const int64_t n = row0 + threadIdx.x;
+        bulk_load(smem_u32(wsm + threadIdx.x * L.wpitch), p.Wq + n * (p.K / 2) + k0 / 2, wbytes, bar);
+        if (p.qtma) {
+            bulk_load(smem_u32(ssm) + threadIdx.x * L.qpitch, p.scales + n * ng + k0 / G, qbytes, bar);
+            bulk_load(smem_u32(osm) + threadIdx.x * L.qpitch, p.offsets + n * ng + k0 / G, qbytes, bar);
         }
-    };
+    }
+    if (!p.qtma) {
+        for (int r = 0; r < nrows; ++r)
+            for (int j = threadIdx.x; j < nqs; j += SK_THREADS) {
+                const int64_t idx = (int64_t)(row0 + r) * ng + k0 / G + j;
+                ssm[r * (L.qpitch / 2) + j] = (uint16_t)ldg_nc_u16(p.scales + idx);
+                osm[r * (L.qpitch / 2) + j] = (uint16_t)ldg_nc_u16(p.offsets + idx);
+            }
+    }
+    // codes and qparams past the slice end inside the last step read as zeros
+    // (w' = 0*0 + 0: never-written shared memory could hold NaN patterns)
+    const int tail16 = (nsteps * 64 - (int)wbytes) / 16;
+    if (tail16 > 0)
+        for (int r = 0; r < nrows; ++r)
+            for (int c = threadIdx.x; c < tail16; c += SK_THREADS)
+                *reinterpret_cast<uint4*>(wsm + r * L.wpitch + wbytes + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
+    const int qsteps = nsteps * SK_KSTEP / G;  // groups the last step touches (> nqs only when !qtma)
+    if (qsteps > nqs)
+        for (int r = 0; r < nrows; ++r)
+            for (int j = nqs + threadIdx.x; j < qsteps; j += SK_THREADS) {
+                ssm[r * (L.qpitch / 2) + j] = 0;
+                osm[r * (L.qpitch / 2) + j] = 0;
+            }
 
-    WBuf<SK_U> w0, w1;
-    load(0, w0);
-
-    // activations may come from the previous kernel: wait for it
+    // ---- activations may come from the previous kernel: wait for it, then stage X
     griddep_wait();
-
-    // stage X[:, k0 + c0 : k0 + c0 + kc] into the token rows; zeros past the slice end
     const int kc_chunks = p.kc / 8;
-    auto stage = [&](int c0) {  // c0 = first k of the sub-chunk, relative to k0
+    auto stage = [&](int c0) {  // X[:, k0 + c0 : k0 + c0 + kc], each 8-k chunk permuted; zeros past the slice
         const int valid = max(0, min(p.kc, klen - c0)) / 8;
         for (int m = 0; m < p.M; ++m) {
             const uint16_t* xrow = p.X + (int64_t)m * p.K + k0 + c0;
-            unsigned char* srow = xs + (size_t)m * pitch;
+            unsigned char* srow = xs + (size_t)m * L.xpitch;
             for (int c = threadIdx.x; c < kc_chunks; c += SK_THREADS) {
                 uint4 o = make_uint4(0u, 0u, 0u, 0u);
                 if (c < valid) {
@@ -160,16 +209,27 @@ skinny_kernel(const SkinnyArgs p) {
     stage(0);
     __syncthreads();
 
-    // per-lane B addresses: token row (or the zero row) + swizzled chunk offsets
+    // ---- weights landed? (bounded; a block that gives up computes garbage but still
+    // meets every barrier of its cluster, and drains its copies before leaving)
+    const bool ok = mbar_wait_bounded(bar, 0, abort_flag, &g_skinny_fault, 1u, SK_WAIT_LIMIT_NS);
+
     uint32_t bbase[MT];
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
         const int m = 8 * t + gid;
-        bbase[t] = smem_u32(m < p.M ? xs + (size_t)m * pitch : zrow);
+        bbase[t] = smem_u32(m < p.M ? xs + (size_t)m * L.xpitch : zrow);
     }
     uint32_t boff[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) boff[j] = 16u * (uint32_t)((4 * tq + j) ^ ((tq >> 1) << 1));
+
+    const int ra = warp * 16 + gid;  // local rows ra and ra + 8
+    const uint32_t wa_addr0 = smem_u32(wsm) + ra * L.wpitch + 16 * tq;
+    const uint32_t wb_addr0 = wa_addr0 + 8 * L.wpitch;
+    const uint16_t* sa_p = ssm + ra * (L.qpitch / 2);
+    const uint16_t* oa_p = osm + ra * (L.qpitch / 2);
+    const uint16_t* sb_p = sa_p + 8 * (L.qpitch / 2);
+    const uint16_t* ob_p = oa_p + 8 * (L.qpitch / 2);
 
     float acc[MT][4];
 #pragma unroll
@@ -177,133 +237,130 @@ skinny_kernel(const SkinnyArgs p) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[t][i] = 0.0f;
 
-    const int bufs_per_chunk = p.kc / (SK_KSTEP * SK_U);
-
-    auto compute = [&](int buf, const WBuf<SK_U>& w) {
-        if (buf > 0 && buf % bufs_per_chunk == 0) {  // next X sub-chunk (block-uniform)
+    const int steps_per_chunk = p.kc / SK_KSTEP;
+    int sc = 0;        // step inside the staged X sub-chunk
+    uint32_t xo = 0;   // its byte offset in a staged row
+#pragma unroll 2
+    for (int s = 0; s < nsteps; ++s) {
+        if (sc == steps_per_chunk) {  // next X sub-chunk (block-uniform)
             __syncthreads();
-            stage((buf / bufs_per_chunk) * p.kc);
+            stage(s * SK_KSTEP);
             __syncthreads();
+            sc = 0;
+            xo = 0;
         }
-        const int sbase = (buf % bufs_per_chunk) * SK_U;  // first step of this buffer inside the sub-chunk
+        const uint4 wa = lds128(wa_addr0 + 64u * s);
+        const uint4 wb = lds128(wb_addr0 + 64u * s);
+        const int jg = (s * SK_KSTEP + 32 * tq) / G;
+        const uint32_t sa2 = __byte_perm(sa_p[jg], 0, 0x1010), oa2 = __byte_perm(oa_p[jg], 0, 0x1010);
+        const uint32_t sb2 = __byte_perm(sb_p[jg], 0, 0x1010), ob2 = __byte_perm(ob_p[jg], 0, 0x1010);
+        const uint32_t wa4[4] = {wa.x, wa.y, wa.z, wa.w};
+        const uint32_t wb4[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
-        for (int u = 0; u < SK_U; ++u) {
-            if (buf * SK_U + u < nsteps) {
-                const uint32_t sa2 = __byte_perm(w.qa[u], 0, 0x1010), oa2 = __byte_perm(w.qa[u], 0, 0x3232);
-                const uint32_t sb2 = __byte_perm(w.qb[u], 0, 0x1010), ob2 = __byte_perm(w.qb[u], 0, 0x3232);
-                const uint32_t wa4[4] = {w.a[u].x, w.a[u].y, w.a[u].z, w.a[u].w};
-                const uint32_t wb4[4] = {w.b[u].x, w.b[u].y, w.b[u].z, w.b[u].w};
-                const uint32_t soff = (uint32_t)(sbase + u) * 256u;  // 16 chunks of 16 bytes per step
+        for (int j = 0; j < 4; ++j) {
+            // A fragments: (n0,n4),(n1,n5),(n2,n6),(n3,n7) of rows a and b
+            const uint32_t a0 = dequant_pair(nib_pair_biased(wa4[j]), sa2, oa2);
+            const uint32_t a1 = dequant_pair(nib_pair_biased(wa4[j] >> 4), sa2, oa2);
+            const uint32_t a2 = dequant_pair(nib_pair_biased(wa4[j] >> 8), sa2, oa2);
+            const uint32_t a3 = dequant_pair(nib_pair_biased(wa4[j] >> 12), sa2, oa2);
+            const uint32_t b0 = dequant_pair(nib_pair_biased(wb4[j]), sb2, ob2);
+            const uint32_t b1 = dequant_pair(nib_pair_biased(wb4[j] >> 4), sb2, ob2);
+            const uint32_t b2 = dequant_pair(nib_pair_biased(wb4[j] >> 8), sb2, ob2);
+            const uint32_t b3 = dequant_pair(nib_pair_biased(wb4[j] >> 12), sb2, ob2);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    // A fragments: (n0,n4),(n1,n5),(n2,n6),(n3,n7) of rows a and b
-                    const uint32_t a0 = dequant_pair(nib_pair_biased(wa4[j]), sa2, oa2);
-                    const uint32_t a1 = dequant_pair(nib_pair_biased(wa4[j] >> 4), sa2, oa2);
-                    const uint32_t a2 = dequant_pair(nib_pair_biased(wa4[j] >> 8), sa2, oa2);
-                    const uint32_t a3 = dequant_pair(nib_pair_biased(wa4[j] >> 12), sa2, oa2);
-                    const uint32_t b0 = dequant_pair(nib_pair_biased(wb4[j]), sb2, ob2);
-                    const uint32_t b1 = dequant_pair(nib_pair_biased(wb4[j] >> 4), sb2, ob2);
-                    const uint32_t b2 = dequant_pair(nib_pair_biased(wb4[j] >> 8), sb2, ob2);
-                    const uint32_t b3 = dequant_pair(nib_pair_biased(wb4[j] >> 12), sb2, ob2);
-#pragma unroll
-                    for (int t = 0; t < MT; ++t) {
-                        const uint4 xv = lds128(bbase[t] + soff + boff[j]);
-                        mma_bf16_16816(acc[t], a0, b0, a1, b1, xv.x, xv.y);
-                        mma_bf16_16816(acc[t], a2, b2, a3, b3, xv.z, xv.w);
-                    }
-                }
+            for (int t = 0; t < MT; ++t) {
+                const uint4 xv = lds128(bbase[t] + xo + boff[j]);
+                mma_bf16_16816(acc[t], a0, b0, a1, b1, xv.x, xv.y);
+                mma_bf16_16816(acc[t], a2, b2, a3, b3, xv.z, xv.w);
             }
         }
-    };
-
-    for (int buf = 0; buf < nbuf; buf += 2) {
-        if (buf + 1 < nbuf) load(buf + 1, w1);
-        compute(buf, w0);
-        if (buf + 1 < nbuf) {
-            if (buf + 2 < nbuf) load(buf + 2, w0);
-            compute(buf + 1, w1);
-        }
+        ++sc;
+        xo += 256u;  // 16 chunks of 16 bytes per step
     }
 
-    // acc[t][i] = D[row gid (i<2) or gid+8][token 8t + 2tq + (i&1)]
+    // acc[t][i] = D[row ra (i<2) or ra+8][token 8t + 2tq + (i&1)]
     if (p.splits == 1) {
 #pragma unroll
         for (int t = 0; t < MT; ++t) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int m = 8 * t + 2 * tq + (i & 1);
-                const int n = (i < 2) ? ra : rb;
+                const int n = row0 + ra + ((i < 2) ? 0 : 8);
                 if (m < p.M && n < p.N) p.Y[(int64_t)m * p.N + n] = (uint16_t)float_to_bf16_bits(acc[t][i]);
             }
         }
-        return;
-    }
-
-    // split K: partial tile -> own shared memory, then a share of the sum over the cluster
+    } else {
+        // split K: partial tile -> own shared memory, then a share of the sum over the cluster
 #pragma unroll
-    for (int t = 0; t < MT; ++t) {
+        for (int t = 0; t < MT; ++t) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int m = 8 * t + 2 * tq + (i & 1);
-            const int r = warp * 16 + gid + ((i < 2) ? 0 : 8);
-            if (m < p.M) part[m * SKINNY_ROWS + r] = acc[t][i];
+            for (int i = 0; i < 4; ++i) {
+                const int m = 8 * t + 2 * tq + (i & 1);
+                if (m < p.M) part[m * SKINNY_ROWS + ra + ((i < 2) ? 0 : 8)] = acc[t][i];
+            }
         }
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();
+        const int total = p.M * SKINNY_ROWS;
+        const int share = (total + p.splits - 1) / p.splits;
+        const int rank = (int)cluster.block_rank();
+        const int lo = rank * share, hi = min(total, lo + share);
+        for (int idx = lo + threadIdx.x; idx < hi; idx += SK_THREADS) {
+            float sum = 0.0f;
+            for (int q = 0; q < p.splits; ++q) sum += cluster.map_shared_rank(part, q)[idx];
+            const int m = idx / SKINNY_ROWS, r = idx % SKINNY_ROWS;
+            const int n = row0 + r;
+            if (n < p.N) p.Y[(int64_t)m * p.N + n] = (uint16_t)float_to_bf16_bits(sum);
+        }
+        cluster.sync();  // no block leaves while its partials may still be read
     }
-    cg::cluster_group cluster = cg::this_cluster();
-    cluster.sync();
-    const int total = p.M * SKINNY_ROWS;
-    const int share = (total + p.splits - 1) / p.splits;
-    const int rank = (int)cluster.block_rank();
-    const int lo = rank * share, hi = min(total, lo + share);
-    for (int idx = lo + threadIdx.x; idx < hi; idx += SK_THREADS) {
-        float s = 0.0f;
-        for (int q = 0; q < p.splits; ++q) s += cluster.map_shared_rank(part, q)[idx];
-        const int m = idx / SKINNY_ROWS, r = idx % SKINNY_ROWS;
-        const int n = row0 + r;
-        if (n < p.N) p.Y[(int64_t)m * p.N + n] = (uint16_t)float_to_bf16_bits(s);
-    }
-    cluster.sync();  // no block leaves while its partials may still be read
+    if (!ok) mbar_drain_bounded(bar, 0, SK_WAIT_LIMIT_NS);  // never leave with copies landing in smem
 }
 
 // ------------------------------------------------------------------ host side
 
-static constexpr int SK_TARGET_BLOCKS = 148 * 6;  // about 6 resident blocks on each of 148 SMs
-static constexpr int SK_MAX_SPLIT = 8;            // portable cluster size
-static constexpr size_t SK_SMEM_CAP = 40 * 1024;  // keeps >= 5 blocks per SM; below the default 48 KB
-
-static size_t skinny_smem_bytes(int M, int kc, int splits) {
-    return (size_t)(M + 1) * (kc * 2 + 16) + (splits > 1 ? (size_t)M * SKINNY_ROWS * 4 : 0);
-}
+static constexpr int SK_TARGET_BLOCKS = 148 * 4;  // ~4 resident blocks (~50 KB of shared memory each) per SM
+static constexpr int SK_MAX_SPLIT = 16;           // cluster size (above 8 needs the non-portable opt-in)
+static constexpr int SK_QUANT = 256;              // slices and sub-chunks are whole 256-k units
+static constexpr int SK_MAX_KS = 2048;            // longest slice: 64 rows x 1 KB of codes
+static constexpr int SK_XCAP = 16 * 1024;         // staged X budget
+static constexpr int SK_SMEM_MAX = 200 * 1024;
 
 bool plan_skinny(int64_t M, int64_t N, int64_t K, int g, SkinnyPlan* plan) {
-    (void)g;
     if (M < 1 || M > SKINNY_MAX_M) return false;
     const int64_t tiles = (N + SKINNY_ROWS - 1) / SKINNY_ROWS;
     if (tiles > 0x7FFFFFFF) return false;
-    const int quantum = SK_KSTEP * SK_U;  // slices and sub-chunks are whole register buffers
-    const int64_t kq = (K + quantum - 1) / quantum;
-    int splits = (int)std::min<int64_t>(SK_MAX_SPLIT, std::max<int64_t>(1, (SK_TARGET_BLOCKS + tiles - 1) / tiles));
-    splits = (int)std::min<int64_t>(splits, kq);
-    const int64_t ks = (kq + splits - 1) / splits * quantum;
-    splits = (int)((K + ks - 1) / ks);
-    // largest sub-chunk (whole quanta, dividing ks) whose staged X fits the cap
-    int64_t kc = ks;
-    while (kc > quantum && skinny_smem_bytes((int)M, (int)kc, splits) > SK_SMEM_CAP) {
-        int64_t q = kc / quantum - 1;
-        while (q > 1 && (ks / quantum) % q != 0) --q;
-        kc = q * quantum;
+    const int64_t kq = (K + SK_QUANT - 1) / SK_QUANT;
+    int64_t splits = std::min<int64_t>(SK_MAX_SPLIT, std::max<int64_t>(1, (K + 1023) / 1024));
+    // few row tiles: more, shorter slices (down to 512 k) so the launch fills the GPU
+    while (splits < SK_MAX_SPLIT && tiles * splits < SK_TARGET_BLOCKS && (kq + splits) / (splits + 1) >= 2) ++splits;
+    int64_t ks = (kq + splits - 1) / splits * SK_QUANT;
+    if (ks > SK_MAX_KS) return false;  // K too long for 16 slices: the tensor-core path takes it
+    splits = (K + ks - 1) / ks;
+    int64_t kc = ks;  // largest sub-chunk (whole units, dividing ks) whose staged X fits
+    while (kc > SK_QUANT && (M + 1) * (2 * kc + 16) > SK_XCAP) {
+        int64_t q = kc / SK_QUANT - 1;
+        while (q > 1 && (ks / SK_QUANT) % q != 0) --q;
+        kc = q * SK_QUANT;
     }
+    const SkLayout L = sk_layout((int)M, (int)ks, (int)kc, g, (int)splits);
+    if (L.total > SK_SMEM_MAX) return false;
+    const int64_t ng = K / g;
+    const int64_t last = K - (splits - 1) * ks;
     plan->tiles = (int)tiles;
-    plan->splits = splits;
+    plan->splits = (int)splits;
     plan->ks = (int)ks;
     plan->kc = (int)kc;
-    plan->smem = skinny_smem_bytes((int)M, (int)kc, splits);
+    plan->smem = (size_t)L.total;
+    plan->qtma = (ng % 8 == 0) && ((ks / g) % 8 == 0) && ((last / g) % 8 == 0);
     return true;
 }
 
 template <int MT, int G>
 static cudaError_t launch_one(const SkinnyPlan& plan, const SkinnyArgs& a, cudaStream_t stream) {
-    auto kern = skinny_kernel<MT, G>;  // dynamic shared memory <= SK_SMEM_CAP, under the default 48 KB
+    auto kern = skinny_kernel<MT, G>;
+    cudaError_t e = ensure_kernel_attrs(reinterpret_cast<const void*>(kern), SK_SMEM_MAX, true);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)plan.tiles, (unsigned)plan.splits, 1);
     cfg.blockDim = dim3(SK_THREADS, 1, 1);
@@ -346,11 +403,19 @@ cudaError_t launch_skinny(const SkinnyPlan& plan, const uint16_t* X, int64_t M, 
     a.ks = plan.ks;
     a.kc = plan.kc;
     a.splits = plan.splits;
+    a.qtma = plan.qtma ? 1 : 0;
     switch (g) {
         case 32: return launch_g<32>(plan, a, stream);
         case 64: return launch_g<64>(plan, a, stream);
         default: return launch_g<128>(plan, a, stream);
     }
+}
+
+cudaError_t read_and_clear_skinny_fault(unsigned int* fault) {
+    cudaError_t e = cudaMemcpyFromSymbol(fault, g_skinny_fault, sizeof(unsigned int));
+    if (e != cudaSuccess || !*fault) return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_skinny_fault, &zero, sizeof(unsigned int));
 }
 
 }  // namespace w4
