@@ -100,8 +100,10 @@ w4_status w4_linear_ex(const uint16_t* X, int64_t M, int64_t K, const uint8_t* W
     if (use_skinny) {
         w4::SkinnyPlan plan;
         if (!w4::plan_skinny(M, N, K, group_size, &plan)) return fail(W4_ERR_INVALID_ARG, "no skinny launch plan");
-        e = w4::launch_skinny(plan, X, M, K, Wq, scales, offsets, N, group_size, Y, (cudaStream_t)stream);
-        return e == cudaSuccess ? W4_OK : cuda_fail(e, "skinny linear launch");
+        const char* detail = "";
+        e = w4::launch_skinny(plan, X, M, K, Wq, scales, offsets, N, group_size, Y, (cudaStream_t)stream, &detail);
+        if (e != cudaSuccess) return fail(W4_ERR_CUDA, "skinny linear: %s %s", cudaGetErrorString(e), detail);
+        return W4_OK;
     }
     const char* detail = "";
     e = w4::launch_gemm(X, M, K, Wq, scales, offsets, N, group_size, Y, (cudaStream_t)stream, &detail);
@@ -159,7 +161,47 @@ int w4_format_version(void) { return W4_FORMAT_VERSION; }
 #include <mutex>
 #include <unordered_map>
 
+#include <cuda.h>
+
 namespace w4 {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+cudaError_t encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+                                 uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                                 CUtensorMapSwizzle swizzle, const char** detail) {
+    EncodeTiledFn encode = encode_fn();
+    if (!encode) {
+        *detail = "cuTensorMapEncodeTiled is not available from the driver";
+        return cudaErrorNotSupported;
+    }
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_stride_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+        *detail = "tensor map rejected by the driver";
+        return cudaErrorInvalidValue;
+    }
+    return cudaSuccess;
+}
 
 cudaError_t ensure_kernel_attrs(const void* kernel, int smem_bytes, bool big_clusters) {
     static std::mutex mu;

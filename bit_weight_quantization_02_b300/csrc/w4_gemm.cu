@@ -25,8 +25,6 @@
 #include "w4_device.cuh"
 #include "w4_internal.h"
 
-#include <cuda.h>
-#include <mutex>
 
 namespace w4 {
 
@@ -266,24 +264,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
 
 // ------------------------------------------------------------------ host side
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn get_encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
 template <int G>
 static cudaError_t launch_gemm_g(const CUtensorMap& tx, const CUtensorMap& tp, const uint16_t* scales,
                                  const uint16_t* offsets, uint16_t* Y, int M, int N, int K, cudaStream_t stream) {
@@ -298,40 +278,19 @@ static cudaError_t launch_gemm_g(const CUtensorMap& tx, const CUtensorMap& tp, c
 cudaError_t launch_gemm(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
                         const uint16_t* offsets, int64_t N, int g, uint16_t* Y, cudaStream_t stream,
                         const char** detail) {
-    EncodeTiledFn encode = get_encode_fn();
-    if (!encode) {
-        *detail = "cuTensorMapEncodeTiled is not available from the driver";
-        return cudaErrorNotSupported;
-    }
     if ((N + GM_BN - 1) / GM_BN > 0x7FFFFFFF || (M + GM_BM - 1) / GM_BM > 65535) {
         *detail = "problem too large for the GEMM grid";
         return cudaErrorInvalidValue;
     }
     CUtensorMap tx, tp;
-    {
-        const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-        const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-        const cuuint32_t box[2] = {GM_BK, GM_BM};
-        const cuuint32_t estr[2] = {1, 1};
-        if (encode(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(X), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
-            *detail = "tensor map for X rejected";
-            return cudaErrorInvalidValue;
-        }
-    }
-    {
-        const cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)N};
-        const cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
-        const cuuint32_t box[2] = {GM_BK / 2, GM_BN};
-        const cuuint32_t estr[2] = {1, 1};
-        if (encode(&tp, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(Wq), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
-            *detail = "tensor map for the packed codes rejected";
-            return cudaErrorInvalidValue;
-        }
-    }
+    // X: [M][K] bf16, box 128 tokens x 64 k (128 bytes), 128-byte swizzle (the UMMA A layout)
+    cudaError_t e = encode_tensor_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)K, (uint64_t)M,
+                                         (uint64_t)K * 2, GM_BK, GM_BM, CU_TENSOR_MAP_SWIZZLE_128B, detail);
+    if (e != cudaSuccess) return e;
+    // codes: [N][K/2] bytes, box 256 rows x 32 bytes
+    e = encode_tensor_map_2d(&tp, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)(K / 2), (uint64_t)N, (uint64_t)(K / 2),
+                             GM_BK / 2, GM_BN, CU_TENSOR_MAP_SWIZZLE_NONE, detail);
+    if (e != cudaSuccess) return e;
     switch (g) {
         case 32: return launch_gemm_g<32>(tx, tp, scales, offsets, Y, (int)M, (int)N, (int)K, stream);
         case 64: return launch_gemm_g<64>(tx, tp, scales, offsets, Y, (int)M, (int)N, (int)K, stream);

@@ -5,6 +5,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace w4 {
@@ -28,7 +29,7 @@ constexpr int SKINNY_MAX_M = 32;
 bool plan_skinny(int64_t M, int64_t N, int64_t K, int g, SkinnyPlan* plan);
 cudaError_t launch_skinny(const SkinnyPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
                           const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
-                          cudaStream_t stream);
+                          cudaStream_t stream, const char** detail);
 
 // tcgen05 tensor-core GEMM (any M).
 cudaError_t launch_gemm(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
@@ -43,5 +44,11 @@ cudaError_t read_and_clear_skinny_fault(unsigned int* fault);
 // cluster sizes above 8 if asked), once per device and kernel: later calls,
 // e.g. during CUDA-graph capture, make no CUDA call.
 cudaError_t ensure_kernel_attrs(const void* kernel, int smem_bytes, bool big_clusters);
+
+// Encodes a 2-D tiled TMA descriptor for a row-major [outer][inner] tensor
+// (driver entry point fetched once; a host-only call, fine during capture).
+cudaError_t encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+                                 uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                                 CUtensorMapSwizzle swizzle, const char** detail);
 
 }  // namespace w4

@@ -7,12 +7,15 @@
 // and k), so the kernel is built to stream them at HBM speed with as few
 // instructions per weight as possible:
 //
-//  * Thread block = 4 warps = 64 output rows x one K slice.  At block start,
-//    64 threads each issue one TMA bulk copy of their row's codes (and, when
-//    16-byte aligned, its scales and offsets) into shared memory, all landing
-//    on one mbarrier: the block's whole slice is in flight at once, before the
-//    block even waits for the previous kernel.  Warps then read 16 bytes (32
-//    codes) of two rows per 128-k step from shared memory.
+//  * Thread block = 4 warps = 64 output rows x one K slice of up to 2048 k.
+//    At block start one thread issues the whole slice as 2-D TMA copies of
+//    64 rows x 256 k (128 bytes, 128-byte swizzle), one mbarrier per copy,
+//    plus the slice's scales and offsets: everything is in flight before the
+//    block even waits for the previous kernel, and compute on the first 256 k
+//    starts as soon as it lands.  TMA zero-fills rows past N and k past K.
+//    Warps read 16 bytes (32 codes) of two rows per 128-k step from shared
+//    memory; the rows of an MMA tile are permuted so the swizzled reads of a
+//    quarter-warp fall in distinct banks.
 //  * In-register dequantization: one LOP3 turns a 32-bit word of codes into
 //    the bf16 pairs (128+q_i, 128+q_{i+4}); an exact subtract and one bf16 FMA
 //    give w' = bf16(q*s + o) with a single rounding.
@@ -38,6 +41,7 @@
 
 #include <algorithm>
 #include <cooperative_groups.h>
+#include <cuda.h>
 
 namespace cg = cooperative_groups;
 
@@ -71,33 +75,38 @@ __device__ __forceinline__ int x_slot(int c) { return c ^ (((c >> 3) & 1) << 1);
 
 struct SkinnyArgs {
     const uint16_t* X;
-    const uint8_t* Wq;
-    const uint16_t* scales;
+    const uint16_t* scales;   // used by the plain-load qparam path only
     const uint16_t* offsets;
     uint16_t* Y;
     int M, N, K;
     int ks;      // k per slice (multiple of 256)
     int kc;      // k per staged X sub-chunk (multiple of 256, divides ks)
     int splits;  // K slices = cluster size along grid.y
-    int qtma;    // 1: qparam rows are 16-byte aligned and copied by TMA; 0: plain loads
+    int qtma;    // 1: qparams arrive by TMA with the first chunk; 0: plain loads
 };
 
+constexpr int SK_CHUNK = 256;                    // k per TMA chunk: 64 rows x 128 bytes of codes
+constexpr int SK_CHUNK_BYTES = SKINNY_ROWS * 128;
+constexpr int SK_MAX_CHUNKS = 8;                 // slices up to 2048 k
+
 // Byte offsets inside the dynamic shared memory of one block (host and device
-// compute the same layout).
+// compute the same layout).  The code chunks come first, 1024-byte aligned
+// for the 128-byte TMA swizzle.
 struct SkLayout {
-    int wpitch, qpitch, xpitch;
+    int qpitch, xpitch;
     int off_s, off_o, off_x, off_z, off_part, off_bar, total;
 };
 __host__ __device__ inline SkLayout sk_layout(int M, int ks, int kc, int g, int splits) {
     SkLayout L;
-    L.wpitch = ks / 2 + 64;  // = 64 (mod 128): the two rows of a quarter-warp use other banks
-    L.qpitch = ((2 * (ks / g) + 15) / 16) * 16 + 16;
+    L.qpitch = 2 * (ks / g);  // bytes per row of staged scales (or offsets); TMA writes rows back to back
     L.xpitch = kc * 2 + 16;
-    int off = SKINNY_ROWS * L.wpitch;
-    L.off_s = off;
+    int off = (ks / SK_CHUNK) * SK_CHUNK_BYTES;
+    L.off_s = off;  // TMA destinations: 128-byte aligned
     off += SKINNY_ROWS * L.qpitch;
+    off = (off + 127) & ~127;
     L.off_o = off;
     off += SKINNY_ROWS * L.qpitch;
+    off = (off + 127) & ~127;
     L.off_x = off;
     off += M * L.xpitch;
     L.off_z = off;
@@ -105,7 +114,7 @@ __host__ __device__ inline SkLayout sk_layout(int M, int ks, int kc, int g, int 
     L.off_part = off;
     off += splits > 1 ? M * SKINNY_ROWS * 4 : 0;
     L.off_bar = off;
-    off += 16;
+    off += 8 * SK_MAX_CHUNKS + 16;
     L.total = off;
     return L;
 }
@@ -115,8 +124,10 @@ constexpr uint64_t SK_WAIT_LIMIT_NS = 2000000000ull;
 
 template <int MT, int G>
 __global__ void __launch_bounds__(SK_THREADS)
-skinny_kernel(const SkinnyArgs p) {
-    extern __shared__ __align__(128) unsigned char smem[];
+skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
+              const __grid_constant__ CUtensorMap tm_o, const SkinnyArgs p) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const SkLayout L = sk_layout(p.M, p.ks, p.kc, G, p.splits);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -125,63 +136,53 @@ skinny_kernel(const SkinnyArgs p) {
     const int k0 = slice * p.ks;
     const int klen = min(p.K - k0, p.ks);  // multiple of 32
     const int nsteps = (klen + SK_KSTEP - 1) / SK_KSTEP;
+    const int nchunks = (klen + SK_CHUNK - 1) / SK_CHUNK;
     const int row0 = tile * SKINNY_ROWS;
-    const int nrows = min(SKINNY_ROWS, p.N - row0);
-    const int ng = p.K / G;
     const int nqs = klen / G;  // groups of this slice (>= 1)
 
-    unsigned char* wsm = smem;                                           // [64][wpitch] codes
-    uint16_t* ssm = reinterpret_cast<uint16_t*>(smem + L.off_s);         // [64][qpitch/2] scales
-    uint16_t* osm = reinterpret_cast<uint16_t*>(smem + L.off_o);         // [64][qpitch/2] offsets
-    unsigned char* xs = smem + L.off_x;                                  // [M][xpitch] staged X
-    unsigned char* zrow = smem + L.off_z;                                // [xpitch] zeros
-    float* part = reinterpret_cast<float*>(smem + L.off_part);           // [M][64] partial sums
-    const uint32_t bar = smem_u32(smem + L.off_bar);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.off_bar + 8);
+    uint16_t* ssm = reinterpret_cast<uint16_t*>(smem + L.off_s);  // [64][ks/G] scales
+    uint16_t* osm = reinterpret_cast<uint16_t*>(smem + L.off_o);  // [64][ks/G] offsets
+    unsigned char* xs = smem + L.off_x;                            // [M][xpitch] staged X
+    unsigned char* zrow = smem + L.off_z;                          // [xpitch] zeros
+    float* part = reinterpret_cast<float*>(smem + L.off_part);     // [M][64] partial sums
+    const uint32_t bar0 = smem_u32(smem + L.off_bar);               // one mbarrier per chunk
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.off_bar + 8 * SK_MAX_CHUNKS);
 
     griddep_launch_dependents();
 
-    // ---- the block's whole weight slice, in flight at once (before waiting on the previous kernel)
+    // ---- every chunk of the slice in flight at once, before waiting on the previous kernel
     if (threadIdx.x == 0) {
-        mbar_init(bar, 1);
+        for (int c = 0; c < nchunks; ++c) mbar_init(bar0 + 8 * c, 1);
         *abort_flag = 0;
         mbar_fence_init();
-    }
-    __syncthreads();
-    const uint32_t wbytes = (uint32_t)klen / 2;
-    const uint32_t qbytes = p.qtma ? (uint32_t)(2 * nqs) : 0u;
-    if (threadIdx.x == 0) mbar_arrive_expect_tx(bar, (uint32_t)nrows * (wbytes + 2u * qbytes));
-    __syncthreads();
-    if ((int)threadIdx.x < nrows) {
-        const int64_t n = row0 + threadIdx.x;
-        bulk_load(smem_u32(wsm + threadIdx.x * L.wpitch), p.Wq + n * (p.K / 2) + k0 / 2, wbytes, bar);
-        if (p.qtma) {
-            bulk_load(smem_u32(ssm) + threadIdx.x * L.qpitch, p.scales + n * ng + k0 / G, qbytes, bar);
-            bulk_load(smem_u32(osm) + threadIdx.x * L.qpitch, p.offsets + n * ng + k0 / G, qbytes, bar);
+        tma_prefetch_desc(&tm_w);
+        const uint32_t qbytes = p.qtma ? (uint32_t)(2 * SKINNY_ROWS * L.qpitch) : 0u;
+        for (int c = 0; c < nchunks; ++c) {
+            const uint32_t bar = bar0 + 8 * c;
+            mbar_arrive_expect_tx(bar, SK_CHUNK_BYTES + (c == 0 ? qbytes : 0u));
+            tma_load_2d(smem_u32(smem) + c * SK_CHUNK_BYTES, &tm_w, bar, (k0 + c * SK_CHUNK) / 2, row0);
+            if (c == 0 && p.qtma) {
+                tma_load_2d(smem_u32(ssm), &tm_s, bar, k0 / G, row0);
+                tma_load_2d(smem_u32(osm), &tm_o, bar, k0 / G, row0);
+            }
         }
     }
-    if (!p.qtma) {
-        for (int r = 0; r < nrows; ++r)
-            for (int j = threadIdx.x; j < nqs; j += SK_THREADS) {
-                const int64_t idx = (int64_t)(row0 + r) * ng + k0 / G + j;
-                ssm[r * (L.qpitch / 2) + j] = (uint16_t)ldg_nc_u16(p.scales + idx);
-                osm[r * (L.qpitch / 2) + j] = (uint16_t)ldg_nc_u16(p.offsets + idx);
+    if (!p.qtma) {  // qparams by plain loads; zeros for rows past N and groups past the slice
+        const int nrows = min(SKINNY_ROWS, p.N - row0);
+        const int qcols = L.qpitch / 2;
+        const int ng = p.K / G;
+        for (int r = 0; r < SKINNY_ROWS; ++r)
+            for (int j = threadIdx.x; j < qcols; j += SK_THREADS) {
+                uint16_t sv = 0, ov = 0;
+                if (r < nrows && j < nqs) {
+                    const int64_t idx = (int64_t)(row0 + r) * ng + k0 / G + j;
+                    sv = (uint16_t)ldg_nc_u16(p.scales + idx);
+                    ov = (uint16_t)ldg_nc_u16(p.offsets + idx);
+                }
+                ssm[r * qcols + j] = sv;
+                osm[r * qcols + j] = ov;
             }
     }
-    // codes and qparams past the slice end inside the last step read as zeros
-    // (w' = 0*0 + 0: never-written shared memory could hold NaN patterns)
-    const int tail16 = (nsteps * 64 - (int)wbytes) / 16;
-    if (tail16 > 0)
-        for (int r = 0; r < nrows; ++r)
-            for (int c = threadIdx.x; c < tail16; c += SK_THREADS)
-                *reinterpret_cast<uint4*>(wsm + r * L.wpitch + wbytes + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
-    const int qsteps = nsteps * SK_KSTEP / G;  // groups the last step touches (> nqs only when !qtma)
-    if (qsteps > nqs)
-        for (int r = 0; r < nrows; ++r)
-            for (int j = nqs + threadIdx.x; j < qsteps; j += SK_THREADS) {
-                ssm[r * (L.qpitch / 2) + j] = 0;
-                osm[r * (L.qpitch / 2) + j] = 0;
-            }
 
     // ---- activations may come from the previous kernel: wait for it, then stage X
     griddep_wait();
@@ -209,10 +210,6 @@ skinny_kernel(const SkinnyArgs p) {
     stage(0);
     __syncthreads();
 
-    // ---- weights landed? (bounded; a block that gives up computes garbage but still
-    // meets every barrier of its cluster, and drains its copies before leaving)
-    const bool ok = mbar_wait_bounded(bar, 0, abort_flag, &g_skinny_fault, 1u, SK_WAIT_LIMIT_NS);
-
     uint32_t bbase[MT];
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
@@ -223,13 +220,19 @@ skinny_kernel(const SkinnyArgs p) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) boff[j] = 16u * (uint32_t)((4 * tq + j) ^ ((tq >> 1) << 1));
 
-    const int ra = warp * 16 + gid;  // local rows ra and ra + 8
-    const uint32_t wa_addr0 = smem_u32(wsm) + ra * L.wpitch + 16 * tq;
-    const uint32_t wb_addr0 = wa_addr0 + 8 * L.wpitch;
-    const uint16_t* sa_p = ssm + ra * (L.qpitch / 2);
-    const uint16_t* oa_p = osm + ra * (L.qpitch / 2);
-    const uint16_t* sb_p = sa_p + 8 * (L.qpitch / 2);
-    const uint16_t* ob_p = oa_p + 8 * (L.qpitch / 2);
+    // A-row gid of the warp's MMA tile is weight row pi(gid) = {0,4,1,5,2,6,3,7}[gid] (+8 for gid+8):
+    // the two rows a quarter-warp reads then differ in bit 2, which the 128-byte swizzle turns into
+    // different bank halves.
+    const int pr = ((gid >> 1) | ((gid & 1) << 2));
+    const int ra = warp * 16 + pr;  // local rows ra and ra + 8
+    const uint32_t wsm = smem_u32(smem);
+    const uint32_t wa_row = wsm + ra * 128, wb_row = wa_row + 8 * 128;
+    const uint32_t swz = (uint32_t)(ra & 7);  // rows ra and ra + 8 share it
+    const int qcols = L.qpitch / 2;
+    const uint16_t* sa_p = ssm + ra * qcols;
+    const uint16_t* oa_p = osm + ra * qcols;
+    const uint16_t* sb_p = sa_p + 8 * qcols;
+    const uint16_t* ob_p = oa_p + 8 * qcols;
 
     float acc[MT][4];
 #pragma unroll
@@ -237,9 +240,10 @@ skinny_kernel(const SkinnyArgs p) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[t][i] = 0.0f;
 
+    bool ok = true;
     const int steps_per_chunk = p.kc / SK_KSTEP;
-    int sc = 0;        // step inside the staged X sub-chunk
-    uint32_t xo = 0;   // its byte offset in a staged row
+    int sc = 0;       // step inside the staged X sub-chunk
+    uint32_t xo = 0;  // its byte offset in a staged row
 #pragma unroll 2
     for (int s = 0; s < nsteps; ++s) {
         if (sc == steps_per_chunk) {  // next X sub-chunk (block-uniform)
@@ -249,8 +253,12 @@ skinny_kernel(const SkinnyArgs p) {
             sc = 0;
             xo = 0;
         }
-        const uint4 wa = lds128(wa_addr0 + 64u * s);
-        const uint4 wb = lds128(wb_addr0 + 64u * s);
+        if ((s & 1) == 0)  // first step of a TMA chunk: wait for it (bounded)
+            ok = mbar_wait_bounded(bar0 + 8 * (s >> 1), 0, abort_flag, &g_skinny_fault, 1u, SK_WAIT_LIMIT_NS) && ok;
+        const uint32_t cbase = (uint32_t)(s >> 1) * SK_CHUNK_BYTES;
+        const uint32_t cpos = (((uint32_t)(4 * (s & 1) + tq)) ^ swz) << 4;
+        const uint4 wa = lds128(wa_row + cbase + cpos);
+        const uint4 wb = lds128(wb_row + cbase + cpos);
         const int jg = (s * SK_KSTEP + 32 * tq) / G;
         const uint32_t sa2 = __byte_perm(sa_p[jg], 0, 0x1010), oa2 = __byte_perm(oa_p[jg], 0, 0x1010);
         const uint32_t sb2 = __byte_perm(sb_p[jg], 0, 0x1010), ob2 = __byte_perm(ob_p[jg], 0, 0x1010);
@@ -314,15 +322,15 @@ skinny_kernel(const SkinnyArgs p) {
         }
         cluster.sync();  // no block leaves while its partials may still be read
     }
-    if (!ok) mbar_drain_bounded(bar, 0, SK_WAIT_LIMIT_NS);  // never leave with copies landing in smem
+    if (!ok)  // never leave with copies still landing in shared memory
+        for (int c = 0; c < nchunks; ++c) mbar_drain_bounded(bar0 + 8 * c, 0, SK_WAIT_LIMIT_NS);
 }
 
 // ------------------------------------------------------------------ host side
 
-static constexpr int SK_TARGET_BLOCKS = 148 * 4;  // ~4 resident blocks (~50 KB of shared memory each) per SM
+static constexpr int SK_TARGET_BLOCKS = 148 * 4;  // ~4-5 resident blocks (~45 KB of shared memory each) per SM
 static constexpr int SK_MAX_SPLIT = 16;           // cluster size (above 8 needs the non-portable opt-in)
-static constexpr int SK_QUANT = 256;              // slices and sub-chunks are whole 256-k units
-static constexpr int SK_MAX_KS = 2048;            // longest slice: 64 rows x 1 KB of codes
+static constexpr int SK_MAX_KS = SK_CHUNK * SK_MAX_CHUNKS;
 static constexpr int SK_XCAP = 16 * 1024;         // staged X budget
 static constexpr int SK_SMEM_MAX = 200 * 1024;
 
@@ -330,34 +338,35 @@ bool plan_skinny(int64_t M, int64_t N, int64_t K, int g, SkinnyPlan* plan) {
     if (M < 1 || M > SKINNY_MAX_M) return false;
     const int64_t tiles = (N + SKINNY_ROWS - 1) / SKINNY_ROWS;
     if (tiles > 0x7FFFFFFF) return false;
-    const int64_t kq = (K + SK_QUANT - 1) / SK_QUANT;
+    const int64_t kq = (K + SK_CHUNK - 1) / SK_CHUNK;
     int64_t splits = std::min<int64_t>(SK_MAX_SPLIT, std::max<int64_t>(1, (K + 1023) / 1024));
     // few row tiles: more, shorter slices (down to 512 k) so the launch fills the GPU
     while (splits < SK_MAX_SPLIT && tiles * splits < SK_TARGET_BLOCKS && (kq + splits) / (splits + 1) >= 2) ++splits;
-    int64_t ks = (kq + splits - 1) / splits * SK_QUANT;
+    int64_t ks = (kq + splits - 1) / splits * SK_CHUNK;
     if (ks > SK_MAX_KS) return false;  // K too long for 16 slices: the tensor-core path takes it
     splits = (K + ks - 1) / ks;
-    int64_t kc = ks;  // largest sub-chunk (whole units, dividing ks) whose staged X fits
-    while (kc > SK_QUANT && (M + 1) * (2 * kc + 16) > SK_XCAP) {
-        int64_t q = kc / SK_QUANT - 1;
-        while (q > 1 && (ks / SK_QUANT) % q != 0) --q;
-        kc = q * SK_QUANT;
+    int64_t kc = ks;  // largest sub-chunk (whole 256-k units, dividing ks) whose staged X fits
+    while (kc > SK_CHUNK && (M + 1) * (2 * kc + 16) > SK_XCAP) {
+        int64_t q = kc / SK_CHUNK - 1;
+        while (q > 1 && (ks / SK_CHUNK) % q != 0) --q;
+        kc = q * SK_CHUNK;
     }
     const SkLayout L = sk_layout((int)M, (int)ks, (int)kc, g, (int)splits);
-    if (L.total > SK_SMEM_MAX) return false;
+    if (L.total + 1024 > SK_SMEM_MAX) return false;
     const int64_t ng = K / g;
-    const int64_t last = K - (splits - 1) * ks;
     plan->tiles = (int)tiles;
     plan->splits = (int)splits;
     plan->ks = (int)ks;
     plan->kc = (int)kc;
-    plan->smem = (size_t)L.total;
-    plan->qtma = (ng % 8 == 0) && ((ks / g) % 8 == 0) && ((last / g) % 8 == 0);
+    plan->smem = (size_t)L.total + 1024;  // + slack to align the swizzled chunks to 1024 bytes
+    // qparams by TMA: row pitch and every slice start 16-byte aligned
+    plan->qtma = (ng % 8 == 0) && ((ks / g) % 8 == 0);
     return true;
 }
 
 template <int MT, int G>
-static cudaError_t launch_one(const SkinnyPlan& plan, const SkinnyArgs& a, cudaStream_t stream) {
+static cudaError_t launch_one(const SkinnyPlan& plan, const CUtensorMap& tw, const CUtensorMap& ts,
+                              const CUtensorMap& to, const SkinnyArgs& a, cudaStream_t stream) {
     auto kern = skinny_kernel<MT, G>;
     cudaError_t e = ensure_kernel_attrs(reinterpret_cast<const void*>(kern), SK_SMEM_MAX, true);
     if (e != cudaSuccess) return e;
@@ -375,25 +384,41 @@ static cudaError_t launch_one(const SkinnyPlan& plan, const SkinnyArgs& a, cudaS
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    return cudaLaunchKernelEx(&cfg, kern, tw, ts, to, a);
 }
 
 template <int G>
-static cudaError_t launch_g(const SkinnyPlan& plan, const SkinnyArgs& a, cudaStream_t stream) {
+static cudaError_t launch_g(const SkinnyPlan& plan, const CUtensorMap& tw, const CUtensorMap& ts,
+                            const CUtensorMap& to, const SkinnyArgs& a, cudaStream_t stream) {
     switch ((a.M + 7) / 8) {
-        case 1: return launch_one<1, G>(plan, a, stream);
-        case 2: return launch_one<2, G>(plan, a, stream);
-        case 3: return launch_one<3, G>(plan, a, stream);
-        default: return launch_one<4, G>(plan, a, stream);
+        case 1: return launch_one<1, G>(plan, tw, ts, to, a, stream);
+        case 2: return launch_one<2, G>(plan, tw, ts, to, a, stream);
+        case 3: return launch_one<3, G>(plan, tw, ts, to, a, stream);
+        default: return launch_one<4, G>(plan, tw, ts, to, a, stream);
     }
 }
 
 cudaError_t launch_skinny(const SkinnyPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
                           const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, const char** detail) {
+    // codes: [N][K/2] bytes, one box = 64 rows x 128 bytes (256 k), 128-byte swizzle
+    CUtensorMap tw, ts, to;
+    cudaError_t e = encode_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)(K / 2), (uint64_t)N,
+                                         (uint64_t)(K / 2), 128, SKINNY_ROWS, CU_TENSOR_MAP_SWIZZLE_128B, detail);
+    if (e != cudaSuccess) return e;
+    ts = tw;
+    to = tw;  // placeholders when the qparams go by plain loads
+    if (plan.qtma) {
+        const uint64_t ng = (uint64_t)(K / g);
+        e = encode_tensor_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, ng, (uint64_t)N, ng * 2,
+                                 (uint32_t)(plan.ks / g), SKINNY_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE, detail);
+        if (e == cudaSuccess)
+            e = encode_tensor_map_2d(&to, CU_TENSOR_MAP_DATA_TYPE_UINT16, offsets, ng, (uint64_t)N, ng * 2,
+                                     (uint32_t)(plan.ks / g), SKINNY_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE, detail);
+        if (e != cudaSuccess) return e;
+    }
     SkinnyArgs a;
     a.X = X;
-    a.Wq = Wq;
     a.scales = scales;
     a.offsets = offsets;
     a.Y = Y;
@@ -405,9 +430,9 @@ cudaError_t launch_skinny(const SkinnyPlan& plan, const uint16_t* X, int64_t M, 
     a.splits = plan.splits;
     a.qtma = plan.qtma ? 1 : 0;
     switch (g) {
-        case 32: return launch_g<32>(plan, a, stream);
-        case 64: return launch_g<64>(plan, a, stream);
-        default: return launch_g<128>(plan, a, stream);
+        case 32: return launch_g<32>(plan, tw, ts, to, a, stream);
+        case 64: return launch_g<64>(plan, tw, ts, to, a, stream);
+        default: return launch_g<128>(plan, tw, ts, to, a, stream);
     }
 }
 
