@@ -198,13 +198,15 @@ class LinearStack:
             self.xv[-1].copy_(wl.gen_activation(c.M, c.K, c.x_seed, device=device))
             xo += c.M * c.K
             yo += c.M * c.N
+        need = max(w4.w4_linear_workspace_bytes(c.M, c.N, c.K, c.group_size) for c in cases)
+        self.ws = w4.Workspace(device, need)
         self.bytes = sum(linear_bytes(c.M, c.N, c.K, c.group_size) for c in cases)
         self.flops = sum(2 * c.M * c.N * c.K for c in cases)
         self.w4 = w4
 
     def run(self):
         for c, x, y, (Wq, sc, of) in zip(self.cases, self.xv, self.yv, self.packed):
-            self.w4.w4_linear(x, Wq, sc, of, c.group_size, out=y)
+            self.w4.w4_linear(x, Wq, sc, of, c.group_size, out=y, workspace=self.ws)
 
     def capture(self, stream):
         import torch
@@ -385,12 +387,13 @@ def other_rows(args, w4, wl, device, stream, peaks, dist):
         reps = [(Wq.clone(), sc.clone(), of.clone()) for _ in range(copies)]
         X = wl.gen_activation(c.M, c.K, c.x_seed, device=device)
         Y = torch.empty((c.M, c.N), dtype=torch.bfloat16, device=device)
+        ws = w4.Workspace(device).reserve_for(c.M, c.N, c.K, c.group_size)
         it = {"i": 0}
 
         def one():
             r = reps[it["i"] % copies]
             it["i"] += 1
-            w4.w4_linear(X, *r, c.group_size, out=Y)
+            w4.w4_linear(X, *r, c.group_size, out=Y, workspace=ws)
 
         with torch.cuda.stream(stream):
             g = torch.cuda.CUDAGraph()

@@ -16,13 +16,14 @@ import threading
 import torch
 
 __all__ = [
-    "W4Error", "W4_FORMAT_VERSION", "KERNEL_AUTO", "KERNEL_SKINNY", "KERNEL_GEMM",
+    "W4Error", "W4_FORMAT_VERSION", "KERNEL_AUTO", "KERNEL_SKINNY", "KERNEL_GEMM", "KERNEL_SKINNY_CLUSTER",
+    "KERNEL_STREAM", "Workspace", "w4_linear_workspace_bytes",
     "library_path", "load_library", "w4_quantize", "w4_dequantize", "w4_linear",
     "w4_linear_ex", "w4_packed_bytes", "w4_qparam_bytes", "w4_device_fault", "w4_format_version",
 ]
 
 W4_FORMAT_VERSION = 1
-KERNEL_AUTO, KERNEL_SKINNY, KERNEL_GEMM = 0, 1, 2
+KERNEL_AUTO, KERNEL_SKINNY, KERNEL_GEMM, KERNEL_SKINNY_CLUSTER, KERNEL_STREAM = 0, 1, 2, 3, 4
 _STATUS = {0: "W4_OK", 1: "W4_ERR_INVALID_ARG", 2: "W4_ERR_UNSUPPORTED", 3: "W4_ERR_MISALIGNED",
            4: "W4_ERR_CUDA", 5: "W4_ERR_TIMEOUT"}
 
@@ -56,8 +57,9 @@ def load_library():
         sigs = {
             "w4_quantize": ([p, i64, i64, i32, p, p, p, p], i32),
             "w4_dequantize": ([p, p, p, i64, i64, i32, p, p], i32),
-            "w4_linear": ([p, i64, i64, p, p, p, i64, i32, p, p], i32),
-            "w4_linear_ex": ([p, i64, i64, p, p, p, i64, i32, p, i32, p], i32),
+            "w4_linear_workspace_bytes": ([i64, i64, i64, i32], sz),
+            "w4_linear": ([p, i64, i64, p, p, p, i64, i32, p, p, sz, p], i32),
+            "w4_linear_ex": ([p, i64, i64, p, p, p, i64, i32, p, p, sz, i32, p], i32),
             "w4_packed_bytes": ([i64, i64], sz),
             "w4_qparam_bytes": ([i64, i64, i32], sz),
             "w4_device_fault": ([p], i32),
@@ -138,22 +140,67 @@ def w4_dequantize(Wq: torch.Tensor, scales: torch.Tensor, offsets: torch.Tensor,
     return W
 
 
+def w4_linear_workspace_bytes(M: int, N: int, K: int, group_size: int) -> int:
+    return load_library().w4_linear_workspace_bytes(M, N, K, group_size)
+
+
+class Workspace:
+    """Zero-filled device workspace for w4_linear (the stream kernel's fp32 partial
+    sums and tile counters).  Every call leaves it zeroed, so it can be reused by
+    calls of any shape in sequence; calls that can overlap on the GPU need one
+    each.  Growing it allocates (through torch): size it before capturing a CUDA
+    graph or timing."""
+
+    def __init__(self, device=None, nbytes: int = 0):
+        self.device = torch.device(device or "cuda")
+        self.buf = None
+        if nbytes:
+            self.reserve(nbytes)
+
+    def reserve(self, nbytes: int):
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=self.device)
+        return self
+
+    def reserve_for(self, M: int, N: int, K: int, group_size: int):
+        return self.reserve(w4_linear_workspace_bytes(M, N, K, group_size))
+
+    @property
+    def nbytes(self) -> int:
+        return 0 if self.buf is None else self.buf.numel()
+
+
+_default_ws = {}
+
+
+def _workspace_for(X: torch.Tensor, M, N, K, g, workspace):
+    """The caller's workspace as given, or this stream's default one grown to fit."""
+    if workspace is not None:
+        return workspace
+    key = (X.device.index, torch.cuda.current_stream(X.device).cuda_stream)
+    ws = _default_ws.get(key)
+    if ws is None:
+        ws = _default_ws[key] = Workspace(X.device)
+    return ws.reserve_for(M, N, K, g)
+
+
 def w4_linear_ex(X: torch.Tensor, Wq: torch.Tensor, scales: torch.Tensor, offsets: torch.Tensor,
-                 group_size: int, kernel: int = KERNEL_AUTO, out=None):
+                 group_size: int, kernel: int = KERNEL_AUTO, out=None, workspace: Workspace | None = None):
     """Y bf16 [M,N] = X bf16 [M,K] . dequant(Wq)^T with fp32 accumulation."""
     lib = load_library()
     _bits16(X, "X")
     M, K = X.shape
     N = Wq.shape[0]
     Y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    ws = _workspace_for(X, M, N, K, group_size, workspace)
     _check(lib.w4_linear_ex(_ptr(X), M, K, _ptr(Wq), _ptr(scales), _ptr(offsets), N, group_size, _ptr(Y),
-                            kernel, _stream(X)), "w4_linear")
+                            _ptr(ws.buf), ws.nbytes, kernel, _stream(X)), "w4_linear")
     return Y
 
 
-def w4_linear(X, Wq, scales, offsets, group_size, out=None):
-    """Y bf16 [M,N] = X . dequant(Wq)^T; skinny kernel for M <= 32, tensor-core GEMM above."""
-    return w4_linear_ex(X, Wq, scales, offsets, group_size, KERNEL_AUTO, out)
+def w4_linear(X, Wq, scales, offsets, group_size, out=None, workspace=None):
+    """Y bf16 [M,N] = X . dequant(Wq)^T (kernel chosen by M; see include/w4.h)."""
+    return w4_linear_ex(X, Wq, scales, offsets, group_size, KERNEL_AUTO, out, workspace)
 
 
 def w4_device_fault(device=None) -> None:

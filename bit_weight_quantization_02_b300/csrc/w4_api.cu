@@ -78,42 +78,72 @@ w4_status w4_dequantize(const uint8_t* Wq, const uint16_t* scales, const uint16_
     return e == cudaSuccess ? W4_OK : cuda_fail(e, "dequantize launch");
 }
 
+size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int group_size) {
+    if (check_shape(N, K, group_size) != W4_OK || M < 1 || N == 0) return 0;
+    w4::StreamPlan plan;
+    if (!w4::plan_stream(M, N, K, group_size, &plan)) return 0;
+    return plan.ws_bytes;
+}
+
 w4_status w4_linear_ex(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
-                       const uint16_t* offsets, int64_t N, int group_size, uint16_t* Y, w4_kernel kernel,
-                       void* stream) {
+                       const uint16_t* offsets, int64_t N, int group_size, uint16_t* Y, void* workspace,
+                       size_t workspace_bytes, w4_kernel kernel, void* stream) {
     W4_TRY(check_shape(N, K, group_size));
     if (M < 0) return fail(W4_ERR_INVALID_ARG, "M = %lld must not be negative", (long long)M);
     if (M > 0x7FFFFFFFLL) return fail(W4_ERR_INVALID_ARG, "M must be below 2^31");
-    if (kernel != W4_KERNEL_AUTO && kernel != W4_KERNEL_SKINNY && kernel != W4_KERNEL_GEMM)
+    if (kernel < W4_KERNEL_AUTO || kernel > W4_KERNEL_STREAM)
         return fail(W4_ERR_INVALID_ARG, "unknown kernel choice %d", (int)kernel);
-    if (kernel == W4_KERNEL_SKINNY && M > w4::SKINNY_MAX_M)
-        return fail(W4_ERR_INVALID_ARG, "the skinny kernel takes M <= %d, got %lld", w4::SKINNY_MAX_M, (long long)M);
+    if ((kernel == W4_KERNEL_SKINNY || kernel == W4_KERNEL_SKINNY_CLUSTER) && M > w4::SKINNY_MAX_M)
+        return fail(W4_ERR_INVALID_ARG, "the skinny kernels take M <= %d, got %lld", w4::SKINNY_MAX_M, (long long)M);
+    if (kernel == W4_KERNEL_STREAM && M > w4::STREAM_MAX_M)
+        return fail(W4_ERR_INVALID_ARG, "the stream kernel takes M <= %d, got %lld", w4::STREAM_MAX_M, (long long)M);
     if (M == 0 || N == 0) return W4_OK;
     W4_TRY(check_ptr(X, "X"));
     W4_TRY(check_ptr(Wq, "Wq"));
     W4_TRY(check_ptr(scales, "scales"));
     W4_TRY(check_ptr(offsets, "offsets"));
     W4_TRY(check_ptr(Y, "Y"));
+    if (workspace == nullptr) workspace_bytes = 0;
+    if (workspace_bytes > 0 && !aligned16(workspace)) return fail(W4_ERR_MISALIGNED, "workspace is not 16-byte aligned");
 
-    const bool use_skinny = (kernel == W4_KERNEL_SKINNY) || (kernel == W4_KERNEL_AUTO && M <= w4::SKINNY_MAX_M);
-    cudaError_t e;
-    if (use_skinny) {
-        w4::SkinnyPlan plan;
-        if (!w4::plan_skinny(M, N, K, group_size, &plan)) return fail(W4_ERR_INVALID_ARG, "no skinny launch plan");
-        const char* detail = "";
-        e = w4::launch_skinny(plan, X, M, K, Wq, scales, offsets, N, group_size, Y, (cudaStream_t)stream, &detail);
-        if (e != cudaSuccess) return fail(W4_ERR_CUDA, "skinny linear: %s %s", cudaGetErrorString(e), detail);
-        return W4_OK;
-    }
     const char* detail = "";
+    cudaError_t e;
+    // stream kernel: M <= 8 with a large enough workspace
+    if (kernel == W4_KERNEL_AUTO || kernel == W4_KERNEL_SKINNY || kernel == W4_KERNEL_STREAM) {
+        w4::StreamPlan sp;
+        const bool can = M <= w4::STREAM_MAX_M && w4::plan_stream(M, N, K, group_size, &sp) &&
+                         workspace_bytes >= sp.ws_bytes;
+        if (kernel == W4_KERNEL_STREAM && !can)
+            return fail(W4_ERR_INVALID_ARG, "the stream kernel needs an even K/group_size and %zu workspace bytes",
+                        w4_linear_workspace_bytes(M, N, K, group_size));
+        if (can) {
+            e = w4::launch_stream(sp, X, M, K, Wq, scales, offsets, N, group_size, Y, workspace, (cudaStream_t)stream,
+                                  &detail);
+            if (e != cudaSuccess) return fail(W4_ERR_CUDA, "stream linear: %s %s", cudaGetErrorString(e), detail);
+            return W4_OK;
+        }
+    }
+    // cluster-split skinny kernel: M <= 32, no workspace
+    if (kernel == W4_KERNEL_SKINNY_CLUSTER || ((kernel == W4_KERNEL_AUTO || kernel == W4_KERNEL_SKINNY) &&
+                                               M <= w4::SKINNY_MAX_M)) {
+        w4::SkinnyPlan plan;
+        if (w4::plan_skinny(M, N, K, group_size, &plan)) {
+            e = w4::launch_skinny(plan, X, M, K, Wq, scales, offsets, N, group_size, Y, (cudaStream_t)stream, &detail);
+            if (e != cudaSuccess) return fail(W4_ERR_CUDA, "skinny linear: %s %s", cudaGetErrorString(e), detail);
+            return W4_OK;
+        }
+        if (kernel != W4_KERNEL_AUTO) return fail(W4_ERR_INVALID_ARG, "no skinny launch plan for this shape");
+    }
     e = w4::launch_gemm(X, M, K, Wq, scales, offsets, N, group_size, Y, (cudaStream_t)stream, &detail);
     if (e != cudaSuccess) return fail(W4_ERR_CUDA, "tensor-core linear: %s %s", cudaGetErrorString(e), detail);
     return W4_OK;
 }
 
 w4_status w4_linear(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
-                    const uint16_t* offsets, int64_t N, int group_size, uint16_t* Y, void* stream) {
-    return w4_linear_ex(X, M, K, Wq, scales, offsets, N, group_size, Y, W4_KERNEL_AUTO, stream);
+                    const uint16_t* offsets, int64_t N, int group_size, uint16_t* Y, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+    return w4_linear_ex(X, M, K, Wq, scales, offsets, N, group_size, Y, workspace, workspace_bytes, W4_KERNEL_AUTO,
+                        stream);
 }
 
 size_t w4_packed_bytes(int64_t N, int64_t K) {
@@ -129,13 +159,14 @@ size_t w4_qparam_bytes(int64_t N, int64_t K, int group_size) {
 w4_status w4_device_fault(void* stream) {
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "synchronizing the stream");
-    unsigned int gemm = 0, skinny = 0;
+    unsigned int gemm = 0, skinny = 0, strm = 0;
     e = w4::read_and_clear_gemm_fault(&gemm);
     if (e == cudaSuccess) e = w4::read_and_clear_skinny_fault(&skinny);
+    if (e == cudaSuccess) e = w4::read_and_clear_stream_fault(&strm);
     if (e != cudaSuccess) return cuda_fail(e, "reading the device fault words");
-    if (gemm || skinny)
-        return fail(W4_ERR_TIMEOUT, "a block gave up a bounded wait (tensor-core linear 0x%x, skinny linear 0x%x)",
-                    gemm, skinny);
+    if (gemm || skinny || strm)
+        return fail(W4_ERR_TIMEOUT, "a block gave up a bounded wait (tensor-core 0x%x, skinny 0x%x, stream 0x%x)",
+                    gemm, skinny, strm);
     return W4_OK;
 }
 
@@ -158,7 +189,9 @@ int w4_format_version(void) { return W4_FORMAT_VERSION; }
 }  // extern "C"
 
 // ------------------------------------------------------------------ internal
+#include <map>
 #include <mutex>
+#include <tuple>
 #include <unordered_map>
 
 #include <cuda.h>
@@ -200,6 +233,26 @@ cudaError_t encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, co
         *detail = "tensor map rejected by the driver";
         return cudaErrorInvalidValue;
     }
+    return cudaSuccess;
+}
+
+cudaError_t resident_blocks(const void* kernel, int threads, size_t smem, int* sms, int* per_sm) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, const void*, int, size_t>, std::pair<int, int>> cache;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const auto key = std::make_tuple(dev, kernel, threads, smem);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it == cache.end()) {
+        int n = 0, b = 0;
+        if ((e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, threads, smem)) != cudaSuccess) return e;
+        it = cache.emplace(key, std::make_pair(n, b > 0 ? b : 1)).first;
+    }
+    *sms = it->second.first;
+    *per_sm = it->second.second;
     return cudaSuccess;
 }
 

@@ -92,8 +92,9 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // Every wait on a barrier is bounded: after `limit_ns` of wall time (or as
-// soon as another role of the block has given up, *abort != 0) it returns
-// false, having raised *abort and or-ed `code` into the device fault word.
+// soon as another role of the block has given up, *abort != 0; `abort` may be
+// null when no other role shares the wait) it returns false, having raised
+// *abort and or-ed `code` into the device fault word.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
                                                   unsigned int* fault_word, unsigned int code,
                                                   uint64_t limit_ns) {
@@ -102,9 +103,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 15u) == 0u) {
-            if (*abort) return false;
+            if (abort && *abort) return false;
             if (globaltimer_ns() - t0 > limit_ns) {
-                *abort = 1;
+                if (abort) *abort = 1;
                 atomicOr(fault_word, code);
                 return false;
             }

@@ -31,6 +31,27 @@ cudaError_t launch_skinny(const SkinnyPlan& plan, const uint16_t* X, int64_t M, 
                           const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
                           cudaStream_t stream, const char** detail);
 
+// Persistent stream-K decode kernel (M <= 8): needs a zero-initialized,
+// self-cleaning workspace of stream_ws_bytes(M, N) bytes.
+struct StreamPlan {
+    int nkc;          // 256-k units per 16-row tile
+    int64_t tiles;    // 16-row tiles
+    int64_t units;    // tiles * nkc
+    size_t smem;      // dynamic shared memory bytes per block
+    size_t ws_bytes;  // workspace bytes
+};
+constexpr int STREAM_MAX_M = 8;
+size_t stream_ws_bytes(int64_t M, int64_t N);
+bool plan_stream(int64_t M, int64_t N, int64_t K, int g, StreamPlan* plan);
+cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
+                          const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
+                          void* workspace, cudaStream_t stream, const char** detail);
+cudaError_t read_and_clear_stream_fault(unsigned int* fault);
+
+// SM count of the current device and resident blocks per SM for a kernel
+// launch shape (cached per device, kernel and shared-memory size).
+cudaError_t resident_blocks(const void* kernel, int threads, size_t smem, int* sms, int* per_sm);
+
 // tcgen05 tensor-core GEMM (any M).
 cudaError_t launch_gemm(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
                         const uint16_t* offsets, int64_t N, int g, uint16_t* Y, cudaStream_t stream,

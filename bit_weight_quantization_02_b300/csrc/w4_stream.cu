@@ -1,0 +1,381 @@
+// w4_stream.cu -- persistent stream-K bf16 x int4 linear for decode (M <= 8).
+//
+// Y[m,n] = sum_k X[m,k] * w'[n,k], w' = bf16(q*s + o), fp32 accumulation
+// (Optimum Quanto: bf16 x int4 matmul, result accumulated at higher precision,
+// "Pitfalls when quantizing activations").  With one to eight tokens the
+// packed codes are almost all of the traffic, and a launch is a few
+// microseconds of HBM time, so the kernel is organised around keeping every
+// SM streaming for the whole launch:
+//
+//  * Work unit = 16 weight rows x 256 k (2 KB of codes).  The units of the
+//    problem, taken in (row tile, k) order, are cut into equal contiguous
+//    ranges, one per warp of a one-wave persistent grid: every warp streams
+//    the same number of bytes (within one unit), whatever N and K are.
+//  * Each warp owns a ring of six unit slots.  Lane 0 fetches a unit's codes
+//    with one 2-D TMA copy (16 rows x 128 bytes, 128-byte swizzle, zero fill
+//    past N and K); the 32 lanes fetch its scales and offsets with 4-byte
+//    cp.async; all complete on the slot's mbarrier.  The first six units are
+//    requested before the programmatic-dependent-launch wait.
+//  * X (only 256 k x M tokens per unit) is loaded one unit ahead into
+//    registers, permuted to the MMA k order and staged in the warp's shared
+//    memory; tokens beyond M read a zero row.
+//  * Dequantization and products as in the skinny kernel: LOP3 nibble pairs,
+//    exact subtract + one bf16 FMA, mma.m16n8k16 with the weights as the A
+//    operand and the tokens as B (swap AB).
+//  * A warp that covers all of a row tile's k writes bf16 Y directly.  A tile
+//    split between warps is summed in fp32 with red.add in the caller's
+//    workspace; the warp that completes the tile's k count (atomic counter,
+//    no waiting) converts the sum to bf16 and zeroes what it used, so the
+//    workspace is all zeros again after every call.
+#include "w4_device.cuh"
+#include "w4_internal.h"
+
+#include <algorithm>
+#include <cuda.h>
+#include <mutex>
+
+namespace w4 {
+
+constexpr int ST_WARPS = 4;
+constexpr int ST_THREADS = ST_WARPS * 32;
+constexpr int ST_UK = 256;                 // k per unit
+constexpr int ST_DEPTH = 6;                // ring slots per warp
+constexpr int ST_WSLOT = 16 * 128;         // codes of one unit: 16 rows x 128 bytes
+constexpr int ST_XPITCH = ST_UK * 2 + 16;  // one staged token row of a unit (+16 bytes against bank conflicts)
+
+struct StreamArgs {
+    const uint16_t* X;
+    const uint16_t* scales;
+    const uint16_t* offsets;
+    uint16_t* Y;
+    float* ws;             // [M][N] fp32 partial sums, zero between calls
+    unsigned int* count;   // [N/16] k units summed so far per row tile, zero between calls
+    int M, N, K;
+    int nkc;               // units per row tile = ceil(K / 256)
+    long long units;       // row tiles x nkc
+    int workers;           // warps of the grid with work
+};
+
+// per-warp shared memory after the code slots: qparam slots, X slots, zero row, barriers
+__host__ __device__ inline int st_qslot_bytes(int g) { return 2 * 16 * (ST_UK / g) * 2; }
+__host__ __device__ inline int st_rest_bytes(int M, int g) {
+    const int b = ST_DEPTH * st_qslot_bytes(g) + (2 * M + 1) * ST_XPITCH + 8 * ST_DEPTH;
+    return (b + 15) & ~15;
+}
+__host__ __device__ inline int st_smem_bytes(int M, int g) {
+    return ST_WARPS * ST_DEPTH * ST_WSLOT + ST_WARPS * st_rest_bytes(M, g) + 1024;  // + 1024-byte alignment slack
+}
+
+__device__ unsigned int g_stream_fault;
+constexpr uint64_t ST_WAIT_LIMIT_NS = 2000000000ull;
+
+__device__ __forceinline__ void mma_bf16_16816_st(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                  uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint4 lds128_st(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u16_st(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+// (w & mask) | magic with both constants in registers (one LOP3, no constant rematerialization)
+__device__ __forceinline__ uint32_t lop_and_or(uint32_t w, uint32_t mask, uint32_t magic) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(w), "r"(mask), "r"(magic));
+    return r;
+}
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
+}
+__device__ __forceinline__ int st_x_slot(int c) { return c ^ (((c >> 3) & 1) << 1); }
+
+template <int G>
+__global__ void __launch_bounds__(ST_THREADS)
+stream_kernel(const __grid_constant__ CUtensorMap tm_w, const StreamArgs p) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    constexpr int QSLOT = 2 * 16 * (ST_UK / G) * 2;  // scales then offsets, 16 rows x (256/G) groups each
+    constexpr int QROW = (ST_UK / G) * 2;            // bytes of one row of one array
+    constexpr int PIECES = 2 * 16 * (ST_UK / G) / 2;  // 4-byte qparam pieces per unit
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gid = lane >> 2, tq = lane & 3;
+    const int worker = blockIdx.x * ST_WARPS + warp;
+
+    griddep_launch_dependents();
+    if (worker >= p.workers) return;
+    const long long u0 = p.units * worker / p.workers;
+    const long long u1 = p.units * (worker + 1) / p.workers;
+    if (u0 >= u1) return;
+
+    const int rest = st_rest_bytes(p.M, G);
+    const uint32_t wslots = smem_u32(smem) + warp * (ST_DEPTH * ST_WSLOT);
+    unsigned char* rbase = smem + ST_WARPS * ST_DEPTH * ST_WSLOT + warp * rest;
+    const uint32_t qslots = smem_u32(rbase);
+    unsigned char* xslots = rbase + ST_DEPTH * QSLOT;                   // 2 slots x M token rows
+    unsigned char* zrow = xslots + 2 * p.M * ST_XPITCH;                 // zeros for tokens >= M
+    const uint32_t bars = smem_u32(zrow + ST_XPITCH);                    // ST_DEPTH mbarriers
+    const int ng = p.K / G;
+
+    if (lane == 0) {
+        for (int d = 0; d < ST_DEPTH; ++d) mbar_init(bars + 8 * d, 33);  // TMA arrive + 32 cp.async arrivals
+        mbar_fence_init();
+    }
+    for (int c = lane; c < ST_XPITCH / 16; c += 32)
+        *reinterpret_cast<uint4*>(zrow + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
+    __syncwarp();
+
+    // request unit u into ring slot d: codes by TMA, scales/offsets by 4-byte cp.async
+    auto issue = [&](long long u, int d) {
+        const int tile = (int)(u / p.nkc), kc = (int)(u % p.nkc);
+        const int row0 = tile * 16, k = kc * ST_UK;
+        const uint32_t bar = bars + 8 * d;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar, ST_WSLOT);
+            tma_load_2d(wslots + d * ST_WSLOT, &tm_w, bar, k / 2, row0);
+        }
+        for (int i = lane; i < PIECES; i += 32) {
+            const int arr = i / (PIECES / 2), rem = i % (PIECES / 2);
+            const int r = rem / (QROW / 4), pc = rem % (QROW / 4);
+            const int n = min(row0 + r, p.N - 1);            // rows past N: any finite qparams (codes are 0)
+            const int j = min(k / G + 2 * pc, ng - 2);       // groups past K: likewise (X is 0 there)
+            const uint16_t* src = (arr ? p.offsets : p.scales) + (int64_t)n * ng + j;
+            cp_async_4(qslots + d * QSLOT + arr * 16 * QROW + r * QROW + 4 * pc, src);
+        }
+        cp_async_arrive_noinc(bar);
+    };
+
+    const int depth = (u1 - u0 < ST_DEPTH) ? (int)(u1 - u0) : ST_DEPTH;
+    for (int d = 0; d < depth; ++d) issue(u0 + d, d);
+
+    // activations may come from the previous kernel: wait for it
+    griddep_wait();
+
+    // X of a unit: lane c holds 8-k chunk c of every token
+    uint4 xr[8];
+    auto load_x = [&](long long u) {
+        const int k = (int)(u % p.nkc) * ST_UK + 8 * lane;
+#pragma unroll
+        for (int m = 0; m < 8; ++m)
+            if (m < p.M) xr[m] = (k < p.K) ? ldg_cg_v4(p.X + (int64_t)m * p.K + k) : make_uint4(0u, 0u, 0u, 0u);
+    };
+    auto store_x = [&](unsigned char* slot) {
+#pragma unroll
+        for (int m = 0; m < 8; ++m)
+            if (m < p.M) {
+                uint4 o;
+                o.x = __byte_perm(xr[m].x, xr[m].z, 0x5410);  // (x0, x4)
+                o.y = __byte_perm(xr[m].x, xr[m].z, 0x7632);  // (x1, x5)
+                o.z = __byte_perm(xr[m].y, xr[m].w, 0x5410);  // (x2, x6)
+                o.w = __byte_perm(xr[m].y, xr[m].w, 0x7632);  // (x3, x7)
+                *reinterpret_cast<uint4*>(slot + m * ST_XPITCH + 16 * st_x_slot(lane)) = o;
+            }
+    };
+
+    const uint32_t c_mask = 0x000F000Fu, c_magic = 0x43004300u;
+    uint32_t cm, cg;  // constants pinned in registers
+    asm volatile("mov.b32 %0, %1;" : "=r"(cm) : "r"(c_mask));
+    asm volatile("mov.b32 %0, %1;" : "=r"(cg) : "r"(c_magic));
+
+    const int pr = ((gid >> 1) | ((gid & 1) << 2));  // MMA row gid <- tile row pr (bank-conflict-free swizzled reads)
+    const uint32_t swz = (uint32_t)pr;                // rows pr and pr + 8 share (row & 7)
+    uint32_t boff[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) boff[j] = 16u * (uint32_t)((4 * tq + j) ^ ((tq >> 1) << 1));
+
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    int kc_first = (int)(u0 % p.nkc);
+    bool ok = true;
+
+    load_x(u0);
+    for (long long u = u0; u < u1; ++u) {
+        const int it = (int)(u - u0);
+        const int d = it % ST_DEPTH;
+        unsigned char* xs = xslots + (it & 1) * p.M * ST_XPITCH;
+        store_x(xs);
+        if (u + 1 < u1) load_x(u + 1);
+        ok = mbar_wait_bounded(bars + 8 * d, (uint32_t)((it / ST_DEPTH) & 1), nullptr, &g_stream_fault, 1u,
+                               ST_WAIT_LIMIT_NS) && ok;
+        __syncwarp();
+
+        const uint32_t ws_a = wslots + d * ST_WSLOT + pr * 128;
+        const uint32_t ws_b = ws_a + 8 * 128;
+        const uint32_t qa = qslots + d * QSLOT + pr * QROW;      // scales of row pr
+        const uint32_t qb = qa + 8 * QROW;                        // scales of row pr + 8
+        const uint32_t bbase = smem_u32(gid < p.M ? xs + gid * ST_XPITCH : zrow);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // two 128-k steps per unit
+            const uint32_t cpos = ((uint32_t)(4 * h + tq) ^ swz) << 4;
+            const uint4 wa = lds128_st(ws_a + cpos);
+            const uint4 wb = lds128_st(ws_b + cpos);
+            const uint32_t jq = (uint32_t)(((128 * h + 32 * tq) / G) * 2);
+            const uint32_t sa = lds_u16_st(qa + jq), oa = lds_u16_st(qa + 16 * QROW + jq);
+            const uint32_t sb = lds_u16_st(qb + jq), ob = lds_u16_st(qb + 16 * QROW + jq);
+            const uint32_t sa2 = __byte_perm(sa, 0, 0x1010), oa2 = __byte_perm(oa, 0, 0x1010);
+            const uint32_t sb2 = __byte_perm(sb, 0, 0x1010), ob2 = __byte_perm(ob, 0, 0x1010);
+            const uint32_t wa4[4] = {wa.x, wa.y, wa.z, wa.w};
+            const uint32_t wb4[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t a0 = dequant_pair(lop_and_or(wa4[j], cm, cg), sa2, oa2);
+                const uint32_t a1 = dequant_pair(lop_and_or(wa4[j] >> 4, cm, cg), sa2, oa2);
+                const uint32_t a2 = dequant_pair(lop_and_or(wa4[j] >> 8, cm, cg), sa2, oa2);
+                const uint32_t a3 = dequant_pair(lop_and_or(wa4[j] >> 12, cm, cg), sa2, oa2);
+                const uint32_t b0 = dequant_pair(lop_and_or(wb4[j], cm, cg), sb2, ob2);
+                const uint32_t b1 = dequant_pair(lop_and_or(wb4[j] >> 4, cm, cg), sb2, ob2);
+                const uint32_t b2 = dequant_pair(lop_and_or(wb4[j] >> 8, cm, cg), sb2, ob2);
+                const uint32_t b3 = dequant_pair(lop_and_or(wb4[j] >> 12, cm, cg), sb2, ob2);
+                const uint4 xv = lds128_st(bbase + 256u * h + boff[j]);
+                mma_bf16_16816_st(acc, a0, b0, a1, b1, xv.x, xv.y);
+                mma_bf16_16816_st(acc, a2, b2, a3, b3, xv.z, xv.w);
+            }
+        }
+        __syncwarp();
+        if (u + ST_DEPTH < u1) {  // refill the slot (its reads are done: order them before the async writes)
+            fence_proxy_async_smem();
+            issue(u + ST_DEPTH, d);
+        }
+
+        // end of a row tile or of the range: hand the tile's sums on
+        const int tile = (int)(u / p.nkc), kc = (int)(u % p.nkc);
+        if (u + 1 == u1 || kc == p.nkc - 1) {
+            const int n_a = tile * 16 + pr, n_b = n_a + 8;
+            const int m0 = 2 * tq;  // acc = D[row n_a: tokens m0, m0+1 | row n_b: tokens m0, m0+1]
+            if (kc_first == 0 && kc == p.nkc - 1) {  // this warp summed all of the tile's k
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int m = m0 + (i & 1), n = (i < 2) ? n_a : n_b;
+                    if (m < p.M && n < p.N) p.Y[(int64_t)m * p.N + n] = (uint16_t)float_to_bf16_bits(acc[i]);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int m = m0 + (i & 1), n = (i < 2) ? n_a : n_b;
+                    if (m < p.M && n < p.N) atomicAdd(p.ws + (int64_t)m * p.N + n, acc[i]);
+                }
+                __threadfence();
+                __syncwarp();
+                unsigned int last = 0;
+                if (lane == 0) {
+                    const unsigned int mine = (unsigned int)(kc - kc_first + 1);
+                    last = (atomicAdd(p.count + tile, mine) + mine == (unsigned int)p.nkc);
+                }
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    __threadfence();
+                    for (int i = lane; i < 16 * p.M; i += 32) {
+                        const int m = i >> 4, n = tile * 16 + (i & 15);
+                        if (n < p.N) {
+                            float* w = p.ws + (int64_t)m * p.N + n;
+                            p.Y[(int64_t)m * p.N + n] = (uint16_t)float_to_bf16_bits(__ldcg(w));
+                            *w = 0.0f;
+                        }
+                    }
+                    if (lane == 0) p.count[tile] = 0u;
+                }
+            }
+            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+            kc_first = 0;
+        }
+    }
+    if (!ok) {  // never leave with copies still landing in shared memory
+        const int issued = (int)(u1 - u0);
+        for (int it = max(0, issued - ST_DEPTH); it < issued; ++it)
+            mbar_drain_bounded(bars + 8 * (it % ST_DEPTH), (uint32_t)((it / ST_DEPTH) & 1), ST_WAIT_LIMIT_NS);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+bool plan_stream(int64_t M, int64_t N, int64_t K, int g, StreamPlan* plan) {
+    if (M < 1 || M > STREAM_MAX_M) return false;
+    const int64_t ng = K / g;
+    if (ng % 2 != 0 || ng < 2) return false;  // 4-byte qparam pieces need an even group count
+    const int64_t tiles = (N + 15) / 16;
+    if (tiles > 0x3FFFFFFF) return false;
+    plan->nkc = (int)((K + ST_UK - 1) / ST_UK);
+    plan->units = tiles * plan->nkc;
+    plan->tiles = tiles;
+    plan->smem = (size_t)st_smem_bytes((int)M, g);
+    plan->ws_bytes = stream_ws_bytes(M, N);
+    return true;
+}
+
+size_t stream_ws_bytes(int64_t M, int64_t N) {
+    const size_t part = ((size_t)M * N * 4 + 255) / 256 * 256;
+    return part + (size_t)((N + 15) / 16) * 4;
+}
+
+template <int G>
+static cudaError_t launch_stream_g(const StreamPlan& plan, const CUtensorMap& tw, StreamArgs a, cudaStream_t stream) {
+    auto kern = stream_kernel<G>;
+    cudaError_t e = ensure_kernel_attrs(reinterpret_cast<const void*>(kern), st_smem_bytes(STREAM_MAX_M, G), false);
+    if (e != cudaSuccess) return e;
+    // one wave: as many resident warps as the SMs hold, but no more than there are units
+    int sms = 0, per_sm = 0;
+    if ((e = resident_blocks(reinterpret_cast<const void*>(kern), ST_THREADS, plan.smem, &sms, &per_sm)) != cudaSuccess)
+        return e;
+    const long long max_workers = (long long)sms * per_sm * ST_WARPS;
+    a.workers = (int)std::min<long long>(max_workers, plan.units);
+    const int blocks = (a.workers + ST_WARPS - 1) / ST_WARPS;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+    cfg.blockDim = dim3(ST_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = plan.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tw, a);
+}
+
+cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
+                          const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
+                          void* workspace, cudaStream_t stream, const char** detail) {
+    CUtensorMap tw;  // codes: [N][K/2] bytes, one box = 16 rows x 128 bytes (256 k), 128-byte swizzle
+    cudaError_t e = encode_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)(K / 2), (uint64_t)N,
+                                         (uint64_t)(K / 2), 128, 16, CU_TENSOR_MAP_SWIZZLE_128B, detail);
+    if (e != cudaSuccess) return e;
+    StreamArgs a;
+    a.X = X;
+    a.scales = scales;
+    a.offsets = offsets;
+    a.Y = Y;
+    const size_t part = ((size_t)M * N * 4 + 255) / 256 * 256;
+    a.ws = static_cast<float*>(workspace);
+    a.count = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + part);
+    a.M = (int)M;
+    a.N = (int)N;
+    a.K = (int)K;
+    a.nkc = plan.nkc;
+    a.units = plan.units;
+    a.workers = 0;
+    switch (g) {
+        case 32: return launch_stream_g<32>(plan, tw, a, stream);
+        case 64: return launch_stream_g<64>(plan, tw, a, stream);
+        default: return launch_stream_g<128>(plan, tw, a, stream);
+    }
+}
+
+cudaError_t read_and_clear_stream_fault(unsigned int* fault) {
+    cudaError_t e = cudaMemcpyFromSymbol(fault, g_stream_fault, sizeof(unsigned int));
+    if (e != cudaSuccess || !*fault) return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_stream_fault, &zero, sizeof(unsigned int));
+}
+
+}  // namespace w4

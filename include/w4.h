@@ -65,9 +65,11 @@ typedef enum w4_status {
 
 /* Kernel choice for w4_linear_ex. */
 typedef enum w4_kernel {
-    W4_KERNEL_AUTO = 0,    /* skinny kernel for M <= 32, tensor-core GEMM above */
-    W4_KERNEL_SKINNY = 1,  /* memory-bound decode kernel; requires M <= 32 */
-    W4_KERNEL_GEMM = 2     /* tcgen05 tensor-core GEMM; any M >= 1 */
+    W4_KERNEL_AUTO = 0,            /* stream kernel for M <= 8 (with workspace), skinny for M <= 32, GEMM above */
+    W4_KERNEL_SKINNY = 1,          /* best memory-bound kernel for M <= 32 (stream, else cluster) */
+    W4_KERNEL_GEMM = 2,            /* tcgen05 tensor-core GEMM; any M >= 1 */
+    W4_KERNEL_SKINNY_CLUSTER = 3,  /* cluster split-K skinny kernel, M <= 32, no workspace */
+    W4_KERNEL_STREAM = 4           /* persistent stream-K kernel, M <= 8, needs the workspace */
 } w4_kernel;
 
 /*
@@ -104,38 +106,56 @@ W4_API w4_status w4_dequantize(const uint8_t *Wq, const uint16_t *scales,
                         int group_size, uint16_t *W_out, void *stream);
 
 /*
+ * w4_linear_workspace_bytes -- workspace bytes w4_linear needs to run this
+ * problem on the persistent stream-K decode kernel (M <= 8 and K/group_size
+ * even); 0 when that kernel does not apply.  Without it the call still works
+ * (cluster split-K kernel), usually slower for decode.
+ */
+W4_API size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int group_size);
+
+/*
  * w4_linear -- Y[M,N] bf16 = X[M,K] bf16 . dequant(Wq, scales, offsets)^T,
  * products and sums in fp32, one rounding to bf16 at the end, no bias.
  * Source: the mixed bf16 x int4 matmul of Optimum Quanto (feature list and
  * "Pitfalls when quantizing activations": accumulation in fp32).
  *
- * M <= 32 runs the memory-bound skinny kernel, larger M the tcgen05
- * tensor-core GEMM.  The kernels dequantize each weight as bf16(q * s + o)
- * with a single rounding, which can differ from w4_dequantize's double
- * rounding by one bf16 ulp; the summation order is the kernel's own, fixed for
- * a given (M, N, K, group_size), so results are deterministic bit for bit.
- * Accuracy contract against y_ref = sum_k X[m,k] W'[n,k] in fp64
- * (W' = w4_dequantize output):
+ * Kernel choice: M <= 8 with a workspace of w4_linear_workspace_bytes runs
+ * the persistent stream-K decode kernel; otherwise M <= 32 runs the cluster
+ * split-K skinny kernel; larger M the tcgen05 tensor-core GEMM.  The kernels
+ * dequantize each weight as bf16(q * s + o) with a single rounding, which can
+ * differ from w4_dequantize's double rounding by one bf16 ulp; the summation
+ * order is each kernel's own.  Accuracy contract against
+ * y_ref = sum_k X[m,k] W'[n,k] in fp64 (W' = w4_dequantize output):
  *   |y - y_ref| <= 4e-3 |y_ref| + 1e-2 rms(y_ref).
- * The call needs no workspace: partial sums of a split K are combined in the
- * distributed shared memory of a thread-block cluster.
+ * The cluster and GEMM kernels are deterministic bit for bit; the stream
+ * kernel adds the partial sums of a row tile split between warps with fp32
+ * atomics, so its last bits can vary from run to run.
+ *
+ * workspace: caller-owned device memory of `workspace_bytes` bytes (NULL with
+ * 0 is allowed).  It must be zero-filled once before its first use; every
+ * call returns it to all zeros, so one workspace serves calls of any shape in
+ * sequence.  Calls that may run at the same time on the GPU must not share a
+ * workspace.
  * Kernels of consecutive w4_linear calls on one stream may overlap (the next
  * one starts streaming its weights while the previous one finishes); each
- * still reads X only after everything earlier on the stream has completed,
- * so the weights of a call must not be written by the call just before it.
+ * still reads X, and touches Y and the workspace, only after everything
+ * earlier on the stream has completed, so the weights of a call must not be
+ * written by the call just before it.
  * Errors as w4_quantize, plus W4_ERR_INVALID_ARG for M < 0.
  */
 W4_API w4_status w4_linear(const uint16_t *X, int64_t M, int64_t K, const uint8_t *Wq,
                            const uint16_t *scales, const uint16_t *offsets, int64_t N,
-                           int group_size, uint16_t *Y, void *stream);
+                           int group_size, uint16_t *Y, void *workspace,
+                           size_t workspace_bytes, void *stream);
 
 /* w4_linear with an explicit kernel choice (tests and benchmarks use it to
- * run both kernels on the same problem).  W4_KERNEL_SKINNY with M > 32 gives
- * W4_ERR_INVALID_ARG. */
+ * run every kernel on the same problem).  A choice that cannot run the
+ * problem (M too large, workspace too small) gives W4_ERR_INVALID_ARG. */
 W4_API w4_status w4_linear_ex(const uint16_t *X, int64_t M, int64_t K,
                               const uint8_t *Wq, const uint16_t *scales,
                               const uint16_t *offsets, int64_t N, int group_size,
-                              uint16_t *Y, w4_kernel kernel, void *stream);
+                              uint16_t *Y, void *workspace, size_t workspace_bytes,
+                              w4_kernel kernel, void *stream);
 
 /* Sizes of the packed outputs: N*K/2 bytes of codes, N*(K/g)*2 bytes for each
  * of scales and offsets.  0 for invalid arguments. */

@@ -30,7 +30,8 @@ def lib():
 
 def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
-    assert {"w4_quantize", "w4_dequantize", "w4_linear", "w4_linear_ex", "w4_device_fault"} <= set(names)
+    assert {"w4_quantize", "w4_dequantize", "w4_linear", "w4_linear_ex", "w4_linear_workspace_bytes",
+            "w4_device_fault"} <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} declared in w4.h but not exported"
 
@@ -60,6 +61,23 @@ def test_sizes(lib):
     assert lib.w4_packed_bytes(-1, 64) == 0
 
 
+def test_workspace_plan(lib):
+    # the stream kernel (M <= 8, even K/g) needs [M][N] fp32 sums + one counter per 16 rows
+    assert lib.w4_linear_workspace_bytes(1, 1024, 4096, 32) == 4096 + 64 * 4
+    assert lib.w4_linear_workspace_bytes(8, 14336, 4096, 128) >= 8 * 14336 * 4 + 896 * 4
+    assert lib.w4_linear_workspace_bytes(9, 1024, 4096, 32) == 0     # M > 8: cluster kernel, no workspace
+    assert lib.w4_linear_workspace_bytes(1, 100, 96, 32) == 0        # K/g odd
+    assert lib.w4_linear_workspace_bytes(0, 100, 128, 32) == 0
+
+
+def test_linear_kernel_choice_rules(lib):
+    # the stream kernel only takes M <= 8 and needs its workspace; the checks run before any launch
+    assert lib.w4_linear_ex(FAKE, 9, 64, FAKE, FAKE, FAKE, 4, 32, FAKE, None, 0, 4, None) == INVALID
+    assert lib.w4_linear_ex(FAKE, 2, 64, FAKE, FAKE, FAKE, 4, 32, FAKE, None, 0, 4, None) == INVALID
+    assert b"workspace" in lib.w4_last_error_detail()
+    assert lib.w4_linear_ex(FAKE, 33, 64, FAKE, FAKE, FAKE, 4, 32, FAKE, None, 0, 3, None) == INVALID
+
+
 FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced: every call below fails its checks first
 
 
@@ -67,14 +85,14 @@ FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced: every ca
 def test_unsupported_group_sizes(lib, g, expect):
     assert lib.w4_quantize(FAKE, 4, 256, g, FAKE, FAKE, FAKE, None) == expect
     assert lib.w4_dequantize(FAKE, FAKE, FAKE, 4, 256, g, FAKE, None) == expect
-    assert lib.w4_linear(FAKE, 1, 256, FAKE, FAKE, FAKE, 4, g, FAKE, None) == expect
+    assert lib.w4_linear(FAKE, 1, 256, FAKE, FAKE, FAKE, 4, g, FAKE, None, 0, None) == expect
 
 
 @pytest.mark.parametrize("N,K", [(4, 0), (4, -32), (-1, 64), (4, 96 + 16), (1 << 31, 64), (4, 1 << 31)])
 def test_invalid_shapes(lib, N, K):
     assert lib.w4_quantize(FAKE, N, K, 32, FAKE, FAKE, FAKE, None) == INVALID
     assert lib.w4_dequantize(FAKE, FAKE, FAKE, N, K, 32, FAKE, None) == INVALID
-    assert lib.w4_linear(FAKE, 1, K, FAKE, FAKE, FAKE, N, 32, FAKE, None) == INVALID
+    assert lib.w4_linear(FAKE, 1, K, FAKE, FAKE, FAKE, N, 32, FAKE, None, 0, None) == INVALID
     assert lib.w4_last_error_detail()
 
 
@@ -84,9 +102,10 @@ def test_null_and_misaligned_pointers(lib):
     assert lib.w4_quantize(FAKE, 4, 64, 32, FAKE + 8, FAKE, FAKE, None) == MISALIGNED
     assert lib.w4_dequantize(FAKE, None, FAKE, 4, 64, 32, FAKE, None) == INVALID
     assert lib.w4_dequantize(FAKE, FAKE, FAKE, 4, 64, 32, FAKE + 4, None) == MISALIGNED
-    assert lib.w4_linear(FAKE, 2, 64, FAKE, FAKE, None, 4, 32, FAKE, None) == INVALID
-    assert lib.w4_linear(FAKE + 2, 2, 64, FAKE, FAKE, FAKE, 4, 32, FAKE, None) == MISALIGNED
-    assert lib.w4_linear(FAKE, 2, 64, FAKE, FAKE, FAKE, 4, 32, FAKE + 8, None) == MISALIGNED
+    assert lib.w4_linear(FAKE, 2, 64, FAKE, FAKE, None, 4, 32, FAKE, None, 0, None) == INVALID
+    assert lib.w4_linear(FAKE + 2, 2, 64, FAKE, FAKE, FAKE, 4, 32, FAKE, None, 0, None) == MISALIGNED
+    assert lib.w4_linear(FAKE, 2, 64, FAKE, FAKE, FAKE, 4, 32, FAKE + 8, None, 0, None) == MISALIGNED
+    assert lib.w4_linear(FAKE, 2, 64, FAKE, FAKE, FAKE, 4, 32, FAKE, FAKE + 8, 64, None) == MISALIGNED
     assert b"aligned" in lib.w4_last_error_detail()
 
 
@@ -94,15 +113,15 @@ def test_empty_problems_succeed_without_launch(lib):
     # N == 0 or M == 0: nothing to do, no pointer is touched, no CUDA call is made
     assert lib.w4_quantize(None, 0, 64, 32, None, None, None, None) == OK
     assert lib.w4_dequantize(None, None, None, 0, 64, 32, None, None) == OK
-    assert lib.w4_linear(None, 0, 64, None, None, None, 8, 32, None, None) == OK
-    assert lib.w4_linear(None, 3, 64, None, None, None, 0, 32, None, None) == OK
+    assert lib.w4_linear(None, 0, 64, None, None, None, 8, 32, None, None, 0, None) == OK
+    assert lib.w4_linear(None, 3, 64, None, None, None, 0, 32, None, None, 0, None) == OK
 
 
 def test_linear_argument_rules(lib):
-    assert lib.w4_linear(FAKE, -1, 64, FAKE, FAKE, FAKE, 4, 32, FAKE, None) == INVALID
+    assert lib.w4_linear(FAKE, -1, 64, FAKE, FAKE, FAKE, 4, 32, FAKE, None, 0, None) == INVALID
     # the skinny kernel only takes M <= 32
-    assert lib.w4_linear_ex(FAKE, 33, 64, FAKE, FAKE, FAKE, 4, 32, FAKE, 1, None) == INVALID
-    assert lib.w4_linear_ex(FAKE, 1, 64, FAKE, FAKE, FAKE, 4, 32, FAKE, 7, None) == INVALID
+    assert lib.w4_linear_ex(FAKE, 33, 64, FAKE, FAKE, FAKE, 4, 32, FAKE, None, 0, 1, None) == INVALID
+    assert lib.w4_linear_ex(FAKE, 1, 64, FAKE, FAKE, FAKE, 4, 32, FAKE, None, 0, 7, None) == INVALID
 
 
 def test_binding_refuses_cpu_tensors(lib):

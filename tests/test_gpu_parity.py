@@ -61,10 +61,10 @@ def gpu_quantize(W, g):
     return tuple(o.t for o in out)
 
 
-def gpu_linear(X, Wq, sc, of, g, kernel=w4.KERNEL_AUTO):
+def gpu_linear(X, Wq, sc, of, g, kernel=w4.KERNEL_AUTO, workspace=None):
     M, N = X.shape[0], Wq.shape[0]
     Y = Guarded((M, N), torch.bfloat16)
-    w4.w4_linear_ex(X, Wq, sc, of, g, kernel, out=Y.t)
+    w4.w4_linear_ex(X, Wq, sc, of, g, kernel, out=Y.t, workspace=workspace)
     Y.check()
     return Y.t
 
@@ -151,13 +151,32 @@ SKINNY_NK = [(200, 4160), (520, 512), (64, 96), (1030, 1024)]
 
 @pytest.mark.parametrize("g", [32, 64, 128])
 @pytest.mark.parametrize("nk", SKINNY_NK, ids=[f"{n}x{k}" for n, k in SKINNY_NK])
-def test_linear_skinny(g, nk):
+def test_linear_skinny_cluster(g, nk):
     N, K = nk
     if K % g:
         pytest.skip("K not a multiple of g")
     for M in SKINNY_M:
         (X, Wq, sc, of), y_ref = _problem(M, N, K, g, seed=7 * M + N + g)
-        assert_linear_ok(gpu_linear(X, Wq, sc, of, g, w4.KERNEL_SKINNY), y_ref, f"skinny M={M} N={N} K={K} g={g}")
+        assert_linear_ok(gpu_linear(X, Wq, sc, of, g, w4.KERNEL_SKINNY_CLUSTER), y_ref,
+                         f"skinny cluster M={M} N={N} K={K} g={g}")
+
+
+STREAM_NK = [(200, 4160), (520, 512), (64, 256), (1030, 1024), (4096, 1536), (48, 14336)]
+
+
+@pytest.mark.parametrize("g", [32, 64, 128])
+@pytest.mark.parametrize("nk", STREAM_NK, ids=[f"{n}x{k}" for n, k in STREAM_NK])
+def test_linear_stream(g, nk):
+    N, K = nk
+    if K % g or (K // g) % 2:
+        pytest.skip("the stream kernel needs an even K/g")
+    ws = w4.Workspace(DEV).reserve_for(8, N, K, g)
+    for M in (1, 2, 3, 5, 8):
+        (X, Wq, sc, of), y_ref = _problem(M, N, K, g, seed=13 * M + N + g)
+        assert_linear_ok(gpu_linear(X, Wq, sc, of, g, w4.KERNEL_STREAM, workspace=ws), y_ref,
+                         f"stream M={M} N={N} K={K} g={g}")
+        torch.cuda.synchronize()
+        assert int(ws.buf.count_nonzero()) == 0, "the stream kernel must leave its workspace zeroed"
 
 
 GEMM_M = [1, 33, 127, 129, 300]
@@ -178,21 +197,45 @@ def test_linear_gemm(g, nk):
 
 def test_linear_auto_dispatch_and_both_kernels_agree():
     (X, Wq, sc, of), y_ref = _problem(32, 768, 2048, 32, seed=5)
-    ys = gpu_linear(X, Wq, sc, of, 32, w4.KERNEL_SKINNY)
+    ys = gpu_linear(X, Wq, sc, of, 32, w4.KERNEL_SKINNY_CLUSTER)
     yg = gpu_linear(X, Wq, sc, of, 32, w4.KERNEL_GEMM)
     ya = gpu_linear(X, Wq, sc, of, 32)
-    assert torch.equal(ys.view(torch.int16), ya.view(torch.int16))  # M <= 32 goes to the skinny kernel
+    assert torch.equal(ys.view(torch.int16), ya.view(torch.int16))  # 8 < M <= 32 goes to the cluster kernel
     assert_linear_ok(ys, y_ref, "skinny")
     assert_linear_ok(yg, y_ref, "gemm")
     # the two kernels round differently but agree to bf16 precision
     assert float((ys.float() - yg.float()).abs().max()) <= 2e-2 * float(yg.float().abs().max())
 
 
+def test_workspace_shared_by_calls_of_different_shapes():
+    """One workspace, stream-kernel calls of different shapes in turn: each
+    leaves it zeroed for the next."""
+    a = _problem(8, 1030, 1024, 32, seed=31)
+    b = _problem(1, 14336, 1024, 32, seed=32)
+    c = _problem(3, 200, 4160, 32, seed=33)
+    ws = w4.Workspace(DEV).reserve(max(w4.w4_linear_workspace_bytes(8, 1030, 1024, 32),
+                                       w4.w4_linear_workspace_bytes(1, 14336, 1024, 32),
+                                       w4.w4_linear_workspace_bytes(3, 200, 4160, 32)))
+    for (dev, y_ref) in (a, b, c, a, c, b):
+        assert_linear_ok(gpu_linear(*dev, 32, w4.KERNEL_STREAM, workspace=ws), y_ref, "shared workspace")
+    torch.cuda.synchronize()
+    assert int(ws.buf.count_nonzero()) == 0
+
+
+def test_auto_uses_the_stream_kernel_only_with_a_workspace():
+    (X, Wq, sc, of), y_ref = _problem(2, 2048, 2048, 64, seed=34)
+    no_ws = w4.Workspace(DEV)  # zero bytes: the cluster kernel runs
+    y0 = gpu_linear(X, Wq, sc, of, 64, w4.KERNEL_AUTO, workspace=no_ws)
+    y1 = gpu_linear(X, Wq, sc, of, 64, w4.KERNEL_SKINNY_CLUSTER)
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+    assert_linear_ok(gpu_linear(X, Wq, sc, of, 64), y_ref, "auto with workspace")
+
+
 def test_linear_is_deterministic():
     (X, Wq, sc, of), y_ref = _problem(3, 2048, 4096, 64, seed=9)
-    first = gpu_linear(X, Wq, sc, of, 64)
+    first = gpu_linear(X, Wq, sc, of, 64, w4.KERNEL_SKINNY_CLUSTER)
     for _ in range(5):
-        again = gpu_linear(X, Wq, sc, of, 64)
+        again = gpu_linear(X, Wq, sc, of, 64, w4.KERNEL_SKINNY_CLUSTER)
         assert torch.equal(first.view(torch.int16), again.view(torch.int16))
     assert_linear_ok(first, y_ref, "repeat")
 
@@ -242,23 +285,25 @@ def test_empty_problems():
 def test_cuda_graph_capture_matches_eager():
     probs = [_problem(1, N, K, 32, seed=20 + i) for i, (N, K) in enumerate([(1024, 4096), (4096, 1024), (768, 2048)])]
     outs = [torch.empty((1, p[0][1].shape[0]), dtype=torch.bfloat16, device=DEV) for p in probs]
-    eager = [gpu_linear(*p[0], 32).clone() for p in probs]
+    ws = w4.Workspace(DEV).reserve(max(w4.w4_linear_workspace_bytes(1, p[0][1].shape[0], p[0][0].shape[1], 32)
+                                       for p in probs))
+    eager = [gpu_linear(*p[0], 32, workspace=ws).clone() for p in probs]
     s = torch.cuda.Stream(DEV)
     s.wait_stream(torch.cuda.current_stream(DEV))
     with torch.cuda.stream(s):
         for (dev, _), out in zip(probs, outs):  # warm up on the capture stream
-            w4.w4_linear(*dev, 32, out=out)
+            w4.w4_linear(*dev, 32, out=out, workspace=ws)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=s):
             for (dev, _), out in zip(probs, outs):
-                w4.w4_linear(*dev, 32, out=out)
+                w4.w4_linear(*dev, 32, out=out, workspace=ws)
     torch.cuda.current_stream(DEV).wait_stream(s)
     for out in outs:
         out.zero_()
     graph.replay()
     torch.cuda.synchronize()
-    for e, o in zip(eager, outs):
-        assert torch.equal(e.view(torch.int16), o.view(torch.int16))
+    for (dev, y_ref), o in zip(probs, outs):
+        assert_linear_ok(o, y_ref, "graph replay")
 
 
 def test_no_device_fault_pending():
