@@ -11,10 +11,10 @@
 //    problem, taken in (row tile, k) order, are cut into equal contiguous
 //    ranges, one per warp of a one-wave persistent grid: every warp streams
 //    the same number of bytes (within one unit), whatever N and K are.
-//  * Each warp owns a ring of six unit slots.  Lane 0 fetches a unit's codes
+//  * Each warp owns a ring of four unit slots.  Lane 0 fetches a unit's codes
 //    with one 2-D TMA copy (16 rows x 128 bytes, 128-byte swizzle, zero fill
 //    past N and K); the 32 lanes fetch its scales and offsets with 4-byte
-//    cp.async; all complete on the slot's mbarrier.  The first six units are
+//    cp.async; all complete on the slot's mbarrier.  The first four units are
 //    requested before the programmatic-dependent-launch wait.
 //  * X (only 256 k x M tokens per unit) is loaded one unit ahead into
 //    registers, permuted to the MMA k order and staged in the warp's shared
@@ -39,7 +39,7 @@ namespace w4 {
 constexpr int ST_WARPS = 4;
 constexpr int ST_THREADS = ST_WARPS * 32;
 constexpr int ST_UK = 256;                 // k per unit
-constexpr int ST_DEPTH = 6;                // ring slots per warp
+constexpr int ST_DEPTH = 4;                // ring slots per warp
 constexpr int ST_WSLOT = 16 * 128;         // codes of one unit: 16 rows x 128 bytes
 constexpr int ST_XPITCH = ST_UK * 2 + 16;  // one staged token row of a unit (+16 bytes against bank conflicts)
 
@@ -101,14 +101,16 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
 }
 __device__ __forceinline__ int st_x_slot(int c) { return c ^ (((c >> 3) & 1) << 1); }
 
-template <int G>
+template <int G, int MX>
 __global__ void __launch_bounds__(ST_THREADS)
 stream_kernel(const __grid_constant__ CUtensorMap tm_w, const StreamArgs p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     constexpr int QSLOT = 2 * 16 * (ST_UK / G) * 2;  // scales then offsets, 16 rows x (256/G) groups each
     constexpr int QROW = (ST_UK / G) * 2;            // bytes of one row of one array
-    constexpr int PIECES = 2 * 16 * (ST_UK / G) / 2;  // 4-byte qparam pieces per unit
+    constexpr int PPR = QROW / 4;                    // 4-byte pieces per row and array
+    constexpr int PIECES = 2 * 16 * PPR;             // 4-byte qparam pieces per unit
+    constexpr int PPL = (PIECES + 31) / 32;          // pieces per lane
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, tq = lane & 3;
@@ -119,6 +121,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const StreamArgs p) {
     const long long u0 = p.units * worker / p.workers;
     const long long u1 = p.units * (worker + 1) / p.workers;
     if (u0 >= u1) return;
+    const int nunits = (int)(u1 - u0);
 
     const int rest = st_rest_bytes(p.M, G);
     const uint32_t wslots = smem_u32(smem) + warp * (ST_DEPTH * ST_WSLOT);
@@ -137,90 +140,126 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const StreamArgs p) {
         *reinterpret_cast<uint4*>(zrow + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
     __syncwarp();
 
-    // request unit u into ring slot d: codes by TMA, scales/offsets by 4-byte cp.async
-    auto issue = [&](long long u, int d) {
-        const int tile = (int)(u / p.nkc), kc = (int)(u % p.nkc);
+    // this lane's qparam pieces: fixed (array, row, piece) for every unit
+    int prow[PPL], pcol[PPL];  // row in the tile, first group of the piece
+    uint32_t pdst[PPL];        // offset inside a qparam slot
+    const uint16_t* pbase[PPL];
+#pragma unroll
+    for (int q = 0; q < PPL; ++q) {
+        const int i = lane + 32 * q;
+        const int arr = (i < PIECES) ? i / (PIECES / 2) : 0, rem = (i < PIECES) ? i % (PIECES / 2) : 0;
+        prow[q] = rem / PPR;
+        pcol[q] = 2 * (rem % PPR);
+        pdst[q] = (uint32_t)(arr * 16 * QROW + prow[q] * QROW + 4 * (rem % PPR));
+        pbase[q] = arr ? p.offsets : p.scales;
+    }
+
+    // request the unit at (tile, kc) into ring slot d: codes by TMA, scales/offsets by 4-byte cp.async
+    auto issue = [&](int tile, int kc, int d) {
         const int row0 = tile * 16, k = kc * ST_UK;
         const uint32_t bar = bars + 8 * d;
         if (lane == 0) {
             mbar_arrive_expect_tx(bar, ST_WSLOT);
             tma_load_2d(wslots + d * ST_WSLOT, &tm_w, bar, k / 2, row0);
         }
-        for (int i = lane; i < PIECES; i += 32) {
-            const int arr = i / (PIECES / 2), rem = i % (PIECES / 2);
-            const int r = rem / (QROW / 4), pc = rem % (QROW / 4);
-            const int n = min(row0 + r, p.N - 1);            // rows past N: any finite qparams (codes are 0)
-            const int j = min(k / G + 2 * pc, ng - 2);       // groups past K: likewise (X is 0 there)
-            const uint16_t* src = (arr ? p.offsets : p.scales) + (int64_t)n * ng + j;
-            cp_async_4(qslots + d * QSLOT + arr * 16 * QROW + r * QROW + 4 * pc, src);
+        const bool edge = (row0 + 16 > p.N) || (k + ST_UK > p.K);  // clamp into the tensor (finite fill values)
+#pragma unroll
+        for (int q = 0; q < PPL; ++q) {
+            if (PIECES % 32 == 0 || lane + 32 * q < PIECES) {
+                int n = row0 + prow[q], j = k / G + pcol[q];
+                if (edge) {
+                    n = min(n, p.N - 1);  // rows past N: any finite qparams (their codes are 0)
+                    j = min(j, ng - 2);   // groups past K: likewise (X is 0 there)
+                }
+                cp_async_4(qslots + d * QSLOT + pdst[q], pbase[q] + (int64_t)n * ng + j);
+            }
         }
         cp_async_arrive_noinc(bar);
     };
 
-    const int depth = (u1 - u0 < ST_DEPTH) ? (int)(u1 - u0) : ST_DEPTH;
-    for (int d = 0; d < depth; ++d) issue(u0 + d, d);
+    // unit cursors, advanced without division
+    const int tile0 = (int)(u0 / p.nkc), kc0 = (int)(u0 % p.nkc);
+    int it_tile = tile0, it_kc = kc0;  // next unit to request
+    auto advance = [&](int& tile, int& kc) {
+        if (++kc == p.nkc) {
+            kc = 0;
+            ++tile;
+        }
+    };
+    const int depth = nunits < ST_DEPTH ? nunits : ST_DEPTH;
+    for (int d = 0; d < depth; ++d) {
+        issue(it_tile, it_kc, d);
+        advance(it_tile, it_kc);
+    }
 
     // activations may come from the previous kernel: wait for it
     griddep_wait();
 
     // X of a unit: lane c holds 8-k chunk c of every token
-    uint4 xr[8];
-    auto load_x = [&](long long u) {
-        const int k = (int)(u % p.nkc) * ST_UK + 8 * lane;
+    uint4 xr[MX];
+    const uint16_t* xlane = p.X + 8 * lane;
+    auto load_x = [&](int kc) {
+        const int k = kc * ST_UK + 8 * lane;
 #pragma unroll
-        for (int m = 0; m < 8; ++m)
-            if (m < p.M) xr[m] = (k < p.K) ? ldg_cg_v4(p.X + (int64_t)m * p.K + k) : make_uint4(0u, 0u, 0u, 0u);
+        for (int m = 0; m < MX; ++m)
+            if (m < p.M) xr[m] = (k < p.K) ? ldg_cg_v4(xlane + (int64_t)m * p.K + kc * ST_UK) : make_uint4(0u, 0u, 0u, 0u);
     };
+    const uint32_t xst = (uint32_t)(16 * st_x_slot(lane));
     auto store_x = [&](unsigned char* slot) {
 #pragma unroll
-        for (int m = 0; m < 8; ++m)
+        for (int m = 0; m < MX; ++m)
             if (m < p.M) {
                 uint4 o;
                 o.x = __byte_perm(xr[m].x, xr[m].z, 0x5410);  // (x0, x4)
                 o.y = __byte_perm(xr[m].x, xr[m].z, 0x7632);  // (x1, x5)
                 o.z = __byte_perm(xr[m].y, xr[m].w, 0x5410);  // (x2, x6)
                 o.w = __byte_perm(xr[m].y, xr[m].w, 0x7632);  // (x3, x7)
-                *reinterpret_cast<uint4*>(slot + m * ST_XPITCH + 16 * st_x_slot(lane)) = o;
+                *reinterpret_cast<uint4*>(slot + m * ST_XPITCH + xst) = o;
             }
     };
 
-    const uint32_t c_mask = 0x000F000Fu, c_magic = 0x43004300u;
-    uint32_t cm, cg;  // constants pinned in registers
-    asm volatile("mov.b32 %0, %1;" : "=r"(cm) : "r"(c_mask));
-    asm volatile("mov.b32 %0, %1;" : "=r"(cg) : "r"(c_magic));
+    uint32_t cm, cg;  // LOP3 constants pinned in registers
+    asm volatile("mov.b32 %0, %1;" : "=r"(cm) : "r"(0x000F000Fu));
+    asm volatile("mov.b32 %0, %1;" : "=r"(cg) : "r"(0x43004300u));
 
     const int pr = ((gid >> 1) | ((gid & 1) << 2));  // MMA row gid <- tile row pr (bank-conflict-free swizzled reads)
-    const uint32_t swz = (uint32_t)pr;                // rows pr and pr + 8 share (row & 7)
+    const uint32_t cpos0 = ((uint32_t)tq ^ (uint32_t)pr) << 4, cpos1 = ((uint32_t)(4 + tq) ^ (uint32_t)pr) << 4;
     uint32_t boff[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) boff[j] = 16u * (uint32_t)((4 * tq + j) ^ ((tq >> 1) << 1));
+    const uint32_t jq0 = (uint32_t)(((32 * tq) / G) * 2), jq1 = (uint32_t)(((128 + 32 * tq) / G) * 2);
+    const uint32_t xrow_off = (uint32_t)(gid * ST_XPITCH);
+    const uint32_t zaddr = smem_u32(zrow);
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    int kc_first = (int)(u0 % p.nkc);
+    int tile = tile0, kc = kc0, kc_first = kc0;  // unit being computed
+    int x_kc = kc0;                               // unit whose X sits in xr
     bool ok = true;
+    int d = 0;
+    uint32_t phase = 0;
 
-    load_x(u0);
-    for (long long u = u0; u < u1; ++u) {
-        const int it = (int)(u - u0);
-        const int d = it % ST_DEPTH;
+    load_x(x_kc);
+    for (int it = 0; it < nunits; ++it) {
         unsigned char* xs = xslots + (it & 1) * p.M * ST_XPITCH;
         store_x(xs);
-        if (u + 1 < u1) load_x(u + 1);
-        ok = mbar_wait_bounded(bars + 8 * d, (uint32_t)((it / ST_DEPTH) & 1), nullptr, &g_stream_fault, 1u,
-                               ST_WAIT_LIMIT_NS) && ok;
+        if (it + 1 < nunits) {
+            if (++x_kc == p.nkc) x_kc = 0;
+            load_x(x_kc);
+        }
+        ok = mbar_wait_bounded(bars + 8 * d, phase, nullptr, &g_stream_fault, 1u, ST_WAIT_LIMIT_NS) && ok;
         __syncwarp();
 
         const uint32_t ws_a = wslots + d * ST_WSLOT + pr * 128;
         const uint32_t ws_b = ws_a + 8 * 128;
-        const uint32_t qa = qslots + d * QSLOT + pr * QROW;      // scales of row pr
-        const uint32_t qb = qa + 8 * QROW;                        // scales of row pr + 8
-        const uint32_t bbase = smem_u32(gid < p.M ? xs + gid * ST_XPITCH : zrow);
+        const uint32_t qa = qslots + d * QSLOT + pr * QROW;  // scales of row pr; offsets 16 rows further
+        const uint32_t qb = qa + 8 * QROW;
+        const uint32_t bbase = gid < p.M ? smem_u32(xs) + xrow_off : zaddr;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {  // two 128-k steps per unit
-            const uint32_t cpos = ((uint32_t)(4 * h + tq) ^ swz) << 4;
+            const uint32_t cpos = h ? cpos1 : cpos0;
+            const uint32_t jq = h ? jq1 : jq0;
             const uint4 wa = lds128_st(ws_a + cpos);
             const uint4 wb = lds128_st(ws_b + cpos);
-            const uint32_t jq = (uint32_t)(((128 * h + 32 * tq) / G) * 2);
             const uint32_t sa = lds_u16_st(qa + jq), oa = lds_u16_st(qa + 16 * QROW + jq);
             const uint32_t sb = lds_u16_st(qb + jq), ob = lds_u16_st(qb + 16 * QROW + jq);
             const uint32_t sa2 = __byte_perm(sa, 0, 0x1010), oa2 = __byte_perm(oa, 0, 0x1010);
@@ -243,14 +282,18 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const StreamArgs p) {
             }
         }
         __syncwarp();
-        if (u + ST_DEPTH < u1) {  // refill the slot (its reads are done: order them before the async writes)
+        if (it + ST_DEPTH < nunits) {  // refill the slot (its reads are done: order them before the async writes)
             fence_proxy_async_smem();
-            issue(u + ST_DEPTH, d);
+            issue(it_tile, it_kc, d);
+            advance(it_tile, it_kc);
+        }
+        if (++d == ST_DEPTH) {
+            d = 0;
+            phase ^= 1u;
         }
 
         // end of a row tile or of the range: hand the tile's sums on
-        const int tile = (int)(u / p.nkc), kc = (int)(u % p.nkc);
-        if (u + 1 == u1 || kc == p.nkc - 1) {
+        if (it + 1 == nunits || kc == p.nkc - 1) {
             const int n_a = tile * 16 + pr, n_b = n_a + 8;
             const int m0 = 2 * tq;  // acc = D[row n_a: tokens m0, m0+1 | row n_b: tokens m0, m0+1]
             if (kc_first == 0 && kc == p.nkc - 1) {  // this warp summed all of the tile's k
@@ -289,10 +332,10 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const StreamArgs p) {
             acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
             kc_first = 0;
         }
+        advance(tile, kc);
     }
     if (!ok) {  // never leave with copies still landing in shared memory
-        const int issued = (int)(u1 - u0);
-        for (int it = max(0, issued - ST_DEPTH); it < issued; ++it)
+        for (int it = max(0, nunits - ST_DEPTH); it < nunits; ++it)
             mbar_drain_bounded(bars + 8 * (it % ST_DEPTH), (uint32_t)((it / ST_DEPTH) & 1), ST_WAIT_LIMIT_NS);
     }
 }
@@ -318,10 +361,10 @@ size_t stream_ws_bytes(int64_t M, int64_t N) {
     return part + (size_t)((N + 15) / 16) * 4;
 }
 
-template <int G>
-static cudaError_t launch_stream_g(const StreamPlan& plan, const CUtensorMap& tw, StreamArgs a, cudaStream_t stream) {
-    auto kern = stream_kernel<G>;
-    cudaError_t e = ensure_kernel_attrs(reinterpret_cast<const void*>(kern), st_smem_bytes(STREAM_MAX_M, G), false);
+template <int G, int MX>
+static cudaError_t launch_stream_gm(const StreamPlan& plan, const CUtensorMap& tw, StreamArgs a, cudaStream_t stream) {
+    auto kern = stream_kernel<G, MX>;
+    cudaError_t e = ensure_kernel_attrs(reinterpret_cast<const void*>(kern), st_smem_bytes(MX, G), false);
     if (e != cudaSuccess) return e;
     // one wave: as many resident warps as the SMs hold, but no more than there are units
     int sms = 0, per_sm = 0;
@@ -341,6 +384,14 @@ static cudaError_t launch_stream_g(const StreamPlan& plan, const CUtensorMap& tw
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, tw, a);
+}
+
+template <int G>
+static cudaError_t launch_stream_g(const StreamPlan& plan, const CUtensorMap& tw, StreamArgs a, cudaStream_t stream) {
+    if (a.M <= 1) return launch_stream_gm<G, 1>(plan, tw, a, stream);
+    if (a.M <= 2) return launch_stream_gm<G, 2>(plan, tw, a, stream);
+    if (a.M <= 4) return launch_stream_gm<G, 4>(plan, tw, a, stream);
+    return launch_stream_gm<G, 8>(plan, tw, a, stream);
 }
 
 cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
