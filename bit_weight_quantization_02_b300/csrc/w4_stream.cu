@@ -11,10 +11,10 @@
 //    problem, taken in (row tile, k) order, are cut into equal contiguous
 //    ranges, one per warp of a one-wave persistent grid: every warp streams
 //    the same number of bytes (within one unit), whatever N and K are.
-//  * Each warp owns a ring of four unit slots.  Lane 0 fetches a unit's codes
+//  * Each warp owns a ring of three unit slots.  Lane 0 fetches a unit's codes
 //    with one 2-D TMA copy (16 rows x 128 bytes, 128-byte swizzle, zero fill
 //    past N and K); the 32 lanes fetch its scales and offsets with 4-byte
-//    cp.async; all complete on the slot's mbarrier.  The first four units are
+//    cp.async; all complete on the slot's mbarrier.  The first three units are
 //    requested before the programmatic-dependent-launch wait.
 //  * X (only 256 k x M tokens per unit) is loaded one unit ahead into
 //    registers, permuted to the MMA k order and staged in the warp's shared
@@ -39,7 +39,7 @@ namespace w4 {
 constexpr int ST_WARPS = 4;
 constexpr int ST_THREADS = ST_WARPS * 32;
 constexpr int ST_UK = 256;                 // k per unit
-constexpr int ST_DEPTH = 4;                // ring slots per warp
+constexpr int ST_DEPTH = 3;                // ring slots per warp
 constexpr int ST_WSLOT = 16 * 128;         // codes of one unit: 16 rows x 128 bytes
 constexpr int ST_XPITCH = ST_UK * 2 + 16;  // one staged token row of a unit (+16 bytes against bank conflicts)
 
@@ -102,7 +102,7 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
 __device__ __forceinline__ int st_x_slot(int c) { return c ^ (((c >> 3) & 1) << 1); }
 
 template <int G, int MX>
-__global__ void __launch_bounds__(ST_THREADS)
+__global__ void __launch_bounds__(ST_THREADS, 6)
 stream_kernel(const __grid_constant__ CUtensorMap tm_w, const StreamArgs p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
