@@ -60,7 +60,7 @@ struct StreamArgs {
 __host__ __device__ inline int st_qslot_bytes(int g) { return 2 * 16 * (ST_UK / g) * 2; }
 __host__ __device__ inline int st_rest_bytes(int M, int g) {
     const int b = ST_DEPTH * st_qslot_bytes(g) + (2 * M + 1) * ST_XPITCH + 8 * ST_DEPTH;
-    return (b + 15) & ~15;
+    return (b + 127) & ~127;  // qparam slots are TMA destinations: 128-byte aligned
 }
 __host__ __device__ inline int st_smem_bytes(int M, int g) {
     return ST_WARPS * ST_DEPTH * ST_WSLOT + ST_WARPS * st_rest_bytes(M, g) + 1024;  // + 1024-byte alignment slack
@@ -101,9 +101,44 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
 }
 __device__ __forceinline__ int st_x_slot(int c) { return c ^ (((c >> 3) & 1) << 1); }
 
-template <int G, int MX>
+// One MMA step from packed codes: nibble pairs (SH, SH+4) and (SH+1... ) of the
+// 32-bit code words of rows a and b become the four A-fragment registers
+// (128+q via LOP3, exact -128, one bf16 FMA with scale and offset) inside the
+// same asm block as the mma.sync, so they are born in the operand registers.
+// SH = 0 takes nibbles (0,4) and (1,5); SH = 8 takes (2,6) and (3,7).
+template <int SH>
+__device__ __forceinline__ void dq_mma(float (&c)[4], uint32_t wa, uint32_t wb, uint32_t sa2, uint32_t oa2,
+                                       uint32_t sb2, uint32_t ob2, uint32_t x0, uint32_t x1, uint32_t cm,
+                                       uint32_t cg, uint32_t c128) {
+    asm volatile(
+        "{\n\t.reg .b32 a0, a1, b0, b1, t;\n\t"
+        "shr.b32 t, %4, %15;\n\t"
+        "lop3.b32 a0, t, %12, %13, 0xEA;\n\t"
+        "shr.b32 t, %4, %16;\n\t"
+        "lop3.b32 a1, t, %12, %13, 0xEA;\n\t"
+        "shr.b32 t, %5, %15;\n\t"
+        "lop3.b32 b0, t, %12, %13, 0xEA;\n\t"
+        "shr.b32 t, %5, %16;\n\t"
+        "lop3.b32 b1, t, %12, %13, 0xEA;\n\t"
+        "sub.rn.bf16x2 a0, a0, %14;\n\t"
+        "sub.rn.bf16x2 a1, a1, %14;\n\t"
+        "sub.rn.bf16x2 b0, b0, %14;\n\t"
+        "sub.rn.bf16x2 b1, b1, %14;\n\t"
+        "fma.rn.bf16x2 a0, a0, %6, %7;\n\t"
+        "fma.rn.bf16x2 a1, a1, %6, %7;\n\t"
+        "fma.rn.bf16x2 b0, b0, %8, %9;\n\t"
+        "fma.rn.bf16x2 b1, b1, %8, %9;\n\t"
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {a0,b0,a1,b1}, {%10,%11}, "
+        "{%0,%1,%2,%3};\n\t}"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(wa), "r"(wb), "r"(sa2), "r"(oa2), "r"(sb2), "r"(ob2), "r"(x0), "r"(x1), "r"(cm), "r"(cg),
+          "r"(c128), "n"(SH), "n"(SH + 4));
+}
+
+template <int G, int MX, bool QT>
 __global__ void __launch_bounds__(ST_THREADS, 6)
-stream_kernel(const __grid_constant__ CUtensorMap tm_w, const StreamArgs p) {
+stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
+              const __grid_constant__ CUtensorMap tm_o, const StreamArgs p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     constexpr int QSLOT = 2 * 16 * (ST_UK / G) * 2;  // scales then offsets, 16 rows x (256/G) groups each
@@ -132,8 +167,8 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const StreamArgs p) {
     const uint32_t bars = smem_u32(zrow + ST_XPITCH);                    // ST_DEPTH mbarriers
     const int ng = p.K / G;
 
-    if (lane == 0) {
-        for (int d = 0; d < ST_DEPTH; ++d) mbar_init(bars + 8 * d, 33);  // TMA arrive + 32 cp.async arrivals
+    if (lane == 0) {  // arrivals per fill: the TMA arrive (+ 32 cp.async arrivals when qparams go that way)
+        for (int d = 0; d < ST_DEPTH; ++d) mbar_init(bars + 8 * d, QT ? 1 : 33);
         mbar_fence_init();
     }
     for (int c = lane; c < ST_XPITCH / 16; c += 32)
@@ -158,6 +193,15 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const StreamArgs p) {
     auto issue = [&](int tile, int kc, int d) {
         const int row0 = tile * 16, k = kc * ST_UK;
         const uint32_t bar = bars + 8 * d;
+        if (QT) {  // qparams as two more TMA boxes of 16 rows x 8 groups (zero fill past N and K)
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar, ST_WSLOT + QSLOT);
+                tma_load_2d(wslots + d * ST_WSLOT, &tm_w, bar, k / 2, row0);
+                tma_load_2d(qslots + d * QSLOT, &tm_s, bar, k / G, row0);
+                tma_load_2d(qslots + d * QSLOT + 16 * QROW, &tm_o, bar, k / G, row0);
+            }
+            return;
+        }
         if (lane == 0) {
             mbar_arrive_expect_tx(bar, ST_WSLOT);
             tma_load_2d(wslots + d * ST_WSLOT, &tm_w, bar, k / 2, row0);
@@ -218,9 +262,10 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const StreamArgs p) {
             }
     };
 
-    uint32_t cm, cg;  // LOP3 constants pinned in registers
+    uint32_t cm, cg, c128;  // constants pinned in registers: nibble mask, bf16 128.0 pair (magic and bias)
     asm volatile("mov.b32 %0, %1;" : "=r"(cm) : "r"(0x000F000Fu));
     asm volatile("mov.b32 %0, %1;" : "=r"(cg) : "r"(0x43004300u));
+    c128 = cg;
 
     const int pr = ((gid >> 1) | ((gid & 1) << 2));  // MMA row gid <- tile row pr (bank-conflict-free swizzled reads)
     const uint32_t cpos0 = ((uint32_t)tq ^ (uint32_t)pr) << 4, cpos1 = ((uint32_t)(4 + tq) ^ (uint32_t)pr) << 4;
@@ -268,17 +313,9 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const StreamArgs p) {
             const uint32_t wb4[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const uint32_t a0 = dequant_pair(lop_and_or(wa4[j], cm, cg), sa2, oa2);
-                const uint32_t a1 = dequant_pair(lop_and_or(wa4[j] >> 4, cm, cg), sa2, oa2);
-                const uint32_t a2 = dequant_pair(lop_and_or(wa4[j] >> 8, cm, cg), sa2, oa2);
-                const uint32_t a3 = dequant_pair(lop_and_or(wa4[j] >> 12, cm, cg), sa2, oa2);
-                const uint32_t b0 = dequant_pair(lop_and_or(wb4[j], cm, cg), sb2, ob2);
-                const uint32_t b1 = dequant_pair(lop_and_or(wb4[j] >> 4, cm, cg), sb2, ob2);
-                const uint32_t b2 = dequant_pair(lop_and_or(wb4[j] >> 8, cm, cg), sb2, ob2);
-                const uint32_t b3 = dequant_pair(lop_and_or(wb4[j] >> 12, cm, cg), sb2, ob2);
                 const uint4 xv = lds128_st(bbase + 256u * h + boff[j]);
-                mma_bf16_16816_st(acc, a0, b0, a1, b1, xv.x, xv.y);
-                mma_bf16_16816_st(acc, a2, b2, a3, b3, xv.z, xv.w);
+                dq_mma<0>(acc, wa4[j], wb4[j], sa2, oa2, sb2, ob2, xv.x, xv.y, cm, cg, c128);
+                dq_mma<8>(acc, wa4[j], wb4[j], sa2, oa2, sb2, ob2, xv.z, xv.w, cm, cg, c128);
             }
         }
         __syncwarp();
@@ -361,9 +398,10 @@ size_t stream_ws_bytes(int64_t M, int64_t N) {
     return part + (size_t)((N + 15) / 16) * 4;
 }
 
-template <int G, int MX>
-static cudaError_t launch_stream_gm(const StreamPlan& plan, const CUtensorMap& tw, StreamArgs a, cudaStream_t stream) {
-    auto kern = stream_kernel<G, MX>;
+template <int G, int MX, bool QT>
+static cudaError_t launch_stream_gm(const StreamPlan& plan, const CUtensorMap& tw, const CUtensorMap& ts,
+                                   const CUtensorMap& to, StreamArgs a, cudaStream_t stream) {
+    auto kern = stream_kernel<G, MX, QT>;
     cudaError_t e = ensure_kernel_attrs(reinterpret_cast<const void*>(kern), st_smem_bytes(MX, G), false);
     if (e != cudaSuccess) return e;
     // one wave: as many resident warps as the SMs hold, but no more than there are units
@@ -383,24 +421,37 @@ static cudaError_t launch_stream_gm(const StreamPlan& plan, const CUtensorMap& t
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tw, a);
+    return cudaLaunchKernelEx(&cfg, kern, tw, ts, to, a);
 }
 
-template <int G>
-static cudaError_t launch_stream_g(const StreamPlan& plan, const CUtensorMap& tw, StreamArgs a, cudaStream_t stream) {
-    if (a.M <= 1) return launch_stream_gm<G, 1>(plan, tw, a, stream);
-    if (a.M <= 2) return launch_stream_gm<G, 2>(plan, tw, a, stream);
-    if (a.M <= 4) return launch_stream_gm<G, 4>(plan, tw, a, stream);
-    return launch_stream_gm<G, 8>(plan, tw, a, stream);
+template <int G, bool QT>
+static cudaError_t launch_stream_g(const StreamPlan& plan, const CUtensorMap& tw, const CUtensorMap& ts,
+                                   const CUtensorMap& to, StreamArgs a, cudaStream_t stream) {
+    if (a.M <= 1) return launch_stream_gm<G, 1, QT>(plan, tw, ts, to, a, stream);
+    if (a.M <= 2) return launch_stream_gm<G, 2, QT>(plan, tw, ts, to, a, stream);
+    if (a.M <= 4) return launch_stream_gm<G, 4, QT>(plan, tw, ts, to, a, stream);
+    return launch_stream_gm<G, 8, QT>(plan, tw, ts, to, a, stream);
 }
 
 cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
                           const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
                           void* workspace, cudaStream_t stream, const char** detail) {
-    CUtensorMap tw;  // codes: [N][K/2] bytes, one box = 16 rows x 128 bytes (256 k), 128-byte swizzle
+    CUtensorMap tw, ts, to;  // codes: [N][K/2] bytes, one box = 16 rows x 128 bytes (256 k), 128-byte swizzle
     cudaError_t e = encode_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)(K / 2), (uint64_t)N,
                                          (uint64_t)(K / 2), 128, 16, CU_TENSOR_MAP_SWIZZLE_128B, detail);
     if (e != cudaSuccess) return e;
+    const int64_t ng = K / g;
+    const bool qt = (g == 32) && (ng % 8 == 0);  // qparam rows 16-byte aligned: 8-group TMA boxes
+    ts = tw;
+    to = tw;
+    if (qt) {
+        e = encode_tensor_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, (uint64_t)ng, (uint64_t)N,
+                                 (uint64_t)ng * 2, 8, 16, CU_TENSOR_MAP_SWIZZLE_NONE, detail);
+        if (e == cudaSuccess)
+            e = encode_tensor_map_2d(&to, CU_TENSOR_MAP_DATA_TYPE_UINT16, offsets, (uint64_t)ng, (uint64_t)N,
+                                     (uint64_t)ng * 2, 8, 16, CU_TENSOR_MAP_SWIZZLE_NONE, detail);
+        if (e != cudaSuccess) return e;
+    }
     StreamArgs a;
     a.X = X;
     a.scales = scales;
@@ -416,9 +467,11 @@ cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, 
     a.units = plan.units;
     a.workers = 0;
     switch (g) {
-        case 32: return launch_stream_g<32>(plan, tw, a, stream);
-        case 64: return launch_stream_g<64>(plan, tw, a, stream);
-        default: return launch_stream_g<128>(plan, tw, a, stream);
+        case 32:
+            return qt ? launch_stream_g<32, true>(plan, tw, ts, to, a, stream)
+                      : launch_stream_g<32, false>(plan, tw, ts, to, a, stream);
+        case 64: return launch_stream_g<64, false>(plan, tw, ts, to, a, stream);
+        default: return launch_stream_g<128, false>(plan, tw, ts, to, a, stream);
     }
 }
 
