@@ -66,6 +66,7 @@ def load_library():
             "w4_status_string": ([i32], ctypes.c_char_p),
             "w4_last_error_detail": ([], ctypes.c_char_p),
             "w4_format_version": ([], i32),
+            "w4_linear_static": ([p, i64, i64, p, p, p, i64, i32, p, p], i32),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -201,6 +202,20 @@ def w4_linear_ex(X: torch.Tensor, Wq: torch.Tensor, scales: torch.Tensor, offset
 def w4_linear(X, Wq, scales, offsets, group_size, out=None, workspace=None):
     """Y bf16 [M,N] = X . dequant(Wq)^T (kernel chosen by M; see include/w4.h)."""
     return w4_linear_ex(X, Wq, scales, offsets, group_size, KERNEL_AUTO, out, workspace)
+
+
+def w4_linear_static(X, Wq, scales, offsets, group_size, out=None):
+    """w4_linear for callers that cannot allocate device memory: the library's
+    own 4 MiB device array serves as workspace (M <= 8; see include/w4.h).
+    Calls that can overlap on the GPU share that array and must be serialized."""
+    lib = load_library()
+    _bits16(X, "X")
+    M, K = X.shape
+    N = Wq.shape[0]
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    _check(lib.w4_linear_static(_ptr(X), M, K, _ptr(Wq), _ptr(scales), _ptr(offsets), N, group_size, _ptr(Y),
+                                _stream(X)), "w4_linear_static")
+    return Y
 
 
 def w4_device_fault(device=None) -> None:

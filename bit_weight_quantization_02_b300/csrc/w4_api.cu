@@ -236,6 +236,8 @@ cudaError_t encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, co
     return cudaSuccess;
 }
 
+void set_error_detail(const char* msg) { snprintf(g_detail, sizeof g_detail, "%s", msg ? msg : ""); }
+
 cudaError_t resident_blocks(const void* kernel, int threads, size_t smem, int* sms, int* per_sm) {
     static std::mutex mu;
     static std::map<std::tuple<int, const void*, int, size_t>, std::pair<int, int>> cache;

@@ -66,6 +66,9 @@ cudaError_t read_and_clear_skinny_fault(unsigned int* fault);
 // e.g. during CUDA-graph capture, make no CUDA call.
 cudaError_t ensure_kernel_attrs(const void* kernel, int smem_bytes, bool big_clusters);
 
+// Sets the text w4_last_error_detail() returns on this host thread.
+void set_error_detail(const char* msg);
+
 // Encodes a 2-D tiled TMA descriptor for a row-major [outer][inner] tensor
 // (driver entry point fetched once; a host-only call, fine during capture).
 cudaError_t encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,

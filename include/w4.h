@@ -178,6 +178,39 @@ W4_API const char *w4_last_error_detail(void);
 /* W4_FORMAT_VERSION of the built library. */
 W4_API int w4_format_version(void);
 
+/* Bytes of the device array w4_linear_static uses as its workspace. */
+#define W4_STATIC_SCRATCH_BYTES (4u << 20)
+
+/*
+ * w4_linear_static -- w4_linear for callers that cannot allocate device
+ * memory.  The pages have no counterpart: this is an interface convenience,
+ * not part of the method.
+ *
+ * Some callers may not call cudaMalloc or any allocating routine (a plugin
+ * inside another framework that owns every device allocation, a service with
+ * a fixed device-memory budget reserved up front), yet the persistent
+ * stream-K decode kernel needs a workspace.  This entry point runs that kernel
+ * with, as workspace, a W4_STATIC_SCRATCH_BYTES (4 MiB) array that libw4 keeps
+ * in device memory: every GPU that loads the library holds it until the
+ * process exits.  The call itself allocates nothing.  Inputs and outputs are
+ * the caller's, as for w4_linear.
+ *
+ * Limits: M <= 8, K / group_size even, and M*N*4 bytes (rounded up to 256)
+ * plus 4 bytes per 16 rows of N within the array; other sizes fail with
+ * W4_ERR_INVALID_ARG and a message in w4_last_error_detail().
+ * Set-up: the first call on each device, with that device current, looks up
+ * the array's device address (cudaGetSymbolAddress); make that first call
+ * before any stream capture.
+ * Every call clears the part of the array it uses (an asynchronous memset on
+ * `stream`) and then shares the one array with every other call on the same
+ * device: calls that overlap on the GPU (different streams) race and give
+ * wrong results; serialize them.
+ */
+W4_API w4_status w4_linear_static(const uint16_t *X, int64_t M, int64_t K,
+                                  const uint8_t *Wq, const uint16_t *scales,
+                                  const uint16_t *offsets, int64_t N, int group_size,
+                                  uint16_t *Y, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
