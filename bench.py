@@ -347,10 +347,11 @@ def gpu_arm(args):
     dist.close()
 
 
-def other_rows(args, w4, wl, device, stream, peaks, dist):
+def other_rows(args, w4, wl, device, stream, peaks, dist, only=None):
     """Prefill GEMMs, batched decode, the g=128 stack, quantize / dequantize."""
     import torch
     rows = {}
+    want = (lambda name: only is None or only == name)
     flush_buf = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)
 
     def flush():
@@ -358,7 +359,7 @@ def other_rows(args, w4, wl, device, stream, peaks, dist):
 
     # prefill (tcgen05 GEMM), L2 flushed before every timed call
     pre = []
-    for c in wl.config4():
+    for c in (wl.config4() if want("prefill") else []):
         (Wq, sc, of), = quantize_linears([c], device, w4, wl)
         X = wl.gen_activation(c.M, c.K, c.x_seed, device=device)
         Y = torch.empty((c.M, c.N), dtype=torch.bfloat16, device=device)
@@ -371,7 +372,7 @@ def other_rows(args, w4, wl, device, stream, peaks, dist):
                     "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
                     "hbm_gbs": round(linear_bytes(c.M, c.N, c.K, c.group_size) / (t * 1e-3) / 1e9, 1)})
         del Wq, sc, of, X, Y
-    best = max(pre, key=lambda r: r["tflops"])
+    best = max(pre, key=lambda r: r["tflops"]) if pre else {"tflops": 0.0}
     rows["prefill_gemm"] = {"unit": "TFLOP/s", "cases": pre, "kernel": "gemm_kernel (tcgen05, TMEM accumulators)",
                             "roofline": {"bound": "tensor", "achieved": best["tflops"], "peak": peaks["bf16_tflops"],
                                          "unit": "TFLOP/s", "frac": round(best["tflops"] / peaks["bf16_tflops"], 4),
@@ -381,7 +382,7 @@ def other_rows(args, w4, wl, device, stream, peaks, dist):
 
     # batched decode, config 3 (g=64): weights rotated through copies totalling > 4x L2
     b3 = []
-    for c in wl.config3():
+    for c in (wl.config3() if want("batched") else []):
         (Wq, sc, of), = quantize_linears([c], device, w4, wl)
         copies = max(2, int(4 * 126e6 // (c.N * c.K * 0.5625)) + 1)
         reps = [(Wq.clone(), sc.clone(), of.clone()) for _ in range(copies)]
@@ -413,7 +414,7 @@ def other_rows(args, w4, wl, device, stream, peaks, dist):
 
     # full 32-block stack at g=128: quantize every weight, then M=1 and M=16 passes
     torch.cuda.synchronize(device)
-    c5 = wl.config5(1)
+    c5 = wl.config5(1) if want("stack") else []
     t0 = time.perf_counter()
     packed = []
     qbytes = 0
@@ -429,11 +430,13 @@ def other_rows(args, w4, wl, device, stream, peaks, dist):
         qbytes += quantize_bytes(c.N, c.K, c.group_size)
         del W
     setup_s = time.perf_counter() - t0
-    stack_rows = {"quantize": {"weights": wl.config5_weight_count(), "ms": round(q_ms, 3),
-                               "gbs": round(qbytes / (q_ms * 1e-3) / 1e9, 1),
-                               "frac_of_hbm_peak": round(qbytes / (q_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-                               "algorithmic_bytes": qbytes, "setup_s": round(setup_s, 1)}}
-    for M in (1, 16):
+    stack_rows = {}
+    if c5:
+        stack_rows["quantize"] = {"weights": wl.config5_weight_count(), "ms": round(q_ms, 3),
+                                  "gbs": round(qbytes / (q_ms * 1e-3) / 1e9, 1),
+                                  "frac_of_hbm_peak": round(qbytes / (q_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                                  "algorithmic_bytes": qbytes, "setup_s": round(setup_s, 1)}
+    for M in ((1, 16) if c5 else ()):
         cases = wl.config5(M)
         st = LinearStack(cases, device, w4, wl, packed=packed)
         g = st.capture(stream)
@@ -447,6 +450,9 @@ def other_rows(args, w4, wl, device, stream, peaks, dist):
     del packed
 
     # dequantize throughput on the gate/up shape, L2 flushed
+    if not want("dequant"):
+        del flush_buf
+        return rows
     c = wl.config2()[4]
     (Wq, sc, of), = quantize_linears([c], device, w4, wl)
     out = torch.empty((c.N, c.K), dtype=torch.bfloat16, device=device)
@@ -544,6 +550,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--prefill-iters", type=int, default=10)
+    ap.add_argument("--section", choices=["all", "prefill", "batched", "stack", "dequant"], default="all",
+                    help="all = the benchmark; the others run one secondary row alone (for profiling) and print it")
     ap.add_argument("--layers", type=int, default=32,
                     help="Llama-3-8B blocks in the headline step (32 = the whole model; fewer only for profiling)")
     a = ap.parse_args(argv)
@@ -552,10 +560,26 @@ def parse_args(argv=None):
     return a
 
 
+def section_only(args):
+    import torch
+    import bit_weight_quantization_02_b300 as w4
+    from bit_weight_quantization_02_b300 import workloads as wl
+    dist = Dist("nccl")
+    device = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(device)
+    w4.load_library()
+    rows = other_rows(args, w4, wl, device, torch.cuda.Stream(device), load_peaks(), dist, only=args.section)
+    if dist.rank == 0:
+        print(json.dumps({"section": args.section, "rows": rows}), flush=True)
+    dist.close()
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         reference_arm(args)
+    elif args.section != "all":
+        section_only(args)
     else:
         gpu_arm(args)
 

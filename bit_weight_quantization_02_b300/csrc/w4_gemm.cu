@@ -35,6 +35,7 @@ constexpr int GM_STAGES = 3;
 constexpr int GM_DEQ_WARPS = 8;
 constexpr int GM_THREADS = 64 + GM_DEQ_WARPS * 32;
 constexpr int GM_TMEM_COLS = 256;
+constexpr int GM_QPF = 4;  // k blocks of qparams prefetched by each dequantization thread
 
 constexpr int GM_X_BYTES = GM_BM * GM_BK * 2;  // 16 KB
 constexpr int GM_W_BYTES = GM_BN * GM_BK * 2;  // 32 KB
@@ -174,8 +175,30 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         // rows 4..7 of each 8 read their two 16-byte halves in the other order:
         // the 8 lanes of a quarter-warp then hit 8 distinct bank groups
         const int hfirst = (r >> 2) & 1;
+        // scale and offset of this row for the two 32-k halves of a k block, as
+        // (first half | second half << 16); loaded GM_QPF blocks ahead so their
+        // latency hides behind the dequantization of earlier blocks
+        auto qload = [&](int kb) {
+            uint2 q = make_uint2(0u, 0u);
+            if (kb < nkb && nvalid) {
+                const int j0 = (kb * GM_BK) / G;
+                const int j1 = (kb * GM_BK + GM_BK / 2) / G;
+                const uint32_t s0 = j0 < ng ? ldg_nc_u16(scales + qrow + j0) : 0u;
+                const uint32_t o0 = j0 < ng ? ldg_nc_u16(offsets + qrow + j0) : 0u;
+                const uint32_t s1 = (j1 == j0) ? s0 : (j1 < ng ? ldg_nc_u16(scales + qrow + j1) : 0u);
+                const uint32_t o1 = (j1 == j0) ? o0 : (j1 < ng ? ldg_nc_u16(offsets + qrow + j1) : 0u);
+                q = make_uint2(s0 | (s1 << 16), o0 | (o1 << 16));
+            }
+            return q;
+        };
+        uint2 q0 = qload(0), q1 = qload(1), q2 = qload(2), q3 = qload(3);
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
+            const uint2 qc = q0;
+            q0 = q1;
+            q1 = q2;
+            q2 = q3;
+            q3 = qload(kb + GM_QPF);
             const int s = kb % GM_STAGES;
             const uint32_t ph = (kb / GM_STAGES) & 1;
             if (!mbar_wait_bounded(full_tma(s), ph, abort_flag, &g_gemm_fault, 4u, GM_WAIT_LIMIT_NS)) {
@@ -190,20 +213,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             const uint32_t words[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
             unsigned char* wtile = smem + GM_OFF_W + s * GM_W_BYTES;
             const int kbase = kb * GM_BK;
-            uint32_t s2 = 0, o2 = 0;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {  // 8 codes (one 16-byte bf16 chunk) per step
                 const int k = kbase + 8 * c;
-                if ((8 * c) % G == 0) {  // first chunk of a group inside this k block
-                    const int j = k / G;
-                    uint32_t sv = 0, ov = 0;
-                    if (nvalid && j < ng) {
-                        sv = ldg_nc_u16(scales + qrow + j);
-                        ov = ldg_nc_u16(offsets + qrow + j);
-                    }
-                    s2 = sv | (sv << 16);
-                    o2 = ov | (ov << 16);
-                }
+                const uint32_t sel = c < 4 ? 0x1010u : 0x3232u;  // first or second 32-k half of the block
+                const uint32_t s2 = __byte_perm(qc.x, 0, sel), o2 = __byte_perm(qc.y, 0, sel);
                 uint4 out = make_uint4(0u, 0u, 0u, 0u);
                 if (k < K) {
                     const uint32_t w = words[c];
