@@ -8,12 +8,15 @@
 // weight), so the int4 codes are expanded to bf16 on chip and fed to UMMA.
 //
 // One thread block computes a BM x BN = 128 tokens x 256 weight rows tile of
-// Y, walking K in BK = 64 steps through a 3-stage shared-memory ring:
+// Y, walking K in BK = 64 steps.  Two shared-memory rings decouple the stages:
+// a 6-deep TMA ring (X tile + packed codes, 24 KB a step) covers the copy
+// latency, a 2-deep ring of dequantized bf16 weight tiles (32 KB) decouples
+// dequantization from the MMAs.
 //   warp 0      TMA producer: X tile (128 x 64 bf16, 128-byte swizzle) and
-//               the packed code tile (256 rows x 32 bytes) per stage;
+//               the packed code tile (256 rows x 32 bytes) per k step;
 //   warp 1      TMEM owner (alloc/dealloc of 256 fp32 columns) and, on one
 //               lane, the UMMA issuer: 4 x tcgen05.mma (M=128, N=256, K=16)
-//               per stage, tcgen05.commit frees the stage;
+//               per k step; tcgen05.commit frees the TMA and weight stages;
 //   warps 2..9  dequantization: one weight row per thread, codes from the
 //               staged tile -> bf16 w' written straight into the UMMA B
 //               operand layout (K-major, 128-byte swizzle), then
@@ -31,7 +34,8 @@ namespace w4 {
 constexpr int GM_BM = 128;
 constexpr int GM_BN = 256;
 constexpr int GM_BK = 64;
-constexpr int GM_STAGES = 3;
+constexpr int GM_TSTAGES = 6;  // TMA ring: X tile + packed code tile per k block
+constexpr int GM_WSTAGES = 2;  // dequantized bf16 weight tiles (the UMMA B operand)
 constexpr int GM_DEQ_WARPS = 8;
 constexpr int GM_THREADS = 64 + GM_DEQ_WARPS * 32;
 constexpr int GM_TMEM_COLS = 256;
@@ -41,13 +45,15 @@ constexpr int GM_X_BYTES = GM_BM * GM_BK * 2;  // 16 KB
 constexpr int GM_W_BYTES = GM_BN * GM_BK * 2;  // 32 KB
 constexpr int GM_P_BYTES = GM_BN * GM_BK / 2;  //  8 KB
 constexpr int GM_OFF_X = 0;
-constexpr int GM_OFF_W = GM_OFF_X + GM_STAGES * GM_X_BYTES;
-constexpr int GM_OFF_P = GM_OFF_W + GM_STAGES * GM_W_BYTES;
-constexpr int GM_OFF_BAR = GM_OFF_P + GM_STAGES * GM_P_BYTES;
-constexpr int GM_NBAR = 3 * GM_STAGES + 2;  // full_tma, full_deq, empty per stage; tmem_full; drain
+constexpr int GM_OFF_W = GM_OFF_X + GM_TSTAGES * GM_X_BYTES;
+constexpr int GM_OFF_P = GM_OFF_W + GM_WSTAGES * GM_W_BYTES;
+constexpr int GM_OFF_BAR = GM_OFF_P + GM_TSTAGES * GM_P_BYTES;
+// full_tma, empty_tma per TMA stage; full_deq, empty_w per weight stage; tmem_full; drain
+constexpr int GM_NBAR = 2 * GM_TSTAGES + 2 * GM_WSTAGES + 2;
 constexpr int GM_OFF_MISC = GM_OFF_BAR + GM_NBAR * 8;
 constexpr int GM_SMEM_USED = GM_OFF_MISC + 16;
 constexpr int GM_SMEM_BYTES = GM_SMEM_USED + 1024;  // + alignment slack for the 1024-byte swizzle atoms
+static_assert(GM_SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 constexpr uint64_t GM_WAIT_LIMIT_NS = 2000000000ull;   // 2 s per wait
 constexpr uint64_t GM_DRAIN_LIMIT_NS = 1000000000ull;  // 1 s per drain wait
@@ -79,6 +85,40 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
     return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
+// Eight codes of one 32-bit word (k0..k7, k0 in the low nibble) -> eight bf16
+// w' = q*s + o in k order: LOP3 gives the pairs (128+q_i, 128+q_{i+4}), an exact
+// subtract of 128 and one bf16 FMA with the (s,s) and (o,o) pairs dequantize
+// them, four PRMTs restore the order.
+__device__ __forceinline__ uint4 dequant8(uint32_t w, uint32_t s2, uint32_t o2, uint32_t cm, uint32_t cg) {
+    uint4 r;
+    asm("{\n\t.reg .b32 t, p0, p1, p2, p3;\n\t"
+        "lop3.b32 p0, %4, %7, %8, 0xEA;\n\t"
+        "shr.b32 t, %4, 4;\n\t"
+        "lop3.b32 p1, t, %7, %8, 0xEA;\n\t"
+        "shr.b32 t, %4, 8;\n\t"
+        "lop3.b32 p2, t, %7, %8, 0xEA;\n\t"
+        "shr.b32 t, %4, 12;\n\t"
+        "lop3.b32 p3, t, %7, %8, 0xEA;\n\t"
+        "sub.rn.bf16x2 p0, p0, %8;\n\t"
+        "sub.rn.bf16x2 p1, p1, %8;\n\t"
+        "sub.rn.bf16x2 p2, p2, %8;\n\t"
+        "sub.rn.bf16x2 p3, p3, %8;\n\t"
+        "fma.rn.bf16x2 p0, p0, %5, %6;\n\t"
+        "fma.rn.bf16x2 p1, p1, %5, %6;\n\t"
+        "fma.rn.bf16x2 p2, p2, %5, %6;\n\t"
+        "fma.rn.bf16x2 p3, p3, %5, %6;\n\t"
+        "prmt.b32 %0, p0, p1, 0x5410;\n\t"
+        "prmt.b32 %1, p2, p3, 0x5410;\n\t"
+        "prmt.b32 %2, p0, p1, 0x7632;\n\t"
+        "prmt.b32 %3, p2, p3, 0x7632;\n\t}"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "r"(w), "r"(s2), "r"(o2), "r"(cm), "r"(cg));
+    return r;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
 template <int G>
 __global__ void __launch_bounds__(GM_THREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_p,
@@ -88,11 +128,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar0 = sbase + GM_OFF_BAR;
-    auto full_tma = [&](int s) { return bar0 + 8u * s; };
-    auto full_deq = [&](int s) { return bar0 + 8u * (GM_STAGES + s); };
-    auto empty = [&](int s) { return bar0 + 8u * (2 * GM_STAGES + s); };
-    const uint32_t tmem_full = bar0 + 8u * (3 * GM_STAGES);
-    const uint32_t drain = bar0 + 8u * (3 * GM_STAGES + 1);
+    auto full_tma = [&](int t) { return bar0 + 8u * t; };
+    auto empty_tma = [&](int t) { return bar0 + 8u * (GM_TSTAGES + t); };
+    auto full_deq = [&](int w) { return bar0 + 8u * (2 * GM_TSTAGES + w); };
+    auto empty_w = [&](int w) { return bar0 + 8u * (2 * GM_TSTAGES + GM_WSTAGES + w); };
+    const uint32_t tmem_full = bar0 + 8u * (2 * GM_TSTAGES + 2 * GM_WSTAGES);
+    const uint32_t drain = tmem_full + 8u;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + GM_OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + GM_OFF_MISC + 4);
 
@@ -101,10 +142,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     const int nkb = (K + GM_BK - 1) / GM_BK;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < GM_STAGES; ++s) {
-            mbar_init(full_tma(s), 1);
-            mbar_init(full_deq(s), GM_DEQ_WARPS * 32);
-            mbar_init(empty(s), 1);
+        for (int t = 0; t < GM_TSTAGES; ++t) {
+            mbar_init(full_tma(t), 1);
+            mbar_init(empty_tma(t), 1);
+        }
+        for (int w = 0; w < GM_WSTAGES; ++w) {
+            mbar_init(full_deq(w), GM_DEQ_WARPS * 32);
+            mbar_init(empty_w(w), 1);
         }
         mbar_init(tmem_full, 1);
         mbar_init(drain, 1);
@@ -127,17 +171,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             tma_prefetch_desc(&tm_p);
             int issued = 0;
             for (int kb = 0; kb < nkb; ++kb) {
-                const int s = kb % GM_STAGES;
-                const uint32_t ph = (kb / GM_STAGES) & 1;
-                if (!mbar_wait_bounded(empty(s), ph ^ 1, abort_flag, &g_gemm_fault, 1u, GM_WAIT_LIMIT_NS)) break;
-                mbar_arrive_expect_tx(full_tma(s), GM_X_BYTES + GM_P_BYTES);
-                tma_load_2d(sbase + GM_OFF_X + s * GM_X_BYTES, &tm_x, full_tma(s), kb * GM_BK, m0);
-                tma_load_2d(sbase + GM_OFF_P + s * GM_P_BYTES, &tm_p, full_tma(s), kb * (GM_BK / 2), n0);
+                const int t = kb % GM_TSTAGES;
+                const uint32_t ph = (kb / GM_TSTAGES) & 1;
+                if (!mbar_wait_bounded(empty_tma(t), ph ^ 1, abort_flag, &g_gemm_fault, 1u, GM_WAIT_LIMIT_NS)) break;
+                mbar_arrive_expect_tx(full_tma(t), GM_X_BYTES + GM_P_BYTES);
+                tma_load_2d(sbase + GM_OFF_X + t * GM_X_BYTES, &tm_x, full_tma(t), kb * GM_BK, m0);
+                tma_load_2d(sbase + GM_OFF_P + t * GM_P_BYTES, &tm_p, full_tma(t), kb * (GM_BK / 2), n0);
                 ++issued;
             }
             // never leave the block with copies still landing in its shared memory
-            for (int kb = (issued > GM_STAGES ? issued - GM_STAGES : 0); kb < issued; ++kb)
-                mbar_drain_bounded(full_tma(kb % GM_STAGES), (kb / GM_STAGES) & 1, GM_DRAIN_LIMIT_NS);
+            for (int kb = (issued > GM_TSTAGES ? issued - GM_TSTAGES : 0); kb < issued; ++kb)
+                mbar_drain_bounded(full_tma(kb % GM_TSTAGES), (kb / GM_TSTAGES) & 1, GM_DRAIN_LIMIT_NS);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ UMMA issuer
@@ -145,17 +189,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             constexpr uint32_t idesc = gm_idesc();
             int issued = 0;
             for (int kb = 0; kb < nkb; ++kb) {
-                const int s = kb % GM_STAGES;
-                const uint32_t ph = (kb / GM_STAGES) & 1;
-                if (!mbar_wait_bounded(full_tma(s), ph, abort_flag, &g_gemm_fault, 2u, GM_WAIT_LIMIT_NS)) break;
-                if (!mbar_wait_bounded(full_deq(s), ph, abort_flag, &g_gemm_fault, 2u, GM_WAIT_LIMIT_NS)) break;
+                const int t = kb % GM_TSTAGES, w = kb % GM_WSTAGES;
+                const uint32_t pt = (kb / GM_TSTAGES) & 1, pw = (kb / GM_WSTAGES) & 1;
+                if (!mbar_wait_bounded(full_tma(t), pt, abort_flag, &g_gemm_fault, 2u, GM_WAIT_LIMIT_NS)) break;
+                if (!mbar_wait_bounded(full_deq(w), pw, abort_flag, &g_gemm_fault, 2u, GM_WAIT_LIMIT_NS)) break;
                 tc_fence_after();
-                const uint64_t adesc = gm_sdesc(sbase + GM_OFF_X + s * GM_X_BYTES);
-                const uint64_t bdesc = gm_sdesc(sbase + GM_OFF_W + s * GM_W_BYTES);
+                const uint64_t adesc = gm_sdesc(sbase + GM_OFF_X + t * GM_X_BYTES);
+                const uint64_t bdesc = gm_sdesc(sbase + GM_OFF_W + w * GM_W_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < GM_BK / 16; ++kk)  // +32 bytes of K per MMA = +2 in the address field
                     umma_bf16(tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc, (kb | kk) != 0);
-                umma_commit(empty(s));
+                umma_commit(empty_tma(t));  // X and codes of this k block consumed
+                umma_commit(empty_w(w));    // dequantized tile consumed
                 ++issued;
             }
             if (issued == nkb) umma_commit(tmem_full);
@@ -177,7 +222,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         const int hfirst = (r >> 2) & 1;
         // scale and offset of this row for the two 32-k halves of a k block, as
         // (first half | second half << 16); loaded GM_QPF blocks ahead so their
-        // latency hides behind the dequantization of earlier blocks
+        // latency hides behind the dequantization of earlier blocks.  Groups past
+        // K read as 0: with the zero-filled codes those weights are exactly 0.
         auto qload = [&](int kb) {
             uint2 q = make_uint2(0u, 0u);
             if (kb < nkb && nvalid) {
@@ -192,6 +238,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             return q;
         };
         uint2 q0 = qload(0), q1 = qload(1), q2 = qload(2), q3 = qload(3);
+        uint32_t cm, cg;  // LOP3 constants pinned in registers (0x4300 pairs are also the 128.0 bias)
+        asm volatile("mov.b32 %0, %1;" : "=r"(cm) : "r"(0x000F000Fu));
+        asm volatile("mov.b32 %0, %1;" : "=r"(cg) : "r"(0x43004300u));
+        // row r of a 128-byte-swizzled tile: chunk c lives at row_base ^ (c << 4)
+        const uint32_t row_sw = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((r & 7) << 4));
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
             const uint2 qc = q0;
@@ -199,41 +250,27 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             q1 = q2;
             q2 = q3;
             q3 = qload(kb + GM_QPF);
-            const int s = kb % GM_STAGES;
-            const uint32_t ph = (kb / GM_STAGES) & 1;
-            if (!mbar_wait_bounded(full_tma(s), ph, abort_flag, &g_gemm_fault, 4u, GM_WAIT_LIMIT_NS)) {
+            const int t = kb % GM_TSTAGES, w = kb % GM_WSTAGES;
+            const uint32_t pt = (kb / GM_TSTAGES) & 1, pw = (kb / GM_WSTAGES) & 1;
+            if (!mbar_wait_bounded(full_tma(t), pt, abort_flag, &g_gemm_fault, 4u, GM_WAIT_LIMIT_NS) ||
+                !mbar_wait_bounded(empty_w(w), pw ^ 1, abort_flag, &g_gemm_fault, 4u, GM_WAIT_LIMIT_NS)) {
                 ok = false;
                 break;
             }
-            const unsigned char* prow = smem + GM_OFF_P + s * GM_P_BYTES + r * 32;
+            const unsigned char* prow = smem + GM_OFF_P + t * GM_P_BYTES + r * 32;
             const uint4 first = *reinterpret_cast<const uint4*>(prow + 16 * hfirst);
             const uint4 second = *reinterpret_cast<const uint4*>(prow + 16 * (hfirst ^ 1));
             const uint4 h0 = hfirst ? second : first;
             const uint4 h1 = hfirst ? first : second;
             const uint32_t words[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-            unsigned char* wtile = smem + GM_OFF_W + s * GM_W_BYTES;
-            const int kbase = kb * GM_BK;
+            const uint32_t wrow = sbase + GM_OFF_W + w * GM_W_BYTES + row_sw;
+            const uint32_t s_lo = __byte_perm(qc.x, 0, 0x1010), s_hi = __byte_perm(qc.x, 0, 0x3232);
+            const uint32_t o_lo = __byte_perm(qc.y, 0, 0x1010), o_hi = __byte_perm(qc.y, 0, 0x3232);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {  // 8 codes (one 16-byte bf16 chunk) per step
-                const int k = kbase + 8 * c;
-                const uint32_t sel = c < 4 ? 0x1010u : 0x3232u;  // first or second 32-k half of the block
-                const uint32_t s2 = __byte_perm(qc.x, 0, sel), o2 = __byte_perm(qc.y, 0, sel);
-                uint4 out = make_uint4(0u, 0u, 0u, 0u);
-                if (k < K) {
-                    const uint32_t w = words[c];
-                    const uint32_t p04 = dequant_pair(nib_pair_biased(w), s2, o2);        // (k0, k4)
-                    const uint32_t p15 = dequant_pair(nib_pair_biased(w >> 4), s2, o2);   // (k1, k5)
-                    const uint32_t p26 = dequant_pair(nib_pair_biased(w >> 8), s2, o2);   // (k2, k6)
-                    const uint32_t p37 = dequant_pair(nib_pair_biased(w >> 12), s2, o2);  // (k3, k7)
-                    out.x = __byte_perm(p04, p15, 0x5410);  // (k0, k1)
-                    out.y = __byte_perm(p26, p37, 0x5410);  // (k2, k3)
-                    out.z = __byte_perm(p04, p15, 0x7632);  // (k4, k5)
-                    out.w = __byte_perm(p26, p37, 0x7632);  // (k6, k7)
-                }
-                *reinterpret_cast<uint4*>(wtile + sw128_offset(r, c)) = out;
-            }
+            for (int c = 0; c < 8; ++c)  // 8 codes (one 16-byte bf16 chunk) per step
+                sts128(wrow ^ (uint32_t)(c << 4), dequant8(words[c], c < 4 ? s_lo : s_hi, c < 4 ? o_lo : o_hi, cm, cg));
             fence_proxy_async_smem();
-            mbar_arrive(full_deq(s));
+            mbar_arrive(full_deq(w));
         }
         // ----------------------------------------------------------------- epilogue
         if (ok && mbar_wait_bounded(tmem_full, 0, abort_flag, &g_gemm_fault, 8u, GM_WAIT_LIMIT_NS)) {
