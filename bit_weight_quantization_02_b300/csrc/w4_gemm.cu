@@ -22,6 +22,10 @@
 //               operand layout (K-major, 128-byte swizzle), then
 //               fence.proxy.async and an mbarrier arrive; afterwards the same
 //               warps run the epilogue (tcgen05.ld -> bf16 -> global).
+// When a row of scales (or offsets) is a whole number of 16-byte pieces, the
+// producer also copies them by TMA, 8 groups x 256 rows a box, into a 2-deep
+// ring that the dequantization threads read once per 8 groups; otherwise
+// each thread loads its row's values from global memory a few k blocks ahead.
 // Every mbarrier wait is bounded in time; a block that gives up sets the
 // device fault word, waits (bounded) for its own copies and MMAs, frees its
 // tensor memory and exits.
@@ -39,17 +43,21 @@ constexpr int GM_WSTAGES = 2;  // dequantized bf16 weight tiles (the UMMA B oper
 constexpr int GM_DEQ_WARPS = 8;
 constexpr int GM_THREADS = 64 + GM_DEQ_WARPS * 32;
 constexpr int GM_TMEM_COLS = 256;
-constexpr int GM_QPF = 4;  // k blocks of qparams prefetched by each dequantization thread
+constexpr int GM_QPF = 4;  // k blocks of qparams prefetched by each thread (no-TMA variant)
+constexpr int GM_QSTAGES = 2;  // TMA ring of qparam boxes (8 groups x 256 rows of scales and offsets)
 
 constexpr int GM_X_BYTES = GM_BM * GM_BK * 2;  // 16 KB
 constexpr int GM_W_BYTES = GM_BN * GM_BK * 2;  // 32 KB
 constexpr int GM_P_BYTES = GM_BN * GM_BK / 2;  //  8 KB
+constexpr int GM_QBOX_BYTES = GM_BN * 16;      //  4 KB: 8 bf16 per row
 constexpr int GM_OFF_X = 0;
 constexpr int GM_OFF_W = GM_OFF_X + GM_TSTAGES * GM_X_BYTES;
 constexpr int GM_OFF_P = GM_OFF_W + GM_WSTAGES * GM_W_BYTES;
-constexpr int GM_OFF_BAR = GM_OFF_P + GM_TSTAGES * GM_P_BYTES;
-// full_tma, empty_tma per TMA stage; full_deq, empty_w per weight stage; tmem_full; drain
-constexpr int GM_NBAR = 2 * GM_TSTAGES + 2 * GM_WSTAGES + 2;
+constexpr int GM_OFF_Q = GM_OFF_P + GM_TSTAGES * GM_P_BYTES;  // per stage: scales box, offsets box
+constexpr int GM_OFF_BAR = GM_OFF_Q + GM_QSTAGES * 2 * GM_QBOX_BYTES;
+// full_tma, empty_tma per TMA stage; full_deq, empty_w per weight stage;
+// full_q, empty_q per qparam stage; tmem_full; drain
+constexpr int GM_NBAR = 2 * GM_TSTAGES + 2 * GM_WSTAGES + 2 * GM_QSTAGES + 2;
 constexpr int GM_OFF_MISC = GM_OFF_BAR + GM_NBAR * 8;
 constexpr int GM_SMEM_USED = GM_OFF_MISC + 16;
 constexpr int GM_SMEM_BYTES = GM_SMEM_USED + 1024;  // + alignment slack for the 1024-byte swizzle atoms
@@ -119,11 +127,24 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
     asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
-template <int G>
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint32_t pick_word(const uint4& v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// QT: scales and offsets arrive by TMA (tm_s, tm_o); otherwise the
+// dequantization threads load them from `scales` / `offsets`.
+template <int G, bool QT>
 __global__ void __launch_bounds__(GM_THREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_p,
+            const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_o,
             const uint16_t* __restrict__ scales, const uint16_t* __restrict__ offsets, uint16_t* __restrict__ Y,
             int M, int N, int K) {
+    constexpr int QSPAN = 8 * G / GM_BK;  // k blocks covered by one qparam box (8 groups)
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -132,7 +153,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     auto empty_tma = [&](int t) { return bar0 + 8u * (GM_TSTAGES + t); };
     auto full_deq = [&](int w) { return bar0 + 8u * (2 * GM_TSTAGES + w); };
     auto empty_w = [&](int w) { return bar0 + 8u * (2 * GM_TSTAGES + GM_WSTAGES + w); };
-    const uint32_t tmem_full = bar0 + 8u * (2 * GM_TSTAGES + 2 * GM_WSTAGES);
+    auto full_q = [&](int q) { return bar0 + 8u * (2 * GM_TSTAGES + 2 * GM_WSTAGES + q); };
+    auto empty_q = [&](int q) { return bar0 + 8u * (2 * GM_TSTAGES + 2 * GM_WSTAGES + GM_QSTAGES + q); };
+    const uint32_t tmem_full = bar0 + 8u * (2 * GM_TSTAGES + 2 * GM_WSTAGES + 2 * GM_QSTAGES);
     const uint32_t drain = tmem_full + 8u;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + GM_OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + GM_OFF_MISC + 4);
@@ -149,6 +172,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         for (int w = 0; w < GM_WSTAGES; ++w) {
             mbar_init(full_deq(w), GM_DEQ_WARPS * 32);
             mbar_init(empty_w(w), 1);
+        }
+        for (int q = 0; q < GM_QSTAGES; ++q) {
+            mbar_init(full_q(q), 1);
+            mbar_init(empty_q(q), GM_DEQ_WARPS * 32);
         }
         mbar_init(tmem_full, 1);
         mbar_init(drain, 1);
@@ -169,8 +196,22 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         if (lane == 0) {
             tma_prefetch_desc(&tm_x);
             tma_prefetch_desc(&tm_p);
-            int issued = 0;
+            if (QT) {
+                tma_prefetch_desc(&tm_s);
+                tma_prefetch_desc(&tm_o);
+            }
+            int issued = 0, q_issued = 0;
             for (int kb = 0; kb < nkb; ++kb) {
+                if (QT && kb % QSPAN == 0) {  // scales and offsets of groups 8u .. 8u+7
+                    const int u = kb / QSPAN, q = u % GM_QSTAGES;
+                    const uint32_t pq = (u / GM_QSTAGES) & 1;
+                    if (!mbar_wait_bounded(empty_q(q), pq ^ 1, abort_flag, &g_gemm_fault, 1u, GM_WAIT_LIMIT_NS)) break;
+                    mbar_arrive_expect_tx(full_q(q), 2 * GM_QBOX_BYTES);
+                    const uint32_t qdst = sbase + GM_OFF_Q + q * 2 * GM_QBOX_BYTES;
+                    tma_load_2d(qdst, &tm_s, full_q(q), 8 * u, n0);
+                    tma_load_2d(qdst + GM_QBOX_BYTES, &tm_o, full_q(q), 8 * u, n0);
+                    ++q_issued;
+                }
                 const int t = kb % GM_TSTAGES;
                 const uint32_t ph = (kb / GM_TSTAGES) & 1;
                 if (!mbar_wait_bounded(empty_tma(t), ph ^ 1, abort_flag, &g_gemm_fault, 1u, GM_WAIT_LIMIT_NS)) break;
@@ -182,6 +223,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             // never leave the block with copies still landing in its shared memory
             for (int kb = (issued > GM_TSTAGES ? issued - GM_TSTAGES : 0); kb < issued; ++kb)
                 mbar_drain_bounded(full_tma(kb % GM_TSTAGES), (kb / GM_TSTAGES) & 1, GM_DRAIN_LIMIT_NS);
+            for (int u = (q_issued > GM_QSTAGES ? q_issued - GM_QSTAGES : 0); u < q_issued; ++u)
+                mbar_drain_bounded(full_q(u % GM_QSTAGES), (u / GM_QSTAGES) & 1, GM_DRAIN_LIMIT_NS);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ UMMA issuer
@@ -220,36 +263,56 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         // rows 4..7 of each 8 read their two 16-byte halves in the other order:
         // the 8 lanes of a quarter-warp then hit 8 distinct bank groups
         const int hfirst = (r >> 2) & 1;
-        // scale and offset of this row for the two 32-k halves of a k block, as
-        // (first half | second half << 16); loaded GM_QPF blocks ahead so their
-        // latency hides behind the dequantization of earlier blocks.  Groups past
-        // K read as 0: with the zero-filled codes those weights are exactly 0.
+        // scale and offset of this row for the two 32-k halves of a k block,
+        // loaded GM_QPF blocks ahead and kept raw (not combined) until used, so
+        // that no instruction waits on them before their block comes up.
+        // Groups past K read as 0: with the zero-filled codes those weights are
+        // exactly 0.  With G >= GM_BK both halves share one group.
+        constexpr bool one_group = G >= GM_BK;
+        struct QRaw {
+            uint32_t s0, s1, o0, o1;
+        };
         auto qload = [&](int kb) {
-            uint2 q = make_uint2(0u, 0u);
-            if (kb < nkb && nvalid) {
+            QRaw q = {0u, 0u, 0u, 0u};
+            if (!QT && kb < nkb && nvalid) {
                 const int j0 = (kb * GM_BK) / G;
-                const int j1 = (kb * GM_BK + GM_BK / 2) / G;
-                const uint32_t s0 = j0 < ng ? ldg_nc_u16(scales + qrow + j0) : 0u;
-                const uint32_t o0 = j0 < ng ? ldg_nc_u16(offsets + qrow + j0) : 0u;
-                const uint32_t s1 = (j1 == j0) ? s0 : (j1 < ng ? ldg_nc_u16(scales + qrow + j1) : 0u);
-                const uint32_t o1 = (j1 == j0) ? o0 : (j1 < ng ? ldg_nc_u16(offsets + qrow + j1) : 0u);
-                q = make_uint2(s0 | (s1 << 16), o0 | (o1 << 16));
+                if (j0 < ng) {
+                    q.s0 = ldg_nc_u16(scales + qrow + j0);
+                    q.o0 = ldg_nc_u16(offsets + qrow + j0);
+                }
+                if (!one_group && j0 + 1 < ng) {
+                    q.s1 = ldg_nc_u16(scales + qrow + j0 + 1);
+                    q.o1 = ldg_nc_u16(offsets + qrow + j0 + 1);
+                }
             }
             return q;
         };
-        uint2 q0 = qload(0), q1 = qload(1), q2 = qload(2), q3 = qload(3);
+        QRaw q0 = qload(0), q1 = qload(1), q2 = qload(2), q3 = qload(3);
         uint32_t cm, cg;  // LOP3 constants pinned in registers (0x4300 pairs are also the 128.0 bias)
         asm volatile("mov.b32 %0, %1;" : "=r"(cm) : "r"(0x000F000Fu));
         asm volatile("mov.b32 %0, %1;" : "=r"(cg) : "r"(0x43004300u));
         // row r of a 128-byte-swizzled tile: chunk c lives at row_base ^ (c << 4)
         const uint32_t row_sw = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((r & 7) << 4));
+        uint4 sq = make_uint4(0u, 0u, 0u, 0u), oq = sq;  // TMA variant: this row's 8 groups
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
-            const uint2 qc = q0;
+            const QRaw qc = q0;
             q0 = q1;
             q1 = q2;
             q2 = q3;
             q3 = qload(kb + GM_QPF);
+            if (QT && kb % QSPAN == 0) {
+                const int u = kb / QSPAN, q = u % GM_QSTAGES;
+                if (!mbar_wait_bounded(full_q(q), (u / GM_QSTAGES) & 1, abort_flag, &g_gemm_fault, 4u,
+                                       GM_WAIT_LIMIT_NS)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t qsrc = sbase + GM_OFF_Q + q * 2 * GM_QBOX_BYTES + r * 16;
+                sq = lds128(qsrc);
+                oq = lds128(qsrc + GM_QBOX_BYTES);
+                mbar_arrive(empty_q(q));
+            }
             const int t = kb % GM_TSTAGES, w = kb % GM_WSTAGES;
             const uint32_t pt = (kb / GM_TSTAGES) & 1, pw = (kb / GM_WSTAGES) & 1;
             if (!mbar_wait_bounded(full_tma(t), pt, abort_flag, &g_gemm_fault, 4u, GM_WAIT_LIMIT_NS) ||
@@ -264,8 +327,26 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             const uint4 h1 = hfirst ? first : second;
             const uint32_t words[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
             const uint32_t wrow = sbase + GM_OFF_W + w * GM_W_BYTES + row_sw;
-            const uint32_t s_lo = __byte_perm(qc.x, 0, 0x1010), s_hi = __byte_perm(qc.x, 0, 0x3232);
-            const uint32_t o_lo = __byte_perm(qc.y, 0, 0x1010), o_hi = __byte_perm(qc.y, 0, 0x3232);
+            uint32_t s_lo, s_hi, o_lo, o_hi;  // (s,s) and (o,o) bf16 pairs of the two 32-k halves
+            if (QT) {
+                const int j0 = (kb % QSPAN) * GM_BK / G;  // group of the first half among the box's 8
+                const uint32_t sw = pick_word(sq, j0 >> 1), ow = pick_word(oq, j0 >> 1);
+                if (one_group) {
+                    const uint32_t sel = (j0 & 1) ? 0x3232u : 0x1010u;
+                    s_lo = s_hi = __byte_perm(sw, 0, sel);
+                    o_lo = o_hi = __byte_perm(ow, 0, sel);
+                } else {  // G == 32: the word holds exactly the two halves' groups
+                    s_lo = __byte_perm(sw, 0, 0x1010);
+                    s_hi = __byte_perm(sw, 0, 0x3232);
+                    o_lo = __byte_perm(ow, 0, 0x1010);
+                    o_hi = __byte_perm(ow, 0, 0x3232);
+                }
+            } else {
+                s_lo = __byte_perm(qc.s0, 0, 0x1010);
+                o_lo = __byte_perm(qc.o0, 0, 0x1010);
+                s_hi = one_group ? s_lo : __byte_perm(qc.s1, 0, 0x1010);
+                o_hi = one_group ? o_lo : __byte_perm(qc.o1, 0, 0x1010);
+            }
 #pragma unroll
             for (int c = 0; c < 8; ++c)  // 8 codes (one 16-byte bf16 chunk) per step
                 sts128(wrow ^ (uint32_t)(c << 4), dequant8(words[c], c < 4 ? s_lo : s_hi, c < 4 ? o_lo : o_hi, cm, cg));
@@ -315,14 +396,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
 
 // ------------------------------------------------------------------ host side
 
-template <int G>
-static cudaError_t launch_gemm_g(const CUtensorMap& tx, const CUtensorMap& tp, const uint16_t* scales,
-                                 const uint16_t* offsets, uint16_t* Y, int M, int N, int K, cudaStream_t stream) {
-    auto kern = gemm_kernel<G>;
+template <int G, bool QT>
+static cudaError_t launch_gemm_g(const CUtensorMap& tx, const CUtensorMap& tp, const CUtensorMap& ts,
+                                 const CUtensorMap& to, const uint16_t* scales, const uint16_t* offsets, uint16_t* Y,
+                                 int M, int N, int K, cudaStream_t stream) {
+    auto kern = gemm_kernel<G, QT>;
     cudaError_t e = ensure_kernel_attrs(reinterpret_cast<const void*>(kern), GM_SMEM_BYTES, false);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((N + GM_BN - 1) / GM_BN), (unsigned)((M + GM_BM - 1) / GM_BM));
-    kern<<<grid, GM_THREADS, GM_SMEM_BYTES, stream>>>(tx, tp, scales, offsets, Y, M, N, K);
+    kern<<<grid, GM_THREADS, GM_SMEM_BYTES, stream>>>(tx, tp, ts, to, scales, offsets, Y, M, N, K);
     return cudaGetLastError();
 }
 
@@ -342,10 +424,30 @@ cudaError_t launch_gemm(const uint16_t* X, int64_t M, int64_t K, const uint8_t* 
     e = encode_tensor_map_2d(&tp, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)(K / 2), (uint64_t)N, (uint64_t)(K / 2),
                              GM_BK / 2, GM_BN, CU_TENSOR_MAP_SWIZZLE_NONE, detail);
     if (e != cudaSuccess) return e;
+    // scales / offsets: [N][K/g] bf16, box 256 rows x 8 groups, when a row is
+    // a whole number of 16-byte pieces (the tensor-map stride rule)
+    const int64_t ng = K / g;
+    const bool qt = ng % 8 == 0;
+    CUtensorMap ts = tp, to = tp;
+    if (qt) {
+        e = encode_tensor_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, (uint64_t)ng, (uint64_t)N,
+                                 (uint64_t)ng * 2, 8, GM_BN, CU_TENSOR_MAP_SWIZZLE_NONE, detail);
+        if (e == cudaSuccess)
+            e = encode_tensor_map_2d(&to, CU_TENSOR_MAP_DATA_TYPE_UINT16, offsets, (uint64_t)ng, (uint64_t)N,
+                                     (uint64_t)ng * 2, 8, GM_BN, CU_TENSOR_MAP_SWIZZLE_NONE, detail);
+        if (e != cudaSuccess) return e;
+    }
+    const int m = (int)M, n = (int)N, k = (int)K;
     switch (g) {
-        case 32: return launch_gemm_g<32>(tx, tp, scales, offsets, Y, (int)M, (int)N, (int)K, stream);
-        case 64: return launch_gemm_g<64>(tx, tp, scales, offsets, Y, (int)M, (int)N, (int)K, stream);
-        default: return launch_gemm_g<128>(tx, tp, scales, offsets, Y, (int)M, (int)N, (int)K, stream);
+        case 32:
+            return qt ? launch_gemm_g<32, true>(tx, tp, ts, to, scales, offsets, Y, m, n, k, stream)
+                      : launch_gemm_g<32, false>(tx, tp, ts, to, scales, offsets, Y, m, n, k, stream);
+        case 64:
+            return qt ? launch_gemm_g<64, true>(tx, tp, ts, to, scales, offsets, Y, m, n, k, stream)
+                      : launch_gemm_g<64, false>(tx, tp, ts, to, scales, offsets, Y, m, n, k, stream);
+        default:
+            return qt ? launch_gemm_g<128, true>(tx, tp, ts, to, scales, offsets, Y, m, n, k, stream)
+                      : launch_gemm_g<128, false>(tx, tp, ts, to, scales, offsets, Y, m, n, k, stream);
     }
 }
 

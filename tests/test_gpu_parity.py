@@ -180,7 +180,7 @@ def test_linear_stream(g, nk):
 
 
 GEMM_M = [1, 33, 127, 129, 300]
-GEMM_NK = [(200, 4160), (520, 512), (256, 64), (1000, 96)]
+GEMM_NK = [(200, 4160), (520, 512), (256, 64), (1000, 96), (136, 3072), (384, 4096)]
 
 
 @pytest.mark.parametrize("g", [32, 64, 128])
