@@ -23,10 +23,17 @@
 //    exact subtract + one bf16 FMA, mma.m16n8k16 with the weights as the A
 //    operand and the tokens as B (swap AB).
 //  * A warp that covers all of a row tile's k writes bf16 Y directly.  A tile
-//    split between warps is summed in fp32 with red.add in the caller's
+//    split between warps is summed in fp32 with atomic adds in the caller's
 //    workspace; the warp that completes the tile's k count (atomic counter,
-//    no waiting) converts the sum to bf16 and zeroes what it used, so the
-//    workspace is all zeros again after every call.
+//    no waiting) takes each sum and puts back zero in one atomic exchange and
+//    writes bf16 Y, so the workspace is all zeros again after every call.
+//    Ordering without a memory fence (a fence here cost ~1.5 us a launch):
+//    a contributor's adds return their old values and a warp vote reads
+//    them before lane 0 bumps the counter, so every add has been performed
+//    at the L2 point of coherence before the counter shows it; the last
+//    contributor's exchanges are issued after its counter atomic returned,
+//    hence after every add.  All of these are .gpu-scope atomics, performed
+//    at L2 in the order they are issued against each address.
 #include "w4_device.cuh"
 #include "w4_internal.h"
 
@@ -340,30 +347,30 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                     if (m < p.M && n < p.N) p.Y[(int64_t)m * p.N + n] = (uint16_t)float_to_bf16_bits(acc[i]);
                 }
             } else {
+                float got = 0.f;  // old values returned by the adds (only their arrival matters)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int m = m0 + (i & 1), n = (i < 2) ? n_a : n_b;
-                    if (m < p.M && n < p.N) atomicAdd(p.ws + (int64_t)m * p.N + n, acc[i]);
+                    if (m < p.M && n < p.N) got += atomicAdd(p.ws + (int64_t)m * p.N + n, acc[i]);
                 }
-                __threadfence();
-                __syncwarp();
+                // the vote reads every lane's `got`, so all adds have returned before the counter
+                // moves; threadIdx.y is 0 in this one-dimensional block, so `done` is always 1
+                const unsigned int dep = __float_as_uint(got) & (0u - threadIdx.y);
+                const unsigned int done = __all_sync(0xffffffffu, dep == 0u);
                 unsigned int last = 0;
                 if (lane == 0) {
-                    const unsigned int mine = (unsigned int)(kc - kc_first + 1);
+                    const unsigned int mine = (unsigned int)(kc - kc_first + 1) * done;
                     last = (atomicAdd(p.count + tile, mine) + mine == (unsigned int)p.nkc);
                 }
                 last = __shfl_sync(0xffffffffu, last, 0);
                 if (last) {
-                    __threadfence();
                     for (int i = lane; i < 16 * p.M; i += 32) {
                         const int m = i >> 4, n = tile * 16 + (i & 15);
-                        if (n < p.N) {
-                            float* w = p.ws + (int64_t)m * p.N + n;
-                            p.Y[(int64_t)m * p.N + n] = (uint16_t)float_to_bf16_bits(__ldcg(w));
-                            *w = 0.0f;
-                        }
+                        if (n < p.N)
+                            p.Y[(int64_t)m * p.N + n] =
+                                (uint16_t)float_to_bf16_bits(atomicExch(p.ws + (int64_t)m * p.N + n, 0.0f));
                     }
-                    if (lane == 0) p.count[tile] = 0u;
+                    if (lane == 0) atomicExch(p.count + tile, 0u);
                 }
             }
             acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
