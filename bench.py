@@ -279,9 +279,10 @@ def gpu_arm(args):
     units = stack.bytes * args.steps * dist.world
     value = units / (ms * 1e-3) / 1e9
     launches = len(cases) * args.steps
-    # dominant kernel: the skinny decode kernel is the only kernel of the step
+    # dominant kernel: the stream-K decode kernel is the only kernel of the step (M=1
+    # always takes it), so its average launch is the step time over the launches
     achieved = stack.bytes / (step_ms * 1e-3) / 1e9
-    tr = traffic.get(("skinny_kernel", "llama3_8b_decode_step"))
+    tr = traffic.get(("stream_kernel", "llama3_8b_decode_step"))
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4),
                 "traffic": (round(tr / len(cases)) if tr is not None else None),
@@ -347,6 +348,38 @@ def gpu_arm(args):
     dist.close()
 
 
+def _rotated_graph_row(c, w4, wl, device, stream, dist, peaks):
+    """Time one linear shape: a graph of back-to-back w4_linear calls over weight copies
+    totalling more than 4x L2 (so every call streams its weights from HBM)."""
+    import torch
+    (Wq, sc, of), = quantize_linears([c], device, w4, wl)
+    copies = max(2, int(4 * 126e6 // (c.N * c.K * 0.5625)) + 1)
+    reps = [(Wq.clone(), sc.clone(), of.clone()) for _ in range(copies)]
+    X = wl.gen_activation(c.M, c.K, c.x_seed, device=device)
+    Y = torch.empty((c.M, c.N), dtype=torch.bfloat16, device=device)
+    ws = w4.Workspace(device).reserve_for(c.M, c.N, c.K, c.group_size)
+    it = {"i": 0}
+
+    def one():
+        r = reps[it["i"] % copies]
+        it["i"] += 1
+        w4.w4_linear(X, *r, c.group_size, out=Y, workspace=ws)
+
+    with torch.cuda.stream(stream):
+        g = torch.cuda.CUDAGraph()
+        one()
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(copies):
+                one()
+        t = time_region(g.replay, 20, 3, stream, dist, device) / (20 * copies)
+    gbs = linear_bytes(c.M, c.N, c.K, c.group_size) / (t * 1e-3) / 1e9
+    del reps, Wq, sc, of, g
+    return {"M": c.M, "N": c.N, "K": c.K, "g": c.group_size, "us": round(t * 1e3, 2), "gbs": round(gbs, 1),
+            "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
+            "tflops": round(2 * c.M * c.N * c.K / (t * 1e-3) / 1e12, 2)}
+
+
 def other_rows(args, w4, wl, device, stream, peaks, dist, only=None):
     """Prefill GEMMs, batched decode, the g=128 stack, quantize / dequantize."""
     import torch
@@ -380,35 +413,21 @@ def other_rows(args, w4, wl, device, stream, peaks, dist, only=None):
                                          "peak_source": "MEASURED_PEAKS bf16_tflops (burst, kernel timed alone)"},
                             "l2": "flushed (512 MB write) before every timed call"}
 
+    # per-linear decode: each distinct Llama-3-8B shape at M=1 g=32, weights
+    # rotated through copies totalling > 4x L2, back-to-back calls in a graph
+    seen, dshape = set(), []
+    for c in (wl.config2(0) if want("shapes") else []):
+        if (c.N, c.K) in seen:
+            continue
+        seen.add((c.N, c.K))
+        dshape.append(_rotated_graph_row(c, w4, wl, device, stream, dist, peaks))
+    rows["decode_shapes_g32"] = {"unit": "GB/s", "cases": dshape,
+                                 "l2": "graph of back-to-back calls over weight copies totalling > 4x L2"}
+
     # batched decode, config 3 (g=64): weights rotated through copies totalling > 4x L2
     b3 = []
     for c in (wl.config3() if want("batched") else []):
-        (Wq, sc, of), = quantize_linears([c], device, w4, wl)
-        copies = max(2, int(4 * 126e6 // (c.N * c.K * 0.5625)) + 1)
-        reps = [(Wq.clone(), sc.clone(), of.clone()) for _ in range(copies)]
-        X = wl.gen_activation(c.M, c.K, c.x_seed, device=device)
-        Y = torch.empty((c.M, c.N), dtype=torch.bfloat16, device=device)
-        ws = w4.Workspace(device).reserve_for(c.M, c.N, c.K, c.group_size)
-        it = {"i": 0}
-
-        def one():
-            r = reps[it["i"] % copies]
-            it["i"] += 1
-            w4.w4_linear(X, *r, c.group_size, out=Y, workspace=ws)
-
-        with torch.cuda.stream(stream):
-            g = torch.cuda.CUDAGraph()
-            one()
-            stream.synchronize()
-            with torch.cuda.graph(g, stream=stream):
-                for _ in range(copies):
-                    one()
-            t = time_region(g.replay, 20, 3, stream, dist, device) / (20 * copies)
-        gbs = linear_bytes(c.M, c.N, c.K, c.group_size) / (t * 1e-3) / 1e9
-        b3.append({"M": c.M, "N": c.N, "K": c.K, "us": round(t * 1e3, 2), "gbs": round(gbs, 1),
-                   "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
-                   "tflops": round(2 * c.M * c.N * c.K / (t * 1e-3) / 1e12, 2)})
-        del reps, Wq, sc, of, g
+        b3.append(_rotated_graph_row(c, w4, wl, device, stream, dist, peaks))
     rows["batched_decode_g64"] = {"unit": "GB/s", "cases": b3,
                                   "l2": "graph of back-to-back calls over weight copies totalling > 4x L2"}
 
@@ -550,7 +569,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--prefill-iters", type=int, default=10)
-    ap.add_argument("--section", choices=["all", "prefill", "batched", "stack", "dequant"], default="all",
+    ap.add_argument("--section", choices=["all", "prefill", "shapes", "batched", "stack", "dequant"], default="all",
                     help="all = the benchmark; the others run one secondary row alone (for profiling) and print it")
     ap.add_argument("--layers", type=int, default=32,
                     help="Llama-3-8B blocks in the headline step (32 = the whole model; fewer only for profiling)")
