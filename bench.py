@@ -181,11 +181,15 @@ class LinearStack:
     """Packed weights, inputs and outputs of a sequence of linears, with all X in
     one device buffer and all Y in another (one copy each way per step)."""
 
-    def __init__(self, cases, device, w4, wl, packed=None):
+    def __init__(self, cases, device, w4, wl, packed=None, layout="canonical"):
         import torch
         self.cases = cases
         self.device = device
         self.packed = packed if packed is not None else quantize_linears(cases, device, w4, wl)
+        self.layout = layout
+        # decode layout: the same weights rearranged once by w4_repack (not timed)
+        self.repacked = ([w4.w4_repack(Wq, sc, of, c.group_size) for c, (Wq, sc, of) in zip(cases, self.packed)]
+                         if layout == "decode" else None)
         xs = sum(c.M * c.K for c in cases)
         ys = sum(c.M * c.N for c in cases)
         self.X = torch.empty(xs, dtype=torch.bfloat16, device=device)
@@ -205,6 +209,10 @@ class LinearStack:
         self.w4 = w4
 
     def run(self):
+        if self.repacked is not None:
+            for x, y, rp in zip(self.xv, self.yv, self.repacked):
+                self.w4.w4_linear_repacked(x, rp, out=y, workspace=self.ws)
+            return
         for c, x, y, (Wq, sc, of) in zip(self.cases, self.xv, self.yv, self.packed):
             self.w4.w4_linear(x, Wq, sc, of, c.group_size, out=y, workspace=self.ws)
 
@@ -322,7 +330,20 @@ def gpu_arm(args):
 
     rows = {}
     if not args.headline_only:
-        rows = other_rows(args, w4, wl, device, stream, peaks, dist)
+        # the same step on the same weights rearranged once by w4_repack (decode layout)
+        dl = LinearStack(cases, device, w4, wl, packed=stack.packed, layout="decode")
+        dl_graph = dl.capture(stream)
+        with torch.cuda.stream(stream):
+            dl_ms = time_region(dl_graph.replay, args.steps, args.warmup, stream, dist, device)
+        dl_gbs = dl.bytes * args.steps * dist.world / (dl_ms * 1e-3) / 1e9
+        rows["decode_layout_step"] = {"unit": "GB/s", "value": round(dl_gbs, 1),
+                                      "ms_per_step": round(dl_ms / args.steps, 4),
+                                      "frac_of_hbm_peak": round(dl_gbs / peaks["hbm_gbs"], 4),
+                                      "kernel": "decode_kernel (w4_linear_repacked)",
+                                      "how": "the headline step with every weight in the decode layout "
+                                             "(w4_repack once, untimed), CUDA graph of the 224 calls"}
+        del dl_graph, dl
+        rows.update(other_rows(args, w4, wl, device, stream, peaks, dist))
 
     step_bytes = stack.bytes
     del graph, stack
@@ -348,13 +369,17 @@ def gpu_arm(args):
     dist.close()
 
 
-def _rotated_graph_row(c, w4, wl, device, stream, dist, peaks):
-    """Time one linear shape: a graph of back-to-back w4_linear calls over weight copies
-    totalling more than 4x L2 (so every call streams its weights from HBM)."""
+def _rotated_graph_row(c, w4, wl, device, stream, dist, peaks, layout="canonical"):
+    """Time one linear shape: a graph of back-to-back calls over weight copies totalling
+    more than 4x L2 (so every call streams its weights from HBM); `layout` "decode" times
+    w4_linear_repacked on w4_repack's rearrangement of the same weights."""
     import torch
     (Wq, sc, of), = quantize_linears([c], device, w4, wl)
     copies = max(2, int(4 * 126e6 // (c.N * c.K * 0.5625)) + 1)
-    reps = [(Wq.clone(), sc.clone(), of.clone()) for _ in range(copies)]
+    if layout == "decode":
+        reps = [w4.w4_repack(Wq, sc, of, c.group_size) for _ in range(copies)]
+    else:
+        reps = [(Wq.clone(), sc.clone(), of.clone()) for _ in range(copies)]
     X = wl.gen_activation(c.M, c.K, c.x_seed, device=device)
     Y = torch.empty((c.M, c.N), dtype=torch.bfloat16, device=device)
     ws = w4.Workspace(device).reserve_for(c.M, c.N, c.K, c.group_size)
@@ -363,7 +388,10 @@ def _rotated_graph_row(c, w4, wl, device, stream, dist, peaks):
     def one():
         r = reps[it["i"] % copies]
         it["i"] += 1
-        w4.w4_linear(X, *r, c.group_size, out=Y, workspace=ws)
+        if layout == "decode":
+            w4.w4_linear_repacked(X, r, out=Y, workspace=ws)
+        else:
+            w4.w4_linear(X, *r, c.group_size, out=Y, workspace=ws)
 
     with torch.cuda.stream(stream):
         g = torch.cuda.CUDAGraph()
@@ -375,7 +403,8 @@ def _rotated_graph_row(c, w4, wl, device, stream, dist, peaks):
         t = time_region(g.replay, 20, 3, stream, dist, device) / (20 * copies)
     gbs = linear_bytes(c.M, c.N, c.K, c.group_size) / (t * 1e-3) / 1e9
     del reps, Wq, sc, of, g
-    return {"M": c.M, "N": c.N, "K": c.K, "g": c.group_size, "us": round(t * 1e3, 2), "gbs": round(gbs, 1),
+    return {"M": c.M, "N": c.N, "K": c.K, "g": c.group_size, "layout": layout, "us": round(t * 1e3, 2),
+            "gbs": round(gbs, 1),
             "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
             "tflops": round(2 * c.M * c.N * c.K / (t * 1e-3) / 1e12, 2)}
 
@@ -421,6 +450,7 @@ def other_rows(args, w4, wl, device, stream, peaks, dist, only=None):
             continue
         seen.add((c.N, c.K))
         dshape.append(_rotated_graph_row(c, w4, wl, device, stream, dist, peaks))
+        dshape.append(_rotated_graph_row(c, w4, wl, device, stream, dist, peaks, layout="decode"))
     rows["decode_shapes_g32"] = {"unit": "GB/s", "cases": dshape,
                                  "l2": "graph of back-to-back calls over weight copies totalling > 4x L2"}
 
@@ -428,6 +458,8 @@ def other_rows(args, w4, wl, device, stream, peaks, dist, only=None):
     b3 = []
     for c in (wl.config3() if want("batched") else []):
         b3.append(_rotated_graph_row(c, w4, wl, device, stream, dist, peaks))
+        if c.M <= 8:
+            b3.append(_rotated_graph_row(c, w4, wl, device, stream, dist, peaks, layout="decode"))
     rows["batched_decode_g64"] = {"unit": "GB/s", "cases": b3,
                                   "l2": "graph of back-to-back calls over weight copies totalling > 4x L2"}
 

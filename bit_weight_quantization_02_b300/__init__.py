@@ -17,7 +17,8 @@ import torch
 
 __all__ = [
     "W4Error", "W4_FORMAT_VERSION", "KERNEL_AUTO", "KERNEL_SKINNY", "KERNEL_GEMM", "KERNEL_SKINNY_CLUSTER",
-    "KERNEL_STREAM", "Workspace", "w4_linear_workspace_bytes",
+    "KERNEL_STREAM", "Workspace", "w4_linear_workspace_bytes", "Repacked", "w4_repacked_bytes", "w4_repack",
+    "w4_linear_repacked",
     "library_path", "load_library", "w4_quantize", "w4_dequantize", "w4_linear",
     "w4_linear_ex", "w4_packed_bytes", "w4_qparam_bytes", "w4_device_fault", "w4_format_version",
 ]
@@ -67,6 +68,9 @@ def load_library():
             "w4_last_error_detail": ([], ctypes.c_char_p),
             "w4_format_version": ([], i32),
             "w4_linear_static": ([p, i64, i64, p, p, p, i64, i32, p, p], i32),
+            "w4_repacked_bytes": ([i64, i64, i32], sz),
+            "w4_repack": ([p, p, p, i64, i64, i32, p, p], i32),
+            "w4_linear_repacked": ([p, i64, i64, p, i64, i32, p, p, sz, p], i32),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -202,6 +206,43 @@ def w4_linear_ex(X: torch.Tensor, Wq: torch.Tensor, scales: torch.Tensor, offset
 def w4_linear(X, Wq, scales, offsets, group_size, out=None, workspace=None):
     """Y bf16 [M,N] = X . dequant(Wq)^T (kernel chosen by M; see include/w4.h)."""
     return w4_linear_ex(X, Wq, scales, offsets, group_size, KERNEL_AUTO, out, workspace)
+
+
+def w4_repacked_bytes(N: int, K: int, group_size: int) -> int:
+    return load_library().w4_repacked_bytes(N, K, group_size)
+
+
+class Repacked:
+    """Weights in the decode layout (include/w4.h): the flat uint8 buffer plus the
+    shape it holds."""
+
+    def __init__(self, buf: torch.Tensor, N: int, K: int, group_size: int):
+        self.buf, self.N, self.K, self.group_size = buf, N, K, group_size
+
+
+def w4_repack(Wq: torch.Tensor, scales: torch.Tensor, offsets: torch.Tensor, group_size: int, out=None) -> Repacked:
+    """Canonical packed weights -> the decode layout (a load-time conversion)."""
+    lib = load_library()
+    N, half = Wq.shape
+    K = 2 * half
+    nbytes = w4_repacked_bytes(N, K, group_size)
+    buf = out if out is not None else torch.empty(max(nbytes, 16), dtype=torch.uint8, device=Wq.device)
+    _check(lib.w4_repack(_ptr(Wq), _ptr(scales), _ptr(offsets), N, K, group_size, _ptr(buf), _stream(Wq)),
+           "w4_repack")
+    return Repacked(buf, N, K, group_size)
+
+
+def w4_linear_repacked(X: torch.Tensor, packed: Repacked, out=None, workspace: Workspace | None = None):
+    """Y bf16 [M,N] = X . dequant(W)^T for M <= 8 with W in the decode layout."""
+    lib = load_library()
+    _bits16(X, "X")
+    M, K = X.shape
+    N, g = packed.N, packed.group_size
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    ws = _workspace_for(X, M, N, K, g, workspace)
+    _check(lib.w4_linear_repacked(_ptr(X), M, K, _ptr(packed.buf), N, g, _ptr(Y), _ptr(ws.buf), ws.nbytes,
+                                  _stream(X)), "w4_linear_repacked")
+    return Y
 
 
 def w4_linear_static(X, Wq, scales, offsets, group_size, out=None):

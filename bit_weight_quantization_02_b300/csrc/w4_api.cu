@@ -184,6 +184,44 @@ const char* w4_status_string(w4_status s) {
 
 const char* w4_last_error_detail(void) { return g_detail; }
 
+size_t w4_repacked_bytes(int64_t N, int64_t K, int group_size) {
+    if (check_shape(N, K, group_size) != W4_OK) return 0;
+    return (size_t)w4::repacked_bytes(N, K, group_size);
+}
+
+w4_status w4_repack(const uint8_t* Wq, const uint16_t* scales, const uint16_t* offsets, int64_t N, int64_t K,
+                    int group_size, uint8_t* packed, void* stream) {
+    W4_TRY(check_shape(N, K, group_size));
+    if (N == 0) return W4_OK;
+    W4_TRY(check_ptr(Wq, "Wq"));
+    W4_TRY(check_ptr(scales, "scales"));
+    W4_TRY(check_ptr(offsets, "offsets"));
+    W4_TRY(check_ptr(packed, "packed"));
+    cudaError_t e = w4::launch_repack(Wq, scales, offsets, N, K, group_size, packed, (cudaStream_t)stream);
+    return e == cudaSuccess ? W4_OK : cuda_fail(e, "repack launch");
+}
+
+w4_status w4_linear_repacked(const uint16_t* X, int64_t M, int64_t K, const uint8_t* packed, int64_t N,
+                             int group_size, uint16_t* Y, void* workspace, size_t workspace_bytes, void* stream) {
+    W4_TRY(check_shape(N, K, group_size));
+    if (M < 0) return fail(W4_ERR_INVALID_ARG, "M = %lld must not be negative", (long long)M);
+    if (M > w4::STREAM_MAX_M)
+        return fail(W4_ERR_INVALID_ARG, "the decode layout is read for M <= %d, got %lld", w4::STREAM_MAX_M,
+                    (long long)M);
+    if (M == 0 || N == 0) return W4_OK;
+    W4_TRY(check_ptr(X, "X"));
+    W4_TRY(check_ptr(packed, "packed"));
+    W4_TRY(check_ptr(Y, "Y"));
+    if (workspace == nullptr) workspace_bytes = 0;
+    if (workspace_bytes > 0 && !aligned16(workspace)) return fail(W4_ERR_MISALIGNED, "workspace is not 16-byte aligned");
+    w4::DecodePlan dp;
+    if (!w4::plan_decode(M, N, K, group_size, &dp)) return fail(W4_ERR_INVALID_ARG, "no decode plan for this shape");
+    if (workspace_bytes < dp.ws_bytes)
+        return fail(W4_ERR_INVALID_ARG, "w4_linear_repacked needs %zu workspace bytes", dp.ws_bytes);
+    cudaError_t e = w4::launch_decode(dp, X, M, K, packed, N, group_size, Y, workspace, (cudaStream_t)stream);
+    return e == cudaSuccess ? W4_OK : cuda_fail(e, "repacked linear launch");
+}
+
 int w4_format_version(void) { return W4_FORMAT_VERSION; }
 
 }  // extern "C"

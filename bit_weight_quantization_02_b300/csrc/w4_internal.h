@@ -48,6 +48,24 @@ cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, 
                           void* workspace, cudaStream_t stream, const char** detail);
 cudaError_t read_and_clear_stream_fault(unsigned int* fault);
 
+// Decode layout (see w4.h): bytes of one 16-row x 256-k unit, of the whole
+// layout, and the repack launch.
+int64_t repacked_unit_bytes(int g);
+int64_t repacked_bytes(int64_t N, int64_t K, int g);
+cudaError_t launch_repack(const uint8_t* Wq, const uint16_t* scales, const uint16_t* offsets, int64_t N, int64_t K,
+                          int g, uint8_t* packed, cudaStream_t stream);
+
+// Persistent stream-K decode kernel on the decode layout (M <= 8), same
+// workspace as the stream kernel (stream_ws_bytes).
+struct DecodePlan {
+    int nkc;          // 256-k units per 16-row tile
+    int64_t units;    // tiles * nkc
+    size_t ws_bytes;  // workspace bytes
+};
+bool plan_decode(int64_t M, int64_t N, int64_t K, int g, DecodePlan* plan);
+cudaError_t launch_decode(const DecodePlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* packed,
+                          int64_t N, int g, uint16_t* Y, void* workspace, cudaStream_t stream);
+
 // SM count of the current device and resident blocks per SM for a kernel
 // launch shape (cached per device, kernel and shared-memory size).
 cudaError_t resident_blocks(const void* kernel, int threads, size_t smem, int* sms, int* per_sm);

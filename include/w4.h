@@ -211,6 +211,58 @@ W4_API w4_status w4_linear_static(const uint16_t *X, int64_t M, int64_t K,
                                   const uint16_t *offsets, int64_t N, int group_size,
                                   uint16_t *Y, void *stream);
 
+/*
+ * Decode layout -- an optional second arrangement of the same codes, scales
+ * and offsets, for the memory-bound decode linear.  The pages name such
+ * arrangements without defining them (torchao README "Quick start":
+ * `tile_packed_to_4d`; TorchAO 0.14.0 release notes: Int4PreshuffledTensor,
+ * Int4TilePackedTo4dTensor): weights are rearranged once, at load time, into
+ * the order the kernel reads them.  The canonical row-major arrays above
+ * remain the format of record; this layout holds exactly the same numbers.
+ *
+ * Layout (byte exact).  Rows are cut into tiles of 16 (tile t = rows
+ * 16t..16t+15) and each row into units of 256 k (unit c = k 256c..256c+255);
+ * units are stored tile-major: unit (t, c) starts at byte
+ * (t * ceil(K/256) + c) * U, U = 2048 + 512 * 32 / group_size
+ * (2560, 2304, 2176 for g = 32, 64, 128).  Inside a unit:
+ *  - bytes 512j + 16l (j = 0..3, l = 0..31; with r = l / 4, q = l % 4) hold
+ *    the 32 codes of row 16t + r + 8(j % 2), k from 256c + 128(j / 2) + 32q,
+ *    as four little-endian 32-bit words of 8 codes each (word w: k from
+ *    256c + 128(j / 2) + 32q + 8w); inside a word, nibble i (bits 4i..4i+3)
+ *    holds the code of k0 + 2i for i < 4 and of k0 + 2(i - 4) + 1 for i >= 4
+ *    (k0 the word's first k), so that nibbles i and i + 4 are two
+ *    consecutive k;
+ *  - bytes 2048 + 16p (p = 0 .. 32*32/group_size - 1) hold the eight bf16
+ *    qparams that lanes l with l / (group_size / 32) = p use: with
+ *    l0 = p * group_size / 32, r = l0 / 4 and q0 = l0 % 4, for h = 0, 1 the
+ *    group j_h = (256c + 128h + 32 q0) / group_size of rows a = 16t + r and
+ *    b = a + 8, stored as scale_a(h=0), offset_a(h=0), scale_b(h=0),
+ *    offset_b(h=0), then the same four for h = 1.
+ * Rows >= N, k >= K and groups >= K/group_size hold zeros.
+ */
+W4_API size_t w4_repacked_bytes(int64_t N, int64_t K, int group_size);
+
+/*
+ * w4_repack -- canonical Wq / scales / offsets -> the decode layout above,
+ * in `packed` (w4_repacked_bytes(N, K, group_size) bytes, caller-owned
+ * device memory, 16-byte aligned, not overlapping the inputs).  Asynchronous
+ * on `stream`, allocates nothing.  Errors as w4_dequantize.
+ */
+W4_API w4_status w4_repack(const uint8_t *Wq, const uint16_t *scales, const uint16_t *offsets,
+                           int64_t N, int64_t K, int group_size, uint8_t *packed, void *stream);
+
+/*
+ * w4_linear_repacked -- w4_linear for weights in the decode layout, M <= 8:
+ * the persistent stream-K decode kernel, each 16-row x 256-k unit fetched by
+ * one contiguous bulk copy.  Same result contract as w4_linear (the same
+ * kernel arithmetic); the workspace rules of w4_linear apply, with
+ * w4_linear_workspace_bytes(M, N, K, group_size) bytes required.  M > 8,
+ * K/group_size odd or a missing workspace give W4_ERR_INVALID_ARG.
+ */
+W4_API w4_status w4_linear_repacked(const uint16_t *X, int64_t M, int64_t K, const uint8_t *packed,
+                                    int64_t N, int group_size, uint16_t *Y, void *workspace,
+                                    size_t workspace_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -139,3 +139,28 @@ def test_product_package_does_not_touch_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 for needle in ("import oracle", "from oracle", "w4_ref_", "libw4_oracle", "w4_oracle"):
                     assert needle not in text, (f, needle)
+
+
+def test_decode_layout_calls(lib):
+    # sizes: ceil(N/16) tiles x ceil(K/256) units x (2048 + 16384/g) bytes
+    assert lib.w4_repacked_bytes(4096, 4096, 32) == 256 * 16 * 2560
+    assert lib.w4_repacked_bytes(17, 300, 64) == 0  # K % g
+    assert lib.w4_repacked_bytes(17, 320, 64) == 2 * 2 * 2304
+    assert lib.w4_repacked_bytes(1, 128, 128) == 2176
+    assert lib.w4_repacked_bytes(4, 256, 48) == 0
+    # w4_repack: argument checks before any launch
+    assert lib.w4_repack(FAKE, FAKE, FAKE, 4, 256, 48, FAKE, None) == UNSUPPORTED
+    assert lib.w4_repack(FAKE, FAKE, FAKE, 4, 100, 32, FAKE, None) == INVALID
+    assert lib.w4_repack(FAKE, None, FAKE, 4, 256, 32, FAKE, None) == INVALID
+    assert lib.w4_repack(FAKE, FAKE, FAKE, 4, 256, 32, FAKE + 8, None) == MISALIGNED
+    assert lib.w4_repack(FAKE, FAKE, FAKE, 0, 256, 32, FAKE, None) == OK  # nothing to do
+    # w4_linear_repacked: M <= 8, a workspace of w4_linear_workspace_bytes
+    ws = lib.w4_linear_workspace_bytes(2, 64, 512, 32)
+    assert lib.w4_linear_repacked(FAKE, 9, 512, FAKE, 64, 32, FAKE, FAKE, ws, None) == INVALID
+    assert lib.w4_linear_repacked(FAKE, -1, 512, FAKE, 64, 32, FAKE, FAKE, ws, None) == INVALID
+    assert lib.w4_linear_repacked(FAKE, 2, 512, FAKE, 64, 32, FAKE, None, 0, None) == INVALID
+    assert lib.w4_linear_repacked(FAKE, 2, 512, FAKE, 64, 32, FAKE, FAKE, ws - 4, None) == INVALID
+    assert lib.w4_linear_repacked(FAKE, 2, 512, FAKE + 4, 64, 32, FAKE, FAKE, ws, None) == MISALIGNED
+    assert lib.w4_linear_repacked(FAKE, 2, 512, FAKE, 64, 32, FAKE, FAKE + 8, ws, None) == MISALIGNED
+    assert lib.w4_linear_repacked(FAKE, 2, 512, FAKE, 64, 96, FAKE, FAKE, ws, None) == UNSUPPORTED
+    assert lib.w4_linear_repacked(FAKE, 0, 512, FAKE, 64, 32, FAKE, None, 0, None) == OK

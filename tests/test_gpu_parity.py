@@ -19,6 +19,7 @@ import oracle
 import bit_weight_quantization_02_b300 as w4
 from bit_weight_quantization_02_b300 import workloads as wl
 from tests.test_oracle_pins import adversarial_matrix
+from tests.decode_layout import repack_ref
 
 pytestmark = pytest.mark.gpu
 
@@ -177,6 +178,51 @@ def test_linear_stream(g, nk):
                          f"stream M={M} N={N} K={K} g={g}")
         torch.cuda.synchronize()
         assert int(ws.buf.count_nonzero()) == 0, "the stream kernel must leave its workspace zeroed"
+
+
+REPACK_NK = [(200, 4160), (520, 512), (64, 96), (1030, 1024), (48, 14336), (16, 256), (33, 1152)]
+
+
+def _repacked(Wq, sc, of, g):
+    """w4_repack into a canary-guarded buffer."""
+    N, K = Wq.shape[0], 2 * Wq.shape[1]
+    out = Guarded((w4.w4_repacked_bytes(N, K, g),), torch.uint8)
+    rp = w4.w4_repack(Wq, sc, of, g, out=out.t)
+    out.check()
+    return rp
+
+
+@pytest.mark.parametrize("g", [32, 64, 128])
+@pytest.mark.parametrize("nk", REPACK_NK, ids=[f"{n}x{k}" for n, k in REPACK_NK])
+def test_repack_bit_exact(g, nk):
+    """w4_repack equals the layout reference byte for byte (ragged tiles and units)."""
+    N, K = nk
+    if K % g:
+        pytest.skip("K not a multiple of g")
+    W = wl.gen_weight(N, K, seed=N + K + g)
+    rq, rs, ro = oracle.ref_quantize(bits(W), g)
+    Wq = torch.from_numpy(rq).to(DEV)
+    sc = torch.from_numpy(rs.view(np.int16)).view(torch.bfloat16).to(DEV)
+    of = torch.from_numpy(ro.view(np.int16)).view(torch.bfloat16).to(DEV)
+    rp = _repacked(Wq, sc, of, g)
+    assert np.array_equal(rp.buf.cpu().numpy(), repack_ref(rq, rs, ro, N, K, g))
+
+
+@pytest.mark.parametrize("g", [32, 64, 128])
+@pytest.mark.parametrize("nk", REPACK_NK, ids=[f"{n}x{k}" for n, k in REPACK_NK])
+def test_linear_repacked(g, nk):
+    """The stream kernel reading the decode layout, against the oracle."""
+    N, K = nk
+    if K % g:
+        pytest.skip("K not a multiple of g")
+    for M in (1, 2, 3, 5, 8):
+        (X, Wq, sc, of), y_ref = _problem(M, N, K, g, seed=19 * M + N + g)
+        rp = _repacked(Wq, sc, of, g)
+        Y = Guarded((M, N), torch.bfloat16)
+        w4.w4_linear_repacked(X, rp, out=Y.t)
+        Y.check()
+        assert_linear_ok(Y.t, y_ref, f"repacked M={M} N={N} K={K} g={g}")
+    w4.w4_device_fault(DEV)
 
 
 GEMM_M = [1, 33, 127, 129, 300]
@@ -338,6 +384,9 @@ def test_full_size_decode_config2(case):
     Y = gpu_linear(X, Wq, sc, of, case.group_size)
     y_ref = oracle.ref_linear(bits(X), rq, rs, ro, case.group_size)
     assert_linear_ok(Y[:, rows], y_ref, f"config2 {case.name}")
+    # the same weights in the decode layout (the benchmark's headline path)
+    Yr = w4.w4_linear_repacked(X, w4.w4_repack(Wq, sc, of, case.group_size))
+    assert_linear_ok(Yr[:, rows], y_ref, f"config2 {case.name} (decode layout)")
 
 
 def test_full_size_batched_decode_config3():
