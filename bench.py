@@ -458,8 +458,7 @@ def other_rows(args, w4, wl, device, stream, peaks, dist, only=None):
     b3 = []
     for c in (wl.config3() if want("batched") else []):
         b3.append(_rotated_graph_row(c, w4, wl, device, stream, dist, peaks))
-        if c.M <= 8:
-            b3.append(_rotated_graph_row(c, w4, wl, device, stream, dist, peaks, layout="decode"))
+        b3.append(_rotated_graph_row(c, w4, wl, device, stream, dist, peaks, layout="decode"))
     rows["batched_decode_g64"] = {"unit": "GB/s", "cases": b3,
                                   "l2": "graph of back-to-back calls over weight copies totalling > 4x L2"}
 
@@ -487,15 +486,16 @@ def other_rows(args, w4, wl, device, stream, peaks, dist, only=None):
                                   "gbs": round(qbytes / (q_ms * 1e-3) / 1e9, 1),
                                   "frac_of_hbm_peak": round(qbytes / (q_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                                   "algorithmic_bytes": qbytes, "setup_s": round(setup_s, 1)}
-    for M in ((1, 16) if c5 else ()):
+    for M, layout in (((1, "canonical"), (16, "canonical"), (1, "decode"), (16, "decode")) if c5 else ()):
         cases = wl.config5(M)
-        st = LinearStack(cases, device, w4, wl, packed=packed)
+        st = LinearStack(cases, device, w4, wl, packed=packed, layout=layout)
         g = st.capture(stream)
         with torch.cuda.stream(stream):
             t = time_region(g.replay, 10, 3, stream, dist, device) / 10
-        stack_rows[f"M{M}"] = {"ms": round(t, 4), "gbs": round(st.bytes / (t * 1e-3) / 1e9, 1),
-                               "frac_of_hbm_peak": round(st.bytes / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-                               "algorithmic_bytes": st.bytes}
+        stack_rows[f"M{M}" if layout == "canonical" else f"M{M}_decode_layout"] = {
+            "ms": round(t, 4), "gbs": round(st.bytes / (t * 1e-3) / 1e9, 1),
+            "frac_of_hbm_peak": round(st.bytes / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "algorithmic_bytes": st.bytes}
         del g, st
     rows["llama3_8b_stack_g128"] = stack_rows
     del packed

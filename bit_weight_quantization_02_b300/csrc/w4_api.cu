@@ -81,8 +81,10 @@ w4_status w4_dequantize(const uint8_t* Wq, const uint16_t* scales, const uint16_
 size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int group_size) {
     if (check_shape(N, K, group_size) != W4_OK || M < 1 || N == 0) return 0;
     w4::StreamPlan plan;
-    if (!w4::plan_stream(M, N, K, group_size, &plan)) return 0;
-    return plan.ws_bytes;
+    if (M <= w4::STREAM_MAX_M && w4::plan_stream(M, N, K, group_size, &plan)) return plan.ws_bytes;
+    w4::DecodePlan dp;  // decode layout (w4_linear_repacked)
+    if (w4::plan_decode(M, N, K, group_size, &dp)) return dp.ws_bytes;
+    return 0;
 }
 
 w4_status w4_linear_ex(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
@@ -205,8 +207,8 @@ w4_status w4_linear_repacked(const uint16_t* X, int64_t M, int64_t K, const uint
                              int group_size, uint16_t* Y, void* workspace, size_t workspace_bytes, void* stream) {
     W4_TRY(check_shape(N, K, group_size));
     if (M < 0) return fail(W4_ERR_INVALID_ARG, "M = %lld must not be negative", (long long)M);
-    if (M > w4::STREAM_MAX_M)
-        return fail(W4_ERR_INVALID_ARG, "the decode layout is read for M <= %d, got %lld", w4::STREAM_MAX_M,
+    if (M > w4::DECODE_MAX_M)
+        return fail(W4_ERR_INVALID_ARG, "the decode layout is read for M <= %d, got %lld", w4::DECODE_MAX_M,
                     (long long)M);
     if (M == 0 || N == 0) return W4_OK;
     W4_TRY(check_ptr(X, "X"));

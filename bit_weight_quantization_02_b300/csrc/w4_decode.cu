@@ -1,4 +1,4 @@
-// w4_decode.cu -- persistent stream-K bf16 x int4 linear for decode (M <= 8)
+// w4_decode.cu -- persistent stream-K bf16 x int4 linear for decode (M <= 32)
 // on weights in the decode layout (include/w4.h, written by w4_repack).
 //
 // Y[m,n] = sum_k X[m,k] * w'[n,k], w' = bf16(q*s + o), fp32 accumulation
@@ -16,8 +16,9 @@
 //    the unit two ahead as soon as it has computed it; the first two units
 //    are requested before the programmatic-dependent-launch wait;
 //  * dequantization: LOP3 nibble pairs (128+q as bf16), an exact subtract of
-//    128 and one bf16 FMA with (scale, offset), inside one asm block with the
-//    mma.sync m16n8k16 that consumes them (weights as A, tokens as B).  The
+//    128 and one bf16 FMA with (scale, offset), then mma.sync m16n8k16 with
+//    the weights as A and the tokens as B, one MMA per group of 8 tokens on
+//    the same dequantized fragment (M up to 32: four groups).  The
 //    layout's nibble order makes every extracted pair two consecutive k, so
 //    the B fragments are X's own 32-bit words, read straight from global
 //    memory through L1 (X is tiny and shared by every warp of the SM);
@@ -83,14 +84,47 @@ __device__ __forceinline__ void dc_mma(float (&c)[4], uint32_t wa, uint32_t wb, 
           "n"(SH), "n"(SH + 4));
 }
 
+// The four A-fragment registers of one MMA step (rows a, b; nibble pairs SH,
+// SH+4 and SH+1, SH+5), dequantized once for every token group.
+template <int SH>
+__device__ __forceinline__ void dc_dequant(uint32_t wa, uint32_t wb, uint32_t sa2, uint32_t oa2, uint32_t sb2,
+                                           uint32_t ob2, uint32_t cm, uint32_t cg, uint32_t (&A)[4]) {
+    asm("{\n\t.reg .b32 t;\n\t"
+        "shr.b32 t, %4, %12;\n\t"
+        "lop3.b32 %0, t, %10, %11, 0xEA;\n\t"
+        "shr.b32 t, %4, %13;\n\t"
+        "lop3.b32 %2, t, %10, %11, 0xEA;\n\t"
+        "shr.b32 t, %5, %12;\n\t"
+        "lop3.b32 %1, t, %10, %11, 0xEA;\n\t"
+        "shr.b32 t, %5, %13;\n\t"
+        "lop3.b32 %3, t, %10, %11, 0xEA;\n\t"
+        "sub.rn.bf16x2 %0, %0, %11;\n\t"
+        "sub.rn.bf16x2 %1, %1, %11;\n\t"
+        "sub.rn.bf16x2 %2, %2, %11;\n\t"
+        "sub.rn.bf16x2 %3, %3, %11;\n\t"
+        "fma.rn.bf16x2 %0, %0, %6, %7;\n\t"
+        "fma.rn.bf16x2 %1, %1, %8, %9;\n\t"
+        "fma.rn.bf16x2 %2, %2, %6, %7;\n\t"
+        "fma.rn.bf16x2 %3, %3, %8, %9;\n\t}"
+        : "=&r"(A[0]), "=&r"(A[1]), "=&r"(A[2]), "=&r"(A[3])
+        : "r"(wa), "r"(wb), "r"(sa2), "r"(oa2), "r"(sb2), "r"(ob2), "r"(cm), "r"(cg), "n"(SH), "n"(SH + 4));
+}
+__device__ __forceinline__ void dc_mma_only(float (&c)[4], const uint32_t (&A)[4], uint32_t x0, uint32_t x1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(A[0]), "r"(A[1]), "r"(A[2]), "r"(A[3]), "r"(x0), "r"(x1));
+}
+
 // One unit's fragments of this lane: code words of rows a / b for the two
 // 128-k halves, and the lane's eight qparams.
 struct DcUnit {
     uint4 a0, b0, a1, b1, q;
 };
 
-template <int G>
-__global__ void __launch_bounds__(DC_THREADS, 5)
+// MT: groups of 8 tokens (M <= 8 MT).
+template <int G, int MT>
+__global__ void __launch_bounds__(DC_THREADS, MT == 4 ? 4 : 5)
 decode_kernel(const DecodeArgs p) {
     constexpr int SLOT16 = (2048 + 16 * 32 * 32 / G) / 16;  // 16-byte pieces per unit
     constexpr int QSH = (G == 32) ? 0 : (G == 64 ? 1 : 2);   // lanes sharing a qparam piece: 1 << QSH
@@ -124,25 +158,22 @@ decode_kernel(const DecodeArgs p) {
     griddep_wait();
 
     // B fragments straight from X (natural k order, L1-cached): lane (gid, tq)
-    // needs token gid's 8-k chunks at 32 tq + 8 j of each 128-k half
-    const bool xon = gid < p.M;
-    const uint16_t* xlane = p.X + (int64_t)(xon ? gid : 0) * p.K + 32 * tq;
+    // needs token (8t + gid)'s 8-k chunks at 32 tq + 8 j of each 128-k half
+    const uint16_t* xlane = p.X + (int64_t)gid * p.K + 32 * tq;
 
     uint32_t cm, cg;  // constants pinned in registers: nibble mask, bf16 128.0 pair (magic and bias)
     asm volatile("mov.b32 %0, %1;" : "=r"(cm) : "r"(0x000F000Fu));
     asm volatile("mov.b32 %0, %1;" : "=r"(cg) : "r"(0x43004300u));
 
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[MT][4];
+#pragma unroll
+    for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
     int tile = (int)(u0 / p.nkc), kc = (int)(u0 % p.nkc), kc_first = kc;
 
     auto compute = [&](const DcUnit& f, int it) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {  // two 128-k halves per unit
             const int kx = kc * 256 + 128 * h;  // first k of the half (its chunks lie inside K or wholly past it)
-            uint4 xv[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                xv[j] = (xon && kx + 32 * tq + 8 * j < p.K) ? ldg_nc_v4(xlane + kx + 8 * j) : make_uint4(0u, 0u, 0u, 0u);
             const uint4 wa = h ? f.a1 : f.a0, wb = h ? f.b1 : f.b0;
             const uint32_t qwa = h ? f.q.z : f.q.x, qwb = h ? f.q.w : f.q.y;  // (scale | offset << 16)
             const uint32_t sa2 = __byte_perm(qwa, 0, 0x1010), oa2 = __byte_perm(qwa, 0, 0x3232);
@@ -153,30 +184,50 @@ decode_kernel(const DecodeArgs p) {
             for (int j = 0; j < 4; ++j) {
                 // nibbles (i, i+4) of a decode-layout word are the consecutive k (2i, 2i+1):
                 // the B pairs are X's own 32-bit words
-                dc_mma<0>(acc, wa4[j], wb4[j], sa2, oa2, sb2, ob2, xv[j].x, xv[j].y, cm, cg);
-                dc_mma<8>(acc, wa4[j], wb4[j], sa2, oa2, sb2, ob2, xv[j].z, xv[j].w, cm, cg);
+                const bool kin = kx + 32 * tq + 8 * j < p.K;
+                uint4 xv[MT];
+#pragma unroll
+                for (int t = 0; t < MT; ++t)
+                    xv[t] = (kin && 8 * t + gid < p.M) ? ldg_nc_v4(xlane + (int64_t)(8 * t) * p.K + kx + 8 * j)
+                                                       : make_uint4(0u, 0u, 0u, 0u);
+                if (MT == 1) {  // dequantization fused with the single MMA
+                    dc_mma<0>(acc[0], wa4[j], wb4[j], sa2, oa2, sb2, ob2, xv[0].x, xv[0].y, cm, cg);
+                    dc_mma<8>(acc[0], wa4[j], wb4[j], sa2, oa2, sb2, ob2, xv[0].z, xv[0].w, cm, cg);
+                } else {
+                    uint32_t A[4];
+                    dc_dequant<0>(wa4[j], wb4[j], sa2, oa2, sb2, ob2, cm, cg, A);
+#pragma unroll
+                    for (int t = 0; t < MT; ++t) dc_mma_only(acc[t], A, xv[t].x, xv[t].y);
+                    dc_dequant<8>(wa4[j], wb4[j], sa2, oa2, sb2, ob2, cm, cg, A);
+#pragma unroll
+                    for (int t = 0; t < MT; ++t) dc_mma_only(acc[t], A, xv[t].z, xv[t].w);
+                }
             }
         }
 
         // end of a row tile or of the range: hand the tile's sums on
         if (it + 1 == nunits || kc == p.nkc - 1) {
             const int n_a = tile * 16 + gid, n_b = n_a + 8;
-            const int m0 = 2 * tq;  // acc = D[row n_a: tokens m0, m0+1 | row n_b: tokens m0, m0+1]
+            // acc[t] = D[row n_a: tokens 8t + 2tq, +1 | row n_b: the same tokens]
             if (kc_first == 0 && kc == p.nkc - 1) {  // this warp summed all of the tile's k
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int m = m0 + (i & 1), n = (i < 2) ? n_a : n_b;
-                    if (m < p.M && n < p.N) p.Y[(int64_t)m * p.N + n] = (uint16_t)float_to_bf16_bits(acc[i]);
-                }
+                for (int t = 0; t < MT; ++t)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int m = 8 * t + 2 * tq + (i & 1), n = (i < 2) ? n_a : n_b;
+                        if (m < p.M && n < p.N) p.Y[(int64_t)m * p.N + n] = (uint16_t)float_to_bf16_bits(acc[t][i]);
+                    }
             } else {
                 // split tile: fence-free ordering, as in the stream kernel -- the adds return
                 // their old values and the vote reads them before lane 0 moves the counter
                 float got = 0.f;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int m = m0 + (i & 1), n = (i < 2) ? n_a : n_b;
-                    if (m < p.M && n < p.N) got += atomicAdd(p.ws + (int64_t)m * p.N + n, acc[i]);
-                }
+                for (int t = 0; t < MT; ++t)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int m = 8 * t + 2 * tq + (i & 1), n = (i < 2) ? n_a : n_b;
+                        if (m < p.M && n < p.N) got += atomicAdd(p.ws + (int64_t)m * p.N + n, acc[t][i]);
+                    }
                 const unsigned int dep = __float_as_uint(got) & (0u - threadIdx.y);  // threadIdx.y == 0
                 const unsigned int done = __all_sync(0xffffffffu, dep == 0u);
                 unsigned int last = 0;
@@ -195,7 +246,8 @@ decode_kernel(const DecodeArgs p) {
                     if (lane == 0) atomicExch(p.count + tile, 0u);
                 }
             }
-            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+#pragma unroll
+            for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
             kc_first = 0;
         }
         if (++kc == p.nkc) {
@@ -218,7 +270,7 @@ decode_kernel(const DecodeArgs p) {
 // ------------------------------------------------------------------ host side
 
 bool plan_decode(int64_t M, int64_t N, int64_t K, int g, DecodePlan* plan) {
-    if (M < 1 || M > STREAM_MAX_M) return false;
+    if (M < 1 || M > DECODE_MAX_M) return false;
     const int64_t tiles = (N + 15) / 16;
     if (tiles > 0x3FFFFFFF) return false;
     plan->nkc = (int)((K + 255) / 256);
@@ -228,9 +280,9 @@ bool plan_decode(int64_t M, int64_t N, int64_t K, int g, DecodePlan* plan) {
     return true;
 }
 
-template <int G>
-static cudaError_t launch_decode_g(const DecodePlan& plan, DecodeArgs a, cudaStream_t stream) {
-    auto kern = decode_kernel<G>;
+template <int G, int MT>
+static cudaError_t launch_decode_gm(const DecodePlan& plan, DecodeArgs a, cudaStream_t stream) {
+    auto kern = decode_kernel<G, MT>;
     // one wave: as many resident warps as the SMs hold, but no more than there are units
     int sms = 0, per_sm = 0;
     cudaError_t e = resident_blocks(reinterpret_cast<const void*>(kern), DC_THREADS, 0, &sms, &per_sm);
@@ -248,6 +300,13 @@ static cudaError_t launch_decode_g(const DecodePlan& plan, DecodeArgs a, cudaStr
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+template <int G>
+static cudaError_t launch_decode_g(const DecodePlan& plan, DecodeArgs a, cudaStream_t stream) {
+    if (a.M <= 8) return launch_decode_gm<G, 1>(plan, a, stream);
+    if (a.M <= 16) return launch_decode_gm<G, 2>(plan, a, stream);
+    return launch_decode_gm<G, 4>(plan, a, stream);
 }
 
 cudaError_t launch_decode(const DecodePlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* packed,

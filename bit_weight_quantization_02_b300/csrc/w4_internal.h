@@ -41,6 +41,7 @@ struct StreamPlan {
     size_t ws_bytes;  // workspace bytes
 };
 constexpr int STREAM_MAX_M = 8;
+constexpr int DECODE_MAX_M = 32;  // decode-layout kernel
 size_t stream_ws_bytes(int64_t M, int64_t N);
 bool plan_stream(int64_t M, int64_t N, int64_t K, int g, StreamPlan* plan);
 cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,

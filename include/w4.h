@@ -106,10 +106,11 @@ W4_API w4_status w4_dequantize(const uint8_t *Wq, const uint16_t *scales,
                         int group_size, uint16_t *W_out, void *stream);
 
 /*
- * w4_linear_workspace_bytes -- workspace bytes w4_linear needs to run this
- * problem on the persistent stream-K decode kernel (M <= 8 and K/group_size
- * even); 0 when that kernel does not apply.  Without it the call still works
- * (cluster split-K kernel), usually slower for decode.
+ * w4_linear_workspace_bytes -- workspace bytes for this problem: what
+ * w4_linear needs to run the persistent stream-K decode kernel (M <= 8 and
+ * K/group_size even; without it the call still works on the cluster split-K
+ * kernel, usually slower for decode), and what w4_linear_repacked needs
+ * (M <= 32).  0 when neither applies (M > 32).
  */
 W4_API size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int group_size);
 
@@ -252,12 +253,14 @@ W4_API w4_status w4_repack(const uint8_t *Wq, const uint16_t *scales, const uint
                            int64_t N, int64_t K, int group_size, uint8_t *packed, void *stream);
 
 /*
- * w4_linear_repacked -- w4_linear for weights in the decode layout, M <= 8:
- * the persistent stream-K decode kernel, each 16-row x 256-k unit fetched by
- * one contiguous bulk copy.  Same result contract as w4_linear (the same
- * kernel arithmetic); the workspace rules of w4_linear apply, with
- * w4_linear_workspace_bytes(M, N, K, group_size) bytes required.  M > 8,
- * K/group_size odd or a missing workspace give W4_ERR_INVALID_ARG.
+ * w4_linear_repacked -- w4_linear for weights in the decode layout, M <= 32:
+ * a persistent stream-K decode kernel that loads each 16-row x 256-k unit
+ * with five coalesced warp loads straight into registers and reads X through
+ * L1.  Same result contract as w4_linear (the same dequantization and fp32
+ * accumulation; the last bits vary from run to run as with the stream
+ * kernel); the workspace rules of w4_linear apply, with
+ * w4_linear_workspace_bytes(M, N, K, group_size) bytes required.  M > 32 or
+ * a missing workspace give W4_ERR_INVALID_ARG.
  */
 W4_API w4_status w4_linear_repacked(const uint16_t *X, int64_t M, int64_t K, const uint8_t *packed,
                                     int64_t N, int group_size, uint16_t *Y, void *workspace,

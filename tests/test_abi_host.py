@@ -65,8 +65,9 @@ def test_workspace_plan(lib):
     # the stream kernel (M <= 8, even K/g) needs [M][N] fp32 sums + one counter per 16 rows
     assert lib.w4_linear_workspace_bytes(1, 1024, 4096, 32) == 4096 + 64 * 4
     assert lib.w4_linear_workspace_bytes(8, 14336, 4096, 128) >= 8 * 14336 * 4 + 896 * 4
-    assert lib.w4_linear_workspace_bytes(9, 1024, 4096, 32) == 0     # M > 8: cluster kernel, no workspace
-    assert lib.w4_linear_workspace_bytes(1, 100, 96, 32) == 0        # K/g odd
+    assert lib.w4_linear_workspace_bytes(9, 1024, 4096, 32) == 9 * 4096 + 64 * 4  # decode layout, M <= 32
+    assert lib.w4_linear_workspace_bytes(33, 1024, 4096, 32) == 0    # M > 32: no kernel uses a workspace
+    assert lib.w4_linear_workspace_bytes(1, 100, 96, 32) == 512 + 7 * 4  # K/g odd: the decode layout's need
     assert lib.w4_linear_workspace_bytes(0, 100, 128, 32) == 0
 
 
@@ -156,7 +157,7 @@ def test_decode_layout_calls(lib):
     assert lib.w4_repack(FAKE, FAKE, FAKE, 0, 256, 32, FAKE, None) == OK  # nothing to do
     # w4_linear_repacked: M <= 8, a workspace of w4_linear_workspace_bytes
     ws = lib.w4_linear_workspace_bytes(2, 64, 512, 32)
-    assert lib.w4_linear_repacked(FAKE, 9, 512, FAKE, 64, 32, FAKE, FAKE, ws, None) == INVALID
+    assert lib.w4_linear_repacked(FAKE, 33, 512, FAKE, 64, 32, FAKE, FAKE, 1 << 20, None) == INVALID
     assert lib.w4_linear_repacked(FAKE, -1, 512, FAKE, 64, 32, FAKE, FAKE, ws, None) == INVALID
     assert lib.w4_linear_repacked(FAKE, 2, 512, FAKE, 64, 32, FAKE, None, 0, None) == INVALID
     assert lib.w4_linear_repacked(FAKE, 2, 512, FAKE, 64, 32, FAKE, FAKE, ws - 4, None) == INVALID

@@ -211,11 +211,11 @@ def test_repack_bit_exact(g, nk):
 @pytest.mark.parametrize("g", [32, 64, 128])
 @pytest.mark.parametrize("nk", REPACK_NK, ids=[f"{n}x{k}" for n, k in REPACK_NK])
 def test_linear_repacked(g, nk):
-    """The stream kernel reading the decode layout, against the oracle."""
+    """The decode-layout kernel (one to four groups of 8 tokens), against the oracle."""
     N, K = nk
     if K % g:
         pytest.skip("K not a multiple of g")
-    for M in (1, 2, 3, 5, 8):
+    for M in (1, 2, 3, 5, 8, 9, 16, 17, 31, 32):
         (X, Wq, sc, of), y_ref = _problem(M, N, K, g, seed=19 * M + N + g)
         rp = _repacked(Wq, sc, of, g)
         Y = Guarded((M, N), torch.bfloat16)
