@@ -7,25 +7,26 @@
 // thousands this is a dense contraction (2*M*N*K flops against ~0.6 bytes per
 // weight), so the int4 codes are expanded to bf16 on chip and fed to UMMA.
 //
-// One thread block computes a BM x BN = 128 tokens x 256 weight rows tile of
-// Y, walking K in BK = 64 steps.  Two shared-memory rings decouple the stages:
-// a 6-deep TMA ring (X tile + packed codes, 24 KB a step) covers the copy
-// latency, a 2-deep ring of dequantized bf16 weight tiles (32 KB) decouples
-// dequantization from the MMAs.
-//   warp 0      TMA producer: X tile (128 x 64 bf16, 128-byte swizzle) and
-//               the packed code tile (256 rows x 32 bytes) per k step;
-//   warp 1      TMEM owner (alloc/dealloc of 256 fp32 columns) and, on one
-//               lane, the UMMA issuer: 4 x tcgen05.mma (M=128, N=256, K=16)
-//               per k step; tcgen05.commit frees the TMA and weight stages;
-//   warps 2..9  dequantization: one weight row per thread, codes from the
-//               staged tile -> bf16 w' written straight into the UMMA B
-//               operand layout (K-major, 128-byte swizzle), then
-//               fence.proxy.async and an mbarrier arrive; afterwards the same
-//               warps run the epilogue (tcgen05.ld -> bf16 -> global).
-// When a row of scales (or offsets) is a whole number of 16-byte pieces, the
-// producer also copies them by TMA, 8 groups x 256 rows a box, into a 2-deep
-// ring that the dequantization threads read once per 8 groups; otherwise
-// each thread loads its row's values from global memory a few k blocks ahead.
+// The weights are the MMA's A operand and live in tensor memory: the
+// dequantization threads write w' straight from registers into TMEM
+// (tcgen05.st), so the bf16 weight tile never passes through shared memory,
+// and the tokens (X, through TMA) are the B operand in shared memory.  One
+// thread block computes a 128 weight rows x 256 tokens tile of Y^T (D in TMEM:
+// lane = weight row, column = token), walking K in 64-k steps; every
+// dequantized weight feeds 256 tokens.
+//   warp 0      TMA producer: a 5-deep ring of the X tile (256 tokens x 64 k,
+//               128-byte swizzle, the UMMA B layout) and the packed code tile
+//               (128 rows x 32 bytes, 32-byte swizzle); every 8 groups, when
+//               the rows allow it, a 2-deep ring of scale / offset boxes;
+//   warp 1      TMEM owner (512 columns: D in 0..255, four 32-column A
+//               stages above) and, on one lane, the UMMA issuer: 4 x
+//               tcgen05.mma (M=128 from TMEM, N=256, K=16) a step;
+//               tcgen05.commit frees the TMA stage and the A stage;
+//   warps 2..9  dequantization: thread (row, 32-k half) of its TMEM
+//               sub-partition turns 32 codes into 16 bf16 pairs and stores
+//               them with one tcgen05.st; afterwards the same warps run the
+//               epilogue (tcgen05.ld -> bf16 -> shared-memory transpose ->
+//               64-byte runs of Y rows).
 // Every mbarrier wait is bounded in time; a block that gives up sets the
 // device fault word, waits (bounded) for its own copies and MMAs, frees its
 // tensor memory and exits.
@@ -35,33 +36,36 @@
 
 namespace w4 {
 
-constexpr int GM_BM = 128;
-constexpr int GM_BN = 256;
+constexpr int GM_BW = 128;  // weight rows per block (UMMA M, TMEM lanes)
+constexpr int GM_BT = 256;  // tokens per block (UMMA N)
 constexpr int GM_BK = 64;
-constexpr int GM_TSTAGES = 6;  // TMA ring: X tile + packed code tile per k block
-constexpr int GM_WSTAGES = 2;  // dequantized bf16 weight tiles (the UMMA B operand)
+constexpr int GM_TSTAGES = 5;  // TMA ring: X tile + packed code tile per k block
+constexpr int GM_WSTAGES = 4;  // dequantized weight tiles in TMEM (the UMMA A operand)
+constexpr int GM_QSTAGES = 2;  // TMA ring of qparam boxes (8 groups x 128 rows of scales and offsets)
+constexpr int GM_QPF = 4;      // k blocks of qparams prefetched by each thread (no-TMA variant)
 constexpr int GM_DEQ_WARPS = 8;
 constexpr int GM_THREADS = 64 + GM_DEQ_WARPS * 32;
-constexpr int GM_TMEM_COLS = 256;
-constexpr int GM_QPF = 4;  // k blocks of qparams prefetched by each thread (no-TMA variant)
-constexpr int GM_QSTAGES = 2;  // TMA ring of qparam boxes (8 groups x 256 rows of scales and offsets)
+constexpr int GM_TMEM_COLS = 512;
+constexpr int GM_ACOL = GM_BT;             // first TMEM column of the A stages
+constexpr int GM_ASTAGE_COLS = GM_BK / 2;  // 64 bf16 of a row = 32 columns
 
-constexpr int GM_X_BYTES = GM_BM * GM_BK * 2;  // 16 KB
-constexpr int GM_W_BYTES = GM_BN * GM_BK * 2;  // 32 KB
-constexpr int GM_P_BYTES = GM_BN * GM_BK / 2;  //  8 KB
-constexpr int GM_QBOX_BYTES = GM_BN * 16;      //  4 KB: 8 bf16 per row
+constexpr int GM_X_BYTES = GM_BT * GM_BK * 2;  // 32 KB
+constexpr int GM_P_BYTES = GM_BW * GM_BK / 2;  //  4 KB
+constexpr int GM_QBOX_BYTES = GM_BW * 16;      //  2 KB: 8 bf16 per row
 constexpr int GM_OFF_X = 0;
-constexpr int GM_OFF_W = GM_OFF_X + GM_TSTAGES * GM_X_BYTES;
-constexpr int GM_OFF_P = GM_OFF_W + GM_WSTAGES * GM_W_BYTES;
+constexpr int GM_OFF_P = GM_OFF_X + GM_TSTAGES * GM_X_BYTES;
 constexpr int GM_OFF_Q = GM_OFF_P + GM_TSTAGES * GM_P_BYTES;  // per stage: scales box, offsets box
 constexpr int GM_OFF_BAR = GM_OFF_Q + GM_QSTAGES * 2 * GM_QBOX_BYTES;
-// full_tma, empty_tma per TMA stage; full_deq, empty_w per weight stage;
+// full_tma, empty_tma per TMA stage; full_deq, empty_w per A stage;
 // full_q, empty_q per qparam stage; tmem_full; drain
 constexpr int GM_NBAR = 2 * GM_TSTAGES + 2 * GM_WSTAGES + 2 * GM_QSTAGES + 2;
 constexpr int GM_OFF_MISC = GM_OFF_BAR + GM_NBAR * 8;
 constexpr int GM_SMEM_USED = GM_OFF_MISC + 16;
 constexpr int GM_SMEM_BYTES = GM_SMEM_USED + 1024;  // + alignment slack for the 1024-byte swizzle atoms
 static_assert(GM_SMEM_BYTES <= 227 * 1024, "shared memory budget");
+constexpr int GM_STAGE_PITCH = 80;                   // epilogue transpose: 32 rows of bf16 + 16 bytes
+constexpr int GM_STAGE_BYTES = 32 * GM_STAGE_PITCH;  // one warp's 32 tokens x 32 rows
+static_assert(GM_DEQ_WARPS * GM_STAGE_BYTES <= GM_TSTAGES * GM_X_BYTES, "epilogue staging reuses the X ring");
 
 constexpr uint64_t GM_WAIT_LIMIT_NS = 2000000000ull;   // 2 s per wait
 constexpr uint64_t GM_DRAIN_LIMIT_NS = 1000000000ull;  // 1 s per drain wait
@@ -72,7 +76,7 @@ __device__ unsigned int g_gemm_fault;
 // A and B bf16 (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0),
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
 constexpr uint32_t gm_idesc() {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(GM_BN >> 3) << 17) | ((uint32_t)(GM_BM >> 4) << 24);
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(GM_BT >> 3) << 17) | ((uint32_t)(GM_BW >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor for a K-major operand stored as rows of
@@ -85,12 +89,26 @@ __device__ __forceinline__ uint64_t gm_sdesc(uint32_t saddr) {
            (1ull << 46) | (2ull << 61);
 }
 
-// Byte offset of 16-byte chunk `c` (k = 8c..8c+7) of row `r` inside a
-// 128-byte-swizzled K-major tile: rows 128 B apart, the chunk index xor-ed
-// with the row's position inside its 8-row atom (what TMA's 128-byte swizzle
-// writes and what the UMMA descriptor above reads).
-__device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
-    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+// D[tmem] (+)= A[tmem] . B[smem desc]^T, kind::f16: the A operand (M=128 rows
+// x K=16) is read from tensor memory, two bf16 of consecutive k a column.
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                 :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+// 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st_16cols(uint32_t taddr, const uint4& a, const uint4& b, const uint4& c,
+                                               const uint4& d) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                 "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                 :: "r"(taddr), "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w),
+                    "r"(c.x), "r"(c.y), "r"(c.z), "r"(c.w), "r"(d.x), "r"(d.y), "r"(d.z), "r"(d.w)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Eight codes of one 32-bit word (k0..k7, k0 in the low nibble) -> eight bf16
@@ -123,10 +141,6 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, uint32_t s2, uint32_t o2, 
         : "r"(w), "r"(s2), "r"(o2), "r"(cm), "r"(cg));
     return r;
 }
-__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
-    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
-}
-
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
@@ -161,7 +175,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + GM_OFF_MISC + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * GM_BN, m0 = blockIdx.y * GM_BM;
+    const int n0 = blockIdx.x * GM_BW, m0 = blockIdx.y * GM_BT;
     const int nkb = (K + GM_BK - 1) / GM_BK;
 
     if (threadIdx.x == 0) {
@@ -237,13 +251,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 if (!mbar_wait_bounded(full_tma(t), pt, abort_flag, &g_gemm_fault, 2u, GM_WAIT_LIMIT_NS)) break;
                 if (!mbar_wait_bounded(full_deq(w), pw, abort_flag, &g_gemm_fault, 2u, GM_WAIT_LIMIT_NS)) break;
                 tc_fence_after();
-                const uint64_t adesc = gm_sdesc(sbase + GM_OFF_X + t * GM_X_BYTES);
-                const uint64_t bdesc = gm_sdesc(sbase + GM_OFF_W + w * GM_W_BYTES);
+                const uint64_t bdesc = gm_sdesc(sbase + GM_OFF_X + t * GM_X_BYTES);
+                const uint32_t a_tmem = tmem + (uint32_t)(GM_ACOL + w * GM_ASTAGE_COLS);
 #pragma unroll
-                for (int kk = 0; kk < GM_BK / 16; ++kk)  // +32 bytes of K per MMA = +2 in the address field
-                    umma_bf16(tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc, (kb | kk) != 0);
+                for (int kk = 0; kk < GM_BK / 16; ++kk)  // K=16 a step: 8 A columns, +32 bytes of B (+2 in the desc)
+                    umma_bf16_tmem_a(tmem, a_tmem + 8u * kk, bdesc + 2u * kk, idesc, (kb | kk) != 0);
                 umma_commit(empty_tma(t));  // X and codes of this k block consumed
-                umma_commit(empty_w(w));    // dequantized tile consumed
+                umma_commit(empty_w(w));    // A stage consumed
                 ++issued;
             }
             if (issued == nkb) umma_commit(tmem_full);
@@ -255,34 +269,27 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         }
     } else {
         // ------------------------------------------------------- dequantization warps
-        const int r = threadIdx.x - 64;  // weight row within the tile, 0..255
+        const int sp = warp & 3;         // TMEM sub-partition: lanes (weight rows) 32 sp .. 32 sp + 31
+        const int hh = (warp - 2) >> 2;  // which 32-k half of each k block
+        const int r = 32 * sp + lane;    // weight row within the tile
         const int n = n0 + r;
         const bool nvalid = n < N;
         const int ng = K / G;
         const int64_t qrow = (int64_t)(nvalid ? n : 0) * ng;
-        // rows 4..7 of each 8 read their two 16-byte halves in the other order:
-        // the 8 lanes of a quarter-warp then hit 8 distinct bank groups
-        const int hfirst = (r >> 2) & 1;
-        // scale and offset of this row for the two 32-k halves of a k block,
-        // loaded GM_QPF blocks ahead and kept raw (not combined) until used, so
-        // that no instruction waits on them before their block comes up.
-        // Groups past K read as 0: with the zero-filled codes those weights are
-        // exactly 0.  With G >= GM_BK both halves share one group.
-        constexpr bool one_group = G >= GM_BK;
+        // scale and offset of this row for this thread's half of a k block,
+        // loaded GM_QPF blocks ahead and kept raw until used (no-TMA variant).
+        // Groups past K read as 0: with the zero-filled codes those weights
+        // are exactly 0.
         struct QRaw {
-            uint32_t s0, s1, o0, o1;
+            uint32_t s, o;
         };
         auto qload = [&](int kb) {
-            QRaw q = {0u, 0u, 0u, 0u};
+            QRaw q = {0u, 0u};
             if (!QT && kb < nkb && nvalid) {
-                const int j0 = (kb * GM_BK) / G;
-                if (j0 < ng) {
-                    q.s0 = ldg_nc_u16(scales + qrow + j0);
-                    q.o0 = ldg_nc_u16(offsets + qrow + j0);
-                }
-                if (!one_group && j0 + 1 < ng) {
-                    q.s1 = ldg_nc_u16(scales + qrow + j0 + 1);
-                    q.o1 = ldg_nc_u16(offsets + qrow + j0 + 1);
+                const int j = (kb * GM_BK + 32 * hh) / G;
+                if (j < ng) {
+                    q.s = ldg_nc_u16(scales + qrow + j);
+                    q.o = ldg_nc_u16(offsets + qrow + j);
                 }
             }
             return q;
@@ -291,8 +298,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         uint32_t cm, cg;  // LOP3 constants pinned in registers (0x4300 pairs are also the 128.0 bias)
         asm volatile("mov.b32 %0, %1;" : "=r"(cm) : "r"(0x000F000Fu));
         asm volatile("mov.b32 %0, %1;" : "=r"(cg) : "r"(0x43004300u));
-        // row r of a 128-byte-swizzled tile: chunk c lives at row_base ^ (c << 4)
-        const uint32_t row_sw = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((r & 7) << 4));
+        // the code tile arrives with the 32-byte swizzle: half hh of row r sits at 16 * (hh ^ bit 2 of r)
+        const uint32_t pcol = (uint32_t)(r * 32 + 16 * (hh ^ ((r >> 2) & 1)));
+        // this thread's 16 columns of an A stage, in its own TMEM lane
+        const uint32_t a_lane = tmem + ((uint32_t)(32 * sp) << 16) + (uint32_t)(GM_ACOL + 16 * hh);
         uint4 sq = make_uint4(0u, 0u, 0u, 0u), oq = sq;  // TMA variant: this row's 8 groups
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
@@ -320,71 +329,61 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 ok = false;
                 break;
             }
-            const unsigned char* prow = smem + GM_OFF_P + t * GM_P_BYTES + r * 32;
-            const uint4 first = *reinterpret_cast<const uint4*>(prow + 16 * hfirst);
-            const uint4 second = *reinterpret_cast<const uint4*>(prow + 16 * (hfirst ^ 1));
-            const uint4 h0 = hfirst ? second : first;
-            const uint4 h1 = hfirst ? first : second;
-            const uint32_t words[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-            const uint32_t wrow = sbase + GM_OFF_W + w * GM_W_BYTES + row_sw;
-            uint32_t s_lo, s_hi, o_lo, o_hi;  // (s,s) and (o,o) bf16 pairs of the two 32-k halves
+            tc_fence_after();  // the MMAs that read this A stage are complete
+            const uint4 words = lds128(sbase + GM_OFF_P + t * GM_P_BYTES + pcol);  // 32 codes of this half
+            uint32_t s2, o2;  // (s,s) and (o,o) bf16 pairs of this half's group
             if (QT) {
-                const int j0 = (kb % QSPAN) * GM_BK / G;  // group of the first half among the box's 8
-                const uint32_t sw = pick_word(sq, j0 >> 1), ow = pick_word(oq, j0 >> 1);
-                if (one_group) {
-                    const uint32_t sel = (j0 & 1) ? 0x3232u : 0x1010u;
-                    s_lo = s_hi = __byte_perm(sw, 0, sel);
-                    o_lo = o_hi = __byte_perm(ow, 0, sel);
-                } else {  // G == 32: the word holds exactly the two halves' groups
-                    s_lo = __byte_perm(sw, 0, 0x1010);
-                    s_hi = __byte_perm(sw, 0, 0x3232);
-                    o_lo = __byte_perm(ow, 0, 0x1010);
-                    o_hi = __byte_perm(ow, 0, 0x3232);
-                }
+                const int j = (kb % QSPAN) * GM_BK / G + (G == 32 ? hh : 0);  // group among the box's 8
+                const uint32_t sel = (j & 1) ? 0x3232u : 0x1010u;
+                s2 = __byte_perm(pick_word(sq, j >> 1), 0, sel);
+                o2 = __byte_perm(pick_word(oq, j >> 1), 0, sel);
             } else {
-                s_lo = __byte_perm(qc.s0, 0, 0x1010);
-                o_lo = __byte_perm(qc.o0, 0, 0x1010);
-                s_hi = one_group ? s_lo : __byte_perm(qc.s1, 0, 0x1010);
-                o_hi = one_group ? o_lo : __byte_perm(qc.o1, 0, 0x1010);
+                s2 = __byte_perm(qc.s, 0, 0x1010);
+                o2 = __byte_perm(qc.o, 0, 0x1010);
             }
-#pragma unroll
-            for (int c = 0; c < 8; ++c)  // 8 codes (one 16-byte bf16 chunk) per step
-                sts128(wrow ^ (uint32_t)(c << 4), dequant8(words[c], c < 4 ? s_lo : s_hi, c < 4 ? o_lo : o_hi, cm, cg));
-            fence_proxy_async_smem();
+            // 32 weights of this row -> 16 columns (two bf16 of consecutive k each) of the A stage
+            tmem_st_16cols(a_lane + (uint32_t)(w * GM_ASTAGE_COLS), dequant8(words.x, s2, o2, cm, cg),
+                           dequant8(words.y, s2, o2, cm, cg), dequant8(words.z, s2, o2, cm, cg),
+                           dequant8(words.w, s2, o2, cm, cg));
+            tmem_st_wait();
+            tc_fence_before();
             mbar_arrive(full_deq(w));
         }
         // ----------------------------------------------------------------- epilogue
         if (ok && mbar_wait_bounded(tmem_full, 0, abort_flag, &g_gemm_fault, 8u, GM_WAIT_LIMIT_NS)) {
             tc_fence_after();
-            const int quad = warp & 3;             // TMEM lanes 32*quad .. +31 (this warp's sub-partition)
-            const int half = (warp - 2) >> 2;      // columns [128*half, 128*half + 128)
-            const int m = m0 + quad * 32 + lane;   // token of this thread's TMEM lane
-            const bool mvalid = m < M;
-            const bool vec = (N % 8) == 0;
+            // D[row][token]: this warp's 32 rows (its TMEM lanes) x tokens [128 hh, 128 hh + 128);
+            // each 32 x 32 block goes through shared memory (the X ring is free now) so that
+            // every lane writes 32 rows of one token as 64 contiguous bytes of Y
+            unsigned char* stage = smem + GM_OFF_X + (warp - 2) * GM_STAGE_BYTES;
+            const uint32_t stage_s = smem_u32(stage);
+            const int nrow0 = n0 + 32 * sp;  // first weight row of this warp
+            const bool vec = (N % 8) == 0 && nrow0 + 32 <= N;
 #pragma unroll 1
             for (int cc = 0; cc < 4; ++cc) {
-                const int col = half * 128 + cc * 32;
+                const int col = 128 * hh + 32 * cc;  // first token column of the block
                 uint32_t v[32];
-                tmem_ld_32cols(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)col, v);
+                tmem_ld_32cols(tmem + ((uint32_t)(32 * sp) << 16) + (uint32_t)col, v);
                 tmem_ld_wait();
-                const int nb = n0 + col;
-                if (!mvalid || nb >= N) continue;
-                uint16_t* yrow = Y + (int64_t)m * N + nb;
-                if (vec && nb + 32 <= N) {
+                // stage[token i][row lane] = bf16(D[row][token])
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint4 o;
-                        o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
-                        o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
-                        o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
-                        o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
-                        *reinterpret_cast<uint4*>(yrow + 8 * q) = o;
+                for (int i = 0; i < 32; ++i)
+                    *reinterpret_cast<uint16_t*>(stage + i * GM_STAGE_PITCH + 2 * lane) =
+                        (uint16_t)float_to_bf16_bits(__uint_as_float(v[i]));
+                __syncwarp();
+                const int m = m0 + col + lane;  // the token this lane writes
+                if (m < M && nrow0 < N) {
+                    uint16_t* yrow = Y + (int64_t)m * N + nrow0;
+                    if (vec) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            *reinterpret_cast<uint4*>(yrow + 8 * q) = lds128(stage_s + lane * GM_STAGE_PITCH + 16 * q);
+                    } else {
+                        for (int i = 0; i < 32 && nrow0 + i < N; ++i)
+                            yrow[i] = *reinterpret_cast<const uint16_t*>(stage + lane * GM_STAGE_PITCH + 2 * i);
                     }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (nb + i < N) yrow[i] = (uint16_t)float_to_bf16_bits(__uint_as_float(v[i]));
                 }
+                __syncwarp();  // the block is rewritten by the next chunk
             }
         }
     }
@@ -403,7 +402,7 @@ static cudaError_t launch_gemm_g(const CUtensorMap& tx, const CUtensorMap& tp, c
     auto kern = gemm_kernel<G, QT>;
     cudaError_t e = ensure_kernel_attrs(reinterpret_cast<const void*>(kern), GM_SMEM_BYTES, false);
     if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)((N + GM_BN - 1) / GM_BN), (unsigned)((M + GM_BM - 1) / GM_BM));
+    const dim3 grid((unsigned)((N + GM_BW - 1) / GM_BW), (unsigned)((M + GM_BT - 1) / GM_BT));
     kern<<<grid, GM_THREADS, GM_SMEM_BYTES, stream>>>(tx, tp, ts, to, scales, offsets, Y, M, N, K);
     return cudaGetLastError();
 }
@@ -411,30 +410,31 @@ static cudaError_t launch_gemm_g(const CUtensorMap& tx, const CUtensorMap& tp, c
 cudaError_t launch_gemm(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
                         const uint16_t* offsets, int64_t N, int g, uint16_t* Y, cudaStream_t stream,
                         const char** detail) {
-    if ((N + GM_BN - 1) / GM_BN > 0x7FFFFFFF || (M + GM_BM - 1) / GM_BM > 65535) {
+    if ((N + GM_BW - 1) / GM_BW > 0x7FFFFFFF || (M + GM_BT - 1) / GM_BT > 65535) {
         *detail = "problem too large for the GEMM grid";
         return cudaErrorInvalidValue;
     }
     CUtensorMap tx, tp;
-    // X: [M][K] bf16, box 128 tokens x 64 k (128 bytes), 128-byte swizzle (the UMMA A layout)
+    // X: [M][K] bf16, box 256 tokens x 64 k (128 bytes), 128-byte swizzle (the UMMA B layout)
     cudaError_t e = encode_tensor_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)K, (uint64_t)M,
-                                         (uint64_t)K * 2, GM_BK, GM_BM, CU_TENSOR_MAP_SWIZZLE_128B, detail);
+                                         (uint64_t)K * 2, GM_BK, GM_BT, CU_TENSOR_MAP_SWIZZLE_128B, detail);
     if (e != cudaSuccess) return e;
-    // codes: [N][K/2] bytes, box 256 rows x 32 bytes
+    // codes: [N][K/2] bytes, box 128 rows x 32 bytes, 32-byte swizzle (the two 16-byte halves of
+    // rows 4..7 of every 8 trade places: conflict-free reads of one half per thread)
     e = encode_tensor_map_2d(&tp, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)(K / 2), (uint64_t)N, (uint64_t)(K / 2),
-                             GM_BK / 2, GM_BN, CU_TENSOR_MAP_SWIZZLE_NONE, detail);
+                             GM_BK / 2, GM_BW, CU_TENSOR_MAP_SWIZZLE_32B, detail);
     if (e != cudaSuccess) return e;
-    // scales / offsets: [N][K/g] bf16, box 256 rows x 8 groups, when a row is
+    // scales / offsets: [N][K/g] bf16, box 128 rows x 8 groups, when a row is
     // a whole number of 16-byte pieces (the tensor-map stride rule)
     const int64_t ng = K / g;
     const bool qt = ng % 8 == 0;
     CUtensorMap ts = tp, to = tp;
     if (qt) {
         e = encode_tensor_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, (uint64_t)ng, (uint64_t)N,
-                                 (uint64_t)ng * 2, 8, GM_BN, CU_TENSOR_MAP_SWIZZLE_NONE, detail);
+                                 (uint64_t)ng * 2, 8, GM_BW, CU_TENSOR_MAP_SWIZZLE_NONE, detail);
         if (e == cudaSuccess)
             e = encode_tensor_map_2d(&to, CU_TENSOR_MAP_DATA_TYPE_UINT16, offsets, (uint64_t)ng, (uint64_t)N,
-                                     (uint64_t)ng * 2, 8, GM_BN, CU_TENSOR_MAP_SWIZZLE_NONE, detail);
+                                     (uint64_t)ng * 2, 8, GM_BW, CU_TENSOR_MAP_SWIZZLE_NONE, detail);
         if (e != cudaSuccess) return e;
     }
     const int m = (int)M, n = (int)N, k = (int)K;

@@ -143,7 +143,7 @@ __device__ __forceinline__ void dq_mma(float (&c)[4], uint32_t wa, uint32_t wb, 
 }
 
 template <int G, int MX, bool QT>
-__global__ void __launch_bounds__(ST_THREADS, 6)
+__global__ void __launch_bounds__(ST_THREADS, MX == 8 ? 5 : 6)
 stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
               const __grid_constant__ CUtensorMap tm_o, const StreamArgs p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
