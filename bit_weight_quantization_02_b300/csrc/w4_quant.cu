@@ -9,7 +9,12 @@
 // Every floating-point step is one IEEE fp32 operation with round-to-nearest
 // (__fsub_rn / __fdiv_rn / __fmul_rn / __fadd_rn: no contraction, no
 // approximate division), so the results are bit-exact and independent of the
-// launch shape.
+// launch shape.  The per-weight quotient (w - o)/s takes a fast route that
+// gives the same code: t' = (w - o) * rcp_rn(s) differs from the correctly
+// rounded quotient t by less than 2^-18 (|t| < 16: two roundings of 2^-24
+// relative plus half an ulp of t), so rint(t') == rint(t) unless t' lies
+// within 2^-16 of a half-integer; those weights (exact ties included) are
+// divided exactly.
 //
 // Both kernels are HBM-bound streams: one thread owns 8 consecutive weights
 // (one 16-byte load of bf16, one 4-byte store of codes); the g/8 threads of a
@@ -65,13 +70,17 @@ quantize_kernel(const uint4* __restrict__ W, int64_t n_chunks, uint32_t* __restr
     const float s = bf16_bits_to_float(s_bits);
     const float o = mn;
 
+    const float rs = __frcp_rn(s);  // correctly rounded 1/s (s >= 1e-6, a normal bf16 value)
     const uint32_t words[4] = {raw.x, raw.y, raw.z, raw.w};
     uint32_t packed = 0;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
         const uint32_t b = (e & 1) ? (words[e >> 1] >> 16) : (words[e >> 1] & 0xFFFFu);
         const float v = bf16_bits_to_float(b);
-        const float t = __fdiv_rn(__fsub_rn(v, o), s);
+        const float d = __fsub_rn(v, o);
+        float t = __fmul_rn(d, rs);
+        if (fabsf(__fsub_rn(t - floorf(t), 0.5f)) < 1.52587890625e-05f)  // within 2^-16 of x.5
+            t = __fdiv_rn(d, s);
         int q = __float2int_rn(t);
         q = min(max(q, 0), 15);
         packed |= (uint32_t)q << (4 * e);
