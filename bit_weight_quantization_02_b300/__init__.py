@@ -233,7 +233,7 @@ def w4_repack(Wq: torch.Tensor, scales: torch.Tensor, offsets: torch.Tensor, gro
 
 
 def w4_linear_repacked(X: torch.Tensor, packed: Repacked, out=None, workspace: Workspace | None = None):
-    """Y bf16 [M,N] = X . dequant(W)^T for M <= 8 with W in the decode layout."""
+    """Y bf16 [M,N] = X . dequant(W)^T for M <= 32 with W in the decode layout."""
     lib = load_library()
     _bits16(X, "X")
     M, K = X.shape

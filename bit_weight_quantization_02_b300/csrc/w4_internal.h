@@ -31,7 +31,7 @@ cudaError_t launch_skinny(const SkinnyPlan& plan, const uint16_t* X, int64_t M, 
                           const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
                           cudaStream_t stream, const char** detail);
 
-// Persistent stream-K decode kernel (M <= 8): needs a zero-initialized,
+// Persistent stream-K decode kernel (M <= 32): needs a zero-initialized,
 // self-cleaning workspace of stream_ws_bytes(M, N) bytes.
 struct StreamPlan {
     int nkc;          // 256-k units per 16-row tile
@@ -40,7 +40,7 @@ struct StreamPlan {
     size_t smem;      // dynamic shared memory bytes per block
     size_t ws_bytes;  // workspace bytes
 };
-constexpr int STREAM_MAX_M = 8;
+constexpr int STREAM_MAX_M = 32;
 constexpr int DECODE_MAX_M = 32;  // decode-layout kernel
 size_t stream_ws_bytes(int64_t M, int64_t N);
 bool plan_stream(int64_t M, int64_t N, int64_t K, int g, StreamPlan* plan);

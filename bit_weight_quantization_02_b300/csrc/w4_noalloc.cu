@@ -57,7 +57,7 @@ extern "C" w4_status w4_linear_static(const uint16_t* X, int64_t M, int64_t K, c
         return static_fail(W4_ERR_UNSUPPORTED, "group_size not in {32, 64, 128}");
     if (K <= 0 || N < 0 || M < 0 || K % group_size != 0 || K > 0x7FFFFFFFLL || N > 0x7FFFFFFFLL)
         return static_fail(W4_ERR_INVALID_ARG, "bad shape (K > 0, N >= 0, M >= 0, K % group_size == 0)");
-    if (M > w4::STREAM_MAX_M) return static_fail(W4_ERR_INVALID_ARG, "w4_linear_static takes M <= 8");
+    if (M > 8) return static_fail(W4_ERR_INVALID_ARG, "w4_linear_static takes M <= 8");
     if (M == 0 || N == 0) return W4_OK;
     if (!X || !Wq || !scales || !offsets || !Y) return static_fail(W4_ERR_INVALID_ARG, "NULL pointer");
     if (((uintptr_t)X | (uintptr_t)Wq | (uintptr_t)scales | (uintptr_t)offsets | (uintptr_t)Y) & 15u)

@@ -1,4 +1,4 @@
-// w4_stream.cu -- persistent stream-K bf16 x int4 linear for decode (M <= 8).
+// w4_stream.cu -- persistent stream-K bf16 x int4 linear for decode (M <= 32).
 //
 // Y[m,n] = sum_k X[m,k] * w'[n,k], w' = bf16(q*s + o), fp32 accumulation
 // (Optimum Quanto: bf16 x int4 matmul, result accumulated at higher precision,
@@ -16,9 +16,12 @@
 //    past N and K); the 32 lanes fetch its scales and offsets with 4-byte
 //    cp.async; all complete on the slot's mbarrier.  The first three units are
 //    requested before the programmatic-dependent-launch wait.
-//  * X (only 256 k x M tokens per unit) is loaded one unit ahead into
-//    registers, permuted to the MMA k order and staged in the warp's shared
-//    memory; tokens beyond M read a zero row.
+//  * X (only 256 k x M tokens per unit), up to 8 tokens: loaded one unit
+//    ahead into registers, permuted to the MMA k order and staged in the
+//    warp's shared memory (tokens beyond M read a zero row).  9 to 32 tokens:
+//    every lane reads its tokens' 8-k chunks straight from global memory
+//    (L1-cached) and permutes them in registers, and one dequantized A
+//    fragment feeds one MMA per group of 8 tokens.
 //  * Dequantization and products as in the skinny kernel: LOP3 nibble pairs,
 //    exact subtract + one bf16 FMA, mma.m16n8k16 with the weights as the A
 //    operand and the tokens as B (swap AB).
@@ -65,8 +68,10 @@ struct StreamArgs {
 
 // per-warp shared memory after the code slots: qparam slots, X slots, zero row, barriers
 __host__ __device__ inline int st_qslot_bytes(int g) { return 2 * 16 * (ST_UK / g) * 2; }
+// X slots (2 units x M token rows) and a zero row: only up to 8 tokens (beyond, X comes through L1)
+__host__ __device__ inline int st_xslot_bytes(int M) { return M <= 8 ? (2 * M + 1) * ST_XPITCH : 0; }
 __host__ __device__ inline int st_rest_bytes(int M, int g) {
-    const int b = ST_DEPTH * st_qslot_bytes(g) + (2 * M + 1) * ST_XPITCH + 8 * ST_DEPTH;
+    const int b = ST_DEPTH * st_qslot_bytes(g) + st_xslot_bytes(M) + 8 * ST_DEPTH;
     return (b + 127) & ~127;  // qparam slots are TMA destinations: 128-byte aligned
 }
 __host__ __device__ inline int st_smem_bytes(int M, int g) {
@@ -142,8 +147,43 @@ __device__ __forceinline__ void dq_mma(float (&c)[4], uint32_t wa, uint32_t wb, 
           "r"(c128), "n"(SH), "n"(SH + 4));
 }
 
+// The four A-fragment registers of one MMA step (as in dq_mma), for reuse by
+// several token groups.
+template <int SH>
+__device__ __forceinline__ void dq_frag(uint32_t wa, uint32_t wb, uint32_t sa2, uint32_t oa2, uint32_t sb2,
+                                        uint32_t ob2, uint32_t cm, uint32_t cg, uint32_t (&A)[4]) {
+    asm("{\n\t.reg .b32 t;\n\t"
+        "shr.b32 t, %4, %12;\n\t"
+        "lop3.b32 %0, t, %10, %11, 0xEA;\n\t"
+        "shr.b32 t, %4, %13;\n\t"
+        "lop3.b32 %2, t, %10, %11, 0xEA;\n\t"
+        "shr.b32 t, %5, %12;\n\t"
+        "lop3.b32 %1, t, %10, %11, 0xEA;\n\t"
+        "shr.b32 t, %5, %13;\n\t"
+        "lop3.b32 %3, t, %10, %11, 0xEA;\n\t"
+        "sub.rn.bf16x2 %0, %0, %11;\n\t"
+        "sub.rn.bf16x2 %1, %1, %11;\n\t"
+        "sub.rn.bf16x2 %2, %2, %11;\n\t"
+        "sub.rn.bf16x2 %3, %3, %11;\n\t"
+        "fma.rn.bf16x2 %0, %0, %6, %7;\n\t"
+        "fma.rn.bf16x2 %1, %1, %8, %9;\n\t"
+        "fma.rn.bf16x2 %2, %2, %6, %7;\n\t"
+        "fma.rn.bf16x2 %3, %3, %8, %9;\n\t}"
+        : "=&r"(A[0]), "=&r"(A[1]), "=&r"(A[2]), "=&r"(A[3])
+        : "r"(wa), "r"(wb), "r"(sa2), "r"(oa2), "r"(sb2), "r"(ob2), "r"(cm), "r"(cg), "n"(SH), "n"(SH + 4));
+}
+__device__ __forceinline__ void mma_frag(float (&c)[4], const uint32_t (&A)[4], uint32_t x0, uint32_t x1) {
+    mma_bf16_16816_st(c, A[0], A[1], A[2], A[3], x0, x1);
+}
+__device__ __forceinline__ uint4 ldg_nc_v4_st(const void* p) {
+    uint4 r;
+    asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
+// MX: token capacity (1, 2, 4, 8: X staged in shared memory; 16, 32: X through L1).
 template <int G, int MX, bool QT>
-__global__ void __launch_bounds__(ST_THREADS, MX == 8 ? 5 : 6)
+__global__ void __launch_bounds__(ST_THREADS, MX == 32 ? 4 : (MX >= 8 ? 5 : 6))
 stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
               const __grid_constant__ CUtensorMap tm_o, const StreamArgs p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -169,17 +209,20 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     const uint32_t wslots = smem_u32(smem) + warp * (ST_DEPTH * ST_WSLOT);
     unsigned char* rbase = smem + ST_WARPS * ST_DEPTH * ST_WSLOT + warp * rest;
     const uint32_t qslots = smem_u32(rbase);
+    constexpr bool L1X = MX > 8;  // X through L1 instead of staged slots
+    constexpr int MT = L1X ? MX / 8 : 1;  // groups of 8 tokens
     unsigned char* xslots = rbase + ST_DEPTH * QSLOT;                   // 2 slots x M token rows
     unsigned char* zrow = xslots + 2 * p.M * ST_XPITCH;                 // zeros for tokens >= M
-    const uint32_t bars = smem_u32(zrow + ST_XPITCH);                    // ST_DEPTH mbarriers
+    const uint32_t bars = smem_u32(rbase + ST_DEPTH * QSLOT + st_xslot_bytes(p.M));  // ST_DEPTH mbarriers
     const int ng = p.K / G;
 
     if (lane == 0) {  // arrivals per fill: the TMA arrive (+ 32 cp.async arrivals when qparams go that way)
         for (int d = 0; d < ST_DEPTH; ++d) mbar_init(bars + 8 * d, QT ? 1 : 33);
         mbar_fence_init();
     }
-    for (int c = lane; c < ST_XPITCH / 16; c += 32)
-        *reinterpret_cast<uint4*>(zrow + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
+    if (!L1X)
+        for (int c = lane; c < ST_XPITCH / 16; c += 32)
+            *reinterpret_cast<uint4*>(zrow + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
     __syncwarp();
 
     // this lane's qparam pieces: fixed (array, row, piece) for every unit
@@ -246,19 +289,19 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     // activations may come from the previous kernel: wait for it
     griddep_wait();
 
-    // X of a unit: lane c holds 8-k chunk c of every token
-    uint4 xr[MX];
+    // X of a unit: lane c holds 8-k chunk c of every token (staged path)
+    uint4 xr[L1X ? 1 : MX];
     const uint16_t* xlane = p.X + 8 * lane;
     auto load_x = [&](int kc) {
         const int k = kc * ST_UK + 8 * lane;
 #pragma unroll
-        for (int m = 0; m < MX; ++m)
+        for (int m = 0; m < (L1X ? 0 : MX); ++m)
             if (m < p.M) xr[m] = (k < p.K) ? ldg_cg_v4(xlane + (int64_t)m * p.K + kc * ST_UK) : make_uint4(0u, 0u, 0u, 0u);
     };
     const uint32_t xst = (uint32_t)(16 * st_x_slot(lane));
     auto store_x = [&](unsigned char* slot) {
 #pragma unroll
-        for (int m = 0; m < MX; ++m)
+        for (int m = 0; m < (L1X ? 0 : MX); ++m)
             if (m < p.M) {
                 uint4 o;
                 o.x = __byte_perm(xr[m].x, xr[m].z, 0x5410);  // (x0, x4)
@@ -283,20 +326,26 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     const uint32_t xrow_off = (uint32_t)(gid * ST_XPITCH);
     const uint32_t zaddr = smem_u32(zrow);
 
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[MT][4];
+#pragma unroll
+    for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+    // L1 path: this lane's tokens (8t + gid) read their 8-k chunk at 32 tq + 8 j of each half
+    const uint16_t* xl1 = p.X + (int64_t)gid * p.K + 32 * tq;
     int tile = tile0, kc = kc0, kc_first = kc0;  // unit being computed
     int x_kc = kc0;                               // unit whose X sits in xr
     bool ok = true;
     int d = 0;
     uint32_t phase = 0;
 
-    load_x(x_kc);
+    if (!L1X) load_x(x_kc);
     for (int it = 0; it < nunits; ++it) {
         unsigned char* xs = xslots + (it & 1) * p.M * ST_XPITCH;
-        store_x(xs);
-        if (it + 1 < nunits) {
-            if (++x_kc == p.nkc) x_kc = 0;
-            load_x(x_kc);
+        if (!L1X) {
+            store_x(xs);
+            if (it + 1 < nunits) {
+                if (++x_kc == p.nkc) x_kc = 0;
+                load_x(x_kc);
+            }
         }
         ok = mbar_wait_bounded(bars + 8 * d, phase, nullptr, &g_stream_fault, 1u, ST_WAIT_LIMIT_NS) && ok;
         __syncwarp();
@@ -320,9 +369,32 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             const uint32_t wb4[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const uint4 xv = lds128_st(bbase + 256u * h + boff[j]);
-                dq_mma<0>(acc, wa4[j], wb4[j], sa2, oa2, sb2, ob2, xv.x, xv.y, cm, cg, c128);
-                dq_mma<8>(acc, wa4[j], wb4[j], sa2, oa2, sb2, ob2, xv.z, xv.w, cm, cg, c128);
+                if (!L1X) {
+                    const uint4 xv = lds128_st(bbase + 256u * h + boff[j]);
+                    dq_mma<0>(acc[0], wa4[j], wb4[j], sa2, oa2, sb2, ob2, xv.x, xv.y, cm, cg, c128);
+                    dq_mma<8>(acc[0], wa4[j], wb4[j], sa2, oa2, sb2, ob2, xv.z, xv.w, cm, cg, c128);
+                } else {
+                    const int kx = kc * ST_UK + 128 * h + 8 * j;  // + 32 tq inside xl1
+                    const bool kin = kx + 32 * tq < p.K;
+                    uint4 xp[MT];
+#pragma unroll
+                    for (int t = 0; t < MT; ++t) {
+                        const uint4 x = (kin && 8 * t + gid < p.M)
+                                            ? ldg_nc_v4_st(xl1 + (int64_t)(8 * t) * p.K + kx)
+                                            : make_uint4(0u, 0u, 0u, 0u);
+                        xp[t].x = __byte_perm(x.x, x.z, 0x5410);  // (x0, x4)
+                        xp[t].y = __byte_perm(x.x, x.z, 0x7632);  // (x1, x5)
+                        xp[t].z = __byte_perm(x.y, x.w, 0x5410);  // (x2, x6)
+                        xp[t].w = __byte_perm(x.y, x.w, 0x7632);  // (x3, x7)
+                    }
+                    uint32_t A[4];
+                    dq_frag<0>(wa4[j], wb4[j], sa2, oa2, sb2, ob2, cm, cg, A);
+#pragma unroll
+                    for (int t = 0; t < MT; ++t) mma_frag(acc[t], A, xp[t].x, xp[t].y);
+                    dq_frag<8>(wa4[j], wb4[j], sa2, oa2, sb2, ob2, cm, cg, A);
+#pragma unroll
+                    for (int t = 0; t < MT; ++t) mma_frag(acc[t], A, xp[t].z, xp[t].w);
+                }
             }
         }
         __syncwarp();
@@ -339,20 +411,24 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         // end of a row tile or of the range: hand the tile's sums on
         if (it + 1 == nunits || kc == p.nkc - 1) {
             const int n_a = tile * 16 + pr, n_b = n_a + 8;
-            const int m0 = 2 * tq;  // acc = D[row n_a: tokens m0, m0+1 | row n_b: tokens m0, m0+1]
+            // acc[t] = D[row n_a: tokens 8t + 2tq, +1 | row n_b: the same tokens]
             if (kc_first == 0 && kc == p.nkc - 1) {  // this warp summed all of the tile's k
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int m = m0 + (i & 1), n = (i < 2) ? n_a : n_b;
-                    if (m < p.M && n < p.N) p.Y[(int64_t)m * p.N + n] = (uint16_t)float_to_bf16_bits(acc[i]);
-                }
+                for (int t = 0; t < MT; ++t)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int m = 8 * t + 2 * tq + (i & 1), n = (i < 2) ? n_a : n_b;
+                        if (m < p.M && n < p.N) p.Y[(int64_t)m * p.N + n] = (uint16_t)float_to_bf16_bits(acc[t][i]);
+                    }
             } else {
                 float got = 0.f;  // old values returned by the adds (only their arrival matters)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int m = m0 + (i & 1), n = (i < 2) ? n_a : n_b;
-                    if (m < p.M && n < p.N) got += atomicAdd(p.ws + (int64_t)m * p.N + n, acc[i]);
-                }
+                for (int t = 0; t < MT; ++t)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int m = 8 * t + 2 * tq + (i & 1), n = (i < 2) ? n_a : n_b;
+                        if (m < p.M && n < p.N) got += atomicAdd(p.ws + (int64_t)m * p.N + n, acc[t][i]);
+                    }
                 // the vote reads every lane's `got`, so all adds have returned before the counter
                 // moves; threadIdx.y is 0 in this one-dimensional block, so `done` is always 1
                 const unsigned int dep = __float_as_uint(got) & (0u - threadIdx.y);
@@ -373,7 +449,8 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                     if (lane == 0) atomicExch(p.count + tile, 0u);
                 }
             }
-            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+#pragma unroll
+            for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
             kc_first = 0;
         }
         advance(tile, kc);
@@ -437,7 +514,9 @@ static cudaError_t launch_stream_g(const StreamPlan& plan, const CUtensorMap& tw
     if (a.M <= 1) return launch_stream_gm<G, 1, QT>(plan, tw, ts, to, a, stream);
     if (a.M <= 2) return launch_stream_gm<G, 2, QT>(plan, tw, ts, to, a, stream);
     if (a.M <= 4) return launch_stream_gm<G, 4, QT>(plan, tw, ts, to, a, stream);
-    return launch_stream_gm<G, 8, QT>(plan, tw, ts, to, a, stream);
+    if (a.M <= 8) return launch_stream_gm<G, 8, QT>(plan, tw, ts, to, a, stream);
+    if (a.M <= 16) return launch_stream_gm<G, 16, QT>(plan, tw, ts, to, a, stream);
+    return launch_stream_gm<G, 32, QT>(plan, tw, ts, to, a, stream);
 }
 
 cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,

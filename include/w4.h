@@ -65,11 +65,11 @@ typedef enum w4_status {
 
 /* Kernel choice for w4_linear_ex. */
 typedef enum w4_kernel {
-    W4_KERNEL_AUTO = 0,            /* stream kernel for M <= 8 (with workspace), skinny for M <= 32, GEMM above */
+    W4_KERNEL_AUTO = 0,            /* stream kernel for M <= 32 (with workspace), else cluster for M <= 32, GEMM above */
     W4_KERNEL_SKINNY = 1,          /* best memory-bound kernel for M <= 32 (stream, else cluster) */
     W4_KERNEL_GEMM = 2,            /* tcgen05 tensor-core GEMM; any M >= 1 */
     W4_KERNEL_SKINNY_CLUSTER = 3,  /* cluster split-K skinny kernel, M <= 32, no workspace */
-    W4_KERNEL_STREAM = 4           /* persistent stream-K kernel, M <= 8, needs the workspace */
+    W4_KERNEL_STREAM = 4           /* persistent stream-K kernel, M <= 32, needs the workspace */
 } w4_kernel;
 
 /*
@@ -107,10 +107,10 @@ W4_API w4_status w4_dequantize(const uint8_t *Wq, const uint16_t *scales,
 
 /*
  * w4_linear_workspace_bytes -- workspace bytes for this problem: what
- * w4_linear needs to run the persistent stream-K decode kernel (M <= 8 and
+ * w4_linear needs to run the persistent stream-K decode kernel (M <= 32 and
  * K/group_size even; without it the call still works on the cluster split-K
- * kernel, usually slower for decode), and what w4_linear_repacked needs
- * (M <= 32).  0 when neither applies (M > 32).
+ * kernel, usually slower), and what w4_linear_repacked needs (M <= 32).
+ * 0 when neither applies (M > 32).
  */
 W4_API size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int group_size);
 
@@ -120,8 +120,8 @@ W4_API size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int gro
  * Source: the mixed bf16 x int4 matmul of Optimum Quanto (feature list and
  * "Pitfalls when quantizing activations": accumulation in fp32).
  *
- * Kernel choice: M <= 8 with a workspace of w4_linear_workspace_bytes runs
- * the persistent stream-K decode kernel; otherwise M <= 32 runs the cluster
+ * Kernel choice: M <= 32 with a workspace of w4_linear_workspace_bytes runs
+ * the persistent stream-K decode kernel; without one M <= 32 runs the cluster
  * split-K skinny kernel; larger M the tcgen05 tensor-core GEMM.  The kernels
  * dequantize each weight as bf16(q * s + o) with a single rounding, which can
  * differ from w4_dequantize's double rounding by one bf16 ulp; the summation

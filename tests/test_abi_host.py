@@ -62,18 +62,19 @@ def test_sizes(lib):
 
 
 def test_workspace_plan(lib):
-    # the stream kernel (M <= 8, even K/g) needs [M][N] fp32 sums + one counter per 16 rows
+    # the stream kernel (M <= 32, even K/g) needs [M][N] fp32 sums + one counter per 16 rows
     assert lib.w4_linear_workspace_bytes(1, 1024, 4096, 32) == 4096 + 64 * 4
     assert lib.w4_linear_workspace_bytes(8, 14336, 4096, 128) >= 8 * 14336 * 4 + 896 * 4
-    assert lib.w4_linear_workspace_bytes(9, 1024, 4096, 32) == 9 * 4096 + 64 * 4  # decode layout, M <= 32
+    assert lib.w4_linear_workspace_bytes(9, 1024, 4096, 32) == 9 * 4096 + 64 * 4
+    assert lib.w4_linear_workspace_bytes(32, 1000, 4096, 32) == 32 * 4000 + 63 * 4  # [M][N] sums padded to 256 B
     assert lib.w4_linear_workspace_bytes(33, 1024, 4096, 32) == 0    # M > 32: no kernel uses a workspace
     assert lib.w4_linear_workspace_bytes(1, 100, 96, 32) == 512 + 7 * 4  # K/g odd: the decode layout's need
     assert lib.w4_linear_workspace_bytes(0, 100, 128, 32) == 0
 
 
 def test_linear_kernel_choice_rules(lib):
-    # the stream kernel only takes M <= 8 and needs its workspace; the checks run before any launch
-    assert lib.w4_linear_ex(FAKE, 9, 64, FAKE, FAKE, FAKE, 4, 32, FAKE, None, 0, 4, None) == INVALID
+    # the stream kernel only takes M <= 32 and needs its workspace; the checks run before any launch
+    assert lib.w4_linear_ex(FAKE, 33, 64, FAKE, FAKE, FAKE, 4, 32, FAKE, FAKE, 1 << 20, 4, None) == INVALID
     assert lib.w4_linear_ex(FAKE, 2, 64, FAKE, FAKE, FAKE, 4, 32, FAKE, None, 0, 4, None) == INVALID
     assert b"workspace" in lib.w4_last_error_detail()
     assert lib.w4_linear_ex(FAKE, 33, 64, FAKE, FAKE, FAKE, 4, 32, FAKE, None, 0, 3, None) == INVALID

@@ -171,8 +171,8 @@ def test_linear_stream(g, nk):
     N, K = nk
     if K % g or (K // g) % 2:
         pytest.skip("the stream kernel needs an even K/g")
-    ws = w4.Workspace(DEV).reserve_for(8, N, K, g)
-    for M in (1, 2, 3, 5, 8):
+    ws = w4.Workspace(DEV).reserve_for(32, N, K, g)
+    for M in (1, 2, 3, 5, 8, 9, 16, 17, 31, 32):
         (X, Wq, sc, of), y_ref = _problem(M, N, K, g, seed=13 * M + N + g)
         assert_linear_ok(gpu_linear(X, Wq, sc, of, g, w4.KERNEL_STREAM, workspace=ws), y_ref,
                          f"stream M={M} N={N} K={K} g={g}")
@@ -245,12 +245,15 @@ def test_linear_auto_dispatch_and_both_kernels_agree():
     (X, Wq, sc, of), y_ref = _problem(32, 768, 2048, 32, seed=5)
     ys = gpu_linear(X, Wq, sc, of, 32, w4.KERNEL_SKINNY_CLUSTER)
     yg = gpu_linear(X, Wq, sc, of, 32, w4.KERNEL_GEMM)
-    ya = gpu_linear(X, Wq, sc, of, 32)
-    assert torch.equal(ys.view(torch.int16), ya.view(torch.int16))  # 8 < M <= 32 goes to the cluster kernel
-    assert_linear_ok(ys, y_ref, "skinny")
-    assert_linear_ok(yg, y_ref, "gemm")
-    # the two kernels round differently but agree to bf16 precision
-    assert float((ys.float() - yg.float()).abs().max()) <= 2e-2 * float(yg.float().abs().max())
+    yt = gpu_linear(X, Wq, sc, of, 32, w4.KERNEL_STREAM)
+    ya = gpu_linear(X, Wq, sc, of, 32)  # M <= 32 with the default workspace: the stream kernel
+    y0 = gpu_linear(X, Wq, sc, of, 32, w4.KERNEL_AUTO, workspace=w4.Workspace(DEV))  # no workspace: cluster
+    assert torch.equal(ys.view(torch.int16), y0.view(torch.int16))
+    for y, what in ((ys, "skinny"), (yg, "gemm"), (yt, "stream"), (ya, "auto")):
+        assert_linear_ok(y, y_ref, what)
+    # the kernels round differently but agree to bf16 precision
+    for y in (ys, yt, ya):
+        assert float((y.float() - yg.float()).abs().max()) <= 2e-2 * float(yg.float().abs().max())
 
 
 def test_workspace_shared_by_calls_of_different_shapes():
