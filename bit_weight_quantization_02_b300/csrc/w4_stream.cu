@@ -25,6 +25,15 @@
 //  * Dequantization and products as in the skinny kernel: LOP3 nibble pairs,
 //    exact subtract + one bf16 FMA, mma.m16n8k16 with the weights as the A
 //    operand and the tokens as B (swap AB).
+//  * One token: the eight token columns of the MMA would hold seven zero
+//    columns, so they hold the unit's eight 32-k slices instead.  Lane
+//    (gid, tq) supplies X only where its column gid is the slice its codes
+//    come from (gid = tq + 4h), zero elsewhere, so column c of D sums slice c
+//    alone.  The A operand is the raw LOP3 value 128 + q (no subtract, no
+//    scale, no offset): D[n][c] = sum (128 + q) x over the slice, and the
+//    group's scale and offset are applied to those sums in fp32,
+//    y += s (D - 128 xs) + o xs with xs the slice's sum of X.  That halves the
+//    per-weight instructions, and the weights are never rounded to bf16.
 //  * A warp that covers all of a row tile's k writes bf16 Y directly.  A tile
 //    split between warps is summed in fp32 with atomic adds in the caller's
 //    workspace; the warp that completes the tile's k count (atomic counter,
@@ -175,6 +184,56 @@ __device__ __forceinline__ void dq_frag(uint32_t wa, uint32_t wb, uint32_t sa2, 
 __device__ __forceinline__ void mma_frag(float (&c)[4], const uint32_t (&A)[4], uint32_t x0, uint32_t x1) {
     mma_bf16_16816_st(c, A[0], A[1], A[2], A[3], x0, x1);
 }
+// One MMA step on raw codes (the one-token path): A = 128 + q straight from
+// LOP3, B = X or zero per lane.  ZC starts from a zero accumulator.
+template <int SH, bool ZC>
+__device__ __forceinline__ void raw_mma(float (&c)[4], uint32_t wa, uint32_t wb, uint32_t x0, uint32_t x1,
+                                        uint32_t cm, uint32_t cg) {
+    if constexpr (ZC) {
+        asm volatile(
+            "{\n\t.reg .b32 a0, a1, b0, b1, t;\n\t"
+            "shr.b32 t, %4, %11;\n\t"
+            "lop3.b32 a0, t, %8, %9, 0xEA;\n\t"
+            "shr.b32 t, %4, %12;\n\t"
+            "lop3.b32 a1, t, %8, %9, 0xEA;\n\t"
+            "shr.b32 t, %5, %11;\n\t"
+            "lop3.b32 b0, t, %8, %9, 0xEA;\n\t"
+            "shr.b32 t, %5, %12;\n\t"
+            "lop3.b32 b1, t, %8, %9, 0xEA;\n\t"
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {a0,b0,a1,b1}, {%6,%7}, "
+            "{%10,%10,%10,%10};\n\t}"
+            : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+            : "r"(wa), "r"(wb), "r"(x0), "r"(x1), "r"(cm), "r"(cg), "f"(0.0f), "n"(SH), "n"(SH + 4));
+    } else {
+        asm volatile(
+            "{\n\t.reg .b32 a0, a1, b0, b1, t;\n\t"
+            "shr.b32 t, %4, %10;\n\t"
+            "lop3.b32 a0, t, %8, %9, 0xEA;\n\t"
+            "shr.b32 t, %4, %11;\n\t"
+            "lop3.b32 a1, t, %8, %9, 0xEA;\n\t"
+            "shr.b32 t, %5, %10;\n\t"
+            "lop3.b32 b0, t, %8, %9, 0xEA;\n\t"
+            "shr.b32 t, %5, %11;\n\t"
+            "lop3.b32 b1, t, %8, %9, 0xEA;\n\t"
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {a0,b0,a1,b1}, {%6,%7}, "
+            "{%0,%1,%2,%3};\n\t}"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(wa), "r"(wb), "r"(x0), "r"(x1), "r"(cm), "r"(cg), "n"(SH), "n"(SH + 4));
+    }
+}
+__device__ __forceinline__ uint32_t lds_u32_st(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+// sum of eight bf16 values in fp32
+__device__ __forceinline__ float bf16x8_sum(uint4 v) {
+    const float a = bf16_lo(v.x) + bf16_hi(v.x), b = bf16_lo(v.y) + bf16_hi(v.y);
+    const float c = bf16_lo(v.z) + bf16_hi(v.z), d = bf16_lo(v.w) + bf16_hi(v.w);
+    return (a + b) + (c + d);
+}
 __device__ __forceinline__ uint4 ldg_nc_v4_st(const void* p) {
     uint4 r;
     asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
@@ -211,6 +270,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     const uint32_t qslots = smem_u32(rbase);
     constexpr bool L1X = MX > 8;  // X through L1 instead of staged slots
     constexpr int MT = L1X ? MX / 8 : 1;  // groups of 8 tokens
+    constexpr bool DIAG = MX == 1;   // one token: slice sums in the MMA columns, scales in fp32
     unsigned char* xslots = rbase + ST_DEPTH * QSLOT;                   // 2 slots x M token rows
     unsigned char* zrow = xslots + 2 * p.M * ST_XPITCH;                 // zeros for tokens >= M
     const uint32_t bars = smem_u32(rbase + ST_DEPTH * QSLOT + st_xslot_bytes(p.M));  // ST_DEPTH mbarriers
@@ -329,6 +389,8 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     float acc[MT][4];
 #pragma unroll
     for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+    float ya = 0.f, yb = 0.f;  // one-token path: rows pr, pr + 8 over this lane's slices of the tile so far
+    float xpart = 0.f;         // one-token path: sum of the lane's 8-k chunk of X
     // L1 path: this lane's tokens (8t + gid) read their 8-k chunk at 32 tq + 8 j of each half
     const uint16_t* xl1 = p.X + (int64_t)gid * p.K + 32 * tq;
     int tile = tile0, kc = kc0, kc_first = kc0;  // unit being computed
@@ -342,6 +404,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         unsigned char* xs = xslots + (it & 1) * p.M * ST_XPITCH;
         if (!L1X) {
             store_x(xs);
+            if (DIAG) xpart = bf16x8_sum(xr[0]);
             if (it + 1 < nunits) {
                 if (++x_kc == p.nkc) x_kc = 0;
                 load_x(x_kc);
@@ -355,18 +418,33 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         const uint32_t qa = qslots + d * QSLOT + pr * QROW;  // scales of row pr; offsets 16 rows further
         const uint32_t qb = qa + 8 * QROW;
         const uint32_t bbase = gid < p.M ? smem_u32(xs) + xrow_off : zaddr;
+        float dacc[4];  // one-token path: D[row][slice] of this unit
 #pragma unroll
         for (int h = 0; h < 2; ++h) {  // two 128-k steps per unit
             const uint32_t cpos = h ? cpos1 : cpos0;
-            const uint32_t jq = h ? jq1 : jq0;
             const uint4 wa = lds128_st(ws_a + cpos);
             const uint4 wb = lds128_st(ws_b + cpos);
+            const uint32_t wa4[4] = {wa.x, wa.y, wa.z, wa.w};
+            const uint32_t wb4[4] = {wb.x, wb.y, wb.z, wb.w};
+            if constexpr (DIAG) {
+                // X only on the lane whose column is its own slice (gid = tq + 4h)
+                const uint32_t bd = (gid == tq + 4 * h) ? smem_u32(xs) : zaddr;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 xv = lds128_st(bd + 256u * h + boff[j]);
+                    if (h == 0 && j == 0)
+                        raw_mma<0, true>(dacc, wa4[j], wb4[j], xv.x, xv.y, cm, cg);
+                    else
+                        raw_mma<0, false>(dacc, wa4[j], wb4[j], xv.x, xv.y, cm, cg);
+                    raw_mma<8, false>(dacc, wa4[j], wb4[j], xv.z, xv.w, cm, cg);
+                }
+                continue;
+            }
+            const uint32_t jq = h ? jq1 : jq0;
             const uint32_t sa = lds_u16_st(qa + jq), oa = lds_u16_st(qa + 16 * QROW + jq);
             const uint32_t sb = lds_u16_st(qb + jq), ob = lds_u16_st(qb + 16 * QROW + jq);
             const uint32_t sa2 = __byte_perm(sa, 0, 0x1010), oa2 = __byte_perm(oa, 0, 0x1010);
             const uint32_t sb2 = __byte_perm(sb, 0, 0x1010), ob2 = __byte_perm(ob, 0, 0x1010);
-            const uint32_t wa4[4] = {wa.x, wa.y, wa.z, wa.w};
-            const uint32_t wb4[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 if (!L1X) {
@@ -397,6 +475,34 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 }
             }
         }
+        if constexpr (DIAG) {  // apply the groups' scales and offsets to the slice sums (before the slot refill)
+            float xsl = xpart;
+            xsl += __shfl_xor_sync(0xffffffffu, xsl, 1);
+            xsl += __shfl_xor_sync(0xffffffffu, xsl, 2);  // lanes 4c .. 4c+3: sum of slice c
+            const float xs0 = __shfl_sync(0xffffffffu, xsl, 8 * tq), xs1 = __shfl_sync(0xffffffffu, xsl, 8 * tq + 4);
+            // this lane's columns are slices 2tq and 2tq+1: D[pr][.] in dacc[0..1], D[pr+8][.] in dacc[2..3]
+            if constexpr (G == 32) {  // two groups, adjacent in the qparam rows
+                const uint32_t sA = lds_u32_st(qa + 4 * tq), oA = lds_u32_st(qa + 16 * QROW + 4 * tq);
+                const uint32_t sB = lds_u32_st(qb + 4 * tq), oB = lds_u32_st(qb + 16 * QROW + 4 * tq);
+                ya = fmaf(bf16_lo(sA), fmaf(-128.f, xs0, dacc[0]), ya);
+                ya = fmaf(bf16_lo(oA), xs0, ya);
+                ya = fmaf(bf16_hi(sA), fmaf(-128.f, xs1, dacc[1]), ya);
+                ya = fmaf(bf16_hi(oA), xs1, ya);
+                yb = fmaf(bf16_lo(sB), fmaf(-128.f, xs0, dacc[2]), yb);
+                yb = fmaf(bf16_lo(oB), xs0, yb);
+                yb = fmaf(bf16_hi(sB), fmaf(-128.f, xs1, dacc[3]), yb);
+                yb = fmaf(bf16_hi(oB), xs1, yb);
+            } else {  // both slices in one group
+                const uint32_t go = (uint32_t)(((64 * tq) / G) * 2);
+                const float x01 = xs0 + xs1;
+                const float sa = bf16_lo(lds_u16_st(qa + go)), oa = bf16_lo(lds_u16_st(qa + 16 * QROW + go));
+                const float sb = bf16_lo(lds_u16_st(qb + go)), ob = bf16_lo(lds_u16_st(qb + 16 * QROW + go));
+                ya = fmaf(sa, fmaf(-128.f, x01, dacc[0] + dacc[1]), ya);
+                ya = fmaf(oa, x01, ya);
+                yb = fmaf(sb, fmaf(-128.f, x01, dacc[2] + dacc[3]), yb);
+                yb = fmaf(ob, x01, yb);
+            }
+        }
         __syncwarp();
         if (it + ST_DEPTH < nunits) {  // refill the slot (its reads are done: order them before the async writes)
             fence_proxy_async_smem();
@@ -410,6 +516,15 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
 
         // end of a row tile or of the range: hand the tile's sums on
         if (it + 1 == nunits || kc == p.nkc - 1) {
+            if constexpr (DIAG) {  // the row sums over the four lanes of a row pair (slices 0..7)
+                ya += __shfl_xor_sync(0xffffffffu, ya, 1);
+                ya += __shfl_xor_sync(0xffffffffu, ya, 2);
+                yb += __shfl_xor_sync(0xffffffffu, yb, 1);
+                yb += __shfl_xor_sync(0xffffffffu, yb, 2);
+                acc[0][0] = ya;  // token 0 of rows pr, pr + 8 (written by the tq = 0 lanes)
+                acc[0][2] = yb;
+                ya = yb = 0.f;
+            }
             const int n_a = tile * 16 + pr, n_b = n_a + 8;
             // acc[t] = D[row n_a: tokens 8t + 2tq, +1 | row n_b: the same tokens]
             if (kc_first == 0 && kc == p.nkc - 1) {  // this warp summed all of the tile's k
