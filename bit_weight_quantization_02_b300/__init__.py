@@ -150,8 +150,8 @@ def w4_linear_workspace_bytes(M: int, N: int, K: int, group_size: int) -> int:
 
 
 class Workspace:
-    """Zero-filled device workspace for w4_linear (the stream kernel's fp32 partial
-    sums and tile counters).  Every call leaves it zeroed, so it can be reused by
+    """Zero-filled device workspace for w4_linear (the stream kernels' slots for
+    the partial sums of row tiles split between warps).  Every call leaves it zeroed, so it can be reused by
     calls of any shape in sequence; calls that can overlap on the GPU need one
     each.  Growing it allocates (through torch): size it before capturing a CUDA
     graph or timing."""

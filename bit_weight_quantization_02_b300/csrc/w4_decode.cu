@@ -22,9 +22,9 @@
 //    layout's nibble order makes every extracted pair two consecutive k, so
 //    the B fragments are X's own 32-bit words, read straight from global
 //    memory through L1 (X is tiny and shared by every warp of the SM);
-//  * a tile split between warps is summed in the caller's fp32 workspace
-//    (adds that return their old values, a warp vote, a tile counter, the
-//    last contributor exchanges each sum for zero and writes Y).
+//  * a tile split between warps is finished by its owner (the warp holding
+//    its first unit) from the partial sums the other sharers leave in their
+//    workspace slots (split_publish / split_collect in w4_device.cuh).
 #include "w4_device.cuh"
 #include "w4_internal.h"
 
@@ -34,13 +34,14 @@ namespace w4 {
 
 constexpr int DC_WARPS = 4;
 constexpr int DC_THREADS = DC_WARPS * 32;
+constexpr uint64_t DC_WAIT_LIMIT_NS = 2000000000ull;
+__device__ unsigned int g_decode_fault;
 
 struct DecodeArgs {
     const uint16_t* X;
     const uint8_t* packed;
     uint16_t* Y;
-    float* ws;            // [M][N] fp32 partial sums, zero between calls
-    unsigned int* count;  // [N/16] k units summed so far per row tile, zero between calls
+    uint64_t* ws;         // split-tile slots, one per warp (split_ws_bytes), zero between calls
     int M, N, K;
     int nkc;              // units per row tile = ceil(K / 256)
     long long units;      // row tiles x nkc
@@ -131,6 +132,7 @@ decode_kernel(const DecodeArgs p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, tq = lane & 3;
     const int worker = blockIdx.x * DC_WARPS + warp;
+    __shared__ float scr[DC_WARPS][16 * 8 * MT];  // split-tile scratch of each warp (a tile's 16 x M sums)
 
     griddep_launch_dependents();
     if (worker >= p.workers) return;
@@ -169,6 +171,7 @@ decode_kernel(const DecodeArgs p) {
 #pragma unroll
     for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
     int tile = (int)(u0 / p.nkc), kc = (int)(u0 % p.nkc), kc_first = kc;
+    bool owner_split = false;  // the range ends inside a tile whose first unit it holds
 
     auto compute = [&](const DcUnit& f, int it) {
 #pragma unroll
@@ -217,34 +220,11 @@ decode_kernel(const DecodeArgs p) {
                         const int m = 8 * t + 2 * tq + (i & 1), n = (i < 2) ? n_a : n_b;
                         if (m < p.M && n < p.N) p.Y[(int64_t)m * p.N + n] = (uint16_t)float_to_bf16_bits(acc[t][i]);
                     }
-            } else {
-                // split tile: fence-free ordering, as in the stream kernel -- the adds return
-                // their old values and the vote reads them before lane 0 moves the counter
-                float got = 0.f;
-#pragma unroll
-                for (int t = 0; t < MT; ++t)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int m = 8 * t + 2 * tq + (i & 1), n = (i < 2) ? n_a : n_b;
-                        if (m < p.M && n < p.N) got += atomicAdd(p.ws + (int64_t)m * p.N + n, acc[t][i]);
-                    }
-                const unsigned int dep = __float_as_uint(got) & (0u - threadIdx.y);  // threadIdx.y == 0
-                const unsigned int done = __all_sync(0xffffffffu, dep == 0u);
-                unsigned int last = 0;
-                if (lane == 0) {
-                    const unsigned int mine = (unsigned int)(kc - kc_first + 1) * done;
-                    last = (atomicAdd(p.count + tile, mine) + mine == (unsigned int)p.nkc);
-                }
-                last = __shfl_sync(0xffffffffu, last, 0);
-                if (last) {
-                    for (int i = lane; i < 16 * p.M; i += 32) {
-                        const int m = i >> 4, n = tile * 16 + (i & 15);
-                        if (n < p.N)
-                            p.Y[(int64_t)m * p.N + n] =
-                                (uint16_t)float_to_bf16_bits(atomicExch(p.ws + (int64_t)m * p.N + n, 0.0f));
-                    }
-                    if (lane == 0) atomicExch(p.count + tile, 0u);
-                }
+            } else if (kc_first != 0) {  // a later share of the tile (the first of this range): publish it
+                split_publish<MT>(p.ws + (size_t)worker * 16 * p.M, acc, p.M, min(16, p.N - tile * 16), gid, tq);
+            } else {  // the tile's owner: its range ends here (last unit); finished after the loop
+                owner_split = true;
+                return;
             }
 #pragma unroll
             for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
@@ -265,6 +245,11 @@ decode_kernel(const DecodeArgs p) {
         compute(fb, it + 1);
         if (it + 3 < nunits) load(u0 + it + 3, fb);
     }
+    if (owner_split) {  // add the later shares of the last tile (their warps publish without waiting), write Y
+        const int wl = split_warp_of((long long)tile * p.nkc + p.nkc - 1, p.units, p.workers);
+        split_collect<MT>(acc, scr[warp], p.ws, worker, wl, p.M, min(16, p.N - tile * 16), gid, tq, lane,
+                          p.Y + (int64_t)tile * 16, p.N, &g_decode_fault, 1u, DC_WAIT_LIMIT_NS);
+    }
 }
 
 // ------------------------------------------------------------------ host side
@@ -275,7 +260,7 @@ bool plan_decode(int64_t M, int64_t N, int64_t K, int g, DecodePlan* plan) {
     if (tiles > 0x3FFFFFFF) return false;
     plan->nkc = (int)((K + 255) / 256);
     plan->units = tiles * plan->nkc;
-    plan->ws_bytes = stream_ws_bytes(M, N);
+    plan->ws_bytes = split_ws_bytes(M, plan->units);
     (void)g;
     return true;
 }
@@ -287,7 +272,7 @@ static cudaError_t launch_decode_gm(const DecodePlan& plan, DecodeArgs a, cudaSt
     int sms = 0, per_sm = 0;
     cudaError_t e = resident_blocks(reinterpret_cast<const void*>(kern), DC_THREADS, 0, &sms, &per_sm);
     if (e != cudaSuccess) return e;
-    const long long max_workers = (long long)sms * per_sm * DC_WARPS;
+    const long long max_workers = std::min<long long>((long long)sms * per_sm * DC_WARPS, SPLIT_MAX_WORKERS);
     a.workers = (int)std::min<long long>(max_workers, plan.units);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((a.workers + DC_WARPS - 1) / DC_WARPS), 1, 1);
@@ -315,9 +300,7 @@ cudaError_t launch_decode(const DecodePlan& plan, const uint16_t* X, int64_t M, 
     a.X = X;
     a.packed = packed;
     a.Y = Y;
-    const size_t part = ((size_t)M * N * 4 + 255) / 256 * 256;
-    a.ws = static_cast<float*>(workspace);
-    a.count = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + part);
+    a.ws = static_cast<uint64_t*>(workspace);
     a.M = (int)M;
     a.N = (int)N;
     a.K = (int)K;
@@ -329,6 +312,13 @@ cudaError_t launch_decode(const DecodePlan& plan, const uint16_t* X, int64_t M, 
         case 64: return launch_decode_g<64>(plan, a, stream);
         default: return launch_decode_g<128>(plan, a, stream);
     }
+}
+
+cudaError_t read_and_clear_decode_fault(unsigned int* fault) {
+    cudaError_t e = cudaMemcpyFromSymbol(fault, g_decode_fault, sizeof(unsigned int));
+    if (e != cudaSuccess || !*fault) return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_decode_fault, &zero, sizeof(unsigned int));
 }
 
 }  // namespace w4

@@ -205,4 +205,129 @@ __device__ __forceinline__ uint32_t dequant_pair(uint32_t biased, uint32_t s2, u
     return *reinterpret_cast<uint32_t*>(&w);
 }
 
+// ------------------------------------------- split row tiles (stream-K decode)
+// The decode kernels cut the (row tile, k) units into equal contiguous warp
+// ranges, so several warps can share a row tile.  The tile's owner is the
+// warp holding its first unit: the shared tile is the last of the owner's
+// range and the first of every other sharer's.  A sharer leaves its partial
+// sums in its own slot of the workspace (16 rows x M tokens of 8-byte words:
+// the fp32 bits in the low half, 1 in the high half, one naturally aligned
+// 64-bit store, so value and flag arrive together) and goes on without
+// waiting.  The owner reads the slots of the warps after it (in one batch of
+// loads; it waits only for a sharer that is still computing), adds them in
+// warp order to its own sums (a fixed order: the result is deterministic),
+// writes Y and stores zeros back, so the workspace is all zeros again after
+// every call.  Liveness of the wait: a dependent grid starts only once every
+// block of this grid has started, so no block an owner waits for can be kept
+// off the GPU by work queued behind this grid; the wait is bounded anyway.
+constexpr int SPLIT_MAX_WORKERS = 4096;
+
+// workspace bytes: one slot per warp, at most SPLIT_MAX_WORKERS warps (no more warps than units)
+__host__ __device__ inline size_t split_ws_bytes(int64_t M, int64_t units) {
+    const int64_t w = units < SPLIT_MAX_WORKERS ? units : SPLIT_MAX_WORKERS;
+    return (size_t)w * 16u * (size_t)M * 8u;
+}
+// the warp whose range [U w / W, U (w + 1) / W) holds unit u
+__device__ __forceinline__ int split_warp_of(long long u, long long units, int workers) {
+    return (int)(((u + 1) * workers - 1) / units);
+}
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+// A sharer's part: acc[t][i] holds rows row_a (i < 2) / row_a + 8 (i >= 2) of
+// the tile for tokens 8t + 2tq + (i & 1) (the mma.m16n8k16 accumulator).
+template <int MT>
+__device__ __forceinline__ void split_publish(uint64_t* slot, const float (&acc)[MT][4], int M, int nrows, int row_a,
+                                              int tq) {
+#pragma unroll
+    for (int t = 0; t < MT; ++t)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int m = 8 * t + 2 * tq + (i & 1), r = row_a + (i & 2) * 4;
+            if (m < M && r < nrows) st_relaxed_u64(slot + m * 16 + r, (1ull << 32) | __float_as_uint(acc[t][i]));
+        }
+}
+
+// The owner's part, after its own sums are in the warp's scratch (16 M floats
+// of shared memory, element m * 16 + r): the slots of warps worker + 1 .. wl,
+// then bf16 Y of the tile (Yt = first column of the tile, ldy = N).  The
+// owner's shared tile is the last of its range, so the kernels call this after
+// their main loop, when the loop's registers are free.  Returns false if a wait
+// timed out.
+__device__ __forceinline__ bool split_sum_shares(const float* scr, uint64_t* ws, int worker, int wl, int M,
+                                                     int nrows, int lane, uint16_t* Yt, int64_t ldy,
+                                                     unsigned int* fault_word, unsigned int code, uint64_t limit_ns) {
+    bool ok = true;
+    const int E = 16 * M;          // words per slot
+    const bool halves = E == 16;   // one token: lanes 16..31 take every other sharer
+    const int sub = halves ? lane >> 4 : 0, step = halves ? 2 : 1;
+    for (int e = halves ? (lane & 15) : lane; e < E; e += halves ? 16 : 32) {
+        const int r = e & 15;
+        float sum = sub == 0 ? scr[e] : 0.f;
+        if (r < nrows) {
+            for (int c0 = worker + 1 + sub; c0 <= wl; c0 += 8 * step) {
+                // a batch of up to 8 slots: load them together, reload together the ones whose
+                // sharer has not published yet (one round trip per poll, not one per slot)
+                uint64_t v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int c = c0 + j * step;
+                    v[j] = c <= wl ? ld_relaxed_u64(ws + (size_t)c * E + e) : (1ull << 32);
+                }
+                uint64_t t0 = 0;
+                for (;;) {
+                    bool all = true;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) all = all && (v[j] >> 32) != 0u;
+                    if (all) break;
+                    const uint64_t now = globaltimer_ns();
+                    if (t0 == 0) t0 = now;
+                    if (now - t0 > limit_ns) {  // give up: count what is missing as zero
+                        atomicOr(fault_word, code);
+                        ok = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if ((v[j] >> 32) == 0u) v[j] = ld_relaxed_u64(ws + (size_t)(c0 + j * step) * E + e);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int c = c0 + j * step;
+                    if (c <= wl) {
+                        sum += __uint_as_float((uint32_t)v[j]);
+                        st_relaxed_u64(ws + (size_t)c * E + e, 0ull);
+                    }
+                }
+            }
+        }
+        if (halves) sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+        if (sub == 0 && r < nrows) Yt[(int64_t)(e >> 4) * ldy + r] = (uint16_t)float_to_bf16_bits(sum);
+    }
+    return ok;
+}
+// The owner's part: its own sums into the scratch, then split_sum_shares.
+template <int MT>
+__device__ __forceinline__ bool split_collect(const float (&acc)[MT][4], float* scr, uint64_t* ws, int worker, int wl,
+                                              int M, int nrows, int row_a, int tq, int lane, uint16_t* Yt,
+                                              int64_t ldy, unsigned int* fault_word, unsigned int code,
+                                              uint64_t limit_ns) {
+#pragma unroll
+    for (int t = 0; t < MT; ++t)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int m = 8 * t + 2 * tq + (i & 1), r = row_a + (i & 2) * 4;
+            if (m < M) scr[m * 16 + r] = acc[t][i];
+        }
+    __syncwarp();
+    const bool ok = split_sum_shares(scr, ws, worker, wl, M, nrows, lane, Yt, ldy, fault_word, code, limit_ns);
+    __syncwarp();
+    return ok;
+}
+
 }  // namespace w4

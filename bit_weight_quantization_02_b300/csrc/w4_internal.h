@@ -32,7 +32,7 @@ cudaError_t launch_skinny(const SkinnyPlan& plan, const uint16_t* X, int64_t M, 
                           cudaStream_t stream, const char** detail);
 
 // Persistent stream-K decode kernel (M <= 32): needs a zero-initialized,
-// self-cleaning workspace of stream_ws_bytes(M, N) bytes.
+// self-cleaning workspace of split_ws_bytes(M, units) bytes (w4_device.cuh).
 struct StreamPlan {
     int nkc;          // 256-k units per 16-row tile
     int64_t tiles;    // 16-row tiles
@@ -42,7 +42,6 @@ struct StreamPlan {
 };
 constexpr int STREAM_MAX_M = 32;
 constexpr int DECODE_MAX_M = 32;  // decode-layout kernel
-size_t stream_ws_bytes(int64_t M, int64_t N);
 bool plan_stream(int64_t M, int64_t N, int64_t K, int g, StreamPlan* plan);
 cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
                           const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
@@ -56,8 +55,8 @@ int64_t repacked_bytes(int64_t N, int64_t K, int g);
 cudaError_t launch_repack(const uint8_t* Wq, const uint16_t* scales, const uint16_t* offsets, int64_t N, int64_t K,
                           int g, uint8_t* packed, cudaStream_t stream);
 
-// Persistent stream-K decode kernel on the decode layout (M <= 8), same
-// workspace as the stream kernel (stream_ws_bytes).
+// Persistent stream-K decode kernel on the decode layout (M <= 32), same
+// workspace as the stream kernel (split_ws_bytes).
 struct DecodePlan {
     int nkc;          // 256-k units per 16-row tile
     int64_t units;    // tiles * nkc
@@ -79,6 +78,7 @@ cudaError_t launch_gemm(const uint16_t* X, int64_t M, int64_t K, const uint8_t* 
 // caller has synchronized the stream.
 cudaError_t read_and_clear_gemm_fault(unsigned int* fault);
 cudaError_t read_and_clear_skinny_fault(unsigned int* fault);
+cudaError_t read_and_clear_decode_fault(unsigned int* fault);
 
 // Raises a kernel's dynamic shared-memory limit to `smem_bytes` (and allows
 // cluster sizes above 8 if asked), once per device and kernel: later calls,

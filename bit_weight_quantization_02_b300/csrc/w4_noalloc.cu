@@ -67,7 +67,7 @@ extern "C" w4_status w4_linear_static(const uint16_t* X, int64_t M, int64_t K, c
         return static_fail(W4_ERR_INVALID_ARG, "w4_linear_static needs an even K / group_size");
     if (plan.ws_bytes > (size_t)W4_STATIC_SCRATCH_BYTES)
         return static_fail(W4_ERR_INVALID_ARG,
-                           "problem too large for the static scratch: needs M*N*4 + N/16*4 bytes (rounded) "
+                           "problem too large for the static scratch: needs w4_linear_workspace_bytes "
                            "<= W4_STATIC_SCRATCH_BYTES");
     void* scratch = nullptr;
     cudaError_t e = scratch_address(&scratch);

@@ -35,17 +35,12 @@
 //    y += s (D - 128 xs) + o xs with xs the slice's sum of X.  That halves the
 //    per-weight instructions, and the weights are never rounded to bf16.
 //  * A warp that covers all of a row tile's k writes bf16 Y directly.  A tile
-//    split between warps is summed in fp32 with atomic adds in the caller's
-//    workspace; the warp that completes the tile's k count (atomic counter,
-//    no waiting) takes each sum and puts back zero in one atomic exchange and
-//    writes bf16 Y, so the workspace is all zeros again after every call.
-//    Ordering without a memory fence (a fence here cost ~1.5 us a launch):
-//    a contributor's adds return their old values and a warp vote reads
-//    them before lane 0 bumps the counter, so every add has been performed
-//    at the L2 point of coherence before the counter shows it; the last
-//    contributor's exchanges are issued after its counter atomic returned,
-//    hence after every add.  All of these are .gpu-scope atomics, performed
-//    at L2 in the order they are issued against each address.
+//    split between warps is finished by its owner, the warp holding its
+//    first unit, from the partial sums the other sharers leave in their
+//    workspace slots (flag and value in one 64-bit store, no atomics, no
+//    fence; split_publish / split_collect in w4_device.cuh): one round trip
+//    to L2 at the end of the owner's range instead of a chain of atomics,
+//    and a fixed summation order.
 #include "w4_device.cuh"
 #include "w4_internal.h"
 
@@ -67,20 +62,21 @@ struct StreamArgs {
     const uint16_t* scales;
     const uint16_t* offsets;
     uint16_t* Y;
-    float* ws;             // [M][N] fp32 partial sums, zero between calls
-    unsigned int* count;   // [N/16] k units summed so far per row tile, zero between calls
+    uint64_t* ws;          // split-tile slots, one per warp (split_ws_bytes), zero between calls
     int M, N, K;
     int nkc;               // units per row tile = ceil(K / 256)
     long long units;       // row tiles x nkc
     int workers;           // warps of the grid with work
 };
 
-// per-warp shared memory after the code slots: qparam slots, X slots, zero row, barriers
+// per-warp shared memory after the code slots: qparam slots, X slots, zero row,
+// split-tile scratch, barriers
 __host__ __device__ inline int st_qslot_bytes(int g) { return 2 * 16 * (ST_UK / g) * 2; }
 // X slots (2 units x M token rows) and a zero row: only up to 8 tokens (beyond, X comes through L1)
 __host__ __device__ inline int st_xslot_bytes(int M) { return M <= 8 ? (2 * M + 1) * ST_XPITCH : 0; }
+__host__ __device__ inline int st_scratch_bytes(int M) { return 16 * M * 4; }  // a tile's 16 x M fp32 sums
 __host__ __device__ inline int st_rest_bytes(int M, int g) {
-    const int b = ST_DEPTH * st_qslot_bytes(g) + st_xslot_bytes(M) + 8 * ST_DEPTH;
+    const int b = ST_DEPTH * st_qslot_bytes(g) + st_xslot_bytes(M) + st_scratch_bytes(M) + 8 * ST_DEPTH;
     return (b + 127) & ~127;  // qparam slots are TMA destinations: 128-byte aligned
 }
 __host__ __device__ inline int st_smem_bytes(int M, int g) {
@@ -273,7 +269,8 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     constexpr bool DIAG = MX == 1;   // one token: slice sums in the MMA columns, scales in fp32
     unsigned char* xslots = rbase + ST_DEPTH * QSLOT;                   // 2 slots x M token rows
     unsigned char* zrow = xslots + 2 * p.M * ST_XPITCH;                 // zeros for tokens >= M
-    const uint32_t bars = smem_u32(rbase + ST_DEPTH * QSLOT + st_xslot_bytes(p.M));  // ST_DEPTH mbarriers
+    float* scr = reinterpret_cast<float*>(rbase + ST_DEPTH * QSLOT + st_xslot_bytes(p.M));  // split-tile scratch
+    const uint32_t bars = smem_u32(rbase + ST_DEPTH * QSLOT + st_xslot_bytes(p.M) + st_scratch_bytes(p.M));
     const int ng = p.K / G;
 
     if (lane == 0) {  // arrivals per fill: the TMA arrive (+ 32 cp.async arrivals when qparams go that way)
@@ -394,6 +391,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     // L1 path: this lane's tokens (8t + gid) read their 8-k chunk at 32 tq + 8 j of each half
     const uint16_t* xl1 = p.X + (int64_t)gid * p.K + 32 * tq;
     int tile = tile0, kc = kc0, kc_first = kc0;  // unit being computed
+    bool owner_split = false;                    // the range ends inside a tile whose first unit it holds
     int x_kc = kc0;                               // unit whose X sits in xr
     bool ok = true;
     int d = 0;
@@ -535,40 +533,23 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                         const int m = 8 * t + 2 * tq + (i & 1), n = (i < 2) ? n_a : n_b;
                         if (m < p.M && n < p.N) p.Y[(int64_t)m * p.N + n] = (uint16_t)float_to_bf16_bits(acc[t][i]);
                     }
-            } else {
-                float got = 0.f;  // old values returned by the adds (only their arrival matters)
-#pragma unroll
-                for (int t = 0; t < MT; ++t)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int m = 8 * t + 2 * tq + (i & 1), n = (i < 2) ? n_a : n_b;
-                        if (m < p.M && n < p.N) got += atomicAdd(p.ws + (int64_t)m * p.N + n, acc[t][i]);
-                    }
-                // the vote reads every lane's `got`, so all adds have returned before the counter
-                // moves; threadIdx.y is 0 in this one-dimensional block, so `done` is always 1
-                const unsigned int dep = __float_as_uint(got) & (0u - threadIdx.y);
-                const unsigned int done = __all_sync(0xffffffffu, dep == 0u);
-                unsigned int last = 0;
-                if (lane == 0) {
-                    const unsigned int mine = (unsigned int)(kc - kc_first + 1) * done;
-                    last = (atomicAdd(p.count + tile, mine) + mine == (unsigned int)p.nkc);
-                }
-                last = __shfl_sync(0xffffffffu, last, 0);
-                if (last) {
-                    for (int i = lane; i < 16 * p.M; i += 32) {
-                        const int m = i >> 4, n = tile * 16 + (i & 15);
-                        if (n < p.N)
-                            p.Y[(int64_t)m * p.N + n] =
-                                (uint16_t)float_to_bf16_bits(atomicExch(p.ws + (int64_t)m * p.N + n, 0.0f));
-                    }
-                    if (lane == 0) atomicExch(p.count + tile, 0u);
-                }
+            } else if (kc_first != 0) {  // a later share of the tile (the first of this range): publish it
+                split_publish<MT>(p.ws + (size_t)worker * 16 * p.M, acc, p.M, min(16, p.N - tile * 16), pr, tq);
+            } else {  // the tile's owner: its range ends here (last iteration); finished after the loop
+                owner_split = true;
+                break;
             }
 #pragma unroll
             for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
             kc_first = 0;
         }
         advance(tile, kc);
+    }
+    if (owner_split) {  // add the later shares of the last tile (their warps publish without waiting), write Y
+        const int wl = split_warp_of((long long)tile * p.nkc + p.nkc - 1, p.units, p.workers);
+        ok = split_collect<MT>(acc, scr, p.ws, worker, wl, p.M, min(16, p.N - tile * 16), pr, tq, lane,
+                               p.Y + (int64_t)tile * 16, p.N, &g_stream_fault, 2u, ST_WAIT_LIMIT_NS) &&
+             ok;
     }
     if (!ok) {  // never leave with copies still landing in shared memory
         for (int it = max(0, nunits - ST_DEPTH); it < nunits; ++it)
@@ -588,13 +569,8 @@ bool plan_stream(int64_t M, int64_t N, int64_t K, int g, StreamPlan* plan) {
     plan->units = tiles * plan->nkc;
     plan->tiles = tiles;
     plan->smem = (size_t)st_smem_bytes((int)M, g);
-    plan->ws_bytes = stream_ws_bytes(M, N);
+    plan->ws_bytes = split_ws_bytes(M, plan->units);
     return true;
-}
-
-size_t stream_ws_bytes(int64_t M, int64_t N) {
-    const size_t part = ((size_t)M * N * 4 + 255) / 256 * 256;
-    return part + (size_t)((N + 15) / 16) * 4;
 }
 
 template <int G, int MX, bool QT>
@@ -607,7 +583,7 @@ static cudaError_t launch_stream_gm(const StreamPlan& plan, const CUtensorMap& t
     int sms = 0, per_sm = 0;
     if ((e = resident_blocks(reinterpret_cast<const void*>(kern), ST_THREADS, plan.smem, &sms, &per_sm)) != cudaSuccess)
         return e;
-    const long long max_workers = (long long)sms * per_sm * ST_WARPS;
+    const long long max_workers = std::min<long long>((long long)sms * per_sm * ST_WARPS, SPLIT_MAX_WORKERS);
     a.workers = (int)std::min<long long>(max_workers, plan.units);
     const int blocks = (a.workers + ST_WARPS - 1) / ST_WARPS;
     cudaLaunchConfig_t cfg = {};
@@ -658,9 +634,7 @@ cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, 
     a.scales = scales;
     a.offsets = offsets;
     a.Y = Y;
-    const size_t part = ((size_t)M * N * 4 + 255) / 256 * 256;
-    a.ws = static_cast<float*>(workspace);
-    a.count = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + part);
+    a.ws = static_cast<uint64_t*>(workspace);
     a.M = (int)M;
     a.N = (int)N;
     a.K = (int)K;

@@ -110,6 +110,9 @@ W4_API w4_status w4_dequantize(const uint8_t *Wq, const uint16_t *scales,
  * w4_linear needs to run the persistent stream-K decode kernel (M <= 32 and
  * K/group_size even; without it the call still works on the cluster split-K
  * kernel, usually slower), and what w4_linear_repacked needs (M <= 32).
+ * Both need one slot of 16 x M 8-byte words per warp of their grid, at most
+ * one warp per 16-row x 256-k unit and at most 4096 warps:
+ * min(ceil(N/16) * ceil(K/256), 4096) * 128 * M bytes.
  * 0 when neither applies (M > 32).
  */
 W4_API size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int group_size);
@@ -124,13 +127,16 @@ W4_API size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int gro
  * the persistent stream-K decode kernel; without one M <= 32 runs the cluster
  * split-K skinny kernel; larger M the tcgen05 tensor-core GEMM.  The kernels
  * dequantize each weight as bf16(q * s + o) with a single rounding, which can
- * differ from w4_dequantize's double rounding by one bf16 ulp; the summation
- * order is each kernel's own.  Accuracy contract against
+ * differ from w4_dequantize's double rounding by one bf16 ulp; the stream
+ * kernel with one token does not round the weights at all: it sums
+ * (128 + q) x per 32-k slice on the tensor cores and adds
+ * s (sum - 128 sum x) + o sum x in fp32.  The summation order is each
+ * kernel's own.  Accuracy contract against
  * y_ref = sum_k X[m,k] W'[n,k] in fp64 (W' = w4_dequantize output):
  *   |y - y_ref| <= 4e-3 |y_ref| + 1e-2 rms(y_ref).
- * The cluster and GEMM kernels are deterministic bit for bit; the stream
- * kernel adds the partial sums of a row tile split between warps with fp32
- * atomics, so its last bits can vary from run to run.
+ * Every kernel is deterministic bit for bit on a given GPU: the stream
+ * kernel adds the partial sums of a row tile split between warps in a fixed
+ * order (its split depends on the GPU's SM count).
  *
  * workspace: caller-owned device memory of `workspace_bytes` bytes (NULL with
  * 0 is allowed).  It must be zero-filled once before its first use; every
@@ -196,8 +202,8 @@ W4_API int w4_format_version(void);
  * process exits.  The call itself allocates nothing.  Inputs and outputs are
  * the caller's, as for w4_linear.
  *
- * Limits: M <= 8, K / group_size even, and M*N*4 bytes (rounded up to 256)
- * plus 4 bytes per 16 rows of N within the array; other sizes fail with
+ * Limits: M <= 8 and K / group_size even (the workspace such a call needs,
+ * at most 4096 * 128 * 8 bytes, always fits the array); other sizes fail with
  * W4_ERR_INVALID_ARG and a message in w4_last_error_detail().
  * Set-up: the first call on each device, with that device current, looks up
  * the array's device address (cudaGetSymbolAddress); make that first call
@@ -257,8 +263,8 @@ W4_API w4_status w4_repack(const uint8_t *Wq, const uint16_t *scales, const uint
  * a persistent stream-K decode kernel that loads each 16-row x 256-k unit
  * with five coalesced warp loads straight into registers and reads X through
  * L1.  Same result contract as w4_linear (the same dequantization and fp32
- * accumulation; the last bits vary from run to run as with the stream
- * kernel); the workspace rules of w4_linear apply, with
+ * accumulation, deterministic like the stream kernel); the workspace rules
+ * of w4_linear apply, with
  * w4_linear_workspace_bytes(M, N, K, group_size) bytes required.  M > 32 or
  * a missing workspace give W4_ERR_INVALID_ARG.
  */

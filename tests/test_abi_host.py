@@ -62,13 +62,16 @@ def test_sizes(lib):
 
 
 def test_workspace_plan(lib):
-    # the stream kernel (M <= 32, even K/g) needs [M][N] fp32 sums + one counter per 16 rows
-    assert lib.w4_linear_workspace_bytes(1, 1024, 4096, 32) == 4096 + 64 * 4
-    assert lib.w4_linear_workspace_bytes(8, 14336, 4096, 128) >= 8 * 14336 * 4 + 896 * 4
-    assert lib.w4_linear_workspace_bytes(9, 1024, 4096, 32) == 9 * 4096 + 64 * 4
-    assert lib.w4_linear_workspace_bytes(32, 1000, 4096, 32) == 32 * 4000 + 63 * 4  # [M][N] sums padded to 256 B
+    # the stream kernels (M <= 32) need one slot of 16 rows x M 8-byte words per warp of their grid:
+    # at most one warp per 16 x 256 unit and at most 4096 warps
+    assert lib.w4_linear_workspace_bytes(1, 1024, 4096, 32) == 64 * 16 * 128       # 1024 units
+    assert lib.w4_linear_workspace_bytes(8, 14336, 4096, 128) == 4096 * 128 * 8    # 14336 units: the cap
+    assert lib.w4_linear_workspace_bytes(8, 10 ** 6, 4096, 32) == 4 << 20          # w4_linear_static's array
+    assert lib.w4_linear_workspace_bytes(9, 1024, 4096, 32) == 1024 * 128 * 9
+    assert lib.w4_linear_workspace_bytes(32, 1000, 4100 - 4, 32) == 63 * 16 * 128 * 32  # ceil(1000/16) tiles
+    assert lib.w4_linear_workspace_bytes(2, 40, 300 - 12, 32) == 3 * 2 * 128 * 2   # ragged: 3 tiles x 2 units
     assert lib.w4_linear_workspace_bytes(33, 1024, 4096, 32) == 0    # M > 32: no kernel uses a workspace
-    assert lib.w4_linear_workspace_bytes(1, 100, 96, 32) == 512 + 7 * 4  # K/g odd: the decode layout's need
+    assert lib.w4_linear_workspace_bytes(1, 100, 96, 32) == 7 * 128  # K/g odd: the decode layout's need
     assert lib.w4_linear_workspace_bytes(0, 100, 128, 32) == 0
 
 

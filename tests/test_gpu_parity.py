@@ -223,6 +223,9 @@ def test_linear_repacked(g, nk):
         Y.check()
         assert_linear_ok(Y.t, y_ref, f"repacked M={M} N={N} K={K} g={g}")
     w4.w4_device_fault(DEV)
+    ws = w4._workspace_for(X, 32, N, K, g, None)
+    torch.cuda.synchronize()
+    assert int(ws.buf.count_nonzero()) == 0, "the decode-layout kernel must leave its workspace zeroed"
 
 
 GEMM_M = [1, 33, 127, 129, 300]
@@ -287,6 +290,29 @@ def test_linear_is_deterministic():
         again = gpu_linear(X, Wq, sc, of, 64, w4.KERNEL_SKINNY_CLUSTER)
         assert torch.equal(first.view(torch.int16), again.view(torch.int16))
     assert_linear_ok(first, y_ref, "repeat")
+
+
+@pytest.mark.parametrize("M", [1, 3, 8, 17, 32])
+def test_stream_kernels_are_deterministic(M):
+    """Row tiles split between warps are summed in a fixed order: repeated calls
+    agree bit for bit (canonical and decode layouts; k/v-like shape, where every
+    tile is split between 16 warps, and a ragged one)."""
+    for (N, K, g) in [(1024, 4096, 32), (520, 4608, 64)]:
+        (X, Wq, sc, of), y_ref = _problem(M, N, K, g, seed=70 + M + N)
+        ws = w4.Workspace(DEV).reserve_for(M, N, K, g)
+        first = gpu_linear(X, Wq, sc, of, g, w4.KERNEL_STREAM, workspace=ws)
+        rp = w4.w4_repack(Wq, sc, of, g)
+        rfirst = w4.w4_linear_repacked(X, rp, workspace=ws)
+        for _ in range(4):
+            again = gpu_linear(X, Wq, sc, of, g, w4.KERNEL_STREAM, workspace=ws)
+            assert torch.equal(first.view(torch.int16), again.view(torch.int16))
+            ragain = w4.w4_linear_repacked(X, rp, workspace=ws)
+            assert torch.equal(rfirst.view(torch.int16), ragain.view(torch.int16))
+        assert_linear_ok(first, y_ref, f"stream M={M} N={N}")
+        assert_linear_ok(rfirst, y_ref, f"repacked M={M} N={N}")
+        torch.cuda.synchronize()
+        assert int(ws.buf.count_nonzero()) == 0
+    w4.w4_device_fault(DEV)
 
 
 def test_consecutive_linears_overlap_safely():

@@ -63,16 +63,17 @@ def test_static_scratch_entry_matches_w4_linear_on_two_calls_in_a_row():
         assert ok, f"w4_linear_static differs from w4_linear (M={M} N={N} K={K} g={g}): worst ratio {worst:.3f}"
 
 
-def test_static_scratch_entry_rejects_sizes_beyond_its_array():
+def test_static_scratch_entry_rejects_what_it_cannot_run():
+    # every M <= 8 problem's workspace fits the array (tests/test_abi_host.py checks the size rule on
+    # the CPU); M > 8 and an odd K / group_size are refused before any launch
     dev = torch.device("cuda:0")
     fn = _static_fn()
     stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
-    X = torch.zeros((8, 256), dtype=torch.bfloat16, device=dev)
-    big_n = 200_000  # 8 * 200000 * 4 bytes of sums > 4 MiB
+    X = torch.zeros((9, 256), dtype=torch.bfloat16, device=dev)
     Wq = torch.zeros((16, 128), dtype=torch.uint8, device=dev)
     sc = torch.zeros((16, 8), dtype=torch.bfloat16, device=dev)
-    Y = torch.zeros((8, 16), dtype=torch.bfloat16, device=dev)
-    st = fn(X.data_ptr(), 8, 256, Wq.data_ptr(), sc.data_ptr(), sc.data_ptr(), big_n, 32, Y.data_ptr(), stream)
-    assert st == 1 and b"static scratch" in w4.load_library().w4_last_error_detail()
+    Y = torch.zeros((9, 16), dtype=torch.bfloat16, device=dev)
     st = fn(X.data_ptr(), 9, 256, Wq.data_ptr(), sc.data_ptr(), sc.data_ptr(), 16, 32, Y.data_ptr(), stream)
-    assert st == 1
+    assert st == 1 and b"M <= 8" in w4.load_library().w4_last_error_detail()
+    st = fn(X.data_ptr(), 1, 96, Wq.data_ptr(), sc.data_ptr(), sc.data_ptr(), 16, 32, Y.data_ptr(), stream)
+    assert st == 1 and b"even" in w4.load_library().w4_last_error_detail()
