@@ -72,8 +72,9 @@ struct StreamArgs {
 // per-warp shared memory after the code slots: qparam slots, X slots, zero row,
 // split-tile scratch, barriers
 __host__ __device__ inline int st_qslot_bytes(int g) { return 2 * 16 * (ST_UK / g) * 2; }
-// X slots (2 units x M token rows) and a zero row: only up to 8 tokens (beyond, X comes through L1)
-__host__ __device__ inline int st_xslot_bytes(int M) { return M <= 8 ? (2 * M + 1) * ST_XPITCH : 0; }
+// X slot (one unit x M token rows; a warp rewrites it only after its reads of the
+// previous unit have returned) and a zero row: only up to 8 tokens (beyond, X comes through L1)
+__host__ __device__ inline int st_xslot_bytes(int M) { return M <= 8 ? (M + 1) * ST_XPITCH : 0; }
 __host__ __device__ inline int st_scratch_bytes(int M) { return 16 * M * 4; }  // a tile's 16 x M fp32 sums
 __host__ __device__ inline int st_rest_bytes(int M, int g) {
     const int b = ST_DEPTH * st_qslot_bytes(g) + st_xslot_bytes(M) + st_scratch_bytes(M) + 8 * ST_DEPTH;
@@ -267,8 +268,8 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     constexpr bool L1X = MX > 8;  // X through L1 instead of staged slots
     constexpr int MT = L1X ? MX / 8 : 1;  // groups of 8 tokens
     constexpr bool DIAG = MX == 1;   // one token: slice sums in the MMA columns, scales in fp32
-    unsigned char* xslots = rbase + ST_DEPTH * QSLOT;                   // 2 slots x M token rows
-    unsigned char* zrow = xslots + 2 * p.M * ST_XPITCH;                 // zeros for tokens >= M
+    unsigned char* xs = rbase + ST_DEPTH * QSLOT;                       // X slot: M token rows
+    unsigned char* zrow = xs + p.M * ST_XPITCH;                         // zeros for tokens >= M
     float* scr = reinterpret_cast<float*>(rbase + ST_DEPTH * QSLOT + st_xslot_bytes(p.M));  // split-tile scratch
     const uint32_t bars = smem_u32(rbase + ST_DEPTH * QSLOT + st_xslot_bytes(p.M) + st_scratch_bytes(p.M));
     const int ng = p.K / G;
@@ -399,7 +400,6 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
 
     if (!L1X) load_x(x_kc);
     for (int it = 0; it < nunits; ++it) {
-        unsigned char* xs = xslots + (it & 1) * p.M * ST_XPITCH;
         if (!L1X) {
             store_x(xs);
             if (DIAG) xpart = bf16x8_sum(xr[0]);
