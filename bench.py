@@ -59,9 +59,13 @@ def load_peaks():
     return dict(FALLBACK_PEAKS)
 
 
-def source_sha(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def source_sha(paths):
+    """First 16 hex digits of the sha256 of the files' contents, concatenated in order."""
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def load_traffic():
@@ -76,7 +80,8 @@ def load_traffic():
         if not line or line.startswith("#"):
             continue
         kernel, shape, src, sha, nbytes = line.split()
-        if os.path.exists(os.path.join(ROOT, src)) and source_sha(os.path.join(ROOT, src)) == sha:
+        paths = [os.path.join(ROOT, f) for f in src.split(",")]  # every source the kernel is built from
+        if all(os.path.exists(f) for f in paths) and source_sha(paths) == sha:
             out[(kernel, shape)] = float(nbytes)
     return out
 
