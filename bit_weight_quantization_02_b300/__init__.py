@@ -165,6 +165,8 @@ class Workspace:
     def reserve(self, nbytes: int):
         if self.buf is None or self.buf.numel() < nbytes:
             self.buf = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=self.device)
+            # the zero fill ran on the current stream; calls may come on any stream
+            torch.cuda.current_stream(self.device).synchronize()
         return self
 
     def reserve_for(self, M: int, N: int, K: int, group_size: int):

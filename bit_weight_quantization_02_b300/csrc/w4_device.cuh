@@ -257,62 +257,81 @@ __device__ __forceinline__ void split_publish(uint64_t* slot, const float (&acc)
 // of shared memory, element m * 16 + r): the slots of warps worker + 1 .. wl,
 // then bf16 Y of the tile (Yt = first column of the tile, ldy = N).  The
 // owner's shared tile is the last of its range, so the kernels call this after
-// their main loop, when the loop's registers are free.  Returns false if a wait
-// timed out.
+// their main loop, when the loop's registers are free.  Each lane takes
+// elements lane, lane + 32, ... (NE of them, at most NEMAX; with one token,
+// lanes 16..31 take every other sharer instead) and loads 8 slot words per
+// batch (NEMAX when that is larger), so a batch costs one round trip to L2.
+// Returns false if a wait timed out.
+template <int NEMAX>
 __device__ __forceinline__ bool split_sum_shares(const float* scr, uint64_t* ws, int worker, int wl, int M,
-                                                     int nrows, int lane, uint16_t* Yt, int64_t ldy,
-                                                     unsigned int* fault_word, unsigned int code, uint64_t limit_ns) {
+                                                 int nrows, int lane, uint16_t* Yt, int64_t ldy,
+                                                 unsigned int* fault_word, unsigned int code, uint64_t limit_ns) {
+    constexpr int BC = NEMAX >= 8 ? 1 : 8 / NEMAX;  // sharers per batch (8 words per lane, 16 for NEMAX 16)
     bool ok = true;
     const int E = 16 * M;          // words per slot
     const bool halves = E == 16;   // one token: lanes 16..31 take every other sharer
     const int sub = halves ? lane >> 4 : 0, step = halves ? 2 : 1;
-    for (int e = halves ? (lane & 15) : lane; e < E; e += halves ? 16 : 32) {
-        const int r = e & 15;
-        float sum = sub == 0 ? scr[e] : 0.f;
-        if (r < nrows) {
-            for (int c0 = worker + 1 + sub; c0 <= wl; c0 += 8 * step) {
-                // a batch of up to 8 slots: load them together, reload together the ones whose
-                // sharer has not published yet (one round trip per poll, not one per slot)
-                uint64_t v[8];
+    const int e0 = halves ? (lane & 15) : lane;
+    float sum[NEMAX];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int c = c0 + j * step;
-                    v[j] = c <= wl ? ld_relaxed_u64(ws + (size_t)c * E + e) : (1ull << 32);
-                }
-                uint64_t t0 = 0;
-                for (;;) {
-                    bool all = true;
+    for (int i = 0; i < NEMAX; ++i) {
+        const int e = e0 + 32 * i;
+        sum[i] = (sub == 0 && e < E) ? scr[e] : 0.f;
+    }
+    for (int c0 = worker + 1 + sub; c0 <= wl; c0 += BC * step) {
+        uint64_t v[NEMAX][BC];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) all = all && (v[j] >> 32) != 0u;
-                    if (all) break;
-                    const uint64_t now = globaltimer_ns();
-                    if (t0 == 0) t0 = now;
-                    if (now - t0 > limit_ns) {  // give up: count what is missing as zero
-                        atomicOr(fault_word, code);
-                        ok = false;
-                        break;
-                    }
+        for (int i = 0; i < NEMAX; ++i)
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        if ((v[j] >> 32) == 0u) v[j] = ld_relaxed_u64(ws + (size_t)(c0 + j * step) * E + e);
-                }
+            for (int j = 0; j < BC; ++j) {
+                const int c = c0 + j * step, e = e0 + 32 * i;
+                const bool use = c <= wl && e < E && (e & 15) < nrows;
+                v[i][j] = use ? ld_relaxed_u64(ws + (size_t)c * E + e) : (1ull << 32);
+            }
+        uint64_t t0 = 0;
+        for (;;) {  // re-poll together the words whose sharer has not published yet
+            bool all = true;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int c = c0 + j * step;
-                    if (c <= wl) {
-                        sum += __uint_as_float((uint32_t)v[j]);
-                        st_relaxed_u64(ws + (size_t)c * E + e, 0ull);
-                    }
+            for (int i = 0; i < NEMAX; ++i)
+#pragma unroll
+                for (int j = 0; j < BC; ++j) all = all && (v[i][j] >> 32) != 0u;
+            if (all) break;
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) t0 = now;
+            if (now - t0 > limit_ns) {  // give up: count what is missing as zero
+                atomicOr(fault_word, code);
+                ok = false;
+                break;
+            }
+#pragma unroll
+            for (int i = 0; i < NEMAX; ++i)
+#pragma unroll
+                for (int j = 0; j < BC; ++j)
+                    if ((v[i][j] >> 32) == 0u) v[i][j] = ld_relaxed_u64(ws + (size_t)(c0 + j * step) * E + e0 + 32 * i);
+        }
+#pragma unroll
+        for (int i = 0; i < NEMAX; ++i)
+#pragma unroll
+            for (int j = 0; j < BC; ++j) {
+                const int c = c0 + j * step, e = e0 + 32 * i;
+                if (c <= wl && e < E && (e & 15) < nrows) {
+                    sum[i] += __uint_as_float((uint32_t)v[i][j]);
+                    st_relaxed_u64(ws + (size_t)c * E + e, 0ull);
                 }
             }
-        }
-        if (halves) sum += __shfl_xor_sync(0xffffffffu, sum, 16);
-        if (sub == 0 && r < nrows) Yt[(int64_t)(e >> 4) * ldy + r] = (uint16_t)float_to_bf16_bits(sum);
+    }
+    if (halves) sum[0] += __shfl_xor_sync(0xffffffffu, sum[0], 16);
+#pragma unroll
+    for (int i = 0; i < NEMAX; ++i) {
+        const int e = e0 + 32 * i;
+        if (sub == 0 && e < E && (e & 15) < nrows)
+            Yt[(int64_t)(e >> 4) * ldy + (e & 15)] = (uint16_t)float_to_bf16_bits(sum[i]);
     }
     return ok;
 }
-// The owner's part: its own sums into the scratch, then split_sum_shares.
-template <int MT>
+// The owner's part: its own sums into the scratch, then split_sum_shares
+// (NEMAX: elements per lane for the largest M of the kernel, 16 M / 32, at least 1).
+template <int MT, int NEMAX>
 __device__ __forceinline__ bool split_collect(const float (&acc)[MT][4], float* scr, uint64_t* ws, int worker, int wl,
                                               int M, int nrows, int row_a, int tq, int lane, uint16_t* Yt,
                                               int64_t ldy, unsigned int* fault_word, unsigned int code,
@@ -325,7 +344,7 @@ __device__ __forceinline__ bool split_collect(const float (&acc)[MT][4], float* 
             if (m < M) scr[m * 16 + r] = acc[t][i];
         }
     __syncwarp();
-    const bool ok = split_sum_shares(scr, ws, worker, wl, M, nrows, lane, Yt, ldy, fault_word, code, limit_ns);
+    const bool ok = split_sum_shares<NEMAX>(scr, ws, worker, wl, M, nrows, lane, Yt, ldy, fault_word, code, limit_ns);
     __syncwarp();
     return ok;
 }

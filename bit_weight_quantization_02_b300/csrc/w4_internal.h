@@ -56,7 +56,7 @@ cudaError_t launch_repack(const uint8_t* Wq, const uint16_t* scales, const uint1
                           int g, uint8_t* packed, cudaStream_t stream);
 
 // Persistent stream-K decode kernel on the decode layout (M <= 32), same
-// workspace as the stream kernel (split_ws_bytes).
+// workspace as the stream kernel.
 struct DecodePlan {
     int nkc;          // 256-k units per 16-row tile
     int64_t units;    // tiles * nkc

@@ -547,8 +547,9 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     }
     if (owner_split) {  // add the later shares of the last tile (their warps publish without waiting), write Y
         const int wl = split_warp_of((long long)tile * p.nkc + p.nkc - 1, p.units, p.workers);
-        ok = split_collect<MT>(acc, scr, p.ws, worker, wl, p.M, min(16, p.N - tile * 16), pr, tq, lane,
-                               p.Y + (int64_t)tile * 16, p.N, &g_stream_fault, 2u, ST_WAIT_LIMIT_NS) &&
+        constexpr int NE = MX / 2 ? MX / 2 : 1;  // slot words per lane (16 M / 32)
+        ok = split_collect<MT, NE>(acc, scr, p.ws, worker, wl, p.M, min(16, p.N - tile * 16), pr, tq, lane,
+                                   p.Y + (int64_t)tile * 16, p.N, &g_stream_fault, 2u, ST_WAIT_LIMIT_NS) &&
              ok;
     }
     if (!ok) {  // never leave with copies still landing in shared memory
