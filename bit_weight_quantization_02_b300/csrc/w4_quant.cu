@@ -10,16 +10,18 @@
 // (__fsub_rn / __fdiv_rn / __fmul_rn / __fadd_rn: no contraction, no
 // approximate division), so the results are bit-exact and independent of the
 // launch shape.  The per-weight quotient (w - o)/s takes a fast route that
-// gives the same code: t' = (w - o) * rcp_rn(s) differs from the correctly
-// rounded quotient t by less than 2^-18 (|t| < 16: two roundings of 2^-24
-// relative plus half an ulp of t), so rint(t') == rint(t) unless t' lies
-// within 2^-16 of a half-integer; those weights (exact ties included) are
-// divided exactly.
+// gives the same code: t' = (w - o) * r, with r the hardware reciprocal of s
+// (relative error below 2^-22), differs from the correctly rounded quotient t
+// by less than 2^-18 (|t| < 16: 2^-22 + 2^-24 relative, plus half an ulp of
+// t), so rint(t') == rint(t) unless t' lies within 2^-16 of a half-integer;
+// those chunks (exact ties included) are divided exactly.  The scale's
+// division by 15 is a correctly rounded multiply-and-correct (div15_rn).
 //
-// Both kernels are HBM-bound streams: one thread owns 8 consecutive weights
-// (one 16-byte load of bf16, one 4-byte store of codes); the g/8 threads of a
-// group reduce min and max with xor shuffles.  Groups never straddle a warp
-// (g/8 divides 32 and rows hold whole groups).
+// Both kernels are HBM-bound streams: a thread owns chunks of 8 consecutive
+// weights (one 16-byte load of bf16, one 4-byte store of codes each), four at a
+// time with all loads issued first; the g/8 threads of a group reduce min and
+// max with xor shuffles.  Groups never straddle a warp (g/8 divides 32 and rows
+// hold whole groups).
 #include "w4_device.cuh"
 #include "w4_internal.h"
 
@@ -28,27 +30,65 @@ namespace w4 {
 constexpr float QUANT_EPS = 1e-6f;
 constexpr int QUANT_THREADS = 256;
 
+// packed fp32 pairs (element 0 in the low half); each element is one IEEE fp32
+// operation with round-to-nearest
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float f32x2_lo(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float f32x2_hi(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+__device__ __forceinline__ uint64_t f32x2_sub(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 // Order-preserving signed key of two packed bf16 values: negative values get
 // their magnitude bits flipped so that the signed 16-bit order of the keys is
 // the numeric order, with -0.0 (key -1) below +0.0 (key 0).  The map is its
 // own inverse.
 __device__ __forceinline__ uint32_t bf16x2_order_key(uint32_t x) {
-    const uint32_t sign = (x >> 15) & 0x00010001u;
-    return x ^ (sign * 0x7FFFu);
+    uint32_t neg;  // 0xFFFF in each lane whose sign bit is set (prmt selectors 9 / 11: byte 1 / 3, sign replicated)
+    asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(neg) : "r"(x));
+    return x ^ (neg & 0x7FFF7FFFu);
+}
+// (mx - mn) / 15 correctly rounded, for 0 <= x < 2^128: q0 = x * RN(1/15), then
+// one correction from the exact residual x - 15 q0 (Markstein's method for
+// division by a constant).  Checked against IEEE division for every finite
+// non-negative fp32 x: identical.
+__device__ __forceinline__ float div15_rn(float x) {
+    constexpr float c = 1.0f / 15.0f;
+    const float q0 = __fmul_rn(x, c);
+    return __fmaf_rn(__fmaf_rn(-q0, 15.0f, x), c, q0);
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
 }
 
+// Quantize one 8-weight chunk (chunk index c; `valid` false past the end, where
+// the lanes still take part in the group's shuffles).
 template <int G>
-__global__ void __launch_bounds__(QUANT_THREADS)
-quantize_kernel(const uint4* __restrict__ W, int64_t n_chunks, uint32_t* __restrict__ Wq,
-                uint16_t* __restrict__ scales, uint16_t* __restrict__ offsets) {
+__device__ __forceinline__ void quantize_chunk(const uint4 raw, int64_t c, bool valid, int lane,
+                                               uint32_t* __restrict__ Wq, uint16_t* __restrict__ scales,
+                                               uint16_t* __restrict__ offsets) {
     constexpr int L = G / 8;  // threads per group
-    const int64_t c = (int64_t)blockIdx.x * QUANT_THREADS + threadIdx.x;
-    const bool active = c < n_chunks;
-    const uint4 raw = active ? ldg_stream_v4(W + c) : make_uint4(0u, 0u, 0u, 0u);
-
     // min / max of the 8 values, on order keys, two lanes per 32-bit word
-    uint32_t k0 = bf16x2_order_key(raw.x), k1 = bf16x2_order_key(raw.y);
-    uint32_t k2 = bf16x2_order_key(raw.z), k3 = bf16x2_order_key(raw.w);
+    const uint32_t k0 = bf16x2_order_key(raw.x), k1 = bf16x2_order_key(raw.y);
+    const uint32_t k2 = bf16x2_order_key(raw.z), k3 = bf16x2_order_key(raw.w);
     uint32_t kmin = __vmins2(__vmins2(k0, k1), __vmins2(k2, k3));
     uint32_t kmax = __vmaxs2(__vmaxs2(k0, k1), __vmaxs2(k2, k3));
 #pragma unroll
@@ -64,34 +104,75 @@ quantize_kernel(const uint4* __restrict__ W, int64_t n_chunks, uint32_t* __restr
 
     const float mn = bf16_bits_to_float(mn_bits);
     const float mx = bf16_bits_to_float(mx_bits);
-    float s32 = __fdiv_rn(__fsub_rn(mx, mn), 15.0f);
+    float s32 = div15_rn(__fsub_rn(mx, mn));
     s32 = (s32 < QUANT_EPS) ? QUANT_EPS : s32;
     const uint32_t s_bits = float_to_bf16_bits(s32);
     const float s = bf16_bits_to_float(s_bits);
     const float o = mn;
 
-    const float rs = __frcp_rn(s);  // correctly rounded 1/s (s >= 1e-6, a normal bf16 value)
+    const float rs = rcp_approx(s);  // 1/s within 2^-22 relative (s >= 1e-6, a normal bf16 value)
+    // Two weights per instruction (packed fp32 pairs, each element one IEEE fp32 operation with
+    // round-to-nearest, as the scalar ops): d = w - o (>= 0: o is the group minimum), t = d * rs,
+    // m = t + 2^23 (its mantissa is rint(t), half to even, for 0 <= t < 2^22), r = m - 2^23,
+    // and t - r exactly.
     const uint32_t words[4] = {raw.x, raw.y, raw.z, raw.w};
-    uint32_t packed = 0;
+    const uint64_t o2 = pack_f32x2(o, o), rs2 = pack_f32x2(rs, rs), mg2 = pack_f32x2(8388608.0f, 8388608.0f);
+    constexpr float NEAR = 0.4999847412109375f;  // |t' - rint(t')| above this: within 2^-16 of a half-integer
+    uint32_t bytes[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const uint32_t b = (e & 1) ? (words[e >> 1] >> 16) : (words[e >> 1] & 0xFFFFu);
-        const float v = bf16_bits_to_float(b);
-        const float d = __fsub_rn(v, o);
-        float t = __fmul_rn(d, rs);
-        if (fabsf(__fsub_rn(t - floorf(t), 0.5f)) < 1.52587890625e-05f)  // within 2^-16 of x.5
-            t = __fdiv_rn(d, s);
-        int q = __float2int_rn(t);
-        q = min(max(q, 0), 15);
-        packed |= (uint32_t)q << (4 * e);
+    for (int j = 0; j < 4; ++j) {
+        // (w[2j], w[2j+1]) as fp32: the low bf16 shifted up, the high one masked in place
+        const uint64_t w2 = pack_f32x2(__uint_as_float(words[j] << 16), __uint_as_float(words[j] & 0xFFFF0000u));
+        const uint64_t d2 = f32x2_sub(w2, o2);
+        const uint64_t t2 = f32x2_mul(d2, rs2);
+        const uint64_t m2 = f32x2_add(t2, mg2);
+        const uint64_t e2 = f32x2_sub(t2, f32x2_sub(m2, mg2));  // t' - rint(t'), exact
+        float mlo = f32x2_lo(m2), mhi = f32x2_hi(m2);
+        // near a half-integer t' may round differently from the correctly rounded quotient:
+        // divide exactly (only the lanes and weights that need it)
+        if (fabsf(f32x2_lo(e2)) > NEAR) mlo = __fadd_rn(__fdiv_rn(f32x2_lo(d2), s), 8388608.0f);
+        if (fabsf(f32x2_hi(e2)) > NEAR) mhi = __fadd_rn(__fdiv_rn(f32x2_hi(d2), s), 8388608.0f);
+        // the low mantissa bits of m are the code (rint(t) <= 15: t <= 15 (1 + 2^-8) because s
+        // rounds Delta/15 to bf16, so the clamp to [0, 15] never changes it);
+        // byte j = q[2j] | q[2j+1] << 4
+        bytes[j] = __float_as_uint(mlo) + (__float_as_uint(mhi) << 4);
     }
-    if (active) {
+    const uint32_t packed = __byte_perm(__byte_perm(bytes[0], bytes[1], 0x0040), __byte_perm(bytes[2], bytes[3], 0x0040),
+                                        0x5410);
+    if (valid) {
         Wq[c] = packed;
-        if ((threadIdx.x & (L - 1)) == 0) {
+        if ((lane & (L - 1)) == 0) {
             const int64_t grp = c / L;
             scales[grp] = (uint16_t)s_bits;
             offsets[grp] = (uint16_t)mn_bits;
         }
+    }
+}
+
+// A warp takes QUANT_UNROLL rows of 32 consecutive chunks at a time and issues
+// all their loads before any arithmetic (more bytes in flight per thread); a
+// persistent grid strides over warps.
+constexpr int QUANT_UNROLL = 4;
+constexpr int QUANT_WARPS = QUANT_THREADS / 32;
+
+template <int G>
+__global__ void __launch_bounds__(QUANT_THREADS)
+quantize_kernel(const uint4* __restrict__ W, int64_t n_chunks, uint32_t* __restrict__ Wq,
+                uint16_t* __restrict__ scales, uint16_t* __restrict__ offsets) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = (int64_t)gridDim.x * QUANT_WARPS;
+    for (int64_t w = (int64_t)blockIdx.x * QUANT_WARPS + (threadIdx.x >> 5); w * (32 * QUANT_UNROLL) < n_chunks;
+         w += nwarps) {
+        const int64_t c0 = w * (32 * QUANT_UNROLL) + lane;
+        uint4 raw[QUANT_UNROLL];
+#pragma unroll
+        for (int u = 0; u < QUANT_UNROLL; ++u) {
+            const int64_t c = c0 + 32 * u;
+            raw[u] = c < n_chunks ? ldg_stream_v4(W + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < QUANT_UNROLL; ++u)
+            quantize_chunk<G>(raw[u], c0 + 32 * u, c0 + 32 * u < n_chunks, lane, Wq, scales, offsets);
     }
 }
 
@@ -100,51 +181,74 @@ __global__ void __launch_bounds__(QUANT_THREADS)
 dequantize_kernel(const uint32_t* __restrict__ Wq, const uint16_t* __restrict__ scales,
                   const uint16_t* __restrict__ offsets, int64_t n_chunks, uint4* __restrict__ W_out) {
     constexpr int L = G / 8;
-    const int64_t c = (int64_t)blockIdx.x * QUANT_THREADS + threadIdx.x;
-    if (c >= n_chunks) return;
-    const uint32_t packed = ldg_nc_u32(Wq + c);
-    const int64_t grp = c / L;
-    const float s = bf16_bits_to_float(ldg_nc_u16(scales + grp));
-    const float o = bf16_bits_to_float(ldg_nc_u16(offsets + grp));
-    uint32_t out[4];
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = (int64_t)gridDim.x * QUANT_WARPS;
+    for (int64_t w = (int64_t)blockIdx.x * QUANT_WARPS + (threadIdx.x >> 5); w * (32 * QUANT_UNROLL) < n_chunks;
+         w += nwarps) {
+        const int64_t c0 = w * (32 * QUANT_UNROLL) + lane;
+        uint32_t packed[QUANT_UNROLL], sb[QUANT_UNROLL], ob[QUANT_UNROLL];
 #pragma unroll
-    for (int e = 0; e < 8; e += 2) {
-        const float q0 = (float)((packed >> (4 * e)) & 15u);
-        const float q1 = (float)((packed >> (4 * e + 4)) & 15u);
-        const uint32_t lo = float_to_bf16_bits(__fadd_rn(__fmul_rn(q0, s), o));
-        const uint32_t hi = float_to_bf16_bits(__fadd_rn(__fmul_rn(q1, s), o));
-        out[e >> 1] = lo | (hi << 16);
+        for (int u = 0; u < QUANT_UNROLL; ++u) {
+            const int64_t c = c0 + 32 * u;
+            const bool in = c < n_chunks;
+            packed[u] = in ? ldg_nc_u32(Wq + c) : 0u;
+            sb[u] = in ? ldg_nc_u16(scales + c / L) : 0u;
+            ob[u] = in ? ldg_nc_u16(offsets + c / L) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < QUANT_UNROLL; ++u) {
+            const int64_t c = c0 + 32 * u;
+            if (c >= n_chunks) continue;
+            const float s = bf16_bits_to_float(sb[u]), o = bf16_bits_to_float(ob[u]);
+            uint32_t out[4];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                const float q0 = (float)((packed[u] >> (4 * e)) & 15u);
+                const float q1 = (float)((packed[u] >> (4 * e + 4)) & 15u);
+                const uint32_t lo = float_to_bf16_bits(__fadd_rn(__fmul_rn(q0, s), o));
+                const uint32_t hi = float_to_bf16_bits(__fadd_rn(__fmul_rn(q1, s), o));
+                out[e >> 1] = lo | (hi << 16);
+            }
+            W_out[c] = make_uint4(out[0], out[1], out[2], out[3]);
+        }
     }
-    W_out[c] = make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// one wave of resident blocks at most (a second, partial wave would run alone
+// at the end), and no more warps than rows of chunks
+static cudaError_t quant_grid(const void* kernel, int64_t n_chunks, unsigned* grid) {
+    int sms = 0, per_sm = 0;
+    const cudaError_t e = resident_blocks(kernel, QUANT_THREADS, 0, &sms, &per_sm);
+    if (e != cudaSuccess) return e;
+    const int64_t want = (n_chunks + 32 * QUANT_UNROLL * QUANT_WARPS - 1) / (32 * QUANT_UNROLL * QUANT_WARPS);
+    const int64_t cap = (int64_t)sms * per_sm;
+    *grid = (unsigned)(want < cap ? want : cap);
+    return cudaSuccess;
 }
 
 cudaError_t launch_quantize(const uint16_t* W, int64_t N, int64_t K, int g, uint8_t* Wq, uint16_t* scales,
                             uint16_t* offsets, cudaStream_t stream) {
     const int64_t n_chunks = N * K / 8;
-    const int64_t blocks = (n_chunks + QUANT_THREADS - 1) / QUANT_THREADS;
-    const dim3 grid((unsigned)blocks);
     const uint4* w = reinterpret_cast<const uint4*>(W);
     uint32_t* q = reinterpret_cast<uint32_t*>(Wq);
-    switch (g) {
-        case 32: quantize_kernel<32><<<grid, QUANT_THREADS, 0, stream>>>(w, n_chunks, q, scales, offsets); break;
-        case 64: quantize_kernel<64><<<grid, QUANT_THREADS, 0, stream>>>(w, n_chunks, q, scales, offsets); break;
-        default: quantize_kernel<128><<<grid, QUANT_THREADS, 0, stream>>>(w, n_chunks, q, scales, offsets); break;
-    }
+    auto kern = g == 32 ? quantize_kernel<32> : g == 64 ? quantize_kernel<64> : quantize_kernel<128>;
+    unsigned grid = 0;
+    const cudaError_t e = quant_grid(reinterpret_cast<const void*>(kern), n_chunks, &grid);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, QUANT_THREADS, 0, stream>>>(w, n_chunks, q, scales, offsets);
     return cudaGetLastError();
 }
 
 cudaError_t launch_dequantize(const uint8_t* Wq, const uint16_t* scales, const uint16_t* offsets, int64_t N,
                               int64_t K, int g, uint16_t* W_out, cudaStream_t stream) {
     const int64_t n_chunks = N * K / 8;
-    const int64_t blocks = (n_chunks + QUANT_THREADS - 1) / QUANT_THREADS;
-    const dim3 grid((unsigned)blocks);
     const uint32_t* q = reinterpret_cast<const uint32_t*>(Wq);
     uint4* out = reinterpret_cast<uint4*>(W_out);
-    switch (g) {
-        case 32: dequantize_kernel<32><<<grid, QUANT_THREADS, 0, stream>>>(q, scales, offsets, n_chunks, out); break;
-        case 64: dequantize_kernel<64><<<grid, QUANT_THREADS, 0, stream>>>(q, scales, offsets, n_chunks, out); break;
-        default: dequantize_kernel<128><<<grid, QUANT_THREADS, 0, stream>>>(q, scales, offsets, n_chunks, out); break;
-    }
+    auto kern = g == 32 ? dequantize_kernel<32> : g == 64 ? dequantize_kernel<64> : dequantize_kernel<128>;
+    unsigned grid = 0;
+    const cudaError_t e = quant_grid(reinterpret_cast<const void*>(kern), n_chunks, &grid);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, QUANT_THREADS, 0, stream>>>(q, scales, offsets, n_chunks, out);
     return cudaGetLastError();
 }
 

@@ -86,7 +86,9 @@ typedef enum w4_kernel {
  * Source: the affine group projection with an offset and torch.round
  * mapping of Optimum Quanto, "Design overview / Tensors"; the formulas are the
  * plainest reading of it (the eps value and coding with the stored bf16 scale
- * are readings).  Results are bit-exact, independent of launch shape.
+ * are readings).  Results are bit-exact, independent of launch shape, for
+ * finite weights (the codes of a group holding an infinity or a NaN are
+ * unspecified).
  * Errors: W4_ERR_UNSUPPORTED (group_size), W4_ERR_INVALID_ARG (K <= 0,
  * N < 0, K % group_size, NULL, N*K >= 2^62), W4_ERR_MISALIGNED, W4_ERR_CUDA.
  */
