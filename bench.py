@@ -348,6 +348,25 @@ def gpu_arm(args):
                                       "how": "the headline step with every weight in the decode layout "
                                              "(w4_repack once, untimed), CUDA graph of the 224 calls"}
         del dl_graph, dl
+        # the same step with the weights that share an input merged row-wise, as serving stacks
+        # store them (q|k|v: 6144 x 4096, gate|up: 28672 x 4096): 4 launches per block instead of
+        # 7, the same codes, scales and offsets per output row (fresh seeded weights of those shapes)
+        merged = [wl.LinearCase(f"L{layer}.{n}", N, K, 32, 1, wl.weight_seed(6, layer, i), outliers=True)
+                  for layer in range(args.layers)
+                  for i, (n, N, K) in enumerate((("qkv", 6144, 4096), ("o", 4096, 4096),
+                                                 ("gate_up", 28672, 4096), ("down", 4096, 14336)))]
+        mg = LinearStack(merged, device, w4, wl)
+        mg_graph = mg.capture(stream)
+        with torch.cuda.stream(stream):
+            mg_ms = time_region(mg_graph.replay, args.steps, args.warmup, stream, dist, device)
+        mg_gbs = mg.bytes * args.steps * dist.world / (mg_ms * 1e-3) / 1e9
+        rows["decode_step_merged_qkv_gateup"] = {
+            "unit": "GB/s", "value": round(mg_gbs, 1), "ms_per_step": round(mg_ms / args.steps, 4),
+            "frac_of_hbm_peak": round(mg_gbs / peaks["hbm_gbs"], 4), "launches_per_step": len(merged),
+            "kernel": "stream_kernel (w4_linear)",
+            "how": "the headline step's weights with q|k|v and gate|up merged row-wise (one w4_linear per "
+                   "merged matrix), CUDA graph of the 128 calls"}
+        del mg_graph, mg
         rows.update(other_rows(args, w4, wl, device, stream, peaks, dist))
 
     step_bytes = stack.bytes

@@ -247,8 +247,8 @@ decode_kernel(const DecodeArgs p) {
     }
     if (owner_split) {  // add the later shares of the last tile (their warps publish without waiting), write Y
         const int wl = split_warp_of((long long)tile * p.nkc + p.nkc - 1, p.units, p.workers);
-        split_collect<MT, 4 * MT>(acc, scr[warp], p.ws, worker, wl, p.M, min(16, p.N - tile * 16), gid, tq, lane,
-                                  p.Y + (int64_t)tile * 16, p.N, &g_decode_fault, 1u, DC_WAIT_LIMIT_NS);
+        split_collect<MT, 4 * MT>(acc, scr[warp], p.ws, (size_t)16 * p.M, worker, wl, p.M, min(16, p.N - tile * 16),
+                                  gid, tq, lane, p.Y + (int64_t)tile * 16, p.N, &g_decode_fault, 1u, DC_WAIT_LIMIT_NS);
     }
 }
 

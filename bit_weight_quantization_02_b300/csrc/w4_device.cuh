@@ -222,9 +222,11 @@ __device__ __forceinline__ uint32_t dequant_pair(uint32_t biased, uint32_t s2, u
 // off the GPU by work queued behind this grid; the wait is bounded anyway.
 constexpr int SPLIT_MAX_WORKERS = 4096;
 
-// workspace bytes: one slot per warp, at most SPLIT_MAX_WORKERS warps (no more warps than units)
+// workspace bytes: one 16-row slot per warp (at most SPLIT_MAX_WORKERS warps, no
+// more than there are 16-row units), two per warp for one token (32-row units)
 __host__ __device__ inline size_t split_ws_bytes(int64_t M, int64_t units) {
-    const int64_t w = units < SPLIT_MAX_WORKERS ? units : SPLIT_MAX_WORKERS;
+    const int64_t cap = M == 1 ? 2 * SPLIT_MAX_WORKERS : SPLIT_MAX_WORKERS;
+    const int64_t w = units < cap ? units : cap;
     return (size_t)w * 16u * (size_t)M * 8u;
 }
 // the warp whose range [U w / W, U (w + 1) / W) holds unit u
@@ -254,7 +256,8 @@ __device__ __forceinline__ void split_publish(uint64_t* slot, const float (&acc)
 }
 
 // The owner's part, after its own sums are in the warp's scratch (16 M floats
-// of shared memory, element m * 16 + r): the slots of warps worker + 1 .. wl,
+// of shared memory, element m * 16 + r): the slots of warps worker + 1 .. wl
+// (warp c's words at ws + c * stride),
 // then bf16 Y of the tile (Yt = first column of the tile, ldy = N).  The
 // owner's shared tile is the last of its range, so the kernels call this after
 // their main loop, when the loop's registers are free.  Each lane takes
@@ -263,7 +266,8 @@ __device__ __forceinline__ void split_publish(uint64_t* slot, const float (&acc)
 // batch (NEMAX when that is larger), so a batch costs one round trip to L2.
 // Returns false if a wait timed out.
 template <int NEMAX>
-__device__ __forceinline__ bool split_sum_shares(const float* scr, uint64_t* ws, int worker, int wl, int M,
+__device__ __forceinline__ bool split_sum_shares(const float* scr, uint64_t* ws, size_t stride, int worker, int wl,
+                                                 int M,
                                                  int nrows, int lane, uint16_t* Yt, int64_t ldy,
                                                  unsigned int* fault_word, unsigned int code, uint64_t limit_ns) {
     constexpr int BC = NEMAX >= 8 ? 1 : 8 / NEMAX;  // sharers per batch (8 words per lane, 16 for NEMAX 16)
@@ -286,7 +290,7 @@ __device__ __forceinline__ bool split_sum_shares(const float* scr, uint64_t* ws,
             for (int j = 0; j < BC; ++j) {
                 const int c = c0 + j * step, e = e0 + 32 * i;
                 const bool use = c <= wl && e < E && (e & 15) < nrows;
-                v[i][j] = use ? ld_relaxed_u64(ws + (size_t)c * E + e) : (1ull << 32);
+                v[i][j] = use ? ld_relaxed_u64(ws + (size_t)c * stride + e) : (1ull << 32);
             }
         uint64_t t0 = 0;
         for (;;) {  // re-poll together the words whose sharer has not published yet
@@ -307,7 +311,8 @@ __device__ __forceinline__ bool split_sum_shares(const float* scr, uint64_t* ws,
             for (int i = 0; i < NEMAX; ++i)
 #pragma unroll
                 for (int j = 0; j < BC; ++j)
-                    if ((v[i][j] >> 32) == 0u) v[i][j] = ld_relaxed_u64(ws + (size_t)(c0 + j * step) * E + e0 + 32 * i);
+                    if ((v[i][j] >> 32) == 0u)
+                        v[i][j] = ld_relaxed_u64(ws + (size_t)(c0 + j * step) * stride + e0 + 32 * i);
         }
 #pragma unroll
         for (int i = 0; i < NEMAX; ++i)
@@ -316,7 +321,7 @@ __device__ __forceinline__ bool split_sum_shares(const float* scr, uint64_t* ws,
                 const int c = c0 + j * step, e = e0 + 32 * i;
                 if (c <= wl && e < E && (e & 15) < nrows) {
                     sum[i] += __uint_as_float((uint32_t)v[i][j]);
-                    st_relaxed_u64(ws + (size_t)c * E + e, 0ull);
+                    st_relaxed_u64(ws + (size_t)c * stride + e, 0ull);
                 }
             }
     }
@@ -332,7 +337,8 @@ __device__ __forceinline__ bool split_sum_shares(const float* scr, uint64_t* ws,
 // The owner's part: its own sums into the scratch, then split_sum_shares
 // (NEMAX: elements per lane for the largest M of the kernel, 16 M / 32, at least 1).
 template <int MT, int NEMAX>
-__device__ __forceinline__ bool split_collect(const float (&acc)[MT][4], float* scr, uint64_t* ws, int worker, int wl,
+__device__ __forceinline__ bool split_collect(const float (&acc)[MT][4], float* scr, uint64_t* ws, size_t stride,
+                                              int worker, int wl,
                                               int M, int nrows, int row_a, int tq, int lane, uint16_t* Yt,
                                               int64_t ldy, unsigned int* fault_word, unsigned int code,
                                               uint64_t limit_ns) {
@@ -344,7 +350,8 @@ __device__ __forceinline__ bool split_collect(const float (&acc)[MT][4], float* 
             if (m < M) scr[m * 16 + r] = acc[t][i];
         }
     __syncwarp();
-    const bool ok = split_sum_shares<NEMAX>(scr, ws, worker, wl, M, nrows, lane, Yt, ldy, fault_word, code, limit_ns);
+    const bool ok =
+        split_sum_shares<NEMAX>(scr, ws, stride, worker, wl, M, nrows, lane, Yt, ldy, fault_word, code, limit_ns);
     __syncwarp();
     return ok;
 }

@@ -53,7 +53,7 @@ namespace w4 {
 constexpr int ST_WARPS = 4;
 constexpr int ST_THREADS = ST_WARPS * 32;
 constexpr int ST_UK = 256;                 // k per unit
-constexpr int ST_DEPTH = 3;                // ring slots per warp
+constexpr int ST_DEPTH = 3;                // ring slots per warp (16-row units)
 constexpr int ST_WSLOT = 16 * 128;         // codes of one unit: 16 rows x 128 bytes
 constexpr int ST_XPITCH = ST_UK * 2 + 16;  // one staged token row of a unit (+16 bytes against bank conflicts)
 
@@ -71,17 +71,20 @@ struct StreamArgs {
 
 // per-warp shared memory after the code slots: qparam slots, X slots, zero row,
 // split-tile scratch, barriers
-__host__ __device__ inline int st_qslot_bytes(int g) { return 2 * 16 * (ST_UK / g) * 2; }
+__host__ __device__ inline int st_qslot_bytes(int g, int rt) { return 2 * 16 * rt * (ST_UK / g) * 2; }
+// ring slots per warp: three 16-row units, or two 32-row units
+__host__ __device__ inline int st_depth(int rt) { return rt == 1 ? ST_DEPTH : 2; }
 // X slot (one unit x M token rows; a warp rewrites it only after its reads of the
 // previous unit have returned) and a zero row: only up to 8 tokens (beyond, X comes through L1)
 __host__ __device__ inline int st_xslot_bytes(int M) { return M <= 8 ? (M + 1) * ST_XPITCH : 0; }
-__host__ __device__ inline int st_scratch_bytes(int M) { return 16 * M * 4; }  // a tile's 16 x M fp32 sums
-__host__ __device__ inline int st_rest_bytes(int M, int g) {
-    const int b = ST_DEPTH * st_qslot_bytes(g) + st_xslot_bytes(M) + st_scratch_bytes(M) + 8 * ST_DEPTH;
+__host__ __device__ inline int st_scratch_bytes(int M, int rt) { return 16 * rt * M * 4; }  // a tile's fp32 sums
+__host__ __device__ inline int st_rest_bytes(int M, int g, int rt) {
+    const int dp = st_depth(rt);
+    const int b = dp * st_qslot_bytes(g, rt) + st_xslot_bytes(M) + st_scratch_bytes(M, rt) + 8 * dp;
     return (b + 127) & ~127;  // qparam slots are TMA destinations: 128-byte aligned
 }
-__host__ __device__ inline int st_smem_bytes(int M, int g) {
-    return ST_WARPS * ST_DEPTH * ST_WSLOT + ST_WARPS * st_rest_bytes(M, g) + 1024;  // + 1024-byte alignment slack
+__host__ __device__ inline int st_smem_bytes(int M, int g, int rt) {
+    return ST_WARPS * st_depth(rt) * ST_WSLOT * rt + ST_WARPS * st_rest_bytes(M, g, rt) + 1024;  // + alignment slack
 }
 
 __device__ unsigned int g_stream_fault;
@@ -238,16 +241,22 @@ __device__ __forceinline__ uint4 ldg_nc_v4_st(const void* p) {
 }
 
 // MX: token capacity (1, 2, 4, 8: X staged in shared memory; 16, 32: X through L1).
-template <int G, int MX, bool QT>
-__global__ void __launch_bounds__(ST_THREADS, MX == 32 ? 4 : (MX >= 8 ? 5 : 6))
+// RT: 16-row tiles per unit, 1, or 2 for one token on large problems (the X
+// staging, slice sums and ring work of a unit then serve 32 weight rows).
+template <int G, int MX, bool QT, int RT>
+__global__ void __launch_bounds__(ST_THREADS, RT == 2 ? 4 : (MX == 32 ? 4 : (MX >= 8 ? 5 : 6)))
 stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
               const __grid_constant__ CUtensorMap tm_o, const StreamArgs p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    constexpr int QSLOT = 2 * 16 * (ST_UK / G) * 2;  // scales then offsets, 16 rows x (256/G) groups each
+    static_assert(RT == 1 || MX == 1, "two row tiles per unit only on the one-token path");
+    constexpr int ROWS = 16 * RT;                    // weight rows per unit
+    constexpr int DEPTH = RT == 1 ? ST_DEPTH : 2;    // ring slots (st_depth)
+    constexpr int WSLOT = ST_WSLOT * RT;             // codes of one unit
+    constexpr int QSLOT = 2 * ROWS * (ST_UK / G) * 2;  // scales then offsets, ROWS rows x (256/G) groups each
     constexpr int QROW = (ST_UK / G) * 2;            // bytes of one row of one array
     constexpr int PPR = QROW / 4;                    // 4-byte pieces per row and array
-    constexpr int PIECES = 2 * 16 * PPR;             // 4-byte qparam pieces per unit
+    constexpr int PIECES = 2 * ROWS * PPR;           // 4-byte qparam pieces per unit
     constexpr int PPL = (PIECES + 31) / 32;          // pieces per lane
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -261,21 +270,21 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     if (u0 >= u1) return;
     const int nunits = (int)(u1 - u0);
 
-    const int rest = st_rest_bytes(p.M, G);
-    const uint32_t wslots = smem_u32(smem) + warp * (ST_DEPTH * ST_WSLOT);
-    unsigned char* rbase = smem + ST_WARPS * ST_DEPTH * ST_WSLOT + warp * rest;
+    const int rest = st_rest_bytes(p.M, G, RT);
+    const uint32_t wslots = smem_u32(smem) + warp * (DEPTH * WSLOT);
+    unsigned char* rbase = smem + ST_WARPS * DEPTH * WSLOT + warp * rest;
     const uint32_t qslots = smem_u32(rbase);
     constexpr bool L1X = MX > 8;  // X through L1 instead of staged slots
     constexpr int MT = L1X ? MX / 8 : 1;  // groups of 8 tokens
     constexpr bool DIAG = MX == 1;   // one token: slice sums in the MMA columns, scales in fp32
-    unsigned char* xs = rbase + ST_DEPTH * QSLOT;                       // X slot: M token rows
+    unsigned char* xs = rbase + DEPTH * QSLOT;                          // X slot: M token rows
     unsigned char* zrow = xs + p.M * ST_XPITCH;                         // zeros for tokens >= M
-    float* scr = reinterpret_cast<float*>(rbase + ST_DEPTH * QSLOT + st_xslot_bytes(p.M));  // split-tile scratch
-    const uint32_t bars = smem_u32(rbase + ST_DEPTH * QSLOT + st_xslot_bytes(p.M) + st_scratch_bytes(p.M));
+    float* scr = reinterpret_cast<float*>(rbase + DEPTH * QSLOT + st_xslot_bytes(p.M));  // split-tile scratch
+    const uint32_t bars = smem_u32(rbase + DEPTH * QSLOT + st_xslot_bytes(p.M) + st_scratch_bytes(p.M, RT));
     const int ng = p.K / G;
 
     if (lane == 0) {  // arrivals per fill: the TMA arrive (+ 32 cp.async arrivals when qparams go that way)
-        for (int d = 0; d < ST_DEPTH; ++d) mbar_init(bars + 8 * d, QT ? 1 : 33);
+        for (int d = 0; d < DEPTH; ++d) mbar_init(bars + 8 * d, QT ? 1 : 33);
         mbar_fence_init();
     }
     if (!L1X)
@@ -293,28 +302,28 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         const int arr = (i < PIECES) ? i / (PIECES / 2) : 0, rem = (i < PIECES) ? i % (PIECES / 2) : 0;
         prow[q] = rem / PPR;
         pcol[q] = 2 * (rem % PPR);
-        pdst[q] = (uint32_t)(arr * 16 * QROW + prow[q] * QROW + 4 * (rem % PPR));
+        pdst[q] = (uint32_t)(arr * ROWS * QROW + prow[q] * QROW + 4 * (rem % PPR));
         pbase[q] = arr ? p.offsets : p.scales;
     }
 
     // request the unit at (tile, kc) into ring slot d: codes by TMA, scales/offsets by 4-byte cp.async
     auto issue = [&](int tile, int kc, int d) {
-        const int row0 = tile * 16, k = kc * ST_UK;
+        const int row0 = tile * ROWS, k = kc * ST_UK;
         const uint32_t bar = bars + 8 * d;
         if (QT) {  // qparams as two more TMA boxes of 16 rows x 8 groups (zero fill past N and K)
             if (lane == 0) {
-                mbar_arrive_expect_tx(bar, ST_WSLOT + QSLOT);
-                tma_load_2d(wslots + d * ST_WSLOT, &tm_w, bar, k / 2, row0);
+                mbar_arrive_expect_tx(bar, WSLOT + QSLOT);
+                tma_load_2d(wslots + d * WSLOT, &tm_w, bar, k / 2, row0);
                 tma_load_2d(qslots + d * QSLOT, &tm_s, bar, k / G, row0);
-                tma_load_2d(qslots + d * QSLOT + 16 * QROW, &tm_o, bar, k / G, row0);
+                tma_load_2d(qslots + d * QSLOT + ROWS * QROW, &tm_o, bar, k / G, row0);
             }
             return;
         }
         if (lane == 0) {
-            mbar_arrive_expect_tx(bar, ST_WSLOT);
-            tma_load_2d(wslots + d * ST_WSLOT, &tm_w, bar, k / 2, row0);
+            mbar_arrive_expect_tx(bar, WSLOT);
+            tma_load_2d(wslots + d * WSLOT, &tm_w, bar, k / 2, row0);
         }
-        const bool edge = (row0 + 16 > p.N) || (k + ST_UK > p.K);  // clamp into the tensor (finite fill values)
+        const bool edge = (row0 + ROWS > p.N) || (k + ST_UK > p.K);  // clamp into the tensor (finite fill values)
 #pragma unroll
         for (int q = 0; q < PPL; ++q) {
             if (PIECES % 32 == 0 || lane + 32 * q < PIECES) {
@@ -338,7 +347,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             ++tile;
         }
     };
-    const int depth = nunits < ST_DEPTH ? nunits : ST_DEPTH;
+    const int depth = nunits < DEPTH ? nunits : DEPTH;
     for (int d = 0; d < depth; ++d) {
         issue(it_tile, it_kc, d);
         advance(it_tile, it_kc);
@@ -387,7 +396,10 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     float acc[MT][4];
 #pragma unroll
     for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-    float ya = 0.f, yb = 0.f;  // one-token path: rows pr, pr + 8 over this lane's slices of the tile so far
+    float ya[RT], yb[RT];      // one-token path: rows pr, pr + 8 (of each row tile) over this lane's slices
+    float oacc[RT][1][4];      // one-token path: the owner's sums of its last tile, kept for after the loop
+#pragma unroll
+    for (int rt = 0; rt < RT; ++rt) ya[rt] = yb[rt] = 0.f;
     float xpart = 0.f;         // one-token path: sum of the lane's 8-k chunk of X
     // L1 path: this lane's tokens (8t + gid) read their 8-k chunk at 32 tq + 8 j of each half
     const uint16_t* xl1 = p.X + (int64_t)gid * p.K + 32 * tq;
@@ -411,36 +423,47 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         ok = mbar_wait_bounded(bars + 8 * d, phase, nullptr, &g_stream_fault, 1u, ST_WAIT_LIMIT_NS) && ok;
         __syncwarp();
 
-        const uint32_t ws_a = wslots + d * ST_WSLOT + pr * 128;
-        const uint32_t ws_b = ws_a + 8 * 128;
-        const uint32_t qa = qslots + d * QSLOT + pr * QROW;  // scales of row pr; offsets 16 rows further
+        const uint32_t ws_a = wslots + d * WSLOT + pr * 128;   // row pr of the (first) row tile; row tile rt
+        const uint32_t ws_b = ws_a + 8 * 128;                  // starts 16 rows (16 x 128 bytes) further
+        const uint32_t qa = qslots + d * QSLOT + pr * QROW;  // scales of row pr; offsets ROWS rows further
         const uint32_t qb = qa + 8 * QROW;
         const uint32_t bbase = gid < p.M ? smem_u32(xs) + xrow_off : zaddr;
-        float dacc[4];  // one-token path: D[row][slice] of this unit
+        float dacc[RT][4];  // one-token path: D[row][slice] of this unit, per row tile
 #pragma unroll
         for (int h = 0; h < 2; ++h) {  // two 128-k steps per unit
             const uint32_t cpos = h ? cpos1 : cpos0;
-            const uint4 wa = lds128_st(ws_a + cpos);
-            const uint4 wb = lds128_st(ws_b + cpos);
-            const uint32_t wa4[4] = {wa.x, wa.y, wa.z, wa.w};
-            const uint32_t wb4[4] = {wb.x, wb.y, wb.z, wb.w};
             if constexpr (DIAG) {
+                uint32_t wa4[RT][4], wb4[RT][4];
+#pragma unroll
+                for (int rt = 0; rt < RT; ++rt) {
+                    const uint4 wa = lds128_st(ws_a + rt * 16 * 128 + cpos);
+                    const uint4 wb = lds128_st(ws_b + rt * 16 * 128 + cpos);
+                    wa4[rt][0] = wa.x, wa4[rt][1] = wa.y, wa4[rt][2] = wa.z, wa4[rt][3] = wa.w;
+                    wb4[rt][0] = wb.x, wb4[rt][1] = wb.y, wb4[rt][2] = wb.z, wb4[rt][3] = wb.w;
+                }
                 // X only on the lane whose column is its own slice (gid = tq + 4h)
                 const uint32_t bd = (gid == tq + 4 * h) ? smem_u32(xs) : zaddr;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const uint4 xv = lds128_st(bd + 256u * h + boff[j]);
-                    if (h == 0 && j == 0)
-                        raw_mma<0, true>(dacc, wa4[j], wb4[j], xv.x, xv.y, cm, cg);
-                    else
-                        raw_mma<0, false>(dacc, wa4[j], wb4[j], xv.x, xv.y, cm, cg);
-                    raw_mma<8, false>(dacc, wa4[j], wb4[j], xv.z, xv.w, cm, cg);
+#pragma unroll
+                    for (int rt = 0; rt < RT; ++rt) {  // one X fragment, every row tile of the unit
+                        if (h == 0 && j == 0)
+                            raw_mma<0, true>(dacc[rt], wa4[rt][j], wb4[rt][j], xv.x, xv.y, cm, cg);
+                        else
+                            raw_mma<0, false>(dacc[rt], wa4[rt][j], wb4[rt][j], xv.x, xv.y, cm, cg);
+                        raw_mma<8, false>(dacc[rt], wa4[rt][j], wb4[rt][j], xv.z, xv.w, cm, cg);
+                    }
                 }
                 continue;
             }
+            const uint4 wa = lds128_st(ws_a + cpos);
+            const uint4 wb = lds128_st(ws_b + cpos);
+            const uint32_t wa4[4] = {wa.x, wa.y, wa.z, wa.w};
+            const uint32_t wb4[4] = {wb.x, wb.y, wb.z, wb.w};
             const uint32_t jq = h ? jq1 : jq0;
-            const uint32_t sa = lds_u16_st(qa + jq), oa = lds_u16_st(qa + 16 * QROW + jq);
-            const uint32_t sb = lds_u16_st(qb + jq), ob = lds_u16_st(qb + 16 * QROW + jq);
+            const uint32_t sa = lds_u16_st(qa + jq), oa = lds_u16_st(qa + ROWS * QROW + jq);
+            const uint32_t sb = lds_u16_st(qb + jq), ob = lds_u16_st(qb + ROWS * QROW + jq);
             const uint32_t sa2 = __byte_perm(sa, 0, 0x1010), oa2 = __byte_perm(oa, 0, 0x1010);
             const uint32_t sb2 = __byte_perm(sb, 0, 0x1010), ob2 = __byte_perm(ob, 0, 0x1010);
 #pragma unroll
@@ -478,51 +501,81 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             xsl += __shfl_xor_sync(0xffffffffu, xsl, 1);
             xsl += __shfl_xor_sync(0xffffffffu, xsl, 2);  // lanes 4c .. 4c+3: sum of slice c
             const float xs0 = __shfl_sync(0xffffffffu, xsl, 8 * tq), xs1 = __shfl_sync(0xffffffffu, xsl, 8 * tq + 4);
-            // this lane's columns are slices 2tq and 2tq+1: D[pr][.] in dacc[0..1], D[pr+8][.] in dacc[2..3]
-            if constexpr (G == 32) {  // two groups, adjacent in the qparam rows
-                const uint32_t sA = lds_u32_st(qa + 4 * tq), oA = lds_u32_st(qa + 16 * QROW + 4 * tq);
-                const uint32_t sB = lds_u32_st(qb + 4 * tq), oB = lds_u32_st(qb + 16 * QROW + 4 * tq);
-                ya = fmaf(bf16_lo(sA), fmaf(-128.f, xs0, dacc[0]), ya);
-                ya = fmaf(bf16_lo(oA), xs0, ya);
-                ya = fmaf(bf16_hi(sA), fmaf(-128.f, xs1, dacc[1]), ya);
-                ya = fmaf(bf16_hi(oA), xs1, ya);
-                yb = fmaf(bf16_lo(sB), fmaf(-128.f, xs0, dacc[2]), yb);
-                yb = fmaf(bf16_lo(oB), xs0, yb);
-                yb = fmaf(bf16_hi(sB), fmaf(-128.f, xs1, dacc[3]), yb);
-                yb = fmaf(bf16_hi(oB), xs1, yb);
-            } else {  // both slices in one group
-                const uint32_t go = (uint32_t)(((64 * tq) / G) * 2);
-                const float x01 = xs0 + xs1;
-                const float sa = bf16_lo(lds_u16_st(qa + go)), oa = bf16_lo(lds_u16_st(qa + 16 * QROW + go));
-                const float sb = bf16_lo(lds_u16_st(qb + go)), ob = bf16_lo(lds_u16_st(qb + 16 * QROW + go));
-                ya = fmaf(sa, fmaf(-128.f, x01, dacc[0] + dacc[1]), ya);
-                ya = fmaf(oa, x01, ya);
-                yb = fmaf(sb, fmaf(-128.f, x01, dacc[2] + dacc[3]), yb);
-                yb = fmaf(ob, x01, yb);
+#pragma unroll
+            for (int rt = 0; rt < RT; ++rt) {
+                // this lane's columns are slices 2tq and 2tq+1: D[pr][.] in dacc[rt][0..1], D[pr+8][.] in [2..3]
+                const uint32_t qra = qa + rt * 16 * QROW, qrb = qb + rt * 16 * QROW;
+                if constexpr (G == 32) {  // two groups, adjacent in the qparam rows
+                    const uint32_t sA = lds_u32_st(qra + 4 * tq), oA = lds_u32_st(qra + ROWS * QROW + 4 * tq);
+                    const uint32_t sB = lds_u32_st(qrb + 4 * tq), oB = lds_u32_st(qrb + ROWS * QROW + 4 * tq);
+                    ya[rt] = fmaf(bf16_lo(sA), fmaf(-128.f, xs0, dacc[rt][0]), ya[rt]);
+                    ya[rt] = fmaf(bf16_lo(oA), xs0, ya[rt]);
+                    ya[rt] = fmaf(bf16_hi(sA), fmaf(-128.f, xs1, dacc[rt][1]), ya[rt]);
+                    ya[rt] = fmaf(bf16_hi(oA), xs1, ya[rt]);
+                    yb[rt] = fmaf(bf16_lo(sB), fmaf(-128.f, xs0, dacc[rt][2]), yb[rt]);
+                    yb[rt] = fmaf(bf16_lo(oB), xs0, yb[rt]);
+                    yb[rt] = fmaf(bf16_hi(sB), fmaf(-128.f, xs1, dacc[rt][3]), yb[rt]);
+                    yb[rt] = fmaf(bf16_hi(oB), xs1, yb[rt]);
+                } else {  // both slices in one group
+                    const uint32_t go = (uint32_t)(((64 * tq) / G) * 2);
+                    const float x01 = xs0 + xs1;
+                    const float sa = bf16_lo(lds_u16_st(qra + go)), oa = bf16_lo(lds_u16_st(qra + ROWS * QROW + go));
+                    const float sb = bf16_lo(lds_u16_st(qrb + go)), ob = bf16_lo(lds_u16_st(qrb + ROWS * QROW + go));
+                    ya[rt] = fmaf(sa, fmaf(-128.f, x01, dacc[rt][0] + dacc[rt][1]), ya[rt]);
+                    ya[rt] = fmaf(oa, x01, ya[rt]);
+                    yb[rt] = fmaf(sb, fmaf(-128.f, x01, dacc[rt][2] + dacc[rt][3]), yb[rt]);
+                    yb[rt] = fmaf(ob, x01, yb[rt]);
+                }
             }
         }
         __syncwarp();
-        if (it + ST_DEPTH < nunits) {  // refill the slot (its reads are done: order them before the async writes)
+        if (it + DEPTH < nunits) {  // refill the slot (its reads are done: order them before the async writes)
             fence_proxy_async_smem();
             issue(it_tile, it_kc, d);
             advance(it_tile, it_kc);
         }
-        if (++d == ST_DEPTH) {
+        if (++d == DEPTH) {
             d = 0;
             phase ^= 1u;
         }
 
         // end of a row tile or of the range: hand the tile's sums on
-        if (it + 1 == nunits || kc == p.nkc - 1) {
-            if constexpr (DIAG) {  // the row sums over the four lanes of a row pair (slices 0..7)
-                ya += __shfl_xor_sync(0xffffffffu, ya, 1);
-                ya += __shfl_xor_sync(0xffffffffu, ya, 2);
-                yb += __shfl_xor_sync(0xffffffffu, yb, 1);
-                yb += __shfl_xor_sync(0xffffffffu, yb, 2);
-                acc[0][0] = ya;  // token 0 of rows pr, pr + 8 (written by the tq = 0 lanes)
-                acc[0][2] = yb;
-                ya = yb = 0.f;
+        if ((it + 1 == nunits || kc == p.nkc - 1) && DIAG) {
+            // the row sums over the four lanes of a row pair (slices 0..7), per row tile
+            float racc[RT][1][4];
+#pragma unroll
+            for (int rt = 0; rt < RT; ++rt) {
+                ya[rt] += __shfl_xor_sync(0xffffffffu, ya[rt], 1);
+                ya[rt] += __shfl_xor_sync(0xffffffffu, ya[rt], 2);
+                yb[rt] += __shfl_xor_sync(0xffffffffu, yb[rt], 1);
+                yb[rt] += __shfl_xor_sync(0xffffffffu, yb[rt], 2);
+                racc[rt][0][0] = ya[rt];  // token 0 of rows pr, pr + 8 of row tile rt (the tq = 0 lanes write)
+                racc[rt][0][2] = yb[rt];
+                racc[rt][0][1] = racc[rt][0][3] = 0.f;
+                ya[rt] = yb[rt] = 0.f;
             }
+            if (kc_first == 0 && kc == p.nkc - 1) {  // this warp summed all of the tile's k
+#pragma unroll
+                for (int rt = 0; rt < RT; ++rt) {
+                    const int n_a = tile * ROWS + 16 * rt + pr, n_b = n_a + 8;
+                    if (tq == 0 && n_a < p.N) p.Y[n_a] = (uint16_t)float_to_bf16_bits(racc[rt][0][0]);
+                    if (tq == 0 && n_b < p.N) p.Y[n_b] = (uint16_t)float_to_bf16_bits(racc[rt][0][2]);
+                }
+            } else if (kc_first != 0) {  // a later share of the tile (the first of this range): publish it
+#pragma unroll
+                for (int rt = 0; rt < RT; ++rt)
+                    split_publish<1>(p.ws + ((size_t)worker * RT + rt) * 16, racc[rt], 1,
+                                     min(16, p.N - (tile * ROWS + 16 * rt)), pr, tq);
+            } else {  // the tile's owner: its range ends here (last iteration); finished after the loop
+#pragma unroll
+                for (int rt = 0; rt < RT; ++rt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) oacc[rt][0][i] = racc[rt][0][i];
+                owner_split = true;
+                break;
+            }
+            kc_first = 0;
+        } else if (it + 1 == nunits || kc == p.nkc - 1) {
             const int n_a = tile * 16 + pr, n_b = n_a + 8;
             // acc[t] = D[row n_a: tokens 8t + 2tq, +1 | row n_b: the same tokens]
             if (kc_first == 0 && kc == p.nkc - 1) {  // this warp summed all of the tile's k
@@ -548,13 +601,24 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     if (owner_split) {  // add the later shares of the last tile (their warps publish without waiting), write Y
         const int wl = split_warp_of((long long)tile * p.nkc + p.nkc - 1, p.units, p.workers);
         constexpr int NE = MX / 2 ? MX / 2 : 1;  // slot words per lane (16 M / 32)
-        ok = split_collect<MT, NE>(acc, scr, p.ws, worker, wl, p.M, min(16, p.N - tile * 16), pr, tq, lane,
-                                   p.Y + (int64_t)tile * 16, p.N, &g_stream_fault, 2u, ST_WAIT_LIMIT_NS) &&
-             ok;
+        if constexpr (DIAG) {
+#pragma unroll
+            for (int rt = 0; rt < RT; ++rt)  // a slot holds the row tiles one after another
+                ok = split_collect<1, NE>(oacc[rt], scr + rt * 16, p.ws + rt * 16, (size_t)RT * 16, worker, wl, 1,
+                                          min(16, p.N - (tile * ROWS + 16 * rt)), pr, tq, lane,
+                                          p.Y + (int64_t)tile * ROWS + 16 * rt, p.N, &g_stream_fault, 2u,
+                                          ST_WAIT_LIMIT_NS) &&
+                     ok;
+        } else {
+            ok = split_collect<MT, NE>(acc, scr, p.ws, (size_t)16 * p.M, worker, wl, p.M, min(16, p.N - tile * 16), pr,
+                                       tq, lane, p.Y + (int64_t)tile * 16, p.N, &g_stream_fault, 2u,
+                                       ST_WAIT_LIMIT_NS) &&
+                 ok;
+        }
     }
     if (!ok) {  // never leave with copies still landing in shared memory
-        for (int it = max(0, nunits - ST_DEPTH); it < nunits; ++it)
-            mbar_drain_bounded(bars + 8 * (it % ST_DEPTH), (uint32_t)((it / ST_DEPTH) & 1), ST_WAIT_LIMIT_NS);
+        for (int it = max(0, nunits - DEPTH); it < nunits; ++it)
+            mbar_drain_bounded(bars + 8 * (it % DEPTH), (uint32_t)((it / DEPTH) & 1), ST_WAIT_LIMIT_NS);
     }
 }
 
@@ -569,28 +633,29 @@ bool plan_stream(int64_t M, int64_t N, int64_t K, int g, StreamPlan* plan) {
     plan->nkc = (int)((K + ST_UK - 1) / ST_UK);
     plan->units = tiles * plan->nkc;
     plan->tiles = tiles;
-    plan->smem = (size_t)st_smem_bytes((int)M, g);
+    plan->smem = (size_t)st_smem_bytes((int)M, g, 1);
     plan->ws_bytes = split_ws_bytes(M, plan->units);
     return true;
 }
 
-template <int G, int MX, bool QT>
-static cudaError_t launch_stream_gm(const StreamPlan& plan, const CUtensorMap& tw, const CUtensorMap& ts,
-                                   const CUtensorMap& to, StreamArgs a, cudaStream_t stream) {
-    auto kern = stream_kernel<G, MX, QT>;
-    cudaError_t e = ensure_kernel_attrs(reinterpret_cast<const void*>(kern), st_smem_bytes(MX, G), false);
+template <int G, int MX, bool QT, int RT>
+static cudaError_t launch_stream_gm(const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& to, StreamArgs a,
+                                    cudaStream_t stream) {
+    auto kern = stream_kernel<G, MX, QT, RT>;
+    const size_t smem = (size_t)st_smem_bytes(a.M, G, RT);
+    cudaError_t e = ensure_kernel_attrs(reinterpret_cast<const void*>(kern), st_smem_bytes(MX, G, RT), false);
     if (e != cudaSuccess) return e;
     // one wave: as many resident warps as the SMs hold, but no more than there are units
     int sms = 0, per_sm = 0;
-    if ((e = resident_blocks(reinterpret_cast<const void*>(kern), ST_THREADS, plan.smem, &sms, &per_sm)) != cudaSuccess)
+    if ((e = resident_blocks(reinterpret_cast<const void*>(kern), ST_THREADS, smem, &sms, &per_sm)) != cudaSuccess)
         return e;
     const long long max_workers = std::min<long long>((long long)sms * per_sm * ST_WARPS, SPLIT_MAX_WORKERS);
-    a.workers = (int)std::min<long long>(max_workers, plan.units);
+    a.workers = (int)std::min<long long>(max_workers, a.units);
     const int blocks = (a.workers + ST_WARPS - 1) / ST_WARPS;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks, 1, 1);
     cfg.blockDim = dim3(ST_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = plan.smem;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -601,33 +666,62 @@ static cudaError_t launch_stream_gm(const StreamPlan& plan, const CUtensorMap& t
 }
 
 template <int G, bool QT>
-static cudaError_t launch_stream_g(const StreamPlan& plan, const CUtensorMap& tw, const CUtensorMap& ts,
-                                   const CUtensorMap& to, StreamArgs a, cudaStream_t stream) {
-    if (a.M <= 1) return launch_stream_gm<G, 1, QT>(plan, tw, ts, to, a, stream);
-    if (a.M <= 2) return launch_stream_gm<G, 2, QT>(plan, tw, ts, to, a, stream);
-    if (a.M <= 4) return launch_stream_gm<G, 4, QT>(plan, tw, ts, to, a, stream);
-    if (a.M <= 8) return launch_stream_gm<G, 8, QT>(plan, tw, ts, to, a, stream);
-    if (a.M <= 16) return launch_stream_gm<G, 16, QT>(plan, tw, ts, to, a, stream);
-    return launch_stream_gm<G, 32, QT>(plan, tw, ts, to, a, stream);
+static cudaError_t launch_stream_g(const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& to, StreamArgs a,
+                                   int rt, cudaStream_t stream) {
+    if (rt == 2) return launch_stream_gm<G, 1, QT, 2>(tw, ts, to, a, stream);
+    if (a.M <= 1) return launch_stream_gm<G, 1, QT, 1>(tw, ts, to, a, stream);
+    if (a.M <= 2) return launch_stream_gm<G, 2, QT, 1>(tw, ts, to, a, stream);
+    if (a.M <= 4) return launch_stream_gm<G, 4, QT, 1>(tw, ts, to, a, stream);
+    if (a.M <= 8) return launch_stream_gm<G, 8, QT, 1>(tw, ts, to, a, stream);
+    if (a.M <= 16) return launch_stream_gm<G, 16, QT, 1>(tw, ts, to, a, stream);
+    return launch_stream_gm<G, 32, QT, 1>(tw, ts, to, a, stream);
+}
+
+// One token takes 32-row units (two row tiles sharing the X staging, slice sums
+// and ring work of a unit) when there are enough of them to give every resident
+// warp one, and the workspace holds two 16-row slots per warp.
+template <int G, bool QT>
+static cudaError_t two_row_tiles(int64_t N, int nkc, size_t ws_bytes, bool* two) {
+    auto kern = stream_kernel<G, 1, QT, 2>;
+    cudaError_t e = ensure_kernel_attrs(reinterpret_cast<const void*>(kern), st_smem_bytes(1, G, 2), false);
+    int sms = 0, per_sm = 0;
+    if (e == cudaSuccess)
+        e = resident_blocks(reinterpret_cast<const void*>(kern), ST_THREADS, st_smem_bytes(1, G, 2), &sms, &per_sm);
+    if (e != cudaSuccess) return e;
+    const long long max_workers = std::min<long long>((long long)sms * per_sm * ST_WARPS, SPLIT_MAX_WORKERS);
+    const long long units = (N + 31) / 32 * (long long)nkc;
+    *two = units >= max_workers && (size_t)max_workers * 2 * 16 * 8 <= ws_bytes;
+    return cudaSuccess;
 }
 
 cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
                           const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
                           void* workspace, cudaStream_t stream, const char** detail) {
-    CUtensorMap tw, ts, to;  // codes: [N][K/2] bytes, one box = 16 rows x 128 bytes (256 k), 128-byte swizzle
-    cudaError_t e = encode_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)(K / 2), (uint64_t)N,
-                                         (uint64_t)(K / 2), 128, 16, CU_TENSOR_MAP_SWIZZLE_128B, detail);
-    if (e != cudaSuccess) return e;
     const int64_t ng = K / g;
     const bool qt = (g == 32) && (ng % 8 == 0);  // qparam rows 16-byte aligned: 8-group TMA boxes
+    cudaError_t e = cudaSuccess;
+    bool two = false;
+    if (M == 1) {
+        e = g == 32 ? (qt ? two_row_tiles<32, true>(N, plan.nkc, plan.ws_bytes, &two)
+                          : two_row_tiles<32, false>(N, plan.nkc, plan.ws_bytes, &two))
+                    : g == 64 ? two_row_tiles<64, false>(N, plan.nkc, plan.ws_bytes, &two)
+                              : two_row_tiles<128, false>(N, plan.nkc, plan.ws_bytes, &two);
+        if (e != cudaSuccess) return e;
+    }
+    const int rt = two ? 2 : 1;
+    // codes: [N][K/2] bytes, one box = 16 rt rows x 128 bytes (256 k), 128-byte swizzle
+    CUtensorMap tw, ts, to;
+    e = encode_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)(K / 2), (uint64_t)N, (uint64_t)(K / 2),
+                             128, 16 * rt, CU_TENSOR_MAP_SWIZZLE_128B, detail);
+    if (e != cudaSuccess) return e;
     ts = tw;
     to = tw;
     if (qt) {
         e = encode_tensor_map_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, (uint64_t)ng, (uint64_t)N,
-                                 (uint64_t)ng * 2, 8, 16, CU_TENSOR_MAP_SWIZZLE_NONE, detail);
+                                 (uint64_t)ng * 2, 8, 16 * rt, CU_TENSOR_MAP_SWIZZLE_NONE, detail);
         if (e == cudaSuccess)
             e = encode_tensor_map_2d(&to, CU_TENSOR_MAP_DATA_TYPE_UINT16, offsets, (uint64_t)ng, (uint64_t)N,
-                                     (uint64_t)ng * 2, 8, 16, CU_TENSOR_MAP_SWIZZLE_NONE, detail);
+                                     (uint64_t)ng * 2, 8, 16 * rt, CU_TENSOR_MAP_SWIZZLE_NONE, detail);
         if (e != cudaSuccess) return e;
     }
     StreamArgs a;
@@ -640,14 +734,14 @@ cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, 
     a.N = (int)N;
     a.K = (int)K;
     a.nkc = plan.nkc;
-    a.units = plan.units;
+    a.units = rt == 2 ? (N + 31) / 32 * (long long)plan.nkc : plan.units;
     a.workers = 0;
     switch (g) {
         case 32:
-            return qt ? launch_stream_g<32, true>(plan, tw, ts, to, a, stream)
-                      : launch_stream_g<32, false>(plan, tw, ts, to, a, stream);
-        case 64: return launch_stream_g<64, false>(plan, tw, ts, to, a, stream);
-        default: return launch_stream_g<128, false>(plan, tw, ts, to, a, stream);
+            return qt ? launch_stream_g<32, true>(tw, ts, to, a, rt, stream)
+                      : launch_stream_g<32, false>(tw, ts, to, a, rt, stream);
+        case 64: return launch_stream_g<64, false>(tw, ts, to, a, rt, stream);
+        default: return launch_stream_g<128, false>(tw, ts, to, a, rt, stream);
     }
 }
 

@@ -180,6 +180,27 @@ def test_linear_stream(g, nk):
         assert int(ws.buf.count_nonzero()) == 0, "the stream kernel must leave its workspace zeroed"
 
 
+# one token on problems large enough for 32-row units (two row tiles per unit), ragged row tails
+ONE_TOKEN_NK = [(4104, 6144), (4120, 6144), (4096, 6080), (8192, 4096)]
+
+
+@pytest.mark.parametrize("g", [32, 64, 128])
+@pytest.mark.parametrize("nk", ONE_TOKEN_NK, ids=[f"{n}x{k}" for n, k in ONE_TOKEN_NK])
+def test_linear_stream_one_token_large(g, nk):
+    N, K = nk
+    if K % g or (K // g) % 2:
+        pytest.skip("the stream kernel needs an even K/g")
+    ws = w4.Workspace(DEV).reserve_for(1, N, K, g)
+    (X, Wq, sc, of), y_ref = _problem(1, N, K, g, seed=N + K + g)
+    y = gpu_linear(X, Wq, sc, of, g, w4.KERNEL_STREAM, workspace=ws)
+    assert_linear_ok(y, y_ref, f"stream M=1 N={N} K={K} g={g}")
+    for _ in range(3):  # deterministic
+        assert torch.equal(y.view(torch.int16), gpu_linear(X, Wq, sc, of, g, w4.KERNEL_STREAM, workspace=ws).view(torch.int16))
+    torch.cuda.synchronize()
+    assert int(ws.buf.count_nonzero()) == 0, "the stream kernel must leave its workspace zeroed"
+    w4.w4_device_fault(DEV)
+
+
 REPACK_NK = [(200, 4160), (520, 512), (64, 96), (1030, 1024), (48, 14336), (16, 256), (33, 1152)]
 
 
