@@ -75,8 +75,9 @@ __host__ __device__ inline int st_qslot_bytes(int g, int rt) { return 2 * 16 * r
 // ring slots per warp: three 16-row units, or two 32-row units
 __host__ __device__ inline int st_depth(int rt) { return rt == 1 ? ST_DEPTH : 2; }
 // X slot (one unit x M token rows; a warp rewrites it only after its reads of the
-// previous unit have returned) and a zero row: only up to 8 tokens (beyond, X comes through L1)
-__host__ __device__ inline int st_xslot_bytes(int M) { return M <= 8 ? (M + 1) * ST_XPITCH : 0; }
+// previous unit have returned): only up to 8 tokens (beyond, X comes through L1).
+// The block's warps share one zero row after their areas.
+__host__ __device__ inline int st_xslot_bytes(int M) { return M <= 8 ? M * ST_XPITCH : 0; }
 __host__ __device__ inline int st_scratch_bytes(int M, int rt) { return 16 * rt * M * 4; }  // a tile's fp32 sums
 __host__ __device__ inline int st_rest_bytes(int M, int g, int rt) {
     const int dp = st_depth(rt);
@@ -84,7 +85,8 @@ __host__ __device__ inline int st_rest_bytes(int M, int g, int rt) {
     return (b + 127) & ~127;  // qparam slots are TMA destinations: 128-byte aligned
 }
 __host__ __device__ inline int st_smem_bytes(int M, int g, int rt) {
-    return ST_WARPS * st_depth(rt) * ST_WSLOT * rt + ST_WARPS * st_rest_bytes(M, g, rt) + 1024;  // + alignment slack
+    return ST_WARPS * st_depth(rt) * ST_WSLOT * rt + ST_WARPS * st_rest_bytes(M, g, rt) + (M <= 8 ? ST_XPITCH : 0) +
+           1024;  // zero row, alignment slack
 }
 
 __device__ unsigned int g_stream_fault;
@@ -278,7 +280,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     constexpr int MT = L1X ? MX / 8 : 1;  // groups of 8 tokens
     constexpr bool DIAG = MX == 1;   // one token: slice sums in the MMA columns, scales in fp32
     unsigned char* xs = rbase + DEPTH * QSLOT;                          // X slot: M token rows
-    unsigned char* zrow = xs + p.M * ST_XPITCH;                         // zeros for tokens >= M
+    unsigned char* zrow = smem + ST_WARPS * (DEPTH * WSLOT + rest);     // zeros for tokens >= M (shared)
     float* scr = reinterpret_cast<float*>(rbase + DEPTH * QSLOT + st_xslot_bytes(p.M));  // split-tile scratch
     const uint32_t bars = smem_u32(rbase + DEPTH * QSLOT + st_xslot_bytes(p.M) + st_scratch_bytes(p.M, RT));
     const int ng = p.K / G;
@@ -287,7 +289,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         for (int d = 0; d < DEPTH; ++d) mbar_init(bars + 8 * d, QT ? 1 : 33);
         mbar_fence_init();
     }
-    if (!L1X)
+    if (!L1X)  // every warp writes the same zeros (no block barrier needed before its own reads)
         for (int c = lane; c < ST_XPITCH / 16; c += 32)
             *reinterpret_cast<uint4*>(zrow + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
     __syncwarp();
