@@ -124,7 +124,9 @@ struct DcUnit {
 };
 
 // MT: groups of 8 tokens (M <= 8 MT).
-template <int G, int MT>
+// NE: slot words per lane of an owner's collect (16 M / 32): 1 for one token,
+// 4 MT otherwise.
+template <int G, int MT, int NE>
 __global__ void __launch_bounds__(DC_THREADS, MT == 4 ? 4 : 5)
 decode_kernel(const DecodeArgs p) {
     constexpr int SLOT16 = (2048 + 16 * 32 * 32 / G) / 16;  // 16-byte pieces per unit
@@ -247,8 +249,8 @@ decode_kernel(const DecodeArgs p) {
     }
     if (owner_split) {  // add the later shares of the last tile (their warps publish without waiting), write Y
         const int wl = split_warp_of((long long)tile * p.nkc + p.nkc - 1, p.units, p.workers);
-        split_collect<MT, 4 * MT>(acc, scr[warp], p.ws, (size_t)16 * p.M, worker, wl, p.M, min(16, p.N - tile * 16),
-                                  gid, tq, lane, p.Y + (int64_t)tile * 16, p.N, &g_decode_fault, 1u, DC_WAIT_LIMIT_NS);
+        split_collect<MT, NE>(acc, scr[warp], p.ws, (size_t)16 * p.M, worker, wl, p.M, min(16, p.N - tile * 16), gid,
+                              tq, lane, p.Y + (int64_t)tile * 16, p.N, &g_decode_fault, 1u, DC_WAIT_LIMIT_NS);
     }
 }
 
@@ -265,9 +267,9 @@ bool plan_decode(int64_t M, int64_t N, int64_t K, int g, DecodePlan* plan) {
     return true;
 }
 
-template <int G, int MT>
+template <int G, int MT, int NE>
 static cudaError_t launch_decode_gm(const DecodePlan& plan, DecodeArgs a, cudaStream_t stream) {
-    auto kern = decode_kernel<G, MT>;
+    auto kern = decode_kernel<G, MT, NE>;
     // one wave: as many resident warps as the SMs hold, but no more than there are units
     int sms = 0, per_sm = 0;
     cudaError_t e = resident_blocks(reinterpret_cast<const void*>(kern), DC_THREADS, 0, &sms, &per_sm);
@@ -289,9 +291,10 @@ static cudaError_t launch_decode_gm(const DecodePlan& plan, DecodeArgs a, cudaSt
 
 template <int G>
 static cudaError_t launch_decode_g(const DecodePlan& plan, DecodeArgs a, cudaStream_t stream) {
-    if (a.M <= 8) return launch_decode_gm<G, 1>(plan, a, stream);
-    if (a.M <= 16) return launch_decode_gm<G, 2>(plan, a, stream);
-    return launch_decode_gm<G, 4>(plan, a, stream);
+    if (a.M <= 1) return launch_decode_gm<G, 1, 1>(plan, a, stream);
+    if (a.M <= 8) return launch_decode_gm<G, 1, 4>(plan, a, stream);
+    if (a.M <= 16) return launch_decode_gm<G, 2, 8>(plan, a, stream);
+    return launch_decode_gm<G, 4, 16>(plan, a, stream);
 }
 
 cudaError_t launch_decode(const DecodePlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* packed,
