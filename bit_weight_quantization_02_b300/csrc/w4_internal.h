@@ -47,6 +47,12 @@ cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, 
                           const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
                           void* workspace, cudaStream_t stream, const char** detail);
 cudaError_t read_and_clear_stream_fault(unsigned int* fault);
+// Batched decode (9 <= M <= 32): 64-row units, the block's X slice staged once
+// by TMA; same plan and workspace as the stream kernel (launch_stream calls it).
+cudaError_t launch_batch(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
+                         const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
+                         void* workspace, cudaStream_t stream, const char** detail);
+cudaError_t read_and_clear_batch_fault(unsigned int* fault);
 
 // Decode layout (see w4.h): bytes of one 16-row x 256-k unit, of the whole
 // layout, and the repack launch.

@@ -699,6 +699,8 @@ static cudaError_t two_row_tiles(int64_t N, int nkc, size_t ws_bytes, bool* two)
 cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
                           const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
                           void* workspace, cudaStream_t stream, const char** detail) {
+    if (M > 8)  // 9..32 tokens: the block-shared X kernel (w4_batch.cu)
+        return launch_batch(plan, X, M, K, Wq, scales, offsets, N, g, Y, workspace, stream, detail);
     const int64_t ng = K / g;
     const bool qt = (g == 32) && (ng % 8 == 0);  // qparam rows 16-byte aligned: 8-group TMA boxes
     cudaError_t e = cudaSuccess;
