@@ -481,8 +481,13 @@ def other_rows(args, w4, wl, device, stream, peaks, dist, only=None):
     # batched decode, config 3 (g=64): weights rotated through copies totalling > 4x L2
     b3 = []
     for c in (wl.config3() if want("batched") else []):
+        if args.batched_m and c.M != args.batched_m:
+            continue
         b3.append(_rotated_graph_row(c, w4, wl, device, stream, dist, peaks))
+        # the auto choice for the canonical layout: per-warp stream-K up to 4 tokens, block-shared X beyond
+        b3[-1]["kernel"] = "stream_kernel" if c.M <= 4 else "batch_kernel"
         b3.append(_rotated_graph_row(c, w4, wl, device, stream, dist, peaks, layout="decode"))
+        b3[-1]["kernel"] = "decode_kernel"
     rows["batched_decode_g64"] = {"unit": "GB/s", "cases": b3,
                                   "l2": "graph of back-to-back calls over weight copies totalling > 4x L2"}
 
@@ -641,6 +646,8 @@ def parse_args(argv=None):
     ap.add_argument("--prefill-iters", type=int, default=10)
     ap.add_argument("--section", choices=["all", "prefill", "shapes", "batched", "stack", "dequant"], default="all",
                     help="all = the benchmark; the others run one secondary row alone (for profiling) and print it")
+    ap.add_argument("--batched-m", type=int, default=0,
+                    help="with --section batched: only the cases with this many tokens (for profiling)")
     ap.add_argument("--layers", type=int, default=32,
                     help="Llama-3-8B blocks in the headline step (32 = the whole model; fewer only for profiling)")
     a = ap.parse_args(argv)

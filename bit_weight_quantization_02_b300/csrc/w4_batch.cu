@@ -1,5 +1,5 @@
 // w4_batch.cu -- persistent stream-K bf16 x int4 linear for batched decode
-// (9 <= M <= 32 tokens) on the canonical layout.
+// (5 <= M <= 32 tokens) on the canonical layout.
 //
 // Y[m,n] = sum_k X[m,k] * w'[n,k], w' = bf16(q*s + o), fp32 accumulation
 // (Optimum Quanto: bf16 x int4 matmul, result accumulated at higher precision,
@@ -75,6 +75,9 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
 }
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
 __device__ __forceinline__ uint4 lds128_b(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
@@ -118,7 +121,7 @@ __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a
 }
 
 template <int G, int MT, bool QT>
-__global__ void __launch_bounds__(BT_THREADS, 3)
+__global__ void __launch_bounds__(BT_THREADS, MT == 1 ? 4 : 3)
 batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
              const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_o, const BatchArgs p) {
     using L = BatchLayout<G, MT>;
@@ -257,12 +260,18 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
                 const int cg8 = 4 * q + 2 * s2 + (li & 1);  // this lane's ldmatrix chunk (8 k) in the unit
                 const uint32_t xrow = xst + (uint32_t)(cg8 >> 3) * L::XBOX +
                                       ((uint32_t)((cg8 & 7) ^ lr) << 4) + (uint32_t)lr * 128;
+                if (MT == 1) {  // one token group: matrices 0, 1 (lanes 0-15 give the addresses)
+                    uint32_t b0, b1;
+                    ldsm_x2(xrow, b0, b1);
+                    mma_16816(acc[0], a0, a1, a2, a3, b0, b1);
+                } else {
 #pragma unroll
-                for (int tp = 0; tp < MT / 2; ++tp) {
-                    uint32_t b0a, b1a, b0b, b1b;  // token groups 2tp (chunks c0, c0+1) and 2tp + 1
-                    ldsm_x4(xrow + (uint32_t)(16 * tp + 8 * (li >> 1)) * 128, b0a, b1a, b0b, b1b);
-                    mma_16816(acc[2 * tp], a0, a1, a2, a3, b0a, b1a);
-                    mma_16816(acc[2 * tp + 1], a0, a1, a2, a3, b0b, b1b);
+                    for (int tp = 0; tp < MT / 2; ++tp) {
+                        uint32_t b0a, b1a, b0b, b1b;  // token groups 2tp (chunks c0, c0+1) and 2tp + 1
+                        ldsm_x4(xrow + (uint32_t)(16 * tp + 8 * (li >> 1)) * 128, b0a, b1a, b0b, b1b);
+                        mma_16816(acc[2 * tp], a0, a1, a2, a3, b0a, b1a);
+                        mma_16816(acc[2 * tp + 1], a0, a1, a2, a3, b0b, b1b);
+                    }
                 }
             }
         }
@@ -356,6 +365,7 @@ static cudaError_t launch_batch_gm(const CUtensorMap& tw, const CUtensorMap& tx,
 template <int G, bool QT>
 static cudaError_t launch_batch_g(const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap& ts,
                                   const CUtensorMap& to, BatchArgs a, size_t ws_bytes, cudaStream_t stream) {
+    if (a.M <= 8) return launch_batch_gm<G, 1, QT>(tw, tx, ts, to, a, ws_bytes, stream);
     if (a.M <= 16) return launch_batch_gm<G, 2, QT>(tw, tx, ts, to, a, ws_bytes, stream);
     return launch_batch_gm<G, 4, QT>(tw, tx, ts, to, a, ws_bytes, stream);
 }
@@ -365,7 +375,7 @@ cudaError_t launch_batch(const StreamPlan& plan, const uint16_t* X, int64_t M, i
                          void* workspace, cudaStream_t stream, const char** detail) {
     const int64_t ng = K / g;
     const bool qt = (g == 32) && (ng % 8 == 0);  // qparam rows 16-byte aligned: 8-group TMA boxes
-    const int mp = M <= 16 ? 16 : 32;
+    const int mp = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
     CUtensorMap tw, tx, ts, to;
     // codes: [N][K/2] bytes, box 64 rows x 128 bytes; X: [M][K] bf16, box mp rows x 64 k (rows past M read 0)
     cudaError_t e = encode_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)(K / 2), (uint64_t)N,

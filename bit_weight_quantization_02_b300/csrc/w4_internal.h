@@ -31,7 +31,8 @@ cudaError_t launch_skinny(const SkinnyPlan& plan, const uint16_t* X, int64_t M, 
                           const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
                           cudaStream_t stream, const char** detail);
 
-// Persistent stream-K decode kernel (M <= 32): needs a zero-initialized,
+// Persistent stream-K decode kernel (M <= 4; launch_stream hands 5 <= M <= 32
+// to launch_batch with the same plan): needs a zero-initialized,
 // self-cleaning workspace of split_ws_bytes(M, units) bytes (w4_device.cuh).
 struct StreamPlan {
     int nkc;          // 256-k units per 16-row tile
@@ -47,7 +48,7 @@ cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, 
                           const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
                           void* workspace, cudaStream_t stream, const char** detail);
 cudaError_t read_and_clear_stream_fault(unsigned int* fault);
-// Batched decode (9 <= M <= 32): 64-row units, the block's X slice staged once
+// Batched decode (5 <= M <= 32): 64-row units, the block's X slice staged once
 // by TMA; same plan and workspace as the stream kernel (launch_stream calls it).
 cudaError_t launch_batch(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
                          const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,

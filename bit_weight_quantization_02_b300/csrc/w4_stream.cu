@@ -1,4 +1,5 @@
-// w4_stream.cu -- persistent stream-K bf16 x int4 linear for decode (M <= 32).
+// w4_stream.cu -- persistent stream-K bf16 x int4 linear for decode (M <= 4;
+// 5 to 32 tokens go to the block-shared X kernel of w4_batch.cu).
 //
 // Y[m,n] = sum_k X[m,k] * w'[n,k], w' = bf16(q*s + o), fp32 accumulation
 // (Optimum Quanto: bf16 x int4 matmul, result accumulated at higher precision,
@@ -16,12 +17,9 @@
 //    past N and K); the 32 lanes fetch its scales and offsets with 4-byte
 //    cp.async; all complete on the slot's mbarrier.  The first three units are
 //    requested before the programmatic-dependent-launch wait.
-//  * X (only 256 k x M tokens per unit), up to 8 tokens: loaded one unit
-//    ahead into registers, permuted to the MMA k order and staged in the
-//    warp's shared memory (tokens beyond M read a zero row).  9 to 32 tokens:
-//    every lane reads its tokens' 8-k chunks straight from global memory
-//    (L1-cached) and permutes them in registers, and one dequantized A
-//    fragment feeds one MMA per group of 8 tokens.
+//  * X (only 256 k x M tokens per unit): loaded one unit ahead into
+//    registers, permuted to the MMA k order and staged in the warp's shared
+//    memory (tokens beyond M read a zero row).
 //  * Dequantization and products as in the skinny kernel: LOP3 nibble pairs,
 //    exact subtract + one bf16 FMA, mma.m16n8k16 with the weights as the A
 //    operand and the tokens as B (swap AB).
@@ -75,8 +73,8 @@ __host__ __device__ inline int st_qslot_bytes(int g, int rt) { return 2 * 16 * r
 // ring slots per warp: three 16-row units, or two 32-row units
 __host__ __device__ inline int st_depth(int rt) { return rt == 1 ? ST_DEPTH : 2; }
 // X slot (one unit x M token rows; a warp rewrites it only after its reads of the
-// previous unit have returned): only up to 8 tokens (beyond, X comes through L1).
-// The block's warps share one zero row after their areas.
+// previous unit have returned); none beyond 8 tokens, which this kernel never
+// runs.  The block's warps share one zero row after their areas.
 __host__ __device__ inline int st_xslot_bytes(int M) { return M <= 8 ? M * ST_XPITCH : 0; }
 __host__ __device__ inline int st_scratch_bytes(int M, int rt) { return 16 * rt * M * 4; }  // a tile's fp32 sums
 __host__ __device__ inline int st_rest_bytes(int M, int g, int rt) {
@@ -158,34 +156,6 @@ __device__ __forceinline__ void dq_mma(float (&c)[4], uint32_t wa, uint32_t wb, 
           "r"(c128), "n"(SH), "n"(SH + 4));
 }
 
-// The four A-fragment registers of one MMA step (as in dq_mma), for reuse by
-// several token groups.
-template <int SH>
-__device__ __forceinline__ void dq_frag(uint32_t wa, uint32_t wb, uint32_t sa2, uint32_t oa2, uint32_t sb2,
-                                        uint32_t ob2, uint32_t cm, uint32_t cg, uint32_t (&A)[4]) {
-    asm("{\n\t.reg .b32 t;\n\t"
-        "shr.b32 t, %4, %12;\n\t"
-        "lop3.b32 %0, t, %10, %11, 0xEA;\n\t"
-        "shr.b32 t, %4, %13;\n\t"
-        "lop3.b32 %2, t, %10, %11, 0xEA;\n\t"
-        "shr.b32 t, %5, %12;\n\t"
-        "lop3.b32 %1, t, %10, %11, 0xEA;\n\t"
-        "shr.b32 t, %5, %13;\n\t"
-        "lop3.b32 %3, t, %10, %11, 0xEA;\n\t"
-        "sub.rn.bf16x2 %0, %0, %11;\n\t"
-        "sub.rn.bf16x2 %1, %1, %11;\n\t"
-        "sub.rn.bf16x2 %2, %2, %11;\n\t"
-        "sub.rn.bf16x2 %3, %3, %11;\n\t"
-        "fma.rn.bf16x2 %0, %0, %6, %7;\n\t"
-        "fma.rn.bf16x2 %1, %1, %8, %9;\n\t"
-        "fma.rn.bf16x2 %2, %2, %6, %7;\n\t"
-        "fma.rn.bf16x2 %3, %3, %8, %9;\n\t}"
-        : "=&r"(A[0]), "=&r"(A[1]), "=&r"(A[2]), "=&r"(A[3])
-        : "r"(wa), "r"(wb), "r"(sa2), "r"(oa2), "r"(sb2), "r"(ob2), "r"(cm), "r"(cg), "n"(SH), "n"(SH + 4));
-}
-__device__ __forceinline__ void mma_frag(float (&c)[4], const uint32_t (&A)[4], uint32_t x0, uint32_t x1) {
-    mma_bf16_16816_st(c, A[0], A[1], A[2], A[3], x0, x1);
-}
 // One MMA step on raw codes (the one-token path): A = 128 + q straight from
 // LOP3, B = X or zero per lane.  ZC starts from a zero accumulator.
 template <int SH, bool ZC>
@@ -236,22 +206,17 @@ __device__ __forceinline__ float bf16x8_sum(uint4 v) {
     const float c = bf16_lo(v.z) + bf16_hi(v.z), d = bf16_lo(v.w) + bf16_hi(v.w);
     return (a + b) + (c + d);
 }
-__device__ __forceinline__ uint4 ldg_nc_v4_st(const void* p) {
-    uint4 r;
-    asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
-    return r;
-}
-
-// MX: token capacity (1, 2, 4, 8: X staged in shared memory; 16, 32: X through L1).
+// MX: token capacity (1, 2, 4; X staged in shared memory).
 // RT: 16-row tiles per unit, 1, or 2 for one token on large problems (the X
 // staging, slice sums and ring work of a unit then serve 32 weight rows).
 template <int G, int MX, bool QT, int RT>
-__global__ void __launch_bounds__(ST_THREADS, RT == 2 ? 4 : (MX == 32 ? 4 : (MX >= 8 ? 5 : 6)))
+__global__ void __launch_bounds__(ST_THREADS, RT == 2 ? 4 : 6)
 stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
               const __grid_constant__ CUtensorMap tm_o, const StreamArgs p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     static_assert(RT == 1 || MX == 1, "two row tiles per unit only on the one-token path");
+    static_assert(MX == 1 || MX == 2 || MX == 4, "one to four tokens");
     constexpr int ROWS = 16 * RT;                    // weight rows per unit
     constexpr int DEPTH = RT == 1 ? ST_DEPTH : 2;    // ring slots (st_depth)
     constexpr int WSLOT = ST_WSLOT * RT;             // codes of one unit
@@ -276,8 +241,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     const uint32_t wslots = smem_u32(smem) + warp * (DEPTH * WSLOT);
     unsigned char* rbase = smem + ST_WARPS * DEPTH * WSLOT + warp * rest;
     const uint32_t qslots = smem_u32(rbase);
-    constexpr bool L1X = MX > 8;  // X through L1 instead of staged slots
-    constexpr int MT = L1X ? MX / 8 : 1;  // groups of 8 tokens
+    constexpr int MT = 1;            // one group of 8 token columns
     constexpr bool DIAG = MX == 1;   // one token: slice sums in the MMA columns, scales in fp32
     unsigned char* xs = rbase + DEPTH * QSLOT;                          // X slot: M token rows
     unsigned char* zrow = smem + ST_WARPS * (DEPTH * WSLOT + rest);     // zeros for tokens >= M (shared)
@@ -289,9 +253,9 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         for (int d = 0; d < DEPTH; ++d) mbar_init(bars + 8 * d, QT ? 1 : 33);
         mbar_fence_init();
     }
-    if (!L1X)  // every warp writes the same zeros (no block barrier needed before its own reads)
-        for (int c = lane; c < ST_XPITCH / 16; c += 32)
-            *reinterpret_cast<uint4*>(zrow + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
+    // every warp writes the same zeros (no block barrier needed before its own reads)
+    for (int c = lane; c < ST_XPITCH / 16; c += 32)
+        *reinterpret_cast<uint4*>(zrow + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
     __syncwarp();
 
     // this lane's qparam pieces: fixed (array, row, piece) for every unit
@@ -359,18 +323,18 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     griddep_wait();
 
     // X of a unit: lane c holds 8-k chunk c of every token (staged path)
-    uint4 xr[L1X ? 1 : MX];
+    uint4 xr[MX];
     const uint16_t* xlane = p.X + 8 * lane;
     auto load_x = [&](int kc) {
         const int k = kc * ST_UK + 8 * lane;
 #pragma unroll
-        for (int m = 0; m < (L1X ? 0 : MX); ++m)
+        for (int m = 0; m < MX; ++m)
             if (m < p.M) xr[m] = (k < p.K) ? ldg_cg_v4(xlane + (int64_t)m * p.K + kc * ST_UK) : make_uint4(0u, 0u, 0u, 0u);
     };
     const uint32_t xst = (uint32_t)(16 * st_x_slot(lane));
     auto store_x = [&](unsigned char* slot) {
 #pragma unroll
-        for (int m = 0; m < (L1X ? 0 : MX); ++m)
+        for (int m = 0; m < MX; ++m)
             if (m < p.M) {
                 uint4 o;
                 o.x = __byte_perm(xr[m].x, xr[m].z, 0x5410);  // (x0, x4)
@@ -403,8 +367,6 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
 #pragma unroll
     for (int rt = 0; rt < RT; ++rt) ya[rt] = yb[rt] = 0.f;
     float xpart = 0.f;         // one-token path: sum of the lane's 8-k chunk of X
-    // L1 path: this lane's tokens (8t + gid) read their 8-k chunk at 32 tq + 8 j of each half
-    const uint16_t* xl1 = p.X + (int64_t)gid * p.K + 32 * tq;
     int tile = tile0, kc = kc0, kc_first = kc0;  // unit being computed
     bool owner_split = false;                    // the range ends inside a tile whose first unit it holds
     int x_kc = kc0;                               // unit whose X sits in xr
@@ -412,15 +374,13 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     int d = 0;
     uint32_t phase = 0;
 
-    if (!L1X) load_x(x_kc);
+    load_x(x_kc);
     for (int it = 0; it < nunits; ++it) {
-        if (!L1X) {
-            store_x(xs);
-            if (DIAG) xpart = bf16x8_sum(xr[0]);
-            if (it + 1 < nunits) {
-                if (++x_kc == p.nkc) x_kc = 0;
-                load_x(x_kc);
-            }
+        store_x(xs);
+        if (DIAG) xpart = bf16x8_sum(xr[0]);
+        if (it + 1 < nunits) {
+            if (++x_kc == p.nkc) x_kc = 0;
+            load_x(x_kc);
         }
         ok = mbar_wait_bounded(bars + 8 * d, phase, nullptr, &g_stream_fault, 1u, ST_WAIT_LIMIT_NS) && ok;
         __syncwarp();
@@ -470,32 +430,9 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             const uint32_t sb2 = __byte_perm(sb, 0, 0x1010), ob2 = __byte_perm(ob, 0, 0x1010);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                if (!L1X) {
-                    const uint4 xv = lds128_st(bbase + 256u * h + boff[j]);
-                    dq_mma<0>(acc[0], wa4[j], wb4[j], sa2, oa2, sb2, ob2, xv.x, xv.y, cm, cg, c128);
-                    dq_mma<8>(acc[0], wa4[j], wb4[j], sa2, oa2, sb2, ob2, xv.z, xv.w, cm, cg, c128);
-                } else {
-                    const int kx = kc * ST_UK + 128 * h + 8 * j;  // + 32 tq inside xl1
-                    const bool kin = kx + 32 * tq < p.K;
-                    uint4 xp[MT];
-#pragma unroll
-                    for (int t = 0; t < MT; ++t) {
-                        const uint4 x = (kin && 8 * t + gid < p.M)
-                                            ? ldg_nc_v4_st(xl1 + (int64_t)(8 * t) * p.K + kx)
-                                            : make_uint4(0u, 0u, 0u, 0u);
-                        xp[t].x = __byte_perm(x.x, x.z, 0x5410);  // (x0, x4)
-                        xp[t].y = __byte_perm(x.x, x.z, 0x7632);  // (x1, x5)
-                        xp[t].z = __byte_perm(x.y, x.w, 0x5410);  // (x2, x6)
-                        xp[t].w = __byte_perm(x.y, x.w, 0x7632);  // (x3, x7)
-                    }
-                    uint32_t A[4];
-                    dq_frag<0>(wa4[j], wb4[j], sa2, oa2, sb2, ob2, cm, cg, A);
-#pragma unroll
-                    for (int t = 0; t < MT; ++t) mma_frag(acc[t], A, xp[t].x, xp[t].y);
-                    dq_frag<8>(wa4[j], wb4[j], sa2, oa2, sb2, ob2, cm, cg, A);
-#pragma unroll
-                    for (int t = 0; t < MT; ++t) mma_frag(acc[t], A, xp[t].z, xp[t].w);
-                }
+                const uint4 xv = lds128_st(bbase + 256u * h + boff[j]);
+                dq_mma<0>(acc[0], wa4[j], wb4[j], sa2, oa2, sb2, ob2, xv.x, xv.y, cm, cg, c128);
+                dq_mma<8>(acc[0], wa4[j], wb4[j], sa2, oa2, sb2, ob2, xv.z, xv.w, cm, cg, c128);
             }
         }
         if constexpr (DIAG) {  // apply the groups' scales and offsets to the slice sums (before the slot refill)
@@ -673,10 +610,7 @@ static cudaError_t launch_stream_g(const CUtensorMap& tw, const CUtensorMap& ts,
     if (rt == 2) return launch_stream_gm<G, 1, QT, 2>(tw, ts, to, a, stream);
     if (a.M <= 1) return launch_stream_gm<G, 1, QT, 1>(tw, ts, to, a, stream);
     if (a.M <= 2) return launch_stream_gm<G, 2, QT, 1>(tw, ts, to, a, stream);
-    if (a.M <= 4) return launch_stream_gm<G, 4, QT, 1>(tw, ts, to, a, stream);
-    if (a.M <= 8) return launch_stream_gm<G, 8, QT, 1>(tw, ts, to, a, stream);
-    if (a.M <= 16) return launch_stream_gm<G, 16, QT, 1>(tw, ts, to, a, stream);
-    return launch_stream_gm<G, 32, QT, 1>(tw, ts, to, a, stream);
+    return launch_stream_gm<G, 4, QT, 1>(tw, ts, to, a, stream);
 }
 
 // One token takes 32-row units (two row tiles sharing the X staging, slice sums
@@ -699,7 +633,7 @@ static cudaError_t two_row_tiles(int64_t N, int nkc, size_t ws_bytes, bool* two)
 cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
                           const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
                           void* workspace, cudaStream_t stream, const char** detail) {
-    if (M > 8)  // 9..32 tokens: the block-shared X kernel (w4_batch.cu)
+    if (M > 4)  // 5..32 tokens: the block-shared X kernel (w4_batch.cu)
         return launch_batch(plan, X, M, K, Wq, scales, offsets, N, g, Y, workspace, stream, detail);
     const int64_t ng = K / g;
     const bool qt = (g == 32) && (ng % 8 == 0);  // qparam rows 16-byte aligned: 8-group TMA boxes

@@ -69,7 +69,8 @@ typedef enum w4_kernel {
     W4_KERNEL_SKINNY = 1,          /* best memory-bound kernel for M <= 32 (stream, else cluster) */
     W4_KERNEL_GEMM = 2,            /* tcgen05 tensor-core GEMM; any M >= 1 */
     W4_KERNEL_SKINNY_CLUSTER = 3,  /* cluster split-K skinny kernel, M <= 32, no workspace */
-    W4_KERNEL_STREAM = 4           /* persistent stream-K kernel, M <= 32, needs the workspace */
+    W4_KERNEL_STREAM = 4           /* persistent stream-K kernels, M <= 32, need the workspace:
+                                      per-warp units up to 4 tokens, block-shared X from 5 */
 } w4_kernel;
 
 /*
@@ -113,8 +114,12 @@ W4_API w4_status w4_dequantize(const uint8_t *Wq, const uint16_t *scales,
  * K/group_size even; without it the call still works on the cluster split-K
  * kernel, usually slower), and what w4_linear_repacked needs (M <= 32).
  * Both need one slot of 16 x M 8-byte words per warp of their grid, at most
- * one warp per 16-row x 256-k unit and at most 4096 warps:
- * min(ceil(N/16) * ceil(K/256), 4096) * 128 * M bytes.
+ * one warp per 16-row x 256-k unit and at most 4096 warps (8192 with one
+ * token, whose warps each stream 32-row units on large problems):
+ * min(ceil(N/16) * ceil(K/256), M == 1 ? 8192 : 4096) * 128 * M bytes.
+ * With 5 to 32 tokens the stream-K work is done by 4-warp blocks that share
+ * one staged slice of X (64-row units); their grid is further capped so that
+ * each of its warps still has such a slot.
  * 0 when neither applies (M > 32).
  */
 W4_API size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int group_size);
@@ -126,7 +131,9 @@ W4_API size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int gro
  * "Pitfalls when quantizing activations": accumulation in fp32).
  *
  * Kernel choice: M <= 32 with a workspace of w4_linear_workspace_bytes runs
- * the persistent stream-K decode kernel; without one M <= 32 runs the cluster
+ * the persistent stream-K decode kernels (one 16- or 32-row unit per warp
+ * step up to 4 tokens; from 5 tokens 64-row units whose X slice a block
+ * stages once for its four warps); without one M <= 32 runs the cluster
  * split-K skinny kernel; larger M the tcgen05 tensor-core GEMM.  The kernels
  * dequantize each weight as bf16(q * s + o) with a single rounding, which can
  * differ from w4_dequantize's double rounding by one bf16 ulp; the stream
@@ -137,8 +144,8 @@ W4_API size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int gro
  * y_ref = sum_k X[m,k] W'[n,k] in fp64 (W' = w4_dequantize output):
  *   |y - y_ref| <= 4e-3 |y_ref| + 1e-2 rms(y_ref).
  * Every kernel is deterministic bit for bit on a given GPU: the stream
- * kernel adds the partial sums of a row tile split between warps in a fixed
- * order (its split depends on the GPU's SM count).
+ * kernels add the partial sums of a row tile split between warps (or
+ * blocks) in a fixed order (the split depends on the GPU's SM count).
  *
  * workspace: caller-owned device memory of `workspace_bytes` bytes (NULL with
  * 0 is allowed).  It must be zero-filled once before its first use; every

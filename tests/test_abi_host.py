@@ -63,9 +63,10 @@ def test_sizes(lib):
 
 def test_workspace_plan(lib):
     # the stream kernels (M <= 32) need one slot of 16 rows x M 8-byte words per warp of their grid:
-    # at most one warp per 16 x 256 unit and at most 4096 warps
+    # at most one warp per 16 x 256 unit and at most 4096 warps (8192 with one token)
     assert lib.w4_linear_workspace_bytes(1, 1024, 4096, 32) == 64 * 16 * 128       # 1024 units
     assert lib.w4_linear_workspace_bytes(8, 14336, 4096, 128) == 4096 * 128 * 8    # 14336 units: the cap
+    assert lib.w4_linear_workspace_bytes(1, 14336, 4096, 32) == 8192 * 128        # one token: cap 8192
     assert lib.w4_linear_workspace_bytes(8, 10 ** 6, 4096, 32) == 4 << 20          # w4_linear_static's array
     assert lib.w4_linear_workspace_bytes(9, 1024, 4096, 32) == 1024 * 128 * 9
     assert lib.w4_linear_workspace_bytes(32, 1000, 4100 - 4, 32) == 63 * 16 * 128 * 32  # ceil(1000/16) tiles
