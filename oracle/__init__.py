@@ -1,4 +1,5 @@
-"""CPU oracle for int4 weight-only quantization and the bf16 x int4 linear.
+"""CPU oracle for int4 weight-only quantization and the bf16 x int4 linear
+(and the same affine path with 2- and 8-bit codes).
 
 TEST INFRASTRUCTURE ONLY.  The test-suite, ``__graft_entry__.smoke()`` and
 the CPU-baseline / reference leg of ``bench.py`` are the only callers allowed
@@ -14,7 +15,9 @@ worked examples derived by hand (``tests/golden/``), exact-arithmetic
 invariants, brute force over the 16 codes and an independent fp64 matmul.
 Parity unpinned (a reading both sides implement, with nothing in the pages to
 check it against): the eps value of the scale clamp, the -0.0 < +0.0 order of
-the group minimum and the nibble order of the packed codes.
+the group minimum, the order of the codes inside a packed byte, and the use of
+the full 2^b - 1 levels of the affine path at 2 and 8 bits (the pages name the
+widths, not their formulas).
 """
 from __future__ import annotations
 
@@ -56,6 +59,12 @@ def _load():
             lib.w4_ref_dequantize.restype = ctypes.c_int
             lib.w4_ref_linear.argtypes = [p, i64, i64, p, p, p, i64, ctypes.c_int, p]
             lib.w4_ref_linear.restype = ctypes.c_int
+            lib.w4_ref_quantize_bits.argtypes = [p, i64, i64, ctypes.c_int, ctypes.c_int, p, p, p]
+            lib.w4_ref_quantize_bits.restype = ctypes.c_int
+            lib.w4_ref_dequantize_bits.argtypes = [p, p, p, i64, i64, ctypes.c_int, ctypes.c_int, p]
+            lib.w4_ref_dequantize_bits.restype = ctypes.c_int
+            lib.w4_ref_linear_bits.argtypes = [p, i64, i64, p, p, p, i64, ctypes.c_int, ctypes.c_int, p]
+            lib.w4_ref_linear_bits.restype = ctypes.c_int
             lib.w4_ref_eps.argtypes = []
             lib.w4_ref_eps.restype = ctypes.c_float
             _lib = lib
@@ -77,48 +86,59 @@ def ref_eps() -> float:
     return float(_load().w4_ref_eps())
 
 
-def ref_quantize(W: np.ndarray, group_size: int):
-    """W: uint16 [N,K] bf16 bits -> (Wq uint8 [N,K/2], scales uint16 [N,K/g], offsets uint16 [N,K/g])."""
+def _check_bits(bits: int) -> int:
+    if bits not in (2, 4, 8):
+        raise ValueError("bits must be 2, 4 or 8")
+    return 8 // bits  # codes per byte
+
+
+def ref_quantize(W: np.ndarray, group_size: int, bits: int = 4):
+    """W: uint16 [N,K] bf16 bits -> (Wq uint8 [N,K*bits/8], scales uint16 [N,K/g], offsets uint16 [N,K/g])."""
+    per_byte = _check_bits(bits)
     W = _u16(W)
     N, K = W.shape
     if group_size not in (32, 64, 128) or K % group_size:
         raise ValueError("unsupported shape / group size")
-    Wq = np.zeros((N, K // 2), np.uint8)
+    Wq = np.zeros((N, K // per_byte), np.uint8)
     sc = np.zeros((N, K // group_size), np.uint16)
     of = np.zeros((N, K // group_size), np.uint16)
-    rc = _load().w4_ref_quantize(_ptr(W), N, K, group_size, _ptr(Wq), _ptr(sc), _ptr(of))
+    rc = _load().w4_ref_quantize_bits(_ptr(W), N, K, group_size, bits, _ptr(Wq), _ptr(sc), _ptr(of))
     if rc:
-        raise RuntimeError(f"w4_ref_quantize failed: {rc}")
+        raise RuntimeError(f"w4_ref_quantize_bits failed: {rc}")
     return Wq, sc, of
 
 
-def ref_dequantize(Wq: np.ndarray, scales: np.ndarray, offsets: np.ndarray, group_size: int) -> np.ndarray:
+def ref_dequantize(Wq: np.ndarray, scales: np.ndarray, offsets: np.ndarray, group_size: int,
+                   bits: int = 4) -> np.ndarray:
     """Packed codes + qparams -> uint16 [N,K] bf16 bits of W'."""
+    per_byte = _check_bits(bits)
     Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
     scales, offsets = _u16(scales), _u16(offsets)
-    N, half = Wq.shape
-    K = 2 * half
+    N, row_bytes = Wq.shape
+    K = per_byte * row_bytes
     out = np.zeros((N, K), np.uint16)
-    rc = _load().w4_ref_dequantize(_ptr(Wq), _ptr(scales), _ptr(offsets), N, K, group_size, _ptr(out))
+    rc = _load().w4_ref_dequantize_bits(_ptr(Wq), _ptr(scales), _ptr(offsets), N, K, group_size, bits, _ptr(out))
     if rc:
-        raise RuntimeError(f"w4_ref_dequantize failed: {rc}")
+        raise RuntimeError(f"w4_ref_dequantize_bits failed: {rc}")
     return out
 
 
 def ref_linear(X: np.ndarray, Wq: np.ndarray, scales: np.ndarray, offsets: np.ndarray,
-               group_size: int) -> np.ndarray:
+               group_size: int, bits: int = 4) -> np.ndarray:
     """X uint16 [M,K] bf16 bits, packed weights of [N,K] -> fp64 [M,N] = X . W'^T."""
+    per_byte = _check_bits(bits)
     X = _u16(X)
     Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
     scales, offsets = _u16(scales), _u16(offsets)
     M, K = X.shape
     N = Wq.shape[0]
-    if Wq.shape[1] * 2 != K:
+    if Wq.shape[1] * per_byte != K:
         raise ValueError("X and Wq disagree on K")
     Y = np.zeros((M, N), np.float64)
-    rc = _load().w4_ref_linear(_ptr(X), M, K, _ptr(Wq), _ptr(scales), _ptr(offsets), N, group_size, _ptr(Y))
+    rc = _load().w4_ref_linear_bits(_ptr(X), M, K, _ptr(Wq), _ptr(scales), _ptr(offsets), N, group_size, bits,
+                                    _ptr(Y))
     if rc:
-        raise RuntimeError(f"w4_ref_linear failed: {rc}")
+        raise RuntimeError(f"w4_ref_linear_bits failed: {rc}")
     return Y
 
 

@@ -1,6 +1,7 @@
 /*
  * w4_oracle.c -- plain, slow CPU oracle for group-wise int4 weight-only
- * quantization and the mixed bf16 x int4 linear.
+ * quantization and the mixed bf16 x int4 linear, and for the same affine
+ * path at 2 and 8 bits.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call this code:
  * only the test-suite, the smoke check and the CPU-baseline leg of the
@@ -26,12 +27,18 @@
  *  - group sizes 32 / 64 / 128:  torchao README "Quick start"; torchao guide
  *    section 3.1; TorchAO 0.14.0 release notes "Deprecations";
  *  - the matmul result is accumulated at higher precision than its inputs:
- *    Optimum Quanto, "Pitfalls when quantizing activations".
+ *    Optimum Quanto, "Pitfalls when quantizing activations";
+ *  - weights of 2, 4 and 8 bits:  Optimum Quanto, feature list ("int2, int4,
+ *    int8 and float8 weights"); int8 weights in groups of 128:  torchao
+ *    README, the diffusers example (Int8WeightOnlyConfig, PerGroup(128)).
  * The concrete formulas (scale = (max-min)/15 with an eps clamp,
  * q = clamp(rne((w-min)/scale), 0, 15), w' = q*scale + min) are the plainest
  * reading consistent with all of the above; the readings of points the pages
  * leave open (eps value, stored-scale coding, -0 ordering, nibble order) are
- * marked "reading" below.
+ * marked "reading" below.  At b bits the same steps run with L = 2^b - 1
+ * levels in place of 15 (reading: the pages give the bit widths, not their
+ * formulas; the affine path with the full code range is the plainest one),
+ * and 8/b codes share a byte, the code of the lowest k in the lowest bits.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -90,29 +97,39 @@ static int ref_group_ok(int64_t N, int64_t K, int g)
     return 1;
 }
 
+/* Code widths of the affine path: 2, 4 or 8 bits. */
+static int ref_bits_ok(int bits)
+{
+    return bits == 2 || bits == 4 || bits == 8;
+}
+
 /* ---- quantize --------------------------------------------------------- */
 
 /*
- * W[N,K] bf16 (row-major)  ->  Wq[N,K/2] packed codes, scales[N,K/g] bf16,
- * offsets[N,K/g] bf16.  For each row n and each group j of g consecutive
- * k, in this order:
+ * W[N,K] bf16 (row-major)  ->  Wq[N,K*b/8] packed codes, scales[N,K/g] bf16,
+ * offsets[N,K/g] bf16, with L = 2^b - 1.  For each row n and each group j of
+ * g consecutive k, in this order:
  *   1. mn, mx = min and max of the group (ref_less order);
- *   2. s32 = (mx - mn) / 15, two IEEE fp32 operations;
+ *   2. s32 = (mx - mn) / L, two IEEE fp32 operations;
  *   3. s32 = eps if s32 < eps;
  *   4. s = bf16(s32): the stored scale; the codes are computed with it
  *      (reading: coding with the stored scale keeps w' self-consistent);
  *   5. o = mn, stored as bf16 (exact, mn already is a bf16 value);
- *   6. q = clamp(round_half_even((w - o) / s), 0, 15), fp32 subtract and
+ *   6. q = clamp(round_half_even((w - o) / s), 0, L), fp32 subtract and
  *      divide, then rintf() in the default round-to-nearest-even mode;
- *   7. codes k = 2p and 2p+1 share byte p of the row: even k in the low
- *      nibble (reading: the pages name packing formats but define none).
- * Returns 0, or -1 on an unsupported shape.
+ *   7. the 8/b codes k = (8/b) p .. (8/b) p + 8/b - 1 share byte p of the
+ *      row, code k at bit b (k mod 8/b): at 4 bits even k in the low nibble
+ *      (reading: the pages name packing formats but define none).
+ * Returns 0, or -1 on an unsupported shape or width.
  */
-int w4_ref_quantize(const uint16_t *W, int64_t N, int64_t K, int g,
-                    uint8_t *Wq, uint16_t *scales, uint16_t *offsets)
+int w4_ref_quantize_bits(const uint16_t *W, int64_t N, int64_t K, int g, int bits,
+                         uint8_t *Wq, uint16_t *scales, uint16_t *offsets)
 {
-    if (!ref_group_ok(N, K, g))
+    if (!ref_group_ok(N, K, g) || !ref_bits_ok(bits))
         return -1;
+    const int levels = (1 << bits) - 1;
+    const int per_byte = 8 / bits;
+    const int64_t row_bytes = K / per_byte;
     const int64_t groups = K / g;
     for (int64_t n = 0; n < N; ++n) {
         for (int64_t j = 0; j < groups; ++j) {
@@ -127,7 +144,7 @@ int w4_ref_quantize(const uint16_t *W, int64_t N, int64_t K, int g,
                     mx = v;
             }
             float range = mx - mn;
-            float s32 = range / 15.0f;
+            float s32 = range / (float)levels;
             if (s32 < REF_EPS)
                 s32 = REF_EPS;
             uint16_t s_bits = ref_float_to_bf16(s32);
@@ -144,32 +161,41 @@ int w4_ref_quantize(const uint16_t *W, int64_t N, int64_t K, int g,
                 int q = (int)r;
                 if (q < 0)
                     q = 0;
-                if (q > 15)
-                    q = 15;
+                if (q > levels)
+                    q = levels;
                 int64_t k = j * g + i;
-                uint8_t *byte = Wq + n * (K / 2) + k / 2;
-                if ((k & 1) == 0)
+                uint8_t *byte = Wq + n * row_bytes + k / per_byte;
+                int shift = (int)(k % per_byte) * bits;
+                if (shift == 0)
                     *byte = (uint8_t)q;
                 else
-                    *byte = (uint8_t)(*byte | (q << 4));
+                    *byte = (uint8_t)(*byte | (q << shift));
             }
         }
     }
     return 0;
 }
 
+/* The int4 case: two codes a byte, even k in the low nibble. */
+int w4_ref_quantize(const uint16_t *W, int64_t N, int64_t K, int g,
+                    uint8_t *Wq, uint16_t *scales, uint16_t *offsets)
+{
+    return w4_ref_quantize_bits(W, N, K, g, 4, Wq, scales, offsets);
+}
+
 /* ---- dequantize ------------------------------------------------------- */
 
-/* One weight: w' = bf16( fp32(q) * s + o ), one fp32 multiply (exact: a
- * 4-bit integer times an 8-bit significand), one fp32 add, then rounding to
- * bf16.  Optimum Quanto, "Pitfalls when quantizing activations": the result
- * of the quantized matmul is brought back to float. */
+/* One weight: w' = bf16( fp32(q) * s + o ), one fp32 multiply (exact: an
+ * integer of at most 8 bits times an 8-bit significand), one fp32 add, then
+ * rounding to bf16.  Optimum Quanto, "Pitfalls when quantizing activations":
+ * the result of the quantized matmul is brought back to float. */
 static uint16_t ref_dequant_one(const uint8_t *Wq, const uint16_t *scales,
                                 const uint16_t *offsets, int64_t K, int g,
-                                int64_t n, int64_t k)
+                                int bits, int64_t n, int64_t k)
 {
-    uint8_t byte = Wq[n * (K / 2) + k / 2];
-    int q = (k & 1) ? (byte >> 4) : (byte & 0x0F);
+    const int per_byte = 8 / bits;
+    uint8_t byte = Wq[n * (K / per_byte) + k / per_byte];
+    int q = (byte >> ((int)(k % per_byte) * bits)) & ((1 << bits) - 1);
     float s = ref_bf16_to_float(scales[n * (K / g) + k / g]);
     float o = ref_bf16_to_float(offsets[n * (K / g) + k / g]);
     float t = (float)q * s;
@@ -177,16 +203,23 @@ static uint16_t ref_dequant_one(const uint8_t *Wq, const uint16_t *scales,
     return ref_float_to_bf16(u);
 }
 
+int w4_ref_dequantize_bits(const uint8_t *Wq, const uint16_t *scales,
+                           const uint16_t *offsets, int64_t N, int64_t K, int g,
+                           int bits, uint16_t *W_out)
+{
+    if (!ref_group_ok(N, K, g) || !ref_bits_ok(bits))
+        return -1;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k)
+            W_out[n * K + k] = ref_dequant_one(Wq, scales, offsets, K, g, bits, n, k);
+    return 0;
+}
+
 int w4_ref_dequantize(const uint8_t *Wq, const uint16_t *scales,
                       const uint16_t *offsets, int64_t N, int64_t K, int g,
                       uint16_t *W_out)
 {
-    if (!ref_group_ok(N, K, g))
-        return -1;
-    for (int64_t n = 0; n < N; ++n)
-        for (int64_t k = 0; k < K; ++k)
-            W_out[n * K + k] = ref_dequant_one(Wq, scales, offsets, K, g, n, k);
-    return 0;
+    return w4_ref_dequantize_bits(Wq, scales, offsets, N, K, g, 4, W_out);
 }
 
 /* ---- linear ----------------------------------------------------------- */
@@ -196,11 +229,11 @@ int w4_ref_dequantize(const uint8_t *Wq, const uint16_t *scales,
  * weights of w4_ref_dequantize: the reference value y_ref of the tolerance
  * |y - y_ref| <= 4e-3 |y_ref| + 1e-2 rms(y_ref).  Y is fp64 [M,N].
  */
-int w4_ref_linear(const uint16_t *X, int64_t M, int64_t K, const uint8_t *Wq,
-                  const uint16_t *scales, const uint16_t *offsets, int64_t N,
-                  int g, double *Y)
+int w4_ref_linear_bits(const uint16_t *X, int64_t M, int64_t K, const uint8_t *Wq,
+                       const uint16_t *scales, const uint16_t *offsets, int64_t N,
+                       int g, int bits, double *Y)
 {
-    if (!ref_group_ok(N, K, g) || M < 0)
+    if (!ref_group_ok(N, K, g) || !ref_bits_ok(bits) || M < 0)
         return -1;
     double *wrow = (double *)malloc((size_t)K * sizeof(double));
     if (wrow == NULL)
@@ -208,7 +241,7 @@ int w4_ref_linear(const uint16_t *X, int64_t M, int64_t K, const uint8_t *Wq,
     for (int64_t n = 0; n < N; ++n) {
         for (int64_t k = 0; k < K; ++k)
             wrow[k] = (double)ref_bf16_to_float(
-                ref_dequant_one(Wq, scales, offsets, K, g, n, k));
+                ref_dequant_one(Wq, scales, offsets, K, g, bits, n, k));
         for (int64_t m = 0; m < M; ++m) {
             double acc = 0.0;
             for (int64_t k = 0; k < K; ++k)
@@ -218,6 +251,13 @@ int w4_ref_linear(const uint16_t *X, int64_t M, int64_t K, const uint8_t *Wq,
     }
     free(wrow);
     return 0;
+}
+
+int w4_ref_linear(const uint16_t *X, int64_t M, int64_t K, const uint8_t *Wq,
+                  const uint16_t *scales, const uint16_t *offsets, int64_t N,
+                  int g, double *Y)
+{
+    return w4_ref_linear_bits(X, M, K, Wq, scales, offsets, N, g, 4, Y);
 }
 
 /* The clamp constant, exported so tests can state which reading they pin. */

@@ -13,17 +13,21 @@ import numpy as np
 import pytest
 
 import oracle
-from tests.test_oracle_pins import GOLDEN_CASES, unpack_codes
+from tests.test_oracle_pins import GOLDEN_BITS_CASES, GOLDEN_CASES, unpack_codes
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "w4_oracle.c")
 
 MUTANTS = {
     "round_half_up": ("float r = rintf(t);", "float r = floorf(t + 0.5f);"),
     "truncate_codes": ("float r = rintf(t);", "float r = truncf(t);"),
-    "scale_over_16": ("float s32 = range / 15.0f;", "float s32 = range / 16.0f;"),
+    "scale_over_2_to_the_b": ("float s32 = range / (float)levels;", "float s32 = range / (float)(levels + 1);"),
     "offset_is_max": ("uint16_t o_bits = ref_float_to_bf16(mn);", "uint16_t o_bits = ref_float_to_bf16(mx);"),
     "code_with_fp32_scale": ("float t = d / s;", "float t = d / s32;"),
-    "odd_k_in_low_nibble": ("if ((k & 1) == 0)\n                    *byte", "if ((k & 1) == 1)\n                    *byte"),
+    "codes_in_reverse_byte_order": ("int shift = (int)(k % per_byte) * bits;",
+                                    "int shift = (int)(per_byte - 1 - k % per_byte) * bits;"),
+    "clamp_at_15": ("if (q > levels)\n                    q = levels;", "if (q > 15)\n                    q = 15;"),
+    "no_upper_clamp": ("if (q > levels)\n                    q = levels;", ""),
+    "dequant_reads_a_nibble": ("& ((1 << bits) - 1);", "& 0x0F;"),
     "dequant_drops_offset": ("float u = t + o;", "float u = t;"),
     "linear_output_transposed": ("Y[m * N + n] = acc;", "Y[n * M + m] = acc;"),
     "no_eps_clamp": ("if (s32 < REF_EPS)\n                s32 = REF_EPS;", ""),
@@ -47,6 +51,8 @@ def _build_mutant(tmp_path, name):
     lib.w4_ref_quantize.argtypes = [p, i64, i64, ctypes.c_int, p, p, p]
     lib.w4_ref_dequantize.argtypes = [p, p, p, i64, i64, ctypes.c_int, p]
     lib.w4_ref_linear.argtypes = [p, i64, i64, p, p, p, i64, ctypes.c_int, p]
+    lib.w4_ref_quantize_bits.argtypes = [p, i64, i64, ctypes.c_int, ctypes.c_int, p, p, p]
+    lib.w4_ref_dequantize_bits.argtypes = [p, p, p, i64, i64, ctypes.c_int, ctypes.c_int, p]
     return lib
 
 
@@ -72,6 +78,19 @@ def _pins_reject(lib) -> bool:
             lib.w4_ref_dequantize(P(Wq), P(sc), P(of), 1, g, g, P(out))
             if not np.array_equal(out[0], case["deq"]):
                 return True
+    for case in GOLDEN_BITS_CASES:
+        g, b = case["g"], case["bits"]
+        W = np.ascontiguousarray(case["values"].reshape(1, g))
+        Wq = np.zeros((1, g * b // 8), np.uint8)
+        sc = np.zeros((1, 1), np.uint16)
+        of = np.zeros((1, 1), np.uint16)
+        lib.w4_ref_quantize_bits(P(W), 1, g, g, b, P(Wq), P(sc), P(of))
+        if sc[0, 0] != case["scale"] or of[0, 0] != case["offset"] or not np.array_equal(Wq[0], case["bytes"]):
+            return True
+        out = np.zeros((1, g), np.uint16)
+        lib.w4_ref_dequantize_bits(P(Wq), P(sc), P(of), 1, g, g, b, P(out))
+        if not np.array_equal(out[0], case["deq"]):
+            return True
     # one-hot closed form of the linear: X = e_k -> Y[k, n] = W'[n, k]
     g, N, K = 32, 3, 32
     case = GOLDEN_CASES[0]
@@ -100,6 +119,8 @@ def test_unmutated_oracle_passes(tmp_path):
     lib.w4_ref_quantize.argtypes = [p, i64, i64, ctypes.c_int, p, p, p]
     lib.w4_ref_dequantize.argtypes = [p, p, p, i64, i64, ctypes.c_int, p]
     lib.w4_ref_linear.argtypes = [p, i64, i64, p, p, p, i64, ctypes.c_int, p]
+    lib.w4_ref_quantize_bits.argtypes = [p, i64, i64, ctypes.c_int, ctypes.c_int, p, p, p]
+    lib.w4_ref_dequantize_bits.argtypes = [p, p, p, i64, i64, ctypes.c_int, ctypes.c_int, p]
     assert not _pins_reject(lib)
 
 

@@ -1,6 +1,7 @@
 """Pins for the CPU oracle: checks against things other than the oracle itself.
 
-* hand-derived worked examples (tests/golden/quantize_worked_examples.txt);
+* hand-derived worked examples (tests/golden/quantize_worked_examples.txt, and
+  tests/golden/quantize_bits_worked_examples.txt for 2- and 8-bit codes);
 * exact-arithmetic invariants of the affine group projection (Optimum Quanto,
   "Design overview / Tensors"): codes in [0, 15], |w - w'| <= s/2, the group
   minimum codes to 0 and the maximum to 15, the scale is range/15 up to bf16
@@ -10,7 +11,10 @@
   "Performance");
 * smaller groups are at least as accurate (torchao guide, section 3.1 tip);
 * the fp64 linear against one-hot closed forms, a pure-Python triple loop and
-  numpy's float64 matmul.
+  numpy's float64 matmul;
+* at 2 and 8 bits (Optimum Quanto's int2 / int8 weights, torchao's int8
+  weight-only per group): the same invariants with 2^b - 1 levels, brute
+  force over all 2^b codes, and more bits never less accurate.
 """
 import os
 
@@ -22,6 +26,7 @@ import oracle
 from bit_weight_quantization_02_b300 import workloads
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "quantize_worked_examples.txt")
+GOLDEN_BITS = os.path.join(os.path.dirname(__file__), "golden", "quantize_bits_worked_examples.txt")
 
 
 def _bits(t: torch.Tensor) -> np.ndarray:
@@ -39,20 +44,22 @@ def _expand(tokens):
     return out
 
 
-def load_golden():
+def load_golden(path=GOLDEN):
     cases, cur = [], None
-    for raw in open(GOLDEN):
+    for raw in open(path):
         line = raw.strip()
         if not line or line.startswith("#"):
             continue
         key, *rest = line.split()
         if key == "case":
-            cur = {"name": rest[0]}
+            cur = {"name": rest[0], "bits": 4}
         elif key == "end":
             cases.append(cur)
             cur = None
         elif key == "g":
             cur["g"] = int(rest[0])
+        elif key == "bits":
+            cur["bits"] = int(rest[0])
         elif key in ("values", "deq"):
             cur[key] = np.array([int(v, 16) for v in _expand(rest)], np.uint16)
         elif key in ("scale", "offset"):
@@ -67,13 +74,15 @@ def load_golden():
 
 
 GOLDEN_CASES = load_golden()
+GOLDEN_BITS_CASES = load_golden(GOLDEN_BITS)
 
 
-def unpack_codes(Wq: np.ndarray) -> np.ndarray:
-    """Packed bytes [N, K/2] -> codes [N, K]; even k in the low nibble."""
-    lo = (Wq & 0x0F).astype(np.int64)
-    hi = (Wq >> 4).astype(np.int64)
-    return np.stack([lo, hi], axis=-1).reshape(Wq.shape[0], -1)
+def unpack_codes(Wq: np.ndarray, bits: int = 4) -> np.ndarray:
+    """Packed bytes [N, K*bits/8] -> codes [N, K]; the code of the lowest k in
+    the lowest bits of its byte (at 4 bits: even k in the low nibble)."""
+    per = 8 // bits
+    parts = [((Wq >> (bits * i)) & ((1 << bits) - 1)).astype(np.int64) for i in range(per)]
+    return np.stack(parts, axis=-1).reshape(Wq.shape[0], -1)
 
 
 def bits_f64(a):
@@ -117,6 +126,41 @@ def test_golden_group_embedded_in_matrix(case):
     np.testing.assert_array_equal(unpack_codes(Wq)[2, 3 * g:4 * g], case["codes"])
     if "deq" in case:
         np.testing.assert_array_equal(oracle.ref_dequantize(Wq, sc, of, g)[2, 3 * g:4 * g], case["deq"])
+
+
+def test_bits_golden_file_is_complete():
+    assert {c["bits"] for c in GOLDEN_BITS_CASES} == {2, 8}
+    assert len(GOLDEN_BITS_CASES) >= 9
+    for c in GOLDEN_BITS_CASES:
+        for key in ("values", "codes", "deq"):
+            assert len(c[key]) == c["g"], (c["name"], key)
+        assert len(c["bytes"]) == c["g"] * c["bits"] // 8, c["name"]
+
+
+@pytest.mark.parametrize("case", GOLDEN_BITS_CASES, ids=[c["name"] for c in GOLDEN_BITS_CASES])
+def test_bits_golden_single_group(case):
+    g, b = case["g"], case["bits"]
+    W = case["values"].reshape(1, g)
+    Wq, sc, of = oracle.ref_quantize(W, g, bits=b)
+    assert Wq.shape == (1, g * b // 8)
+    assert sc[0, 0] == case["scale"], f"scale {sc[0,0]:04X} != {case['scale']:04X}"
+    assert of[0, 0] == case["offset"], f"offset {of[0,0]:04X} != {case['offset']:04X}"
+    np.testing.assert_array_equal(Wq[0], case["bytes"])
+    np.testing.assert_array_equal(unpack_codes(Wq, b)[0], case["codes"])
+    np.testing.assert_array_equal(oracle.ref_dequantize(Wq, sc, of, g, bits=b)[0], case["deq"])
+
+
+@pytest.mark.parametrize("case", GOLDEN_BITS_CASES, ids=[c["name"] for c in GOLDEN_BITS_CASES])
+def test_bits_golden_group_embedded_in_matrix(case):
+    """The worked group at row 1, group 2 of a random 3 x 4g matrix."""
+    g, b = case["g"], case["bits"]
+    rng = np.random.default_rng(8)
+    W = _bits(torch.from_numpy(rng.normal(0, 0.02, (3, 4 * g)).astype(np.float32)).to(torch.bfloat16)).copy()
+    W[1, 2 * g:3 * g] = case["values"]
+    Wq, sc, of = oracle.ref_quantize(W, g, bits=b)
+    assert sc[1, 2] == case["scale"] and of[1, 2] == case["offset"]
+    np.testing.assert_array_equal(unpack_codes(Wq, b)[1, 2 * g:3 * g], case["codes"])
+    np.testing.assert_array_equal(oracle.ref_dequantize(Wq, sc, of, g, bits=b)[1, 2 * g:3 * g], case["deq"])
 
 
 def adversarial_matrix(g: int, seed: int = 3) -> np.ndarray:
@@ -253,6 +297,137 @@ def test_unsupported_shapes_rejected():
         oracle.ref_quantize(np.zeros((2, 64), np.uint16), 16)
 
 
+# ---- 2 and 8 bits ----------------------------------------------------------
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("g", [32, 128])
+@pytest.mark.parametrize("src", ["normal_outliers", "adversarial"])
+def test_bits_affine_projection_invariants(bits, g, src):
+    """With L = 2^b - 1 levels: codes in [0, L], |w - (q s + o)| <= s/2, the
+    minimum codes to 0 and is the offset, s = range/L up to bf16 rounding, and
+    the maximum codes to L whenever the eps clamp is inactive."""
+    L = (1 << bits) - 1
+    if src == "normal_outliers":
+        W = _bits(workloads.gen_weight(48, 4 * g, seed=13 + bits, outliers=True))
+    else:
+        W = adversarial_matrix(g, seed=4 + bits)
+    N, K = W.shape
+    Wq, sc, of = oracle.ref_quantize(W, g, bits=bits)
+    assert Wq.shape == (N, K * bits // 8)
+    q = unpack_codes(Wq, bits)
+    assert q.min() >= 0 and q.max() <= L
+    w = bits_f64(W).reshape(N, K // g, g)
+    s = bits_f64(sc)[..., None]
+    o = bits_f64(of)[..., None]
+    qg = q.reshape(N, K // g, g).astype(np.float64)
+    # fp32 rounding of the subtract and the divide: t carries up to ~2^-23 * L relative slack.
+    # Codes below L are the nearest level: |w - (q s + o)| <= s/2.  A code at L may be a clamped
+    # one: the stored scale can be up to 2^-8 (relative) below range/L, which leaves
+    # t <= L / (1 - 2^-8); at 2 and 4 bits that is below L + 1/2, at 8 bits up to L + 1.
+    err = np.abs(w - (qg * s + o))
+    slack = 1 + L * 2.0 ** -20
+    top = L / (1 - 2.0 ** -8) - L
+    bound = np.where(qg == L, np.maximum(0.5, top) * s * slack, s / 2 * slack)
+    assert np.all(err <= bound), float(np.max(err / s))
+    if bits < 8:
+        assert np.all(err <= s / 2 * slack)
+    np.testing.assert_array_equal(o[..., 0], w.min(axis=-1))
+    amin = w.argmin(axis=-1)
+    assert np.all(np.take_along_axis(qg, amin[..., None], -1) == 0)
+    rng_ = w.max(axis=-1) - w.min(axis=-1)
+    ideal = rng_ / L
+    unclamped = ideal > oracle.ref_eps() * (1 + 2.0 ** -8)
+    rel = np.abs(s[..., 0] - ideal) / np.where(ideal > 0, ideal, 1.0)
+    assert np.all(rel[unclamped] <= 2.0 ** -8)
+    amax = w.argmax(axis=-1)
+    qmax = np.take_along_axis(qg, amax[..., None], -1)[..., 0]
+    # the stored scale may exceed range/L by up to 2^-9 relative: the maximum codes to L,
+    # or (8 bits: L 2^-9 > 1/2 can move it) to L - 1
+    if bits < 8:
+        assert np.all(qmax[unclamped] == L)
+    else:
+        assert np.all(qmax[unclamped] >= L - 1)
+
+
+def _nearest_even_code_upto(t, L):
+    best, best_d = None, None
+    for c in range(L + 1):
+        d = abs(float(t) - c)
+        if best is None or d < best_d or (d == best_d and c % 2 == 0):
+            best, best_d = c, d
+    return best
+
+
+@pytest.mark.parametrize("bits", [2, 8])
+def test_bits_rounding_by_brute_force(bits):
+    """Every code is the nearest of the 2^b codes to the fp32 quotient, ties to even."""
+    g = 32
+    L = (1 << bits) - 1
+    W = np.concatenate([_bits(workloads.gen_weight(4, 2 * g, seed=71 + bits)), adversarial_matrix(g)[:12, :2 * g]])
+    Wq, sc, of = oracle.ref_quantize(W, g, bits=bits)
+    q = unpack_codes(Wq, bits)
+    N, K = W.shape
+    wf = (W.astype(np.uint32) << 16).view(np.float32)
+    sf = (sc.astype(np.uint32) << 16).view(np.float32)
+    of_ = (of.astype(np.uint32) << 16).view(np.float32)
+    for n in range(N):
+        for k in range(K):
+            j = k // g
+            t = np.float32(np.float32(wf[n, k]) - of_[n, j]) / sf[n, j]
+            assert q[n, k] == _nearest_even_code_upto(t, L), (n, k, float(t))
+
+
+@pytest.mark.parametrize("bits", [2, 8])
+def test_bits_dequantize_is_q_times_s_plus_o(bits):
+    g = 64
+    W = _bits(workloads.gen_weight(16, 4 * g, seed=15, outliers=True))
+    Wq, sc, of = oracle.ref_quantize(W, g, bits=bits)
+    Wd = oracle.ref_dequantize(Wq, sc, of, g, bits=bits)
+    exact = (unpack_codes(Wq, bits).astype(np.float64) * np.repeat(bits_f64(sc), g, axis=1)
+             + np.repeat(bits_f64(of), g, axis=1))
+    wd = bits_f64(Wd)
+    ulp_bf16 = np.spacing(np.abs(wd).astype(np.float32)).astype(np.float64) * 2 ** 16
+    assert np.all(np.abs(wd - exact) <= ulp_bf16 / 2 + ulp_bf16 / 2 ** 17)
+
+
+@pytest.mark.parametrize("bits", [2, 8])
+@pytest.mark.parametrize("g", [32, 64, 128])
+def test_bits_memory_ratio(bits, g):
+    """Codes take bits/16 of the bf16 weights, plus two bf16 qparams per group."""
+    W = _bits(workloads.gen_weight(8, 2 * g, seed=1))
+    Wq, sc, of = oracle.ref_quantize(W, g, bits=bits)
+    assert (Wq.nbytes + sc.nbytes + of.nbytes) / W.nbytes == pytest.approx((bits + 32 / g) / 16, abs=0)
+
+
+def test_more_bits_are_at_least_as_accurate():
+    """Mean |w - w'| falls from 2 to 4 to 8 bits on the same weights, by about
+    the factor the level counts (3, 15, 255) predict."""
+    W = _bits(workloads.gen_weight(128, 1024, seed=19, outliers=True))
+    errs = {}
+    for b in (2, 4, 8):
+        Wq, sc, of = oracle.ref_quantize(W, 128, bits=b)
+        errs[b] = float(np.mean(np.abs(bits_f64(oracle.ref_dequantize(Wq, sc, of, 128, bits=b)) - bits_f64(W))))
+    assert errs[2] > errs[4] > errs[8], errs
+    assert 3.0 < errs[2] / errs[4] < 7.0, errs
+
+
+@pytest.mark.parametrize("bits", [2, 8])
+def test_bits_smaller_groups_are_at_least_as_accurate(bits):
+    W = _bits(workloads.gen_weight(128, 1024, seed=9, outliers=True))
+    errs = []
+    for g in (32, 64, 128):
+        Wq, sc, of = oracle.ref_quantize(W, g, bits=bits)
+        errs.append(float(np.mean(np.abs(bits_f64(oracle.ref_dequantize(Wq, sc, of, g, bits=bits)) - bits_f64(W)))))
+    assert errs[0] <= errs[1] <= errs[2], errs
+
+
+def test_bits_rejected():
+    W = np.zeros((2, 64), np.uint16)
+    for b in (1, 3, 16):
+        with pytest.raises(ValueError):
+            oracle.ref_quantize(W, 32, bits=b)
+
+
 # ---- the fp64 linear -------------------------------------------------------
 
 def _packed(N, K, g, seed):
@@ -313,3 +488,18 @@ def test_tolerance_rule():
     assert ok
     ok, worst = oracle.within_linear_tolerance(y_ref + np.array([0, 0, 0.0251, 0]), y_ref)
     assert not ok and worst > 1.0
+
+
+@pytest.mark.parametrize("bits", [2, 8])
+def test_bits_linear_one_hot_and_numpy(bits):
+    """X = e_k picks column k of W' exactly; a random X matches numpy's fp64 matmul."""
+    g, N, K = 32, 10, 96
+    W = _bits(workloads.gen_weight(N, K, seed=81 + bits, outliers=True))
+    Wq, sc, of = oracle.ref_quantize(W, g, bits=bits)
+    Wd = bits_f64(oracle.ref_dequantize(Wq, sc, of, g, bits=bits))
+    X = np.zeros((K, K), np.uint16)
+    X[np.arange(K), np.arange(K)] = 0x3F80
+    np.testing.assert_array_equal(oracle.ref_linear(X, Wq, sc, of, g, bits=bits), Wd.T)
+    Xr = _bits(workloads.gen_activation(5, K, seed=82))
+    np.testing.assert_allclose(oracle.ref_linear(Xr, Wq, sc, of, g, bits=bits), bits_f64(Xr) @ Wd.T,
+                               rtol=1e-12, atol=1e-12)
