@@ -45,8 +45,13 @@ def linear_bytes(M, N, K, g):
     return N * K // 2 + 4 * N * K // g + 2 * M * K + 2 * M * N
 
 
-def quantize_bytes(N, K, g):
-    return 2 * N * K + N * K // 2 + 4 * N * K // g
+def quantize_bytes(N, K, g, bits=4):
+    return 2 * N * K + N * K * bits // 8 + 4 * N * K // g
+
+
+def linear_bytes_bits(M, N, K, g, bits):
+    """Algorithmic bytes of one linear on `bits`-bit codes."""
+    return N * K * bits // 8 + 4 * N * K // g + 2 * M * K + 2 * M * N
 
 
 def load_peaks():
@@ -433,6 +438,73 @@ def _rotated_graph_row(c, w4, wl, device, stream, dist, peaks, layout="canonical
             "tflops": round(2 * c.M * c.N * c.K / (t * 1e-3) / 1e12, 2)}
 
 
+def _code_width_rows(w4, wl, device, stream, dist, peaks, flush):
+    """2- and 8-bit codes (8 bits in groups of 128, 2 bits in groups of 32) on Llama-3-8B shapes:
+    quantize (L2 flushed), decode at M = 1 and 16 (graphs of back-to-back calls over weight copies
+    totalling > 4x L2) and prefill at M = 2048 (L2 flushed)."""
+    import torch
+    cases = []
+    for b, g in ((8, 128), (2, 32)):
+        N, K = 14336, 4096
+        W = wl.gen_weight(N, K, wl.weight_seed(7, 0, b), outliers=True, device=device)
+        with torch.cuda.stream(stream):
+            out = w4.w4_quantize_bits(W, g, b)
+            t = time_each(lambda: w4.w4_quantize_bits(W, g, b, out=out), 20, stream, flush)
+        qb = quantize_bytes(N, K, g, b)
+        cases.append({"bits": b, "g": g, "op": "quantize", "N": N, "K": K, "us": round(t * 1e3, 2),
+                      "gbs": round(qb / (t * 1e-3) / 1e9, 1), "frac_of_hbm_peak": round(qb / (t * 1e-3) / 1e9 /
+                                                                                     peaks["hbm_gbs"], 4)})
+        del W, out
+        for (N, K) in ((14336, 4096), (4096, 14336)):
+            W = wl.gen_weight(N, K, wl.weight_seed(7, 1, b), outliers=True, device=device)
+            Wq, sc, of = w4.w4_quantize_bits(W, g, b)
+            del W
+            per = N * K * b // 8 + 4 * N * K // g
+            copies = max(2, int(4 * 126e6 // per) + 1)
+            reps = [(Wq.clone(), sc.clone(), of.clone()) for _ in range(copies)]
+            for M in (1, 16):
+                X = wl.gen_activation(M, K, 8 + M, device=device)
+                Y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+                ws = w4.Workspace(device).reserve_for(M, N, K, g)
+                it = {"i": 0}
+
+                def one():
+                    r = reps[it["i"] % copies]
+                    it["i"] += 1
+                    w4.w4_linear_bits(X, *r, g, b, out=Y, workspace=ws)
+
+                with torch.cuda.stream(stream):
+                    graph = torch.cuda.CUDAGraph()
+                    one()
+                    stream.synchronize()
+                    with torch.cuda.graph(graph, stream=stream):
+                        for _ in range(copies):
+                            one()
+                    t = time_region(graph.replay, 20, 3, stream, dist, device) / (20 * copies)
+                by = linear_bytes_bits(M, N, K, g, b)
+                gbs = by / (t * 1e-3) / 1e9
+                cases.append({"bits": b, "g": g, "op": "linear", "kernel": "batch_kernel", "M": M, "N": N, "K": K,
+                              "us": round(t * 1e3, 2), "gbs": round(gbs, 1),
+                              "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4)})
+                del graph
+            del reps
+            if (N, K) == (14336, 4096):
+                M = 2048
+                X = wl.gen_activation(M, K, 9, device=device)
+                Y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+                with torch.cuda.stream(stream):
+                    for _ in range(3):
+                        w4.w4_linear_bits(X, Wq, sc, of, g, b, out=Y)
+                    t = time_each(lambda: w4.w4_linear_bits(X, Wq, sc, of, g, b, out=Y), 10, stream, flush)
+                tf = 2 * M * N * K / (t * 1e-3) / 1e12
+                cases.append({"bits": b, "g": g, "op": "linear", "kernel": "gemm_kernel", "M": M, "N": N, "K": K,
+                              "ms": round(t, 4), "tflops": round(tf, 1),
+                              "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4)})
+            del Wq, sc, of
+    return {"cases": cases, "l2": "quantize and prefill: 512 MB flush before every call; decode: graphs over weight "
+                                  "copies totalling > 4x L2"}
+
+
 def other_rows(args, w4, wl, device, stream, peaks, dist, only=None):
     """Prefill GEMMs, batched decode, the g=128 stack, quantize / dequantize."""
     import torch
@@ -490,6 +562,9 @@ def other_rows(args, w4, wl, device, stream, peaks, dist, only=None):
         b3[-1]["kernel"] = "decode_kernel"
     rows["batched_decode_g64"] = {"unit": "GB/s", "cases": b3,
                                   "l2": "graph of back-to-back calls over weight copies totalling > 4x L2"}
+
+    if want("widths"):
+        rows["other_code_widths"] = _code_width_rows(w4, wl, device, stream, dist, peaks, flush)
 
     # full 32-block stack at g=128: quantize every weight (all 6.98 B bf16 weights resident,
     # the 224 quantize calls back to back between two events), then M=1 and M=16 passes
@@ -644,7 +719,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--prefill-iters", type=int, default=10)
-    ap.add_argument("--section", choices=["all", "prefill", "shapes", "batched", "stack", "dequant"], default="all",
+    ap.add_argument("--section", choices=["all", "prefill", "shapes", "batched", "widths", "stack", "dequant"],
+                    default="all",
                     help="all = the benchmark; the others run one secondary row alone (for profiling) and print it")
     ap.add_argument("--batched-m", type=int, default=0,
                     help="with --section batched: only the cases with this many tokens (for profiling)")

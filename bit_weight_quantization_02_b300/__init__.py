@@ -71,6 +71,10 @@ def load_library():
             "w4_repacked_bytes": ([i64, i64, i32], sz),
             "w4_repack": ([p, p, p, i64, i64, i32, p, p], i32),
             "w4_linear_repacked": ([p, i64, i64, p, i64, i32, p, p, sz, p], i32),
+            "w4_packed_bytes_bits": ([i64, i64, i32], sz),
+            "w4_quantize_bits": ([p, i64, i64, i32, i32, p, p, p, p], i32),
+            "w4_dequantize_bits": ([p, p, p, i64, i64, i32, i32, p, p], i32),
+            "w4_linear_bits": ([p, i64, i64, p, p, p, i64, i32, i32, p, p, sz, p], i32),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -143,6 +147,57 @@ def w4_dequantize(Wq: torch.Tensor, scales: torch.Tensor, offsets: torch.Tensor,
     _check(lib.w4_dequantize(_ptr(Wq), _ptr(scales), _ptr(offsets), N, K, group_size, _ptr(W), _stream(Wq)),
            "w4_dequantize")
     return W
+
+
+def w4_packed_bytes_bits(N: int, K: int, bits: int) -> int:
+    return load_library().w4_packed_bytes_bits(N, K, bits)
+
+
+def w4_quantize_bits(W: torch.Tensor, group_size: int, bits: int, out=None):
+    """W bf16 [N,K] (CUDA) -> (Wq uint8 [N,K*bits/8], scales bf16 [N,K/g], offsets bf16 [N,K/g]),
+    codes of 2, 4 or 8 bits (the lowest k in the lowest bits of a byte)."""
+    lib = load_library()
+    _bits16(W, "W")
+    N, K = W.shape
+    if out is None:
+        ng = K // group_size if group_size and K % group_size == 0 else 0
+        row = K * bits // 8 if bits in (2, 4, 8) else 0
+        Wq = torch.empty((N, row), dtype=torch.uint8, device=W.device)
+        sc = torch.empty((N, ng), dtype=torch.bfloat16, device=W.device)
+        of = torch.empty((N, ng), dtype=torch.bfloat16, device=W.device)
+    else:
+        Wq, sc, of = out
+    _check(lib.w4_quantize_bits(_ptr(W), N, K, group_size, bits, _ptr(Wq), _ptr(sc), _ptr(of), _stream(W)),
+           "w4_quantize_bits")
+    return Wq, sc, of
+
+
+def w4_dequantize_bits(Wq: torch.Tensor, scales: torch.Tensor, offsets: torch.Tensor, group_size: int, bits: int,
+                       out=None):
+    """Packed `bits`-bit weights -> bf16 [N,K]."""
+    lib = load_library()
+    if bits not in (2, 4, 8):
+        raise ValueError("bits must be 2, 4 or 8")
+    N, row = Wq.shape
+    K = row * 8 // bits
+    W = out if out is not None else torch.empty((N, K), dtype=torch.bfloat16, device=Wq.device)
+    _check(lib.w4_dequantize_bits(_ptr(Wq), _ptr(scales), _ptr(offsets), N, K, group_size, bits, _ptr(W),
+                                  _stream(Wq)), "w4_dequantize_bits")
+    return W
+
+
+def w4_linear_bits(X: torch.Tensor, Wq: torch.Tensor, scales: torch.Tensor, offsets: torch.Tensor,
+                   group_size: int, bits: int, out=None, workspace=None):
+    """Y bf16 [M,N] = X . dequant(Wq)^T for `bits`-bit codes (see include/w4.h)."""
+    lib = load_library()
+    _bits16(X, "X")
+    M, K = X.shape
+    N = Wq.shape[0]
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    ws = _workspace_for(X, M, N, K, group_size, workspace)
+    _check(lib.w4_linear_bits(_ptr(X), M, K, _ptr(Wq), _ptr(scales), _ptr(offsets), N, group_size, bits, _ptr(Y),
+                              _ptr(ws.buf), ws.nbytes, _stream(X)), "w4_linear_bits")
+    return Y
 
 
 def w4_linear_workspace_bytes(M: int, N: int, K: int, group_size: int) -> int:

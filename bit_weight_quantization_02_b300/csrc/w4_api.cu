@@ -62,7 +62,7 @@ w4_status w4_quantize(const uint16_t* W, int64_t N, int64_t K, int group_size, u
     W4_TRY(check_ptr(Wq, "Wq"));
     W4_TRY(check_ptr(scales, "scales"));
     W4_TRY(check_ptr(offsets, "offsets"));
-    cudaError_t e = w4::launch_quantize(W, N, K, group_size, Wq, scales, offsets, (cudaStream_t)stream);
+    cudaError_t e = w4::launch_quantize(W, N, K, group_size, 4, Wq, scales, offsets, (cudaStream_t)stream);
     return e == cudaSuccess ? W4_OK : cuda_fail(e, "quantize launch");
 }
 
@@ -74,7 +74,7 @@ w4_status w4_dequantize(const uint8_t* Wq, const uint16_t* scales, const uint16_
     W4_TRY(check_ptr(scales, "scales"));
     W4_TRY(check_ptr(offsets, "offsets"));
     W4_TRY(check_ptr(W_out, "W_out"));
-    cudaError_t e = w4::launch_dequantize(Wq, scales, offsets, N, K, group_size, W_out, (cudaStream_t)stream);
+    cudaError_t e = w4::launch_dequantize(Wq, scales, offsets, N, K, group_size, 4, W_out, (cudaStream_t)stream);
     return e == cudaSuccess ? W4_OK : cuda_fail(e, "dequantize launch");
 }
 
@@ -136,7 +136,7 @@ w4_status w4_linear_ex(const uint16_t* X, int64_t M, int64_t K, const uint8_t* W
         }
         if (kernel != W4_KERNEL_AUTO) return fail(W4_ERR_INVALID_ARG, "no skinny launch plan for this shape");
     }
-    e = w4::launch_gemm(X, M, K, Wq, scales, offsets, N, group_size, Y, (cudaStream_t)stream, &detail);
+    e = w4::launch_gemm(X, M, K, Wq, scales, offsets, N, group_size, 4, Y, (cudaStream_t)stream, &detail);
     if (e != cudaSuccess) return fail(W4_ERR_CUDA, "tensor-core linear: %s %s", cudaGetErrorString(e), detail);
     return W4_OK;
 }
@@ -226,6 +226,79 @@ w4_status w4_linear_repacked(const uint16_t* X, int64_t M, int64_t K, const uint
         return fail(W4_ERR_INVALID_ARG, "w4_linear_repacked needs %zu workspace bytes", dp.ws_bytes);
     cudaError_t e = w4::launch_decode(dp, X, M, K, packed, N, group_size, Y, workspace, (cudaStream_t)stream);
     return e == cudaSuccess ? W4_OK : cuda_fail(e, "repacked linear launch");
+}
+
+size_t w4_packed_bytes_bits(int64_t N, int64_t K, int bits) {
+    if (bits != 2 && bits != 4 && bits != 8) return 0;
+    if (N < 0 || K <= 0 || K % (8 / bits) != 0 || (N > 0 && K > (int64_t(1) << 62) / N)) return 0;
+    return (size_t)(N * (K * bits / 8));
+}
+
+namespace {
+w4_status check_bits(int bits) {
+    if (bits != 2 && bits != 4 && bits != 8) return fail(W4_ERR_UNSUPPORTED, "bits %d not in {2, 4, 8}", bits);
+    return W4_OK;
+}
+}  // namespace
+
+w4_status w4_quantize_bits(const uint16_t* W, int64_t N, int64_t K, int group_size, int bits, uint8_t* Wq,
+                           uint16_t* scales, uint16_t* offsets, void* stream) {
+    W4_TRY(check_bits(bits));
+    W4_TRY(check_shape(N, K, group_size));
+    if (N == 0) return W4_OK;
+    W4_TRY(check_ptr(W, "W"));
+    W4_TRY(check_ptr(Wq, "Wq"));
+    W4_TRY(check_ptr(scales, "scales"));
+    W4_TRY(check_ptr(offsets, "offsets"));
+    cudaError_t e = w4::launch_quantize(W, N, K, group_size, bits, Wq, scales, offsets, (cudaStream_t)stream);
+    return e == cudaSuccess ? W4_OK : cuda_fail(e, "quantize launch");
+}
+
+w4_status w4_dequantize_bits(const uint8_t* Wq, const uint16_t* scales, const uint16_t* offsets, int64_t N, int64_t K,
+                             int group_size, int bits, uint16_t* W_out, void* stream) {
+    W4_TRY(check_bits(bits));
+    W4_TRY(check_shape(N, K, group_size));
+    if (N == 0) return W4_OK;
+    W4_TRY(check_ptr(Wq, "Wq"));
+    W4_TRY(check_ptr(scales, "scales"));
+    W4_TRY(check_ptr(offsets, "offsets"));
+    W4_TRY(check_ptr(W_out, "W_out"));
+    cudaError_t e = w4::launch_dequantize(Wq, scales, offsets, N, K, group_size, bits, W_out, (cudaStream_t)stream);
+    return e == cudaSuccess ? W4_OK : cuda_fail(e, "dequantize launch");
+}
+
+w4_status w4_linear_bits(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
+                         const uint16_t* offsets, int64_t N, int group_size, int bits, uint16_t* Y, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+    W4_TRY(check_bits(bits));
+    if (bits == 4)
+        return w4_linear(X, M, K, Wq, scales, offsets, N, group_size, Y, workspace, workspace_bytes, stream);
+    W4_TRY(check_shape(N, K, group_size));
+    if (M < 0) return fail(W4_ERR_INVALID_ARG, "M = %lld must not be negative", (long long)M);
+    if (M > 0x7FFFFFFFLL) return fail(W4_ERR_INVALID_ARG, "M must be below 2^31");
+    if (bits == 2 && K % 64 != 0)
+        return fail(W4_ERR_UNSUPPORTED, "2-bit codes need K %% 64 == 0 (16-byte code rows), got K = %lld",
+                    (long long)K);
+    if (M == 0 || N == 0) return W4_OK;
+    W4_TRY(check_ptr(X, "X"));
+    W4_TRY(check_ptr(Wq, "Wq"));
+    W4_TRY(check_ptr(scales, "scales"));
+    W4_TRY(check_ptr(offsets, "offsets"));
+    W4_TRY(check_ptr(Y, "Y"));
+    if (workspace == nullptr) workspace_bytes = 0;
+    if (workspace_bytes > 0 && !aligned16(workspace)) return fail(W4_ERR_MISALIGNED, "workspace is not 16-byte aligned");
+    const char* detail = "";
+    cudaError_t e;
+    w4::StreamPlan sp;
+    if (M <= w4::STREAM_MAX_M && w4::plan_stream(M, N, K, group_size, &sp) && workspace_bytes >= sp.ws_bytes) {
+        e = w4::launch_batch(sp, X, M, K, Wq, scales, offsets, N, group_size, bits, Y, workspace, (cudaStream_t)stream,
+                             &detail);
+        if (e != cudaSuccess) return fail(W4_ERR_CUDA, "batched linear: %s %s", cudaGetErrorString(e), detail);
+        return W4_OK;
+    }
+    e = w4::launch_gemm(X, M, K, Wq, scales, offsets, N, group_size, bits, Y, (cudaStream_t)stream, &detail);
+    if (e != cudaSuccess) return fail(W4_ERR_CUDA, "tensor-core linear: %s %s", cudaGetErrorString(e), detail);
+    return W4_OK;
 }
 
 int w4_format_version(void) { return W4_FORMAT_VERSION; }

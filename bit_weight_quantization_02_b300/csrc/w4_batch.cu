@@ -1,5 +1,6 @@
 // w4_batch.cu -- persistent stream-K bf16 x int4 linear for batched decode
-// (5 <= M <= 32 tokens) on the canonical layout.
+// (5 <= M <= 32 tokens) on the canonical layout; also the decode linear
+// (1 <= M <= 32) of 2- and 8-bit codes.
 //
 // Y[m,n] = sum_k X[m,k] * w'[n,k], w' = bf16(q*s + o), fp32 accumulation
 // (Optimum Quanto: bf16 x int4 matmul, result accumulated at higher precision,
@@ -22,6 +23,15 @@
 //    by side, then LOP3 magic (128 + q), an exact subtract and one bf16 FMA
 //    with the group's scale and offset, and one mma.m16n8k16 per group of 8
 //    tokens uses that fragment.
+//  * 2- and 8-bit codes (Optimum Quanto's int2 / int8 weights) use the same
+//    unit with 4 KB / 16 KB of codes (one 64-byte-swizzled box / two
+//    128-byte-swizzled boxes).  2 bits: each lane extracts the nibble holding
+//    its pair and spreads its two codes into the two bf16 halves (one
+//    multiply by 0x4001), then the LOP3 magic, subtract and FMA as above.
+//    8 bits: a bf16 of 128 + q cannot hold q up to 255, so each code goes
+//    through fp32 (prmt into 2^23 + q, exact subtract, FMA with s and o,
+//    round to bf16): w' is then bf16(fp32(q s + o)), the dequantized weight
+//    bit for bit.
 //  * The (row group, k) units are cut into equal contiguous block ranges; a
 //    row group split between blocks is finished by the block holding its
 //    first unit: each of its warps adds the partial sums that warp w of every
@@ -54,10 +64,11 @@ struct BatchArgs {
 };
 
 // Shared-memory layout of one ring stage (every piece 1024-byte aligned for the swizzled boxes).
-template <int G, int MT>
+template <int G, int MT, int B>
 struct BatchLayout {
     static constexpr int MP = 8 * MT;                       // token rows staged (M padded)
-    static constexpr int CODES = BT_ROWS * 128;             // 64 rows x 256 k of codes
+    static constexpr int CROW = BT_UK * B / 8;              // bytes of one row of a unit's codes
+    static constexpr int CODES = BT_ROWS * CROW;            // 64 rows x 256 k of codes
     static constexpr int XBOX = MP * 128;                   // one 64-k box of X
     static constexpr int XBYTES = 4 * XBOX;
     static constexpr int QROW = (BT_UK / G) * 2;            // bytes of one row of one qparam array
@@ -120,11 +131,50 @@ __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int G, int MT, bool QT>
+// 2-bit codes: the pair (k, k+1) at bits `sh` .. `sh` + 3 of w as a bf16 pair
+// w' = bf16(q*s + o): the nibble times 0x4001 puts its low code at bit 0 and
+// its high code at bit 16, LOP3 masks them into 128 + q, exact subtract, FMA.
+__device__ __forceinline__ uint32_t pair2(uint32_t w, uint32_t sh, uint32_t s2, uint32_t o2, uint32_t cg) {
+    uint32_t r;
+    asm("{\n\t.reg .b32 t;\n\t"
+        "bfe.u32 t, %1, %2, 4;\n\t"
+        "mul.lo.u32 t, t, 0x4001;\n\t"
+        "lop3.b32 t, t, 0x00030003, %5, 0xEA;\n\t"
+        "sub.rn.bf16x2 t, t, %5;\n\t"
+        "fma.rn.bf16x2 %0, t, %3, %4;\n\t}"
+        : "=r"(r)
+        : "r"(w), "r"(sh), "r"(s2), "r"(o2), "r"(cg));
+    return r;
+}
+// 8-bit codes: bytes sel0 and sel0 + 1 of w (k, k+1) as a bf16 pair
+// bf16(fp32(q*s + o)): prmt builds 2^23 + q, an exact subtract gives q, one
+// fp32 FMA (q*s is exact), one rounding to bf16.
+__device__ __forceinline__ uint32_t pair8(uint32_t w, uint32_t sel0, float s, float o, uint32_t mg) {
+    uint32_t lo, hi, r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(w), "r"(mg), "r"(sel0));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(w), "r"(mg), "r"(sel0 + 1u));
+    const float a = __fmaf_rn(__fsub_rn(__uint_as_float(lo), 8388608.0f), s, o);
+    const float b = __fmaf_rn(__fsub_rn(__uint_as_float(hi), 8388608.0f), s, o);
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    return r;
+}
+__device__ __forceinline__ uint2 lds64_b(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds32_b(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+template <int G, int MT, bool QT, int B>
 __global__ void __launch_bounds__(BT_THREADS, MT == 1 ? 4 : 3)
 batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
              const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_o, const BatchArgs p) {
-    using L = BatchLayout<G, MT>;
+    static_assert(B == 2 || B == 4 || B == 8, "code width");
+    using L = BatchLayout<G, MT, B>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     constexpr int PPR = L::QROW / 4;               // 4-byte qparam pieces per row and array
@@ -173,7 +223,12 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
         const int row0 = grp * BT_ROWS, k = kc * BT_UK;
         const uint32_t st = sbase + d * L::STAGE, bar = bars + 8 * d;
         if (threadIdx.x == 0) {
-            tma_load_2d(st, &tm_w, bar, k / 2, row0);
+            if (B == 8) {  // two boxes of 128 k
+                tma_load_2d(st, &tm_w, bar, k, row0);
+                tma_load_2d(st + L::CODES / 2, &tm_w, bar, k + 128, row0);
+            } else {
+                tma_load_2d(st, &tm_w, bar, k * B / 8, row0);
+            }
             if (QT) {
                 tma_load_2d(st + L::CODES + L::XBYTES, &tm_s, bar, k / G, row0);
                 tma_load_2d(st + L::CODES + L::XBYTES + BT_ROWS * L::QROW, &tm_o, bar, k / G, row0);
@@ -220,6 +275,11 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
     asm volatile("mov.b32 %0, %1;" : "=r"(cm) : "r"(0x000F000Fu));
     asm volatile("mov.b32 %0, %1;" : "=r"(cg) : "r"(0x43004300u));
     const uint32_t sel = (uint32_t)tq | ((uint32_t)(4 + tq) << 8);  // prmt: byte tq of w, byte tq of w >> 4
+    const uint32_t sh2 = 4u * (uint32_t)tq;                          // 2 bits: nibble of the pair (2tq, 2tq+1)
+    const uint32_t w8 = 4u * (uint32_t)(tq >> 1);                    // 8 bits: word of bytes 2tq, 2tq+1 in a chunk
+    const uint32_t sel8 = 0x7540u | (2u * (uint32_t)(tq & 1));       // prmt: that byte, then 0x00, 0x00, 0x4B
+    uint32_t mg;                                                     // 2^23 as fp32 bits
+    asm volatile("mov.b32 %0, %1;" : "=r"(mg) : "r"(0x4B000000u));
     // ldmatrix row addresses of this lane: matrix i = lane / 8 (token group 2tp + i / 2, chunk c0 + i % 2),
     // row r = lane % 8 (token 8 (2tp + i / 2) + r); the 128-byte swizzle XORs the chunk with r
     const int lr = lane & 7, li = lane >> 3;
@@ -237,26 +297,58 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
     for (int it = 0; it < nunits; ++it) {
         ok = mbar_wait_bounded(bars + 8 * d, phase, nullptr, &g_batch_fault, 1u, BT_WAIT_LIMIT_NS) && ok;
         const uint32_t st = sbase + d * L::STAGE;
-        const uint32_t crow = st + (16 * warp + gid) * 128;            // code row gid of this warp's tile
+        // code row gid of this warp's tile (8 bits: in the first of the two 128-k boxes)
+        const uint32_t crow = st + (16 * warp + gid) * (uint32_t)(B == 8 ? 128 : L::CROW);
         const uint32_t qa = st + L::CODES + L::XBYTES + (16 * warp + gid) * L::QROW;
         const uint32_t xst = st + L::CODES;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {  // 16-byte code pieces: 32 k, two 16-k steps
-            const uint4 wa = lds128_b(crow + ((uint32_t)(q ^ gid) << 4));
-            const uint4 wb = lds128_b(crow + 8 * 128 + ((uint32_t)(q ^ gid) << 4));
+        for (int q = 0; q < 8; ++q) {  // 32 k of codes per row, two 16-k steps
             const uint32_t jq = (uint32_t)(((32 * q) / G) * 2);  // the piece's group, bytes into the row
-            const uint32_t sa2 = __byte_perm(lds16_b(qa + jq), 0, 0x1010);
-            const uint32_t oa2 = __byte_perm(lds16_b(qa + BT_ROWS * L::QROW + jq), 0, 0x1010);
-            const uint32_t sb2 = __byte_perm(lds16_b(qa + 8 * L::QROW + jq), 0, 0x1010);
-            const uint32_t ob2 = __byte_perm(lds16_b(qa + 8 * L::QROW + BT_ROWS * L::QROW + jq), 0, 0x1010);
-            const uint32_t wa4[4] = {wa.x, wa.y, wa.z, wa.w};
-            const uint32_t wb4[4] = {wb.x, wb.y, wb.z, wb.w};
+            uint32_t sa2, oa2, sb2, ob2;  // (s,s), (o,o) bf16 pairs of rows gid and gid + 8 (2 and 4 bits)
+            float saf, oaf, sbf, obf;     // the same as fp32 (8 bits)
+            {
+                const uint32_t sa = lds16_b(qa + jq), oa = lds16_b(qa + BT_ROWS * L::QROW + jq);
+                const uint32_t sb = lds16_b(qa + 8 * L::QROW + jq), ob = lds16_b(qa + 8 * L::QROW + BT_ROWS * L::QROW + jq);
+                sa2 = __byte_perm(sa, 0, 0x1010), oa2 = __byte_perm(oa, 0, 0x1010);
+                sb2 = __byte_perm(sb, 0, 0x1010), ob2 = __byte_perm(ob, 0, 0x1010);
+                saf = __uint_as_float(sa << 16), oaf = __uint_as_float(oa << 16);
+                sbf = __uint_as_float(sb << 16), obf = __uint_as_float(ob << 16);
+            }
+            uint32_t wa4[4], wb4[4];  // 4 bits: the row's 32 k as four words (8 k each)
+            uint32_t wa2[2], wb2[2];  // 2 bits: two words (16 k each)
+            if constexpr (B == 4) {
+                const uint4 wa = lds128_b(crow + ((uint32_t)(q ^ gid) << 4));
+                const uint4 wb = lds128_b(crow + 8 * 128 + ((uint32_t)(q ^ gid) << 4));
+                wa4[0] = wa.x, wa4[1] = wa.y, wa4[2] = wa.z, wa4[3] = wa.w;
+                wb4[0] = wb.x, wb4[1] = wb.y, wb4[2] = wb.z, wb4[3] = wb.w;
+            } else if constexpr (B == 2) {  // 64-byte rows, 64-byte swizzle: chunk c at c ^ ((row >> 1) & 3)
+                const uint32_t off = ((uint32_t)((q >> 1) ^ ((gid >> 1) & 3)) << 4) + 8u * (uint32_t)(q & 1);
+                const uint2 wa = lds64_b(crow + off), wb = lds64_b(crow + 8 * L::CROW + off);
+                wa2[0] = wa.x, wa2[1] = wa.y, wb2[0] = wb.x, wb2[1] = wb.y;
+            }
 #pragma unroll
             for (int s2 = 0; s2 < 2; ++s2) {  // 16-k step: chunks c0 = 4q + 2 s2 (k 0..7) and c0 + 1 (k 8..15)
-                const uint32_t a0 = nat_pair(wa4[2 * s2], sel, sa2, oa2, cm, cg);
-                const uint32_t a1 = nat_pair(wb4[2 * s2], sel, sb2, ob2, cm, cg);
-                const uint32_t a2 = nat_pair(wa4[2 * s2 + 1], sel, sa2, oa2, cm, cg);
-                const uint32_t a3 = nat_pair(wb4[2 * s2 + 1], sel, sb2, ob2, cm, cg);
+                uint32_t a0, a1, a2, a3;
+                if constexpr (B == 4) {
+                    a0 = nat_pair(wa4[2 * s2], sel, sa2, oa2, cm, cg);
+                    a1 = nat_pair(wb4[2 * s2], sel, sb2, ob2, cm, cg);
+                    a2 = nat_pair(wa4[2 * s2 + 1], sel, sa2, oa2, cm, cg);
+                    a3 = nat_pair(wb4[2 * s2 + 1], sel, sb2, ob2, cm, cg);
+                } else if constexpr (B == 2) {  // k 2tq, 2tq+1 at bits 4tq; k + 8 at bits 16 + 4tq
+                    a0 = pair2(wa2[s2], sh2, sa2, oa2, cg);
+                    a1 = pair2(wb2[s2], sh2, sb2, ob2, cg);
+                    a2 = pair2(wa2[s2], sh2 + 16u, sa2, oa2, cg);
+                    a3 = pair2(wb2[s2], sh2 + 16u, sb2, ob2, cg);
+                } else {  // 128-byte rows in two boxes of 128 k, 128-byte swizzle: chunk c at c ^ (row & 7)
+                    const int c = 2 * (q & 3) + s2;
+                    const uint32_t base = crow + (uint32_t)(q >> 2) * (L::CODES / 2) + ((uint32_t)(c ^ gid) << 4) + w8;
+                    const uint32_t xa = lds32_b(base), xa8 = lds32_b(base + 8);
+                    const uint32_t xb = lds32_b(base + 8 * 128), xb8 = lds32_b(base + 8 * 128 + 8);
+                    a0 = pair8(xa, sel8, saf, oaf, mg);
+                    a1 = pair8(xb, sel8, sbf, obf, mg);
+                    a2 = pair8(xa8, sel8, saf, oaf, mg);
+                    a3 = pair8(xb8, sel8, sbf, obf, mg);
+                }
                 const int cg8 = 4 * q + 2 * s2 + (li & 1);  // this lane's ldmatrix chunk (8 k) in the unit
                 const uint32_t xrow = xst + (uint32_t)(cg8 >> 3) * L::XBOX +
                                       ((uint32_t)((cg8 & 7) ^ lr) << 4) + (uint32_t)lr * 128;
@@ -334,11 +426,11 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
 
 // ------------------------------------------------------------------ host side
 
-template <int G, int MT, bool QT>
+template <int G, int MT, bool QT, int B>
 static cudaError_t launch_batch_gm(const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap& ts,
                                    const CUtensorMap& to, BatchArgs a, size_t ws_bytes, cudaStream_t stream) {
-    using L = BatchLayout<G, MT>;
-    auto kern = batch_kernel<G, MT, QT>;
+    using L = BatchLayout<G, MT, B>;
+    auto kern = batch_kernel<G, MT, QT, B>;
     cudaError_t e = ensure_kernel_attrs(reinterpret_cast<const void*>(kern), L::SMEM, false);
     if (e != cudaSuccess) return e;
     int sms = 0, per_sm = 0;
@@ -362,24 +454,28 @@ static cudaError_t launch_batch_gm(const CUtensorMap& tw, const CUtensorMap& tx,
     return cudaLaunchKernelEx(&cfg, kern, tw, tx, ts, to, a);
 }
 
-template <int G, bool QT>
+template <int G, bool QT, int B>
 static cudaError_t launch_batch_g(const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap& ts,
                                   const CUtensorMap& to, BatchArgs a, size_t ws_bytes, cudaStream_t stream) {
-    if (a.M <= 8) return launch_batch_gm<G, 1, QT>(tw, tx, ts, to, a, ws_bytes, stream);
-    if (a.M <= 16) return launch_batch_gm<G, 2, QT>(tw, tx, ts, to, a, ws_bytes, stream);
-    return launch_batch_gm<G, 4, QT>(tw, tx, ts, to, a, ws_bytes, stream);
+    if (a.M <= 8) return launch_batch_gm<G, 1, QT, B>(tw, tx, ts, to, a, ws_bytes, stream);
+    if (a.M <= 16) return launch_batch_gm<G, 2, QT, B>(tw, tx, ts, to, a, ws_bytes, stream);
+    return launch_batch_gm<G, 4, QT, B>(tw, tx, ts, to, a, ws_bytes, stream);
 }
 
 cudaError_t launch_batch(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
-                         const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
+                         const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, int bits, uint16_t* Y,
                          void* workspace, cudaStream_t stream, const char** detail) {
     const int64_t ng = K / g;
-    const bool qt = (g == 32) && (ng % 8 == 0);  // qparam rows 16-byte aligned: 8-group TMA boxes
+    // qparam rows 16-byte aligned: 8-group TMA boxes (4-bit codes only; the other widths use cp.async)
+    const bool qt = bits == 4 && (g == 32) && (ng % 8 == 0);
     const int mp = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
     CUtensorMap tw, tx, ts, to;
-    // codes: [N][K/2] bytes, box 64 rows x 128 bytes; X: [M][K] bf16, box mp rows x 64 k (rows past M read 0)
-    cudaError_t e = encode_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)(K / 2), (uint64_t)N,
-                                         (uint64_t)(K / 2), 128, BT_ROWS, CU_TENSOR_MAP_SWIZZLE_128B, detail);
+    // codes: [N][K bits/8] bytes, box 64 rows x 128 bytes (2 bits: 64 bytes, 64-byte swizzle);
+    // X: [M][K] bf16, box mp rows x 64 k (rows past M read 0)
+    const uint64_t row_bytes = (uint64_t)(K * bits / 8);
+    cudaError_t e = encode_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, row_bytes, (uint64_t)N, row_bytes,
+                                         bits == 2 ? 64 : 128, BT_ROWS,
+                                         bits == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, detail);
     if (e == cudaSuccess)
         e = encode_tensor_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT16, X, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2,
                                  64, (uint32_t)mp, CU_TENSOR_MAP_SWIZZLE_128B, detail);
@@ -405,12 +501,27 @@ cudaError_t launch_batch(const StreamPlan& plan, const uint16_t* X, int64_t M, i
     a.nkc = plan.nkc;
     a.units = (N + BT_ROWS - 1) / BT_ROWS * (long long)plan.nkc;
     a.ctas = 0;
+    const size_t ws = plan.ws_bytes;
+    if (bits == 2) {
+        switch (g) {
+            case 32: return launch_batch_g<32, false, 2>(tw, tx, ts, to, a, ws, stream);
+            case 64: return launch_batch_g<64, false, 2>(tw, tx, ts, to, a, ws, stream);
+            default: return launch_batch_g<128, false, 2>(tw, tx, ts, to, a, ws, stream);
+        }
+    }
+    if (bits == 8) {
+        switch (g) {
+            case 32: return launch_batch_g<32, false, 8>(tw, tx, ts, to, a, ws, stream);
+            case 64: return launch_batch_g<64, false, 8>(tw, tx, ts, to, a, ws, stream);
+            default: return launch_batch_g<128, false, 8>(tw, tx, ts, to, a, ws, stream);
+        }
+    }
     switch (g) {
         case 32:
-            return qt ? launch_batch_g<32, true>(tw, tx, ts, to, a, plan.ws_bytes, stream)
-                      : launch_batch_g<32, false>(tw, tx, ts, to, a, plan.ws_bytes, stream);
-        case 64: return launch_batch_g<64, false>(tw, tx, ts, to, a, plan.ws_bytes, stream);
-        default: return launch_batch_g<128, false>(tw, tx, ts, to, a, plan.ws_bytes, stream);
+            return qt ? launch_batch_g<32, true, 4>(tw, tx, ts, to, a, ws, stream)
+                      : launch_batch_g<32, false, 4>(tw, tx, ts, to, a, ws, stream);
+        case 64: return launch_batch_g<64, false, 4>(tw, tx, ts, to, a, ws, stream);
+        default: return launch_batch_g<128, false, 4>(tw, tx, ts, to, a, ws, stream);
     }
 }
 

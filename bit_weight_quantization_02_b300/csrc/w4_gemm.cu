@@ -27,6 +27,13 @@
 //               them with one tcgen05.st; afterwards the same warps run the
 //               epilogue (tcgen05.ld -> bf16 -> shared-memory transpose ->
 //               64-byte runs of Y rows).
+// 2- and 8-bit codes (Optimum Quanto's int2 / int8 weights) run the same
+// pipeline with a code tile of 128 rows x 16 / 64 bytes per k block (no
+// swizzle / 64-byte swizzle).  2 bits: the pairs (q_i, q_i+8) of a 16-code
+// word come out of LOP3 magic like the 4-bit nibble pairs, PRMTs restore k
+// order.  8 bits: 128 + q does not fit a bf16, so each code goes through fp32
+// (prmt into 2^23 + q, exact subtract, FMA with s and o) and the pairs are
+// rounded to bf16 together: w' = bf16(fp32(q s + o)) exactly.
 // Every mbarrier wait is bounded in time; a block that gives up sets the
 // device fault word, waits (bounded) for its own copies and MMAs, frees its
 // tensor memory and exits.
@@ -50,19 +57,23 @@ constexpr int GM_ACOL = GM_BT;             // first TMEM column of the A stages
 constexpr int GM_ASTAGE_COLS = GM_BK / 2;  // 64 bf16 of a row = 32 columns
 
 constexpr int GM_X_BYTES = GM_BT * GM_BK * 2;  // 32 KB
-constexpr int GM_P_BYTES = GM_BW * GM_BK / 2;  //  4 KB
 constexpr int GM_QBOX_BYTES = GM_BW * 16;      //  2 KB: 8 bf16 per row
 constexpr int GM_OFF_X = 0;
 constexpr int GM_OFF_P = GM_OFF_X + GM_TSTAGES * GM_X_BYTES;
-constexpr int GM_OFF_Q = GM_OFF_P + GM_TSTAGES * GM_P_BYTES;  // per stage: scales box, offsets box
-constexpr int GM_OFF_BAR = GM_OFF_Q + GM_QSTAGES * 2 * GM_QBOX_BYTES;
 // full_tma, empty_tma per TMA stage; full_deq, empty_w per A stage;
 // full_q, empty_q per qparam stage; tmem_full; drain
 constexpr int GM_NBAR = 2 * GM_TSTAGES + 2 * GM_WSTAGES + 2 * GM_QSTAGES + 2;
-constexpr int GM_OFF_MISC = GM_OFF_BAR + GM_NBAR * 8;
-constexpr int GM_SMEM_USED = GM_OFF_MISC + 16;
-constexpr int GM_SMEM_BYTES = GM_SMEM_USED + 1024;  // + alignment slack for the 1024-byte swizzle atoms
-static_assert(GM_SMEM_BYTES <= 227 * 1024, "shared memory budget");
+// Shared-memory layout after the X ring, for B-bit codes.
+template <int B>
+struct GmLayout {
+    static constexpr int PROW = GM_BK * B / 8;                     // code bytes of one row per k block
+    static constexpr int P_BYTES = GM_BW * PROW;                   // 2 / 4 / 8 KB
+    static constexpr int OFF_Q = GM_OFF_P + GM_TSTAGES * P_BYTES;  // per stage: scales box, offsets box
+    static constexpr int OFF_BAR = OFF_Q + GM_QSTAGES * 2 * GM_QBOX_BYTES;
+    static constexpr int OFF_MISC = OFF_BAR + GM_NBAR * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;        // + alignment slack for the swizzle atoms
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
 constexpr int GM_STAGE_PITCH = 80;                   // epilogue transpose: 32 rows of bf16 + 16 bytes
 constexpr int GM_STAGE_BYTES = 32 * GM_STAGE_PITCH;  // one warp's 32 tokens x 32 rows
 static_assert(GM_DEQ_WARPS * GM_STAGE_BYTES <= GM_TSTAGES * GM_X_BYTES, "epilogue staging reuses the X ring");
@@ -141,6 +152,48 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, uint32_t s2, uint32_t o2, 
         : "r"(w), "r"(s2), "r"(o2), "r"(cm), "r"(cg));
     return r;
 }
+// Sixteen 2-bit codes of one word (k0..k15, k0 in the low bits) -> sixteen bf16
+// w' = q*s + o in k order (two uint4): LOP3 on w >> 2i gives the pair
+// (128 + q_i, 128 + q_i+8), exact subtract, one bf16 FMA, PRMTs restore k order.
+__device__ __forceinline__ void dequant16_2b(uint32_t w, uint32_t s2, uint32_t o2, uint32_t cg, uint4& lo, uint4& hi) {
+    uint32_t p[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t t;
+        asm("{\n\t.reg .b32 u;\n\t"
+            "shr.b32 u, %1, %4;\n\t"
+            "lop3.b32 u, u, 0x00030003, %2, 0xEA;\n\t"
+            "sub.rn.bf16x2 u, u, %2;\n\t"
+            "fma.rn.bf16x2 %0, u, %3, %5;\n\t}"
+            : "=r"(t)
+            : "r"(w), "r"(cg), "r"(s2), "r"(2 * i), "r"(o2));
+        p[i] = t;
+    }
+    lo.x = __byte_perm(p[0], p[1], 0x5410), lo.y = __byte_perm(p[2], p[3], 0x5410);
+    lo.z = __byte_perm(p[4], p[5], 0x5410), lo.w = __byte_perm(p[6], p[7], 0x5410);
+    hi.x = __byte_perm(p[0], p[1], 0x7632), hi.y = __byte_perm(p[2], p[3], 0x7632);
+    hi.z = __byte_perm(p[4], p[5], 0x7632), hi.w = __byte_perm(p[6], p[7], 0x7632);
+}
+// Four 8-bit codes of one word -> two bf16 pairs bf16(fp32(q*s + o)) in k order:
+// prmt builds 2^23 + q, an exact subtract gives q, one fp32 FMA, one rounding.
+__device__ __forceinline__ uint2 dequant4_8b(uint32_t w, float s, float o, uint32_t mg) {
+    float f[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t t;
+        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(t) : "r"(w), "r"(mg), "r"(0x7540 + i));
+        f[i] = __fmaf_rn(__fsub_rn(__uint_as_float(t), 8388608.0f), s, o);
+    }
+    uint2 r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r.x) : "f"(f[1]), "f"(f[0]));
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r.y) : "f"(f[3]), "f"(f[2]));
+    return r;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+    return v;
+}
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
@@ -152,17 +205,18 @@ __device__ __forceinline__ uint32_t pick_word(const uint4& v, int i) {
 
 // QT: scales and offsets arrive by TMA (tm_s, tm_o); otherwise the
 // dequantization threads load them from `scales` / `offsets`.
-template <int G, bool QT>
+template <int G, bool QT, int B>
 __global__ void __launch_bounds__(GM_THREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_p,
             const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_o,
             const uint16_t* __restrict__ scales, const uint16_t* __restrict__ offsets, uint16_t* __restrict__ Y,
             int M, int N, int K) {
+    using LY = GmLayout<B>;
     constexpr int QSPAN = 8 * G / GM_BK;  // k blocks covered by one qparam box (8 groups)
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t bar0 = sbase + GM_OFF_BAR;
+    const uint32_t bar0 = sbase + LY::OFF_BAR;
     auto full_tma = [&](int t) { return bar0 + 8u * t; };
     auto empty_tma = [&](int t) { return bar0 + 8u * (GM_TSTAGES + t); };
     auto full_deq = [&](int w) { return bar0 + 8u * (2 * GM_TSTAGES + w); };
@@ -171,8 +225,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     auto empty_q = [&](int q) { return bar0 + 8u * (2 * GM_TSTAGES + 2 * GM_WSTAGES + GM_QSTAGES + q); };
     const uint32_t tmem_full = bar0 + 8u * (2 * GM_TSTAGES + 2 * GM_WSTAGES + 2 * GM_QSTAGES);
     const uint32_t drain = tmem_full + 8u;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + GM_OFF_MISC);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + GM_OFF_MISC + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + LY::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + LY::OFF_MISC + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * GM_BW, m0 = blockIdx.y * GM_BT;
@@ -221,7 +275,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                     const uint32_t pq = (u / GM_QSTAGES) & 1;
                     if (!mbar_wait_bounded(empty_q(q), pq ^ 1, abort_flag, &g_gemm_fault, 1u, GM_WAIT_LIMIT_NS)) break;
                     mbar_arrive_expect_tx(full_q(q), 2 * GM_QBOX_BYTES);
-                    const uint32_t qdst = sbase + GM_OFF_Q + q * 2 * GM_QBOX_BYTES;
+                    const uint32_t qdst = sbase + LY::OFF_Q + q * 2 * GM_QBOX_BYTES;
                     tma_load_2d(qdst, &tm_s, full_q(q), 8 * u, n0);
                     tma_load_2d(qdst + GM_QBOX_BYTES, &tm_o, full_q(q), 8 * u, n0);
                     ++q_issued;
@@ -229,9 +283,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 const int t = kb % GM_TSTAGES;
                 const uint32_t ph = (kb / GM_TSTAGES) & 1;
                 if (!mbar_wait_bounded(empty_tma(t), ph ^ 1, abort_flag, &g_gemm_fault, 1u, GM_WAIT_LIMIT_NS)) break;
-                mbar_arrive_expect_tx(full_tma(t), GM_X_BYTES + GM_P_BYTES);
+                mbar_arrive_expect_tx(full_tma(t), GM_X_BYTES + LY::P_BYTES);
                 tma_load_2d(sbase + GM_OFF_X + t * GM_X_BYTES, &tm_x, full_tma(t), kb * GM_BK, m0);
-                tma_load_2d(sbase + GM_OFF_P + t * GM_P_BYTES, &tm_p, full_tma(t), kb * (GM_BK / 2), n0);
+                tma_load_2d(sbase + GM_OFF_P + t * LY::P_BYTES, &tm_p, full_tma(t), kb * LY::PROW, n0);
                 ++issued;
             }
             // never leave the block with copies still landing in its shared memory
@@ -295,11 +349,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             return q;
         };
         QRaw q0 = qload(0), q1 = qload(1), q2 = qload(2), q3 = qload(3);
-        uint32_t cm, cg;  // LOP3 constants pinned in registers (0x4300 pairs are also the 128.0 bias)
+        uint32_t cm, cg, mg;  // LOP3 constants pinned in registers (0x4300 pairs are also the 128.0 bias); 2^23
         asm volatile("mov.b32 %0, %1;" : "=r"(cm) : "r"(0x000F000Fu));
         asm volatile("mov.b32 %0, %1;" : "=r"(cg) : "r"(0x43004300u));
-        // the code tile arrives with the 32-byte swizzle: half hh of row r sits at 16 * (hh ^ bit 2 of r)
-        const uint32_t pcol = (uint32_t)(r * 32 + 16 * (hh ^ ((r >> 2) & 1)));
+        asm volatile("mov.b32 %0, %1;" : "=r"(mg) : "r"(0x4B000000u));
+        // this thread's 32 codes of a k block in the code tile: 4 bits: 32-byte rows, 32-byte swizzle,
+        // half hh of row r at 16 * (hh ^ bit 2 of r); 2 bits: 16-byte rows, half hh at 8 hh;
+        // 8 bits: 64-byte rows, 64-byte swizzle, 16-byte chunks 2hh, 2hh+1 at 16 * (c ^ ((r >> 1) & 3))
+        const uint32_t pcol = B == 4 ? (uint32_t)(r * 32 + 16 * (hh ^ ((r >> 2) & 1)))
+                              : B == 2 ? (uint32_t)(r * 16 + 8 * hh)
+                                       : (uint32_t)(r * 64 + 16 * ((2 * hh) ^ ((r >> 1) & 3)));
+        const uint32_t pcol1 = (uint32_t)(r * 64 + 16 * ((2 * hh + 1) ^ ((r >> 1) & 3)));  // 8 bits: second chunk
         // this thread's 16 columns of an A stage, in its own TMEM lane
         const uint32_t a_lane = tmem + ((uint32_t)(32 * sp) << 16) + (uint32_t)(GM_ACOL + 16 * hh);
         uint4 sq = make_uint4(0u, 0u, 0u, 0u), oq = sq;  // TMA variant: this row's 8 groups
@@ -317,7 +377,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                     ok = false;
                     break;
                 }
-                const uint32_t qsrc = sbase + GM_OFF_Q + q * 2 * GM_QBOX_BYTES + r * 16;
+                const uint32_t qsrc = sbase + LY::OFF_Q + q * 2 * GM_QBOX_BYTES + r * 16;
                 sq = lds128(qsrc);
                 oq = lds128(qsrc + GM_QBOX_BYTES);
                 mbar_arrive(empty_q(q));
@@ -330,7 +390,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 break;
             }
             tc_fence_after();  // the MMAs that read this A stage are complete
-            const uint4 words = lds128(sbase + GM_OFF_P + t * GM_P_BYTES + pcol);  // 32 codes of this half
+            const uint32_t ptile = sbase + GM_OFF_P + t * LY::P_BYTES;
             uint32_t s2, o2;  // (s,s) and (o,o) bf16 pairs of this half's group
             if (QT) {
                 const int j = (kb % QSPAN) * GM_BK / G + (G == 32 ? hh : 0);  // group among the box's 8
@@ -342,9 +402,27 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 o2 = __byte_perm(qc.o, 0, 0x1010);
             }
             // 32 weights of this row -> 16 columns (two bf16 of consecutive k each) of the A stage
-            tmem_st_16cols(a_lane + (uint32_t)(w * GM_ASTAGE_COLS), dequant8(words.x, s2, o2, cm, cg),
-                           dequant8(words.y, s2, o2, cm, cg), dequant8(words.z, s2, o2, cm, cg),
-                           dequant8(words.w, s2, o2, cm, cg));
+            const uint32_t acol = a_lane + (uint32_t)(w * GM_ASTAGE_COLS);
+            if constexpr (B == 4) {
+                const uint4 words = lds128(ptile + pcol);  // 32 codes of this half
+                tmem_st_16cols(acol, dequant8(words.x, s2, o2, cm, cg), dequant8(words.y, s2, o2, cm, cg),
+                               dequant8(words.z, s2, o2, cm, cg), dequant8(words.w, s2, o2, cm, cg));
+            } else if constexpr (B == 2) {
+                const uint2 words = lds64(ptile + pcol);
+                uint4 c0, c1, c2, c3;
+                dequant16_2b(words.x, s2, o2, cg, c0, c1);
+                dequant16_2b(words.y, s2, o2, cg, c2, c3);
+                tmem_st_16cols(acol, c0, c1, c2, c3);
+            } else {
+                const uint4 wa = lds128(ptile + pcol), wb = lds128(ptile + pcol1);
+                const float sf = __uint_as_float(s2 << 16), of = __uint_as_float(o2 << 16);
+                const uint2 d0 = dequant4_8b(wa.x, sf, of, mg), d1 = dequant4_8b(wa.y, sf, of, mg);
+                const uint2 d2 = dequant4_8b(wa.z, sf, of, mg), d3 = dequant4_8b(wa.w, sf, of, mg);
+                const uint2 d4 = dequant4_8b(wb.x, sf, of, mg), d5 = dequant4_8b(wb.y, sf, of, mg);
+                const uint2 d6 = dequant4_8b(wb.z, sf, of, mg), d7 = dequant4_8b(wb.w, sf, of, mg);
+                tmem_st_16cols(acol, make_uint4(d0.x, d0.y, d1.x, d1.y), make_uint4(d2.x, d2.y, d3.x, d3.y),
+                               make_uint4(d4.x, d4.y, d5.x, d5.y), make_uint4(d6.x, d6.y, d7.x, d7.y));
+            }
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(full_deq(w));
@@ -395,20 +473,38 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
 
 // ------------------------------------------------------------------ host side
 
-template <int G, bool QT>
+template <int G, bool QT, int B>
 static cudaError_t launch_gemm_g(const CUtensorMap& tx, const CUtensorMap& tp, const CUtensorMap& ts,
                                  const CUtensorMap& to, const uint16_t* scales, const uint16_t* offsets, uint16_t* Y,
                                  int M, int N, int K, cudaStream_t stream) {
-    auto kern = gemm_kernel<G, QT>;
-    cudaError_t e = ensure_kernel_attrs(reinterpret_cast<const void*>(kern), GM_SMEM_BYTES, false);
+    auto kern = gemm_kernel<G, QT, B>;
+    constexpr int SMEM = GmLayout<B>::SMEM_BYTES;
+    cudaError_t e = ensure_kernel_attrs(reinterpret_cast<const void*>(kern), SMEM, false);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((N + GM_BW - 1) / GM_BW), (unsigned)((M + GM_BT - 1) / GM_BT));
-    kern<<<grid, GM_THREADS, GM_SMEM_BYTES, stream>>>(tx, tp, ts, to, scales, offsets, Y, M, N, K);
+    kern<<<grid, GM_THREADS, SMEM, stream>>>(tx, tp, ts, to, scales, offsets, Y, M, N, K);
     return cudaGetLastError();
 }
 
+template <int B>
+static cudaError_t launch_gemm_b(const CUtensorMap& tx, const CUtensorMap& tp, const CUtensorMap& ts,
+                                 const CUtensorMap& to, bool qt, const uint16_t* scales, const uint16_t* offsets,
+                                 uint16_t* Y, int m, int n, int k, int g, cudaStream_t stream) {
+    switch (g) {
+        case 32:
+            return qt ? launch_gemm_g<32, true, B>(tx, tp, ts, to, scales, offsets, Y, m, n, k, stream)
+                      : launch_gemm_g<32, false, B>(tx, tp, ts, to, scales, offsets, Y, m, n, k, stream);
+        case 64:
+            return qt ? launch_gemm_g<64, true, B>(tx, tp, ts, to, scales, offsets, Y, m, n, k, stream)
+                      : launch_gemm_g<64, false, B>(tx, tp, ts, to, scales, offsets, Y, m, n, k, stream);
+        default:
+            return qt ? launch_gemm_g<128, true, B>(tx, tp, ts, to, scales, offsets, Y, m, n, k, stream)
+                      : launch_gemm_g<128, false, B>(tx, tp, ts, to, scales, offsets, Y, m, n, k, stream);
+    }
+}
+
 cudaError_t launch_gemm(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
-                        const uint16_t* offsets, int64_t N, int g, uint16_t* Y, cudaStream_t stream,
+                        const uint16_t* offsets, int64_t N, int g, int bits, uint16_t* Y, cudaStream_t stream,
                         const char** detail) {
     if ((N + GM_BW - 1) / GM_BW > 0x7FFFFFFF || (M + GM_BT - 1) / GM_BT > 65535) {
         *detail = "problem too large for the GEMM grid";
@@ -419,10 +515,16 @@ cudaError_t launch_gemm(const uint16_t* X, int64_t M, int64_t K, const uint8_t* 
     cudaError_t e = encode_tensor_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)K, (uint64_t)M,
                                          (uint64_t)K * 2, GM_BK, GM_BT, CU_TENSOR_MAP_SWIZZLE_128B, detail);
     if (e != cudaSuccess) return e;
-    // codes: [N][K/2] bytes, box 128 rows x 32 bytes, 32-byte swizzle (the two 16-byte halves of
-    // rows 4..7 of every 8 trade places: conflict-free reads of one half per thread)
-    e = encode_tensor_map_2d(&tp, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)(K / 2), (uint64_t)N, (uint64_t)(K / 2),
-                             GM_BK / 2, GM_BW, CU_TENSOR_MAP_SWIZZLE_32B, detail);
+    // codes: [N][K bits/8] bytes, box 128 rows x (64 k of codes): 4 bits: 32 bytes, 32-byte swizzle
+    // (the two 16-byte halves of rows 4..7 of every 8 trade places: conflict-free reads of one half
+    // per thread); 2 bits: 16 bytes, no swizzle; 8 bits: 64 bytes, 64-byte swizzle
+    const uint64_t row_bytes = (uint64_t)(K * bits / 8);
+    e = encode_tensor_map_2d(&tp, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, row_bytes, (uint64_t)N, row_bytes,
+                             (uint32_t)(GM_BK * bits / 8), GM_BW,
+                             bits == 4   ? CU_TENSOR_MAP_SWIZZLE_32B
+                             : bits == 2 ? CU_TENSOR_MAP_SWIZZLE_NONE
+                                         : CU_TENSOR_MAP_SWIZZLE_64B,
+                             detail);
     if (e != cudaSuccess) return e;
     // scales / offsets: [N][K/g] bf16, box 128 rows x 8 groups, when a row is
     // a whole number of 16-byte pieces (the tensor-map stride rule)
@@ -438,17 +540,9 @@ cudaError_t launch_gemm(const uint16_t* X, int64_t M, int64_t K, const uint8_t* 
         if (e != cudaSuccess) return e;
     }
     const int m = (int)M, n = (int)N, k = (int)K;
-    switch (g) {
-        case 32:
-            return qt ? launch_gemm_g<32, true>(tx, tp, ts, to, scales, offsets, Y, m, n, k, stream)
-                      : launch_gemm_g<32, false>(tx, tp, ts, to, scales, offsets, Y, m, n, k, stream);
-        case 64:
-            return qt ? launch_gemm_g<64, true>(tx, tp, ts, to, scales, offsets, Y, m, n, k, stream)
-                      : launch_gemm_g<64, false>(tx, tp, ts, to, scales, offsets, Y, m, n, k, stream);
-        default:
-            return qt ? launch_gemm_g<128, true>(tx, tp, ts, to, scales, offsets, Y, m, n, k, stream)
-                      : launch_gemm_g<128, false>(tx, tp, ts, to, scales, offsets, Y, m, n, k, stream);
-    }
+    if (bits == 2) return launch_gemm_b<2>(tx, tp, ts, to, qt, scales, offsets, Y, m, n, k, g, stream);
+    if (bits == 8) return launch_gemm_b<8>(tx, tp, ts, to, qt, scales, offsets, Y, m, n, k, g, stream);
+    return launch_gemm_b<4>(tx, tp, ts, to, qt, scales, offsets, Y, m, n, k, g, stream);
 }
 
 cudaError_t read_and_clear_gemm_fault(unsigned int* fault) {

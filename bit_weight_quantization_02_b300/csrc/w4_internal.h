@@ -10,10 +10,11 @@
 
 namespace w4 {
 
-cudaError_t launch_quantize(const uint16_t* W, int64_t N, int64_t K, int g, uint8_t* Wq, uint16_t* scales,
+// bits: code width, 2, 4 or 8
+cudaError_t launch_quantize(const uint16_t* W, int64_t N, int64_t K, int g, int bits, uint8_t* Wq, uint16_t* scales,
                             uint16_t* offsets, cudaStream_t stream);
 cudaError_t launch_dequantize(const uint8_t* Wq, const uint16_t* scales, const uint16_t* offsets, int64_t N,
-                              int64_t K, int g, uint16_t* W_out, cudaStream_t stream);
+                              int64_t K, int g, int bits, uint16_t* W_out, cudaStream_t stream);
 
 // Skinny (M <= 32) decode kernel.
 struct SkinnyPlan {
@@ -51,7 +52,7 @@ cudaError_t read_and_clear_stream_fault(unsigned int* fault);
 // Batched decode (5 <= M <= 32): 64-row units, the block's X slice staged once
 // by TMA; same plan and workspace as the stream kernel (launch_stream calls it).
 cudaError_t launch_batch(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
-                         const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
+                         const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, int bits, uint16_t* Y,
                          void* workspace, cudaStream_t stream, const char** detail);
 cudaError_t read_and_clear_batch_fault(unsigned int* fault);
 
@@ -79,7 +80,7 @@ cudaError_t resident_blocks(const void* kernel, int threads, size_t smem, int* s
 
 // tcgen05 tensor-core GEMM (any M).
 cudaError_t launch_gemm(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
-                        const uint16_t* offsets, int64_t N, int g, uint16_t* Y, cudaStream_t stream,
+                        const uint16_t* offsets, int64_t N, int g, int bits, uint16_t* Y, cudaStream_t stream,
                         const char** detail);
 // Read and clear the kernels' device fault words (bounded-wait timeouts); the
 // caller has synchronized the stream.

@@ -634,7 +634,7 @@ cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, 
                           const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
                           void* workspace, cudaStream_t stream, const char** detail) {
     if (M > 4)  // 5..32 tokens: the block-shared X kernel (w4_batch.cu)
-        return launch_batch(plan, X, M, K, Wq, scales, offsets, N, g, Y, workspace, stream, detail);
+        return launch_batch(plan, X, M, K, Wq, scales, offsets, N, g, 4, Y, workspace, stream, detail);
     const int64_t ng = K / g;
     const bool qt = (g == 32) && (ng % 8 == 0);  // qparam rows 16-byte aligned: 8-group TMA boxes
     cudaError_t e = cudaSuccess;

@@ -281,6 +281,53 @@ W4_API w4_status w4_linear_repacked(const uint16_t *X, int64_t M, int64_t K, con
                                     int64_t N, int group_size, uint16_t *Y, void *workspace,
                                     size_t workspace_bytes, void *stream);
 
+/*
+ * Other code widths on the same affine path.  Optimum Quanto's feature list
+ * names int2, int4 and int8 weights; the torchao README quantizes a
+ * diffusion transformer to int8 weight-only in groups of 128.  The pages give
+ * the widths, not their formulas; libw4 runs the 4-bit method unchanged with
+ * L = 2^bits - 1 levels in place of 15:
+ *   s = bf16(max(fp32(max - min) / L, 1e-6)),  o = min,
+ *   q = clamp(rne((w - o) / s), 0, L),  w' = bf16(fp32(q * s + o)).
+ * (At 8 bits the rounding of the scale to bf16, up to 2^-8 relative, can put
+ * a group's maximum above L + 1/2; the clamp then makes its code L.)
+ * Packed codes: row n holds K * bits / 8 bytes; byte p of a row holds the
+ * 8/bits codes k = (8/bits) p .. (8/bits) p + 8/bits - 1, code k at bits
+ * bits * (k mod 8/bits) (the lowest k in the lowest bits; at 4 bits this is
+ * the w4_quantize layout).  Scales and offsets as for w4_quantize.
+ * bits = 4 calls are exactly w4_quantize / w4_dequantize / w4_linear.
+ * bits not in {2, 4, 8} give W4_ERR_UNSUPPORTED; other errors as the 4-bit
+ * calls.
+ */
+W4_API size_t w4_packed_bytes_bits(int64_t N, int64_t K, int bits); /* N * K * bits / 8 */
+
+/* Group-wise quantization to `bits`-bit codes: Wq [N][K*bits/8] bytes,
+ * scales / offsets [N][K/group_size] bf16.  Bit-exact. */
+W4_API w4_status w4_quantize_bits(const uint16_t *W, int64_t N, int64_t K, int group_size,
+                                  int bits, uint8_t *Wq, uint16_t *scales, uint16_t *offsets,
+                                  void *stream);
+
+/* W_out[n,k] = bf16(fp32(q) * s + o) for `bits`-bit codes.  Bit-exact. */
+W4_API w4_status w4_dequantize_bits(const uint8_t *Wq, const uint16_t *scales,
+                                    const uint16_t *offsets, int64_t N, int64_t K,
+                                    int group_size, int bits, uint16_t *W_out, void *stream);
+
+/*
+ * Y[M,N] bf16 = X[M,K] . dequant(Wq)^T for `bits`-bit codes, fp32 sums, one
+ * rounding at the end, same accuracy contract as w4_linear.  M <= 32 with K /
+ * group_size even and a workspace of w4_linear_workspace_bytes(M, N, K,
+ * group_size) bytes runs the persistent stream-K decode kernel with 64-row
+ * units; anything else runs the tcgen05 tensor-core GEMM (any M).  8-bit
+ * weights enter the products as bf16(fp32(q s + o)), the w4_dequantize_bits
+ * value; 2-bit weights as bf16(q s + o) with one rounding.  The workspace
+ * rules of w4_linear apply.  2-bit codes need K % 64 == 0 (their rows are
+ * then a whole number of 16-byte pieces); other K give W4_ERR_UNSUPPORTED.
+ */
+W4_API w4_status w4_linear_bits(const uint16_t *X, int64_t M, int64_t K, const uint8_t *Wq,
+                                const uint16_t *scales, const uint16_t *offsets, int64_t N,
+                                int group_size, int bits, uint16_t *Y, void *workspace,
+                                size_t workspace_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

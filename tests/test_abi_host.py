@@ -170,3 +170,30 @@ def test_decode_layout_calls(lib):
     assert lib.w4_linear_repacked(FAKE, 2, 512, FAKE, 64, 32, FAKE, FAKE + 8, ws, None) == MISALIGNED
     assert lib.w4_linear_repacked(FAKE, 2, 512, FAKE, 64, 96, FAKE, FAKE, ws, None) == UNSUPPORTED
     assert lib.w4_linear_repacked(FAKE, 0, 512, FAKE, 64, 32, FAKE, None, 0, None) == OK
+
+
+def test_other_code_widths_host_rules(lib):
+    """2- and 8-bit calls: sizes, the width check and the 2-bit row rule, all before any launch."""
+    assert lib.w4_packed_bytes_bits(14336, 4096, 2) == 14336 * 1024
+    assert lib.w4_packed_bytes_bits(14336, 4096, 4) == lib.w4_packed_bytes(14336, 4096)
+    assert lib.w4_packed_bytes_bits(14336, 4096, 8) == 14336 * 4096
+    assert lib.w4_packed_bytes_bits(4, 64, 3) == 0
+    assert lib.w4_packed_bytes_bits(4, 66, 2) == 0  # K not a whole number of bytes
+    for bits in (0, 1, 3, 16):
+        assert lib.w4_quantize_bits(FAKE, 4, 256, 32, bits, FAKE, FAKE, FAKE, None) == UNSUPPORTED
+        assert lib.w4_dequantize_bits(FAKE, FAKE, FAKE, 4, 256, 32, bits, FAKE, None) == UNSUPPORTED
+        assert lib.w4_linear_bits(FAKE, 1, 256, FAKE, FAKE, FAKE, 4, 32, bits, FAKE, None, 0, None) == UNSUPPORTED
+        assert b"bits" in lib.w4_last_error_detail()
+    for bits in (2, 8):
+        assert lib.w4_quantize_bits(FAKE, 4, 256, 16, bits, FAKE, FAKE, FAKE, None) == UNSUPPORTED
+        assert lib.w4_quantize_bits(FAKE, 4, 96 + 16, 32, bits, FAKE, FAKE, FAKE, None) == INVALID
+        assert lib.w4_quantize_bits(FAKE + 2, 4, 64, 32, bits, FAKE, FAKE, FAKE, None) == MISALIGNED
+        assert lib.w4_dequantize_bits(FAKE, FAKE, FAKE, 4, 64, 32, bits, FAKE + 4, None) == MISALIGNED
+        assert lib.w4_linear_bits(FAKE, -1, 64, FAKE, FAKE, FAKE, 4, 32, bits, FAKE, None, 0, None) == INVALID
+        assert lib.w4_linear_bits(FAKE, 2, 64, FAKE, FAKE, FAKE, 4, 32, bits, FAKE + 8, None, 0, None) == MISALIGNED
+        # empty problems: no pointer touched, no launch
+        assert lib.w4_quantize_bits(None, 0, 64, 32, bits, None, None, None, None) == OK
+        assert lib.w4_linear_bits(None, 0, 64, None, None, None, 8, 32, bits, None, None, 0, None) == OK
+    # 2-bit rows must be whole 16-byte pieces for the linear (K % 64), quantize takes any K % g == 0
+    assert lib.w4_linear_bits(FAKE, 1, 96, FAKE, FAKE, FAKE, 4, 32, 2, FAKE, None, 0, None) == UNSUPPORTED
+    assert b"K % 64" in lib.w4_last_error_detail()
