@@ -438,13 +438,15 @@ def _rotated_graph_row(c, w4, wl, device, stream, dist, peaks, layout="canonical
             "tflops": round(2 * c.M * c.N * c.K / (t * 1e-3) / 1e12, 2)}
 
 
-def _code_width_rows(w4, wl, device, stream, dist, peaks, flush):
+def _code_width_rows(w4, wl, device, stream, dist, peaks, flush, only_bits=0):
     """2- and 8-bit codes (8 bits in groups of 128, 2 bits in groups of 32) on Llama-3-8B shapes:
     quantize (L2 flushed), decode at M = 1 and 16 (graphs of back-to-back calls over weight copies
     totalling > 4x L2) and prefill at M = 2048 (L2 flushed)."""
     import torch
     cases = []
     for b, g in ((8, 128), (2, 32)):
+        if only_bits and b != only_bits:
+            continue
         N, K = 14336, 4096
         W = wl.gen_weight(N, K, wl.weight_seed(7, 0, b), outliers=True, device=device)
         with torch.cuda.stream(stream):
@@ -564,7 +566,7 @@ def other_rows(args, w4, wl, device, stream, peaks, dist, only=None):
                                   "l2": "graph of back-to-back calls over weight copies totalling > 4x L2"}
 
     if want("widths"):
-        rows["other_code_widths"] = _code_width_rows(w4, wl, device, stream, dist, peaks, flush)
+        rows["other_code_widths"] = _code_width_rows(w4, wl, device, stream, dist, peaks, flush, args.widths_bits)
 
     # full 32-block stack at g=128: quantize every weight (all 6.98 B bf16 weights resident,
     # the 224 quantize calls back to back between two events), then M=1 and M=16 passes
@@ -724,6 +726,8 @@ def parse_args(argv=None):
                     help="all = the benchmark; the others run one secondary row alone (for profiling) and print it")
     ap.add_argument("--batched-m", type=int, default=0,
                     help="with --section batched: only the cases with this many tokens (for profiling)")
+    ap.add_argument("--widths-bits", type=int, default=0, choices=[0, 2, 8],
+                    help="with --section widths: only this code width (for profiling)")
     ap.add_argument("--layers", type=int, default=32,
                     help="Llama-3-8B blocks in the headline step (32 = the whole model; fewer only for profiling)")
     a = ap.parse_args(argv)
