@@ -32,6 +32,14 @@
 //    through fp32 (prmt into 2^23 + q, exact subtract, FMA with s and o,
 //    round to bf16): w' is then bf16(fp32(q s + o)), the dequantized weight
 //    bit for bit.
+//  * One token at 2 or 8 bits: seven of the MMA's eight token columns would
+//    be zero, so they carry the unit's eight 32-k slices instead (as in the
+//    4-bit one-token stream kernel): the ldmatrix row of column c points at
+//    the token's X only while the MMA works on slice c, at a zero row
+//    otherwise, and A is the raw code (128 + q at 2 bits, q at 8 bits, both
+//    exact in bf16) with no per-weight subtract or FMA.  Each unit then adds
+//    s (D - 128 xs) + o xs (8 bits: s D + o xs) per row and slice in fp32,
+//    D the slice's MMA sum and xs the slice's sum of X.
 //  * The (row group, k) units are cut into equal contiguous block ranges; a
 //    row group split between blocks is finished by the block holding its
 //    first unit: each of its warps adds the partial sums that warp w of every
@@ -158,6 +166,28 @@ __device__ __forceinline__ uint32_t pair8(uint32_t w, uint32_t sel0, float s, fl
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
     return r;
 }
+// 2-bit codes, one-token path: the raw pair (128 + q_k, 128 + q_k+1) at bits `sh` .. `sh` + 3 of w.
+__device__ __forceinline__ uint32_t raw2(uint32_t w, uint32_t sh, uint32_t cg) {
+    uint32_t r;
+    asm("{\n\t.reg .b32 t;\n\t"
+        "bfe.u32 t, %1, %2, 4;\n\t"
+        "mul.lo.u32 t, t, 0x4001;\n\t"
+        "lop3.b32 %0, t, 0x00030003, %3, 0xEA;\n\t}"
+        : "=r"(r)
+        : "r"(w), "r"(sh), "r"(cg));
+    return r;
+}
+// 8-bit codes, one-token path: bytes sel0 and sel0 + 1 of w as the bf16 pair (q_k, q_k+1), exact.
+__device__ __forceinline__ uint32_t raw8(uint32_t w, uint32_t sel0, uint32_t mg) {
+    uint32_t lo, hi, r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(w), "r"(mg), "r"(sel0));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(w), "r"(mg), "r"(sel0 + 1u));
+    const float a = __fsub_rn(__uint_as_float(lo), 8388608.0f), b = __fsub_rn(__uint_as_float(hi), 8388608.0f);
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    return r;
+}
+__device__ __forceinline__ float bf16lo_b(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi_b(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 __device__ __forceinline__ uint2 lds64_b(uint32_t addr) {
     uint2 v;
     asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
@@ -169,11 +199,13 @@ __device__ __forceinline__ uint32_t lds32_b(uint32_t addr) {
     return v;
 }
 
-template <int G, int MT, bool QT, int B>
+// ONE: the one-token slice-sum path (M == 1, 2- and 8-bit codes).
+template <int G, int MT, bool QT, int B, bool ONE>
 __global__ void __launch_bounds__(BT_THREADS, MT == 1 ? 4 : 3)
 batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
              const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_o, const BatchArgs p) {
     static_assert(B == 2 || B == 4 || B == 8, "code width");
+    static_assert(!ONE || (MT == 1 && B != 4), "the one-token path is for 2- and 8-bit codes");
     using L = BatchLayout<G, MT, B>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -287,6 +319,7 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
     float acc[MT][4];
 #pragma unroll
     for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+    float ya = 0.f, yb = 0.f;  // one-token path: rows gid, gid + 8 over this lane's slices of the tile so far
     const long long g0 = u0 / p.nkc;
     int grp = (int)g0, kc = (int)(u0 - g0 * p.nkc), kc_first = kc;
     bool owner_split = false, ok = true;
@@ -301,6 +334,17 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
         const uint32_t crow = st + (16 * warp + gid) * (uint32_t)(B == 8 ? 128 : L::CROW);
         const uint32_t qa = st + L::CODES + L::XBYTES + (16 * warp + gid) * L::QROW;
         const uint32_t xst = st + L::CODES;
+        float dacc[4] = {0.f, 0.f, 0.f, 0.f};  // one-token path: D[row gid / gid+8][slice 2tq / 2tq+1]
+        float xs0 = 0.f, xs1 = 0.f;            // one-token path: sums of X over slices 2tq, 2tq+1
+        if constexpr (ONE) {  // lane l sums k 8l .. 8l+7 of the token (row 0 of the boxes: no swizzle shift)
+            const uint4 xv = lds128_b(xst + (uint32_t)(lane >> 3) * L::XBOX + ((uint32_t)(lane & 7) << 4));
+            float xsl = ((bf16lo_b(xv.x) + bf16hi_b(xv.x)) + (bf16lo_b(xv.y) + bf16hi_b(xv.y))) +
+                        ((bf16lo_b(xv.z) + bf16hi_b(xv.z)) + (bf16lo_b(xv.w) + bf16hi_b(xv.w)));
+            xsl += __shfl_xor_sync(0xffffffffu, xsl, 1);
+            xsl += __shfl_xor_sync(0xffffffffu, xsl, 2);  // lanes 4c .. 4c+3: slice c
+            xs0 = __shfl_sync(0xffffffffu, xsl, 8 * tq);
+            xs1 = __shfl_sync(0xffffffffu, xsl, 8 * tq + 4);
+        }
 #pragma unroll
         for (int q = 0; q < 8; ++q) {  // 32 k of codes per row, two 16-k steps
             const uint32_t jq = (uint32_t)(((32 * q) / G) * 2);  // the piece's group, bytes into the row
@@ -329,7 +373,19 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
 #pragma unroll
             for (int s2 = 0; s2 < 2; ++s2) {  // 16-k step: chunks c0 = 4q + 2 s2 (k 0..7) and c0 + 1 (k 8..15)
                 uint32_t a0, a1, a2, a3;
-                if constexpr (B == 4) {
+                if constexpr (ONE && B == 2) {  // raw 128 + q
+                    a0 = raw2(wa2[s2], sh2, cg);
+                    a1 = raw2(wb2[s2], sh2, cg);
+                    a2 = raw2(wa2[s2], sh2 + 16u, cg);
+                    a3 = raw2(wb2[s2], sh2 + 16u, cg);
+                } else if constexpr (ONE) {  // raw q (8 bits)
+                    const int c = 2 * (q & 3) + s2;
+                    const uint32_t base = crow + (uint32_t)(q >> 2) * (L::CODES / 2) + ((uint32_t)(c ^ gid) << 4) + w8;
+                    a0 = raw8(lds32_b(base), sel8, mg);
+                    a1 = raw8(lds32_b(base + 8 * 128), sel8, mg);
+                    a2 = raw8(lds32_b(base + 8), sel8, mg);
+                    a3 = raw8(lds32_b(base + 8 * 128 + 8), sel8, mg);
+                } else if constexpr (B == 4) {
                     a0 = nat_pair(wa4[2 * s2], sel, sa2, oa2, cm, cg);
                     a1 = nat_pair(wb4[2 * s2], sel, sb2, ob2, cm, cg);
                     a2 = nat_pair(wa4[2 * s2 + 1], sel, sa2, oa2, cm, cg);
@@ -352,7 +408,12 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
                 const int cg8 = 4 * q + 2 * s2 + (li & 1);  // this lane's ldmatrix chunk (8 k) in the unit
                 const uint32_t xrow = xst + (uint32_t)(cg8 >> 3) * L::XBOX +
                                       ((uint32_t)((cg8 & 7) ^ lr) << 4) + (uint32_t)lr * 128;
-                if (MT == 1) {  // one token group: matrices 0, 1 (lanes 0-15 give the addresses)
+                if constexpr (ONE) {  // column lr: the token's row 0 while on slice q = lr, zero row 1 otherwise
+                    const uint32_t rs = lr == q ? 0u : 1u;
+                    uint32_t b0, b1;
+                    ldsm_x2(xst + (uint32_t)(cg8 >> 3) * L::XBOX + ((uint32_t)((cg8 & 7) ^ rs) << 4) + rs * 128, b0, b1);
+                    mma_16816(dacc, a0, a1, a2, a3, b0, b1);
+                } else if (MT == 1) {  // one token group: matrices 0, 1 (lanes 0-15 give the addresses)
                     uint32_t b0, b1;
                     ldsm_x2(xrow, b0, b1);
                     mma_16816(acc[0], a0, a1, a2, a3, b0, b1);
@@ -366,6 +427,31 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
                     }
                 }
             }
+        }
+        if constexpr (ONE) {  // this unit's slices: scales and offsets applied in fp32 (before the refill)
+            const uint32_t oq = (uint32_t)(BT_ROWS * L::QROW);  // offsets after the scales
+            float sA0, sA1, oA0, oA1, sB0, sB1, oB0, oB1;    // rows gid (A), gid + 8 (B); slices 2tq, 2tq + 1
+            if constexpr (G == 32) {  // groups 2tq, 2tq + 1: adjacent in the row
+                const uint32_t sa = lds32_b(qa + 4 * tq), oa = lds32_b(qa + oq + 4 * tq);
+                const uint32_t sb = lds32_b(qa + 8 * L::QROW + 4 * tq), ob = lds32_b(qa + 8 * L::QROW + oq + 4 * tq);
+                sA0 = bf16lo_b(sa), sA1 = bf16hi_b(sa), oA0 = bf16lo_b(oa), oA1 = bf16hi_b(oa);
+                sB0 = bf16lo_b(sb), sB1 = bf16hi_b(sb), oB0 = bf16lo_b(ob), oB1 = bf16hi_b(ob);
+            } else {  // both slices in group (64 tq) / G
+                const uint32_t go = (uint32_t)(((64 * tq) / G) * 2);
+                sA0 = sA1 = bf16lo_b(lds16_b(qa + go)), oA0 = oA1 = bf16lo_b(lds16_b(qa + oq + go));
+                sB0 = sB1 = bf16lo_b(lds16_b(qa + 8 * L::QROW + go));
+                oB0 = oB1 = bf16lo_b(lds16_b(qa + 8 * L::QROW + oq + go));
+            }
+            // 2 bits: D sums (128 + q) x, so D - 128 xs sums q x; 8 bits: D sums q x
+            const float bias0 = B == 2 ? -128.f * xs0 : 0.f, bias1 = B == 2 ? -128.f * xs1 : 0.f;
+            ya = fmaf(sA0, dacc[0] + bias0, ya);
+            ya = fmaf(oA0, xs0, ya);
+            ya = fmaf(sA1, dacc[1] + bias1, ya);
+            ya = fmaf(oA1, xs1, ya);
+            yb = fmaf(sB0, dacc[2] + bias0, yb);
+            yb = fmaf(oB0, xs0, yb);
+            yb = fmaf(sB1, dacc[3] + bias1, yb);
+            yb = fmaf(oB1, xs1, yb);
         }
         __syncthreads();  // every warp is done with stage d
         if (next < u1) {  // refill it with the unit DEPTH ahead
@@ -386,6 +472,16 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
         if (it + 1 == nunits || kc == p.nkc - 1) {
             const int tile = grp * BT_WARPS + warp;
             const int nrows = min(16, p.N - tile * 16);
+            if constexpr (ONE) {  // row sums over the four lanes of a row pair (slices 0..7) -> token 0's column
+                ya += __shfl_xor_sync(0xffffffffu, ya, 1);
+                ya += __shfl_xor_sync(0xffffffffu, ya, 2);
+                yb += __shfl_xor_sync(0xffffffffu, yb, 1);
+                yb += __shfl_xor_sync(0xffffffffu, yb, 2);
+                acc[0][0] = ya;
+                acc[0][2] = yb;
+                acc[0][1] = acc[0][3] = 0.f;
+                ya = yb = 0.f;
+            }
             if (kc_first == 0 && kc == p.nkc - 1) {  // this block summed all of the group's k
 #pragma unroll
                 for (int t = 0; t < MT; ++t)
@@ -426,11 +522,11 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
 
 // ------------------------------------------------------------------ host side
 
-template <int G, int MT, bool QT, int B>
+template <int G, int MT, bool QT, int B, bool ONE = false>
 static cudaError_t launch_batch_gm(const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap& ts,
                                    const CUtensorMap& to, BatchArgs a, size_t ws_bytes, cudaStream_t stream) {
     using L = BatchLayout<G, MT, B>;
-    auto kern = batch_kernel<G, MT, QT, B>;
+    auto kern = batch_kernel<G, MT, QT, B, ONE>;
     cudaError_t e = ensure_kernel_attrs(reinterpret_cast<const void*>(kern), L::SMEM, false);
     if (e != cudaSuccess) return e;
     int sms = 0, per_sm = 0;
@@ -457,6 +553,8 @@ static cudaError_t launch_batch_gm(const CUtensorMap& tw, const CUtensorMap& tx,
 template <int G, bool QT, int B>
 static cudaError_t launch_batch_g(const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap& ts,
                                   const CUtensorMap& to, BatchArgs a, size_t ws_bytes, cudaStream_t stream) {
+    if constexpr (B != 4)
+        if (a.M == 1) return launch_batch_gm<G, 1, QT, B, true>(tw, tx, ts, to, a, ws_bytes, stream);
     if (a.M <= 8) return launch_batch_gm<G, 1, QT, B>(tw, tx, ts, to, a, ws_bytes, stream);
     if (a.M <= 16) return launch_batch_gm<G, 2, QT, B>(tw, tx, ts, to, a, ws_bytes, stream);
     return launch_batch_gm<G, 4, QT, B>(tw, tx, ts, to, a, ws_bytes, stream);
