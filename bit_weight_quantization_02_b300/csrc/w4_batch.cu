@@ -139,21 +139,6 @@ __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// 2-bit codes: the pair (k, k+1) at bits `sh` .. `sh` + 3 of w as a bf16 pair
-// w' = bf16(q*s + o): the nibble times 0x4001 puts its low code at bit 0 and
-// its high code at bit 16, LOP3 masks them into 128 + q, exact subtract, FMA.
-__device__ __forceinline__ uint32_t pair2(uint32_t w, uint32_t sh, uint32_t s2, uint32_t o2, uint32_t cg) {
-    uint32_t r;
-    asm("{\n\t.reg .b32 t;\n\t"
-        "bfe.u32 t, %1, %2, 4;\n\t"
-        "mul.lo.u32 t, t, 0x4001;\n\t"
-        "lop3.b32 t, t, 0x00030003, %5, 0xEA;\n\t"
-        "sub.rn.bf16x2 t, t, %5;\n\t"
-        "fma.rn.bf16x2 %0, t, %3, %4;\n\t}"
-        : "=r"(r)
-        : "r"(w), "r"(sh), "r"(s2), "r"(o2), "r"(cg));
-    return r;
-}
 // 8-bit codes: bytes sel0 and sel0 + 1 of w (k, k+1) as a bf16 pair
 // bf16(fp32(q*s + o)): prmt builds 2^23 + q, an exact subtract gives q, one
 // fp32 FMA (q*s is exact), one rounding to bf16.
@@ -166,16 +151,29 @@ __device__ __forceinline__ uint32_t pair8(uint32_t w, uint32_t sel0, float s, fl
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
     return r;
 }
-// 2-bit codes, one-token path: the raw pair (128 + q_k, 128 + q_k+1) at bits `sh` .. `sh` + 3 of w.
-__device__ __forceinline__ uint32_t raw2(uint32_t w, uint32_t sh, uint32_t cg) {
-    uint32_t r;
-    asm("{\n\t.reg .b32 t;\n\t"
-        "bfe.u32 t, %1, %2, 4;\n\t"
-        "mul.lo.u32 t, t, 0x4001;\n\t"
-        "lop3.b32 %0, t, 0x00030003, %3, 0xEA;\n\t}"
-        : "=r"(r)
+// 2-bit codes: a lane's two pairs of one 16-code word as raw bf16 pairs, (128 + q_2t, 128 + q_2t+1) and
+// (128 + q_8+2t, 128 + q_9+2t), t = sh / 4: one shift brings both nibbles down (bits 0-3 and 16-19), LOP3
+// magic takes codes (2t, 8+2t) and, after a shift by 2, (2t+1, 9+2t), two PRMTs pair them in k order.
+__device__ __forceinline__ void raw2x2(uint32_t w, uint32_t sh, uint32_t cg, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b32 t, p, q;\n\t"
+        "shr.b32 t, %2, %3;\n\t"
+        "lop3.b32 p, t, 0x00030003, %4, 0xEA;\n\t"
+        "shr.b32 t, t, 2;\n\t"
+        "lop3.b32 q, t, 0x00030003, %4, 0xEA;\n\t"
+        "prmt.b32 %0, p, q, 0x5410;\n\t"
+        "prmt.b32 %1, p, q, 0x7632;\n\t}"
+        : "=r"(lo), "=r"(hi)
         : "r"(w), "r"(sh), "r"(cg));
-    return r;
+}
+// (128 + q) pair -> bf16 w' pair: exact subtract of 128, one bf16 FMA with (s, s) and (o, o)
+__device__ __forceinline__ uint32_t deq_raw(uint32_t r, uint32_t s2, uint32_t o2, uint32_t cg) {
+    uint32_t v;
+    asm("{\n\t.reg .b32 t;\n\t"
+        "sub.rn.bf16x2 t, %1, %4;\n\t"
+        "fma.rn.bf16x2 %0, t, %2, %3;\n\t}"
+        : "=r"(v)
+        : "r"(r), "r"(s2), "r"(o2), "r"(cg));
+    return v;
 }
 // 8-bit codes, one-token path: bytes sel0 and sel0 + 1 of w as the bf16 pair (q_k, q_k+1), exact.
 __device__ __forceinline__ uint32_t raw8(uint32_t w, uint32_t sel0, uint32_t mg) {
@@ -315,6 +313,7 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
     // ldmatrix row addresses of this lane: matrix i = lane / 8 (token group 2tp + i / 2, chunk c0 + i % 2),
     // row r = lane % 8 (token 8 (2tp + i / 2) + r); the 128-byte swizzle XORs the chunk with r
     const int lr = lane & 7, li = lane >> 3;
+    const uint32_t xo0 = (uint32_t)(li & 1) << 4, xo1 = 128u + ((uint32_t)((li & 1) ^ 1) << 4);  // one-token path
 
     float acc[MT][4];
 #pragma unroll
@@ -350,7 +349,7 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
             const uint32_t jq = (uint32_t)(((32 * q) / G) * 2);  // the piece's group, bytes into the row
             uint32_t sa2, oa2, sb2, ob2;  // (s,s), (o,o) bf16 pairs of rows gid and gid + 8 (2 and 4 bits)
             float saf, oaf, sbf, obf;     // the same as fp32 (8 bits)
-            {
+            if constexpr (!ONE) {
                 const uint32_t sa = lds16_b(qa + jq), oa = lds16_b(qa + BT_ROWS * L::QROW + jq);
                 const uint32_t sb = lds16_b(qa + 8 * L::QROW + jq), ob = lds16_b(qa + 8 * L::QROW + BT_ROWS * L::QROW + jq);
                 sa2 = __byte_perm(sa, 0, 0x1010), oa2 = __byte_perm(oa, 0, 0x1010);
@@ -374,10 +373,8 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
             for (int s2 = 0; s2 < 2; ++s2) {  // 16-k step: chunks c0 = 4q + 2 s2 (k 0..7) and c0 + 1 (k 8..15)
                 uint32_t a0, a1, a2, a3;
                 if constexpr (ONE && B == 2) {  // raw 128 + q
-                    a0 = raw2(wa2[s2], sh2, cg);
-                    a1 = raw2(wb2[s2], sh2, cg);
-                    a2 = raw2(wa2[s2], sh2 + 16u, cg);
-                    a3 = raw2(wb2[s2], sh2 + 16u, cg);
+                    raw2x2(wa2[s2], sh2, cg, a0, a2);
+                    raw2x2(wb2[s2], sh2, cg, a1, a3);
                 } else if constexpr (ONE) {  // raw q (8 bits)
                     const int c = 2 * (q & 3) + s2;
                     const uint32_t base = crow + (uint32_t)(q >> 2) * (L::CODES / 2) + ((uint32_t)(c ^ gid) << 4) + w8;
@@ -391,10 +388,12 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
                     a2 = nat_pair(wa4[2 * s2 + 1], sel, sa2, oa2, cm, cg);
                     a3 = nat_pair(wb4[2 * s2 + 1], sel, sb2, ob2, cm, cg);
                 } else if constexpr (B == 2) {  // k 2tq, 2tq+1 at bits 4tq; k + 8 at bits 16 + 4tq
-                    a0 = pair2(wa2[s2], sh2, sa2, oa2, cg);
-                    a1 = pair2(wb2[s2], sh2, sb2, ob2, cg);
-                    a2 = pair2(wa2[s2], sh2 + 16u, sa2, oa2, cg);
-                    a3 = pair2(wb2[s2], sh2 + 16u, sb2, ob2, cg);
+                    raw2x2(wa2[s2], sh2, cg, a0, a2);
+                    raw2x2(wb2[s2], sh2, cg, a1, a3);
+                    a0 = deq_raw(a0, sa2, oa2, cg);
+                    a2 = deq_raw(a2, sa2, oa2, cg);
+                    a1 = deq_raw(a1, sb2, ob2, cg);
+                    a3 = deq_raw(a3, sb2, ob2, cg);
                 } else {  // 128-byte rows in two boxes of 128 k, 128-byte swizzle: chunk c at c ^ (row & 7)
                     const int c = 2 * (q & 3) + s2;
                     const uint32_t base = crow + (uint32_t)(q >> 2) * (L::CODES / 2) + ((uint32_t)(c ^ gid) << 4) + w8;
@@ -409,9 +408,10 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
                 const uint32_t xrow = xst + (uint32_t)(cg8 >> 3) * L::XBOX +
                                       ((uint32_t)((cg8 & 7) ^ lr) << 4) + (uint32_t)lr * 128;
                 if constexpr (ONE) {  // column lr: the token's row 0 while on slice q = lr, zero row 1 otherwise
-                    const uint32_t rs = lr == q ? 0u : 1u;
+                    // chunk c0 + (li & 1) of row 0, or (c0 + (li & 1)) ^ 1 of row 1 (c0 = 4q + 2 s2 is even)
+                    const int c0 = 4 * q + 2 * s2;
                     uint32_t b0, b1;
-                    ldsm_x2(xst + (uint32_t)(cg8 >> 3) * L::XBOX + ((uint32_t)((cg8 & 7) ^ rs) << 4) + rs * 128, b0, b1);
+                    ldsm_x2(xst + (uint32_t)((c0 >> 3) * L::XBOX + ((c0 & 7) << 4)) + (lr == q ? xo0 : xo1), b0, b1);
                     mma_16816(dacc, a0, a1, a2, a3, b0, b1);
                 } else if (MT == 1) {  // one token group: matrices 0, 1 (lanes 0-15 give the addresses)
                     uint32_t b0, b1;
@@ -564,8 +564,8 @@ cudaError_t launch_batch(const StreamPlan& plan, const uint16_t* X, int64_t M, i
                          const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, int bits, uint16_t* Y,
                          void* workspace, cudaStream_t stream, const char** detail) {
     const int64_t ng = K / g;
-    // qparam rows 16-byte aligned: 8-group TMA boxes (4-bit codes only; the other widths use cp.async)
-    const bool qt = bits == 4 && (g == 32) && (ng % 8 == 0);
+    // qparam rows 16-byte aligned: 8-group TMA boxes (4- and 2-bit codes; 8-bit codes use cp.async)
+    const bool qt = bits != 8 && (g == 32) && (ng % 8 == 0);
     const int mp = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
     CUtensorMap tw, tx, ts, to;
     // codes: [N][K bits/8] bytes, box 64 rows x 128 bytes (2 bits: 64 bytes, 64-byte swizzle);
@@ -602,7 +602,9 @@ cudaError_t launch_batch(const StreamPlan& plan, const uint16_t* X, int64_t M, i
     const size_t ws = plan.ws_bytes;
     if (bits == 2) {
         switch (g) {
-            case 32: return launch_batch_g<32, false, 2>(tw, tx, ts, to, a, ws, stream);
+            case 32:
+                return qt ? launch_batch_g<32, true, 2>(tw, tx, ts, to, a, ws, stream)
+                          : launch_batch_g<32, false, 2>(tw, tx, ts, to, a, ws, stream);
             case 64: return launch_batch_g<64, false, 2>(tw, tx, ts, to, a, ws, stream);
             default: return launch_batch_g<128, false, 2>(tw, tx, ts, to, a, ws, stream);
         }
