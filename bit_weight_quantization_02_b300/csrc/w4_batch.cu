@@ -72,15 +72,18 @@ struct BatchArgs {
 };
 
 // Shared-memory layout of one ring stage (every piece 1024-byte aligned for the swizzled boxes).
-template <int G, int MT, int B>
+template <int G, int MT, int B, bool QT>
 struct BatchLayout {
     static constexpr int MP = 8 * MT;                       // token rows staged (M padded)
     static constexpr int CROW = BT_UK * B / 8;              // bytes of one row of a unit's codes
     static constexpr int CODES = BT_ROWS * CROW;            // 64 rows x 256 k of codes
     static constexpr int XBOX = MP * 128;                   // one 64-k box of X
     static constexpr int XBYTES = 4 * XBOX;
-    static constexpr int QROW = (BT_UK / G) * 2;            // bytes of one row of one qparam array
-    static constexpr int QBYTES = 2 * BT_ROWS * QROW;       // scales, then offsets
+    static constexpr int QROW = (BT_UK / G) * 2;            // bytes of one row of one qparam array (a unit's groups)
+    // staged row pitch: by TMA a box of 8 groups (16 bytes) per row holding the unit's groups
+    // (g = 64 / 128: also its neighbours'), by cp.async just the unit's groups
+    static constexpr int SQROW = QT ? 16 : QROW;
+    static constexpr int QBYTES = 2 * BT_ROWS * SQROW;      // scales, then offsets
     static constexpr int STAGE = (CODES + XBYTES + QBYTES + 1023) / 1024 * 1024;
     static constexpr int DEPTH = MT == 4 ? 2 : 3;
     static constexpr int SCRATCH = BT_WARPS * 16 * MP * 4;  // owners' own sums, per warp 16 x M fp32
@@ -204,7 +207,7 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
              const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_o, const BatchArgs p) {
     static_assert(B == 2 || B == 4 || B == 8, "code width");
     static_assert(!ONE || (MT == 1 && B != 4), "the one-token path is for 2- and 8-bit codes");
-    using L = BatchLayout<G, MT, B>;
+    using L = BatchLayout<G, MT, B, QT>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     constexpr int PPR = L::QROW / 4;               // 4-byte qparam pieces per row and array
@@ -244,7 +247,7 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
         const int arr = (i < PIECES) ? i / (PIECES / 2) : 0, rem = (i < PIECES) ? i % (PIECES / 2) : 0;
         prow[q] = rem / PPR;
         pcol[q] = 2 * (rem % PPR);
-        pdst[q] = (uint32_t)(L::CODES + L::XBYTES + arr * BT_ROWS * L::QROW + prow[q] * L::QROW + 4 * (rem % PPR));
+        pdst[q] = (uint32_t)(L::CODES + L::XBYTES + arr * BT_ROWS * L::SQROW + prow[q] * L::SQROW + 4 * (rem % PPR));
         pbase[q] = arr ? p.offsets : p.scales;
     }
     // codes and qparams of unit u into stage d (thread 0's TMA; every thread's cp.async when !QT)
@@ -259,9 +262,9 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
             } else {
                 tma_load_2d(st, &tm_w, bar, k * B / 8, row0);
             }
-            if (QT) {
-                tma_load_2d(st + L::CODES + L::XBYTES, &tm_s, bar, k / G, row0);
-                tma_load_2d(st + L::CODES + L::XBYTES + BT_ROWS * L::QROW, &tm_o, bar, k / G, row0);
+            if (QT) {  // the 8-group box holding the unit's groups (its first group rounded down to 8)
+                tma_load_2d(st + L::CODES + L::XBYTES, &tm_s, bar, (k / G) & ~7, row0);
+                tma_load_2d(st + L::CODES + L::XBYTES + BT_ROWS * L::SQROW, &tm_o, bar, (k / G) & ~7, row0);
             }
         }
         if (!QT) {
@@ -331,7 +334,9 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
         const uint32_t st = sbase + d * L::STAGE;
         // code row gid of this warp's tile (8 bits: in the first of the two 128-k boxes)
         const uint32_t crow = st + (16 * warp + gid) * (uint32_t)(B == 8 ? 128 : L::CROW);
-        const uint32_t qa = st + L::CODES + L::XBYTES + (16 * warp + gid) * L::QROW;
+        // scales of row gid of this warp's tile, from the unit's first group (TMA box: byte 2 (first group % 8))
+        const uint32_t qa = st + L::CODES + L::XBYTES + (16 * warp + gid) * L::SQROW +
+                            (QT ? (uint32_t)(((kc * (BT_UK / G)) & 7) * 2) : 0u);
         const uint32_t xst = st + L::CODES;
         float dacc[4] = {0.f, 0.f, 0.f, 0.f};  // one-token path: D[row gid / gid+8][slice 2tq / 2tq+1]
         float xs0 = 0.f, xs1 = 0.f;            // one-token path: sums of X over slices 2tq, 2tq+1
@@ -350,8 +355,8 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
             uint32_t sa2, oa2, sb2, ob2;  // (s,s), (o,o) bf16 pairs of rows gid and gid + 8 (2 and 4 bits)
             float saf, oaf, sbf, obf;     // the same as fp32 (8 bits)
             if constexpr (!ONE) {
-                const uint32_t sa = lds16_b(qa + jq), oa = lds16_b(qa + BT_ROWS * L::QROW + jq);
-                const uint32_t sb = lds16_b(qa + 8 * L::QROW + jq), ob = lds16_b(qa + 8 * L::QROW + BT_ROWS * L::QROW + jq);
+                const uint32_t sa = lds16_b(qa + jq), oa = lds16_b(qa + BT_ROWS * L::SQROW + jq);
+                const uint32_t sb = lds16_b(qa + 8 * L::SQROW + jq), ob = lds16_b(qa + 8 * L::SQROW + BT_ROWS * L::SQROW + jq);
                 sa2 = __byte_perm(sa, 0, 0x1010), oa2 = __byte_perm(oa, 0, 0x1010);
                 sb2 = __byte_perm(sb, 0, 0x1010), ob2 = __byte_perm(ob, 0, 0x1010);
                 saf = __uint_as_float(sa << 16), oaf = __uint_as_float(oa << 16);
@@ -429,18 +434,18 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
             }
         }
         if constexpr (ONE) {  // this unit's slices: scales and offsets applied in fp32 (before the refill)
-            const uint32_t oq = (uint32_t)(BT_ROWS * L::QROW);  // offsets after the scales
+            const uint32_t oq = (uint32_t)(BT_ROWS * L::SQROW);  // offsets after the scales
             float sA0, sA1, oA0, oA1, sB0, sB1, oB0, oB1;    // rows gid (A), gid + 8 (B); slices 2tq, 2tq + 1
             if constexpr (G == 32) {  // groups 2tq, 2tq + 1: adjacent in the row
                 const uint32_t sa = lds32_b(qa + 4 * tq), oa = lds32_b(qa + oq + 4 * tq);
-                const uint32_t sb = lds32_b(qa + 8 * L::QROW + 4 * tq), ob = lds32_b(qa + 8 * L::QROW + oq + 4 * tq);
+                const uint32_t sb = lds32_b(qa + 8 * L::SQROW + 4 * tq), ob = lds32_b(qa + 8 * L::SQROW + oq + 4 * tq);
                 sA0 = bf16lo_b(sa), sA1 = bf16hi_b(sa), oA0 = bf16lo_b(oa), oA1 = bf16hi_b(oa);
                 sB0 = bf16lo_b(sb), sB1 = bf16hi_b(sb), oB0 = bf16lo_b(ob), oB1 = bf16hi_b(ob);
             } else {  // both slices in group (64 tq) / G
                 const uint32_t go = (uint32_t)(((64 * tq) / G) * 2);
                 sA0 = sA1 = bf16lo_b(lds16_b(qa + go)), oA0 = oA1 = bf16lo_b(lds16_b(qa + oq + go));
-                sB0 = sB1 = bf16lo_b(lds16_b(qa + 8 * L::QROW + go));
-                oB0 = oB1 = bf16lo_b(lds16_b(qa + 8 * L::QROW + oq + go));
+                sB0 = sB1 = bf16lo_b(lds16_b(qa + 8 * L::SQROW + go));
+                oB0 = oB1 = bf16lo_b(lds16_b(qa + 8 * L::SQROW + oq + go));
             }
             // 2 bits: D sums (128 + q) x, so D - 128 xs sums q x; 8 bits: D sums q x
             const float bias0 = B == 2 ? -128.f * xs0 : 0.f, bias1 = B == 2 ? -128.f * xs1 : 0.f;
@@ -525,7 +530,7 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
 template <int G, int MT, bool QT, int B, bool ONE = false>
 static cudaError_t launch_batch_gm(const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap& ts,
                                    const CUtensorMap& to, BatchArgs a, size_t ws_bytes, cudaStream_t stream) {
-    using L = BatchLayout<G, MT, B>;
+    using L = BatchLayout<G, MT, B, QT>;
     auto kern = batch_kernel<G, MT, QT, B, ONE>;
     cudaError_t e = ensure_kernel_attrs(reinterpret_cast<const void*>(kern), L::SMEM, false);
     if (e != cudaSuccess) return e;
@@ -560,12 +565,28 @@ static cudaError_t launch_batch_g(const CUtensorMap& tw, const CUtensorMap& tx, 
     return launch_batch_gm<G, 4, QT, B>(tw, tx, ts, to, a, ws_bytes, stream);
 }
 
+template <int B>
+static cudaError_t launch_batch_b(const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap& ts,
+                                  const CUtensorMap& to, BatchArgs a, size_t ws, bool qt, int g, cudaStream_t stream) {
+    switch (g) {
+        case 32:
+            return qt ? launch_batch_g<32, true, B>(tw, tx, ts, to, a, ws, stream)
+                      : launch_batch_g<32, false, B>(tw, tx, ts, to, a, ws, stream);
+        case 64:
+            return qt ? launch_batch_g<64, true, B>(tw, tx, ts, to, a, ws, stream)
+                      : launch_batch_g<64, false, B>(tw, tx, ts, to, a, ws, stream);
+        default:
+            return qt ? launch_batch_g<128, true, B>(tw, tx, ts, to, a, ws, stream)
+                      : launch_batch_g<128, false, B>(tw, tx, ts, to, a, ws, stream);
+    }
+}
+
 cudaError_t launch_batch(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
                          const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, int bits, uint16_t* Y,
                          void* workspace, cudaStream_t stream, const char** detail) {
     const int64_t ng = K / g;
-    // qparam rows 16-byte aligned: 8-group TMA boxes (4- and 2-bit codes; 8-bit codes use cp.async)
-    const bool qt = bits != 8 && (g == 32) && (ng % 8 == 0);
+    // qparam rows whole 16-byte pieces: 8-group TMA boxes (K is then a multiple of 256); else cp.async
+    const bool qt = ng % 8 == 0;
     const int mp = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
     CUtensorMap tw, tx, ts, to;
     // codes: [N][K bits/8] bytes, box 64 rows x 128 bytes (2 bits: 64 bytes, 64-byte swizzle);
@@ -600,29 +621,9 @@ cudaError_t launch_batch(const StreamPlan& plan, const uint16_t* X, int64_t M, i
     a.units = (N + BT_ROWS - 1) / BT_ROWS * (long long)plan.nkc;
     a.ctas = 0;
     const size_t ws = plan.ws_bytes;
-    if (bits == 2) {
-        switch (g) {
-            case 32:
-                return qt ? launch_batch_g<32, true, 2>(tw, tx, ts, to, a, ws, stream)
-                          : launch_batch_g<32, false, 2>(tw, tx, ts, to, a, ws, stream);
-            case 64: return launch_batch_g<64, false, 2>(tw, tx, ts, to, a, ws, stream);
-            default: return launch_batch_g<128, false, 2>(tw, tx, ts, to, a, ws, stream);
-        }
-    }
-    if (bits == 8) {
-        switch (g) {
-            case 32: return launch_batch_g<32, false, 8>(tw, tx, ts, to, a, ws, stream);
-            case 64: return launch_batch_g<64, false, 8>(tw, tx, ts, to, a, ws, stream);
-            default: return launch_batch_g<128, false, 8>(tw, tx, ts, to, a, ws, stream);
-        }
-    }
-    switch (g) {
-        case 32:
-            return qt ? launch_batch_g<32, true, 4>(tw, tx, ts, to, a, ws, stream)
-                      : launch_batch_g<32, false, 4>(tw, tx, ts, to, a, ws, stream);
-        case 64: return launch_batch_g<64, false, 4>(tw, tx, ts, to, a, ws, stream);
-        default: return launch_batch_g<128, false, 4>(tw, tx, ts, to, a, ws, stream);
-    }
+    if (bits == 2) return launch_batch_b<2>(tw, tx, ts, to, a, ws, qt, g, stream);
+    if (bits == 8) return launch_batch_b<8>(tw, tx, ts, to, a, ws, qt, g, stream);
+    return launch_batch_b<4>(tw, tx, ts, to, a, ws, qt, g, stream);
 }
 
 cudaError_t read_and_clear_batch_fault(unsigned int* fault) {
