@@ -54,6 +54,12 @@ def linear_bytes_bits(M, N, K, g, bits):
     return N * K * bits // 8 + 4 * N * K // g + 2 * M * K + 2 * M * N
 
 
+def replica_gbs(bytes_per_step, steps, world, ms):
+    """Whole-job GB/s of `world` replicas that each ran `steps` steps of `bytes_per_step`
+    algorithmic bytes, timed as the slowest rank's `ms` (weak scaling: per-GPU work is fixed)."""
+    return bytes_per_step * steps * world / (ms * 1e-3) / 1e9
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -294,8 +300,7 @@ def gpu_arm(args):
     with torch.cuda.stream(stream):
         ms = time_region(graph.replay, args.steps, args.warmup, stream, dist, device)
     step_ms = ms / args.steps
-    units = stack.bytes * args.steps * dist.world
-    value = units / (ms * 1e-3) / 1e9
+    value = replica_gbs(stack.bytes, args.steps, dist.world, ms)
     launches = len(cases) * args.steps
     # dominant kernel: the stream-K decode kernel is the only kernel of the step (M=1
     # always takes it), so its average launch is the step time over the launches
@@ -322,7 +327,7 @@ def gpu_arm(args):
 
     with torch.cuda.stream(stream):
         e2e_ms = time_region(e2e_step, args.steps, args.warmup, stream, dist, device)
-    e2e_val = stack.bytes * args.steps * dist.world / (e2e_ms * 1e-3) / 1e9
+    e2e_val = replica_gbs(stack.bytes, args.steps, dist.world, e2e_ms)
 
     def e2e_eager_step():
         stack.X.copy_(xh, non_blocking=True)
@@ -335,7 +340,7 @@ def gpu_arm(args):
     e2e = {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": stack.X.numel() * 2,
            "d2h_bytes_per_step": stack.Y.numel() * 2, "ms_per_step": round(e2e_ms / args.steps, 4),
            "how": "pinned X -> device, CUDA graph of the 224 w4_linear calls, Y -> pinned host, per step",
-           "eager_python_calls": {"value": round(stack.bytes * eager_steps * dist.world / (eager_ms * 1e-3) / 1e9, 1),
+           "eager_python_calls": {"value": round(replica_gbs(stack.bytes, eager_steps, dist.world, eager_ms), 1),
                                   "ms_per_step": round(eager_ms / eager_steps, 4)}}
 
     rows = {}
@@ -345,7 +350,7 @@ def gpu_arm(args):
         dl_graph = dl.capture(stream)
         with torch.cuda.stream(stream):
             dl_ms = time_region(dl_graph.replay, args.steps, args.warmup, stream, dist, device)
-        dl_gbs = dl.bytes * args.steps * dist.world / (dl_ms * 1e-3) / 1e9
+        dl_gbs = replica_gbs(dl.bytes, args.steps, dist.world, dl_ms)
         rows["decode_layout_step"] = {"unit": "GB/s", "value": round(dl_gbs, 1),
                                       "ms_per_step": round(dl_ms / args.steps, 4),
                                       "frac_of_hbm_peak": round(dl_gbs / peaks["hbm_gbs"], 4),
@@ -364,7 +369,7 @@ def gpu_arm(args):
         mg_graph = mg.capture(stream)
         with torch.cuda.stream(stream):
             mg_ms = time_region(mg_graph.replay, args.steps, args.warmup, stream, dist, device)
-        mg_gbs = mg.bytes * args.steps * dist.world / (mg_ms * 1e-3) / 1e9
+        mg_gbs = replica_gbs(mg.bytes, args.steps, dist.world, mg_ms)
         rows["decode_step_merged_qkv_gateup"] = {
             "unit": "GB/s", "value": round(mg_gbs, 1), "ms_per_step": round(mg_ms / args.steps, 4),
             "frac_of_hbm_peak": round(mg_gbs / peaks["hbm_gbs"], 4), "launches_per_step": len(merged),
