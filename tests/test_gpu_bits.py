@@ -87,9 +87,10 @@ def test_quantize_adversarial_groups(b, g):
 
 @pytest.mark.parametrize("b", [2, 8])
 @pytest.mark.parametrize("M", [1, 3, 8, 13, 32])
-@pytest.mark.parametrize("N,K,g", [(512, 512, 32), (300, 4224, 64), (1000, 1024, 128)])
+@pytest.mark.parametrize("N,K,g", [(512, 512, 32), (300, 4224, 64), (1000, 1024, 128), (200, 1024, 64)])
 def test_linear_batched_decode(b, M, N, K, g):
-    """M <= 32 with a workspace: the stream-K kernel with 64-row units (ragged N, ragged K tail)."""
+    """M <= 32 with a workspace: the stream-K kernel with 64-row units (ragged N, ragged K tail;
+    qparams by TMA boxes of 8 groups where K/g is a multiple of 8, by cp.async otherwise)."""
     W = _w(N, K, seed=1000 + N + M)
     X = wl.gen_activation(M, K, seed=1100 + M).to(DEV)
     Wq, sc, of = gpu_quantize_bits(W, g, b)
