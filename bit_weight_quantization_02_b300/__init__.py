@@ -1,4 +1,5 @@
-"""libw4: int4 weight-only quantization and the bf16 x int4 linear on B300.
+"""libw4: int4 weight-only quantization and the bf16 x int4 linear on B300
+(and the same affine path with 2- and 8-bit codes: ``w4_*_bits``).
 
 Thin Python binding over the C ABI in ``include/w4.h``.  The functions keep
 the C names (``w4_quantize``, ``w4_dequantize``, ``w4_linear`` ...); they only
@@ -21,6 +22,7 @@ __all__ = [
     "w4_linear_repacked",
     "library_path", "load_library", "w4_quantize", "w4_dequantize", "w4_linear",
     "w4_linear_ex", "w4_packed_bytes", "w4_qparam_bytes", "w4_device_fault", "w4_format_version",
+    "w4_linear_static", "w4_packed_bytes_bits", "w4_quantize_bits", "w4_dequantize_bits", "w4_linear_bits",
 ]
 
 W4_FORMAT_VERSION = 1
