@@ -93,7 +93,7 @@ w4_status w4_linear_ex(const uint16_t* X, int64_t M, int64_t K, const uint8_t* W
     W4_TRY(check_shape(N, K, group_size));
     if (M < 0) return fail(W4_ERR_INVALID_ARG, "M = %lld must not be negative", (long long)M);
     if (M > 0x7FFFFFFFLL) return fail(W4_ERR_INVALID_ARG, "M must be below 2^31");
-    if (kernel < W4_KERNEL_AUTO || kernel > W4_KERNEL_STREAM)
+    if (kernel < W4_KERNEL_AUTO || kernel > W4_KERNEL_PAIR)
         return fail(W4_ERR_INVALID_ARG, "unknown kernel choice %d", (int)kernel);
     if ((kernel == W4_KERNEL_SKINNY || kernel == W4_KERNEL_SKINNY_CLUSTER) && M > w4::SKINNY_MAX_M)
         return fail(W4_ERR_INVALID_ARG, "the skinny kernels take M <= %d, got %lld", w4::SKINNY_MAX_M, (long long)M);
@@ -110,7 +110,23 @@ w4_status w4_linear_ex(const uint16_t* X, int64_t M, int64_t K, const uint8_t* W
 
     const char* detail = "";
     cudaError_t e;
-    // stream kernel: M <= 8 with a large enough workspace
+    // one token without a workspace (or when asked for): the SM-pair kernel, which needs none
+    w4::StreamPlan sp0;
+    const bool stream_ws = M <= w4::STREAM_MAX_M && w4::plan_stream(M, N, K, group_size, &sp0) &&
+                           workspace_bytes >= sp0.ws_bytes;
+    if (kernel == W4_KERNEL_PAIR || ((kernel == W4_KERNEL_AUTO || kernel == W4_KERNEL_SKINNY) && !stream_ws)) {
+        w4::PairPlan pp;
+        const bool can = w4::plan_pair(M, N, K, group_size, &pp);
+        if (kernel == W4_KERNEL_PAIR && !can)
+            return fail(W4_ERR_INVALID_ARG,
+                        "the pair kernel takes M == 1, K <= 16384 and K / group_size a multiple of 8");
+        if (can) {
+            e = w4::launch_pair(pp, X, K, Wq, scales, offsets, N, group_size, Y, (cudaStream_t)stream, &detail);
+            if (e != cudaSuccess) return fail(W4_ERR_CUDA, "pair linear: %s %s", cudaGetErrorString(e), detail);
+            return W4_OK;
+        }
+    }
+    // stream kernel: M <= 32 with a large enough workspace
     if (kernel == W4_KERNEL_AUTO || kernel == W4_KERNEL_SKINNY || kernel == W4_KERNEL_STREAM) {
         w4::StreamPlan sp;
         const bool can = M <= w4::STREAM_MAX_M && w4::plan_stream(M, N, K, group_size, &sp) &&
@@ -161,18 +177,19 @@ size_t w4_qparam_bytes(int64_t N, int64_t K, int group_size) {
 w4_status w4_device_fault(void* stream) {
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "synchronizing the stream");
-    unsigned int gemm = 0, skinny = 0, strm = 0, dec = 0, bat = 0;
+    unsigned int gemm = 0, skinny = 0, strm = 0, dec = 0, bat = 0, pair = 0;
     e = w4::read_and_clear_gemm_fault(&gemm);
     if (e == cudaSuccess) e = w4::read_and_clear_skinny_fault(&skinny);
     if (e == cudaSuccess) e = w4::read_and_clear_stream_fault(&strm);
     if (e == cudaSuccess) e = w4::read_and_clear_decode_fault(&dec);
     if (e == cudaSuccess) e = w4::read_and_clear_batch_fault(&bat);
+    if (e == cudaSuccess) e = w4::read_and_clear_pair_fault(&pair);
     if (e != cudaSuccess) return cuda_fail(e, "reading the device fault words");
-    if (gemm || skinny || strm || dec || bat)
+    if (gemm || skinny || strm || dec || bat || pair)
         return fail(W4_ERR_TIMEOUT,
                     "a block gave up a bounded wait (tensor-core 0x%x, skinny 0x%x, stream 0x%x, decode 0x%x, "
-                    "batched 0x%x)",
-                    gemm, skinny, strm, dec, bat);
+                    "batched 0x%x, pair 0x%x)",
+                    gemm, skinny, strm, dec, bat, pair);
     return W4_OK;
 }
 
@@ -353,6 +370,26 @@ cudaError_t encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, co
     return cudaSuccess;
 }
 
+cudaError_t encode_tensor_map_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, const uint64_t dims[3],
+                                 const uint64_t strides_bytes[2], const uint32_t box[3], CUtensorMapSwizzle swizzle,
+                                 const char** detail) {
+    EncodeTiledFn encode = encode_fn();
+    if (!encode) {
+        *detail = "cuTensorMapEncodeTiled is not available from the driver";
+        return cudaErrorNotSupported;
+    }
+    const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+    const cuuint64_t st[2] = {strides_bytes[0], strides_bytes[1]};
+    const cuuint32_t bx[3] = {box[0], box[1], box[2]};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (encode(map, dtype, 3, const_cast<void*>(base), d, st, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+        *detail = "3-D tensor map rejected by the driver";
+        return cudaErrorInvalidValue;
+    }
+    return cudaSuccess;
+}
+
 void set_error_detail(const char* msg) { snprintf(g_detail, sizeof g_detail, "%s", msg ? msg : ""); }
 
 cudaError_t resident_blocks(const void* kernel, int threads, size_t smem, int* sms, int* per_sm) {
@@ -385,6 +422,11 @@ cudaError_t ensure_kernel_attrs(const void* kernel, int smem_bytes, bool big_clu
     std::lock_guard<std::mutex> lock(mu);
     if (bit && (done[kernel] & bit)) return cudaSuccess;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    // every kernel asks for the largest shared-memory carveout, so consecutive launches of
+    // different shapes (different dynamic shared memory) never need the SM's L1 / shared split
+    // changed between them, which would keep the next launch's blocks off an SM until it drains
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e == cudaSuccess && big_clusters) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e == cudaSuccess && bit) done[kernel] |= bit;
     return e;

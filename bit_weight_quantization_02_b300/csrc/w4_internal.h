@@ -74,6 +74,18 @@ bool plan_decode(int64_t M, int64_t N, int64_t K, int g, DecodePlan* plan);
 cudaError_t launch_decode(const DecodePlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* packed,
                           int64_t N, int g, uint16_t* Y, void* workspace, cudaStream_t stream);
 
+// One-token decode on pairs of SMs (thread-block clusters of two), no
+// workspace: M == 1, K <= 16384, K / g a multiple of 8.
+struct PairPlan {
+    int nks;      // 512-k stages per row
+    size_t smem;  // dynamic shared memory bytes per block
+};
+bool plan_pair(int64_t M, int64_t N, int64_t K, int g, PairPlan* plan);
+cudaError_t launch_pair(const PairPlan& plan, const uint16_t* X, int64_t K, const uint8_t* Wq, const uint16_t* scales,
+                        const uint16_t* offsets, int64_t N, int g, uint16_t* Y, cudaStream_t stream,
+                        const char** detail);
+cudaError_t read_and_clear_pair_fault(unsigned int* fault);
+
 // SM count of the current device and resident blocks per SM for a kernel
 // launch shape (cached per device, kernel and shared-memory size).
 cudaError_t resident_blocks(const void* kernel, int threads, size_t smem, int* sms, int* per_sm);
@@ -92,6 +104,12 @@ cudaError_t read_and_clear_decode_fault(unsigned int* fault);
 // cluster sizes above 8 if asked), once per device and kernel: later calls,
 // e.g. during CUDA-graph capture, make no CUDA call.
 cudaError_t ensure_kernel_attrs(const void* kernel, int smem_bytes, bool big_clusters);
+
+// The same for a 3-D [outer][mid][inner] tensor: dims and box innermost first,
+// strides of the two outer dimensions in bytes.
+cudaError_t encode_tensor_map_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, const uint64_t dims[3],
+                                 const uint64_t strides_bytes[2], const uint32_t box[3], CUtensorMapSwizzle swizzle,
+                                 const char** detail);
 
 // Sets the text w4_last_error_detail() returns on this host thread.
 void set_error_detail(const char* msg);

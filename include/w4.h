@@ -65,12 +65,15 @@ typedef enum w4_status {
 
 /* Kernel choice for w4_linear_ex. */
 typedef enum w4_kernel {
-    W4_KERNEL_AUTO = 0,            /* stream kernel for M <= 32 (with workspace), else cluster for M <= 32, GEMM above */
+    W4_KERNEL_AUTO = 0,            /* M <= 32 with a workspace: stream kernels; without one: the pair kernel
+                                      for M == 1, the cluster kernel for M <= 32; GEMM above */
     W4_KERNEL_SKINNY = 1,          /* best memory-bound kernel for M <= 32 (stream, else cluster) */
     W4_KERNEL_GEMM = 2,            /* tcgen05 tensor-core GEMM; any M >= 1 */
     W4_KERNEL_SKINNY_CLUSTER = 3,  /* cluster split-K skinny kernel, M <= 32, no workspace */
-    W4_KERNEL_STREAM = 4           /* persistent stream-K kernels, M <= 32, need the workspace:
+    W4_KERNEL_STREAM = 4,          /* persistent stream-K kernels, M <= 32, need the workspace:
                                       per-warp units up to 4 tokens, block-shared X from 5 */
+    W4_KERNEL_PAIR = 5             /* one token on pairs of SMs (clusters of two), no workspace:
+                                      M == 1, K <= 16384, K / group_size a multiple of 8 */
 } w4_kernel;
 
 /*
@@ -133,8 +136,15 @@ W4_API size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int gro
  * Kernel choice: M <= 32 with a workspace of w4_linear_workspace_bytes runs
  * the persistent stream-K decode kernels (one 16- or 32-row unit per warp
  * step up to 4 tokens; from 5 tokens 64-row units whose X slice a block
- * stages once for its four warps); without one M <= 32 runs the cluster
- * split-K skinny kernel; larger M the tcgen05 tensor-core GEMM.  The kernels
+ * stages once for its four warps).  Without a workspace (NULL, 0) one token
+ * runs the SM-pair kernel (thread-block clusters of two that split K and add
+ * their partial sums in shared memory; K <= 16384 and K / group_size a
+ * multiple of 8), other M <= 32 the cluster split-K skinny kernel; larger M
+ * the tcgen05 tensor-core GEMM.  The workspace arguments extend the plain
+ * (X, M, K, Wq, scales, offsets, N, group_size, Y, stream) call: passing none
+ * gives that call exactly, at a speed cost that is small with one token (the
+ * 224 one-token Llama-3-8B linears take about 1.17x the time) and larger with
+ * 2 to 32 tokens (the cluster kernel: 2 to 5x).  The kernels
  * dequantize each weight as bf16(q * s + o) with a single rounding, which can
  * differ from w4_dequantize's double rounding by one bf16 ulp; the stream
  * kernel with one token does not round the weights at all: it sums
