@@ -177,19 +177,20 @@ size_t w4_qparam_bytes(int64_t N, int64_t K, int group_size) {
 w4_status w4_device_fault(void* stream) {
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "synchronizing the stream");
-    unsigned int gemm = 0, skinny = 0, strm = 0, dec = 0, bat = 0, pair = 0;
+    unsigned int gemm = 0, skinny = 0, strm = 0, dec = 0, bat = 0, pair = 0, self = 0;
     e = w4::read_and_clear_gemm_fault(&gemm);
     if (e == cudaSuccess) e = w4::read_and_clear_skinny_fault(&skinny);
     if (e == cudaSuccess) e = w4::read_and_clear_stream_fault(&strm);
     if (e == cudaSuccess) e = w4::read_and_clear_decode_fault(&dec);
     if (e == cudaSuccess) e = w4::read_and_clear_batch_fault(&bat);
     if (e == cudaSuccess) e = w4::read_and_clear_pair_fault(&pair);
+    if (e == cudaSuccess) e = w4::read_and_clear_selftest_fault(&self);
     if (e != cudaSuccess) return cuda_fail(e, "reading the device fault words");
-    if (gemm || skinny || strm || dec || bat || pair)
+    if (gemm || skinny || strm || dec || bat || pair || self)
         return fail(W4_ERR_TIMEOUT,
                     "a block gave up a bounded wait (tensor-core 0x%x, skinny 0x%x, stream 0x%x, decode 0x%x, "
-                    "batched 0x%x, pair 0x%x)",
-                    gemm, skinny, strm, dec, bat, pair);
+                    "batched 0x%x, pair 0x%x, self-test 0x%x)",
+                    gemm, skinny, strm, dec, bat, pair, self);
     return W4_OK;
 }
 

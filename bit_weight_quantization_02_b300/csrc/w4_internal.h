@@ -85,6 +85,7 @@ cudaError_t launch_pair(const PairPlan& plan, const uint16_t* X, int64_t K, cons
                         const uint16_t* offsets, int64_t N, int g, uint16_t* Y, cudaStream_t stream,
                         const char** detail);
 cudaError_t read_and_clear_pair_fault(unsigned int* fault);
+cudaError_t read_and_clear_selftest_fault(unsigned int* fault);  // w4_selftest.cu
 
 // SM count of the current device and resident blocks per SM for a kernel
 // launch shape (cached per device, kernel and shared-memory size).

@@ -192,7 +192,11 @@ W4_API size_t w4_qparam_bytes(int64_t N, int64_t K, int group_size);
  * w4_device_fault -- synchronizes `stream`, then reports whether any libw4
  * kernel on the current device gave up a bounded wait since the last call
  * (W4_ERR_TIMEOUT), and clears the flag.  Kernels that time out set the flag,
- * release what they hold and return; their outputs are then undefined.
+ * release what they hold and return; their outputs are then undefined, and a
+ * workspace they used must be zero-filled again before its next use.  W4_OK
+ * from w4_linear (or any call) only means the work was enqueued: it does not
+ * cover a wait that gives up later, which only this call reports.
+ * (include/w4_selftest.h has a hook that makes the waits run out on purpose.)
  */
 W4_API w4_status w4_device_fault(void *stream);
 

@@ -2,6 +2,7 @@
 include/w4.h declares, and rejects bad arguments before touching the GPU.
 Nothing here launches a kernel, so it runs without a GPU."""
 import ctypes
+import glob
 import os
 import re
 
@@ -11,12 +12,13 @@ import bit_weight_quantization_02_b300 as w4
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "w4.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 OK, INVALID, UNSUPPORTED, MISALIGNED = 0, 1, 2, 3
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "\n".join(open(h).read() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(w4_[a-z0-9_]+)\s*\(", text)))
 
@@ -33,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
     assert {"w4_quantize", "w4_dequantize", "w4_linear", "w4_linear_ex", "w4_linear_workspace_bytes",
             "w4_device_fault"} <= set(names)
     for n in names:
-        assert hasattr(lib, n), f"{n} declared in w4.h but not exported"
+        assert hasattr(lib, n), f"{n} declared in include/*.h but not exported"
 
 
 def test_only_the_abi_is_exported(lib):
