@@ -77,6 +77,7 @@ def load_library():
             "w4_quantize_bits": ([p, i64, i64, i32, i32, p, p, p, p], i32),
             "w4_dequantize_bits": ([p, p, p, i64, i64, i32, i32, p, p], i32),
             "w4_linear_bits": ([p, i64, i64, p, p, p, i64, i32, i32, p, p, sz, p], i32),
+            "w4_selftest_bounded_waits": ([p, sz, p, ctypes.c_uint64, p], i32),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -313,8 +314,10 @@ def w4_linear_static(X, Wq, scales, offsets, group_size, out=None):
     M, K = X.shape
     N = Wq.shape[0]
     Y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
-    _check(lib.w4_linear_static(_ptr(X), M, K, _ptr(Wq), _ptr(scales), _ptr(offsets), N, group_size, _ptr(Y),
-                                _stream(X)), "w4_linear_static")
+    # the library finds its array on the current device: make it X's
+    with torch.cuda.device(X.device):
+        _check(lib.w4_linear_static(_ptr(X), M, K, _ptr(Wq), _ptr(scales), _ptr(offsets), N, group_size, _ptr(Y),
+                                    _stream(X)), "w4_linear_static")
     return Y
 
 

@@ -9,13 +9,18 @@
 // its own.
 //
 // The array is a file-scope __device__ variable: every GPU that loads the
-// library holds W4_STATIC_SCRATCH_BYTES of it until the process exits.  Host
-// code cannot use the array's name as a device address, so the first call on
-// each device (with that device current) asks the runtime for the address
-// with cudaGetSymbolAddress and caches it.
+// library's device code holds W4_STATIC_SCRATCH_BYTES of it until the process
+// exits.  With lazy module loading (the CUDA default since 12.2) that code is
+// loaded, and the array set aside, at its first use on a device -- here, the
+// first call's cudaGetSymbolAddress -- so the first call on each device is where
+// the array is allocated, and it can fail there when device memory is short;
+// later calls allocate nothing.  Host code cannot use the array's name as a
+// device address, so that first call (with the device current) asks the runtime
+// for the address and caches it.
 #include "w4.h"
 #include "w4_internal.h"
 
+#include <cstdio>
 #include <mutex>
 
 namespace {
@@ -29,6 +34,11 @@ void* g_scratch_ptr[kMaxDevices] = {};
 w4_status static_fail(w4_status s, const char* msg) {
     w4::set_error_detail(msg);  // read back with w4_last_error_detail()
     return s;
+}
+w4_status static_cuda_fail(const char* what, cudaError_t e) {
+    char msg[200];
+    snprintf(msg, sizeof msg, "%s: %s", what, cudaGetErrorString(e));
+    return static_fail(W4_ERR_CUDA, msg);
 }
 
 // Device address of the scratch array on the current device (looked up once per device).
@@ -71,12 +81,13 @@ extern "C" w4_status w4_linear_static(const uint16_t* X, int64_t M, int64_t K, c
                            "<= W4_STATIC_SCRATCH_BYTES");
     void* scratch = nullptr;
     cudaError_t e = scratch_address(&scratch);
-    if (e != cudaSuccess) return static_fail(W4_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed");
+    if (e != cudaSuccess)
+        return static_cuda_fail("looking up (and on a device's first call, loading) the static scratch array", e);
     // The kernel leaves what it used at zero, but a call that gave up mid-way
     // could not: clear the part this call uses first (an asynchronous memset,
     // no allocation).
     e = cudaMemsetAsync(scratch, 0, plan.ws_bytes, (cudaStream_t)stream);
-    if (e != cudaSuccess) return static_fail(W4_ERR_CUDA, "clearing the static scratch failed");
+    if (e != cudaSuccess) return static_cuda_fail("clearing the static scratch array", e);
     const char* detail = "";
     e = w4::launch_stream(plan, X, M, K, Wq, scales, offsets, N, group_size, Y, scratch, (cudaStream_t)stream,
                           &detail);

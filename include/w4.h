@@ -230,7 +230,11 @@ W4_API int w4_format_version(void);
  * W4_ERR_INVALID_ARG and a message in w4_last_error_detail().
  * Set-up: the first call on each device, with that device current, looks up
  * the array's device address (cudaGetSymbolAddress); make that first call
- * before any stream capture.
+ * before any stream capture.  With lazy module loading (the CUDA default) the
+ * library's device code, and with it the array, is loaded at that first call:
+ * the first call on a device is where the 4 MiB are set aside, and it can fail
+ * with W4_ERR_CUDA when device memory is short (w4_last_error_detail() has the
+ * CUDA error).  Later calls on that device allocate nothing.
  * Every call clears the part of the array it uses (an asynchronous memset on
  * `stream`) and then shares the one array with every other call on the same
  * device: calls that overlap on the GPU (different streams) race and give
