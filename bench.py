@@ -197,7 +197,7 @@ class LinearStack:
     """Packed weights, inputs and outputs of a sequence of linears, with all X in
     one device buffer and all Y in another (one copy each way per step)."""
 
-    def __init__(self, cases, device, w4, wl, packed=None, layout="canonical"):
+    def __init__(self, cases, device, w4, wl, packed=None, layout="canonical", workspace=None):
         import torch
         self.cases = cases
         self.device = device
@@ -219,7 +219,7 @@ class LinearStack:
             xo += c.M * c.K
             yo += c.M * c.N
         need = max(w4.w4_linear_workspace_bytes(c.M, c.N, c.K, c.group_size) for c in cases)
-        self.ws = w4.Workspace(device, need)
+        self.ws = workspace if workspace is not None else w4.Workspace(device, need)
         self.bytes = sum(linear_bytes(c.M, c.N, c.K, c.group_size) for c in cases)
         self.flops = sum(2 * c.M * c.N * c.K for c in cases)
         self.w4 = w4
@@ -241,6 +241,16 @@ class LinearStack:
             with torch.cuda.graph(g, stream=stream):
                 self.run()
         return g
+
+
+def device_fault(w4, device):
+    """None if no libw4 kernel gave up a bounded wait since the last check, else its detail
+    (a timed-out kernel's output is undefined, so the numbers timed over it are not reported)."""
+    try:
+        w4.w4_device_fault(device)
+        return None
+    except w4.W4Error as e:
+        return str(e)
 
 
 def time_region(fn, steps, warmup, stream, dist, device):
@@ -337,6 +347,22 @@ def gpu_arm(args):
     eager_steps = max(3, args.steps // 10)
     with torch.cuda.stream(stream):
         eager_ms = time_region(e2e_eager_step, eager_steps, 2, stream, dist, device)
+    faults = [f for f in [device_fault(w4, device)] if f]
+
+    # the same step without a workspace: w4_linear's call with no workspace (the SM-pair kernel)
+    nows = LinearStack(cases, device, w4, wl, packed=stack.packed, workspace=w4.Workspace(device))
+    nows_graph = nows.capture(stream)
+    with torch.cuda.stream(stream):
+        nows_ms = time_region(nows_graph.replay, args.steps, args.warmup, stream, dist, device)
+    nows_gbs = replica_gbs(nows.bytes, args.steps, dist.world, nows_ms)
+    no_workspace = {"value": round(nows_gbs, 1), "unit": "GB/s", "ms_per_step": round(nows_ms / args.steps, 4),
+                    "frac_of_hbm_peak": round(nows_gbs / peaks["hbm_gbs"], 4),
+                    "time_vs_workspace_step": round(nows_ms / ms, 3), "kernel": "pair_kernel (w4_linear, no workspace)",
+                    "how": "the headline step's 224 w4_linear calls with no workspace passed (thread-block clusters "
+                           "of two SMs split K and add their partial sums in shared memory), CUDA graph"}
+    del nows_graph, nows
+    faults += [f for f in [device_fault(w4, device)] if f]
+
     e2e = {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": stack.X.numel() * 2,
            "d2h_bytes_per_step": stack.Y.numel() * 2, "ms_per_step": round(e2e_ms / args.steps, 4),
            "how": "pinned X -> device, CUDA graph of the 224 w4_linear calls, Y -> pinned host, per step",
@@ -378,6 +404,7 @@ def gpu_arm(args):
                    "merged matrix), CUDA graph of the 128 calls"}
         del mg_graph, mg
         rows.update(other_rows(args, w4, wl, device, stream, peaks, dist))
+        faults += [f for f in [device_fault(w4, device)] if f]
 
     step_bytes = stack.bytes
     del graph, stack
@@ -386,6 +413,7 @@ def gpu_arm(args):
     if dist.rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline_sample(args.cpu_seconds)
 
+    prefill, batched = summary_rows(rows, peaks)
     if dist.rank == 0:
         line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": dist.world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
@@ -395,15 +423,36 @@ def gpu_arm(args):
                            "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB of packed weights per step)",
                            "group_size": 32, "M": 1, "linears_per_step": len(cases),
                            "parallelism": "replicas" if dist.world > 1 else "single GPU"},
-                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+                "roofline": roofline, "prefill": prefill, "batched": batched, "no_workspace": no_workspace,
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
                 "clocks": clk, "peaks": {k: peaks.get(k) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained",
                                                                      "source")},
+                "device_fault": faults[0] if faults else None,
                 "rows": rows}
+        if faults:  # a kernel gave up a bounded wait: its outputs, and so these numbers, are not valid
+            line["value"] = None
+            line["e2e"]["value"] = None
         print(json.dumps(line), flush=True)
     dist.close()
 
 
-def _rotated_graph_row(c, w4, wl, device, stream, dist, peaks, layout="canonical"):
+def summary_rows(rows, peaks):
+    """Compact prefill (TFLOP/s) and batched-decode (GB/s) results for the top of the JSON line."""
+    pre = rows.get("prefill_gemm", {}).get("cases", [])
+    prefill = {"unit": "TFLOP/s", "kernel": "gemm_kernel (tcgen05)", "peak": peaks["bf16_tflops"],
+               "peak_source": "MEASURED_PEAKS bf16_tflops (burst)", "l2": "flushed before every call",
+               "cases": [{"M": c["M"], "N": c["N"], "K": c["K"], "g": 32, "tflops": c["tflops"],
+                          "frac": c["frac_of_bf16_peak"]} for c in pre]} if pre else None
+    b3 = [c for c in rows.get("batched_decode_g64", {}).get("cases", []) if c.get("layout", "canonical") == "canonical"]
+    # with a workspace first; the no-workspace rows say so in their kernel name
+    batched = {"unit": "GB/s", "peak": peaks["hbm_gbs"], "peak_source": "MEASURED_PEAKS hbm_gbs (copy)",
+               "l2": "graph of calls over weight copies > 4x L2",
+               "cases": [{"M": c.get("M"), "N": c.get("N"), "K": c.get("K"), "g": 64, "kernel": c.get("kernel"),
+                          "gbs": c.get("gbs"), "frac": c.get("frac_of_hbm_peak")} for c in b3]} if b3 else None
+    return prefill, batched
+
+
+def _rotated_graph_row(c, w4, wl, device, stream, dist, peaks, layout="canonical", no_workspace=False):
     """Time one linear shape: a graph of back-to-back calls over weight copies totalling
     more than 4x L2 (so every call streams its weights from HBM); `layout` "decode" times
     w4_linear_repacked on w4_repack's rearrangement of the same weights."""
@@ -416,7 +465,7 @@ def _rotated_graph_row(c, w4, wl, device, stream, dist, peaks, layout="canonical
         reps = [(Wq.clone(), sc.clone(), of.clone()) for _ in range(copies)]
     X = wl.gen_activation(c.M, c.K, c.x_seed, device=device)
     Y = torch.empty((c.M, c.N), dtype=torch.bfloat16, device=device)
-    ws = w4.Workspace(device).reserve_for(c.M, c.N, c.K, c.group_size)
+    ws = w4.Workspace(device) if no_workspace else w4.Workspace(device).reserve_for(c.M, c.N, c.K, c.group_size)
     it = {"i": 0}
 
     def one():
@@ -437,7 +486,8 @@ def _rotated_graph_row(c, w4, wl, device, stream, dist, peaks, layout="canonical
         t = time_region(g.replay, 20, 3, stream, dist, device) / (20 * copies)
     gbs = linear_bytes(c.M, c.N, c.K, c.group_size) / (t * 1e-3) / 1e9
     del reps, Wq, sc, of, g
-    return {"M": c.M, "N": c.N, "K": c.K, "g": c.group_size, "layout": layout, "us": round(t * 1e3, 2),
+    return {"M": c.M, "N": c.N, "K": c.K, "g": c.group_size, "layout": layout, "workspace": not no_workspace,
+            "us": round(t * 1e3, 2),
             "gbs": round(gbs, 1),
             "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
             "tflops": round(2 * c.M * c.N * c.K / (t * 1e-3) / 1e12, 2)}
@@ -567,6 +617,9 @@ def other_rows(args, w4, wl, device, stream, peaks, dist, only=None):
         b3[-1]["kernel"] = "stream_kernel" if c.M <= 4 else "batch_kernel"
         b3.append(_rotated_graph_row(c, w4, wl, device, stream, dist, peaks, layout="decode"))
         b3[-1]["kernel"] = "decode_kernel"
+        if c.N == 4096 and c.M in (2, 16, 32):  # w4_linear without a workspace: the cluster split-K kernel
+            b3.append(_rotated_graph_row(c, w4, wl, device, stream, dist, peaks, no_workspace=True))
+            b3[-1]["kernel"] = "skinny_kernel (no workspace)"
     rows["batched_decode_g64"] = {"unit": "GB/s", "cases": b3,
                                   "l2": "graph of back-to-back calls over weight copies totalling > 4x L2"}
 
@@ -659,23 +712,101 @@ def _oracle_decode_inputs(cases):
 
 
 def cpu_baseline_sample(seconds):
-    """The oracle, as it stands (single-threaded C, fp64 accumulation), on one block's
-    7 decode linears repeated for about `seconds`; GB/s of algorithmic bytes."""
+    """The oracle, as it stands (plain C, fp64 accumulation), on the host's cores: the headline
+    metric on one block's 7 decode linears, single-threaded and on every core (OpenMP over
+    output rows; the results do not depend on the thread count), w4_quantize's work on the
+    gate matrix, and a bounded sample of every config with the extrapolations labelled."""
+    import numpy as np
+    import torch
     import oracle
     from bit_weight_quantization_02_b300 import workloads as wl
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    cores = oracle.set_threads(0)
     prepared = _oracle_decode_inputs(wl.config2(0))
-    nbytes, t_total, passes = 0, 0.0, 0
-    while t_total < seconds or passes == 0:
-        for c, X, (Wq, sc, of) in prepared:
-            t = time.perf_counter()
-            oracle.ref_linear(X, Wq, sc, of, c.group_size)
-            t_total += time.perf_counter() - t
-            nbytes += linear_bytes(c.M, c.N, c.K, c.group_size)
-        passes += 1
-    return {"value": round(nbytes / t_total / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{passes} pass(es) of the 7 M=1 g=32 decode linears of one Llama-3-8B block "
-                      f"({t_total:.1f} s of single-threaded C, fp64 accumulation)",
-            "host_cores_available": os.cpu_count()}
+
+    def linear_pass_rate(threads, budget):
+        oracle.set_threads(threads)
+        nbytes, el, passes = 0, 0.0, 0
+        while el < budget or passes == 0:
+            for c, X, (Wq, sc, of) in prepared:
+                t = time.perf_counter()
+                oracle.ref_linear(X, Wq, sc, of, c.group_size)
+                el += time.perf_counter() - t
+                nbytes += linear_bytes(c.M, c.N, c.K, c.group_size)
+            passes += 1
+        return nbytes / el / 1e9, passes, el
+
+    single, p1, t1 = linear_pass_rate(1, 0.35 * seconds)
+    multi, pn, tn = linear_pass_rate(0, 0.1 * seconds)
+
+    def quant_rate(W, g, threads):
+        oracle.set_threads(threads)
+        t = time.perf_counter()
+        oracle.ref_quantize(W, g)
+        return time.perf_counter() - t
+
+    gate = wl.config2()[4]
+    Wg = bits(wl.gen_weight(gate.N, gate.K, gate.w_seed, outliers=True))
+    qb = quantize_bytes(gate.N, gate.K, 32)
+    q1, qn = quant_rate(Wg, 32, 1), quant_rate(Wg, 32, 0)
+    del Wg
+
+    # every config, on every core (one sample each; scaled where noted)
+    oracle.set_threads(0)
+    per = {}
+
+    def lin_time(c, M=None, rows=None):
+        W = bits(wl.gen_weight(c.N, c.K, c.w_seed, outliers=c.outliers))
+        t = time.perf_counter()
+        q = oracle.ref_quantize(W, c.group_size)
+        tq = time.perf_counter() - t
+        X = bits(wl.gen_activation(M or c.M, c.K, c.x_seed))
+        if rows is not None:
+            X = X[:rows]
+        t = time.perf_counter()
+        oracle.ref_linear(X, *q, c.group_size)
+        return tq, time.perf_counter() - t
+
+    c1 = wl.config1()[0]
+    tq, tl = lin_time(c1)
+    per["config1"] = {"quantize_ms": round(tq * 1e3, 3), "linear_ms": round(tl * 1e3, 3), "scaled": False}
+    per["config2"] = {"linear_gbs": round(multi, 4), "quantize_gbs_gate": round(qb / qn / 1e9, 4), "scaled": False,
+                      "note": "one block's 7 linears are the whole config"}
+    down3 = [c for c in wl.config3() if c.N == 4096 and c.M in (2, 32)]
+    c3 = {}
+    for c in down3:
+        tq, tl = lin_time(c)
+        c3[f"M{c.M}"] = {"quantize_ms": round(tq * 1e3, 1), "linear_ms": round(tl * 1e3, 1)}
+    per["config3_down_g64"] = dict(c3, scaled=False, note="the other M and the up shape scale with M*N*K")
+    c4 = wl.config4()[0]
+    tq, tl = lin_time(c4, rows=64)
+    per["config4_gate_g32"] = {"quantize_ms": round(tq * 1e3, 1), "linear_ms_64_tokens": round(tl * 1e3, 1),
+                               "linear_s_extrapolated_M2048": round(tl * 2048 / 64, 1),
+                               "linear_s_extrapolated_M8192": round(tl * 8192 / 64, 1), "scaled": True,
+                               "note": "64 of the tokens timed; the full M extrapolated linearly (labelled)"}
+    c5 = wl.config5(1)[:7]  # one block at g=128
+    tq5 = tl5 = 0.0
+    for c in c5:
+        a, b = lin_time(c)
+        tq5 += a
+        tl5 += b
+    per["config5_g128"] = {"quantize_s_one_block": round(tq5, 2), "linear_M1_s_one_block": round(tl5, 2),
+                           "quantize_s_extrapolated_32_blocks": round(32 * tq5, 1),
+                           "linear_M1_s_extrapolated_32_blocks": round(32 * tl5, 1), "scaled": True,
+                           "note": "one of the 32 blocks timed, the stack extrapolated x32 (labelled)"}
+    oracle.set_threads(1)
+    return {"value": round(multi, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{pn} pass(es) of the 7 M=1 g=32 decode linears of one Llama-3-8B block on {cores} "
+                      f"threads ({tn:.1f} s; plain C, fp64 accumulation, OpenMP over output rows)",
+            "single_thread": {"value": round(single, 4), "unit": "GB/s", "cores": 1,
+                              "sample": f"{p1} pass(es) of the same 7 linears ({t1:.1f} s)"},
+            "quantize": {"unit": "GB/s", "shape": [gate.N, gate.K], "group_size": 32,
+                         "single_thread": round(qb / q1 / 1e9, 4), "all_cores": round(qb / qn / 1e9, 4),
+                         "cores": cores},
+            "per_config": per, "host_cores_available": os.cpu_count()}
 
 
 def reference_arm(args):
@@ -688,6 +819,7 @@ def reference_arm(args):
     import oracle
     from bit_weight_quantization_02_b300 import workloads as wl
     prepared = _oracle_decode_inputs(wl.config2(0))
+    cores = oracle.set_threads(0)  # every host core (OpenMP over output rows)
 
     def step(i):
         c, X, (Wq, sc, of) = prepared[i % len(prepared)]
@@ -707,9 +839,9 @@ def reference_arm(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded; random-init Llama-3-8B-shaped weights)",
             "config": {"workload": WORKLOAD, "group_size": 32, "M": 1},
-            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                              "sample": "one of the 7 decode linears of a block per step, in turn "
-                                       "(single-threaded C oracle: dequantize + fp64 dot products)"},
+                                       f"(C oracle on {cores} threads: dequantize + fp64 dot products)"},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -724,7 +856,7 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["libw4", "reference"], default="libw4")
     ap.add_argument("--headline-only", action="store_true", help="skip the secondary rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--prefill-iters", type=int, default=10)
     ap.add_argument("--section", choices=["all", "prefill", "shapes", "batched", "widths", "stack", "dequant"],
                     default="all",

@@ -31,7 +31,7 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "w4_oracle.c")
 _LIB = os.path.join(_HERE, "libw4_oracle.so")
-_CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+_CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-fPIC", "-shared"]
 
 _lock = threading.Lock()
 _lib = None
@@ -67,6 +67,8 @@ def _load():
             lib.w4_ref_linear_bits.restype = ctypes.c_int
             lib.w4_ref_eps.argtypes = []
             lib.w4_ref_eps.restype = ctypes.c_float
+            lib.w4_ref_threads.argtypes = [ctypes.c_int]
+            lib.w4_ref_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -80,6 +82,12 @@ def _u16(a) -> np.ndarray:
 
 def _ptr(a: np.ndarray):
     return ctypes.c_void_p(a.ctypes.data)
+
+
+def set_threads(n: int) -> int:
+    """Threads the oracle's row loops use (n <= 0: every core); returns the count in use.
+    Results do not depend on it: each row is computed the same way on any thread."""
+    return _load().w4_ref_threads(int(n))
 
 
 def ref_eps() -> float:

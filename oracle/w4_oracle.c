@@ -9,7 +9,10 @@
  * CUDA library; the only thing both sides share is the seeded input
  * generator, which holds none of the method's arithmetic.
  *
- * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -shared -fPIC.
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -fopenmp -shared -fPIC.
+ * Rows are independent, so the row loops may run on several threads (OpenMP,
+ * w4_ref_threads); each row is still computed sequentially in the order
+ * written, so results do not depend on the thread count.
  * On x86-64 float arithmetic is IEEE binary32 with round-to-nearest-even, and
  * -ffp-contract=off forbids fusing a*b+c, so every float operation below is
  * exactly one correctly rounded IEEE operation.
@@ -44,6 +47,7 @@
 #include <stdlib.h>
 #include <string.h>
 #include <math.h>
+#include <omp.h>
 
 /* reading: the pages say nothing about the clamp; 1e-6 (fp32) keeps the
  * clamp inactive for every non-constant group of realistic weights. */
@@ -131,6 +135,7 @@ int w4_ref_quantize_bits(const uint16_t *W, int64_t N, int64_t K, int g, int bit
     const int per_byte = 8 / bits;
     const int64_t row_bytes = K / per_byte;
     const int64_t groups = K / g;
+#pragma omp parallel for schedule(static)
     for (int64_t n = 0; n < N; ++n) {
         for (int64_t j = 0; j < groups; ++j) {
             const uint16_t *wg = W + n * K + j * g;
@@ -209,6 +214,7 @@ int w4_ref_dequantize_bits(const uint8_t *Wq, const uint16_t *scales,
 {
     if (!ref_group_ok(N, K, g) || !ref_bits_ok(bits))
         return -1;
+#pragma omp parallel for schedule(static)
     for (int64_t n = 0; n < N; ++n)
         for (int64_t k = 0; k < K; ++k)
             W_out[n * K + k] = ref_dequant_one(Wq, scales, offsets, K, g, bits, n, k);
@@ -235,10 +241,14 @@ int w4_ref_linear_bits(const uint16_t *X, int64_t M, int64_t K, const uint8_t *W
 {
     if (!ref_group_ok(N, K, g) || !ref_bits_ok(bits) || M < 0)
         return -1;
-    double *wrow = (double *)malloc((size_t)K * sizeof(double));
-    if (wrow == NULL)
+    /* one dequantized row per thread */
+    const int nt = omp_get_max_threads();
+    double *wbuf = (double *)malloc((size_t)nt * (size_t)K * sizeof(double));
+    if (wbuf == NULL)
         return -2;
+#pragma omp parallel for schedule(static)
     for (int64_t n = 0; n < N; ++n) {
+        double *wrow = wbuf + (size_t)omp_get_thread_num() * (size_t)K;
         for (int64_t k = 0; k < K; ++k)
             wrow[k] = (double)ref_bf16_to_float(
                 ref_dequant_one(Wq, scales, offsets, K, g, bits, n, k));
@@ -249,7 +259,7 @@ int w4_ref_linear_bits(const uint16_t *X, int64_t M, int64_t K, const uint8_t *W
             Y[m * N + n] = acc;
         }
     }
-    free(wrow);
+    free(wbuf);
     return 0;
 }
 
@@ -262,3 +272,11 @@ int w4_ref_linear(const uint16_t *X, int64_t M, int64_t K, const uint8_t *Wq,
 
 /* The clamp constant, exported so tests can state which reading they pin. */
 float w4_ref_eps(void) { return REF_EPS; }
+
+/* Threads of the row loops: n > 0 sets n, n <= 0 every core the host offers;
+ * returns the number now in use. */
+int w4_ref_threads(int n)
+{
+    omp_set_num_threads(n > 0 ? n : omp_get_num_procs());
+    return omp_get_max_threads();
+}

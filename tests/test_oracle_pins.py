@@ -503,3 +503,20 @@ def test_bits_linear_one_hot_and_numpy(bits):
     Xr = _bits(workloads.gen_activation(5, K, seed=82))
     np.testing.assert_allclose(oracle.ref_linear(Xr, Wq, sc, of, g, bits=bits), bits_f64(Xr) @ Wd.T,
                                rtol=1e-12, atol=1e-12)
+
+
+def test_results_do_not_depend_on_the_thread_count():
+    """The oracle's row loops may run on several threads: each row is computed the
+    same way on any of them, so codes, qparams and the fp64 products are identical."""
+    import torch
+    from bit_weight_quantization_02_b300 import workloads as wl
+    W = wl.gen_weight(300, 1024, seed=17, outliers=True).view(torch.int16).numpy().view(np.uint16)
+    X = wl.gen_activation(3, 1024, seed=18).view(torch.int16).numpy().view(np.uint16)
+    results = []
+    for n in (1, 0):
+        oracle.set_threads(n)
+        q = oracle.ref_quantize(W, 64)
+        results.append((q, oracle.ref_dequantize(*q, 64), oracle.ref_linear(X, *q, 64)))
+    (qa, da, ya), (qb, db, yb) = results
+    assert all(np.array_equal(a, b) for a, b in zip(qa, qb))
+    assert np.array_equal(da, db) and np.array_equal(ya, yb)
