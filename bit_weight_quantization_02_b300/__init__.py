@@ -22,7 +22,7 @@ __all__ = [
     "w4_linear_repacked",
     "library_path", "load_library", "w4_quantize", "w4_dequantize", "w4_linear",
     "w4_linear_ex", "w4_packed_bytes", "w4_qparam_bytes", "w4_device_fault", "w4_format_version",
-    "w4_linear_static", "w4_packed_bytes_bits", "w4_quantize_bits", "w4_dequantize_bits", "w4_linear_bits",
+    "w4_linear_static", "w4_linear_bias", "w4_packed_bytes_bits", "w4_quantize_bits", "w4_dequantize_bits", "w4_linear_bits",
 ]
 
 W4_FORMAT_VERSION = 1
@@ -78,6 +78,8 @@ def load_library():
             "w4_dequantize_bits": ([p, p, p, i64, i64, i32, i32, p, p], i32),
             "w4_linear_bits": ([p, i64, i64, p, p, p, i64, i32, i32, p, p, sz, p], i32),
             "w4_selftest_bounded_waits": ([p, sz, p, ctypes.c_uint64, p], i32),
+            "w4_linear_bias": ([p, i64, i64, p, p, p, i64, i32, p, p, p, sz, p], i32),
+            "w4_linear_bias_ex": ([p, i64, i64, p, p, p, i64, i32, p, p, p, sz, i32, p], i32),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -260,6 +262,25 @@ def w4_linear_ex(X: torch.Tensor, Wq: torch.Tensor, scales: torch.Tensor, offset
     ws = _workspace_for(X, M, N, K, group_size, workspace)
     _check(lib.w4_linear_ex(_ptr(X), M, K, _ptr(Wq), _ptr(scales), _ptr(offsets), N, group_size, _ptr(Y),
                             _ptr(ws.buf), ws.nbytes, kernel, _stream(X)), "w4_linear")
+    return Y
+
+
+def w4_linear_bias(X: torch.Tensor, Wq: torch.Tensor, scales: torch.Tensor, offsets: torch.Tensor,
+                   group_size: int, bias: torch.Tensor | None, kernel: int = KERNEL_AUTO, out=None,
+                   workspace: Workspace | None = None):
+    """Y bf16 [M,N] = X . dequant(Wq)^T + bias (bf16 [N], added in fp32 before the rounding; None: no bias)."""
+    lib = load_library()
+    _bits16(X, "X")
+    M, K = X.shape
+    N = Wq.shape[0]
+    if bias is not None:
+        _bits16(bias, "bias")
+        if bias.numel() != N:
+            raise ValueError("bias must hold N values")
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    ws = _workspace_for(X, M, N, K, group_size, workspace)
+    _check(lib.w4_linear_bias_ex(_ptr(X), M, K, _ptr(Wq), _ptr(scales), _ptr(offsets), N, group_size, _ptr(bias),
+                                 _ptr(Y), _ptr(ws.buf), ws.nbytes, kernel, _stream(X)), "w4_linear_bias")
     return Y
 
 

@@ -87,9 +87,14 @@ size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int group_size
     return 0;
 }
 
-w4_status w4_linear_ex(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
-                       const uint16_t* offsets, int64_t N, int group_size, uint16_t* Y, void* workspace,
-                       size_t workspace_bytes, w4_kernel kernel, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The linear with an optional bias (null: none): argument checks, kernel choice, launch.
+w4_status linear_impl(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
+                      const uint16_t* offsets, int64_t N, int group_size, const uint16_t* bias, uint16_t* Y,
+                      void* workspace, size_t workspace_bytes, w4_kernel kernel, void* stream) {
     W4_TRY(check_shape(N, K, group_size));
     if (M < 0) return fail(W4_ERR_INVALID_ARG, "M = %lld must not be negative", (long long)M);
     if (M > 0x7FFFFFFFLL) return fail(W4_ERR_INVALID_ARG, "M must be below 2^31");
@@ -105,6 +110,8 @@ w4_status w4_linear_ex(const uint16_t* X, int64_t M, int64_t K, const uint8_t* W
     W4_TRY(check_ptr(scales, "scales"));
     W4_TRY(check_ptr(offsets, "offsets"));
     W4_TRY(check_ptr(Y, "Y"));
+    if (bias != nullptr && (reinterpret_cast<uintptr_t>(bias) & 1u))
+        return fail(W4_ERR_MISALIGNED, "bias is not 2-byte aligned");
     if (workspace == nullptr) workspace_bytes = 0;
     if (workspace_bytes > 0 && !aligned16(workspace)) return fail(W4_ERR_MISALIGNED, "workspace is not 16-byte aligned");
 
@@ -121,7 +128,7 @@ w4_status w4_linear_ex(const uint16_t* X, int64_t M, int64_t K, const uint8_t* W
             return fail(W4_ERR_INVALID_ARG,
                         "the pair kernel takes M == 1, K <= 16384 and K / group_size a multiple of 8");
         if (can) {
-            e = w4::launch_pair(pp, X, K, Wq, scales, offsets, N, group_size, Y, (cudaStream_t)stream, &detail);
+            e = w4::launch_pair(pp, X, K, Wq, scales, offsets, N, group_size, Y, (cudaStream_t)stream, &detail, bias);
             if (e != cudaSuccess) return fail(W4_ERR_CUDA, "pair linear: %s %s", cudaGetErrorString(e), detail);
             return W4_OK;
         }
@@ -136,7 +143,7 @@ w4_status w4_linear_ex(const uint16_t* X, int64_t M, int64_t K, const uint8_t* W
                         w4_linear_workspace_bytes(M, N, K, group_size));
         if (can) {
             e = w4::launch_stream(sp, X, M, K, Wq, scales, offsets, N, group_size, Y, workspace, (cudaStream_t)stream,
-                                  &detail);
+                                  &detail, bias);
             if (e != cudaSuccess) return fail(W4_ERR_CUDA, "stream linear: %s %s", cudaGetErrorString(e), detail);
             return W4_OK;
         }
@@ -146,15 +153,41 @@ w4_status w4_linear_ex(const uint16_t* X, int64_t M, int64_t K, const uint8_t* W
                                                M <= w4::SKINNY_MAX_M)) {
         w4::SkinnyPlan plan;
         if (w4::plan_skinny(M, N, K, group_size, &plan)) {
-            e = w4::launch_skinny(plan, X, M, K, Wq, scales, offsets, N, group_size, Y, (cudaStream_t)stream, &detail);
+            e = w4::launch_skinny(plan, X, M, K, Wq, scales, offsets, N, group_size, Y, (cudaStream_t)stream, &detail,
+                                  bias);
             if (e != cudaSuccess) return fail(W4_ERR_CUDA, "skinny linear: %s %s", cudaGetErrorString(e), detail);
             return W4_OK;
         }
         if (kernel != W4_KERNEL_AUTO) return fail(W4_ERR_INVALID_ARG, "no skinny launch plan for this shape");
     }
-    e = w4::launch_gemm(X, M, K, Wq, scales, offsets, N, group_size, 4, Y, (cudaStream_t)stream, &detail);
+    e = w4::launch_gemm(X, M, K, Wq, scales, offsets, N, group_size, 4, Y, (cudaStream_t)stream, &detail, bias);
     if (e != cudaSuccess) return fail(W4_ERR_CUDA, "tensor-core linear: %s %s", cudaGetErrorString(e), detail);
     return W4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+w4_status w4_linear_ex(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
+                       const uint16_t* offsets, int64_t N, int group_size, uint16_t* Y, void* workspace,
+                       size_t workspace_bytes, w4_kernel kernel, void* stream) {
+    return linear_impl(X, M, K, Wq, scales, offsets, N, group_size, nullptr, Y, workspace, workspace_bytes, kernel,
+                       stream);
+}
+
+w4_status w4_linear_bias_ex(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
+                            const uint16_t* offsets, int64_t N, int group_size, const uint16_t* bias, uint16_t* Y,
+                            void* workspace, size_t workspace_bytes, w4_kernel kernel, void* stream) {
+    return linear_impl(X, M, K, Wq, scales, offsets, N, group_size, bias, Y, workspace, workspace_bytes, kernel,
+                       stream);
+}
+
+w4_status w4_linear_bias(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
+                         const uint16_t* offsets, int64_t N, int group_size, const uint16_t* bias, uint16_t* Y,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+    return linear_impl(X, M, K, Wq, scales, offsets, N, group_size, bias, Y, workspace, workspace_bytes,
+                       W4_KERNEL_AUTO, stream);
 }
 
 w4_status w4_linear(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,

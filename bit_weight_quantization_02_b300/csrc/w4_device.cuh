@@ -48,6 +48,12 @@ __device__ __forceinline__ uint32_t ldg_nc_u32(const void* p) {
     return v;
 }
 
+// The bias of output row n in fp32 (bf16 bits; no bias when b is null), added to
+// the fp32 sum before the one rounding to bf16.
+__device__ __forceinline__ float bias_f32(const uint16_t* b, int64_t n) {
+    return b ? bf16_bits_to_float(ldg_nc_u16(b + n)) : 0.f;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
 }
@@ -258,7 +264,8 @@ __device__ __forceinline__ void split_publish(uint64_t* slot, const float (&acc)
 // The owner's part, after its own sums are in the warp's scratch (16 M floats
 // of shared memory, element m * 16 + r): the slots of warps worker + 1 .. wl
 // (warp c's words at ws + c * stride),
-// then bf16 Y of the tile (Yt = first column of the tile, ldy = N).  The
+// then bf16 Y of the tile (Yt = first column of the tile, ldy = N; bias_t, when
+// given, the bias of the tile's first row, added in fp32 before the rounding).  The
 // owner's shared tile is the last of its range, so the kernels call this after
 // their main loop, when the loop's registers are free.  Each lane takes
 // elements lane, lane + 32, ... (NE of them, at most NEMAX; with one token,
@@ -269,7 +276,8 @@ template <int NEMAX>
 __device__ __forceinline__ bool split_sum_shares(const float* scr, uint64_t* ws, size_t stride, int worker, int wl,
                                                  int M,
                                                  int nrows, int lane, uint16_t* Yt, int64_t ldy,
-                                                 unsigned int* fault_word, unsigned int code, uint64_t limit_ns) {
+                                                 unsigned int* fault_word, unsigned int code, uint64_t limit_ns,
+                                                 const uint16_t* bias_t = nullptr) {
     constexpr int BC = NEMAX >= 8 ? 1 : 8 / NEMAX;  // sharers per batch (8 words per lane, 16 for NEMAX 16)
     bool ok = true;
     const int E = 16 * M;          // words per slot
@@ -330,7 +338,7 @@ __device__ __forceinline__ bool split_sum_shares(const float* scr, uint64_t* ws,
     for (int i = 0; i < NEMAX; ++i) {
         const int e = e0 + 32 * i;
         if (sub == 0 && e < E && (e & 15) < nrows)
-            Yt[(int64_t)(e >> 4) * ldy + (e & 15)] = (uint16_t)float_to_bf16_bits(sum[i]);
+            Yt[(int64_t)(e >> 4) * ldy + (e & 15)] = (uint16_t)float_to_bf16_bits(sum[i] + bias_f32(bias_t, e & 15));
     }
     return ok;
 }
@@ -341,7 +349,7 @@ __device__ __forceinline__ bool split_collect(const float (&acc)[MT][4], float* 
                                               int worker, int wl,
                                               int M, int nrows, int row_a, int tq, int lane, uint16_t* Yt,
                                               int64_t ldy, unsigned int* fault_word, unsigned int code,
-                                              uint64_t limit_ns) {
+                                              uint64_t limit_ns, const uint16_t* bias_t = nullptr) {
 #pragma unroll
     for (int t = 0; t < MT; ++t)
 #pragma unroll
@@ -351,7 +359,7 @@ __device__ __forceinline__ bool split_collect(const float (&acc)[MT][4], float* 
         }
     __syncwarp();
     const bool ok =
-        split_sum_shares<NEMAX>(scr, ws, stride, worker, wl, M, nrows, lane, Yt, ldy, fault_word, code, limit_ns);
+        split_sum_shares<NEMAX>(scr, ws, stride, worker, wl, M, nrows, lane, Yt, ldy, fault_word, code, limit_ns, bias_t);
     __syncwarp();
     return ok;
 }

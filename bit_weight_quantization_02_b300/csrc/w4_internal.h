@@ -30,7 +30,7 @@ constexpr int SKINNY_MAX_M = 32;
 bool plan_skinny(int64_t M, int64_t N, int64_t K, int g, SkinnyPlan* plan);
 cudaError_t launch_skinny(const SkinnyPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
                           const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
-                          cudaStream_t stream, const char** detail);
+                          cudaStream_t stream, const char** detail, const uint16_t* bias = nullptr);
 
 // Persistent stream-K decode kernel (M <= 4; launch_stream hands 5 <= M <= 32
 // to launch_batch with the same plan): needs a zero-initialized,
@@ -45,15 +45,16 @@ struct StreamPlan {
 constexpr int STREAM_MAX_M = 32;
 constexpr int DECODE_MAX_M = 32;  // decode-layout kernel
 bool plan_stream(int64_t M, int64_t N, int64_t K, int g, StreamPlan* plan);
+// bias: [N] bf16 added in fp32 before the one rounding of Y, or null (every linear launcher).
 cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
                           const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
-                          void* workspace, cudaStream_t stream, const char** detail);
+                          void* workspace, cudaStream_t stream, const char** detail, const uint16_t* bias = nullptr);
 cudaError_t read_and_clear_stream_fault(unsigned int* fault);
 // Batched decode (5 <= M <= 32): 64-row units, the block's X slice staged once
 // by TMA; same plan and workspace as the stream kernel (launch_stream calls it).
 cudaError_t launch_batch(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
                          const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, int bits, uint16_t* Y,
-                         void* workspace, cudaStream_t stream, const char** detail);
+                         void* workspace, cudaStream_t stream, const char** detail, const uint16_t* bias = nullptr);
 cudaError_t read_and_clear_batch_fault(unsigned int* fault);
 
 // Decode layout (see w4.h): bytes of one 16-row x 256-k unit, of the whole
@@ -83,7 +84,7 @@ struct PairPlan {
 bool plan_pair(int64_t M, int64_t N, int64_t K, int g, PairPlan* plan);
 cudaError_t launch_pair(const PairPlan& plan, const uint16_t* X, int64_t K, const uint8_t* Wq, const uint16_t* scales,
                         const uint16_t* offsets, int64_t N, int g, uint16_t* Y, cudaStream_t stream,
-                        const char** detail);
+                        const char** detail, const uint16_t* bias = nullptr);
 cudaError_t read_and_clear_pair_fault(unsigned int* fault);
 cudaError_t read_and_clear_selftest_fault(unsigned int* fault);  // w4_selftest.cu
 
@@ -94,7 +95,7 @@ cudaError_t resident_blocks(const void* kernel, int threads, size_t smem, int* s
 // tcgen05 tensor-core GEMM (any M).
 cudaError_t launch_gemm(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
                         const uint16_t* offsets, int64_t N, int g, int bits, uint16_t* Y, cudaStream_t stream,
-                        const char** detail);
+                        const char** detail, const uint16_t* bias = nullptr);
 // Read and clear the kernels' device fault words (bounded-wait timeouts); the
 // caller has synchronized the stream.
 cudaError_t read_and_clear_gemm_fault(unsigned int* fault);

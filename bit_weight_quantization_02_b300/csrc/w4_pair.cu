@@ -64,6 +64,7 @@ constexpr int PK_MAX_CLUSTERS = 128;
 struct PairArgs {
     const uint16_t* X;
     uint16_t* Y;
+    const uint16_t* bias;  // [N] bf16 added before the rounding, or null
     int N, K;
     int nks;        // 512-k stages per row
     int nclusters;  // gridDim.x / 2
@@ -517,7 +518,7 @@ __global__ void __launch_bounds__(PK_THREADS, 2) pair_kernel(const __grid_consta
         if (mine) {
             const float other = got ? recv[(ps & 1) * PK_PASS + i] : 0.f;
             const float y = rank == 0 ? sv + other : other + sv;  // block 0's sum first, on either block
-            p.Y[row] = (uint16_t)float_to_bf16_bits(y);
+            p.Y[row] = (uint16_t)float_to_bf16_bits(y + bias_f32(p.bias, row));
         }
         if (!got) *abort_flag = 1;
         named_bar_sync(1, PK_CW * 32);
@@ -582,7 +583,7 @@ static cudaError_t launch_pair_g(const PairMaps& maps, PairArgs a, size_t smem, 
 
 cudaError_t launch_pair(const PairPlan& plan, const uint16_t* X, int64_t K, const uint8_t* Wq, const uint16_t* scales,
                         const uint16_t* offsets, int64_t N, int g, uint16_t* Y, cudaStream_t stream,
-                        const char** detail) {
+                        const char** detail, const uint16_t* bias) {
     PairMaps maps;
     const int64_t ng = K / g;
     cudaError_t e = cudaSuccess;
@@ -603,6 +604,7 @@ cudaError_t launch_pair(const PairPlan& plan, const uint16_t* X, int64_t K, cons
     PairArgs a;
     a.X = X;
     a.Y = Y;
+    a.bias = bias;
     a.N = (int)N;
     a.K = (int)K;
     a.nks = plan.nks;

@@ -78,6 +78,7 @@ struct SkinnyArgs {
     const uint16_t* scales;   // used by the plain-load qparam path only
     const uint16_t* offsets;
     uint16_t* Y;
+    const uint16_t* bias;  // [N] bf16 added before the rounding, or null
     int M, N, K;
     int ks;      // k per slice (multiple of 256)
     int kc;      // k per staged X sub-chunk (multiple of 256, divides ks)
@@ -294,7 +295,8 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             for (int i = 0; i < 4; ++i) {
                 const int m = 8 * t + 2 * tq + (i & 1);
                 const int n = row0 + ra + ((i < 2) ? 0 : 8);
-                if (m < p.M && n < p.N) p.Y[(int64_t)m * p.N + n] = (uint16_t)float_to_bf16_bits(acc[t][i]);
+                if (m < p.M && n < p.N)
+                    p.Y[(int64_t)m * p.N + n] = (uint16_t)float_to_bf16_bits(acc[t][i] + bias_f32(p.bias, n));
             }
         }
     } else {
@@ -318,7 +320,7 @@ skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
             for (int q = 0; q < p.splits; ++q) sum += cluster.map_shared_rank(part, q)[idx];
             const int m = idx / SKINNY_ROWS, r = idx % SKINNY_ROWS;
             const int n = row0 + r;
-            if (n < p.N) p.Y[(int64_t)m * p.N + n] = (uint16_t)float_to_bf16_bits(sum);
+            if (n < p.N) p.Y[(int64_t)m * p.N + n] = (uint16_t)float_to_bf16_bits(sum + bias_f32(p.bias, n));
         }
         cluster.sync();  // no block leaves while its partials may still be read
     }
@@ -400,7 +402,7 @@ static cudaError_t launch_g(const SkinnyPlan& plan, const CUtensorMap& tw, const
 
 cudaError_t launch_skinny(const SkinnyPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
                           const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
-                          cudaStream_t stream, const char** detail) {
+                          cudaStream_t stream, const char** detail, const uint16_t* bias) {
     // codes: [N][K/2] bytes, one box = 64 rows x 128 bytes (256 k), 128-byte swizzle
     CUtensorMap tw, ts, to;
     cudaError_t e = encode_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)(K / 2), (uint64_t)N,
@@ -422,6 +424,7 @@ cudaError_t launch_skinny(const SkinnyPlan& plan, const uint16_t* X, int64_t M, 
     a.scales = scales;
     a.offsets = offsets;
     a.Y = Y;
+    a.bias = bias;
     a.M = (int)M;
     a.N = (int)N;
     a.K = (int)K;

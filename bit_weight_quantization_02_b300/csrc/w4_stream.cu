@@ -60,6 +60,7 @@ struct StreamArgs {
     const uint16_t* scales;
     const uint16_t* offsets;
     uint16_t* Y;
+    const uint16_t* bias;  // [N] bf16 added before the rounding, or null
     uint64_t* ws;          // split-tile slots, one per warp (split_ws_bytes), zero between calls
     int M, N, K;
     int nkc;               // units per row tile = ceil(K / 256)
@@ -497,8 +498,10 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
 #pragma unroll
                 for (int rt = 0; rt < RT; ++rt) {
                     const int n_a = tile * ROWS + 16 * rt + pr, n_b = n_a + 8;
-                    if (tq == 0 && n_a < p.N) p.Y[n_a] = (uint16_t)float_to_bf16_bits(racc[rt][0][0]);
-                    if (tq == 0 && n_b < p.N) p.Y[n_b] = (uint16_t)float_to_bf16_bits(racc[rt][0][2]);
+                    if (tq == 0 && n_a < p.N)
+                        p.Y[n_a] = (uint16_t)float_to_bf16_bits(racc[rt][0][0] + bias_f32(p.bias, n_a));
+                    if (tq == 0 && n_b < p.N)
+                        p.Y[n_b] = (uint16_t)float_to_bf16_bits(racc[rt][0][2] + bias_f32(p.bias, n_b));
                 }
             } else if (kc_first != 0) {  // a later share of the tile (the first of this range): publish it
 #pragma unroll
@@ -523,7 +526,8 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int m = 8 * t + 2 * tq + (i & 1), n = (i < 2) ? n_a : n_b;
-                        if (m < p.M && n < p.N) p.Y[(int64_t)m * p.N + n] = (uint16_t)float_to_bf16_bits(acc[t][i]);
+                        if (m < p.M && n < p.N)
+                            p.Y[(int64_t)m * p.N + n] = (uint16_t)float_to_bf16_bits(acc[t][i] + bias_f32(p.bias, n));
                     }
             } else if (kc_first != 0) {  // a later share of the tile (the first of this range): publish it
                 split_publish<MT>(p.ws + (size_t)worker * 16 * p.M, acc, p.M, min(16, p.N - tile * 16), pr, tq);
@@ -546,12 +550,12 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 ok = split_collect<1, NE>(oacc[rt], scr + rt * 16, p.ws + rt * 16, (size_t)RT * 16, worker, wl, 1,
                                           min(16, p.N - (tile * ROWS + 16 * rt)), pr, tq, lane,
                                           p.Y + (int64_t)tile * ROWS + 16 * rt, p.N, &g_stream_fault, 2u,
-                                          ST_WAIT_LIMIT_NS) &&
+                                          ST_WAIT_LIMIT_NS, p.bias ? p.bias + tile * ROWS + 16 * rt : nullptr) &&
                      ok;
         } else {
             ok = split_collect<MT, NE>(acc, scr, p.ws, (size_t)16 * p.M, worker, wl, p.M, min(16, p.N - tile * 16), pr,
                                        tq, lane, p.Y + (int64_t)tile * 16, p.N, &g_stream_fault, 2u,
-                                       ST_WAIT_LIMIT_NS) &&
+                                       ST_WAIT_LIMIT_NS, p.bias ? p.bias + tile * 16 : nullptr) &&
                  ok;
         }
     }
@@ -632,9 +636,9 @@ static cudaError_t two_row_tiles(int64_t N, int nkc, size_t ws_bytes, bool* two)
 
 cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
                           const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
-                          void* workspace, cudaStream_t stream, const char** detail) {
+                          void* workspace, cudaStream_t stream, const char** detail, const uint16_t* bias) {
     if (M > 4)  // 5..32 tokens: the block-shared X kernel (w4_batch.cu)
-        return launch_batch(plan, X, M, K, Wq, scales, offsets, N, g, 4, Y, workspace, stream, detail);
+        return launch_batch(plan, X, M, K, Wq, scales, offsets, N, g, 4, Y, workspace, stream, detail, bias);
     const int64_t ng = K / g;
     const bool qt = (g == 32) && (ng % 8 == 0);  // qparam rows 16-byte aligned: 8-group TMA boxes
     cudaError_t e = cudaSuccess;
@@ -667,6 +671,7 @@ cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, 
     a.scales = scales;
     a.offsets = offsets;
     a.Y = Y;
+    a.bias = bias;
     a.ws = static_cast<uint64_t*>(workspace);
     a.M = (int)M;
     a.N = (int)N;

@@ -15,7 +15,7 @@
  *  - groups run along the first axis, the output features (Optimum Quanto,
  *    "Design overview / Modules"), so for W[N,K] a group is g consecutive k
  *    of one output row n;
- *  - bias is not quantized (same section); this ABI has no bias argument;
+ *  - bias is not quantized (same section): w4_linear_bias adds it in fp32;
  *  - the matmul result is accumulated at higher precision than its inputs
  *    (Optimum Quanto, "Pitfalls when quantizing activations"); bf16 x int4
  *    matmuls are accelerated on CUDA (Optimum Quanto, feature list).
@@ -182,6 +182,26 @@ W4_API w4_status w4_linear_ex(const uint16_t *X, int64_t M, int64_t K,
                               const uint16_t *offsets, int64_t N, int group_size,
                               uint16_t *Y, void *workspace, size_t workspace_bytes,
                               w4_kernel kernel, void *stream);
+
+/*
+ * w4_linear_bias -- w4_linear with the layer's bias: Y[m,n] = bf16(sum_k
+ * X[m,k] w'[n,k] + bias[n]), the bias added to the fp32 sum before the one
+ * rounding to bf16.  Source: Optimum Quanto, "Design overview / Modules": a
+ * quantized module quantizes its weights, and its bias is not quantized (it
+ * stays in float).  bias: [N] bf16 (bit patterns), a device pointer, 2-byte
+ * aligned; NULL gives exactly w4_linear.  Kernel choice, workspace rules,
+ * accuracy contract (with y_ref = sum_k X[m,k] W'[n,k] + bias[n] in fp64) and
+ * errors as w4_linear / w4_linear_ex (W4_ERR_MISALIGNED for an odd bias
+ * address).
+ */
+W4_API w4_status w4_linear_bias(const uint16_t *X, int64_t M, int64_t K, const uint8_t *Wq,
+                                const uint16_t *scales, const uint16_t *offsets, int64_t N,
+                                int group_size, const uint16_t *bias, uint16_t *Y, void *workspace,
+                                size_t workspace_bytes, void *stream);
+W4_API w4_status w4_linear_bias_ex(const uint16_t *X, int64_t M, int64_t K, const uint8_t *Wq,
+                                   const uint16_t *scales, const uint16_t *offsets, int64_t N,
+                                   int group_size, const uint16_t *bias, uint16_t *Y, void *workspace,
+                                   size_t workspace_bytes, w4_kernel kernel, void *stream);
 
 /* Sizes of the packed outputs: N*K/2 bytes of codes, N*(K/g)*2 bytes for each
  * of scales and offsets.  0 for invalid arguments. */

@@ -67,6 +67,8 @@ def _load():
             lib.w4_ref_linear_bits.restype = ctypes.c_int
             lib.w4_ref_eps.argtypes = []
             lib.w4_ref_eps.restype = ctypes.c_float
+            lib.w4_ref_linear_bias_bits.argtypes = [p, i64, i64, p, p, p, i64, ctypes.c_int, ctypes.c_int, p, p]
+            lib.w4_ref_linear_bias_bits.restype = ctypes.c_int
             lib.w4_ref_threads.argtypes = [ctypes.c_int]
             lib.w4_ref_threads.restype = ctypes.c_int
             _lib = lib
@@ -132,8 +134,8 @@ def ref_dequantize(Wq: np.ndarray, scales: np.ndarray, offsets: np.ndarray, grou
 
 
 def ref_linear(X: np.ndarray, Wq: np.ndarray, scales: np.ndarray, offsets: np.ndarray,
-               group_size: int, bits: int = 4) -> np.ndarray:
-    """X uint16 [M,K] bf16 bits, packed weights of [N,K] -> fp64 [M,N] = X . W'^T."""
+               group_size: int, bits: int = 4, bias: np.ndarray | None = None) -> np.ndarray:
+    """X uint16 [M,K] bf16 bits, packed weights of [N,K] -> fp64 [M,N] = X . W'^T (+ bias [N], bf16 bits)."""
     per_byte = _check_bits(bits)
     X = _u16(X)
     Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
@@ -143,10 +145,17 @@ def ref_linear(X: np.ndarray, Wq: np.ndarray, scales: np.ndarray, offsets: np.nd
     if Wq.shape[1] * per_byte != K:
         raise ValueError("X and Wq disagree on K")
     Y = np.zeros((M, N), np.float64)
-    rc = _load().w4_ref_linear_bits(_ptr(X), M, K, _ptr(Wq), _ptr(scales), _ptr(offsets), N, group_size, bits,
-                                    _ptr(Y))
+    if bias is not None:
+        bias = _u16(bias)
+        if bias.shape != (N,):
+            raise ValueError("bias must hold N values")
+        rc = _load().w4_ref_linear_bias_bits(_ptr(X), M, K, _ptr(Wq), _ptr(scales), _ptr(offsets), N, group_size,
+                                             bits, _ptr(bias), _ptr(Y))
+    else:
+        rc = _load().w4_ref_linear_bits(_ptr(X), M, K, _ptr(Wq), _ptr(scales), _ptr(offsets), N, group_size, bits,
+                                        _ptr(Y))
     if rc:
-        raise RuntimeError(f"w4_ref_linear_bits failed: {rc}")
+        raise RuntimeError(f"w4_ref_linear failed: {rc}")
     return Y
 
 

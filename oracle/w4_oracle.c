@@ -263,6 +263,25 @@ int w4_ref_linear_bits(const uint16_t *X, int64_t M, int64_t K, const uint8_t *W
     return 0;
 }
 
+/*
+ * The linear with the layer's bias: Y[m,n] = sum_k X[m,k] W'[n,k] + bias[n]
+ * in fp64.  Optimum Quanto, "Design overview / Modules": the bias of a
+ * quantized module is not quantized, so it enters in float (bf16 here, widened
+ * exactly) on top of the product.
+ */
+int w4_ref_linear_bias_bits(const uint16_t *X, int64_t M, int64_t K, const uint8_t *Wq,
+                            const uint16_t *scales, const uint16_t *offsets, int64_t N,
+                            int g, int bits, const uint16_t *bias, double *Y)
+{
+    int rc = w4_ref_linear_bits(X, M, K, Wq, scales, offsets, N, g, bits, Y);
+    if (rc != 0)
+        return rc;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            Y[m * N + n] += (double)ref_bf16_to_float(bias[n]);
+    return 0;
+}
+
 int w4_ref_linear(const uint16_t *X, int64_t M, int64_t K, const uint8_t *Wq,
                   const uint16_t *scales, const uint16_t *offsets, int64_t N,
                   int g, double *Y)

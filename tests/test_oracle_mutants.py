@@ -34,6 +34,9 @@ MUTANTS = {
     "bf16_truncates": ("upper += 1u;", "upper += 0u;"),
     "zero_order_ignored": ("return signbit(a) && !signbit(b);", "return 0;"),
     "scale_not_rounded_to_bf16": ("float s = ref_bf16_to_float(s_bits);", "float s = s32;"),
+    "bias_dropped": ("Y[m * N + n] += (double)ref_bf16_to_float(bias[n]);", ""),
+    "bias_of_the_token": ("Y[m * N + n] += (double)ref_bf16_to_float(bias[n]);",
+                          "Y[m * N + n] += (double)ref_bf16_to_float(bias[m]);"),
 }
 
 
@@ -44,13 +47,18 @@ def _build_mutant(tmp_path, name):
     c = tmp_path / f"{name}.c"
     c.write_text(src.replace(old, new))
     so = tmp_path / f"{name}.so"
-    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+    return _compile(c, so)
+
+
+def _compile(c, so):
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-fPIC", "-shared",
                     "-o", str(so), str(c), "-lm"], check=True)
     lib = ctypes.CDLL(str(so))
     p, i64 = ctypes.c_void_p, ctypes.c_int64
     lib.w4_ref_quantize.argtypes = [p, i64, i64, ctypes.c_int, p, p, p]
     lib.w4_ref_dequantize.argtypes = [p, p, p, i64, i64, ctypes.c_int, p]
     lib.w4_ref_linear.argtypes = [p, i64, i64, p, p, p, i64, ctypes.c_int, p]
+    lib.w4_ref_linear_bias_bits.argtypes = [p, i64, i64, p, p, p, i64, ctypes.c_int, ctypes.c_int, p, p]
     lib.w4_ref_quantize_bits.argtypes = [p, i64, i64, ctypes.c_int, ctypes.c_int, p, p, p]
     lib.w4_ref_dequantize_bits.argtypes = [p, p, p, i64, i64, ctypes.c_int, ctypes.c_int, p]
     return lib
@@ -104,24 +112,23 @@ def _pins_reject(lib) -> bool:
     Y = np.zeros((K, N), np.float64)
     lib.w4_ref_linear(P(X), K, K, P(Wq), P(sc), P(of), N, g, P(Y))
     expect = oracle.bf16_bits_to_f64(case["deq"])
-    return not np.array_equal(Y, np.tile(expect[:, None], (1, N)))
+    if not np.array_equal(Y, np.tile(expect[:, None], (1, N))):
+        return True
+    # the bias closed form: every w' = 0 (codes 0, offsets 0) -> Y[m, n] = bias[n]
+    Wz = np.zeros((N, K // 2), np.uint8)
+    sz = np.full((N, 1), 0x3C00, np.uint16)
+    oz = np.zeros((N, 1), np.uint16)
+    bias = np.array([0x3F80, 0xC000, 0x4049], np.uint16)  # 1, -2, 3.140625
+    Yb = np.zeros((2, N), np.float64)
+    lib.w4_ref_linear_bias_bits(P(X[:2].copy()), 2, K, P(Wz), P(sz), P(oz), N, g, 4, P(bias), P(Yb))
+    return not np.array_equal(Yb, np.tile([1.0, -2.0, 3.140625], (2, 1)))
 
 
 def test_unmutated_oracle_passes(tmp_path):
     src = open(SRC).read()
     c = tmp_path / "clean.c"
     c.write_text(src)
-    so = tmp_path / "clean.so"
-    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
-                    "-o", str(so), str(c), "-lm"], check=True)
-    lib = ctypes.CDLL(str(so))
-    p, i64 = ctypes.c_void_p, ctypes.c_int64
-    lib.w4_ref_quantize.argtypes = [p, i64, i64, ctypes.c_int, p, p, p]
-    lib.w4_ref_dequantize.argtypes = [p, p, p, i64, i64, ctypes.c_int, p]
-    lib.w4_ref_linear.argtypes = [p, i64, i64, p, p, p, i64, ctypes.c_int, p]
-    lib.w4_ref_quantize_bits.argtypes = [p, i64, i64, ctypes.c_int, ctypes.c_int, p, p, p]
-    lib.w4_ref_dequantize_bits.argtypes = [p, p, p, i64, i64, ctypes.c_int, ctypes.c_int, p]
-    assert not _pins_reject(lib)
+    assert not _pins_reject(_compile(c, tmp_path / "clean.so"))
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))

@@ -520,3 +520,40 @@ def test_results_do_not_depend_on_the_thread_count():
     (qa, da, ya), (qb, db, yb) = results
     assert all(np.array_equal(a, b) for a, b in zip(qa, qb))
     assert np.array_equal(da, db) and np.array_equal(ya, yb)
+
+
+# ---------------------------------------------------------------- bias
+
+def test_bias_alone_when_every_weight_is_zero():
+    """Codes 0 with zero offsets make every w' = 0: the linear is the bias, exactly."""
+    N, K, g = 5, 64, 32
+    Wq = np.zeros((N, K // 2), np.uint8)
+    sc = np.full((N, K // g), 0x3C00, np.uint16)  # scale 2^-7, unused (q = 0)
+    of = np.zeros((N, K // g), np.uint16)
+    X = workloads.gen_activation(3, K, seed=5).view(torch.int16).numpy().view(np.uint16)
+    bias = np.array([0x3F80, 0xC000, 0x0000, 0x4049, 0xBE00], np.uint16)  # 1, -2, 0, 3.140625, -0.125
+    y = oracle.ref_linear(X, Wq, sc, of, g, bias=bias)
+    np.testing.assert_array_equal(y, np.tile([1.0, -2.0, 0.0, 3.140625, -0.125], (3, 1)))
+
+
+def test_bias_adds_its_value_to_the_product():
+    """y(bias) - y(no bias) is the bias, up to the one fp64 rounding of the addition; a
+    worked case: X = (1, 2, 0 ...), w' = 2^-7 q with q = (1, 3, 0 ...), bias 0.5 gives
+    1 * 2^-7 + 2 * 3 * 2^-7 + 0.5 = 7/128 + 0.5 = 0.5546875."""
+    W = workloads.gen_weight(64, 256, seed=21, outliers=True).view(torch.int16).numpy().view(np.uint16)
+    X = workloads.gen_activation(4, 256, seed=22).view(torch.int16).numpy().view(np.uint16)
+    q = oracle.ref_quantize(W, 32)
+    bias = workloads.gen_activation(1, 64, seed=23).view(torch.int16).numpy().view(np.uint16)[0]
+    yb = oracle.ref_linear(X, *q, 32, bias=bias)
+    y0 = oracle.ref_linear(X, *q, 32)
+    bf = oracle.bf16_bits_to_f64(bias)
+    np.testing.assert_allclose(yb - y0, np.tile(bf, (4, 1)), rtol=0, atol=4 * np.finfo(np.float64).eps * np.abs(yb).max())
+    # the worked case
+    Wq = np.zeros((1, 16), np.uint8)
+    Wq[0, 0] = 1 | (3 << 4)  # k = 0: q = 1, k = 1: q = 3
+    sc = np.array([[0x3C00]], np.uint16)  # 2^-7
+    of = np.zeros((1, 1), np.uint16)
+    Xw = np.zeros((1, 32), np.uint16)
+    Xw[0, 0], Xw[0, 1] = 0x3F80, 0x4000  # 1, 2
+    y = oracle.ref_linear(Xw, Wq, sc, of, 32, bias=np.array([0x3F00], np.uint16))  # bias 0.5
+    assert y[0, 0] == 7 / 128 + 0.5
