@@ -197,7 +197,7 @@ class LinearStack:
     """Packed weights, inputs and outputs of a sequence of linears, with all X in
     one device buffer and all Y in another (one copy each way per step)."""
 
-    def __init__(self, cases, device, w4, wl, packed=None, layout="canonical", workspace=None):
+    def __init__(self, cases, device, w4, wl, packed=None, layout="canonical", workspace=None, bias=False):
         import torch
         self.cases = cases
         self.device = device
@@ -223,11 +223,21 @@ class LinearStack:
         self.bytes = sum(linear_bytes(c.M, c.N, c.K, c.group_size) for c in cases)
         self.flops = sum(2 * c.M * c.N * c.K for c in cases)
         self.w4 = w4
+        # a bf16 bias per output row of every linear (N(0, 1), seeded by the weight seed), read once
+        # per call: 2N more algorithmic bytes
+        self.bias = ([wl.gen_activation(1, c.N, c.w_seed + 2_000_000, device=device).view(c.N) for c in cases]
+                     if bias else None)
+        if bias:
+            self.bytes += sum(2 * c.N for c in cases)
 
     def run(self):
         if self.repacked is not None:
             for x, y, rp in zip(self.xv, self.yv, self.repacked):
                 self.w4.w4_linear_repacked(x, rp, out=y, workspace=self.ws)
+            return
+        if self.bias is not None:
+            for c, x, y, (Wq, sc, of), b in zip(self.cases, self.xv, self.yv, self.packed, self.bias):
+                self.w4.w4_linear_bias(x, Wq, sc, of, c.group_size, b, out=y, workspace=self.ws)
             return
         for c, x, y, (Wq, sc, of) in zip(self.cases, self.xv, self.yv, self.packed):
             self.w4.w4_linear(x, Wq, sc, of, c.group_size, out=y, workspace=self.ws)
@@ -384,6 +394,21 @@ def gpu_arm(args):
                                       "how": "the headline step with every weight in the decode layout "
                                              "(w4_repack once, untimed), CUDA graph of the 224 calls"}
         del dl_graph, dl
+        # the same step with a bf16 bias on every linear (w4_linear_bias: added to the fp32 sum
+        # in each kernel's epilogue, before the one rounding)
+        bs = LinearStack(cases, device, w4, wl, packed=stack.packed, bias=True)
+        bs_graph = bs.capture(stream)
+        with torch.cuda.stream(stream):
+            bs_ms = time_region(bs_graph.replay, args.steps, args.warmup, stream, dist, device)
+        bs_gbs = replica_gbs(bs.bytes, args.steps, dist.world, bs_ms)
+        rows["decode_step_bias"] = {"unit": "GB/s", "value": round(bs_gbs, 1),
+                                    "ms_per_step": round(bs_ms / args.steps, 4),
+                                    "frac_of_hbm_peak": round(bs_gbs / peaks["hbm_gbs"], 4),
+                                    "time_vs_no_bias": round(bs_ms / ms, 3),
+                                    "kernel": "stream_kernel (w4_linear_bias)",
+                                    "how": "the headline step with a bf16 bias on each of the 224 linears "
+                                           "(2N more bytes a call), CUDA graph"}
+        del bs_graph, bs
         # the same step with the weights that share an input merged row-wise, as serving stacks
         # store them (q|k|v: 6144 x 4096, gate|up: 28672 x 4096): 4 launches per block instead of
         # 7, the same codes, scales and offsets per output row (fresh seeded weights of those shapes)
