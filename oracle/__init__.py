@@ -1,5 +1,6 @@
 """CPU oracle for int4 weight-only quantization and the bf16 x int4 linear
-(and the same affine path with 2- and 8-bit codes).
+(and the same affine path with 2- and 8-bit codes, and the linear on
+dynamically quantized int8 activations).
 
 TEST INFRASTRUCTURE ONLY.  The test-suite, ``__graft_entry__.smoke()`` and
 the CPU-baseline / reference leg of ``bench.py`` are the only callers allowed
@@ -17,7 +18,8 @@ Parity unpinned (a reading both sides implement, with nothing in the pages to
 check it against): the eps value of the scale clamp, the -0.0 < +0.0 order of
 the group minimum, the order of the codes inside a packed byte, and the use of
 the full 2^b - 1 levels of the affine path at 2 and 8 bits (the pages name the
-widths, not their formulas).
+widths, not their formulas), and for int8 activations the symmetric range
++-127, the eps clamp of their scale and the per-token variant.
 """
 from __future__ import annotations
 
@@ -69,6 +71,10 @@ def _load():
             lib.w4_ref_eps.restype = ctypes.c_float
             lib.w4_ref_linear_bias_bits.argtypes = [p, i64, i64, p, p, p, i64, ctypes.c_int, ctypes.c_int, p, p]
             lib.w4_ref_linear_bias_bits.restype = ctypes.c_int
+            lib.w4_ref_quantize_activation_i8.argtypes = [p, i64, i64, ctypes.c_int, p, p]
+            lib.w4_ref_quantize_activation_i8.restype = ctypes.c_int
+            lib.w4_ref_linear_i8.argtypes = [p, p, ctypes.c_int, i64, i64, p, p, p, i64, ctypes.c_int, p, p]
+            lib.w4_ref_linear_i8.restype = ctypes.c_int
             lib.w4_ref_threads.argtypes = [ctypes.c_int]
             lib.w4_ref_threads.restype = ctypes.c_int
             _lib = lib
@@ -156,6 +162,45 @@ def ref_linear(X: np.ndarray, Wq: np.ndarray, scales: np.ndarray, offsets: np.nd
                                         _ptr(Y))
     if rc:
         raise RuntimeError(f"w4_ref_linear failed: {rc}")
+    return Y
+
+
+def ref_quantize_activation_i8(X: np.ndarray, per_token: bool = False):
+    """X uint16 [M,K] bf16 bits -> (Xq int8 [M,K], x_scale float32 [1] per tensor or [M] per token):
+    s_x = max|x| / 127 (eps-clamped), q_x = clamp(rne(x / s_x), -127, 127), fp32."""
+    X = _u16(X)
+    M, K = X.shape
+    Xq = np.zeros((M, K), np.int8)
+    xs = np.zeros((M if per_token else 1,), np.float32)
+    rc = _load().w4_ref_quantize_activation_i8(_ptr(X), M, K, int(bool(per_token)), _ptr(Xq), _ptr(xs))
+    if rc:
+        raise RuntimeError(f"w4_ref_quantize_activation_i8 failed: {rc}")
+    return Xq, xs
+
+
+def ref_linear_i8(Xq: np.ndarray, x_scale: np.ndarray, per_token: bool, Wq: np.ndarray, scales: np.ndarray,
+                  offsets: np.ndarray, group_size: int, bias: np.ndarray | None = None) -> np.ndarray:
+    """int8 codes [M,K] with their scale(s), 4-bit weights of [N,K] -> fp64 [M,N]
+    = s_x * sum_j (s_j I_j + o_j S_j) (+ bias [N], bf16 bits)."""
+    Xq = np.ascontiguousarray(Xq, dtype=np.int8)
+    x_scale = np.ascontiguousarray(x_scale, dtype=np.float32)
+    Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+    scales, offsets = _u16(scales), _u16(offsets)
+    M, K = Xq.shape
+    N = Wq.shape[0]
+    if Wq.shape[1] * 2 != K:
+        raise ValueError("Xq and Wq disagree on K")
+    if x_scale.shape != ((M,) if per_token else (1,)):
+        raise ValueError("x_scale must hold 1 value per tensor or M per token")
+    if bias is not None:
+        bias = _u16(bias)
+        if bias.shape != (N,):
+            raise ValueError("bias must hold N values")
+    Y = np.zeros((M, N), np.float64)
+    rc = _load().w4_ref_linear_i8(_ptr(Xq), _ptr(x_scale), int(bool(per_token)), M, K, _ptr(Wq), _ptr(scales),
+                                  _ptr(offsets), N, group_size, _ptr(bias) if bias is not None else None, _ptr(Y))
+    if rc:
+        raise RuntimeError(f"w4_ref_linear_i8 failed: {rc}")
     return Y
 
 

@@ -33,7 +33,10 @@
  *    Optimum Quanto, "Pitfalls when quantizing activations";
  *  - weights of 2, 4 and 8 bits:  Optimum Quanto, feature list ("int2, int4,
  *    int8 and float8 weights"); int8 weights in groups of 128:  torchao
- *    README, the diffusers example (Int8WeightOnlyConfig, PerGroup(128)).
+ *    README, the diffusers example (Int8WeightOnlyConfig, PerGroup(128));
+ *  - int8 activations quantized at run time beside int4 group-wise weights:
+ *    torchao's Int8DynamicActivationInt4WeightConfig (README, guide); one
+ *    symmetric scale per tensor:  Optimum Quanto, "Design overview / Modules".
  * The concrete formulas (scale = (max-min)/15 with an eps clamp,
  * q = clamp(rne((w-min)/scale), 0, 15), w' = q*scale + min) are the plainest
  * reading consistent with all of the above; the readings of points the pages
@@ -287,6 +290,97 @@ int w4_ref_linear(const uint16_t *X, int64_t M, int64_t K, const uint8_t *Wq,
                   int g, double *Y)
 {
     return w4_ref_linear_bits(X, M, K, Wq, scales, offsets, N, g, 4, Y);
+}
+
+/* ---- int8 dynamic activations x int4 weights ------------------------- */
+
+/*
+ * Dynamic symmetric int8 quantization of the activations X[M,K] (bf16).
+ * torchao README "Training / QAT" and torchao guide (QAT, edge deployment):
+ * Int8DynamicActivationInt4WeightConfig quantizes the activations to int8 at
+ * run time and the weights to int4 in groups.  Optimum Quanto, "Design
+ * overview / Modules" and "Pitfalls when quantizing activations": activations
+ * are quantized per tensor, with a symmetric range (the default [-1, 1]);
+ * the integer mapping rounds half to even (torch.round, "Design overview /
+ * Tensors").
+ * Readings: "dynamic" means the scale comes from the tensor itself at run
+ * time, s_x = a / 127 with a = max |x| (fp32 IEEE division), clamped below at
+ * the weights' eps; the codes are q_x = clamp(rne(x / s_x), -127, 127), so the
+ * largest magnitude codes to +-127 and zero to 0.  The torchao pages leave the
+ * granularity open, so one scale per row of X (per token) is offered beside
+ * Quanto's one scale per tensor.  x_scale gets 1 value (per tensor) or M.
+ */
+int w4_ref_quantize_activation_i8(const uint16_t *X, int64_t M, int64_t K, int per_token,
+                                  int8_t *Xq, float *x_scale)
+{
+    if (M < 0 || K <= 0)
+        return -1;
+    const int64_t nscales = per_token ? M : (M > 0 ? 1 : 0);
+    for (int64_t r = 0; r < nscales; ++r) {
+        const int64_t m0 = per_token ? r : 0, m1 = per_token ? r + 1 : M;
+        float a = 0.0f;
+        for (int64_t m = m0; m < m1; ++m)
+            for (int64_t k = 0; k < K; ++k) {
+                float v = fabsf(ref_bf16_to_float(X[m * K + k]));
+                if (v > a)
+                    a = v;
+            }
+        float s = a / 127.0f;
+        if (s < REF_EPS)
+            s = REF_EPS;
+        x_scale[r] = s;
+        for (int64_t m = m0; m < m1; ++m)
+            for (int64_t k = 0; k < K; ++k) {
+                float t = ref_bf16_to_float(X[m * K + k]) / s;
+                float q = rintf(t);
+                if (q > 127.0f)
+                    q = 127.0f;
+                if (q < -127.0f)
+                    q = -127.0f;
+                Xq[m * K + k] = (int8_t)q;
+            }
+    }
+    return 0;
+}
+
+/*
+ * The linear on int8 activation codes and int4 weight codes:
+ *   Y[m,n] = s_x(m) * sum_j ( s_j * I_j + o_j * S_j ) + bias[n]      (fp64)
+ * with, over the k of group j, I_j = sum q_x[m,k] q[n,k] and S_j = sum q_x[m,k]
+ * accumulated exactly in integers.  This is sum_k (s_x q_x)(q s_j + o_j): the
+ * integer product of the codes, accumulated wider than its inputs and then
+ * brought back to float with the activation scale and each group's scale and
+ * offset, and the float bias added last (Optimum Quanto, "Pitfalls when
+ * quantizing activations").  s_x(m) = x_scale[m] per token, x_scale[0] per
+ * tensor.  bias may be NULL.  Weights: 4-bit codes, the layout of w4_ref_quantize.
+ */
+int w4_ref_linear_i8(const int8_t *Xq, const float *x_scale, int per_token, int64_t M, int64_t K,
+                     const uint8_t *Wq, const uint16_t *scales, const uint16_t *offsets, int64_t N,
+                     int g, const uint16_t *bias, double *Y)
+{
+    if (!ref_group_ok(N, K, g) || M < 0)
+        return -1;
+    const int64_t ng = K / g;
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t m = 0; m < M; ++m) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < ng; ++j) {
+                int64_t I = 0, S = 0;
+                for (int64_t k = j * g; k < (j + 1) * g; ++k) {
+                    int q = (Wq[n * (K / 2) + k / 2] >> ((int)(k % 2) * 4)) & 0xF;
+                    I += (int64_t)Xq[m * K + k] * q;
+                    S += (int64_t)Xq[m * K + k];
+                }
+                acc += (double)ref_bf16_to_float(scales[n * ng + j]) * (double)I
+                     + (double)ref_bf16_to_float(offsets[n * ng + j]) * (double)S;
+            }
+            double y = (double)x_scale[per_token ? m : 0] * acc;
+            if (bias != NULL)
+                y += (double)ref_bf16_to_float(bias[n]);
+            Y[m * N + n] = y;
+        }
+    return 0;
 }
 
 /* The clamp constant, exported so tests can state which reading they pin. */

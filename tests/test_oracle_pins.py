@@ -557,3 +557,180 @@ def test_bias_adds_its_value_to_the_product():
     Xw[0, 0], Xw[0, 1] = 0x3F80, 0x4000  # 1, 2
     y = oracle.ref_linear(Xw, Wq, sc, of, 32, bias=np.array([0x3F00], np.uint16))  # bias 0.5
     assert y[0, 0] == 7 / 128 + 0.5
+
+
+# ---------------------------------------------------------------- int8 activations
+
+GOLDEN_ACT = os.path.join(os.path.dirname(__file__), "golden", "activation_i8_worked_examples.txt")
+
+
+def load_activation_golden(path=GOLDEN_ACT):
+    """Cases of the activation file: name -> {per_token, X uint16 [M,K], scale uint32 [.], codes int8 [M,K]}."""
+    cases, cur = {}, None
+    for raw in open(path):
+        line = raw.split("#", 1)[0].strip()
+        if not line:
+            continue
+        key, *vals = line.split()
+        if key == "case":
+            cur = {"name": vals[0], "rows": [], "codes": []}
+        elif key == "granularity":
+            cur["per_token"] = vals[0] == "token"
+        elif key == "row":
+            cur["rows"].append([int(v, 16) for v in vals])
+        elif key == "scale":
+            cur["scale"] = np.array([int(v, 16) for v in vals], np.uint32)
+        elif key == "codes":
+            cur["codes"].append([int(v) for v in vals])
+        elif key == "end":
+            cases[cur["name"]] = {"per_token": cur["per_token"], "X": np.array(cur["rows"], np.uint16),
+                                  "scale": cur["scale"], "codes": np.array(cur["codes"], np.int8)}
+    return cases
+
+
+ACT_CASES = load_activation_golden()
+
+
+def test_activation_golden_file_is_complete():
+    assert set(ACT_CASES) == {"unit_scale_half_even", "scale_two_ties", "inexact_scale", "negative_extreme",
+                              "all_zero_eps",
+                              "tiny_values_eps_binds", "two_rows_per_tensor", "two_rows_per_token"}
+    for c in ACT_CASES.values():
+        assert c["X"].shape == c["codes"].shape
+        assert c["scale"].shape == ((c["X"].shape[0],) if c["per_token"] else (1,))
+
+
+@pytest.mark.parametrize("name", sorted(ACT_CASES))
+def test_activation_golden(name):
+    c = ACT_CASES[name]
+    Xq, xs = oracle.ref_quantize_activation_i8(c["X"], per_token=c["per_token"])
+    np.testing.assert_array_equal(xs.view(np.uint32), c["scale"])
+    np.testing.assert_array_equal(Xq, c["codes"])
+
+
+@pytest.mark.parametrize("per_token", [False, True])
+def test_activation_invariants(per_token):
+    """|x - s_x q_x| <= s_x / 2 plus the fp32 quotient's rounding (at most 2^-24 |t| <= 128 2^-24
+    code units, which can carry a value just inside a tie across it), |q| <= 127, the
+    largest magnitude codes to +-127, q(-x) = -q(x), and zeros code to 0."""
+    X = workloads.gen_activation(6, 512, seed=41)
+    X[2] *= 1e-3  # a row far below the others (per tensor: coarse codes there)
+    X[3, 7] = 0.0
+    Xb = _bits(X)
+    Xq, xs = oracle.ref_quantize_activation_i8(Xb, per_token=per_token)
+    x = bits_f64(Xb)
+    s = xs.astype(np.float64)[:, None] if per_token else np.float64(xs[0])
+    assert np.abs(Xq.astype(np.int32)).max() <= 127
+    assert np.all(np.abs(x - s * Xq) <= s * (0.5 + 128 * 2.0 ** -24))
+    rows = range(6) if per_token else [int(np.argmax(np.abs(x).max(axis=1)))]
+    for m in rows:
+        k = int(np.argmax(np.abs(x[m])))
+        assert abs(int(Xq[m, k])) == 127
+    assert Xq[3, 7] == 0
+    Xn = (Xb ^ np.uint16(0x8000))  # -x, bit for bit
+    Xqn, xsn = oracle.ref_quantize_activation_i8(Xn, per_token=per_token)
+    np.testing.assert_array_equal(xsn, xs)
+    np.testing.assert_array_equal(Xqn, -Xq)
+
+
+def test_activation_rounding_by_brute_force():
+    """Each code is the integer nearest to the fp32 quotient x / s_x, ties to the even one."""
+    X = workloads.gen_activation(4, 256, seed=42)
+    Xb = _bits(X)
+    Xq, xs = oracle.ref_quantize_activation_i8(Xb, per_token=True)
+    for m in range(4):
+        t = (bits_f64(Xb[m]).astype(np.float32) / xs[m]).astype(np.float64)  # the fp32 quotient
+        cand = np.arange(-127, 128)[None, :]
+        d = np.abs(t[:, None] - cand)
+        best = d.min(axis=1, keepdims=True)
+        ties = (d == best)
+        for k in range(256):
+            opts = cand[0][ties[k]]
+            want = opts[0] if len(opts) == 1 else opts[opts % 2 == 0][0]
+            assert Xq[m, k] == want
+
+
+def test_activation_powers_of_two_scale_exactly():
+    """X * 2^e gives s_x * 2^e and the same codes (no clamp active)."""
+    Xb = _bits(workloads.gen_activation(3, 256, seed=43))
+    Xq, xs = oracle.ref_quantize_activation_i8(Xb)
+    X4 = (bits_f64(Xb) * 16).astype(np.float32).view(np.uint32) >> 16  # exact: bf16 * 16 is bf16
+    Xq4, xs4 = oracle.ref_quantize_activation_i8(X4.astype(np.uint16))
+    assert xs4[0] == np.float32(xs[0] * 16)
+    np.testing.assert_array_equal(Xq4, Xq)
+
+
+def _exact_weights(N, K, g, seed):
+    """4-bit codes with s = 2^-7 and o = -2^-4 in every group: w' = (q - 8) 2^-7 is
+    exact in bf16, so the bf16 linear and the int8 linear see the same real weights."""
+    rng = np.random.default_rng(seed)
+    q = rng.integers(0, 16, size=(N, K), dtype=np.uint8)
+    Wq = (q[:, 0::2] | (q[:, 1::2] << 4)).astype(np.uint8)
+    sc = np.full((N, K // g), 0x3C00, np.uint16)  # 2^-7
+    of = np.full((N, K // g), 0xBD80, np.uint16)  # -2^-4
+    return Wq, sc, of
+
+
+@pytest.mark.parametrize("g", [32, 64, 128])
+@pytest.mark.parametrize("per_token", [False, True])
+def test_linear_i8_matches_the_bf16_linear_on_exact_inputs(g, per_token):
+    """X = 2^-3 * integers in [-127, 127] with one +-127 per row: s_x = 2^-3 exactly and
+    q_x = the integers, so the int8 linear must equal the bf16 oracle linear (pinned
+    separately against a triple loop and numpy) exactly: every product and sum is exact."""
+    M, N, K = 3, 40, 256
+    rng = np.random.default_rng(g + per_token)
+    ints = rng.integers(-127, 128, size=(M, K))
+    ints[:, 5] = 127
+    ints[1, 9] = -127
+    X = (ints.astype(np.float32) * np.float32(0.125)).view(np.uint32) >> 16  # exact in bf16 (8 significant bits)
+    X = X.astype(np.uint16)
+    Wq, sc, of = _exact_weights(N, K, g, seed=g)
+    Xq, xs = oracle.ref_quantize_activation_i8(X, per_token=per_token)
+    assert np.all(xs == np.float32(0.125))
+    np.testing.assert_array_equal(Xq, ints.astype(np.int8))
+    y8 = oracle.ref_linear_i8(Xq, xs, per_token, Wq, sc, of, g)
+    y16 = oracle.ref_linear(X, Wq, sc, of, g)
+    np.testing.assert_array_equal(y8, y16)
+
+
+def test_linear_i8_uses_each_tokens_scale():
+    """Row 1 = 2 x row 0 per token: the same codes, scale 2x, so y[1] = 2 y[0] exactly;
+    per tensor the shared scale is row 1's."""
+    K, N, g = 128, 24, 32
+    X0 = workloads.gen_activation(1, K, seed=44)
+    Xb = _bits(torch.cat([X0, X0 * 2]))
+    W = _bits(workloads.gen_weight(N, K, seed=45))
+    Wq, sc, of = oracle.ref_quantize(W, g)
+    Xq, xs = oracle.ref_quantize_activation_i8(Xb, per_token=True)
+    np.testing.assert_array_equal(Xq[0], Xq[1])
+    assert xs[1] == 2 * xs[0]
+    y = oracle.ref_linear_i8(Xq, xs, True, Wq, sc, of, g)
+    np.testing.assert_array_equal(y[1], 2 * y[0])
+    Xqt, xst = oracle.ref_quantize_activation_i8(Xb, per_token=False)
+    assert xst[0] == xs[1]
+    np.testing.assert_array_equal(Xqt[1], Xq[1])
+
+
+def test_linear_i8_offset_term_closed_form():
+    """Codes q = 0 everywhere leave only the offsets: with every activation code c,
+    y = s_x * c * g * sum_j o_j (exact: small integers times bf16 values)."""
+    N, K, g = 6, 128, 32
+    Wq = np.zeros((N, K // 2), np.uint8)
+    sc = np.full((N, K // g), 0x3C00, np.uint16)
+    of = np.array([[0x3F80, 0xBF00, 0x3E80, 0x4000]] * N, np.uint16)  # 1, -0.5, 0.25, 2
+    Xq = np.full((2, K), 5, np.int8)
+    xs = np.array([0.25], np.float32)
+    y = oracle.ref_linear_i8(Xq, xs, False, Wq, sc, of, g)
+    np.testing.assert_array_equal(y, np.full((2, N), 0.25 * 5 * 32 * (1 - 0.5 + 0.25 + 2)))
+
+
+def test_linear_i8_bias():
+    N, K, g = 16, 256, 64
+    Xb = _bits(workloads.gen_activation(2, K, seed=46))
+    Wq, sc, of = oracle.ref_quantize(_bits(workloads.gen_weight(N, K, seed=47)), g)
+    bias = _bits(workloads.gen_activation(1, N, seed=48))[0]
+    Xq, xs = oracle.ref_quantize_activation_i8(Xb)
+    y0 = oracle.ref_linear_i8(Xq, xs, False, Wq, sc, of, g)
+    yb = oracle.ref_linear_i8(Xq, xs, False, Wq, sc, of, g, bias=bias)
+    np.testing.assert_allclose(yb - y0, np.tile(bits_f64(bias), (2, 1)), rtol=0,
+                               atol=4 * np.finfo(np.float64).eps * np.abs(yb).max())
