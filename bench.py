@@ -409,6 +409,7 @@ def gpu_arm(args):
                                     "how": "the headline step with a bf16 bias on each of the 224 linears "
                                            "(2N more bytes a call), CUDA graph"}
         del bs_graph, bs
+        rows.update(int8_rows(args, w4, wl, device, stream, dist, peaks, cases, stack, ms))
         # the same step with the weights that share an input merged row-wise, as serving stacks
         # store them (q|k|v: 6144 x 4096, gate|up: 28672 x 4096): 4 launches per block instead of
         # 7, the same codes, scales and offsets per output row (fresh seeded weights of those shapes)
@@ -459,6 +460,77 @@ def gpu_arm(args):
             line["e2e"]["value"] = None
         print(json.dumps(line), flush=True)
     dist.close()
+
+
+def int8_rows(args, w4, wl, device, stream, dist, peaks, cases, stack, ws_ms):
+    """The headline step on int8 activations (w4_quantize_activation_i8 + w4_linear_i8, one
+    scale per tensor): with the codes made beforehand (the linear alone) and with the
+    quantization inside the step (the whole dynamic path, two launches a linear); and the
+    M = 2048 prefill of the gate projection (quantize, widen, tensor-core GEMM)."""
+    import torch
+    out = {}
+    xq = [w4.w4_quantize_activation_i8(x) for x in stack.xv]
+    need = max(w4.w4_linear_i8_workspace_bytes(c.M, c.N, c.K, c.group_size) for c in cases)
+    ws = w4.Workspace(device, need)
+    qws = w4.Workspace(device, 4096)
+
+    def lin_only():
+        for c, (q, s_), y, (Wq, sc, of) in zip(cases, xq, stack.yv, stack.packed):
+            w4.w4_linear_i8(q, s_, False, Wq, sc, of, c.group_size, out=y, workspace=ws)
+
+    def dynamic():
+        for c, x, (q, s_), y, (Wq, sc, of) in zip(cases, stack.xv, xq, stack.yv, stack.packed):
+            w4.w4_quantize_activation_i8(x, False, out=(q, s_), workspace=qws)
+            w4.w4_linear_i8(q, s_, False, Wq, sc, of, c.group_size, out=y, workspace=ws)
+
+    act_bytes = sum(2 * c.M * c.K + c.M * c.K + 4 for c in cases)  # X read, codes written, the scale
+    for name, fn, extra, launches in (("decode_step_int8_codes", lin_only, 0, 1), ("decode_step_int8_dynamic", dynamic,
+                                                                                   act_bytes, 2)):
+        with torch.cuda.stream(stream):
+            fn()
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            t = time_region(g.replay, args.steps, args.warmup, stream, dist, device)
+        # the linear reads int8 codes: M K fewer bytes of X than the bf16 linear
+        lin_bytes = stack.bytes - sum(c.M * c.K for c in cases)
+        gbs = replica_gbs(lin_bytes + extra, args.steps, dist.world, t)
+        out[name] = {"unit": "GB/s", "value": round(gbs, 1), "ms_per_step": round(t / args.steps, 4),
+                     "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4), "time_vs_bf16_step": round(t / ws_ms, 3),
+                     "launches_per_step": launches * len(cases),
+                     "kernel": "stream_kernel on int8 codes (w4_linear_i8)" +
+                               (" + act_rows_kernel (w4_quantize_activation_i8)" if launches == 2 else ""),
+                     "how": "the headline step's 224 linears on int8 activation codes, one scale per tensor, CUDA graph" +
+                            ("; each linear's activations quantized inside the step" if launches == 2 else
+                             "; codes made before the timed region")}
+        del g
+    # prefill: the gate projection at M = 2048 on int8 activations, L2 flushed before each call
+    M, N, K, gs = 2048, 14336, 4096, 32
+    W = wl.gen_weight(N, K, seed=wl.weight_seed(4, 0, 0), outliers=False, device=device)
+    Wq, sc, of = w4.w4_quantize(W, gs)
+    del W
+    X = wl.gen_activation(M, K, seed=wl.weight_seed(4, 0, 0) + 1, device=device)
+    q, s_ = w4.w4_quantize_activation_i8(X, per_token=True)
+    pws = w4.Workspace(device, w4.w4_linear_i8_workspace_bytes(M, N, K, gs))
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+
+    def pre():
+        w4.w4_quantize_activation_i8(X, True, out=(q, s_))
+        w4.w4_linear_i8(q, s_, True, Wq, sc, of, gs, out=Y, workspace=pws)
+    with torch.cuda.stream(stream):
+        pre()
+        ts = time_each(pre, 10, stream, flush=lambda: flush.zero_())
+    tf = 2 * M * N * K / (ts * 1e-3) / 1e12
+    out["prefill_int8_dynamic"] = {"unit": "TFLOP/s", "M": M, "N": N, "K": K, "g": gs, "ms": round(ts, 4),
+                                   "tflops": round(tf, 1), "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+                                   "kernel": "act_rows_kernel + widen_kernel + gemm_kernel (tcgen05, bf16 operands "
+                                             "holding the int8 codes exactly)",
+                                   "how": "per-token int8 quantization of X, the codes widened to bf16, the "
+                                          "tensor-core GEMM with the activation scale in its epilogue; L2 flushed"}
+    del flush, pws, Y, q, X
+    return out
 
 
 def summary_rows(rows, peaks):

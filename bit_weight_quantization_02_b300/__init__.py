@@ -23,6 +23,7 @@ __all__ = [
     "library_path", "load_library", "w4_quantize", "w4_dequantize", "w4_linear",
     "w4_linear_ex", "w4_packed_bytes", "w4_qparam_bytes", "w4_device_fault", "w4_format_version",
     "w4_linear_static", "w4_linear_bias", "w4_packed_bytes_bits", "w4_quantize_bits", "w4_dequantize_bits", "w4_linear_bits",
+    "w4_quantize_activation_i8", "w4_linear_i8", "w4_linear_i8_workspace_bytes",
 ]
 
 W4_FORMAT_VERSION = 1
@@ -80,6 +81,10 @@ def load_library():
             "w4_selftest_bounded_waits": ([p, sz, p, ctypes.c_uint64, p], i32),
             "w4_linear_bias": ([p, i64, i64, p, p, p, i64, i32, p, p, p, sz, p], i32),
             "w4_linear_bias_ex": ([p, i64, i64, p, p, p, i64, i32, p, p, p, sz, i32, p], i32),
+            "w4_quantize_activation_workspace_bytes": ([i64, i64, i32], sz),
+            "w4_quantize_activation_i8": ([p, i64, i64, i32, p, p, p, sz, p], i32),
+            "w4_linear_i8_workspace_bytes": ([i64, i64, i64, i32], sz),
+            "w4_linear_i8": ([p, p, i32, i64, i64, p, p, p, i64, i32, p, p, p, sz, p], i32),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -281,6 +286,60 @@ def w4_linear_bias(X: torch.Tensor, Wq: torch.Tensor, scales: torch.Tensor, offs
     ws = _workspace_for(X, M, N, K, group_size, workspace)
     _check(lib.w4_linear_bias_ex(_ptr(X), M, K, _ptr(Wq), _ptr(scales), _ptr(offsets), N, group_size, _ptr(bias),
                                  _ptr(Y), _ptr(ws.buf), ws.nbytes, kernel, _stream(X)), "w4_linear_bias")
+    return Y
+
+
+def w4_quantize_activation_i8(X: torch.Tensor, per_token: bool = False, out=None, workspace: Workspace | None = None):
+    """X bf16 [M,K] -> (Xq int8 [M,K], x_scale fp32 [1] or [M]): s = max|x| / 127 per tensor
+    (or per row), Xq = clamp(rne(x / s), -127, 127)."""
+    lib = load_library()
+    _bits16(X, "X")
+    M, K = X.shape
+    if out is None:
+        Xq = torch.empty((M, K), dtype=torch.int8, device=X.device)
+        xs = torch.empty((M if per_token else 1,), dtype=torch.float32, device=X.device)
+    else:
+        Xq, xs = out
+    need = lib.w4_quantize_activation_workspace_bytes(M, K, int(bool(per_token)))
+    ws = workspace if workspace is not None else (Workspace(X.device, need) if need else None)
+    _check(lib.w4_quantize_activation_i8(_ptr(X), M, K, int(bool(per_token)), _ptr(Xq), _ptr(xs),
+                                         _ptr(ws.buf) if ws is not None else None, ws.nbytes if ws is not None else 0,
+                                         _stream(X)), "w4_quantize_activation_i8")
+    return Xq, xs
+
+
+def w4_linear_i8_workspace_bytes(M: int, N: int, K: int, group_size: int) -> int:
+    return load_library().w4_linear_i8_workspace_bytes(M, N, K, group_size)
+
+
+def w4_linear_i8(Xq: torch.Tensor, x_scale: torch.Tensor, per_token: bool, Wq: torch.Tensor, scales: torch.Tensor,
+                 offsets: torch.Tensor, group_size: int, bias: torch.Tensor | None = None, out=None,
+                 workspace: Workspace | None = None):
+    """Y bf16 [M,N] = s_x * sum_j (s_j I_j + o_j S_j) (+ bias [N]) on int8 activation codes Xq [M,K]
+    (x_scale fp32: [1] per tensor, [M] per token) and 4-bit weights."""
+    lib = load_library()
+    if Xq.dtype != torch.int8 or not Xq.is_contiguous():
+        raise TypeError("Xq must be a contiguous int8 tensor")
+    if x_scale.dtype != torch.float32:
+        raise TypeError("x_scale must be float32")
+    M, K = Xq.shape
+    N = Wq.shape[0]
+    if x_scale.numel() != (M if per_token else 1):
+        raise ValueError("x_scale must hold M values per token, 1 per tensor")
+    if bias is not None:
+        _bits16(bias, "bias")
+        if bias.numel() != N:
+            raise ValueError("bias must hold N values")
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=Xq.device)
+    if workspace is None:
+        key = ("i8", Xq.device.index, torch.cuda.current_stream(Xq.device).cuda_stream)
+        workspace = _default_ws.get(key)
+        if workspace is None:
+            workspace = _default_ws[key] = Workspace(Xq.device)
+        workspace.reserve(lib.w4_linear_i8_workspace_bytes(M, N, K, group_size))
+    _check(lib.w4_linear_i8(_ptr(Xq), _ptr(x_scale), int(bool(per_token)), M, K, _ptr(Wq), _ptr(scales), _ptr(offsets),
+                            N, group_size, _ptr(bias), _ptr(Y), _ptr(workspace.buf), workspace.nbytes, _stream(Xq)),
+           "w4_linear_i8")
     return Y
 
 

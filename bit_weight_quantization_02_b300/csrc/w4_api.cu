@@ -117,6 +117,8 @@ w4_status linear_impl(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq
 
     const char* detail = "";
     cudaError_t e;
+    w4::Epilogue ep;
+    ep.bias = bias;
     // one token without a workspace (or when asked for): the SM-pair kernel, which needs none
     w4::StreamPlan sp0;
     const bool stream_ws = M <= w4::STREAM_MAX_M && w4::plan_stream(M, N, K, group_size, &sp0) &&
@@ -143,7 +145,7 @@ w4_status linear_impl(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq
                         w4_linear_workspace_bytes(M, N, K, group_size));
         if (can) {
             e = w4::launch_stream(sp, X, M, K, Wq, scales, offsets, N, group_size, Y, workspace, (cudaStream_t)stream,
-                                  &detail, bias);
+                                  &detail, ep);
             if (e != cudaSuccess) return fail(W4_ERR_CUDA, "stream linear: %s %s", cudaGetErrorString(e), detail);
             return W4_OK;
         }
@@ -160,7 +162,7 @@ w4_status linear_impl(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq
         }
         if (kernel != W4_KERNEL_AUTO) return fail(W4_ERR_INVALID_ARG, "no skinny launch plan for this shape");
     }
-    e = w4::launch_gemm(X, M, K, Wq, scales, offsets, N, group_size, 4, Y, (cudaStream_t)stream, &detail, bias);
+    e = w4::launch_gemm(X, M, K, Wq, scales, offsets, N, group_size, 4, Y, (cudaStream_t)stream, &detail, ep);
     if (e != cudaSuccess) return fail(W4_ERR_CUDA, "tensor-core linear: %s %s", cudaGetErrorString(e), detail);
     return W4_OK;
 }
@@ -195,6 +197,120 @@ w4_status w4_linear(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, 
                     size_t workspace_bytes, void* stream) {
     return w4_linear_ex(X, M, K, Wq, scales, offsets, N, group_size, Y, workspace, workspace_bytes, W4_KERNEL_AUTO,
                         stream);
+}
+
+// ---- int8 dynamic activations x int4 weights
+
+size_t w4_quantize_activation_workspace_bytes(int64_t M, int64_t K, int per_token) {
+    if (M <= 1 || K <= 0 || per_token) return 0;
+    return (size_t)w4::ACT_MAX_PARTIALS * sizeof(uint32_t);
+}
+
+w4_status w4_quantize_activation_i8(const uint16_t* X, int64_t M, int64_t K, int per_token, int8_t* Xq,
+                                    float* x_scale, void* workspace, size_t workspace_bytes, void* stream) {
+    if (K <= 0 || K % 32 != 0) return fail(W4_ERR_INVALID_ARG, "K = %lld must be a positive multiple of 32", (long long)K);
+    if (M < 0 || M > 0x7FFFFFFFLL || K > 0x7FFFFFFFLL) return fail(W4_ERR_INVALID_ARG, "M and K must lie in [0, 2^31)");
+    if (M > 0 && K > (int64_t(1) << 62) / M) return fail(W4_ERR_INVALID_ARG, "M*K overflows");
+    if (per_token != 0 && per_token != 1) return fail(W4_ERR_INVALID_ARG, "per_token must be 0 or 1");
+    if (M == 0) return W4_OK;
+    W4_TRY(check_ptr(X, "X"));
+    W4_TRY(check_ptr(Xq, "Xq"));
+    if (x_scale == nullptr) return fail(W4_ERR_INVALID_ARG, "x_scale is NULL");
+    if (reinterpret_cast<uintptr_t>(x_scale) & 3u) return fail(W4_ERR_MISALIGNED, "x_scale is not 4-byte aligned");
+    const size_t need = w4_quantize_activation_workspace_bytes(M, K, per_token);
+    if (need > 0) {
+        if (workspace == nullptr || workspace_bytes < need)
+            return fail(W4_ERR_INVALID_ARG, "one scale for the tensor over %lld rows needs %zu workspace bytes",
+                        (long long)M, need);
+        if (!aligned16(workspace)) return fail(W4_ERR_MISALIGNED, "workspace is not 16-byte aligned");
+    }
+    const cudaError_t e = w4::launch_quantize_activation(X, M, K, per_token != 0, Xq, x_scale,
+                                                         static_cast<uint32_t*>(workspace), (cudaStream_t)stream);
+    return e == cudaSuccess ? W4_OK : cuda_fail(e, "activation quantize launch");
+}
+
+}  // extern "C"
+
+namespace {
+
+// How the int8 linear runs: codes read straight by the stream kernel (M <= 4), or
+// widened to bf16 in the workspace first (then the batch or tensor-core kernel).
+// The linear's own slots (zero between calls) start at 0; the bf16 copy of the
+// codes (scratch) at I8_SCRATCH_OFFSET, past any call's slots.
+struct I8Plan {
+    bool direct;       // stream kernel on the int8 codes
+    bool stream_ok;    // the stream / batch kernels take the shape (M <= 32, even K/g)
+    w4::StreamPlan sp;
+    size_t lin_bytes;  // the linear's own slots
+    size_t wide_bytes; // the bf16 copy of the codes
+    size_t total;      // workspace bytes the call needs
+};
+
+I8Plan plan_i8(int64_t M, int64_t N, int64_t K, int g) {
+    I8Plan p{};
+    p.stream_ok = M <= w4::STREAM_MAX_M && w4::plan_stream(M, N, K, g, &p.sp);
+    p.direct = M <= 4 && p.stream_ok;
+    p.lin_bytes = p.stream_ok ? p.sp.ws_bytes : 0;
+    p.wide_bytes = p.direct ? 0 : (size_t)(M * K * 2);
+    p.total = p.direct ? p.lin_bytes : w4::I8_SCRATCH_OFFSET + p.wide_bytes;
+    return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t w4_linear_i8_workspace_bytes(int64_t M, int64_t N, int64_t K, int group_size) {
+    if (check_shape(N, K, group_size) != W4_OK || M < 1 || N == 0 || M > 0x7FFFFFFFLL) return 0;
+    return plan_i8(M, N, K, group_size).total;
+}
+
+w4_status w4_linear_i8(const int8_t* Xq, const float* x_scale, int per_token, int64_t M, int64_t K,
+                       const uint8_t* Wq, const uint16_t* scales, const uint16_t* offsets, int64_t N,
+                       int group_size, const uint16_t* bias, uint16_t* Y, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+    W4_TRY(check_shape(N, K, group_size));
+    if (M < 0 || M > 0x7FFFFFFFLL) return fail(W4_ERR_INVALID_ARG, "M = %lld must lie in [0, 2^31)", (long long)M);
+    if (per_token != 0 && per_token != 1) return fail(W4_ERR_INVALID_ARG, "per_token must be 0 or 1");
+    if (M == 0 || N == 0) return W4_OK;
+    W4_TRY(check_ptr(Xq, "Xq"));
+    W4_TRY(check_ptr(Wq, "Wq"));
+    W4_TRY(check_ptr(scales, "scales"));
+    W4_TRY(check_ptr(offsets, "offsets"));
+    W4_TRY(check_ptr(Y, "Y"));
+    if (x_scale == nullptr) return fail(W4_ERR_INVALID_ARG, "x_scale is NULL");
+    if (reinterpret_cast<uintptr_t>(x_scale) & 3u) return fail(W4_ERR_MISALIGNED, "x_scale is not 4-byte aligned");
+    if (bias != nullptr && (reinterpret_cast<uintptr_t>(bias) & 1u))
+        return fail(W4_ERR_MISALIGNED, "bias is not 2-byte aligned");
+    const I8Plan p = plan_i8(M, N, K, group_size);
+    if (p.total > 0) {
+        if (workspace == nullptr || workspace_bytes < p.total)
+            return fail(W4_ERR_INVALID_ARG, "the int8 linear needs %zu workspace bytes (w4_linear_i8_workspace_bytes)",
+                        p.total);
+        if (!aligned16(workspace)) return fail(W4_ERR_MISALIGNED, "workspace is not 16-byte aligned");
+    }
+    w4::Epilogue ep;
+    ep.bias = bias;
+    ep.yscale = x_scale;
+    ep.ys_stride = per_token ? 1 : 0;
+    const char* detail = "";
+    cudaError_t e;
+    if (p.direct) {
+        e = w4::launch_stream_i8(p.sp, Xq, M, K, Wq, scales, offsets, N, group_size, Y, workspace,
+                                 (cudaStream_t)stream, &detail, ep);
+        if (e != cudaSuccess) return fail(W4_ERR_CUDA, "int8 stream linear: %s %s", cudaGetErrorString(e), detail);
+        return W4_OK;
+    }
+    uint16_t* Xb = reinterpret_cast<uint16_t*>(static_cast<unsigned char*>(workspace) + w4::I8_SCRATCH_OFFSET);
+    e = w4::launch_widen_i8(Xq, M * K, Xb, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "int8 widen launch");
+    if (p.stream_ok)
+        e = w4::launch_stream(p.sp, Xb, M, K, Wq, scales, offsets, N, group_size, Y, workspace, (cudaStream_t)stream,
+                              &detail, ep);
+    else
+        e = w4::launch_gemm(Xb, M, K, Wq, scales, offsets, N, group_size, 4, Y, (cudaStream_t)stream, &detail, ep);
+    if (e != cudaSuccess) return fail(W4_ERR_CUDA, "int8 linear: %s %s", cudaGetErrorString(e), detail);
+    return W4_OK;
 }
 
 size_t w4_packed_bytes(int64_t N, int64_t K) {

@@ -64,7 +64,7 @@ struct BatchArgs {
     const uint16_t* scales;  // the cp.async qparam route
     const uint16_t* offsets;
     uint16_t* Y;
-    const uint16_t* bias;  // [N] bf16 added before the rounding, or null
+    Epilogue ep;           // bias and output scale, applied before the rounding
     uint64_t* ws;            // split-tile slots, one per warp, zero between calls
     int M, N, K;
     int nkc;                 // units per row group = ceil(K / 256)
@@ -496,7 +496,7 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
                         const int m = 8 * t + 2 * tq + (i & 1), r = gid + (i & 2) * 4;
                         if (m < p.M && r < nrows)
                             p.Y[(int64_t)m * p.N + tile * 16 + r] =
-                                (uint16_t)float_to_bf16_bits(acc[t][i] + bias_f32(p.bias, tile * 16 + r));
+                                (uint16_t)float_to_bf16_bits(epilogue_f32(p.ep, acc[t][i], m, (int64_t)tile * 16 + r));
                     }
             } else if (kc_first != 0) {  // a later share of the group (the first of this range): publish it
                 split_publish<MT>(p.ws + ((size_t)cta * BT_WARPS + warp) * 16 * p.M, acc, p.M, nrows, gid, tq);
@@ -518,7 +518,7 @@ batch_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
         const int wl = split_warp_of((long long)grp * p.nkc + p.nkc - 1, p.units, p.ctas);
         ok = split_collect<MT, NE>(acc, scr, p.ws + (size_t)warp * 16 * p.M, (size_t)BT_WARPS * 16 * p.M, cta, wl,
                                    p.M, min(16, p.N - tile * 16), gid, tq, lane, p.Y + (int64_t)tile * 16, p.N,
-                                   &g_batch_fault, 2u, BT_WAIT_LIMIT_NS, p.bias ? p.bias + tile * 16 : nullptr) &&
+                                   &g_batch_fault, 2u, BT_WAIT_LIMIT_NS, epilogue_at(p.ep, (int64_t)tile * 16)) &&
              ok;
     }
     if (!ok) {  // never leave with copies still landing in shared memory (the last DEPTH fills)
@@ -585,7 +585,7 @@ static cudaError_t launch_batch_b(const CUtensorMap& tw, const CUtensorMap& tx, 
 
 cudaError_t launch_batch(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
                          const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, int bits, uint16_t* Y,
-                         void* workspace, cudaStream_t stream, const char** detail, const uint16_t* bias) {
+                         void* workspace, cudaStream_t stream, const char** detail, const Epilogue& ep) {
     const int64_t ng = K / g;
     // qparam rows whole 16-byte pieces: 8-group TMA boxes (K is then a multiple of 256); else cp.async
     const bool qt = ng % 8 == 0;
@@ -615,7 +615,7 @@ cudaError_t launch_batch(const StreamPlan& plan, const uint16_t* X, int64_t M, i
     a.scales = scales;
     a.offsets = offsets;
     a.Y = Y;
-    a.bias = bias;
+    a.ep = ep;
     a.ws = static_cast<uint64_t*>(workspace);
     a.M = (int)M;
     a.N = (int)N;

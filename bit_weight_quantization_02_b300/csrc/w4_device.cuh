@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
+#include "w4_internal.h"  // Epilogue
+
 namespace w4 {
 
 // ---------------------------------------------------------------- bf16 bits
@@ -37,6 +39,22 @@ __device__ __forceinline__ uint4 ldg_cg_v4(const void* p) {
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
     return r;
 }
+__device__ __forceinline__ uint2 ldg_cg_v2(const void* p) {
+    uint2 r;
+    asm volatile("ld.global.cg.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+// Eight int8 codes (bytes of v, lowest first) as eight bf16 values, exactly
+// (|q| <= 128 has at most 8 significant bits), in the order of eight bf16 in memory.
+__device__ __forceinline__ uint4 widen_i8x8(uint2 v) {
+    uint32_t h[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int q = (int)(int8_t)(((i < 4 ? v.x : v.y) >> (8 * (i & 3))) & 0xFFu);
+        h[i] = __float_as_uint((float)q) >> 16;
+    }
+    return make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+}
 __device__ __forceinline__ uint32_t ldg_nc_u16(const uint16_t* p) {
     unsigned short v;
     asm("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
@@ -52,6 +70,21 @@ __device__ __forceinline__ uint32_t ldg_nc_u32(const void* p) {
 // the fp32 sum before the one rounding to bf16.
 __device__ __forceinline__ float bias_f32(const uint16_t* b, int64_t n) {
     return b ? bf16_bits_to_float(ldg_nc_u16(b + n)) : 0.f;
+}
+// The output scale of token m (1 when there is none).  A plain load: the scale may
+// come from the kernel before this one (read after the dependency wait).
+__device__ __forceinline__ float yscale_f32(const Epilogue& ep, int m) {
+    return ep.yscale ? ep.yscale[(int64_t)m * ep.ys_stride] : 1.f;
+}
+// The value rounded to bf16 for output (m, n): sum * yscale + bias in one fp32
+// rounding (with neither, exactly the sum; with a bias only, sum + bias).
+__device__ __forceinline__ float epilogue_f32(const Epilogue& ep, float sum, int m, int64_t n) {
+    return fmaf(sum, yscale_f32(ep, m), bias_f32(ep.bias, n));
+}
+// The epilogue of a tile whose first output row is n0 (bias pointer moved to it).
+__device__ __forceinline__ Epilogue epilogue_at(Epilogue ep, int64_t n0) {
+    if (ep.bias) ep.bias += n0;
+    return ep;
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -264,8 +297,8 @@ __device__ __forceinline__ void split_publish(uint64_t* slot, const float (&acc)
 // The owner's part, after its own sums are in the warp's scratch (16 M floats
 // of shared memory, element m * 16 + r): the slots of warps worker + 1 .. wl
 // (warp c's words at ws + c * stride),
-// then bf16 Y of the tile (Yt = first column of the tile, ldy = N; bias_t, when
-// given, the bias of the tile's first row, added in fp32 before the rounding).  The
+// then bf16 Y of the tile (Yt = first column of the tile, ldy = N; ep_t, the
+// epilogue with its bias moved to the tile's first row, applied before the rounding).  The
 // owner's shared tile is the last of its range, so the kernels call this after
 // their main loop, when the loop's registers are free.  Each lane takes
 // elements lane, lane + 32, ... (NE of them, at most NEMAX; with one token,
@@ -277,7 +310,7 @@ __device__ __forceinline__ bool split_sum_shares(const float* scr, uint64_t* ws,
                                                  int M,
                                                  int nrows, int lane, uint16_t* Yt, int64_t ldy,
                                                  unsigned int* fault_word, unsigned int code, uint64_t limit_ns,
-                                                 const uint16_t* bias_t = nullptr) {
+                                                 const Epilogue ep_t = Epilogue()) {
     constexpr int BC = NEMAX >= 8 ? 1 : 8 / NEMAX;  // sharers per batch (8 words per lane, 16 for NEMAX 16)
     bool ok = true;
     const int E = 16 * M;          // words per slot
@@ -338,7 +371,7 @@ __device__ __forceinline__ bool split_sum_shares(const float* scr, uint64_t* ws,
     for (int i = 0; i < NEMAX; ++i) {
         const int e = e0 + 32 * i;
         if (sub == 0 && e < E && (e & 15) < nrows)
-            Yt[(int64_t)(e >> 4) * ldy + (e & 15)] = (uint16_t)float_to_bf16_bits(sum[i] + bias_f32(bias_t, e & 15));
+            Yt[(int64_t)(e >> 4) * ldy + (e & 15)] = (uint16_t)float_to_bf16_bits(epilogue_f32(ep_t, sum[i], e >> 4, e & 15));
     }
     return ok;
 }
@@ -349,7 +382,7 @@ __device__ __forceinline__ bool split_collect(const float (&acc)[MT][4], float* 
                                               int worker, int wl,
                                               int M, int nrows, int row_a, int tq, int lane, uint16_t* Yt,
                                               int64_t ldy, unsigned int* fault_word, unsigned int code,
-                                              uint64_t limit_ns, const uint16_t* bias_t = nullptr) {
+                                              uint64_t limit_ns, const Epilogue ep_t = Epilogue()) {
 #pragma unroll
     for (int t = 0; t < MT; ++t)
 #pragma unroll
@@ -359,7 +392,7 @@ __device__ __forceinline__ bool split_collect(const float (&acc)[MT][4], float* 
         }
     __syncwarp();
     const bool ok =
-        split_sum_shares<NEMAX>(scr, ws, stride, worker, wl, M, nrows, lane, Yt, ldy, fault_word, code, limit_ns, bias_t);
+        split_sum_shares<NEMAX>(scr, ws, stride, worker, wl, M, nrows, lane, Yt, ldy, fault_word, code, limit_ns, ep_t);
     __syncwarp();
     return ok;
 }

@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_p,
             const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_o,
             const uint16_t* __restrict__ scales, const uint16_t* __restrict__ offsets, uint16_t* __restrict__ Y,
-            const uint16_t* __restrict__ bias, int M, int N, int K) {
+            const Epilogue ep, int M, int N, int K) {
     using LY = GmLayout<B>;
     constexpr int QSPAN = 8 * G / GM_BK;  // k blocks covered by one qparam box (8 groups)
     extern __shared__ unsigned char smem_raw[];
@@ -437,18 +437,20 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             const uint32_t stage_s = smem_u32(stage);
             const int nrow0 = n0 + 32 * sp;  // first weight row of this warp
             const bool vec = (N % 8) == 0 && nrow0 + 32 <= N;
-            const float bl = nrow0 + lane < N ? bias_f32(bias, nrow0 + lane) : 0.f;  // this lane's row
+            const float bl = nrow0 + lane < N ? bias_f32(ep.bias, nrow0 + lane) : 0.f;  // this lane's row
 #pragma unroll 1
             for (int cc = 0; cc < 4; ++cc) {
                 const int col = 128 * hh + 32 * cc;  // first token column of the block
                 uint32_t v[32];
                 tmem_ld_32cols(tmem + ((uint32_t)(32 * sp) << 16) + (uint32_t)col, v);
+                // the output scale of token column col + lane (lane i hands column i's to the warp)
+                const float fl = yscale_f32(ep, min(m0 + col + lane, M - 1));
                 tmem_ld_wait();
-                // stage[token i][row lane] = bf16(D[row][token])
+                // stage[token i][row lane] = bf16(D[row][token] * scale + bias)
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
                     *reinterpret_cast<uint16_t*>(stage + i * GM_STAGE_PITCH + 2 * lane) =
-                        (uint16_t)float_to_bf16_bits(__uint_as_float(v[i]) + bl);
+                        (uint16_t)float_to_bf16_bits(fmaf(__uint_as_float(v[i]), __shfl_sync(0xffffffffu, fl, i), bl));
                 __syncwarp();
                 const int m = m0 + col + lane;  // the token this lane writes
                 if (m < M && nrow0 < N) {
@@ -477,36 +479,36 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
 template <int G, bool QT, int B>
 static cudaError_t launch_gemm_g(const CUtensorMap& tx, const CUtensorMap& tp, const CUtensorMap& ts,
                                  const CUtensorMap& to, const uint16_t* scales, const uint16_t* offsets, uint16_t* Y,
-                                 const uint16_t* bias, int M, int N, int K, cudaStream_t stream) {
+                                 const Epilogue& ep, int M, int N, int K, cudaStream_t stream) {
     auto kern = gemm_kernel<G, QT, B>;
     constexpr int SMEM = GmLayout<B>::SMEM_BYTES;
     cudaError_t e = ensure_kernel_attrs(reinterpret_cast<const void*>(kern), SMEM, false);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((N + GM_BW - 1) / GM_BW), (unsigned)((M + GM_BT - 1) / GM_BT));
-    kern<<<grid, GM_THREADS, SMEM, stream>>>(tx, tp, ts, to, scales, offsets, Y, bias, M, N, K);
+    kern<<<grid, GM_THREADS, SMEM, stream>>>(tx, tp, ts, to, scales, offsets, Y, ep, M, N, K);
     return cudaGetLastError();
 }
 
 template <int B>
 static cudaError_t launch_gemm_b(const CUtensorMap& tx, const CUtensorMap& tp, const CUtensorMap& ts,
                                  const CUtensorMap& to, bool qt, const uint16_t* scales, const uint16_t* offsets,
-                                 uint16_t* Y, const uint16_t* bias, int m, int n, int k, int g, cudaStream_t stream) {
+                                 uint16_t* Y, const Epilogue& ep, int m, int n, int k, int g, cudaStream_t stream) {
     switch (g) {
         case 32:
-            return qt ? launch_gemm_g<32, true, B>(tx, tp, ts, to, scales, offsets, Y, bias, m, n, k, stream)
-                      : launch_gemm_g<32, false, B>(tx, tp, ts, to, scales, offsets, Y, bias, m, n, k, stream);
+            return qt ? launch_gemm_g<32, true, B>(tx, tp, ts, to, scales, offsets, Y, ep, m, n, k, stream)
+                      : launch_gemm_g<32, false, B>(tx, tp, ts, to, scales, offsets, Y, ep, m, n, k, stream);
         case 64:
-            return qt ? launch_gemm_g<64, true, B>(tx, tp, ts, to, scales, offsets, Y, bias, m, n, k, stream)
-                      : launch_gemm_g<64, false, B>(tx, tp, ts, to, scales, offsets, Y, bias, m, n, k, stream);
+            return qt ? launch_gemm_g<64, true, B>(tx, tp, ts, to, scales, offsets, Y, ep, m, n, k, stream)
+                      : launch_gemm_g<64, false, B>(tx, tp, ts, to, scales, offsets, Y, ep, m, n, k, stream);
         default:
-            return qt ? launch_gemm_g<128, true, B>(tx, tp, ts, to, scales, offsets, Y, bias, m, n, k, stream)
-                      : launch_gemm_g<128, false, B>(tx, tp, ts, to, scales, offsets, Y, bias, m, n, k, stream);
+            return qt ? launch_gemm_g<128, true, B>(tx, tp, ts, to, scales, offsets, Y, ep, m, n, k, stream)
+                      : launch_gemm_g<128, false, B>(tx, tp, ts, to, scales, offsets, Y, ep, m, n, k, stream);
     }
 }
 
 cudaError_t launch_gemm(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
                         const uint16_t* offsets, int64_t N, int g, int bits, uint16_t* Y, cudaStream_t stream,
-                        const char** detail, const uint16_t* bias) {
+                        const char** detail, const Epilogue& ep) {
     if ((N + GM_BW - 1) / GM_BW > 0x7FFFFFFF || (M + GM_BT - 1) / GM_BT > 65535) {
         *detail = "problem too large for the GEMM grid";
         return cudaErrorInvalidValue;
@@ -541,9 +543,9 @@ cudaError_t launch_gemm(const uint16_t* X, int64_t M, int64_t K, const uint8_t* 
         if (e != cudaSuccess) return e;
     }
     const int m = (int)M, n = (int)N, k = (int)K;
-    if (bits == 2) return launch_gemm_b<2>(tx, tp, ts, to, qt, scales, offsets, Y, bias, m, n, k, g, stream);
-    if (bits == 8) return launch_gemm_b<8>(tx, tp, ts, to, qt, scales, offsets, Y, bias, m, n, k, g, stream);
-    return launch_gemm_b<4>(tx, tp, ts, to, qt, scales, offsets, Y, bias, m, n, k, g, stream);
+    if (bits == 2) return launch_gemm_b<2>(tx, tp, ts, to, qt, scales, offsets, Y, ep, m, n, k, g, stream);
+    if (bits == 8) return launch_gemm_b<8>(tx, tp, ts, to, qt, scales, offsets, Y, ep, m, n, k, g, stream);
+    return launch_gemm_b<4>(tx, tp, ts, to, qt, scales, offsets, Y, ep, m, n, k, g, stream);
 }
 
 cudaError_t read_and_clear_gemm_fault(unsigned int* fault) {

@@ -10,6 +10,18 @@
 
 namespace w4 {
 
+// What a linear kernel does to the fp32 sum of output (m, n) before its one
+// rounding to bf16: y = sum * yscale[m * ys_stride] + bias[n].  A null yscale is
+// the factor 1 and a null bias adds 0, so the default is the plain product.
+// yscale is the activation scale of int8 activation codes (ys_stride 0: one
+// for the tensor, 1: one per token); kernels read it after their dependency
+// wait, so the kernel before them may write it.
+struct Epilogue {
+    const uint16_t* bias = nullptr;  // [N] bf16
+    const float* yscale = nullptr;
+    int ys_stride = 0;
+};
+
 // bits: code width, 2, 4 or 8
 cudaError_t launch_quantize(const uint16_t* W, int64_t N, int64_t K, int g, int bits, uint8_t* Wq, uint16_t* scales,
                             uint16_t* offsets, cudaStream_t stream);
@@ -44,17 +56,27 @@ struct StreamPlan {
 };
 constexpr int STREAM_MAX_M = 32;
 constexpr int DECODE_MAX_M = 32;  // decode-layout kernel
+// Where the int8 linear puts its bf16 copy of the codes in a caller's
+// workspace: past the largest slot region any linear keeps at zero (4096 warps
+// x 16 rows x 32 tokens x 8 bytes), so calls of any shape can share one workspace.
+constexpr size_t I8_SCRATCH_OFFSET = size_t(16) << 20;
 bool plan_stream(int64_t M, int64_t N, int64_t K, int g, StreamPlan* plan);
-// bias: [N] bf16 added in fp32 before the one rounding of Y, or null (every linear launcher).
+// bias: [N] bf16 added in fp32 before the one rounding of Y, or null; ep: the same
+// and an output scale (the stream, batch and GEMM launchers).
 cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
                           const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
-                          void* workspace, cudaStream_t stream, const char** detail, const uint16_t* bias = nullptr);
+                          void* workspace, cudaStream_t stream, const char** detail, const Epilogue& ep = Epilogue());
+// The same kernel on int8 activation codes (M <= 4; Xq [M][K] bytes), widened to
+// bf16 as they are loaded; ep carries their scale.
+cudaError_t launch_stream_i8(const StreamPlan& plan, const int8_t* Xq, int64_t M, int64_t K, const uint8_t* Wq,
+                             const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
+                             void* workspace, cudaStream_t stream, const char** detail, const Epilogue& ep);
 cudaError_t read_and_clear_stream_fault(unsigned int* fault);
 // Batched decode (5 <= M <= 32): 64-row units, the block's X slice staged once
 // by TMA; same plan and workspace as the stream kernel (launch_stream calls it).
 cudaError_t launch_batch(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
                          const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, int bits, uint16_t* Y,
-                         void* workspace, cudaStream_t stream, const char** detail, const uint16_t* bias = nullptr);
+                         void* workspace, cudaStream_t stream, const char** detail, const Epilogue& ep = Epilogue());
 cudaError_t read_and_clear_batch_fault(unsigned int* fault);
 
 // Decode layout (see w4.h): bytes of one 16-row x 256-k unit, of the whole
@@ -88,6 +110,15 @@ cudaError_t launch_pair(const PairPlan& plan, const uint16_t* X, int64_t K, cons
 cudaError_t read_and_clear_pair_fault(unsigned int* fault);
 cudaError_t read_and_clear_selftest_fault(unsigned int* fault);  // w4_selftest.cu
 
+// int8 activations (w4_act.cu): dynamic symmetric quantization, per token
+// (per_token) or per tensor, and the widening of codes to bf16 for the kernels
+// that stage X by TMA.  `partials` holds ACT_MAX_PARTIALS 32-bit words, used
+// per tensor when M > 1.
+constexpr int ACT_MAX_PARTIALS = 1024;
+cudaError_t launch_quantize_activation(const uint16_t* X, int64_t M, int64_t K, bool per_token, int8_t* Xq,
+                                       float* x_scale, uint32_t* partials, cudaStream_t stream);
+cudaError_t launch_widen_i8(const int8_t* Xq, int64_t n, uint16_t* Xb, cudaStream_t stream);
+
 // SM count of the current device and resident blocks per SM for a kernel
 // launch shape (cached per device, kernel and shared-memory size).
 cudaError_t resident_blocks(const void* kernel, int threads, size_t smem, int* sms, int* per_sm);
@@ -95,7 +126,7 @@ cudaError_t resident_blocks(const void* kernel, int threads, size_t smem, int* s
 // tcgen05 tensor-core GEMM (any M).
 cudaError_t launch_gemm(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
                         const uint16_t* offsets, int64_t N, int g, int bits, uint16_t* Y, cudaStream_t stream,
-                        const char** detail, const uint16_t* bias = nullptr);
+                        const char** detail, const Epilogue& ep = Epilogue());
 // Read and clear the kernels' device fault words (bounded-wait timeouts); the
 // caller has synchronized the stream.
 cudaError_t read_and_clear_gemm_fault(unsigned int* fault);

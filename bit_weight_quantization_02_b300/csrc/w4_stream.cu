@@ -60,7 +60,7 @@ struct StreamArgs {
     const uint16_t* scales;
     const uint16_t* offsets;
     uint16_t* Y;
-    const uint16_t* bias;  // [N] bf16 added before the rounding, or null
+    Epilogue ep;           // bias and output scale, applied before the rounding
     uint64_t* ws;          // split-tile slots, one per warp (split_ws_bytes), zero between calls
     int M, N, K;
     int nkc;               // units per row tile = ceil(K / 256)
@@ -210,7 +210,9 @@ __device__ __forceinline__ float bf16x8_sum(uint4 v) {
 // MX: token capacity (1, 2, 4; X staged in shared memory).
 // RT: 16-row tiles per unit, 1, or 2 for one token on large problems (the X
 // staging, slice sums and ring work of a unit then serve 32 weight rows).
-template <int G, int MX, bool QT, int RT>
+// XI8: X holds int8 activation codes (p.X points at bytes), widened to bf16 when
+// loaded; the activation scale is applied by the epilogue.
+template <int G, int MX, bool QT, int RT, bool XI8>
 __global__ void __launch_bounds__(ST_THREADS, RT == 2 ? 4 : 6)
 stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
               const __grid_constant__ CUtensorMap tm_o, const StreamArgs p) {
@@ -330,7 +332,14 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         const int k = kc * ST_UK + 8 * lane;
 #pragma unroll
         for (int m = 0; m < MX; ++m)
-            if (m < p.M) xr[m] = (k < p.K) ? ldg_cg_v4(xlane + (int64_t)m * p.K + kc * ST_UK) : make_uint4(0u, 0u, 0u, 0u);
+            if (m < p.M) {
+                if constexpr (XI8)
+                    xr[m] = (k < p.K) ? widen_i8x8(ldg_cg_v2(reinterpret_cast<const int8_t*>(p.X) + 8 * lane +
+                                                             (int64_t)m * p.K + kc * ST_UK))
+                                      : make_uint4(0u, 0u, 0u, 0u);
+                else
+                    xr[m] = (k < p.K) ? ldg_cg_v4(xlane + (int64_t)m * p.K + kc * ST_UK) : make_uint4(0u, 0u, 0u, 0u);
+            }
     };
     const uint32_t xst = (uint32_t)(16 * st_x_slot(lane));
     auto store_x = [&](unsigned char* slot) {
@@ -499,9 +508,9 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 for (int rt = 0; rt < RT; ++rt) {
                     const int n_a = tile * ROWS + 16 * rt + pr, n_b = n_a + 8;
                     if (tq == 0 && n_a < p.N)
-                        p.Y[n_a] = (uint16_t)float_to_bf16_bits(racc[rt][0][0] + bias_f32(p.bias, n_a));
+                        p.Y[n_a] = (uint16_t)float_to_bf16_bits(epilogue_f32(p.ep, racc[rt][0][0], 0, n_a));
                     if (tq == 0 && n_b < p.N)
-                        p.Y[n_b] = (uint16_t)float_to_bf16_bits(racc[rt][0][2] + bias_f32(p.bias, n_b));
+                        p.Y[n_b] = (uint16_t)float_to_bf16_bits(epilogue_f32(p.ep, racc[rt][0][2], 0, n_b));
                 }
             } else if (kc_first != 0) {  // a later share of the tile (the first of this range): publish it
 #pragma unroll
@@ -527,7 +536,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                     for (int i = 0; i < 4; ++i) {
                         const int m = 8 * t + 2 * tq + (i & 1), n = (i < 2) ? n_a : n_b;
                         if (m < p.M && n < p.N)
-                            p.Y[(int64_t)m * p.N + n] = (uint16_t)float_to_bf16_bits(acc[t][i] + bias_f32(p.bias, n));
+                            p.Y[(int64_t)m * p.N + n] = (uint16_t)float_to_bf16_bits(epilogue_f32(p.ep, acc[t][i], m, n));
                     }
             } else if (kc_first != 0) {  // a later share of the tile (the first of this range): publish it
                 split_publish<MT>(p.ws + (size_t)worker * 16 * p.M, acc, p.M, min(16, p.N - tile * 16), pr, tq);
@@ -550,12 +559,12 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 ok = split_collect<1, NE>(oacc[rt], scr + rt * 16, p.ws + rt * 16, (size_t)RT * 16, worker, wl, 1,
                                           min(16, p.N - (tile * ROWS + 16 * rt)), pr, tq, lane,
                                           p.Y + (int64_t)tile * ROWS + 16 * rt, p.N, &g_stream_fault, 2u,
-                                          ST_WAIT_LIMIT_NS, p.bias ? p.bias + tile * ROWS + 16 * rt : nullptr) &&
+                                          ST_WAIT_LIMIT_NS, epilogue_at(p.ep, (int64_t)tile * ROWS + 16 * rt)) &&
                      ok;
         } else {
             ok = split_collect<MT, NE>(acc, scr, p.ws, (size_t)16 * p.M, worker, wl, p.M, min(16, p.N - tile * 16), pr,
                                        tq, lane, p.Y + (int64_t)tile * 16, p.N, &g_stream_fault, 2u,
-                                       ST_WAIT_LIMIT_NS, p.bias ? p.bias + tile * 16 : nullptr) &&
+                                       ST_WAIT_LIMIT_NS, epilogue_at(p.ep, (int64_t)tile * 16)) &&
                  ok;
         }
     }
@@ -566,6 +575,10 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
 }
 
 // ------------------------------------------------------------------ host side
+
+static_assert((size_t)SPLIT_MAX_WORKERS * 16 * STREAM_MAX_M * 8 <= I8_SCRATCH_OFFSET &&
+                  (size_t)2 * SPLIT_MAX_WORKERS * 16 * 8 <= I8_SCRATCH_OFFSET,
+              "the int8 linear's scratch must lie past every slot region");
 
 bool plan_stream(int64_t M, int64_t N, int64_t K, int g, StreamPlan* plan) {
     if (M < 1 || M > STREAM_MAX_M) return false;
@@ -581,10 +594,10 @@ bool plan_stream(int64_t M, int64_t N, int64_t K, int g, StreamPlan* plan) {
     return true;
 }
 
-template <int G, int MX, bool QT, int RT>
+template <int G, int MX, bool QT, int RT, bool XI8>
 static cudaError_t launch_stream_gm(const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& to, StreamArgs a,
                                     cudaStream_t stream) {
-    auto kern = stream_kernel<G, MX, QT, RT>;
+    auto kern = stream_kernel<G, MX, QT, RT, XI8>;
     const size_t smem = (size_t)st_smem_bytes(a.M, G, RT);
     cudaError_t e = ensure_kernel_attrs(reinterpret_cast<const void*>(kern), st_smem_bytes(MX, G, RT), false);
     if (e != cudaSuccess) return e;
@@ -608,13 +621,13 @@ static cudaError_t launch_stream_gm(const CUtensorMap& tw, const CUtensorMap& ts
     return cudaLaunchKernelEx(&cfg, kern, tw, ts, to, a);
 }
 
-template <int G, bool QT>
+template <int G, bool QT, bool XI8>
 static cudaError_t launch_stream_g(const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& to, StreamArgs a,
                                    int rt, cudaStream_t stream) {
-    if (rt == 2) return launch_stream_gm<G, 1, QT, 2>(tw, ts, to, a, stream);
-    if (a.M <= 1) return launch_stream_gm<G, 1, QT, 1>(tw, ts, to, a, stream);
-    if (a.M <= 2) return launch_stream_gm<G, 2, QT, 1>(tw, ts, to, a, stream);
-    return launch_stream_gm<G, 4, QT, 1>(tw, ts, to, a, stream);
+    if (rt == 2) return launch_stream_gm<G, 1, QT, 2, XI8>(tw, ts, to, a, stream);
+    if (a.M <= 1) return launch_stream_gm<G, 1, QT, 1, XI8>(tw, ts, to, a, stream);
+    if (a.M <= 2) return launch_stream_gm<G, 2, QT, 1, XI8>(tw, ts, to, a, stream);
+    return launch_stream_gm<G, 4, QT, 1, XI8>(tw, ts, to, a, stream);
 }
 
 // One token takes 32-row units (two row tiles sharing the X staging, slice sums
@@ -622,7 +635,7 @@ static cudaError_t launch_stream_g(const CUtensorMap& tw, const CUtensorMap& ts,
 // warp one, and the workspace holds two 16-row slots per warp.
 template <int G, bool QT>
 static cudaError_t two_row_tiles(int64_t N, int nkc, size_t ws_bytes, bool* two) {
-    auto kern = stream_kernel<G, 1, QT, 2>;
+    auto kern = stream_kernel<G, 1, QT, 2, false>;
     cudaError_t e = ensure_kernel_attrs(reinterpret_cast<const void*>(kern), st_smem_bytes(1, G, 2), false);
     int sms = 0, per_sm = 0;
     if (e == cudaSuccess)
@@ -634,11 +647,14 @@ static cudaError_t two_row_tiles(int64_t N, int nkc, size_t ws_bytes, bool* two)
     return cudaSuccess;
 }
 
-cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
-                          const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
-                          void* workspace, cudaStream_t stream, const char** detail, const uint16_t* bias) {
-    if (M > 4)  // 5..32 tokens: the block-shared X kernel (w4_batch.cu)
-        return launch_batch(plan, X, M, K, Wq, scales, offsets, N, g, 4, Y, workspace, stream, detail, bias);
+template <bool XI8>
+static cudaError_t launch_stream_t(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
+                                   const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
+                                   void* workspace, cudaStream_t stream, const char** detail, const Epilogue& ep) {
+    if (M > 4) {  // 5..32 tokens: the block-shared X kernel (w4_batch.cu), bf16 X only
+        if (XI8) return cudaErrorInvalidValue;
+        return launch_batch(plan, X, M, K, Wq, scales, offsets, N, g, 4, Y, workspace, stream, detail, ep);
+    }
     const int64_t ng = K / g;
     const bool qt = (g == 32) && (ng % 8 == 0);  // qparam rows 16-byte aligned: 8-group TMA boxes
     cudaError_t e = cudaSuccess;
@@ -671,7 +687,7 @@ cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, 
     a.scales = scales;
     a.offsets = offsets;
     a.Y = Y;
-    a.bias = bias;
+    a.ep = ep;
     a.ws = static_cast<uint64_t*>(workspace);
     a.M = (int)M;
     a.N = (int)N;
@@ -681,12 +697,26 @@ cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, 
     a.workers = 0;
     switch (g) {
         case 32:
-            return qt ? launch_stream_g<32, true>(tw, ts, to, a, rt, stream)
-                      : launch_stream_g<32, false>(tw, ts, to, a, rt, stream);
-        case 64: return launch_stream_g<64, false>(tw, ts, to, a, rt, stream);
-        default: return launch_stream_g<128, false>(tw, ts, to, a, rt, stream);
+            return qt ? launch_stream_g<32, true, XI8>(tw, ts, to, a, rt, stream)
+                      : launch_stream_g<32, false, XI8>(tw, ts, to, a, rt, stream);
+        case 64: return launch_stream_g<64, false, XI8>(tw, ts, to, a, rt, stream);
+        default: return launch_stream_g<128, false, XI8>(tw, ts, to, a, rt, stream);
     }
 }
+
+cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
+                          const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
+                          void* workspace, cudaStream_t stream, const char** detail, const Epilogue& ep) {
+    return launch_stream_t<false>(plan, X, M, K, Wq, scales, offsets, N, g, Y, workspace, stream, detail, ep);
+}
+
+cudaError_t launch_stream_i8(const StreamPlan& plan, const int8_t* Xq, int64_t M, int64_t K, const uint8_t* Wq,
+                             const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
+                             void* workspace, cudaStream_t stream, const char** detail, const Epilogue& ep) {
+    return launch_stream_t<true>(plan, reinterpret_cast<const uint16_t*>(Xq), M, K, Wq, scales, offsets, N, g, Y,
+                                 workspace, stream, detail, ep);
+}
+
 
 cudaError_t read_and_clear_stream_fault(unsigned int* fault) {
     cudaError_t e = cudaMemcpyFromSymbol(fault, g_stream_fault, sizeof(unsigned int));

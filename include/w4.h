@@ -203,6 +203,60 @@ W4_API w4_status w4_linear_bias_ex(const uint16_t *X, int64_t M, int64_t K, cons
                                    int group_size, const uint16_t *bias, uint16_t *Y, void *workspace,
                                    size_t workspace_bytes, w4_kernel kernel, void *stream);
 
+/*
+ * int8 dynamic activations x int4 weights.  Source: torchao README "Training /
+ * QAT" and torchao guide (QAT; edge deployment): Int8DynamicActivationInt4-
+ * WeightConfig quantizes a linear's activations to int8 at run time and its
+ * weights to int4 in groups; Optimum Quanto, "Design overview / Modules" and
+ * "Pitfalls when quantizing activations": activations are quantized
+ * symmetrically with one scale per tensor, the integer product is accumulated
+ * wider than its inputs and brought back to float, then the float bias added.
+ *
+ * w4_quantize_activation_i8 -- X [M][K] bf16 -> Xq [M][K] int8 and x_scale (fp32):
+ *   a = max |x| over the tensor (per_token = 0: one scale, x_scale[0]) or over
+ *   each row (per_token = 1: x_scale[m]);  s = a / 127 (fp32 IEEE division, at
+ *   least 1e-6);  Xq = clamp(rne(x / s), -127, 127) (fp32 IEEE division, round
+ *   half to even).  Bit-exact against the reference.
+ * K: a positive multiple of 32; M >= 0 (0: nothing is launched).  X, Xq: 16-byte
+ * aligned; x_scale: 4-byte aligned.  workspace: per tensor with M > 1, at least
+ * w4_quantize_activation_workspace_bytes (16-byte aligned, any contents, used
+ * as scratch); otherwise it may be NULL.  Errors: W4_ERR_INVALID_ARG,
+ * W4_ERR_MISALIGNED, W4_ERR_CUDA.
+ */
+W4_API size_t w4_quantize_activation_workspace_bytes(int64_t M, int64_t K, int per_token);
+W4_API w4_status w4_quantize_activation_i8(const uint16_t *X, int64_t M, int64_t K, int per_token,
+                                           int8_t *Xq, float *x_scale, void *workspace,
+                                           size_t workspace_bytes, void *stream);
+
+/*
+ * w4_linear_i8 -- the linear on int8 activation codes and 4-bit weights (the
+ * layout of w4_quantize):
+ *   Y[m,n] = bf16( s_x(m) * sum_j (s_j I_j + o_j S_j) + bias[n] ),
+ *   I_j = sum_{k in group j} Xq[m,k] q[n,k],  S_j = sum_{k in group j} Xq[m,k],
+ * s_x(m) = x_scale[m] (per_token = 1) or x_scale[0] (per_token = 0), bias [N]
+ * bf16 or NULL.  The codes are exact in bf16, so the kernels run the bf16
+ * tensor-core path on them: with at most 4 tokens they read Xq directly and
+ * sum (128 + q) Xq over 16-k slices, exactly in fp32 (every partial sum is an
+ * integer below 2^24); with more, the codes are widened to bf16 in the
+ * workspace and the weights dequantized to bf16 as in w4_linear.  s_x, the
+ * group's scale and offset and the bias are applied in fp32, rounded once.
+ * Accuracy: |y - y_ref| <= 4e-3 |y_ref| + 1e-2 rms(y_ref), y_ref the fp64
+ * value above.
+ * workspace: w4_linear_i8_workspace_bytes(M, N, K, g) bytes, 16-byte aligned,
+ * zero-filled once before the first use.  Its first 16 MiB hold the kernels'
+ * split-tile slots (as for w4_linear; every call leaves them at zero); calls
+ * with more than 4 tokens also write the codes widened to bf16 after them
+ * (scratch, 2 M K bytes from 16 MiB on).  So one workspace serves int8 and
+ * bf16 calls of any shape in sequence.  Other arguments and errors as
+ * w4_linear_bias; x_scale 4-byte aligned.
+ */
+W4_API size_t w4_linear_i8_workspace_bytes(int64_t M, int64_t N, int64_t K, int group_size);
+W4_API w4_status w4_linear_i8(const int8_t *Xq, const float *x_scale, int per_token, int64_t M,
+                              int64_t K, const uint8_t *Wq, const uint16_t *scales,
+                              const uint16_t *offsets, int64_t N, int group_size,
+                              const uint16_t *bias, uint16_t *Y, void *workspace,
+                              size_t workspace_bytes, void *stream);
+
 /* Sizes of the packed outputs: N*K/2 bytes of codes, N*(K/g)*2 bytes for each
  * of scales and offsets.  0 for invalid arguments. */
 W4_API size_t w4_packed_bytes(int64_t N, int64_t K);
