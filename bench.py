@@ -549,7 +549,7 @@ def summary_rows(rows, peaks):
     return prefill, batched
 
 
-def _rotated_graph_row(c, w4, wl, device, stream, dist, peaks, layout="canonical", no_workspace=False):
+def _rotated_graph_row(c, w4, wl, device, stream, dist, peaks, layout="canonical", no_workspace=False, kernel=None):
     """Time one linear shape: a graph of back-to-back calls over weight copies totalling
     more than 4x L2 (so every call streams its weights from HBM); `layout` "decode" times
     w4_linear_repacked on w4_repack's rearrangement of the same weights."""
@@ -570,6 +570,8 @@ def _rotated_graph_row(c, w4, wl, device, stream, dist, peaks, layout="canonical
         it["i"] += 1
         if layout == "decode":
             w4.w4_linear_repacked(X, r, out=Y, workspace=ws)
+        elif kernel is not None:
+            w4.w4_linear_ex(X, *r, c.group_size, kernel, out=Y, workspace=ws)
         else:
             w4.w4_linear(X, *r, c.group_size, out=Y, workspace=ws)
 
@@ -717,6 +719,9 @@ def other_rows(args, w4, wl, device, stream, peaks, dist, only=None):
         if c.N == 4096 and c.M in (2, 16, 32):  # w4_linear without a workspace: the cluster split-K kernel
             b3.append(_rotated_graph_row(c, w4, wl, device, stream, dist, peaks, no_workspace=True))
             b3[-1]["kernel"] = "skinny_kernel (no workspace)"
+        if c.M in (8, 16, 32):  # the tcgen05 batched-decode kernel, on request (not the automatic choice)
+            b3.append(_rotated_graph_row(c, w4, wl, device, stream, dist, peaks, kernel=w4.KERNEL_TC_DECODE))
+            b3[-1]["kernel"] = "tcdec_kernel (tcgen05, W4_KERNEL_TC_DECODE)"
     rows["batched_decode_g64"] = {"unit": "GB/s", "cases": b3,
                                   "l2": "graph of back-to-back calls over weight copies totalling > 4x L2"}
 

@@ -18,7 +18,7 @@ import torch
 
 __all__ = [
     "W4Error", "W4_FORMAT_VERSION", "KERNEL_AUTO", "KERNEL_SKINNY", "KERNEL_GEMM", "KERNEL_SKINNY_CLUSTER",
-    "KERNEL_STREAM", "KERNEL_PAIR", "Workspace", "w4_linear_workspace_bytes", "Repacked", "w4_repacked_bytes", "w4_repack",
+    "KERNEL_STREAM", "KERNEL_PAIR", "KERNEL_TC_DECODE", "Workspace", "w4_linear_workspace_bytes", "Repacked", "w4_repacked_bytes", "w4_repack",
     "w4_linear_repacked",
     "library_path", "load_library", "w4_quantize", "w4_dequantize", "w4_linear",
     "w4_linear_ex", "w4_packed_bytes", "w4_qparam_bytes", "w4_device_fault", "w4_format_version",
@@ -27,7 +27,8 @@ __all__ = [
 ]
 
 W4_FORMAT_VERSION = 1
-KERNEL_AUTO, KERNEL_SKINNY, KERNEL_GEMM, KERNEL_SKINNY_CLUSTER, KERNEL_STREAM, KERNEL_PAIR = 0, 1, 2, 3, 4, 5
+KERNEL_AUTO, KERNEL_SKINNY, KERNEL_GEMM, KERNEL_SKINNY_CLUSTER, KERNEL_STREAM, KERNEL_PAIR, KERNEL_TC_DECODE = (
+    0, 1, 2, 3, 4, 5, 6)
 _STATUS = {0: "W4_OK", 1: "W4_ERR_INVALID_ARG", 2: "W4_ERR_UNSUPPORTED", 3: "W4_ERR_MISALIGNED",
            4: "W4_ERR_CUDA", 5: "W4_ERR_TIMEOUT"}
 

@@ -4,6 +4,7 @@
 #include "w4.h"
 #include "w4_internal.h"
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -81,7 +82,10 @@ w4_status w4_dequantize(const uint8_t* Wq, const uint16_t* scales, const uint16_
 size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int group_size) {
     if (check_shape(N, K, group_size) != W4_OK || M < 1 || N == 0) return 0;
     w4::StreamPlan plan;
-    if (M <= w4::STREAM_MAX_M && w4::plan_stream(M, N, K, group_size, &plan)) return plan.ws_bytes;
+    w4::TcDecPlan tp;  // the tensor-core decode kernel's slots, when a device is there to size them
+    const size_t tc = M <= w4::TCDEC_MAX_M && w4::plan_tcdec(M, N, K, group_size, &tp) ? tp.ws_bytes : 0;
+    if (M <= w4::STREAM_MAX_M && w4::plan_stream(M, N, K, group_size, &plan)) return std::max(plan.ws_bytes, tc);
+    if (tc) return tc;
     w4::DecodePlan dp;  // decode layout (w4_linear_repacked)
     if (w4::plan_decode(M, N, K, group_size, &dp)) return dp.ws_bytes;
     return 0;
@@ -98,7 +102,7 @@ w4_status linear_impl(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq
     W4_TRY(check_shape(N, K, group_size));
     if (M < 0) return fail(W4_ERR_INVALID_ARG, "M = %lld must not be negative", (long long)M);
     if (M > 0x7FFFFFFFLL) return fail(W4_ERR_INVALID_ARG, "M must be below 2^31");
-    if (kernel < W4_KERNEL_AUTO || kernel > W4_KERNEL_PAIR)
+    if (kernel < W4_KERNEL_AUTO || kernel > W4_KERNEL_TC_DECODE)
         return fail(W4_ERR_INVALID_ARG, "unknown kernel choice %d", (int)kernel);
     if ((kernel == W4_KERNEL_SKINNY || kernel == W4_KERNEL_SKINNY_CLUSTER) && M > w4::SKINNY_MAX_M)
         return fail(W4_ERR_INVALID_ARG, "the skinny kernels take M <= %d, got %lld", w4::SKINNY_MAX_M, (long long)M);
@@ -119,6 +123,16 @@ w4_status linear_impl(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq
     cudaError_t e;
     w4::Epilogue ep;
     ep.bias = bias;
+    if (kernel == W4_KERNEL_TC_DECODE) {  // the tensor-core decode kernel, on request
+        w4::TcDecPlan tp;
+        if (!w4::plan_tcdec(M, N, K, group_size, &tp) || workspace_bytes < tp.ws_bytes)
+            return fail(W4_ERR_INVALID_ARG, "the tensor-core decode kernel takes M <= %d and %zu workspace bytes",
+                        w4::TCDEC_MAX_M, w4_linear_workspace_bytes(M, N, K, group_size));
+        e = w4::launch_tcdec(tp, X, M, K, Wq, scales, offsets, N, group_size, Y, workspace, (cudaStream_t)stream,
+                             &detail, ep);
+        if (e != cudaSuccess) return fail(W4_ERR_CUDA, "tensor-core decode linear: %s %s", cudaGetErrorString(e), detail);
+        return W4_OK;
+    }
     // one token without a workspace (or when asked for): the SM-pair kernel, which needs none
     w4::StreamPlan sp0;
     const bool stream_ws = M <= w4::STREAM_MAX_M && w4::plan_stream(M, N, K, group_size, &sp0) &&
@@ -326,7 +340,7 @@ size_t w4_qparam_bytes(int64_t N, int64_t K, int group_size) {
 w4_status w4_device_fault(void* stream) {
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "synchronizing the stream");
-    unsigned int gemm = 0, skinny = 0, strm = 0, dec = 0, bat = 0, pair = 0, self = 0;
+    unsigned int gemm = 0, skinny = 0, strm = 0, dec = 0, bat = 0, pair = 0, self = 0, tcd = 0;
     e = w4::read_and_clear_gemm_fault(&gemm);
     if (e == cudaSuccess) e = w4::read_and_clear_skinny_fault(&skinny);
     if (e == cudaSuccess) e = w4::read_and_clear_stream_fault(&strm);
@@ -334,12 +348,13 @@ w4_status w4_device_fault(void* stream) {
     if (e == cudaSuccess) e = w4::read_and_clear_batch_fault(&bat);
     if (e == cudaSuccess) e = w4::read_and_clear_pair_fault(&pair);
     if (e == cudaSuccess) e = w4::read_and_clear_selftest_fault(&self);
+    if (e == cudaSuccess) e = w4::read_and_clear_tcdec_fault(&tcd);
     if (e != cudaSuccess) return cuda_fail(e, "reading the device fault words");
-    if (gemm || skinny || strm || dec || bat || pair || self)
+    if (gemm || skinny || strm || dec || bat || pair || self || tcd)
         return fail(W4_ERR_TIMEOUT,
                     "a block gave up a bounded wait (tensor-core 0x%x, skinny 0x%x, stream 0x%x, decode 0x%x, "
-                    "batched 0x%x, pair 0x%x, self-test 0x%x)",
-                    gemm, skinny, strm, dec, bat, pair, self);
+                    "batched 0x%x, pair 0x%x, self-test 0x%x, tensor-core decode 0x%x)",
+                    gemm, skinny, strm, dec, bat, pair, self, tcd);
     return W4_OK;
 }
 

@@ -123,6 +123,24 @@ cudaError_t launch_widen_i8(const int8_t* Xq, int64_t n, uint16_t* Xb, cudaStrea
 // launch shape (cached per device, kernel and shared-memory size).
 cudaError_t resident_blocks(const void* kernel, int threads, size_t smem, int* sms, int* per_sm);
 
+// Batched decode on the tcgen05 tensor cores (1 <= M <= 32, 4-bit codes): a
+// persistent grid of one block per SM over 128-row x 256-k units (stream-K),
+// split tiles finished by their owner block from a zero-initialized,
+// self-cleaning workspace of ws_bytes.
+constexpr int TCDEC_MAX_M = 32;
+struct TcDecPlan {
+    int nkc;          // 256-k units per 128-row tile
+    long long units;  // tiles * nkc
+    int ctas;         // blocks (at most one per SM and per unit)
+    int mt;           // token tile: 16 or 32
+    size_t ws_bytes;  // workspace bytes
+};
+bool plan_tcdec(int64_t M, int64_t N, int64_t K, int g, TcDecPlan* plan);
+cudaError_t launch_tcdec(const TcDecPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
+                         const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
+                         void* workspace, cudaStream_t stream, const char** detail, const Epilogue& ep = Epilogue());
+cudaError_t read_and_clear_tcdec_fault(unsigned int* fault);
+
 // tcgen05 tensor-core GEMM (any M).
 cudaError_t launch_gemm(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
                         const uint16_t* offsets, int64_t N, int g, int bits, uint16_t* Y, cudaStream_t stream,

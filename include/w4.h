@@ -72,8 +72,10 @@ typedef enum w4_kernel {
     W4_KERNEL_SKINNY_CLUSTER = 3,  /* cluster split-K skinny kernel, M <= 32, no workspace */
     W4_KERNEL_STREAM = 4,          /* persistent stream-K kernels, M <= 32, need the workspace:
                                       per-warp units up to 4 tokens, block-shared X from 5 */
-    W4_KERNEL_PAIR = 5             /* one token on pairs of SMs (clusters of two), no workspace:
+    W4_KERNEL_PAIR = 5,            /* one token on pairs of SMs (clusters of two), no workspace:
                                       M == 1, K <= 16384, K / group_size a multiple of 8 */
+    W4_KERNEL_TC_DECODE = 6        /* M <= 32 on the tcgen05 tensor cores: a persistent block per
+                                      SM over 128-row x 256-k units; needs the workspace */
 } w4_kernel;
 
 /*
