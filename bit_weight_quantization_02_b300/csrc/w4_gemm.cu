@@ -226,8 +226,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             int issued = 0;
             for (int kb = 0; kb < nkb; ++kb) {
                 const int t = kb % GM_TSTAGES, w = kb % GM_WSTAGES;
-                const uint32_t pt = (kb / GM_TSTAGES) & 1, pw = (kb / GM_WSTAGES) & 1;
-                if (!mbar_wait_bounded(full_tma(t), pt, abort_flag, &g_gemm_fault, 2u, GM_WAIT_LIMIT_NS)) break;
+                const uint32_t pw = (kb / GM_WSTAGES) & 1;
+                // Only the A stage is waited for: every dequantization thread waited for this
+                // k block's TMA stage (X and codes) before its arrive, so full_deq orders the X
+                // tile too.  One wait less a step keeps the tensor pipe fed (each N=256 MMA
+                // takes ~128 cycles, and the issuing thread's gaps between steps leave it idle).
                 if (!mbar_wait_bounded(full_deq(w), pw, abort_flag, &g_gemm_fault, 2u, GM_WAIT_LIMIT_NS)) break;
                 tc_fence_after();
                 const uint64_t bdesc = sw128_kmajor_desc(sbase + GM_OFF_X + t * GM_X_BYTES);
