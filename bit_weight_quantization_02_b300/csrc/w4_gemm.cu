@@ -18,10 +18,13 @@
 //               128-byte swizzle, the UMMA B layout) and the packed code tile
 //               (128 rows x 32 bytes, 32-byte swizzle); every 8 groups, when
 //               the rows allow it, a 2-deep ring of scale / offset boxes;
-//   warp 1      TMEM owner (512 columns: D in 0..255, four 32-column A
+//   warp 1      TMEM owner (512 columns: D in 0..255, five 32-column A
 //               stages above) and, on one lane, the UMMA issuer: 4 x
 //               tcgen05.mma (M=128 from TMEM, N=256, K=16) a step;
-//               tcgen05.commit frees the TMA stage and the A stage;
+//               one tcgen05.commit a step frees the stage (the TMA buffers and
+//               the A tile of the same index), and the issuer waits only for
+//               the A tile: the dequantization threads waited for the TMA
+//               stage first;
 //   warps 2..9  dequantization: thread (row, 32-k half) of its TMEM
 //               sub-partition turns 32 codes into 16 bf16 pairs and stores
 //               them with one tcgen05.st; afterwards the same warps run the
@@ -48,7 +51,7 @@ constexpr int GM_BW = 128;  // weight rows per block (UMMA M, TMEM lanes)
 constexpr int GM_BT = 256;  // tokens per block (UMMA N)
 constexpr int GM_BK = 64;
 constexpr int GM_TSTAGES = 5;  // TMA ring: X tile + packed code tile per k block
-constexpr int GM_WSTAGES = 4;  // dequantized weight tiles in TMEM (the UMMA A operand)
+constexpr int GM_WSTAGES = GM_TSTAGES;  // dequantized weight tiles in TMEM (the UMMA A operand), one per TMA stage
 constexpr int GM_QSTAGES = 2;  // TMA ring of qparam boxes (8 groups x 128 rows of scales and offsets)
 constexpr int GM_QPF = 4;      // k blocks of qparams prefetched by each thread (no-TMA variant)
 constexpr int GM_DEQ_WARPS = 8;
@@ -61,9 +64,9 @@ constexpr int GM_X_BYTES = GM_BT * GM_BK * 2;  // 32 KB
 constexpr int GM_QBOX_BYTES = GM_BW * 16;      //  2 KB: 8 bf16 per row
 constexpr int GM_OFF_X = 0;
 constexpr int GM_OFF_P = GM_OFF_X + GM_TSTAGES * GM_X_BYTES;
-// full_tma, empty_tma per TMA stage; full_deq, empty_w per A stage;
+// full_tma, empty_tma per stage (empty_tma also frees the stage's A tile); full_deq per stage;
 // full_q, empty_q per qparam stage; tmem_full; drain
-constexpr int GM_NBAR = 2 * GM_TSTAGES + 2 * GM_WSTAGES + 2 * GM_QSTAGES + 2;
+constexpr int GM_NBAR = 2 * GM_TSTAGES + GM_WSTAGES + 2 * GM_QSTAGES + 2;
 // Shared-memory layout after the X ring, for B-bit codes.
 template <int B>
 struct GmLayout {
@@ -145,10 +148,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     auto full_tma = [&](int t) { return bar0 + 8u * t; };
     auto empty_tma = [&](int t) { return bar0 + 8u * (GM_TSTAGES + t); };
     auto full_deq = [&](int w) { return bar0 + 8u * (2 * GM_TSTAGES + w); };
-    auto empty_w = [&](int w) { return bar0 + 8u * (2 * GM_TSTAGES + GM_WSTAGES + w); };
-    auto full_q = [&](int q) { return bar0 + 8u * (2 * GM_TSTAGES + 2 * GM_WSTAGES + q); };
-    auto empty_q = [&](int q) { return bar0 + 8u * (2 * GM_TSTAGES + 2 * GM_WSTAGES + GM_QSTAGES + q); };
-    const uint32_t tmem_full = bar0 + 8u * (2 * GM_TSTAGES + 2 * GM_WSTAGES + 2 * GM_QSTAGES);
+    auto full_q = [&](int q) { return bar0 + 8u * (2 * GM_TSTAGES + GM_WSTAGES + q); };
+    auto empty_q = [&](int q) { return bar0 + 8u * (2 * GM_TSTAGES + GM_WSTAGES + GM_QSTAGES + q); };
+    const uint32_t tmem_full = bar0 + 8u * (2 * GM_TSTAGES + GM_WSTAGES + 2 * GM_QSTAGES);
     const uint32_t drain = tmem_full + 8u;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + LY::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + LY::OFF_MISC + 4);
@@ -164,7 +166,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         }
         for (int w = 0; w < GM_WSTAGES; ++w) {
             mbar_init(full_deq(w), GM_DEQ_WARPS * 32);
-            mbar_init(empty_w(w), 1);
         }
         for (int q = 0; q < GM_QSTAGES; ++q) {
             mbar_init(full_q(q), 1);
@@ -238,8 +239,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
 #pragma unroll
                 for (int kk = 0; kk < GM_BK / 16; ++kk)  // K=16 a step: 8 A columns, +32 bytes of B (+2 in the desc)
                     umma_bf16_tmem_a(tmem, a_tmem + 8u * kk, bdesc + 2u * kk, idesc, (kb | kk) != 0);
-                umma_commit(empty_tma(t));  // X and codes of this k block consumed
-                umma_commit(empty_w(w));    // A stage consumed
+                umma_commit(empty_tma(t));  // X, codes and the A tile of this k block consumed (one commit)
                 ++issued;
             }
             if (issued == nkb) umma_commit(tmem_full);
@@ -313,7 +313,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             const int t = kb % GM_TSTAGES, w = kb % GM_WSTAGES;
             const uint32_t pt = (kb / GM_TSTAGES) & 1, pw = (kb / GM_WSTAGES) & 1;
             if (!mbar_wait_bounded(full_tma(t), pt, abort_flag, &g_gemm_fault, 4u, GM_WAIT_LIMIT_NS) ||
-                !mbar_wait_bounded(empty_w(w), pw ^ 1, abort_flag, &g_gemm_fault, 4u, GM_WAIT_LIMIT_NS)) {
+                !mbar_wait_bounded(empty_tma(w), pw ^ 1, abort_flag, &g_gemm_fault, 4u, GM_WAIT_LIMIT_NS)) {
                 ok = false;
                 break;
             }
