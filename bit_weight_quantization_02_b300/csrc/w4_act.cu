@@ -70,6 +70,8 @@ __device__ __forceinline__ uint2 act_codes8(uint4 v, float s) {
 // one block per row of X: its maximum, its scale, its codes
 __global__ void __launch_bounds__(ACT_THREADS) act_rows_kernel(const uint16_t* X, int K, int8_t* Xq, float* x_scale) {
     __shared__ uint32_t red[ACT_THREADS / 32];
+    griddep_launch_dependents();  // the linear after this may start streaming its weights now
+    griddep_wait();               // X may come from the kernel before this one
     const uint16_t* x = X + (int64_t)blockIdx.x * K;
     int8_t* q = Xq + (int64_t)blockIdx.x * K;
     const int nch = K / 8;
@@ -85,6 +87,8 @@ __global__ void __launch_bounds__(ACT_THREADS) act_rows_kernel(const uint16_t* X
 __global__ void __launch_bounds__(ACT_THREADS) act_partial_max_kernel(const uint16_t* X, int64_t nch,
                                                                        uint32_t* partials) {
     __shared__ uint32_t red[ACT_THREADS / 32];
+    griddep_launch_dependents();
+    griddep_wait();
     uint32_t mx = 0u;
     for (int64_t c = (int64_t)blockIdx.x * ACT_THREADS + threadIdx.x; c < nch; c += (int64_t)gridDim.x * ACT_THREADS)
         mx = max(mx, mag_max8(ldg_cg_v4(X + 8 * c)));
@@ -97,6 +101,8 @@ __global__ void __launch_bounds__(ACT_THREADS) act_tensor_codes_kernel(const uin
                                                                         const uint32_t* partials, int nparts,
                                                                         int8_t* Xq, float* x_scale) {
     __shared__ uint32_t red[ACT_THREADS / 32];
+    griddep_launch_dependents();
+    griddep_wait();
     uint32_t mx = 0u;
     for (int i = threadIdx.x; i < nparts; i += ACT_THREADS) mx = max(mx, partials[i]);
     const float s = act_scale(block_max(mx, red));
@@ -107,8 +113,27 @@ __global__ void __launch_bounds__(ACT_THREADS) act_tensor_codes_kernel(const uin
 
 // int8 codes -> the same values in bf16 (exact), eight a thread per step
 __global__ void __launch_bounds__(ACT_THREADS) widen_kernel(const int8_t* Xq, int64_t n8, uint16_t* Xb) {
+    griddep_launch_dependents();
+    griddep_wait();
     for (int64_t i = (int64_t)blockIdx.x * ACT_THREADS + threadIdx.x; i < n8; i += (int64_t)gridDim.x * ACT_THREADS)
         *reinterpret_cast<uint4*>(Xb + 8 * i) = widen_i8x8(*reinterpret_cast<const uint2*>(Xq + 8 * i));
+}
+
+// launch with programmatic dependent launch: the kernel waits for the one before it
+// (griddepcontrol.wait) before reading its input, and lets the one after it start
+template <typename... Args>
+static cudaError_t launch_pdl(void (*kern)(Args...), int blocks, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+    cfg.blockDim = dim3(ACT_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 // blocks of a grid-stride launch: one wave, no more than the chunks need
@@ -124,20 +149,17 @@ static cudaError_t wave_blocks(const void* kern, int64_t nch, int cap, int* bloc
 cudaError_t launch_quantize_activation(const uint16_t* X, int64_t M, int64_t K, bool per_token, int8_t* Xq,
                                        float* x_scale, uint32_t* partials, cudaStream_t stream) {
     if (per_token || M == 1) {
-        act_rows_kernel<<<(unsigned)M, ACT_THREADS, 0, stream>>>(X, (int)K, Xq, x_scale);
-        return cudaGetLastError();
+        return launch_pdl(act_rows_kernel, (int)M, stream, X, (int)K, Xq, x_scale);
     }
     const int64_t nch = M * K / 8;
     int blocks = 0;
     cudaError_t e = wave_blocks(reinterpret_cast<const void*>(act_partial_max_kernel), nch, ACT_MAX_PARTIALS, &blocks);
     if (e != cudaSuccess) return e;
-    act_partial_max_kernel<<<blocks, ACT_THREADS, 0, stream>>>(X, nch, partials);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_pdl(act_partial_max_kernel, blocks, stream, X, nch, partials)) != cudaSuccess) return e;
     const int nparts = blocks;
     if ((e = wave_blocks(reinterpret_cast<const void*>(act_tensor_codes_kernel), nch, 1 << 30, &blocks)) != cudaSuccess)
         return e;
-    act_tensor_codes_kernel<<<blocks, ACT_THREADS, 0, stream>>>(X, nch, partials, nparts, Xq, x_scale);
-    return cudaGetLastError();
+    return launch_pdl(act_tensor_codes_kernel, blocks, stream, X, nch, (const uint32_t*)partials, nparts, Xq, x_scale);
 }
 
 cudaError_t launch_widen_i8(const int8_t* Xq, int64_t n, uint16_t* Xb, cudaStream_t stream) {
@@ -145,8 +167,7 @@ cudaError_t launch_widen_i8(const int8_t* Xq, int64_t n, uint16_t* Xb, cudaStrea
     int blocks = 0;
     const cudaError_t e = wave_blocks(reinterpret_cast<const void*>(widen_kernel), n8, 1 << 30, &blocks);
     if (e != cudaSuccess) return e;
-    widen_kernel<<<blocks, ACT_THREADS, 0, stream>>>(Xq, n8, Xb);
-    return cudaGetLastError();
+    return launch_pdl(widen_kernel, blocks, stream, Xq, n8, Xb);
 }
 
 }  // namespace w4
