@@ -483,9 +483,17 @@ def int8_rows(args, w4, wl, device, stream, dist, peaks, cases, stack, ws_ms):
             w4.w4_quantize_activation_i8(x, False, out=(q, s_), workspace=qws)
             w4.w4_linear_i8(q, s_, False, Wq, sc, of, c.group_size, out=y, workspace=ws)
 
+    dws = w4.Workspace(device, max(w4.w4_linear_i8_dynamic_workspace_bytes(c.M, c.N, c.K, c.group_size)
+                                   for c in cases))
+
+    def fused():
+        for c, x, y, (Wq, sc, of) in zip(cases, stack.xv, stack.yv, stack.packed):
+            w4.w4_linear_i8_dynamic(x, Wq, sc, of, c.group_size, out=y, workspace=dws)
+
     act_bytes = sum(2 * c.M * c.K + c.M * c.K + 4 for c in cases)  # X read, codes written, the scale
-    for name, fn, extra, launches in (("decode_step_int8_codes", lin_only, 0, 1), ("decode_step_int8_dynamic", dynamic,
-                                                                                   act_bytes, 2)):
+    for name, fn, extra, launches in (("decode_step_int8_codes", lin_only, 0, 1),
+                                      ("decode_step_int8_dynamic", dynamic, act_bytes, 2),
+                                      ("decode_step_int8_one_call", fused, sum(2 * c.M * c.K for c in cases), 1)):
         with torch.cuda.stream(stream):
             fn()
             stream.synchronize()
@@ -499,10 +507,12 @@ def int8_rows(args, w4, wl, device, stream, dist, peaks, cases, stack, ws_ms):
         out[name] = {"unit": "GB/s", "value": round(gbs, 1), "ms_per_step": round(t / args.steps, 4),
                      "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4), "time_vs_bf16_step": round(t / ws_ms, 3),
                      "launches_per_step": launches * len(cases),
-                     "kernel": "stream_kernel on int8 codes (w4_linear_i8)" +
-                               (" + act_rows_kernel (w4_quantize_activation_i8)" if launches == 2 else ""),
+                     "kernel": ("stream_kernel quantizing bf16 X itself (w4_linear_i8_dynamic)" if name.endswith("one_call")
+                                else "stream_kernel on int8 codes (w4_linear_i8)" +
+                                (" + act_rows_kernel (w4_quantize_activation_i8)" if launches == 2 else "")),
                      "how": "the headline step's 224 linears on int8 activation codes, one scale per tensor, CUDA graph" +
                             ("; each linear's activations quantized inside the step" if launches == 2 else
+                             "; one call a linear: the kernel quantizes its bf16 X" if name.endswith("one_call") else
                              "; codes made before the timed region")}
         del g
     # prefill: the gate projection at M = 2048 on int8 activations, L2 flushed before each call

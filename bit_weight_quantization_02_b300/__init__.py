@@ -23,7 +23,8 @@ __all__ = [
     "library_path", "load_library", "w4_quantize", "w4_dequantize", "w4_linear",
     "w4_linear_ex", "w4_packed_bytes", "w4_qparam_bytes", "w4_device_fault", "w4_format_version",
     "w4_linear_static", "w4_linear_bias", "w4_packed_bytes_bits", "w4_quantize_bits", "w4_dequantize_bits", "w4_linear_bits",
-    "w4_quantize_activation_i8", "w4_linear_i8", "w4_linear_i8_workspace_bytes",
+    "w4_quantize_activation_i8", "w4_linear_i8", "w4_linear_i8_workspace_bytes", "w4_linear_i8_dynamic",
+    "w4_linear_i8_dynamic_workspace_bytes",
 ]
 
 W4_FORMAT_VERSION = 1
@@ -86,6 +87,8 @@ def load_library():
             "w4_quantize_activation_i8": ([p, i64, i64, i32, p, p, p, sz, p], i32),
             "w4_linear_i8_workspace_bytes": ([i64, i64, i64, i32], sz),
             "w4_linear_i8": ([p, p, i32, i64, i64, p, p, p, i64, i32, p, p, p, sz, p], i32),
+            "w4_linear_i8_dynamic_workspace_bytes": ([i64, i64, i64, i32], sz),
+            "w4_linear_i8_dynamic": ([p, i32, i64, i64, p, p, p, i64, i32, p, p, p, sz, p], i32),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -341,6 +344,36 @@ def w4_linear_i8(Xq: torch.Tensor, x_scale: torch.Tensor, per_token: bool, Wq: t
     _check(lib.w4_linear_i8(_ptr(Xq), _ptr(x_scale), int(bool(per_token)), M, K, _ptr(Wq), _ptr(scales), _ptr(offsets),
                             N, group_size, _ptr(bias), _ptr(Y), _ptr(workspace.buf), workspace.nbytes, _stream(Xq)),
            "w4_linear_i8")
+    return Y
+
+
+def w4_linear_i8_dynamic_workspace_bytes(M: int, N: int, K: int, group_size: int) -> int:
+    return load_library().w4_linear_i8_dynamic_workspace_bytes(M, N, K, group_size)
+
+
+def w4_linear_i8_dynamic(X: torch.Tensor, Wq: torch.Tensor, scales: torch.Tensor, offsets: torch.Tensor,
+                         group_size: int, per_token: bool = False, bias: torch.Tensor | None = None, out=None,
+                         workspace: Workspace | None = None):
+    """Y bf16 [M,N]: X bf16 [M,K] quantized to int8 (one scale per tensor, or per token) and the
+    int8 linear on the codes, in one call (bit-identical to the two separate calls)."""
+    lib = load_library()
+    _bits16(X, "X")
+    M, K = X.shape
+    N = Wq.shape[0]
+    if bias is not None:
+        _bits16(bias, "bias")
+        if bias.numel() != N:
+            raise ValueError("bias must hold N values")
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    if workspace is None:
+        key = ("i8", X.device.index, torch.cuda.current_stream(X.device).cuda_stream)
+        workspace = _default_ws.get(key)
+        if workspace is None:
+            workspace = _default_ws[key] = Workspace(X.device)
+        workspace.reserve(lib.w4_linear_i8_dynamic_workspace_bytes(M, N, K, group_size))
+    _check(lib.w4_linear_i8_dynamic(_ptr(X), int(bool(per_token)), M, K, _ptr(Wq), _ptr(scales), _ptr(offsets), N,
+                                    group_size, _ptr(bias), _ptr(Y), _ptr(workspace.buf), workspace.nbytes, _stream(X)),
+           "w4_linear_i8_dynamic")
     return Y
 
 

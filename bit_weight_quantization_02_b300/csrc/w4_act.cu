@@ -23,13 +23,6 @@
 namespace w4 {
 
 constexpr int ACT_THREADS = 256;
-constexpr float ACT_EPS = 1e-6f;  // the scale's lower bound (an all-zero X)
-
-__device__ __forceinline__ uint32_t mag_max8(uint4 v) {
-    const uint32_t a = max(v.x & 0x7FFFu, (v.x >> 16) & 0x7FFFu), b = max(v.y & 0x7FFFu, (v.y >> 16) & 0x7FFFu);
-    const uint32_t c = max(v.z & 0x7FFFu, (v.z >> 16) & 0x7FFFu), d = max(v.w & 0x7FFFu, (v.w >> 16) & 0x7FFFu);
-    return max(max(a, b), max(c, d));
-}
 
 // the maximum over the block's ACT_THREADS threads (red: ACT_THREADS / 32 words)
 __device__ __forceinline__ uint32_t block_max(uint32_t v, uint32_t* red) {
@@ -48,20 +41,13 @@ __device__ __forceinline__ uint32_t block_max(uint32_t v, uint32_t* red) {
     return red[0];
 }
 
-__device__ __forceinline__ float act_scale(uint32_t mag_bits) {
-    const float s = __fdiv_rn(__uint_as_float(mag_bits << 16), 127.0f);
-    return s < ACT_EPS ? ACT_EPS : s;
-}
-
 // eight bf16 values -> eight int8 codes (the lowest k in the lowest byte)
 __device__ __forceinline__ uint2 act_codes8(uint4 v, float s) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t out[2] = {0u, 0u};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const uint32_t h = (w[i >> 1] >> (16 * (i & 1))) & 0xFFFFu;
-        int q = __float2int_rn(__fdiv_rn(__uint_as_float(h << 16), s));
-        q = min(127, max(-127, q));
+        const int q = act_code((w[i >> 1] >> (16 * (i & 1))) & 0xFFFFu, s);
         out[i >> 2] |= ((uint32_t)q & 0xFFu) << (8 * (i & 3));
     }
     return make_uint2(out[0], out[1]);
@@ -76,8 +62,8 @@ __global__ void __launch_bounds__(ACT_THREADS) act_rows_kernel(const uint16_t* X
     int8_t* q = Xq + (int64_t)blockIdx.x * K;
     const int nch = K / 8;
     uint32_t mx = 0u;
-    for (int c = threadIdx.x; c < nch; c += ACT_THREADS) mx = max(mx, mag_max8(ldg_cg_v4(x + 8 * c)));
-    const float s = act_scale(block_max(mx, red));
+    for (int c = threadIdx.x; c < nch; c += ACT_THREADS) mx = max(mx, act_mag_max8(ldg_cg_v4(x + 8 * c)));
+    const float s = act_scale_of(block_max(mx, red));
     for (int c = threadIdx.x; c < nch; c += ACT_THREADS)
         *reinterpret_cast<uint2*>(q + 8 * c) = act_codes8(ldg_cg_v4(x + 8 * c), s);
     if (threadIdx.x == 0) x_scale[blockIdx.x] = s;
@@ -91,7 +77,7 @@ __global__ void __launch_bounds__(ACT_THREADS) act_partial_max_kernel(const uint
     griddep_wait();
     uint32_t mx = 0u;
     for (int64_t c = (int64_t)blockIdx.x * ACT_THREADS + threadIdx.x; c < nch; c += (int64_t)gridDim.x * ACT_THREADS)
-        mx = max(mx, mag_max8(ldg_cg_v4(X + 8 * c)));
+        mx = max(mx, act_mag_max8(ldg_cg_v4(X + 8 * c)));
     mx = block_max(mx, red);
     if (threadIdx.x == 0) partials[blockIdx.x] = mx;
 }
@@ -105,7 +91,7 @@ __global__ void __launch_bounds__(ACT_THREADS) act_tensor_codes_kernel(const uin
     griddep_wait();
     uint32_t mx = 0u;
     for (int i = threadIdx.x; i < nparts; i += ACT_THREADS) mx = max(mx, partials[i]);
-    const float s = act_scale(block_max(mx, red));
+    const float s = act_scale_of(block_max(mx, red));
     for (int64_t c = (int64_t)blockIdx.x * ACT_THREADS + threadIdx.x; c < nch; c += (int64_t)gridDim.x * ACT_THREADS)
         *reinterpret_cast<uint2*>(Xq + 8 * c) = act_codes8(ldg_cg_v4(X + 8 * c), s);
     if (blockIdx.x == 0 && threadIdx.x == 0) x_scale[0] = s;

@@ -270,6 +270,63 @@ I8Plan plan_i8(int64_t M, int64_t N, int64_t K, int g) {
     return p;
 }
 
+size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+// The int8 linear's launches, arguments already checked (the workspace holds p.total bytes).
+w4_status linear_i8_run(const I8Plan& p, const int8_t* Xq, const float* x_scale, int per_token, int64_t M, int64_t K,
+                        const uint8_t* Wq, const uint16_t* scales, const uint16_t* offsets, int64_t N, int group_size,
+                        const uint16_t* bias, uint16_t* Y, void* workspace, void* stream) {
+    w4::Epilogue ep;
+    ep.bias = bias;
+    ep.yscale = x_scale;
+    ep.ys_stride = per_token ? 1 : 0;
+    const char* detail = "";
+    cudaError_t e;
+    if (p.direct) {
+        e = w4::launch_stream_i8(p.sp, Xq, M, K, Wq, scales, offsets, N, group_size, Y, workspace,
+                                 (cudaStream_t)stream, &detail, ep);
+        if (e != cudaSuccess) return fail(W4_ERR_CUDA, "int8 stream linear: %s %s", cudaGetErrorString(e), detail);
+        return W4_OK;
+    }
+    uint16_t* Xb = reinterpret_cast<uint16_t*>(static_cast<unsigned char*>(workspace) + w4::I8_SCRATCH_OFFSET);
+    e = w4::launch_widen_i8(Xq, M * K, Xb, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "int8 widen launch");
+    if (p.stream_ok)
+        e = w4::launch_stream(p.sp, Xb, M, K, Wq, scales, offsets, N, group_size, Y, workspace, (cudaStream_t)stream,
+                              &detail, ep);
+    else
+        e = w4::launch_gemm(Xb, M, K, Wq, scales, offsets, N, group_size, 4, Y, (cudaStream_t)stream, &detail, ep);
+    if (e != cudaSuccess) return fail(W4_ERR_CUDA, "int8 linear: %s %s", cudaGetErrorString(e), detail);
+    return W4_OK;
+}
+
+// The dynamic int8 linear: up to 4 tokens one fused kernel (the stream kernel codes X
+// itself); otherwise the activation quantization into the workspace (codes, scales and
+// partial maxima after the int8 linear's own scratch), then the int8 linear.
+struct DynI8Plan {
+    bool fused;
+    w4::StreamPlan sp;
+    I8Plan lin;
+    size_t xq_off, xs_off, part_off;  // composed path: offsets in the workspace
+    size_t total;
+};
+
+DynI8Plan plan_dyn_i8(int64_t M, int64_t N, int64_t K, int g) {
+    DynI8Plan d{};
+    d.fused = M <= 4 && w4::plan_stream(M, N, K, g, &d.sp);
+    if (d.fused) {
+        d.total = d.sp.ws_bytes;
+        return d;
+    }
+    d.lin = plan_i8(M, N, K, g);
+    const size_t base = std::max(d.lin.total, (size_t)w4::I8_SCRATCH_OFFSET);
+    d.xq_off = round256(base);
+    d.xs_off = d.xq_off + round256((size_t)(M * K));
+    d.part_off = d.xs_off + round256((size_t)M * 4);
+    d.total = d.part_off + (size_t)w4::ACT_MAX_PARTIALS * 4;
+    return d;
+}
+
 }  // namespace
 
 extern "C" {
@@ -303,28 +360,57 @@ w4_status w4_linear_i8(const int8_t* Xq, const float* x_scale, int per_token, in
                         p.total);
         if (!aligned16(workspace)) return fail(W4_ERR_MISALIGNED, "workspace is not 16-byte aligned");
     }
-    w4::Epilogue ep;
-    ep.bias = bias;
-    ep.yscale = x_scale;
-    ep.ys_stride = per_token ? 1 : 0;
-    const char* detail = "";
-    cudaError_t e;
-    if (p.direct) {
-        e = w4::launch_stream_i8(p.sp, Xq, M, K, Wq, scales, offsets, N, group_size, Y, workspace,
-                                 (cudaStream_t)stream, &detail, ep);
-        if (e != cudaSuccess) return fail(W4_ERR_CUDA, "int8 stream linear: %s %s", cudaGetErrorString(e), detail);
+    return linear_i8_run(p, Xq, x_scale, per_token, M, K, Wq, scales, offsets, N, group_size, bias, Y, workspace,
+                         stream);
+}
+
+size_t w4_linear_i8_dynamic_workspace_bytes(int64_t M, int64_t N, int64_t K, int group_size) {
+    if (check_shape(N, K, group_size) != W4_OK || M < 1 || N == 0 || M > 0x7FFFFFFFLL) return 0;
+    return plan_dyn_i8(M, N, K, group_size).total;
+}
+
+w4_status w4_linear_i8_dynamic(const uint16_t* X, int per_token, int64_t M, int64_t K, const uint8_t* Wq,
+                               const uint16_t* scales, const uint16_t* offsets, int64_t N, int group_size,
+                               const uint16_t* bias, uint16_t* Y, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+    W4_TRY(check_shape(N, K, group_size));
+    if (M < 0 || M > 0x7FFFFFFFLL) return fail(W4_ERR_INVALID_ARG, "M = %lld must lie in [0, 2^31)", (long long)M);
+    if (M > 0 && K > (int64_t(1) << 62) / M) return fail(W4_ERR_INVALID_ARG, "M*K overflows");
+    if (per_token != 0 && per_token != 1) return fail(W4_ERR_INVALID_ARG, "per_token must be 0 or 1");
+    if (M == 0 || N == 0) return W4_OK;
+    W4_TRY(check_ptr(X, "X"));
+    W4_TRY(check_ptr(Wq, "Wq"));
+    W4_TRY(check_ptr(scales, "scales"));
+    W4_TRY(check_ptr(offsets, "offsets"));
+    W4_TRY(check_ptr(Y, "Y"));
+    if (bias != nullptr && (reinterpret_cast<uintptr_t>(bias) & 1u))
+        return fail(W4_ERR_MISALIGNED, "bias is not 2-byte aligned");
+    const DynI8Plan d = plan_dyn_i8(M, N, K, group_size);
+    if (workspace == nullptr || workspace_bytes < d.total)
+        return fail(W4_ERR_INVALID_ARG,
+                    "the dynamic int8 linear needs %zu workspace bytes (w4_linear_i8_dynamic_workspace_bytes)",
+                    d.total);
+    if (!aligned16(workspace)) return fail(W4_ERR_MISALIGNED, "workspace is not 16-byte aligned");
+    if (d.fused) {
+        w4::Epilogue ep;
+        ep.bias = bias;
+        ep.ys_stride = per_token ? 1 : 0;
+        const char* detail = "";
+        const cudaError_t e = w4::launch_stream_qx(d.sp, X, M, K, Wq, scales, offsets, N, group_size, Y, workspace,
+                                                   (cudaStream_t)stream, &detail, ep);
+        if (e != cudaSuccess)
+            return fail(W4_ERR_CUDA, "dynamic int8 stream linear: %s %s", cudaGetErrorString(e), detail);
         return W4_OK;
     }
-    uint16_t* Xb = reinterpret_cast<uint16_t*>(static_cast<unsigned char*>(workspace) + w4::I8_SCRATCH_OFFSET);
-    e = w4::launch_widen_i8(Xq, M * K, Xb, (cudaStream_t)stream);
-    if (e != cudaSuccess) return cuda_fail(e, "int8 widen launch");
-    if (p.stream_ok)
-        e = w4::launch_stream(p.sp, Xb, M, K, Wq, scales, offsets, N, group_size, Y, workspace, (cudaStream_t)stream,
-                              &detail, ep);
-    else
-        e = w4::launch_gemm(Xb, M, K, Wq, scales, offsets, N, group_size, 4, Y, (cudaStream_t)stream, &detail, ep);
-    if (e != cudaSuccess) return fail(W4_ERR_CUDA, "int8 linear: %s %s", cudaGetErrorString(e), detail);
-    return W4_OK;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    int8_t* Xq = reinterpret_cast<int8_t*>(ws + d.xq_off);
+    float* xs = reinterpret_cast<float*>(ws + d.xs_off);
+    const cudaError_t e = w4::launch_quantize_activation(X, M, K, per_token != 0, Xq, xs,
+                                                         reinterpret_cast<uint32_t*>(ws + d.part_off),
+                                                         (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "activation quantize launch");
+    return linear_i8_run(d.lin, Xq, xs, per_token, M, K, Wq, scales, offsets, N, group_size, bias, Y, workspace,
+                         stream);
 }
 
 size_t w4_packed_bytes(int64_t N, int64_t K) {

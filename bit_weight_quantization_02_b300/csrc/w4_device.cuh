@@ -55,6 +55,36 @@ __device__ __forceinline__ uint4 widen_i8x8(uint2 v) {
     }
     return make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
 }
+// Dynamic int8 activation quantization (w4_act.cu, and the stream kernel's
+// fused mode): the largest magnitude of eight bf16 values as magnitude bits
+// (bits & 0x7FFF order like magnitudes for finite values), the scale
+// s = max|x| / 127 (one IEEE division, at least 1e-6), and eight codes
+// q = clamp(rne(x / s), -127, 127) (one IEEE division each).
+__device__ __forceinline__ uint32_t act_mag_max8(uint4 v) {
+    const uint32_t a = max(v.x & 0x7FFFu, (v.x >> 16) & 0x7FFFu), b = max(v.y & 0x7FFFu, (v.y >> 16) & 0x7FFFu);
+    const uint32_t c = max(v.z & 0x7FFFu, (v.z >> 16) & 0x7FFFu), d = max(v.w & 0x7FFFu, (v.w >> 16) & 0x7FFFu);
+    return max(max(a, b), max(c, d));
+}
+__device__ __forceinline__ float act_scale_of(uint32_t mag_bits) {
+    const float s = __fdiv_rn(__uint_as_float(mag_bits << 16), 127.0f);
+    return s < 1e-6f ? 1e-6f : s;
+}
+__device__ __forceinline__ int act_code(uint32_t h, float s) {
+    const int q = __float2int_rn(__fdiv_rn(__uint_as_float(h << 16), s));
+    return min(127, max(-127, q));
+}
+// eight bf16 values -> their eight codes as bf16 (exact), in the same order
+__device__ __forceinline__ uint4 act_codes_bf16x8(uint4 v, float s) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t lo = __float_as_uint((float)act_code(w[i] & 0xFFFFu, s)) >> 16;
+        const uint32_t hi = __float_as_uint((float)act_code(w[i] >> 16, s)) >> 16;
+        o[i] = lo | (hi << 16);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
 __device__ __forceinline__ uint32_t ldg_nc_u16(const uint16_t* p) {
     unsigned short v;
     asm("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));

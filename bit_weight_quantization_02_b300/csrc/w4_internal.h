@@ -71,6 +71,12 @@ cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, 
 cudaError_t launch_stream_i8(const StreamPlan& plan, const int8_t* Xq, int64_t M, int64_t K, const uint8_t* Wq,
                              const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
                              void* workspace, cudaStream_t stream, const char** detail, const Epilogue& ep);
+// The same kernel on bf16 X that it quantizes to int8 codes itself (M <= 4), with
+// w4_quantize_activation_i8's scale (ep.ys_stride 1: one per token, else one for
+// the tensor); ep.yscale is ignored (each block uses the scale it computes).
+cudaError_t launch_stream_qx(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
+                             const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
+                             void* workspace, cudaStream_t stream, const char** detail, const Epilogue& ep);
 cudaError_t read_and_clear_stream_fault(unsigned int* fault);
 // Batched decode (5 <= M <= 32): 64-row units, the block's X slice staged once
 // by TMA; same plan and workspace as the stream kernel (launch_stream calls it).

@@ -92,9 +92,15 @@ __host__ __device__ inline int st_smem_bytes(int M, int g, int rt) {
 __device__ unsigned int g_stream_fault;
 constexpr uint64_t ST_WAIT_LIMIT_NS = 2000000000ull;
 
-// XI8: X holds int8 activation codes (p.X points at bytes), widened to bf16 when
-// loaded; the activation scale is applied by the epilogue.
-template <int G, int MX, bool QT, int RT, bool XI8>
+// XM, what X holds: 0 bf16 activations; 1 int8 activation codes (p.X points at
+// bytes), widened to bf16 when loaded, their scale applied by the epilogue
+// (p.ep.yscale); 2 bf16 activations quantized here to int8 codes with the
+// dynamic symmetric scale of w4_quantize_activation_i8 (one for the tensor, or
+// one per token when p.ep.ys_stride is 1): each block finds the maximum
+// magnitude of X first (after the dependency wait, with its weight copies in
+// flight), then codes every X chunk as it loads it, exactly as the separate
+// quantization would, and its epilogue applies the scale.
+template <int G, int MX, bool QT, int RT, int XM>
 __global__ void __launch_bounds__(ST_THREADS, RT == 2 ? 4 : 6)
 stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
               const __grid_constant__ CUtensorMap tm_o, const StreamArgs p) {
@@ -116,11 +122,50 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
     const int worker = blockIdx.x * ST_WARPS + warp;
 
     griddep_launch_dependents();
-    if (worker >= p.workers) return;
-    const long long u0 = p.units * worker / p.workers;
-    const long long u1 = p.units * (worker + 1) / p.workers;
-    if (u0 >= u1) return;
+    const bool idle = worker >= p.workers;
+    const long long u0 = idle ? 0 : p.units * worker / p.workers;
+    const long long u1 = idle ? 0 : p.units * (worker + 1) / p.workers;
+    // XM 2: the block's scale(s) of X, found by all of its warps (two block barriers)
+    __shared__ uint32_t qx_red[ST_WARPS][MX];
+    __shared__ float qx_scale[MX];
+    auto find_scales = [&]() {
+        uint32_t mx[MX];
+#pragma unroll
+        for (int m = 0; m < MX; ++m) {
+            mx[m] = 0u;
+            if (m < p.M)
+                for (int c = threadIdx.x; c < p.K / 8; c += ST_THREADS)
+                    mx[m] = max(mx[m], act_mag_max8(ldg_cg_v4(p.X + (int64_t)m * p.K + 8 * c)));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx[m] = max(mx[m], __shfl_xor_sync(0xffffffffu, mx[m], o));
+            if (lane == 0) qx_red[warp][m] = mx[m];
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            uint32_t all = 0u;  // one scale for the tensor: the maximum over its rows
+            for (int m = 0; m < p.M; ++m)
+                for (int w = 0; w < ST_WARPS; ++w) all = max(all, qx_red[w][m]);
+            for (int m = 0; m < p.M; ++m) {
+                uint32_t row = 0u;
+                for (int w = 0; w < ST_WARPS; ++w) row = max(row, qx_red[w][m]);
+                qx_scale[m] = act_scale_of(p.ep.ys_stride ? row : all);
+            }
+        }
+        __syncthreads();
+    };
+    if (u0 >= u1) {
+        if constexpr (XM == 2) {  // an idle warp still helps its block find the scales
+            griddep_wait();
+            find_scales();
+        }
+        return;
+    }
     const int nunits = (int)(u1 - u0);
+    Epilogue ep = p.ep;  // XM 2: the output scale is the block's own
+    if constexpr (XM == 2) {
+        ep.yscale = qx_scale;
+        ep.ys_stride = p.ep.ys_stride ? 1 : 0;
+    }
 
     const int rest = st_rest_bytes(p.M, G, RT);
     const uint32_t wslots = smem_u32(smem) + warp * (DEPTH * WSLOT);
@@ -206,6 +251,15 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
 
     // activations may come from the previous kernel: wait for it
     griddep_wait();
+    float qs[MX];  // XM 2: the scale of each token's codes
+#pragma unroll
+    for (int m = 0; m < MX; ++m) qs[m] = 1.f;
+    if constexpr (XM == 2) {
+        find_scales();
+#pragma unroll
+        for (int m = 0; m < MX; ++m)
+            if (m < p.M) qs[m] = qx_scale[m];
+    }
 
     // X of a unit: lane c holds 8-k chunk c of every token (staged path)
     uint4 xr[MX];
@@ -215,9 +269,12 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
 #pragma unroll
         for (int m = 0; m < MX; ++m)
             if (m < p.M) {
-                if constexpr (XI8)
+                if constexpr (XM == 1)
                     xr[m] = (k < p.K) ? widen_i8x8(ldg_cg_v2(reinterpret_cast<const int8_t*>(p.X) + 8 * lane +
                                                              (int64_t)m * p.K + kc * ST_UK))
+                                      : make_uint4(0u, 0u, 0u, 0u);
+                else if constexpr (XM == 2)
+                    xr[m] = (k < p.K) ? act_codes_bf16x8(ldg_cg_v4(xlane + (int64_t)m * p.K + kc * ST_UK), qs[m])
                                       : make_uint4(0u, 0u, 0u, 0u);
                 else
                     xr[m] = (k < p.K) ? ldg_cg_v4(xlane + (int64_t)m * p.K + kc * ST_UK) : make_uint4(0u, 0u, 0u, 0u);
@@ -390,9 +447,9 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 for (int rt = 0; rt < RT; ++rt) {
                     const int n_a = tile * ROWS + 16 * rt + pr, n_b = n_a + 8;
                     if (tq == 0 && n_a < p.N)
-                        p.Y[n_a] = (uint16_t)float_to_bf16_bits(epilogue_f32(p.ep, racc[rt][0][0], 0, n_a));
+                        p.Y[n_a] = (uint16_t)float_to_bf16_bits(epilogue_f32(ep, racc[rt][0][0], 0, n_a));
                     if (tq == 0 && n_b < p.N)
-                        p.Y[n_b] = (uint16_t)float_to_bf16_bits(epilogue_f32(p.ep, racc[rt][0][2], 0, n_b));
+                        p.Y[n_b] = (uint16_t)float_to_bf16_bits(epilogue_f32(ep, racc[rt][0][2], 0, n_b));
                 }
             } else if (kc_first != 0) {  // a later share of the tile (the first of this range): publish it
 #pragma unroll
@@ -418,7 +475,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                     for (int i = 0; i < 4; ++i) {
                         const int m = 8 * t + 2 * tq + (i & 1), n = (i < 2) ? n_a : n_b;
                         if (m < p.M && n < p.N)
-                            p.Y[(int64_t)m * p.N + n] = (uint16_t)float_to_bf16_bits(epilogue_f32(p.ep, acc[t][i], m, n));
+                            p.Y[(int64_t)m * p.N + n] = (uint16_t)float_to_bf16_bits(epilogue_f32(ep, acc[t][i], m, n));
                     }
             } else if (kc_first != 0) {  // a later share of the tile (the first of this range): publish it
                 split_publish<MT>(p.ws + (size_t)worker * 16 * p.M, acc, p.M, min(16, p.N - tile * 16), pr, tq);
@@ -441,12 +498,12 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
                 ok = split_collect<1, NE>(oacc[rt], scr + rt * 16, p.ws + rt * 16, (size_t)RT * 16, worker, wl, 1,
                                           min(16, p.N - (tile * ROWS + 16 * rt)), pr, tq, lane,
                                           p.Y + (int64_t)tile * ROWS + 16 * rt, p.N, &g_stream_fault, 2u,
-                                          ST_WAIT_LIMIT_NS, epilogue_at(p.ep, (int64_t)tile * ROWS + 16 * rt)) &&
+                                          ST_WAIT_LIMIT_NS, epilogue_at(ep, (int64_t)tile * ROWS + 16 * rt)) &&
                      ok;
         } else {
             ok = split_collect<MT, NE>(acc, scr, p.ws, (size_t)16 * p.M, worker, wl, p.M, min(16, p.N - tile * 16), pr,
                                        tq, lane, p.Y + (int64_t)tile * 16, p.N, &g_stream_fault, 2u,
-                                       ST_WAIT_LIMIT_NS, epilogue_at(p.ep, (int64_t)tile * 16)) &&
+                                       ST_WAIT_LIMIT_NS, epilogue_at(ep, (int64_t)tile * 16)) &&
                  ok;
         }
     }
@@ -476,10 +533,10 @@ bool plan_stream(int64_t M, int64_t N, int64_t K, int g, StreamPlan* plan) {
     return true;
 }
 
-template <int G, int MX, bool QT, int RT, bool XI8>
+template <int G, int MX, bool QT, int RT, int XM>
 static cudaError_t launch_stream_gm(const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& to, StreamArgs a,
                                     cudaStream_t stream) {
-    auto kern = stream_kernel<G, MX, QT, RT, XI8>;
+    auto kern = stream_kernel<G, MX, QT, RT, XM>;
     const size_t smem = (size_t)st_smem_bytes(a.M, G, RT);
     cudaError_t e = ensure_kernel_attrs(reinterpret_cast<const void*>(kern), st_smem_bytes(MX, G, RT), false);
     if (e != cudaSuccess) return e;
@@ -503,13 +560,13 @@ static cudaError_t launch_stream_gm(const CUtensorMap& tw, const CUtensorMap& ts
     return cudaLaunchKernelEx(&cfg, kern, tw, ts, to, a);
 }
 
-template <int G, bool QT, bool XI8>
+template <int G, bool QT, int XM>
 static cudaError_t launch_stream_g(const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& to, StreamArgs a,
                                    int rt, cudaStream_t stream) {
-    if (rt == 2) return launch_stream_gm<G, 1, QT, 2, XI8>(tw, ts, to, a, stream);
-    if (a.M <= 1) return launch_stream_gm<G, 1, QT, 1, XI8>(tw, ts, to, a, stream);
-    if (a.M <= 2) return launch_stream_gm<G, 2, QT, 1, XI8>(tw, ts, to, a, stream);
-    return launch_stream_gm<G, 4, QT, 1, XI8>(tw, ts, to, a, stream);
+    if (rt == 2) return launch_stream_gm<G, 1, QT, 2, XM>(tw, ts, to, a, stream);
+    if (a.M <= 1) return launch_stream_gm<G, 1, QT, 1, XM>(tw, ts, to, a, stream);
+    if (a.M <= 2) return launch_stream_gm<G, 2, QT, 1, XM>(tw, ts, to, a, stream);
+    return launch_stream_gm<G, 4, QT, 1, XM>(tw, ts, to, a, stream);
 }
 
 // One token takes 32-row units (two row tiles sharing the X staging, slice sums
@@ -517,7 +574,7 @@ static cudaError_t launch_stream_g(const CUtensorMap& tw, const CUtensorMap& ts,
 // warp one, and the workspace holds two 16-row slots per warp.
 template <int G, bool QT>
 static cudaError_t two_row_tiles(int64_t N, int nkc, size_t ws_bytes, bool* two) {
-    auto kern = stream_kernel<G, 1, QT, 2, false>;
+    auto kern = stream_kernel<G, 1, QT, 2, 0>;
     cudaError_t e = ensure_kernel_attrs(reinterpret_cast<const void*>(kern), st_smem_bytes(1, G, 2), false);
     int sms = 0, per_sm = 0;
     if (e == cudaSuccess)
@@ -529,12 +586,12 @@ static cudaError_t two_row_tiles(int64_t N, int nkc, size_t ws_bytes, bool* two)
     return cudaSuccess;
 }
 
-template <bool XI8>
+template <int XM>
 static cudaError_t launch_stream_t(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
                                    const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
                                    void* workspace, cudaStream_t stream, const char** detail, const Epilogue& ep) {
     if (M > 4) {  // 5..32 tokens: the block-shared X kernel (w4_batch.cu), bf16 X only
-        if (XI8) return cudaErrorInvalidValue;
+        if (XM != 0) return cudaErrorInvalidValue;
         return launch_batch(plan, X, M, K, Wq, scales, offsets, N, g, 4, Y, workspace, stream, detail, ep);
     }
     const int64_t ng = K / g;
@@ -579,24 +636,30 @@ static cudaError_t launch_stream_t(const StreamPlan& plan, const uint16_t* X, in
     a.workers = 0;
     switch (g) {
         case 32:
-            return qt ? launch_stream_g<32, true, XI8>(tw, ts, to, a, rt, stream)
-                      : launch_stream_g<32, false, XI8>(tw, ts, to, a, rt, stream);
-        case 64: return launch_stream_g<64, false, XI8>(tw, ts, to, a, rt, stream);
-        default: return launch_stream_g<128, false, XI8>(tw, ts, to, a, rt, stream);
+            return qt ? launch_stream_g<32, true, XM>(tw, ts, to, a, rt, stream)
+                      : launch_stream_g<32, false, XM>(tw, ts, to, a, rt, stream);
+        case 64: return launch_stream_g<64, false, XM>(tw, ts, to, a, rt, stream);
+        default: return launch_stream_g<128, false, XM>(tw, ts, to, a, rt, stream);
     }
 }
 
 cudaError_t launch_stream(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
                           const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
                           void* workspace, cudaStream_t stream, const char** detail, const Epilogue& ep) {
-    return launch_stream_t<false>(plan, X, M, K, Wq, scales, offsets, N, g, Y, workspace, stream, detail, ep);
+    return launch_stream_t<0>(plan, X, M, K, Wq, scales, offsets, N, g, Y, workspace, stream, detail, ep);
 }
 
 cudaError_t launch_stream_i8(const StreamPlan& plan, const int8_t* Xq, int64_t M, int64_t K, const uint8_t* Wq,
                              const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
                              void* workspace, cudaStream_t stream, const char** detail, const Epilogue& ep) {
-    return launch_stream_t<true>(plan, reinterpret_cast<const uint16_t*>(Xq), M, K, Wq, scales, offsets, N, g, Y,
-                                 workspace, stream, detail, ep);
+    return launch_stream_t<1>(plan, reinterpret_cast<const uint16_t*>(Xq), M, K, Wq, scales, offsets, N, g, Y,
+                              workspace, stream, detail, ep);
+}
+
+cudaError_t launch_stream_qx(const StreamPlan& plan, const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq,
+                             const uint16_t* scales, const uint16_t* offsets, int64_t N, int g, uint16_t* Y,
+                             void* workspace, cudaStream_t stream, const char** detail, const Epilogue& ep) {
+    return launch_stream_t<2>(plan, X, M, K, Wq, scales, offsets, N, g, Y, workspace, stream, detail, ep);
 }
 
 

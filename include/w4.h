@@ -259,6 +259,25 @@ W4_API w4_status w4_linear_i8(const int8_t *Xq, const float *x_scale, int per_to
                               const uint16_t *bias, uint16_t *Y, void *workspace,
                               size_t workspace_bytes, void *stream);
 
+/*
+ * w4_linear_i8_dynamic -- w4_quantize_activation_i8 and w4_linear_i8 in one call,
+ * on bf16 X [M][K]: Y is bit for bit what the two calls give (the same codes,
+ * scales and sums), without the codes leaving the GPU.  With at most 4 tokens
+ * one kernel does both: each of its blocks finds X's largest magnitude (of the
+ * tensor, or of each token with per_token = 1) while its first weights are on
+ * their way, then codes X as it stages it.  With more tokens, or a group count
+ * the stream kernel does not take, the two steps run in turn with the codes in
+ * the workspace.  workspace: w4_linear_i8_dynamic_workspace_bytes(M, N, K, g)
+ * bytes, 16-byte aligned, zero-filled once before the first use (its first
+ * 16 MiB as for w4_linear_i8; the rest is scratch).  Other arguments, accuracy
+ * and errors as w4_linear_i8 (X 16-byte aligned).
+ */
+W4_API size_t w4_linear_i8_dynamic_workspace_bytes(int64_t M, int64_t N, int64_t K, int group_size);
+W4_API w4_status w4_linear_i8_dynamic(const uint16_t *X, int per_token, int64_t M, int64_t K,
+                                      const uint8_t *Wq, const uint16_t *scales, const uint16_t *offsets,
+                                      int64_t N, int group_size, const uint16_t *bias, uint16_t *Y,
+                                      void *workspace, size_t workspace_bytes, void *stream);
+
 /* Sizes of the packed outputs: N*K/2 bytes of codes, N*(K/g)*2 bytes for each
  * of scales and offsets.  0 for invalid arguments. */
 W4_API size_t w4_packed_bytes(int64_t N, int64_t K);

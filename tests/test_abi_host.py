@@ -199,3 +199,15 @@ def test_other_code_widths_host_rules(lib):
     # 2-bit rows must be whole 16-byte pieces for the linear (K % 64), quantize takes any K % g == 0
     assert lib.w4_linear_bits(FAKE, 1, 96, FAKE, FAKE, FAKE, 4, 32, 2, FAKE, None, 0, None) == UNSUPPORTED
     assert b"K % 64" in lib.w4_last_error_detail()
+
+
+def test_every_exported_python_name_exists_and_covers_the_header():
+    """The binding carries the C calls under the same names; the few it does not wrap are
+    used inside it (error strings, the workspace-size helper behind the default workspace,
+    the _ex form behind keyword arguments, the wait self-test behind its own test)."""
+    missing = [n for n in w4.__all__ if not hasattr(w4, n)]
+    assert not missing, missing
+    internal = {"w4_last_error_detail", "w4_status_string", "w4_linear_bias_ex",
+                "w4_quantize_activation_workspace_bytes", "w4_selftest_bounded_waits"}
+    unbound = [n for n in declared_functions() if not hasattr(w4, n) and n not in internal]
+    assert not unbound, f"declared in include/*.h with no Python binding: {unbound}"

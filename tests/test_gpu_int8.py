@@ -217,3 +217,33 @@ def test_one_workspace_serves_every_shape_in_sequence():
     assert_ok = oracle.within_linear_tolerance(f64(gpu_linear(X, Wq, sc, of, g, workspace=ws)), y_ref)
     assert assert_ok[0], f"bf16 linear on the shared workspace: worst ratio {assert_ok[1]:.3f}"
     assert int(ws.buf[: 16 << 20].count_nonzero()) == 0  # the slots came back to zero
+
+
+DYN_SHAPES = [(1, 520, 512, 32), (2, 1030, 1024, 64), (3, 200, 4160, 32), (4, 4096, 4096, 128), (1, 8, 256, 32),
+              (1, 14336, 4096, 32), (1, 4096, 14336, 32), (5, 1030, 1024, 32), (33, 520, 512, 64), (4, 136, 96, 32)]
+
+
+@pytest.mark.parametrize("per_token", [False, True], ids=["tensor", "token"])
+@pytest.mark.parametrize("shape", DYN_SHAPES, ids=[f"m{m}_{n}x{k}g{g}" for m, n, k, g in DYN_SHAPES])
+def test_dynamic_call_is_the_two_calls_bit_for_bit(shape, per_token):
+    """w4_linear_i8_dynamic (one kernel up to 4 tokens, the two steps in turn beyond, or for
+    an odd group count) equals w4_quantize_activation_i8 + w4_linear_i8 bit for bit, and is
+    within the tolerance of the oracle; the workspace's slots come back to zero."""
+    M, N, K, g = shape
+    W = wl.gen_weight(N, K, seed=N + K, outliers=True)
+    Wq, sc, of = w4.w4_quantize(W.to(DEV), g)
+    X = wl.gen_activation(M, K, seed=M + 3).to(DEV)
+    bias = wl.gen_activation(1, N, seed=9)[0].to(DEV) if M % 2 else None
+    ws = w4.Workspace(DEV, w4.w4_linear_i8_dynamic_workspace_bytes(M, N, K, g))
+    Y = Guarded((M, N), torch.bfloat16)
+    w4.w4_linear_i8_dynamic(X, Wq, sc, of, g, per_token=per_token, bias=bias, out=Y.t, workspace=ws)
+    Y.check()
+    Xq, xs = w4.w4_quantize_activation_i8(X, per_token)
+    y2 = w4.w4_linear_i8(Xq, xs, per_token, Wq, sc, of, g, bias=bias)
+    assert torch.equal(Y.t.view(torch.int16), y2.view(torch.int16)), "one call and two calls differ"
+    y_ref = oracle.ref_linear_i8(Xq.cpu().numpy(), xs.cpu().numpy(), per_token, Wq.cpu().numpy(), bits(sc), bits(of),
+                                 g, bias=bits(bias.cpu()) if bias is not None else None)
+    ok, worst = oracle.within_linear_tolerance(f64(Y.t), y_ref)
+    assert ok, f"dynamic int8 M={M} N={N} K={K} g={g}: worst ratio {worst:.3f}"
+    assert int(ws.buf[: 16 << 20].count_nonzero()) == 0
+    w4.w4_device_fault(DEV)
