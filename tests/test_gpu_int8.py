@@ -84,6 +84,71 @@ def test_activation_quantize_exact_ties():
     np.testing.assert_array_equal(Xq.cpu().numpy(), rq)
 
 
+def _near_half_integer_rows(R, K, seed, common=False):
+    """R rows of K bf16 values, each row led by its own maximum m (one m for all rows when
+    common, for one scale per tensor), the rest mostly values x
+    for which the fp32 quotient x / s (s = m / 127) lies within 2^-13 of a half-integer: the
+    codes there come from the kernels' division fallback, or from their multiply path right at
+    its threshold.  Found by scanning every positive bf16 value below m on the host (IEEE fp32
+    division in numpy, as the method states it)."""
+    rng = np.random.default_rng(seed)
+    pos = np.arange(1, 0x7F80, dtype=np.uint32)          # positive finite bf16 bit patterns
+    vals = (pos << 16).view(np.float32)
+    X = np.zeros((R, K), np.uint16)
+    near_total = 0
+    for r in range(R):
+        if not common:
+            mb = int(rng.integers(0x3F80, 0x42C8))  # m in [1, 100)
+        elif r == 0:  # the m in [1, 100) with the most quotients near, but not on, a half-integer
+            best = -1
+            for cb in range(0x3F80, 0x42C8):
+                cm = np.array([cb << 16], np.uint32).view(np.float32)[0]
+                cs = np.float32(cm / np.float32(127.0))
+                cq = (vals[vals <= cm] / cs).astype(np.float32)
+                cd = np.abs(np.abs(cq - np.rint(cq)) - np.float32(0.5))
+                n = int(((cd > 0) & (cd < np.float32(2.0 ** -13))).sum())
+                if n > best:
+                    best, mb = n, cb
+        m = np.float32(np.array([mb << 16], np.uint32).view(np.float32)[0])
+        s = np.float32(m / np.float32(127.0))
+        below = vals <= m
+        q = (vals[below] / s).astype(np.float32)
+        d = np.abs(q - np.rint(q))
+        near = pos[below][np.abs(d - np.float32(0.5)) < np.float32(2.0 ** -13)]
+        rng.shuffle(near)
+        near = near[: K - 1 - K // 4]
+        near_total += len(near)
+        fill = rng.choice(pos[below], size=K - 1 - len(near))
+        row = np.concatenate([near, fill]).astype(np.uint16)
+        row |= (rng.integers(0, 2, size=row.size) << 15).astype(np.uint16)  # random signs
+        X[r, 0] = mb
+        X[r, 1:] = row
+    return X, near_total
+
+
+@pytest.mark.parametrize("per_token", [False, True], ids=["tensor", "token"])
+def test_activation_codes_near_half_integers(per_token):
+    """Codes of quotients within 2^-13 of a half-integer are bit-exact against the oracle, in the
+    activation kernels and in the stream kernel that quantizes X itself."""
+    R, K = 256, 512
+    X, near = _near_half_integer_rows(R, K, seed=11, common=not per_token)
+    assert near >= 200, near  # enough values on the fallback side of the threshold
+    rq, rs = oracle.ref_quantize_activation_i8(X, per_token=per_token)
+    Xq, xs = gpu_act(_x16(X), per_token)
+    np.testing.assert_array_equal(xs.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    np.testing.assert_array_equal(Xq.cpu().numpy(), rq)
+    W = wl.gen_weight(136, K, seed=5, outliers=False)
+    Wq, sc, of = w4.w4_quantize(W.to(DEV), 32)
+    for r0 in range(0, 16, 4):  # the one-call path (one kernel for up to 4 tokens) on the same rows
+        x4 = _x16(X[r0:r0 + 4])
+        y1 = w4.w4_linear_i8_dynamic(x4, Wq, sc, of, 32, per_token=per_token)
+        q4, s4 = w4.w4_quantize_activation_i8(x4, per_token)
+        y2 = w4.w4_linear_i8(q4, s4, per_token, Wq, sc, of, 32)
+        assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+        rq4, rs4 = oracle.ref_quantize_activation_i8(X[r0:r0 + 4], per_token=per_token)
+        np.testing.assert_array_equal(q4.cpu().numpy(), rq4)
+
+
 def _int8_problem(M, N, K, g, seed, per_token, with_bias):
     W = wl.gen_weight(N, K, seed=seed, outliers=True)
     X = wl.gen_activation(M, K, seed=seed + wl.ACT_SEED_OFFSET)
