@@ -10,26 +10,31 @@
 // The weights are the MMA's A operand and live in tensor memory: the
 // dequantization threads write w' straight from registers into TMEM
 // (tcgen05.st), so the bf16 weight tile never passes through shared memory,
-// and the tokens (X, through TMA) are the B operand in shared memory.  One
-// thread block computes a 128 weight rows x 256 tokens tile of Y^T (D in TMEM:
-// lane = weight row, column = token), walking K in 64-k steps; every
-// dequantized weight feeds 256 tokens.
-//   warp 0      TMA producer: a 5-deep ring of the X tile (256 tokens x 64 k,
-//               128-byte swizzle, the UMMA B layout) and the packed code tile
-//               (128 rows x 32 bytes, 32-byte swizzle); every 8 groups, when
-//               the rows allow it, a 2-deep ring of scale / offset boxes;
-//   warp 1      TMEM owner (512 columns: D in 0..255, five 32-column A
-//               stages above) and, on one lane, the UMMA issuer: 4 x
-//               tcgen05.mma (M=128 from TMEM, N=256, K=16) a step;
-//               one tcgen05.commit a step frees the stage (the TMA buffers and
-//               the A tile of the same index), and the issuer waits only for
-//               the A tile: the dequantization threads waited for the TMA
-//               stage first;
+// and the tokens (X, through TMA) are the B operand in shared memory.  A tile
+// is 128 weight rows x 256 tokens of Y^T (D in TMEM: lane = weight row,
+// column = token), walked along K in 64-k steps; every dequantized weight
+// feeds 256 tokens.  The grid is persistent: one block per SM takes tiles
+// blockIdx.x, + gridDim.x, ..., and every ring below runs on across tiles.
+//   warp 0      TMA producer: a 5-stage ring of the X tile (256 tokens x 64
+//               k, 128-byte swizzle, the UMMA B layout) and the packed code
+//               tile (128 rows x 32 bytes, 32-byte swizzle); every 8 groups,
+//               when the rows allow it, a 2-deep ring of scale / offset boxes;
+//   warp 1      TMEM owner (512 columns: D in 0..255, one 32-column A stage
+//               per ring stage above) and, on one lane, the UMMA issuer: 4 x
+//               tcgen05.mma (M=128 from TMEM, N=256, K=16) a step; one
+//               tcgen05.commit a step frees the stage (the TMA buffers and the
+//               A tile of the same index); it waits only for the A tile (the
+//               dequantization threads waited for the TMA stage first), and
+//               before a tile's first step for the epilogue to have read D;
 //   warps 2..9  dequantization: thread (row, 32-k half) of its TMEM
 //               sub-partition turns 32 codes into 16 bf16 pairs and stores
-//               them with one tcgen05.st; afterwards the same warps run the
-//               epilogue (tcgen05.ld -> bf16 -> shared-memory transpose ->
-//               64-byte runs of Y rows).
+//               them with one tcgen05.st;
+//   warps 10..17 epilogue, two per TMEM sub-partition (128 tokens each): D
+//               -> scale / bias -> bf16 pairs in registers, then D goes back
+//               to the issuer; the pairs go through a [token][row] slice of
+//               128 tokens in shared memory to a TMA store (plain stores when
+//               Y's rows are not 16-byte multiples), overlapping the next
+//               tile's main loop.
 // 2- and 8-bit codes (Optimum Quanto's int2 / int8 weights) run the same
 // pipeline with a code tile of 128 rows x 16 / 64 bytes per k block (no
 // swizzle / 64-byte swizzle).  2 bits: the pairs (q_i, q_i+8) of a 16-code
@@ -47,45 +52,101 @@
 
 namespace w4 {
 
-constexpr int GM_BW = 128;  // weight rows per block (UMMA M, TMEM lanes)
-constexpr int GM_BT = 256;  // tokens per block (UMMA N)
+constexpr int GM_BW = 128;  // weight rows per tile (UMMA M, TMEM lanes)
+constexpr int GM_BT = 256;  // tokens per tile (UMMA N)
 constexpr int GM_BK = 64;
-constexpr int GM_TSTAGES = 5;  // TMA ring: X tile + packed code tile per k block
-constexpr int GM_WSTAGES = GM_TSTAGES;  // dequantized weight tiles in TMEM (the UMMA A operand), one per TMA stage
+constexpr int GM_STAGES = 5;   // TMA ring: X tile + packed code tile per k block; one TMEM A tile each
 constexpr int GM_QSTAGES = 2;  // TMA ring of qparam boxes (8 groups x 128 rows of scales and offsets)
 constexpr int GM_QPF = 4;      // k blocks of qparams prefetched by each thread (no-TMA variant)
 constexpr int GM_DEQ_WARPS = 8;
-constexpr int GM_THREADS = 64 + GM_DEQ_WARPS * 32;
+constexpr int GM_EPI_WARPS = 8;
+constexpr int GM_EPI_WARP0 = 2 + GM_DEQ_WARPS;  // first epilogue warp
+constexpr int GM_THREADS = (GM_EPI_WARP0 + GM_EPI_WARPS) * 32;
+constexpr int GM_EPI_BAR = 1;  // named barrier of the epilogue warps
 constexpr int GM_TMEM_COLS = 512;
 constexpr int GM_ACOL = GM_BT;             // first TMEM column of the A stages
 constexpr int GM_ASTAGE_COLS = GM_BK / 2;  // 64 bf16 of a row = 32 columns
+constexpr int GM_YT = GM_BT / 2;           // tokens of one staged Y slice (one epilogue warp's columns)
 
 constexpr int GM_X_BYTES = GM_BT * GM_BK * 2;  // 32 KB
 constexpr int GM_QBOX_BYTES = GM_BW * 16;      //  2 KB: 8 bf16 per row
-constexpr int GM_OFF_X = 0;
-constexpr int GM_OFF_P = GM_OFF_X + GM_TSTAGES * GM_X_BYTES;
-// full_tma, empty_tma per stage (empty_tma also frees the stage's A tile); full_deq per stage;
-// full_q, empty_q per qparam stage; tmem_full; drain
-constexpr int GM_NBAR = 2 * GM_TSTAGES + GM_WSTAGES + 2 * GM_QSTAGES + 2;
-// Shared-memory layout after the X ring, for B-bit codes.
+constexpr int GM_Y_BYTES = GM_YT * GM_BW * 2;  // 32 KB: a bf16 [token][row] slice
+// Shared-memory layout for B-bit codes.  Barriers: full_tma, empty_tma (which
+// also frees the stage's A tile) and full_deq per stage; full_q, empty_q per
+// qparam stage; tmem_full, tmem_empty, drain.
 template <int B>
 struct GmLayout {
-    static constexpr int PROW = GM_BK * B / 8;                     // code bytes of one row per k block
-    static constexpr int P_BYTES = GM_BW * PROW;                   // 2 / 4 / 8 KB
-    static constexpr int OFF_Q = GM_OFF_P + GM_TSTAGES * P_BYTES;  // per stage: scales box, offsets box
-    static constexpr int OFF_BAR = OFF_Q + GM_QSTAGES * 2 * GM_QBOX_BYTES;
-    static constexpr int OFF_MISC = OFF_BAR + GM_NBAR * 8;
-    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;        // + alignment slack for the swizzle atoms
+    static constexpr int STAGES = B == 8 ? 4 : GM_STAGES;
+    static constexpr int PROW = GM_BK * B / 8;                 // code bytes of one row per k block
+    static constexpr int P_BYTES = GM_BW * PROW;               // 2 / 4 / 8 KB
+    static constexpr int OFF_X = 0;
+    static constexpr int OFF_P = OFF_X + STAGES * GM_X_BYTES;
+    static constexpr int OFF_Q = OFF_P + STAGES * P_BYTES;     // per stage: scales box, offsets box
+    static constexpr int OFF_Y = (OFF_Q + GM_QSTAGES * 2 * GM_QBOX_BYTES + 1023) / 1024 * 1024;
+    static constexpr int NBAR = 3 * STAGES + 2 * GM_QSTAGES + 3;
+    static constexpr int OFF_BAR = OFF_Y + GM_Y_BYTES;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;    // + alignment slack for the swizzle atoms
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static_assert(GM_ACOL + STAGES * GM_ASTAGE_COLS <= GM_TMEM_COLS, "tensor memory budget");
 };
-constexpr int GM_STAGE_PITCH = 80;                   // epilogue transpose: 32 rows of bf16 + 16 bytes
-constexpr int GM_STAGE_BYTES = 32 * GM_STAGE_PITCH;  // one warp's 32 tokens x 32 rows
-static_assert(GM_DEQ_WARPS * GM_STAGE_BYTES <= GM_TSTAGES * GM_X_BYTES, "epilogue staging reuses the X ring");
 
 constexpr uint64_t GM_WAIT_LIMIT_NS = 2000000000ull;   // 2 s per wait
 constexpr uint64_t GM_DRAIN_LIMIT_NS = 1000000000ull;  // 1 s per drain wait
 
 __device__ unsigned int g_gemm_fault;
+
+// Tiled store of a shared-memory box to global memory (a bulk async group of
+// this thread); elements outside the tensor are not written.  The start
+// coordinates are never negative and x * element size is a multiple of 16.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+                 :: "l"(tmap), "r"(src), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// this thread's bulk stores have finished reading shared memory / are complete
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// One test of an mbarrier phase that may suspend the thread until the phase
+// completes or about `hint_ns` have passed (no polling while it sleeps).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity), "r"(hint_ns) : "memory");
+    return ok != 0;
+}
+// 16 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+// mbar_wait_bounded with the thread suspended between tests (no spinning):
+// woken when the phase completes, re-checks the abort flag and the time limit
+// at least every ~20 us.
+__device__ __forceinline__ bool gm_wait(uint32_t bar, uint32_t parity, volatile int* abort, unsigned int* fault_word,
+                                        unsigned int code, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (abort && *abort) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            if (abort) *abort = 1;
+            atomicOr(fault_word, code);
+            return false;
+        }
+    }
+}
+// barrier `id` over `threads` threads of the block (a multiple of 32)
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
+}
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
 // A and B bf16 (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0),
@@ -132,46 +193,48 @@ __device__ __forceinline__ uint2 dequant4_8b(uint32_t w, float s, float o, uint3
     return r;
 }
 // QT: scales and offsets arrive by TMA (tm_s, tm_o); otherwise the
-// dequantization threads load them from `scales` / `offsets`.
+// dequantization threads load them from `scales` / `offsets`.  y_tma: Y is
+// written by TMA stores (tm_y); otherwise by plain stores.
 template <int G, bool QT, int B>
 __global__ void __launch_bounds__(GM_THREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_p,
             const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_o,
-            const uint16_t* __restrict__ scales, const uint16_t* __restrict__ offsets, uint16_t* __restrict__ Y,
-            const Epilogue ep, int M, int N, int K) {
+            const __grid_constant__ CUtensorMap tm_y, const uint16_t* __restrict__ scales,
+            const uint16_t* __restrict__ offsets, uint16_t* __restrict__ Y, const Epilogue ep, int M, int N, int K,
+            int ntn, int ntiles, int y_tma) {
     using LY = GmLayout<B>;
+    constexpr int ST = LY::STAGES;
     constexpr int QSPAN = 8 * G / GM_BK;  // k blocks covered by one qparam box (8 groups)
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar0 = sbase + LY::OFF_BAR;
     auto full_tma = [&](int t) { return bar0 + 8u * t; };
-    auto empty_tma = [&](int t) { return bar0 + 8u * (GM_TSTAGES + t); };
-    auto full_deq = [&](int w) { return bar0 + 8u * (2 * GM_TSTAGES + w); };
-    auto full_q = [&](int q) { return bar0 + 8u * (2 * GM_TSTAGES + GM_WSTAGES + q); };
-    auto empty_q = [&](int q) { return bar0 + 8u * (2 * GM_TSTAGES + GM_WSTAGES + GM_QSTAGES + q); };
-    const uint32_t tmem_full = bar0 + 8u * (2 * GM_TSTAGES + GM_WSTAGES + 2 * GM_QSTAGES);
-    const uint32_t drain = tmem_full + 8u;
+    auto empty_tma = [&](int t) { return bar0 + 8u * (ST + t); };
+    auto full_deq = [&](int t) { return bar0 + 8u * (2 * ST + t); };
+    auto full_q = [&](int q) { return bar0 + 8u * (3 * ST + q); };
+    auto empty_q = [&](int q) { return bar0 + 8u * (3 * ST + GM_QSTAGES + q); };
+    const uint32_t tmem_full = bar0 + 8u * (3 * ST + 2 * GM_QSTAGES);
+    const uint32_t tmem_empty = tmem_full + 8u;
+    const uint32_t drain = tmem_full + 16u;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + LY::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + LY::OFF_MISC + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * GM_BW, m0 = blockIdx.y * GM_BT;
     const int nkb = (K + GM_BK - 1) / GM_BK;
 
     if (threadIdx.x == 0) {
-        for (int t = 0; t < GM_TSTAGES; ++t) {
+        for (int t = 0; t < ST; ++t) {
             mbar_init(full_tma(t), 1);
             mbar_init(empty_tma(t), 1);
-        }
-        for (int w = 0; w < GM_WSTAGES; ++w) {
-            mbar_init(full_deq(w), GM_DEQ_WARPS * 32);
+            mbar_init(full_deq(t), GM_DEQ_WARPS * 32);
         }
         for (int q = 0; q < GM_QSTAGES; ++q) {
             mbar_init(full_q(q), 1);
             mbar_init(empty_q(q), GM_DEQ_WARPS * 32);
         }
         mbar_init(tmem_full, 1);
+        mbar_init(tmem_empty, GM_EPI_WARPS * 32);
         mbar_init(drain, 1);
         *abort_flag = 0;
         mbar_fence_init();
@@ -194,29 +257,39 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 tma_prefetch_desc(&tm_s);
                 tma_prefetch_desc(&tm_o);
             }
-            int issued = 0, q_issued = 0;
-            for (int kb = 0; kb < nkb; ++kb) {
-                if (QT && kb % QSPAN == 0) {  // scales and offsets of groups 8u .. 8u+7
-                    const int u = kb / QSPAN, q = u % GM_QSTAGES;
-                    const uint32_t pq = (u / GM_QSTAGES) & 1;
-                    if (!mbar_wait_bounded(empty_q(q), pq ^ 1, abort_flag, &g_gemm_fault, 1u, GM_WAIT_LIMIT_NS)) break;
-                    mbar_arrive_expect_tx(full_q(q), 2 * GM_QBOX_BYTES);
-                    const uint32_t qdst = sbase + LY::OFF_Q + q * 2 * GM_QBOX_BYTES;
-                    tma_load_2d(qdst, &tm_s, full_q(q), 8 * u, n0);
-                    tma_load_2d(qdst + GM_QBOX_BYTES, &tm_o, full_q(q), 8 * u, n0);
-                    ++q_issued;
+            int issued = 0, q_issued = 0;  // k blocks and qparam boxes requested, over all tiles
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+                const int n0 = (tile % ntn) * GM_BW, m0 = (tile / ntn) * GM_BT;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (QT && kb % QSPAN == 0) {  // scales and offsets of groups 8u .. 8u+7
+                        const int q = q_issued % GM_QSTAGES;
+                        if (!gm_wait(empty_q(q), ((q_issued / GM_QSTAGES) & 1) ^ 1, abort_flag,
+                                               &g_gemm_fault, 1u, GM_WAIT_LIMIT_NS)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(full_q(q), 2 * GM_QBOX_BYTES);
+                        const uint32_t qdst = sbase + LY::OFF_Q + q * 2 * GM_QBOX_BYTES;
+                        tma_load_2d(qdst, &tm_s, full_q(q), 8 * (kb / QSPAN), n0);
+                        tma_load_2d(qdst + GM_QBOX_BYTES, &tm_o, full_q(q), 8 * (kb / QSPAN), n0);
+                        ++q_issued;
+                    }
+                    const int t = issued % ST;
+                    if (!gm_wait(empty_tma(t), ((issued / ST) & 1) ^ 1, abort_flag, &g_gemm_fault, 1u,
+                                           GM_WAIT_LIMIT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full_tma(t), GM_X_BYTES + LY::P_BYTES);
+                    tma_load_2d(sbase + LY::OFF_X + t * GM_X_BYTES, &tm_x, full_tma(t), kb * GM_BK, m0);
+                    tma_load_2d(sbase + LY::OFF_P + t * LY::P_BYTES, &tm_p, full_tma(t), kb * LY::PROW, n0);
+                    ++issued;
                 }
-                const int t = kb % GM_TSTAGES;
-                const uint32_t ph = (kb / GM_TSTAGES) & 1;
-                if (!mbar_wait_bounded(empty_tma(t), ph ^ 1, abort_flag, &g_gemm_fault, 1u, GM_WAIT_LIMIT_NS)) break;
-                mbar_arrive_expect_tx(full_tma(t), GM_X_BYTES + LY::P_BYTES);
-                tma_load_2d(sbase + GM_OFF_X + t * GM_X_BYTES, &tm_x, full_tma(t), kb * GM_BK, m0);
-                tma_load_2d(sbase + GM_OFF_P + t * LY::P_BYTES, &tm_p, full_tma(t), kb * LY::PROW, n0);
-                ++issued;
             }
             // never leave the block with copies still landing in its shared memory
-            for (int kb = (issued > GM_TSTAGES ? issued - GM_TSTAGES : 0); kb < issued; ++kb)
-                mbar_drain_bounded(full_tma(kb % GM_TSTAGES), (kb / GM_TSTAGES) & 1, GM_DRAIN_LIMIT_NS);
+            for (int g = (issued > ST ? issued - ST : 0); g < issued; ++g)
+                mbar_drain_bounded(full_tma(g % ST), (g / ST) & 1, GM_DRAIN_LIMIT_NS);
             for (int u = (q_issued > GM_QSTAGES ? q_issued - GM_QSTAGES : 0); u < q_issued; ++u)
                 mbar_drain_bounded(full_q(u % GM_QSTAGES), (u / GM_QSTAGES) & 1, GM_DRAIN_LIMIT_NS);
         }
@@ -224,59 +297,48 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         // ------------------------------------------------------------------ UMMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = gm_idesc();
-            int issued = 0;
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int t = kb % GM_TSTAGES, w = kb % GM_WSTAGES;
-                const uint32_t pw = (kb / GM_WSTAGES) & 1;
-                // Only the A stage is waited for: every dequantization thread waited for this
-                // k block's TMA stage (X and codes) before its arrive, so full_deq orders the X
-                // tile too.  One wait less a step keeps the tensor pipe fed (each N=256 MMA
-                // takes ~128 cycles, and the issuing thread's gaps between steps leave it idle).
-                if (!mbar_wait_bounded(full_deq(w), pw, abort_flag, &g_gemm_fault, 2u, GM_WAIT_LIMIT_NS)) break;
+            int issued = 0, j = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++j) {
+                // the epilogue has read the previous tile's D out of tensor memory
+                if (j > 0 && !gm_wait(tmem_empty, (j - 1) & 1, abort_flag, &g_gemm_fault, 2u,
+                                                GM_WAIT_LIMIT_NS))
+                    break;
                 tc_fence_after();
-                const uint64_t bdesc = sw128_kmajor_desc(sbase + GM_OFF_X + t * GM_X_BYTES);
-                const uint32_t a_tmem = tmem + (uint32_t)(GM_ACOL + w * GM_ASTAGE_COLS);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    const int t = issued % ST;
+                    // Only the A stage is waited for: every dequantization thread waited for this
+                    // k block's TMA stage (X and codes) before its arrive, so full_deq orders the X
+                    // tile too.  One wait less a step keeps the tensor pipe fed (each N=256 MMA
+                    // takes ~128 cycles, and the issuing thread's gaps between steps leave it idle).
+                    if (!gm_wait(full_deq(t), (issued / ST) & 1, abort_flag, &g_gemm_fault, 2u,
+                                           GM_WAIT_LIMIT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t bdesc = sw128_kmajor_desc(sbase + LY::OFF_X + t * GM_X_BYTES);
+                    const uint32_t a_tmem = tmem + (uint32_t)(GM_ACOL + t * GM_ASTAGE_COLS);
 #pragma unroll
-                for (int kk = 0; kk < GM_BK / 16; ++kk)  // K=16 a step: 8 A columns, +32 bytes of B (+2 in the desc)
-                    umma_bf16_tmem_a(tmem, a_tmem + 8u * kk, bdesc + 2u * kk, idesc, (kb | kk) != 0);
-                umma_commit(empty_tma(t));  // X, codes and the A tile of this k block consumed (one commit)
-                ++issued;
+                    for (int kk = 0; kk < GM_BK / 16; ++kk)  // K=16 a step: 8 A columns, +32 bytes of B (+2 in the desc)
+                        umma_bf16_tmem_a(tmem, a_tmem + 8u * kk, bdesc + 2u * kk, idesc, (kb | kk) != 0);
+                    umma_commit(empty_tma(t));  // X, codes and the A tile of this k block consumed (one commit)
+                    ++issued;
+                }
+                if (ok) umma_commit(tmem_full);  // D of this tile is complete once its MMAs are
             }
-            if (issued == nkb) umma_commit(tmem_full);
             // the MMAs must be finished before tensor memory is released
             if (issued > 0) {
                 umma_commit(drain);
                 mbar_drain_bounded(drain, 0, GM_DRAIN_LIMIT_NS);
             }
         }
-    } else {
+    } else if (warp < GM_EPI_WARP0) {
         // ------------------------------------------------------- dequantization warps
         const int sp = warp & 3;         // TMEM sub-partition: lanes (weight rows) 32 sp .. 32 sp + 31
         const int hh = (warp - 2) >> 2;  // which 32-k half of each k block
         const int r = 32 * sp + lane;    // weight row within the tile
-        const int n = n0 + r;
-        const bool nvalid = n < N;
         const int ng = K / G;
-        const int64_t qrow = (int64_t)(nvalid ? n : 0) * ng;
-        // scale and offset of this row for this thread's half of a k block,
-        // loaded GM_QPF blocks ahead and kept raw until used (no-TMA variant).
-        // Groups past K read as 0: with the zero-filled codes those weights
-        // are exactly 0.
-        struct QRaw {
-            uint32_t s, o;
-        };
-        auto qload = [&](int kb) {
-            QRaw q = {0u, 0u};
-            if (!QT && kb < nkb && nvalid) {
-                const int j = (kb * GM_BK + 32 * hh) / G;
-                if (j < ng) {
-                    q.s = ldg_nc_u16(scales + qrow + j);
-                    q.o = ldg_nc_u16(offsets + qrow + j);
-                }
-            }
-            return q;
-        };
-        QRaw q0 = qload(0), q1 = qload(1), q2 = qload(2), q3 = qload(3);
         uint32_t cm, cg, mg;  // LOP3 constants pinned in registers (0x4300 pairs are also the 128.0 bias); 2^23
         asm volatile("mov.b32 %0, %1;" : "=r"(cm) : "r"(0x000F000Fu));
         asm volatile("mov.b32 %0, %1;" : "=r"(cg) : "r"(0x43004300u));
@@ -291,110 +353,170 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         // this thread's 16 columns of an A stage, in its own TMEM lane
         const uint32_t a_lane = tmem + ((uint32_t)(32 * sp) << 16) + (uint32_t)(GM_ACOL + 16 * hh);
         uint4 sq = make_uint4(0u, 0u, 0u, 0u), oq = sq;  // TMA variant: this row's 8 groups
+        int done = 0, q_done = 0;  // k blocks and qparam boxes consumed, over all tiles
         bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb) {
-            const QRaw qc = q0;
-            q0 = q1;
-            q1 = q2;
-            q2 = q3;
-            q3 = qload(kb + GM_QPF);
-            if (QT && kb % QSPAN == 0) {
-                const int u = kb / QSPAN, q = u % GM_QSTAGES;
-                if (!mbar_wait_bounded(full_q(q), (u / GM_QSTAGES) & 1, abort_flag, &g_gemm_fault, 4u,
-                                       GM_WAIT_LIMIT_NS)) {
+        for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+            const int n = (tile % ntn) * GM_BW + r;
+            const bool nvalid = n < N;
+            const int64_t qrow = (int64_t)(nvalid ? n : 0) * ng;
+            // scale and offset of this row for this thread's half of a k block,
+            // loaded GM_QPF blocks ahead and kept raw until used (no-TMA variant).
+            // Groups past K read as 0: with the zero-filled codes those weights
+            // are exactly 0.
+            struct QRaw {
+                uint32_t s, o;
+            };
+            auto qload = [&](int kb) {
+                QRaw q = {0u, 0u};
+                if (!QT && kb < nkb && nvalid) {
+                    const int jg = (kb * GM_BK + 32 * hh) / G;
+                    if (jg < ng) {
+                        q.s = ldg_nc_u16(scales + qrow + jg);
+                        q.o = ldg_nc_u16(offsets + qrow + jg);
+                    }
+                }
+                return q;
+            };
+            QRaw q0 = qload(0), q1 = qload(1), q2 = qload(2), q3 = qload(3);
+            for (int kb = 0; kb < nkb; ++kb) {
+                const QRaw qc = q0;
+                q0 = q1;
+                q1 = q2;
+                q2 = q3;
+                q3 = qload(kb + GM_QPF);
+                if (QT && kb % QSPAN == 0) {
+                    const int q = q_done % GM_QSTAGES;
+                    if (!gm_wait(full_q(q), (q_done / GM_QSTAGES) & 1, abort_flag, &g_gemm_fault, 4u,
+                                           GM_WAIT_LIMIT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t qsrc = sbase + LY::OFF_Q + q * 2 * GM_QBOX_BYTES + r * 16;
+                    sq = lds128(qsrc);
+                    oq = lds128(qsrc + GM_QBOX_BYTES);
+                    mbar_arrive(empty_q(q));
+                    ++q_done;
+                }
+                const int t = done % ST;
+                const uint32_t pt = (done / ST) & 1;
+                if (!gm_wait(full_tma(t), pt, abort_flag, &g_gemm_fault, 4u, GM_WAIT_LIMIT_NS) ||
+                    !gm_wait(empty_tma(t), pt ^ 1, abort_flag, &g_gemm_fault, 4u, GM_WAIT_LIMIT_NS)) {
                     ok = false;
                     break;
                 }
-                const uint32_t qsrc = sbase + LY::OFF_Q + q * 2 * GM_QBOX_BYTES + r * 16;
-                sq = lds128(qsrc);
-                oq = lds128(qsrc + GM_QBOX_BYTES);
-                mbar_arrive(empty_q(q));
+                tc_fence_after();  // the MMAs that read this A stage are complete
+                const uint32_t ptile = sbase + LY::OFF_P + t * LY::P_BYTES;
+                uint32_t s2, o2;  // (s,s) and (o,o) bf16 pairs of this half's group
+                if (QT) {
+                    const int jg = (kb % QSPAN) * GM_BK / G + (G == 32 ? hh : 0);  // group among the box's 8
+                    const uint32_t sel = (jg & 1) ? 0x3232u : 0x1010u;
+                    s2 = __byte_perm(pick_word(sq, jg >> 1), 0, sel);
+                    o2 = __byte_perm(pick_word(oq, jg >> 1), 0, sel);
+                } else {
+                    s2 = __byte_perm(qc.s, 0, 0x1010);
+                    o2 = __byte_perm(qc.o, 0, 0x1010);
+                }
+                // 32 weights of this row -> 16 columns (two bf16 of consecutive k each) of the A stage
+                const uint32_t acol = a_lane + (uint32_t)(t * GM_ASTAGE_COLS);
+                if constexpr (B == 4) {
+                    const uint4 words = lds128(ptile + pcol);  // 32 codes of this half
+                    tmem_st_16cols(acol, dequant8(words.x, s2, o2, cm, cg), dequant8(words.y, s2, o2, cm, cg),
+                                   dequant8(words.z, s2, o2, cm, cg), dequant8(words.w, s2, o2, cm, cg));
+                } else if constexpr (B == 2) {
+                    const uint2 words = lds64(ptile + pcol);
+                    uint4 c0, c1, c2, c3;
+                    dequant16_2b(words.x, s2, o2, cg, c0, c1);
+                    dequant16_2b(words.y, s2, o2, cg, c2, c3);
+                    tmem_st_16cols(acol, c0, c1, c2, c3);
+                } else {
+                    const uint4 wa = lds128(ptile + pcol), wb = lds128(ptile + pcol1);
+                    const float sf = __uint_as_float(s2 << 16), of = __uint_as_float(o2 << 16);
+                    const uint2 d0 = dequant4_8b(wa.x, sf, of, mg), d1 = dequant4_8b(wa.y, sf, of, mg);
+                    const uint2 d2 = dequant4_8b(wa.z, sf, of, mg), d3 = dequant4_8b(wa.w, sf, of, mg);
+                    const uint2 d4 = dequant4_8b(wb.x, sf, of, mg), d5 = dequant4_8b(wb.y, sf, of, mg);
+                    const uint2 d6 = dequant4_8b(wb.z, sf, of, mg), d7 = dequant4_8b(wb.w, sf, of, mg);
+                    tmem_st_16cols(acol, make_uint4(d0.x, d0.y, d1.x, d1.y), make_uint4(d2.x, d2.y, d3.x, d3.y),
+                                   make_uint4(d4.x, d4.y, d5.x, d5.y), make_uint4(d6.x, d6.y, d7.x, d7.y));
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(full_deq(t));
+                ++done;
             }
-            const int t = kb % GM_TSTAGES, w = kb % GM_WSTAGES;
-            const uint32_t pt = (kb / GM_TSTAGES) & 1, pw = (kb / GM_WSTAGES) & 1;
-            if (!mbar_wait_bounded(full_tma(t), pt, abort_flag, &g_gemm_fault, 4u, GM_WAIT_LIMIT_NS) ||
-                !mbar_wait_bounded(empty_tma(w), pw ^ 1, abort_flag, &g_gemm_fault, 4u, GM_WAIT_LIMIT_NS)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();  // the MMAs that read this A stage are complete
-            const uint32_t ptile = sbase + GM_OFF_P + t * LY::P_BYTES;
-            uint32_t s2, o2;  // (s,s) and (o,o) bf16 pairs of this half's group
-            if (QT) {
-                const int j = (kb % QSPAN) * GM_BK / G + (G == 32 ? hh : 0);  // group among the box's 8
-                const uint32_t sel = (j & 1) ? 0x3232u : 0x1010u;
-                s2 = __byte_perm(pick_word(sq, j >> 1), 0, sel);
-                o2 = __byte_perm(pick_word(oq, j >> 1), 0, sel);
-            } else {
-                s2 = __byte_perm(qc.s, 0, 0x1010);
-                o2 = __byte_perm(qc.o, 0, 0x1010);
-            }
-            // 32 weights of this row -> 16 columns (two bf16 of consecutive k each) of the A stage
-            const uint32_t acol = a_lane + (uint32_t)(w * GM_ASTAGE_COLS);
-            if constexpr (B == 4) {
-                const uint4 words = lds128(ptile + pcol);  // 32 codes of this half
-                tmem_st_16cols(acol, dequant8(words.x, s2, o2, cm, cg), dequant8(words.y, s2, o2, cm, cg),
-                               dequant8(words.z, s2, o2, cm, cg), dequant8(words.w, s2, o2, cm, cg));
-            } else if constexpr (B == 2) {
-                const uint2 words = lds64(ptile + pcol);
-                uint4 c0, c1, c2, c3;
-                dequant16_2b(words.x, s2, o2, cg, c0, c1);
-                dequant16_2b(words.y, s2, o2, cg, c2, c3);
-                tmem_st_16cols(acol, c0, c1, c2, c3);
-            } else {
-                const uint4 wa = lds128(ptile + pcol), wb = lds128(ptile + pcol1);
-                const float sf = __uint_as_float(s2 << 16), of = __uint_as_float(o2 << 16);
-                const uint2 d0 = dequant4_8b(wa.x, sf, of, mg), d1 = dequant4_8b(wa.y, sf, of, mg);
-                const uint2 d2 = dequant4_8b(wa.z, sf, of, mg), d3 = dequant4_8b(wa.w, sf, of, mg);
-                const uint2 d4 = dequant4_8b(wb.x, sf, of, mg), d5 = dequant4_8b(wb.y, sf, of, mg);
-                const uint2 d6 = dequant4_8b(wb.z, sf, of, mg), d7 = dequant4_8b(wb.w, sf, of, mg);
-                tmem_st_16cols(acol, make_uint4(d0.x, d0.y, d1.x, d1.y), make_uint4(d2.x, d2.y, d3.x, d3.y),
-                               make_uint4(d4.x, d4.y, d5.x, d5.y), make_uint4(d6.x, d6.y, d7.x, d7.y));
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(full_deq(w));
         }
-        // ----------------------------------------------------------------- epilogue
-        if (ok && mbar_wait_bounded(tmem_full, 0, abort_flag, &g_gemm_fault, 8u, GM_WAIT_LIMIT_NS)) {
-            tc_fence_after();
-            // D[row][token]: this warp's 32 rows (its TMEM lanes) x tokens [128 hh, 128 hh + 128);
-            // each 32 x 32 block goes through shared memory (the X ring is free now) so that
-            // every lane writes 32 rows of one token as 64 contiguous bytes of Y
-            unsigned char* stage = smem + GM_OFF_X + (warp - 2) * GM_STAGE_BYTES;
-            const uint32_t stage_s = smem_u32(stage);
-            const int nrow0 = n0 + 32 * sp;  // first weight row of this warp
-            const bool vec = (N % 8) == 0 && nrow0 + 32 <= N;
-            const float bl = nrow0 + lane < N ? bias_f32(ep.bias, nrow0 + lane) : 0.f;  // this lane's row
-#pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
-                const int col = 128 * hh + 32 * cc;  // first token column of the block
-                uint32_t v[32];
-                tmem_ld_32cols(tmem + ((uint32_t)(32 * sp) << 16) + (uint32_t)col, v);
-                // the output scale of token column col + lane (lane i hands column i's to the warp)
-                const float fl = yscale_f32(ep, min(m0 + col + lane, M - 1));
-                tmem_ld_wait();
-                // stage[token i][row lane] = bf16(D[row][token] * scale + bias)
+    } else {
+        // ----------------------------------------------------------------- epilogue warps
+        // Warp e (0..7) takes the 32 rows of TMEM sub-partition warp & 3 and the 128 tokens
+        // [128 half, 128 half + 128), half = e / 4.  It reads its part of D into registers as bf16
+        // pairs of neighbouring tokens and hands D back; the two halves then go one after the
+        // other through the [token][row] slice in shared memory to a TMA store.  Every epilogue
+        // warp passes the same four named barriers per tile, whatever happened to the others.
+        const int e = warp - GM_EPI_WARP0;
+        const int sp = warp & 3, half = e >> 2;
+        const int row = 32 * sp + lane;
+        unsigned char* ystage = smem + LY::OFF_Y;
+        const bool storer = e == 0 && lane == 0;
+        volatile int* tile_ok = reinterpret_cast<volatile int*>(smem + LY::OFF_MISC + 8);  // the waiter's verdict
+        bool ok = true;
+        int j = 0;
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
+            const int n0 = (tile % ntn) * GM_BW, m0 = (tile / ntn) * GM_BT;
+            // one thread waits for the tile's sums (suspended, not spinning); the other epilogue
+            // threads are blocked on the named barrier meanwhile
+            if (storer) *tile_ok = (ok && gm_wait(tmem_full, j & 1, abort_flag, &g_gemm_fault, 8u, GM_WAIT_LIMIT_NS)) ? 1 : 0;
+            named_barrier(GM_EPI_BAR, GM_EPI_WARPS * 32);
+            ok = *tile_ok != 0;
+            uint32_t pk[64];  // bf16 pairs (token 2i, token 2i + 1) of this lane's row
+            if (ok) {
+                tc_fence_after();
+                const float bl = n0 + row < N ? bias_f32(ep.bias, n0 + row) : 0.f;  // this lane's row
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    *reinterpret_cast<uint16_t*>(stage + i * GM_STAGE_PITCH + 2 * lane) =
-                        (uint16_t)float_to_bf16_bits(fmaf(__uint_as_float(v[i]), __shfl_sync(0xffffffffu, fl, i), bl));
-                __syncwarp();
-                const int m = m0 + col + lane;  // the token this lane writes
-                if (m < M && nrow0 < N) {
-                    uint16_t* yrow = Y + (int64_t)m * N + nrow0;
-                    if (vec) {
+                for (int cc = 0; cc < 8; ++cc) {
+                    const int col = GM_YT * half + 16 * cc;  // first token (TMEM column) of the piece
+                    uint32_t v[16];
+                    tmem_ld_16cols(tmem + ((uint32_t)(32 * sp) << 16) + (uint32_t)col, v);
+                    // the output scale of token col + (lane & 15) (lane i hands token i's to the warp)
+                    const float fl = yscale_f32(ep, min(m0 + col + (lane & 15), M - 1));
+                    tmem_ld_wait();
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            *reinterpret_cast<uint4*>(yrow + 8 * q) = lds128(stage_s + lane * GM_STAGE_PITCH + 16 * q);
-                    } else {
-                        for (int i = 0; i < 32 && nrow0 + i < N; ++i)
-                            yrow[i] = *reinterpret_cast<const uint16_t*>(stage + lane * GM_STAGE_PITCH + 2 * i);
+                    for (int i = 0; i < 8; ++i)
+                        pk[8 * cc + i] =
+                            (float_to_bf16_bits(fmaf(__uint_as_float(v[2 * i]), __shfl_sync(0xffffffffu, fl, 2 * i), bl))) |
+                            (float_to_bf16_bits(
+                                 fmaf(__uint_as_float(v[2 * i + 1]), __shfl_sync(0xffffffffu, fl, 2 * i + 1), bl))
+                             << 16);
+                }
+                tc_fence_before();
+                mbar_arrive(tmem_empty);  // the next tile's MMAs may overwrite D
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (storer && y_tma && (j > 0 || h > 0)) bulk_wait_read_all();  // the last slice has left
+                named_barrier(GM_EPI_BAR, GM_EPI_WARPS * 32);
+                if (ok && half == h) {  // stage[token t][row] for this warp's 128 tokens
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) {
+                        unsigned char* dst = ystage + (2 * i) * (GM_BW * 2) + 2 * row;
+                        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)(pk[i] & 0xFFFFu);
+                        *reinterpret_cast<uint16_t*>(dst + GM_BW * 2) = (uint16_t)(pk[i] >> 16);
                     }
                 }
-                __syncwarp();  // the block is rewritten by the next chunk
+                if (y_tma) fence_proxy_async_smem();  // the slice's writes, seen by the TMA store
+                named_barrier(GM_EPI_BAR, GM_EPI_WARPS * 32);
+                if (y_tma) {
+                    if (storer && ok && !*abort_flag) {
+                        tma_store_2d(&tm_y, smem_u32(ystage), n0, m0 + GM_YT * h);
+                        bulk_commit_group();
+                    }
+                } else if (ok) {  // plain stores: consecutive rows of one token per warp, inside Y only
+                    for (int x = threadIdx.x - GM_EPI_WARP0 * 32; x < GM_YT * GM_BW; x += GM_EPI_WARPS * 32) {
+                        const int m = m0 + GM_YT * h + x / GM_BW, n = n0 + x % GM_BW;
+                        if (m < M && n < N) Y[(int64_t)m * N + n] = *reinterpret_cast<const uint16_t*>(ystage + 2 * x);
+                    }
+                }
             }
         }
+        if (storer && y_tma) bulk_wait_all();  // the last store is complete before the block exits
     }
 
     tc_fence_before();
@@ -404,41 +526,50 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
 
 // ------------------------------------------------------------------ host side
 
+// one block per SM (persistent), no more blocks than tiles
 template <int G, bool QT, int B>
 static cudaError_t launch_gemm_g(const CUtensorMap& tx, const CUtensorMap& tp, const CUtensorMap& ts,
-                                 const CUtensorMap& to, const uint16_t* scales, const uint16_t* offsets, uint16_t* Y,
-                                 const Epilogue& ep, int M, int N, int K, cudaStream_t stream) {
+                                 const CUtensorMap& to, const CUtensorMap& ty, bool y_tma, const uint16_t* scales,
+                                 const uint16_t* offsets, uint16_t* Y, const Epilogue& ep, int M, int N, int K,
+                                 cudaStream_t stream) {
     auto kern = gemm_kernel<G, QT, B>;
     constexpr int SMEM = GmLayout<B>::SMEM_BYTES;
     cudaError_t e = ensure_kernel_attrs(reinterpret_cast<const void*>(kern), SMEM, false);
     if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)((N + GM_BW - 1) / GM_BW), (unsigned)((M + GM_BT - 1) / GM_BT));
-    kern<<<grid, GM_THREADS, SMEM, stream>>>(tx, tp, ts, to, scales, offsets, Y, ep, M, N, K);
+    int sms = 0, per_sm = 0;
+    if ((e = resident_blocks(reinterpret_cast<const void*>(kern), GM_THREADS, SMEM, &sms, &per_sm)) != cudaSuccess)
+        return e;
+    const int ntn = (N + GM_BW - 1) / GM_BW;
+    const int ntiles = ntn * ((M + GM_BT - 1) / GM_BT);
+    const int grid = std::max(1, std::min(ntiles, sms * std::max(per_sm, 1)));
+    kern<<<grid, GM_THREADS, SMEM, stream>>>(tx, tp, ts, to, ty, scales, offsets, Y, ep, M, N, K, ntn, ntiles,
+                                              y_tma ? 1 : 0);
     return cudaGetLastError();
 }
 
 template <int B>
 static cudaError_t launch_gemm_b(const CUtensorMap& tx, const CUtensorMap& tp, const CUtensorMap& ts,
-                                 const CUtensorMap& to, bool qt, const uint16_t* scales, const uint16_t* offsets,
-                                 uint16_t* Y, const Epilogue& ep, int m, int n, int k, int g, cudaStream_t stream) {
+                                 const CUtensorMap& to, const CUtensorMap& ty, bool y_tma, bool qt,
+                                 const uint16_t* scales, const uint16_t* offsets, uint16_t* Y, const Epilogue& ep,
+                                 int m, int n, int k, int g, cudaStream_t stream) {
     switch (g) {
         case 32:
-            return qt ? launch_gemm_g<32, true, B>(tx, tp, ts, to, scales, offsets, Y, ep, m, n, k, stream)
-                      : launch_gemm_g<32, false, B>(tx, tp, ts, to, scales, offsets, Y, ep, m, n, k, stream);
+            return qt ? launch_gemm_g<32, true, B>(tx, tp, ts, to, ty, y_tma, scales, offsets, Y, ep, m, n, k, stream)
+                      : launch_gemm_g<32, false, B>(tx, tp, ts, to, ty, y_tma, scales, offsets, Y, ep, m, n, k, stream);
         case 64:
-            return qt ? launch_gemm_g<64, true, B>(tx, tp, ts, to, scales, offsets, Y, ep, m, n, k, stream)
-                      : launch_gemm_g<64, false, B>(tx, tp, ts, to, scales, offsets, Y, ep, m, n, k, stream);
+            return qt ? launch_gemm_g<64, true, B>(tx, tp, ts, to, ty, y_tma, scales, offsets, Y, ep, m, n, k, stream)
+                      : launch_gemm_g<64, false, B>(tx, tp, ts, to, ty, y_tma, scales, offsets, Y, ep, m, n, k, stream);
         default:
-            return qt ? launch_gemm_g<128, true, B>(tx, tp, ts, to, scales, offsets, Y, ep, m, n, k, stream)
-                      : launch_gemm_g<128, false, B>(tx, tp, ts, to, scales, offsets, Y, ep, m, n, k, stream);
+            return qt ? launch_gemm_g<128, true, B>(tx, tp, ts, to, ty, y_tma, scales, offsets, Y, ep, m, n, k, stream)
+                      : launch_gemm_g<128, false, B>(tx, tp, ts, to, ty, y_tma, scales, offsets, Y, ep, m, n, k, stream);
     }
 }
 
 cudaError_t launch_gemm(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
                         const uint16_t* offsets, int64_t N, int g, int bits, uint16_t* Y, cudaStream_t stream,
                         const char** detail, const Epilogue& ep) {
-    if ((N + GM_BW - 1) / GM_BW > 0x7FFFFFFF || (M + GM_BT - 1) / GM_BT > 65535) {
-        *detail = "problem too large for the GEMM grid";
+    if ((N + GM_BW - 1) / GM_BW * ((M + GM_BT - 1) / GM_BT) > 0x7FFFFFFF) {
+        *detail = "problem too large for the GEMM's tile count";
         return cudaErrorInvalidValue;
     }
     CUtensorMap tx, tp;
@@ -470,10 +601,19 @@ cudaError_t launch_gemm(const uint16_t* X, int64_t M, int64_t K, const uint8_t* 
                                      (uint64_t)ng * 2, 8, GM_BW, CU_TENSOR_MAP_SWIZZLE_NONE, detail);
         if (e != cudaSuccess) return e;
     }
+    // Y: [M][N] bf16, box 128 rows x one 128-token slice, stored by TMA when the base and the row
+    // pitch are 16-byte multiples (the tensor-map rules)
+    const bool y_tma = (reinterpret_cast<uintptr_t>(Y) & 15u) == 0 && N % 8 == 0;
+    CUtensorMap ty = tx;  // not read when !y_tma
+    if (y_tma) {
+        e = encode_tensor_map_2d(&ty, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Y, (uint64_t)N, (uint64_t)M, (uint64_t)N * 2,
+                                 GM_BW, GM_YT, CU_TENSOR_MAP_SWIZZLE_NONE, detail);
+        if (e != cudaSuccess) return e;
+    }
     const int m = (int)M, n = (int)N, k = (int)K;
-    if (bits == 2) return launch_gemm_b<2>(tx, tp, ts, to, qt, scales, offsets, Y, ep, m, n, k, g, stream);
-    if (bits == 8) return launch_gemm_b<8>(tx, tp, ts, to, qt, scales, offsets, Y, ep, m, n, k, g, stream);
-    return launch_gemm_b<4>(tx, tp, ts, to, qt, scales, offsets, Y, ep, m, n, k, g, stream);
+    if (bits == 2) return launch_gemm_b<2>(tx, tp, ts, to, ty, y_tma, qt, scales, offsets, Y, ep, m, n, k, g, stream);
+    if (bits == 8) return launch_gemm_b<8>(tx, tp, ts, to, ty, y_tma, qt, scales, offsets, Y, ep, m, n, k, g, stream);
+    return launch_gemm_b<4>(tx, tp, ts, to, ty, y_tma, qt, scales, offsets, Y, ep, m, n, k, g, stream);
 }
 
 cudaError_t read_and_clear_gemm_fault(unsigned int* fault) {
