@@ -546,7 +546,8 @@ def int8_rows(args, w4, wl, device, stream, dist, peaks, cases, stack, ws_ms):
 def summary_rows(rows, peaks):
     """Compact prefill (TFLOP/s) and batched-decode (GB/s) results for the top of the JSON line."""
     pre = rows.get("prefill_gemm", {}).get("cases", [])
-    prefill = {"unit": "TFLOP/s", "kernel": "gemm_kernel (tcgen05)", "peak": peaks["bf16_tflops"],
+    prefill = {"unit": "TFLOP/s", "kernel": "gemm_kernel (tcgen05, persistent, stream-K tail with the default workspace)",
+               "peak": peaks["bf16_tflops"],
                "peak_source": "MEASURED_PEAKS bf16_tflops (burst)", "l2": "flushed before every call",
                "cases": [{"M": c["M"], "N": c["N"], "K": c["K"], "g": 32, "tflops": c["tflops"],
                           "frac": c["frac_of_bf16_peak"]} for c in pre]} if pre else None
@@ -697,7 +698,8 @@ def other_rows(args, w4, wl, device, stream, peaks, dist, only=None):
                     "hbm_gbs": round(linear_bytes(c.M, c.N, c.K, c.group_size) / (t * 1e-3) / 1e9, 1)})
         del Wq, sc, of, X, Y
     best = max(pre, key=lambda r: r["tflops"]) if pre else {"tflops": 0.0}
-    rows["prefill_gemm"] = {"unit": "TFLOP/s", "cases": pre, "kernel": "gemm_kernel (tcgen05, TMEM accumulators)",
+    rows["prefill_gemm"] = {"unit": "TFLOP/s", "cases": pre,
+                            "kernel": "gemm_kernel (tcgen05, TMEM accumulators, persistent, stream-K tail)",
                             "roofline": {"bound": "tensor", "achieved": best["tflops"], "peak": peaks["bf16_tflops"],
                                          "unit": "TFLOP/s", "frac": round(best["tflops"] / peaks["bf16_tflops"], 4),
                                          "traffic": None,

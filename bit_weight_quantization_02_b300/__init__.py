@@ -220,10 +220,11 @@ def w4_linear_workspace_bytes(M: int, N: int, K: int, group_size: int) -> int:
 
 class Workspace:
     """Zero-filled device workspace for w4_linear (the stream kernels' slots for
-    the partial sums of row tiles split between warps).  Every call leaves it zeroed, so it can be reused by
-    calls of any shape in sequence; calls that can overlap on the GPU need one
-    each.  Growing it allocates (through torch): size it before capturing a CUDA
-    graph or timing."""
+    the partial sums of row tiles split between warps, and past 16 MiB the
+    tensor-core GEMM's partial tiles).  Every call leaves its first 16 MiB
+    zeroed, so it can be reused by calls of any shape in sequence; calls that
+    can overlap on the GPU need one each.  Growing it allocates (through torch):
+    size it before capturing a CUDA graph or timing."""
 
     def __init__(self, device=None, nbytes: int = 0):
         self.device = torch.device(device or "cuda")

@@ -88,7 +88,12 @@ size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int group_size
     if (tc) return tc;
     w4::DecodePlan dp;  // decode layout (w4_linear_repacked)
     if (w4::plan_decode(M, N, K, group_size, &dp)) return dp.ws_bytes;
-    return 0;
+    size_t gb = 0;  // the tensor-core GEMM's split tail (flags at 0, partial tiles past the slot region)
+    if (w4::gemm_split_bytes(M, N, K, w4::I8_SCRATCH_OFFSET, &gb) != cudaSuccess) {
+        cudaGetLastError();  // no device to size it for: the GEMM then splits nothing
+        return 0;
+    }
+    return gb;
 }
 
 }  // extern "C"
@@ -176,7 +181,8 @@ w4_status linear_impl(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq
         }
         if (kernel != W4_KERNEL_AUTO) return fail(W4_ERR_INVALID_ARG, "no skinny launch plan for this shape");
     }
-    e = w4::launch_gemm(X, M, K, Wq, scales, offsets, N, group_size, 4, Y, (cudaStream_t)stream, &detail, ep);
+    e = w4::launch_gemm(X, M, K, Wq, scales, offsets, N, group_size, 4, Y, (cudaStream_t)stream, &detail, ep, workspace,
+                        workspace_bytes, w4::I8_SCRATCH_OFFSET);
     if (e != cudaSuccess) return fail(W4_ERR_CUDA, "tensor-core linear: %s %s", cudaGetErrorString(e), detail);
     return W4_OK;
 }
@@ -257,6 +263,7 @@ struct I8Plan {
     w4::StreamPlan sp;
     size_t lin_bytes;  // the linear's own slots
     size_t wide_bytes; // the bf16 copy of the codes
+    size_t part_off;   // the GEMM's partial tiles (past the bf16 codes)
     size_t total;      // workspace bytes the call needs
 };
 
@@ -267,6 +274,10 @@ I8Plan plan_i8(int64_t M, int64_t N, int64_t K, int g) {
     p.lin_bytes = p.stream_ok ? p.sp.ws_bytes : 0;
     p.wide_bytes = p.direct ? 0 : (size_t)(M * K * 2);
     p.total = p.direct ? p.lin_bytes : w4::I8_SCRATCH_OFFSET + p.wide_bytes;
+    p.part_off = (w4::I8_SCRATCH_OFFSET + p.wide_bytes + 255) / 256 * 256;
+    size_t gb = 0;  // the tensor-core GEMM's split tail, when a device is there to size it
+    if (!p.stream_ok && w4::gemm_split_bytes(M, N, K, p.part_off, &gb) != cudaSuccess) cudaGetLastError();
+    p.total = std::max(p.total, gb);
     return p;
 }
 
@@ -295,7 +306,8 @@ w4_status linear_i8_run(const I8Plan& p, const int8_t* Xq, const float* x_scale,
         e = w4::launch_stream(p.sp, Xb, M, K, Wq, scales, offsets, N, group_size, Y, workspace, (cudaStream_t)stream,
                               &detail, ep);
     else
-        e = w4::launch_gemm(Xb, M, K, Wq, scales, offsets, N, group_size, 4, Y, (cudaStream_t)stream, &detail, ep);
+        e = w4::launch_gemm(Xb, M, K, Wq, scales, offsets, N, group_size, 4, Y, (cudaStream_t)stream, &detail, ep,
+                            workspace, p.total, p.part_off);
     if (e != cudaSuccess) return fail(W4_ERR_CUDA, "int8 linear: %s %s", cudaGetErrorString(e), detail);
     return W4_OK;
 }
@@ -564,7 +576,8 @@ w4_status w4_linear_bits(const uint16_t* X, int64_t M, int64_t K, const uint8_t*
         if (e != cudaSuccess) return fail(W4_ERR_CUDA, "batched linear: %s %s", cudaGetErrorString(e), detail);
         return W4_OK;
     }
-    e = w4::launch_gemm(X, M, K, Wq, scales, offsets, N, group_size, bits, Y, (cudaStream_t)stream, &detail);
+    e = w4::launch_gemm(X, M, K, Wq, scales, offsets, N, group_size, bits, Y, (cudaStream_t)stream, &detail,
+                        w4::Epilogue(), workspace, workspace_bytes, w4::I8_SCRATCH_OFFSET);
     if (e != cudaSuccess) return fail(W4_ERR_CUDA, "tensor-core linear: %s %s", cudaGetErrorString(e), detail);
     return W4_OK;
 }

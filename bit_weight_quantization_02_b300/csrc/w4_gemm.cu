@@ -89,7 +89,53 @@ struct GmLayout {
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;    // + alignment slack for the swizzle atoms
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static_assert(GM_ACOL + STAGES * GM_ASTAGE_COLS <= GM_TMEM_COLS, "tensor memory budget");
+    static_assert(STAGES * GM_X_BYTES >= 2 * GM_Y_BYTES, "an owner stages its whole Y tile in the X ring");
 };
+
+// A block's work list.  Tiles 0 .. dp_tiles-1 are computed whole, tile b, b + G, ... by block b
+// of the G blocks.  With a workspace, the tiles after those (the last full round and the
+// part-empty one) are cut by k blocks into G equal contiguous ranges, one per block, taken after
+// its whole tiles (stream-K): at most 3 pieces, the end of a tile (the block shares it: it
+// publishes its fp32 sums and a flag), whole tiles, and the start of a tile (it owns it: it adds
+// the sums of the blocks after it that share it, in block order, and writes Y).
+struct GmWork {
+    int ntn;              // row tiles per token tile
+    int ntiles;
+    int dp_tiles;         // tiles computed whole (all of them without a split)
+    long long sk_units;   // (ntiles - dp_tiles) * k blocks (0: no split)
+    float* part;          // one slot of 128 x 256 fp32 sums per block
+    unsigned int* flags;  // one word per block, zero between calls (an owner clears what it used)
+};
+struct GmItem {
+    int tile, kb0, kb1;
+};
+constexpr size_t GM_PART_FLOATS = (size_t)GM_BW * GM_BT;  // 128 KB a slot
+
+__device__ __forceinline__ long long gm_sk_start(const GmWork& wk, int b) {
+    return wk.sk_units * b / (long long)gridDim.x;
+}
+// item k of this block's list (false past its end); the same list in every role
+__device__ __forceinline__ bool gm_item(const GmWork& wk, int nkb, int k, GmItem* it) {
+    const int G = gridDim.x, b = blockIdx.x;
+    const int nwhole = wk.dp_tiles > b ? (wk.dp_tiles - 1 - b) / G + 1 : 0;
+    if (k < nwhole) {
+        *it = GmItem{b + G * k, 0, nkb};
+        return true;
+    }
+    if (wk.sk_units == 0) return false;
+    long long u = gm_sk_start(wk, b);
+    const long long u1 = gm_sk_start(wk, b + 1);
+    for (int p = k - nwhole; u < u1; --p) {  // the host keeps a range under two tiles: 3 pieces at most
+        const int t = (int)(u / nkb), kb0 = (int)(u % nkb);
+        const int kb1 = (int)(kb0 + (u1 - u) < nkb ? kb0 + (u1 - u) : nkb);
+        if (p == 0) {
+            *it = GmItem{wk.dp_tiles + t, kb0, kb1};
+            return true;
+        }
+        u += kb1 - kb0;
+    }
+    return false;
+}
 
 constexpr uint64_t GM_WAIT_LIMIT_NS = 2000000000ull;   // 2 s per wait
 constexpr uint64_t GM_DRAIN_LIMIT_NS = 1000000000ull;  // 1 s per drain wait
@@ -140,6 +186,40 @@ __device__ __forceinline__ bool gm_wait(uint32_t bar, uint32_t parity, volatile 
             if (abort) *abort = 1;
             atomicOr(fault_word, code);
             return false;
+        }
+    }
+}
+// Split-tile flags: published with a release store after the block's sums,
+// read with acquire loads; the sums themselves are read at L2 (ld.global.cg).
+__device__ __forceinline__ void st_release_gpu_u32(unsigned int* p, unsigned int v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned int ld_acquire_gpu_u32(const unsigned int* p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ float ldcg_f32(const float* p) {
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+    return v;
+}
+// Wait until *flag != 0, bounded like every other wait: false after limit_ns or
+// once another role has given up (*abort), raising *abort and the fault code.
+__device__ __forceinline__ bool wait_flag_bounded(const unsigned int* flag, volatile int* abort, unsigned int* fault_word,
+                                                  unsigned int code, uint64_t limit_ns) {
+    if (ld_acquire_gpu_u32(flag) != 0u) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        __nanosleep(128);
+        if (ld_acquire_gpu_u32(flag) != 0u) return true;
+        if ((it & 15u) == 0u) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > limit_ns) {
+                *abort = 1;
+                atomicOr(fault_word, code);
+                return false;
+            }
         }
     }
 }
@@ -201,7 +281,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_o,
             const __grid_constant__ CUtensorMap tm_y, const uint16_t* __restrict__ scales,
             const uint16_t* __restrict__ offsets, uint16_t* __restrict__ Y, const Epilogue ep, int M, int N, int K,
-            int ntn, int ntiles, int y_tma) {
+            const GmWork wk, int y_tma) {
     using LY = GmLayout<B>;
     constexpr int ST = LY::STAGES;
     constexpr int QSPAN = 8 * G / GM_BK;  // k blocks covered by one qparam box (8 groups)
@@ -259,10 +339,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             }
             int issued = 0, q_issued = 0;  // k blocks and qparam boxes requested, over all tiles
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
-                const int n0 = (tile % ntn) * GM_BW, m0 = (tile / ntn) * GM_BT;
-                for (int kb = 0; kb < nkb; ++kb) {
-                    if (QT && kb % QSPAN == 0) {  // scales and offsets of groups 8u .. 8u+7
+            GmItem it;
+            for (int k = 0; ok && gm_item(wk, nkb, k, &it); ++k) {
+                const int n0 = (it.tile % wk.ntn) * GM_BW, m0 = (it.tile / wk.ntn) * GM_BT;
+                for (int kb = it.kb0; kb < it.kb1; ++kb) {
+                    if (QT && (kb % QSPAN == 0 || kb == it.kb0)) {  // scales and offsets of groups 8u .. 8u+7
                         const int q = q_issued % GM_QSTAGES;
                         if (!gm_wait(empty_q(q), ((q_issued / GM_QSTAGES) & 1) ^ 1, abort_flag,
                                                &g_gemm_fault, 1u, GM_WAIT_LIMIT_NS)) {
@@ -299,13 +380,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             constexpr uint32_t idesc = gm_idesc();
             int issued = 0, j = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++j) {
-                // the epilogue has read the previous tile's D out of tensor memory
+            GmItem it;
+            for (int k = 0; ok && gm_item(wk, nkb, k, &it); ++k, ++j) {
+                // the epilogue has read the previous item's D out of tensor memory
                 if (j > 0 && !gm_wait(tmem_empty, (j - 1) & 1, abort_flag, &g_gemm_fault, 2u,
                                                 GM_WAIT_LIMIT_NS))
                     break;
                 tc_fence_after();
-                for (int kb = 0; kb < nkb; ++kb) {
+                for (int kb = it.kb0; kb < it.kb1; ++kb) {
                     const int t = issued % ST;
                     // Only the A stage is waited for: every dequantization thread waited for this
                     // k block's TMA stage (X and codes) before its arrive, so full_deq orders the X
@@ -321,11 +403,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                     const uint32_t a_tmem = tmem + (uint32_t)(GM_ACOL + t * GM_ASTAGE_COLS);
 #pragma unroll
                     for (int kk = 0; kk < GM_BK / 16; ++kk)  // K=16 a step: 8 A columns, +32 bytes of B (+2 in the desc)
-                        umma_bf16_tmem_a(tmem, a_tmem + 8u * kk, bdesc + 2u * kk, idesc, (kb | kk) != 0);
+                        umma_bf16_tmem_a(tmem, a_tmem + 8u * kk, bdesc + 2u * kk, idesc, (kb != it.kb0) | (kk != 0));
                     umma_commit(empty_tma(t));  // X, codes and the A tile of this k block consumed (one commit)
                     ++issued;
                 }
-                if (ok) umma_commit(tmem_full);  // D of this tile is complete once its MMAs are
+                if (ok) umma_commit(tmem_full);  // D of this item is complete once its MMAs are
             }
             // the MMAs must be finished before tensor memory is released
             if (issued > 0) {
@@ -355,8 +437,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         uint4 sq = make_uint4(0u, 0u, 0u, 0u), oq = sq;  // TMA variant: this row's 8 groups
         int done = 0, q_done = 0;  // k blocks and qparam boxes consumed, over all tiles
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
-            const int n = (tile % ntn) * GM_BW + r;
+        GmItem it;
+        for (int k = 0; ok && gm_item(wk, nkb, k, &it); ++k) {
+            const int n = (it.tile % wk.ntn) * GM_BW + r;
             const bool nvalid = n < N;
             const int64_t qrow = (int64_t)(nvalid ? n : 0) * ng;
             // scale and offset of this row for this thread's half of a k block,
@@ -377,14 +460,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 }
                 return q;
             };
-            QRaw q0 = qload(0), q1 = qload(1), q2 = qload(2), q3 = qload(3);
-            for (int kb = 0; kb < nkb; ++kb) {
+            QRaw q0 = qload(it.kb0), q1 = qload(it.kb0 + 1), q2 = qload(it.kb0 + 2), q3 = qload(it.kb0 + 3);
+            for (int kb = it.kb0; kb < it.kb1; ++kb) {
                 const QRaw qc = q0;
                 q0 = q1;
                 q1 = q2;
                 q2 = q3;
                 q3 = qload(kb + GM_QPF);
-                if (QT && kb % QSPAN == 0) {
+                if (QT && (kb % QSPAN == 0 || kb == it.kb0)) {
                     const int q = q_done % GM_QSTAGES;
                     if (!gm_wait(full_q(q), (q_done / GM_QSTAGES) & 1, abort_flag, &g_gemm_fault, 4u,
                                            GM_WAIT_LIMIT_NS)) {
@@ -449,23 +532,113 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         // Warp e (0..7) takes the 32 rows of TMEM sub-partition warp & 3 and the 128 tokens
         // [128 half, 128 half + 128), half = e / 4.  It reads its part of D into registers as bf16
         // pairs of neighbouring tokens and hands D back; the two halves then go one after the
-        // other through the [token][row] slice in shared memory to a TMA store.  Every epilogue
-        // warp passes the same four named barriers per tile, whatever happened to the others.
+        // other through the [token][row] slice in shared memory to a TMA store.  A shared piece's
+        // fp32 sums go to this block's workspace slot instead, [warp][16 tokens][token][lane].
+        // Every epilogue warp passes the same named barriers per item, whatever happened to the
+        // others (the item's kind is the same for all of them).
         const int e = warp - GM_EPI_WARP0;
         const int sp = warp & 3, half = e >> 2;
         const int row = 32 * sp + lane;
         unsigned char* ystage = smem + LY::OFF_Y;
         const bool storer = e == 0 && lane == 0;
         volatile int* tile_ok = reinterpret_cast<volatile int*>(smem + LY::OFF_MISC + 8);  // the waiter's verdict
+        const int b = blockIdx.x;
         bool ok = true;
         int j = 0;
-        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
-            const int n0 = (tile % ntn) * GM_BW, m0 = (tile / ntn) * GM_BT;
-            // one thread waits for the tile's sums (suspended, not spinning); the other epilogue
-            // threads are blocked on the named barrier meanwhile
-            if (storer) *tile_ok = (ok && gm_wait(tmem_full, j & 1, abort_flag, &g_gemm_fault, 8u, GM_WAIT_LIMIT_NS)) ? 1 : 0;
+        GmItem it;
+        for (int k = 0; gm_item(wk, nkb, k, &it); ++k, ++j) {
+            const int n0 = (it.tile % wk.ntn) * GM_BW, m0 = (it.tile / wk.ntn) * GM_BT;
+            const bool sharer = it.kb0 > 0;                    // its sums go to the owner
+            const bool owner = it.kb0 == 0 && it.kb1 < nkb;   // adds the sums of the blocks after it
+            int nsh = 0;
+            if (owner) {
+                const long long t_rel = it.tile - wk.dp_tiles;
+                while (b + 1 + nsh < (int)gridDim.x && gm_sk_start(wk, b + 1 + nsh) / nkb == t_rel) ++nsh;
+            }
+            // one thread waits for the item's sums (suspended, not spinning) and, for an owner,
+            // for its sharers' flags; the other epilogue threads are blocked on the named barrier
+            if (storer) {
+                bool got = ok && gm_wait(tmem_full, j & 1, abort_flag, &g_gemm_fault, 8u, GM_WAIT_LIMIT_NS);
+                for (int sh = 0; got && sh < nsh; ++sh)
+                    got = wait_flag_bounded(wk.flags + b + 1 + sh, abort_flag, &g_gemm_fault, 16u, GM_WAIT_LIMIT_NS);
+                *tile_ok = got ? 1 : 0;
+            }
             named_barrier(GM_EPI_BAR, GM_EPI_WARPS * 32);
             ok = *tile_ok != 0;
+            if (sharer) {
+                if (ok) {
+                    tc_fence_after();
+                    float* slot = wk.part + (size_t)b * GM_PART_FLOATS + (size_t)e * (GM_YT * 32) + lane;
+#pragma unroll 1
+                    for (int cc = 0; cc < 8; ++cc) {
+                        uint32_t v[16];
+                        tmem_ld_16cols(tmem + ((uint32_t)(32 * sp) << 16) + (uint32_t)(GM_YT * half + 16 * cc), v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) slot[(cc * 16 + i) * 32] = __uint_as_float(v[i]);
+                    }
+                    tc_fence_before();
+                    mbar_arrive(tmem_empty);  // the next item's MMAs may overwrite D
+                }
+                __threadfence();  // this thread's sums before the flag
+                named_barrier(GM_EPI_BAR, GM_EPI_WARPS * 32);
+                if (storer && ok && !*abort_flag) st_release_gpu_u32(wk.flags + b, 1u);
+                continue;
+            }
+            if (owner) {
+                // the block's last item (its range ends inside the tile), so the X ring is free: the
+                // whole [token][row] tile is staged there, the sharers' sums added in block order
+                // on the way (the first sharer's loads in flight during the TMEM read)
+                unsigned char* ost = smem + LY::OFF_X;
+                if (ok) {
+                    tc_fence_after();
+                    const float bl = n0 + row < N ? bias_f32(ep.bias, n0 + row) : 0.f;  // this lane's row
+#pragma unroll 1
+                    for (int cc = 0; cc < 8; ++cc) {
+                        const int col = GM_YT * half + 16 * cc;  // first token (TMEM column) of the piece
+                        const float fl = yscale_f32(ep, min(m0 + col + (lane & 15), M - 1));
+                        uint32_t v[16];
+#pragma unroll 1
+                        for (int sh = 0; sh < nsh; ++sh) {
+                            const float* src = wk.part + (size_t)(b + 1 + sh) * GM_PART_FLOATS +
+                                               (size_t)e * (GM_YT * 32) + (size_t)(cc * 16) * 32 + lane;
+                            float pv[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) pv[i] = ldcg_f32(src + i * 32);
+                            if (sh == 0) {  // the first sharer's loads are in flight during the TMEM read
+                                tmem_ld_16cols(tmem + ((uint32_t)(32 * sp) << 16) + (uint32_t)col, v);
+                                tmem_ld_wait();
+                            }
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + pv[i]);
+                        }
+                        unsigned char* dst = ost + col * (GM_BW * 2) + 2 * row;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            *reinterpret_cast<uint16_t*>(dst + i * (GM_BW * 2)) = (uint16_t)float_to_bf16_bits(
+                                fmaf(__uint_as_float(v[i]), __shfl_sync(0xffffffffu, fl, i), bl));
+                    }
+                    tc_fence_before();
+                    mbar_arrive(tmem_empty);
+                    if (storer)  // the consumed flags back to zero for the next call
+                        for (int sh = 0; sh < nsh; ++sh) st_release_gpu_u32(wk.flags + b + 1 + sh, 0u);
+                }
+                if (y_tma) fence_proxy_async_smem();  // the tile's writes, seen by the TMA stores
+                named_barrier(GM_EPI_BAR, GM_EPI_WARPS * 32);
+                if (y_tma) {
+                    if (storer && ok && !*abort_flag) {
+                        tma_store_2d(&tm_y, smem_u32(ost), n0, m0);
+                        tma_store_2d(&tm_y, smem_u32(ost) + GM_Y_BYTES, n0, m0 + GM_YT);
+                        bulk_commit_group();
+                    }
+                } else if (ok) {
+                    for (int x = threadIdx.x - GM_EPI_WARP0 * 32; x < GM_BT * GM_BW; x += GM_EPI_WARPS * 32) {
+                        const int m = m0 + x / GM_BW, n = n0 + x % GM_BW;
+                        if (m < M && n < N) Y[(int64_t)m * N + n] = *reinterpret_cast<const uint16_t*>(ost + 2 * x);
+                    }
+                }
+                continue;
+            }
             uint32_t pk[64];  // bf16 pairs (token 2i, token 2i + 1) of this lane's row
             if (ok) {
                 tc_fence_after();
@@ -487,7 +660,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                              << 16);
                 }
                 tc_fence_before();
-                mbar_arrive(tmem_empty);  // the next tile's MMAs may overwrite D
+                mbar_arrive(tmem_empty);  // the next item's MMAs may overwrite D
             }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -526,12 +699,51 @@ gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
 
 // ------------------------------------------------------------------ host side
 
-// one block per SM (persistent), no more blocks than tiles
+// The stream-K tail for T tiles of nkb k blocks on `sms` SMs: the blocks, the whole tiles and
+// the split units, or false when whole tiles are as good.  Split when the last round is
+// part-empty and the estimate saves at least 3%.  The estimate counts k blocks of one block
+// plus 40 for the split's fixed cost (measured: the sharers' partial tiles out and the owners'
+// in, an extra tile boundary, the owners' waits; ~20 us at ~0.45 us a k block).  A split range
+// stays under two tiles of k blocks (at most 3 pieces) and at least 8 k blocks.
+static bool gemm_split_plan(int64_t T, int64_t nkb, int sms, int* blocks, int64_t* dp_tiles, int64_t* units) {
+    if (sms < 2 || T < 1 || nkb < 8 || T % sms == 0) return false;
+    const int64_t gw = std::min<int64_t>(T, sms);
+    const double whole = (double)((T + gw - 1) / gw) * nkb;
+    const int64_t rounds = T / sms;
+    const int64_t dp = rounds >= 1 ? (rounds - 1) * sms : 0;  // whole tiles, the same count per block
+    const int64_t u = (T - dp) * nkb;
+    const int64_t g = std::min<int64_t>(sms, u / 8);
+    if (g < 2 || (dp > 0 && g != sms)) return false;
+    const int64_t span = (u + g - 1) / g;
+    if (span > 2 * nkb - 1) return false;
+    const double split = (double)(dp / g) * nkb + span + 40.0;
+    if (split > 0.97 * whole) return false;
+    *blocks = (int)g;
+    *dp_tiles = dp;
+    *units = u;
+    return true;
+}
+
+cudaError_t gemm_split_bytes(int64_t M, int64_t N, int64_t K, size_t part_off, size_t* bytes) {
+    *bytes = 0;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    int g = 0;
+    int64_t dp = 0, u = 0;
+    const int64_t T = ((N + GM_BW - 1) / GM_BW) * ((M + GM_BT - 1) / GM_BT);
+    if (gemm_split_plan(T, (K + GM_BK - 1) / GM_BK, sms, &g, &dp, &u)) *bytes = part_off + g * GM_PART_FLOATS * 4;
+    return cudaSuccess;
+}
+
+// one block per SM (persistent), no more blocks than tiles; the stream-K tail when the workspace
+// holds its flags (from byte 0) and partial sums (from part_off)
 template <int G, bool QT, int B>
 static cudaError_t launch_gemm_g(const CUtensorMap& tx, const CUtensorMap& tp, const CUtensorMap& ts,
                                  const CUtensorMap& to, const CUtensorMap& ty, bool y_tma, const uint16_t* scales,
                                  const uint16_t* offsets, uint16_t* Y, const Epilogue& ep, int M, int N, int K,
-                                 cudaStream_t stream) {
+                                 void* workspace, size_t workspace_bytes, size_t part_off, cudaStream_t stream) {
     auto kern = gemm_kernel<G, QT, B>;
     constexpr int SMEM = GmLayout<B>::SMEM_BYTES;
     cudaError_t e = ensure_kernel_attrs(reinterpret_cast<const void*>(kern), SMEM, false);
@@ -539,11 +751,23 @@ static cudaError_t launch_gemm_g(const CUtensorMap& tx, const CUtensorMap& tp, c
     int sms = 0, per_sm = 0;
     if ((e = resident_blocks(reinterpret_cast<const void*>(kern), GM_THREADS, SMEM, &sms, &per_sm)) != cudaSuccess)
         return e;
-    const int ntn = (N + GM_BW - 1) / GM_BW;
-    const int ntiles = ntn * ((M + GM_BT - 1) / GM_BT);
-    const int grid = std::max(1, std::min(ntiles, sms * std::max(per_sm, 1)));
-    kern<<<grid, GM_THREADS, SMEM, stream>>>(tx, tp, ts, to, ty, scales, offsets, Y, ep, M, N, K, ntn, ntiles,
-                                              y_tma ? 1 : 0);
+    GmWork wk{};
+    wk.ntn = (N + GM_BW - 1) / GM_BW;
+    wk.ntiles = wk.ntn * ((M + GM_BT - 1) / GM_BT);
+    wk.dp_tiles = wk.ntiles;
+    int grid = std::max(1, std::min(wk.ntiles, sms * std::max(per_sm, 1)));
+    int g = 0;
+    int64_t dp = 0, u = 0;
+    if (workspace != nullptr && per_sm == 1 && part_off % 16 == 0 &&
+        gemm_split_plan(wk.ntiles, (K + GM_BK - 1) / GM_BK, sms, &g, &dp, &u) && (size_t)g * 4 <= part_off &&
+        workspace_bytes >= part_off + (size_t)g * GM_PART_FLOATS * 4) {
+        grid = g;
+        wk.dp_tiles = (int)dp;
+        wk.sk_units = u;
+        wk.part = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + part_off);
+        wk.flags = static_cast<unsigned int*>(workspace);
+    }
+    kern<<<grid, GM_THREADS, SMEM, stream>>>(tx, tp, ts, to, ty, scales, offsets, Y, ep, M, N, K, wk, y_tma ? 1 : 0);
     return cudaGetLastError();
 }
 
@@ -551,23 +775,25 @@ template <int B>
 static cudaError_t launch_gemm_b(const CUtensorMap& tx, const CUtensorMap& tp, const CUtensorMap& ts,
                                  const CUtensorMap& to, const CUtensorMap& ty, bool y_tma, bool qt,
                                  const uint16_t* scales, const uint16_t* offsets, uint16_t* Y, const Epilogue& ep,
-                                 int m, int n, int k, int g, cudaStream_t stream) {
+                                 int m, int n, int k, int g, void* ws, size_t ws_bytes, size_t part_off,
+                                 cudaStream_t stream) {
     switch (g) {
         case 32:
-            return qt ? launch_gemm_g<32, true, B>(tx, tp, ts, to, ty, y_tma, scales, offsets, Y, ep, m, n, k, stream)
-                      : launch_gemm_g<32, false, B>(tx, tp, ts, to, ty, y_tma, scales, offsets, Y, ep, m, n, k, stream);
+            return qt ? launch_gemm_g<32, true, B>(tx, tp, ts, to, ty, y_tma, scales, offsets, Y, ep, m, n, k, ws, ws_bytes, part_off, stream)
+                      : launch_gemm_g<32, false, B>(tx, tp, ts, to, ty, y_tma, scales, offsets, Y, ep, m, n, k, ws, ws_bytes, part_off, stream);
         case 64:
-            return qt ? launch_gemm_g<64, true, B>(tx, tp, ts, to, ty, y_tma, scales, offsets, Y, ep, m, n, k, stream)
-                      : launch_gemm_g<64, false, B>(tx, tp, ts, to, ty, y_tma, scales, offsets, Y, ep, m, n, k, stream);
+            return qt ? launch_gemm_g<64, true, B>(tx, tp, ts, to, ty, y_tma, scales, offsets, Y, ep, m, n, k, ws, ws_bytes, part_off, stream)
+                      : launch_gemm_g<64, false, B>(tx, tp, ts, to, ty, y_tma, scales, offsets, Y, ep, m, n, k, ws, ws_bytes, part_off, stream);
         default:
-            return qt ? launch_gemm_g<128, true, B>(tx, tp, ts, to, ty, y_tma, scales, offsets, Y, ep, m, n, k, stream)
-                      : launch_gemm_g<128, false, B>(tx, tp, ts, to, ty, y_tma, scales, offsets, Y, ep, m, n, k, stream);
+            return qt ? launch_gemm_g<128, true, B>(tx, tp, ts, to, ty, y_tma, scales, offsets, Y, ep, m, n, k, ws, ws_bytes, part_off, stream)
+                      : launch_gemm_g<128, false, B>(tx, tp, ts, to, ty, y_tma, scales, offsets, Y, ep, m, n, k, ws, ws_bytes, part_off, stream);
     }
 }
 
 cudaError_t launch_gemm(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
                         const uint16_t* offsets, int64_t N, int g, int bits, uint16_t* Y, cudaStream_t stream,
-                        const char** detail, const Epilogue& ep) {
+                        const char** detail, const Epilogue& ep, void* workspace, size_t workspace_bytes,
+                        size_t part_off) {
     if ((N + GM_BW - 1) / GM_BW * ((M + GM_BT - 1) / GM_BT) > 0x7FFFFFFF) {
         *detail = "problem too large for the GEMM's tile count";
         return cudaErrorInvalidValue;
@@ -611,9 +837,9 @@ cudaError_t launch_gemm(const uint16_t* X, int64_t M, int64_t K, const uint8_t* 
         if (e != cudaSuccess) return e;
     }
     const int m = (int)M, n = (int)N, k = (int)K;
-    if (bits == 2) return launch_gemm_b<2>(tx, tp, ts, to, ty, y_tma, qt, scales, offsets, Y, ep, m, n, k, g, stream);
-    if (bits == 8) return launch_gemm_b<8>(tx, tp, ts, to, ty, y_tma, qt, scales, offsets, Y, ep, m, n, k, g, stream);
-    return launch_gemm_b<4>(tx, tp, ts, to, ty, y_tma, qt, scales, offsets, Y, ep, m, n, k, g, stream);
+    if (bits == 2) return launch_gemm_b<2>(tx, tp, ts, to, ty, y_tma, qt, scales, offsets, Y, ep, m, n, k, g, workspace, workspace_bytes, part_off, stream);
+    if (bits == 8) return launch_gemm_b<8>(tx, tp, ts, to, ty, y_tma, qt, scales, offsets, Y, ep, m, n, k, g, workspace, workspace_bytes, part_off, stream);
+    return launch_gemm_b<4>(tx, tp, ts, to, ty, y_tma, qt, scales, offsets, Y, ep, m, n, k, g, workspace, workspace_bytes, part_off, stream);
 }
 
 cudaError_t read_and_clear_gemm_fault(unsigned int* fault) {

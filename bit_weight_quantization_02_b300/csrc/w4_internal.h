@@ -147,10 +147,17 @@ cudaError_t launch_tcdec(const TcDecPlan& plan, const uint16_t* X, int64_t M, in
                          void* workspace, cudaStream_t stream, const char** detail, const Epilogue& ep = Epilogue());
 cudaError_t read_and_clear_tcdec_fault(unsigned int* fault);
 
-// tcgen05 tensor-core GEMM (any M).
+// tcgen05 tensor-core GEMM (any M).  With a workspace that holds them, a
+// part-empty last round of tiles is split by k blocks over the blocks
+// (stream-K): flags from the workspace's start (zero between calls, under
+// part_off bytes), fp32 partial tiles from byte part_off on (16-byte aligned).
 cudaError_t launch_gemm(const uint16_t* X, int64_t M, int64_t K, const uint8_t* Wq, const uint16_t* scales,
                         const uint16_t* offsets, int64_t N, int g, int bits, uint16_t* Y, cudaStream_t stream,
-                        const char** detail, const Epilogue& ep = Epilogue());
+                        const char** detail, const Epilogue& ep = Epilogue(), void* workspace = nullptr,
+                        size_t workspace_bytes = 0, size_t part_off = 0);
+// Workspace bytes a GEMM call with its partial tiles at part_off uses on the
+// current device (0: it splits nothing).
+cudaError_t gemm_split_bytes(int64_t M, int64_t N, int64_t K, size_t part_off, size_t* bytes);
 // Read and clear the kernels' device fault words (bounded-wait timeouts); the
 // caller has synchronized the stream.
 cudaError_t read_and_clear_gemm_fault(unsigned int* fault);

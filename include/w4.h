@@ -160,10 +160,14 @@ W4_API size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int gro
  * blocks) in a fixed order (the split depends on the GPU's SM count).
  *
  * workspace: caller-owned device memory of `workspace_bytes` bytes (NULL with
- * 0 is allowed).  It must be zero-filled once before its first use; every
- * call returns it to all zeros, so one workspace serves calls of any shape in
- * sequence.  Calls that may run at the same time on the GPU must not share a
- * workspace.
+ * 0 is allowed).  It must be zero-filled once before its first use.  Its
+ * first 16 MiB hold flags and split-tile slots, and every call returns them to
+ * zero, so one workspace serves calls of any shape in sequence.  Past 16 MiB
+ * (prefill shapes whose last round of tiles is split, w4_linear_workspace_bytes
+ * > 16 MiB) the tensor-core GEMM keeps fp32 partial tiles, which it writes
+ * before it reads them and leaves behind.  Without that room the GEMM computes
+ * whole tiles only.  Calls that may run at the same time on the GPU must not
+ * share a workspace.
  * Kernels of consecutive w4_linear calls on one stream may overlap (the next
  * one starts streaming its weights while the previous one finishes); each
  * still reads X, and touches Y and the workspace, only after everything

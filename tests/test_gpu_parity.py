@@ -244,9 +244,11 @@ def test_linear_repacked(g, nk):
         Y.check()
         assert_linear_ok(Y.t, y_ref, f"repacked M={M} N={N} K={K} g={g}")
     w4.w4_device_fault(DEV)
-    ws = w4._workspace_for(X, 32, N, K, g, None)
+    ws = w4._workspace_for(X, 32, N, K, g, None)  # the stream's default workspace, shared with other calls
     torch.cuda.synchronize()
-    assert int(ws.buf.count_nonzero()) == 0, "the decode-layout kernel must leave its workspace zeroed"
+    # its slot region (the first 16 MiB) comes back to zero; past it, the tensor-core GEMM keeps
+    # partial sums that it always writes before reading
+    assert int(ws.buf[: 16 << 20].count_nonzero()) == 0, "the decode-layout kernel must leave its slots zeroed"
 
 
 GEMM_M = [1, 33, 127, 129, 300]
