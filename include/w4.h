@@ -125,7 +125,10 @@ W4_API w4_status w4_dequantize(const uint8_t *Wq, const uint16_t *scales,
  * With 5 to 32 tokens the stream-K work is done by 4-warp blocks that share
  * one staged slice of X (64-row units); their grid is further capped so that
  * each of its warps still has such a slot.
- * 0 when neither applies (M > 32).
+ * M > 32 (the tcgen05 GEMM): 0, or, when the last round of 128-row x
+ * 256-token tiles on this device's SMs is part-empty and splitting it pays,
+ * 16 MiB + 128 KB per SM (flags in the first 16 MiB, fp32 partial tiles
+ * after; the GEMM splits only with that much room).
  */
 W4_API size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int group_size);
 
@@ -142,7 +145,9 @@ W4_API size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int gro
  * runs the SM-pair kernel (thread-block clusters of two that split K and add
  * their partial sums in shared memory; K <= 16384 and K / group_size a
  * multiple of 8), other M <= 32 the cluster split-K skinny kernel; larger M
- * the tcgen05 tensor-core GEMM.  The workspace arguments extend the plain
+ * the tcgen05 tensor-core GEMM (persistent, one block per SM; with a large
+ * enough workspace the last round of tiles is split by k blocks between the
+ * blocks, deterministically).  The workspace arguments extend the plain
  * (X, M, K, Wq, scales, offsets, N, group_size, Y, stream) call: passing none
  * gives that call exactly, at a speed cost that is small with one token (the
  * 224 one-token Llama-3-8B linears take about 1.17x the time) and larger with
