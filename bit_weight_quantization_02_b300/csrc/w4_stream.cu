@@ -92,6 +92,13 @@ __host__ __device__ inline int st_smem_bytes(int M, int g, int rt) {
 __device__ unsigned int g_stream_fault;
 constexpr uint64_t ST_WAIT_LIMIT_NS = 2000000000ull;
 
+// 16 bytes of read-only data through L1 (the blocks of an SM that read the same lines share them)
+__device__ __forceinline__ uint4 ldg_l1_v4(const void* ptr) {
+    uint4 v;
+    asm("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(ptr));
+    return v;
+}
+
 // XM, what X holds: 0 bf16 activations; 1 int8 activation codes (p.X points at
 // bytes), widened to bf16 when loaded, their scale applied by the epilogue
 // (p.ep.yscale); 2 bf16 activations quantized here to int8 codes with the
@@ -134,8 +141,8 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         for (int m = 0; m < MX; ++m) {
             mx[m] = 0u;
             if (m < p.M)
-                for (int c = threadIdx.x; c < p.K / 8; c += ST_THREADS)
-                    mx[m] = max(mx[m], act_mag_max8(ldg_cg_v4(p.X + (int64_t)m * p.K + 8 * c)));
+                for (int c = threadIdx.x; c < p.K / 8; c += ST_THREADS)  // through L1: the SM's blocks share X
+                    mx[m] = max(mx[m], act_mag_max8(ldg_l1_v4(p.X + (int64_t)m * p.K + 8 * c)));
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) mx[m] = max(mx[m], __shfl_xor_sync(0xffffffffu, mx[m], o));
             if (lane == 0) qx_red[warp][m] = mx[m];
