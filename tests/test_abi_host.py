@@ -7,6 +7,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import bit_weight_quantization_02_b300 as w4
 
