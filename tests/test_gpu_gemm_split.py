@@ -105,3 +105,23 @@ def test_split_tail_large_sampled(shape):
     assert torch.equal(_linear(X, Wq, sc, of, g, ws).view(torch.int16), Y.view(torch.int16))
     assert int(ws.buf[: 16 << 20].count_nonzero()) == 0
     w4.w4_device_fault(DEV)
+
+
+@pytest.mark.parametrize("split", [False, True], ids=["whole", "split"])
+def test_gemm_rows_not_16_byte_multiples(split):
+    """N = 1030 (Y's rows are not 16-byte multiples, so no TMA store): the GEMM writes Y with plain
+    stores, whole tiles and split ones, within tolerance of the oracle and inside Y only."""
+    M, N, K, g = 300, 1030, 4096, 32
+    (X, Wq, sc, of), y_ref = _problem(M, N, K, g, seed=41)
+    if split:
+        need = w4.w4_linear_workspace_bytes(M, N, K, g)
+        assert need > 16 << 20, "this shape is meant to split its last round"
+        ws = w4.Workspace(DEV, need)
+    else:
+        ws = w4.Workspace(DEV)
+    Y = Guarded((M, N), torch.bfloat16)
+    w4.w4_linear_ex(X, Wq, sc, of, g, w4.KERNEL_GEMM, out=Y.t, workspace=ws)
+    Y.check()
+    ok, worst = oracle.within_linear_tolerance(f64(Y.t), y_ref)
+    assert ok, f"N={N} ({'split' if split else 'whole'}): worst ratio {worst:.3f}"
+    w4.w4_device_fault(DEV)
