@@ -113,7 +113,10 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint3
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 __device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b) {
     uint32_t r;
@@ -140,8 +143,10 @@ constexpr int QSEG_PIECES = QSEG_W / 8;             // 16-byte pieces per segmen
 constexpr int QSEG_PITCH = 2 * QSEG_W + 16;         // bytes per segment in shared memory
 constexpr int QTILE_PIECES = 32 * QSEG_PIECES;      // per warp tile
 constexpr int QUANT_WARPS = QUANT_THREADS / 32;
-constexpr int QBUF = 32 * QSEG_PITCH;              // one tile buffer
-constexpr int QUANT_SMEM = QUANT_WARPS * 2 * QBUF;  // two per warp
+constexpr int QBUF = 32 * QSEG_PITCH;                     // one tile buffer
+constexpr int QSTAGES = 2;                                // tile buffers per warp
+constexpr int QUANT_SMEM = QUANT_WARPS * QSTAGES * QBUF;
+constexpr int QUANT_MIN_BLOCKS = QSTAGES == 2 ? 3 : 2;    // blocks per SM the registers are capped for
 
 // The codes of 8 weights from the bits of m = rint(t) + 2^23 (the code is in the low mantissa
 // bits: rint(t) <= L at 2 and 4 bits, as t <= L / (1 - 2^-8) < L + 1/2 because s rounds Delta/L
@@ -335,15 +340,15 @@ __device__ __forceinline__ void quantize_segment(uint32_t ga, int lane, int nval
 }
 
 // A persistent grid of one wave strides over warp tiles; each warp keeps its next tile's copies in
-// flight while it quantizes the current one.
+// flight (QSTAGES - 1 tiles ahead) while it quantizes the current one.
 template <int G, int B>
-__global__ void __launch_bounds__(QUANT_THREADS, 3)
+__global__ void __launch_bounds__(QUANT_THREADS, QUANT_MIN_BLOCKS)
 quantize_kernel(const uint4* __restrict__ W, int64_t n_groups, uint8_t* __restrict__ Wq,
                 uint16_t* __restrict__ scales, uint16_t* __restrict__ offsets) {
     constexpr int GPS = G <= QSEG_W ? QSEG_W / G : 1;
     extern __shared__ __align__(16) unsigned char q_smem[];
     const int lane = threadIdx.x & 31;
-    const uint32_t area = smem_u32(q_smem) + (threadIdx.x >> 5) * (2 * QBUF);
+    const uint32_t area = smem_u32(q_smem) + (threadIdx.x >> 5) * (QSTAGES * QBUF);
     // piece lane + 32u of the tile is piece (lane % 8) of segment 4u + lane / 8
     const uint32_t cp_off = (lane >> 3) * QSEG_PITCH + 16 * (lane & 7);
     const int64_t n_pieces = n_groups * (G / 8);
@@ -360,11 +365,12 @@ quantize_kernel(const uint4* __restrict__ W, int64_t n_groups, uint8_t* __restri
         }
         cp_async_commit();  // possibly empty: one group per tile slot keeps the wait count uniform
     };
-    copy_tile(t, area);
+#pragma unroll
+    for (int k = 0; k < QSTAGES - 1; ++k) copy_tile(t + k * nwarps, area + k * QBUF);
     for (int i = 0; t * 32 < n_segs; t += nwarps, ++i) {
-        const uint32_t buf = area + (i & 1) * QBUF;
-        copy_tile(t + nwarps, area + ((i + 1) & 1) * QBUF);
-        cp_async_wait_1();  // this lane's copies of tile t are done
+        const uint32_t buf = area + (i % QSTAGES) * QBUF;
+        copy_tile(t + (QSTAGES - 1) * nwarps, area + ((i + QSTAGES - 1) % QSTAGES) * QBUF);
+        cp_async_wait<QSTAGES - 1>();  // this lane's copies of tile t are done
         __syncwarp();       // and every lane's
         const int64_t seg = t * 32 + lane;
         const int64_t first = seg * QSEG_W / G;  // the segment's first group
