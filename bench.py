@@ -793,17 +793,37 @@ def other_rows(args, w4, wl, device, stream, peaks, dist, only=None):
     del packed
 
     # dequantize throughput on the gate/up shape, L2 flushed
-    if not want("dequant"):
-        del flush_buf
-        return rows
-    c = wl.config2()[4]
-    (Wq, sc, of), = quantize_linears([c], device, w4, wl)
-    out = torch.empty((c.N, c.K), dtype=torch.bfloat16, device=device)
-    with torch.cuda.stream(stream):
-        t = time_each(lambda: w4.w4_dequantize(Wq, sc, of, c.group_size, out=out), 20, stream, flush)
-    db = c.N * c.K // 2 + 4 * c.N * c.K // c.group_size + 2 * c.N * c.K
-    rows["dequantize"] = {"N": c.N, "K": c.K, "g": c.group_size, "us": round(t * 1e3, 2),
-                          "gbs": round(db / (t * 1e-3) / 1e9, 1), "frac_of_hbm_peak": round(db / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+    if want("dequant"):
+        c = wl.config2()[4]
+        (Wq, sc, of), = quantize_linears([c], device, w4, wl)
+        out = torch.empty((c.N, c.K), dtype=torch.bfloat16, device=device)
+        with torch.cuda.stream(stream):
+            t = time_each(lambda: w4.w4_dequantize(Wq, sc, of, c.group_size, out=out), 20, stream, flush)
+        db = c.N * c.K // 2 + 4 * c.N * c.K // c.group_size + 2 * c.N * c.K
+        rows["dequantize"] = {"N": c.N, "K": c.K, "g": c.group_size, "us": round(t * 1e3, 2),
+                              "gbs": round(db / (t * 1e-3) / 1e9, 1),
+                              "frac_of_hbm_peak": round(db / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+        del Wq, sc, of, out
+    # 4-bit quantize throughput on the gate/up shape at every group size: back-to-back calls over
+    # weight copies that together exceed L2 (single calls are too short for the event clock)
+    if want("quantize"):
+        c = wl.config2()[4]
+        copies = max(1, args.quant_copies)
+        Ws = [wl.gen_weight(c.N, c.K, seed=c.w_seed + i, outliers=c.outliers, device=device) for i in range(copies)]
+        qcases = []
+        for g in (32, 64, 128):
+            outs = [w4.w4_quantize(W, g) for W in Ws]
+            with torch.cuda.stream(stream):
+                for W, o in zip(Ws, outs):
+                    w4.w4_quantize(W, g, out=o)
+                t = time_each(lambda: [w4.w4_quantize(W, g, out=o) for W, o in zip(Ws, outs)], 5, stream) / copies
+            qb = 2 * c.N * c.K + c.N * c.K // 2 + 4 * c.N * c.K // g
+            qcases.append({"g": g, "us": round(t * 1e3, 2), "gbs": round(qb / (t * 1e-3) / 1e9, 1),
+                           "frac_of_hbm_peak": round(qb / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)})
+            del outs
+        rows["quantize"] = {"N": c.N, "K": c.K, "bits": 4, "copies": copies, "cases": qcases,
+                            "l2": f"{copies} weight copies of {2 * c.N * c.K / 1e6:.0f} MB quantized back to back"}
+        del Ws
     del flush_buf
     return rows
 
@@ -972,13 +992,15 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--prefill-iters", type=int, default=10)
-    ap.add_argument("--section", choices=["all", "prefill", "shapes", "batched", "widths", "stack", "dequant"],
+    ap.add_argument("--section", choices=["all", "prefill", "shapes", "batched", "widths", "stack", "dequant", "quantize"],
                     default="all",
                     help="all = the benchmark; the others run one secondary row alone (for profiling) and print it")
     ap.add_argument("--batched-m", type=int, default=0,
                     help="with --section batched: only the cases with this many tokens (for profiling)")
     ap.add_argument("--widths-bits", type=int, default=0, choices=[0, 2, 8],
                     help="with --section widths: only this code width (for profiling)")
+    ap.add_argument("--quant-copies", type=int, default=8,
+                    help="with --section quantize: weight copies quantized back to back (fewer only for profiling)")
     ap.add_argument("--layers", type=int, default=32,
                     help="Llama-3-8B blocks in the headline step (32 = the whole model; fewer only for profiling)")
     a = ap.parse_args(argv)
