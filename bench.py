@@ -813,6 +813,7 @@ def other_rows(args, w4, wl, device, stream, peaks, dist, only=None):
         qcases = []
         for g in (32, 64, 128):
             outs = [w4.w4_quantize(W, g) for W in Ws]
+            torch.cuda.synchronize(device)  # the copies and outputs were made on the default stream
             with torch.cuda.stream(stream):
                 for W, o in zip(Ws, outs):
                     w4.w4_quantize(W, g, out=o)
