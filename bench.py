@@ -529,6 +529,7 @@ def int8_rows(args, w4, wl, device, stream, dist, peaks, cases, stack, ws_ms):
     def pre():
         w4.w4_quantize_activation_i8(X, True, out=(q, s_))
         w4.w4_linear_i8(q, s_, True, Wq, sc, of, gs, out=Y, workspace=pws)
+    torch.cuda.synchronize(device)  # the inputs were made on the default stream
     with torch.cuda.stream(stream):
         pre()
         ts = time_each(pre, 10, stream, flush=lambda: flush.zero_())
