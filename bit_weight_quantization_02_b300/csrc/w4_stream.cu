@@ -107,6 +107,86 @@ __device__ __forceinline__ uint4 ldg_l1_v4(const void* ptr) {
 // magnitude of X first (after the dependency wait, with its weight copies in
 // flight), then codes every X chunk as it loads it, exactly as the separate
 // quantization would, and its epilogue applies the scale.
+// The owner's part of a split tile on the one-token path, for all RT row tiles of the unit at once
+// (a sharer's slot holds them one after another, 16 words each).  It is split_collect's
+// owner collect with one token, but one batch of loads covers the same sharers' words of every
+// row tile, so the owner pays one round trip to L2 per batch instead of one per row tile.  Lanes
+// 0-15 take row lane of even sharers and lanes 16-31 the odd ones, 8 sharers each per batch.
+// The sums are added in warp order (deterministic); each word is zeroed after use.  Returns false
+// if a wait timed out.
+template <int RT>
+__device__ __forceinline__ bool collect_one_token(const float (&oacc)[RT][1][4], float* scr, uint64_t* ws, int worker,
+                                                  int wl, const int (&nrows)[RT], int row_a, int tq, int lane,
+                                                  uint16_t* Yt, unsigned int* fault_word, unsigned int code,
+                                                  uint64_t limit_ns, const Epilogue ep_t) {
+    constexpr int BC = 8;                   // sharers per half-warp and batch
+    constexpr size_t STRIDE = (size_t)RT * 16;
+    if (tq == 0) {  // token 0 of rows row_a, row_a + 8 of each row tile
+#pragma unroll
+        for (int rt = 0; rt < RT; ++rt) {
+            scr[rt * 16 + row_a] = oacc[rt][0][0];
+            scr[rt * 16 + row_a + 8] = oacc[rt][0][2];
+        }
+    }
+    __syncwarp();
+    const int sub = lane >> 4, e0 = lane & 15;
+    bool ok = true;
+    float sum[RT];
+#pragma unroll
+    for (int rt = 0; rt < RT; ++rt) sum[rt] = sub == 0 ? scr[rt * 16 + e0] : 0.f;
+    for (int c0 = worker + 1 + sub; c0 <= wl; c0 += 2 * BC) {
+        uint64_t v[RT][BC];
+#pragma unroll
+        for (int rt = 0; rt < RT; ++rt)
+#pragma unroll
+            for (int j = 0; j < BC; ++j) {
+                const int c = c0 + 2 * j;
+                v[rt][j] = (c <= wl && e0 < nrows[rt]) ? ld_relaxed_u64(ws + (size_t)c * STRIDE + rt * 16 + e0)
+                                                       : (1ull << 32);
+            }
+        uint64_t t0 = 0;
+        for (;;) {  // re-poll together the words whose sharer has not published yet
+            bool all = true;
+#pragma unroll
+            for (int rt = 0; rt < RT; ++rt)
+#pragma unroll
+                for (int j = 0; j < BC; ++j) all = all && (v[rt][j] >> 32) != 0u;
+            if (all) break;
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) t0 = now;
+            if (now - t0 > limit_ns) {  // give up: count what is missing as zero
+                atomicOr(fault_word, code);
+                ok = false;
+                break;
+            }
+#pragma unroll
+            for (int rt = 0; rt < RT; ++rt)
+#pragma unroll
+                for (int j = 0; j < BC; ++j)
+                    if ((v[rt][j] >> 32) == 0u)
+                        v[rt][j] = ld_relaxed_u64(ws + (size_t)(c0 + 2 * j) * STRIDE + rt * 16 + e0);
+        }
+#pragma unroll
+        for (int rt = 0; rt < RT; ++rt)
+#pragma unroll
+            for (int j = 0; j < BC; ++j) {
+                const int c = c0 + 2 * j;
+                if (c <= wl && e0 < nrows[rt]) {
+                    sum[rt] += __uint_as_float((uint32_t)v[rt][j]);
+                    st_relaxed_u64(ws + (size_t)c * STRIDE + rt * 16 + e0, 0ull);
+                }
+            }
+    }
+#pragma unroll
+    for (int rt = 0; rt < RT; ++rt) {
+        sum[rt] += __shfl_xor_sync(0xffffffffu, sum[rt], 16);
+        if (sub == 0 && e0 < nrows[rt])
+            Yt[16 * rt + e0] = (uint16_t)float_to_bf16_bits(epilogue_f32(epilogue_at(ep_t, 16 * rt), sum[rt], 0, e0));
+    }
+    __syncwarp();
+    return ok;
+}
+
 template <int G, int MX, bool QT, int RT, int XM>
 __global__ void __launch_bounds__(ST_THREADS, RT == 2 ? 4 : 6)
 stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
@@ -500,13 +580,12 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ 
         const int wl = split_warp_of((long long)tile * p.nkc + p.nkc - 1, p.units, p.workers);
         constexpr int NE = MX / 2 ? MX / 2 : 1;  // slot words per lane (16 M / 32)
         if constexpr (DIAG) {
+            int nrows[RT];
 #pragma unroll
-            for (int rt = 0; rt < RT; ++rt)  // a slot holds the row tiles one after another
-                ok = split_collect<1, NE>(oacc[rt], scr + rt * 16, p.ws + rt * 16, (size_t)RT * 16, worker, wl, 1,
-                                          min(16, p.N - (tile * ROWS + 16 * rt)), pr, tq, lane,
-                                          p.Y + (int64_t)tile * ROWS + 16 * rt, p.N, &g_stream_fault, 2u,
-                                          ST_WAIT_LIMIT_NS, epilogue_at(ep, (int64_t)tile * ROWS + 16 * rt)) &&
-                     ok;
+            for (int rt = 0; rt < RT; ++rt) nrows[rt] = min(16, p.N - (tile * ROWS + 16 * rt));
+            ok = collect_one_token<RT>(oacc, scr, p.ws, worker, wl, nrows, pr, tq, lane, p.Y + (int64_t)tile * ROWS,
+                                       &g_stream_fault, 2u, ST_WAIT_LIMIT_NS, epilogue_at(ep, (int64_t)tile * ROWS)) &&
+                 ok;
         } else {
             ok = split_collect<MT, NE>(acc, scr, p.ws, (size_t)16 * p.M, worker, wl, p.M, min(16, p.N - tile * 16), pr,
                                        tq, lane, p.Y + (int64_t)tile * 16, p.N, &g_stream_fault, 2u,
