@@ -149,9 +149,9 @@ W4_API size_t w4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int gro
  * enough workspace the last round of tiles is split by k blocks between the
  * blocks, deterministically).  The workspace arguments extend the plain
  * (X, M, K, Wq, scales, offsets, N, group_size, Y, stream) call: passing none
- * gives that call exactly, at a speed cost that is small with one token (the
- * 224 one-token Llama-3-8B linears take about 1.17x the time) and larger with
- * 2 to 32 tokens (the cluster kernel: 2 to 5x).  The kernels
+ * gives that call exactly, at a speed cost that is moderate with one token
+ * (the 224 one-token Llama-3-8B linears take about 1.29x the time) and larger
+ * with 2 to 32 tokens (the cluster kernel: 2 to 5x).  The kernels
  * dequantize each weight as bf16(q * s + o) with a single rounding, which can
  * differ from w4_dequantize's double rounding by one bf16 ulp; the stream
  * kernel with one token does not round the weights at all: it sums
